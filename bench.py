@@ -1,0 +1,362 @@
+"""Throughput of the FP8 MoE expert-FFN forward on GB300.
+
+One step = one pass of the whole forward path (activation quantisation,
+ragged sort + gather, gmm wi_0|wi_1, SwiGLU + requantisation, gmm wo, ragged
+gather-reduce) over one batch of synthetic tokens.  Default workload: the
+Mixtral-shaped layer (T=8192, d_model=4096, 8 experts, top-2, d_ff=14336),
+per-token activation scales, per-channel weight scales.
+
+Prints one JSON line (rank 0).  Launch with torchrun for several GPUs: every
+rank runs its own batch (data parallel over tokens, no collective on the data
+path), the timing is the max over ranks, and `value` counts the tokens of all
+ranks.  `--impl reference` times the CPU oracle instead, on a bounded sample.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE FFN fwd tokens/s & gmm_fp8 TFLOP/s as % of GB300 FP8 dense peak"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="mixtral", choices=list(synth.CONFIGS))
+    ap.add_argument("--cpu-sample-tokens", type=int, default=0, help="oracle sample size (0 = auto)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_name(cfg) -> str:
+    modes = {0: "per-token", 1: "per-token-per-128", 2: "static"}
+    wmodes = {0: "per-channel", 1: "blockwise [E, K/128, N]", 2: "static"}
+    return (f"{cfg.name} MoE expert FFN fwd: T={cfg.T} d_model={cfg.D} E={cfg.E} top-k={cfg.k} d_ff={cfg.F} SwiGLU; "
+            f"e4m3 {modes[cfg.act_mode]} activation scales, {wmodes[cfg.w_mode]} weight scales")
+
+
+def fwd_flops(cfg) -> dict:
+    R = cfg.T * cfg.k
+    return {"gmm_in": 2.0 * R * cfg.D * 2 * cfg.F, "gmm_out": 2.0 * R * cfg.F * cfg.D}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_setup(cfg, x_bits, ids, w, w_in, w_out, static):
+    import oracle
+    wq = oracle.prepare_weights(w_in, w_out, cfg.w_mode, static)
+    return wq
+
+
+def oracle_time(cfg, x_bits, ids, w, wq, static, n_tokens: int, seed: int = 0):
+    """Time the oracle's forward on a sample of n_tokens tokens (the sort and
+    the activation quantisation run over the whole batch, as they must)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(cfg.T, n_tokens, replace=False))
+    t0 = time.perf_counter()
+    oracle.ffn_forward(x_bits, ids, w, wq, cfg.E, cfg.act_mode, static, tokens=toks)
+    return time.perf_counter() - t0
+
+
+def host_inputs(cfg, seed=0):
+    x = synth.activations(cfg, seed)
+    ids, w = synth.routing(cfg, seed)
+    return x, ids, w
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, cfg, rank, world, local):
+    import fp8_quantized_moe_gb300 as moe
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    static = synth.calibration_scales(cfg, 0) if cfg.act_mode == synth.PER_TENSOR else None
+    sx = sh = None
+    if static:
+        sx = torch.tensor([static["x"]], dtype=torch.float32, device=dev)
+        sh = torch.tensor([static["h"]], dtype=torch.float32, device=dev)
+
+    # inputs: each rank its own batch (seed = rank)
+    x_host, ids_np, w_np = host_inputs(cfg, seed=rank)
+    w_in, w_out = synth.expert_weights(cfg, 0, device=dev)
+    W = moe.prepare_weights(w_in, w_out, cfg.w_mode, static)
+    x = x_host.to(dev)
+    ids = torch.from_numpy(ids_np).to(dev)
+    w = torch.from_numpy(w_np).to(dev)
+    buf = moe.FFNBuffers(cfg.T, cfg.D, cfg.E, cfg.k, cfg.F, cfg.act_mode, dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is None:
+            return moe.ffn_forward(x, ids, w, W, cfg.act_mode, buf, sx, sh)
+        # the same calls as ffn_forward, with events around the two gmms
+        E = W.w_in.shape[0]
+        moe.quantize_rows(x, cfg.act_mode, sx, q=buf.x_q, scale=buf.x_s)
+        s = moe.ragged_sort(ids, E, buf.x_q, buf.x_s if cfg.act_mode != 2 else sx, cfg.act_mode, out=buf.sort)
+        xs_s = s["xs_scale"] if cfg.act_mode != 2 else sx
+        ev[0].record(stream)
+        moe.gmm(s["xs_q"], xs_s, cfg.act_mode, W.w_in, W.s_in, W.in_mode, s["group_sizes"], out=buf.a)
+        ev[1].record(stream)
+        moe.swiglu_quant(buf.a, cfg.act_mode, sh, h_q=buf.h_q, h_scale=buf.h_s)
+        h_s = buf.h_s if cfg.act_mode != 2 else sh
+        ev[2].record(stream)
+        moe.gmm(buf.h_q, h_s, cfg.act_mode, W.w_out, W.s_out, W.out_mode, s["group_sizes"], out=buf.o)
+        ev[3].record(stream)
+        moe.ragged_gather_reduce(buf.o, s["pos"], w, cfg.k, out=buf.y)
+        return buf.y
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if moe.device_error():
+        raise RuntimeError("device error during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms = start.elapsed_time(end) / args.steps
+    gmm_ms = [(e[0].elapsed_time(e[1]), e[2].elapsed_time(e[3])) for e in evs]
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    if moe.device_error():
+        raise RuntimeError("device error during the timed steps")
+
+    # end to end through the public API: pinned host inputs in, y out
+    e2e = None
+    if not args.no_e2e:
+        xh = x_host.pin_memory()
+        idh = torch.from_numpy(ids_np).pin_memory()
+        wh = torch.from_numpy(w_np).pin_memory()
+        yh = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16).pin_memory()
+        for _ in range(3):
+            x.copy_(xh, non_blocking=True)
+            ids.copy_(idh, non_blocking=True)
+            w.copy_(wh, non_blocking=True)
+            yh.copy_(step(), non_blocking=True)
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.steps):
+            x.copy_(xh, non_blocking=True)
+            ids.copy_(idh, non_blocking=True)
+            w.copy_(wh, non_blocking=True)
+            yh.copy_(step(), non_blocking=True)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        ems = s0.elapsed_time(s1) / args.steps
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        h2d = xh.numel() * 2 + idh.numel() * 4 + wh.numel() * 4
+        e2e = {"value": cfg.T * world / (ems / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": yh.numel() * 2, "ms_per_step": ems}
+
+    fl = fwd_flops(cfg)
+    g_in = float(np.mean([a for a, _ in gmm_ms]))
+    g_out = float(np.mean([b for _, b in gmm_ms]))
+    gmm_flops = fl["gmm_in"] + fl["gmm_out"]
+    achieved = gmm_flops / ((g_in + g_out) / 1e3) / 1e12
+    pk, pk_kind = peaks()
+    fp8_peak = 2.0 * pk["bf16_tflops_sustained"]
+    result = {
+        "metric": METRIC,
+        "value": cfg.T * world / (ms / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3 (fp32 accumulate, bf16 in/out)",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, random-init)",
+        "config": {"workload": workload_name(cfg), "tokens_per_gpu": cfg.T, "parallelism": f"dp{world} (replicas)",
+                   "l2": "inputs larger than L2: fp8 expert weights %.2f GB streamed every step"
+                         % ((2 * cfg.F * cfg.D + cfg.D * cfg.F) * cfg.E / 1e9)},
+        "roofline": {"bound": "tensor", "kernel": "gmm_fp8", "achieved": achieved, "peak": fp8_peak,
+                     "unit": "TFLOP/s", "frac": achieved / fp8_peak, "traffic": None,
+                     "peak_note": f"fp8 = 2 x {pk_kind} sustained bf16 cuBLAS ({pk['bf16_tflops_sustained']} TFLOP/s)",
+                     "gmm_in_ms": g_in, "gmm_out_ms": g_out},
+        "gpu_launches": 9 * args.steps,
+        "clocks": clk,
+    }
+    if e2e:
+        result["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args, cfg, x_host, ids_np, w_np, w_in, w_out, static)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return result
+
+
+def cpu_baseline(args, cfg, x_host, ids_np, w_np, w_in, w_out, static):
+    import oracle
+
+    def host_bits(t):
+        return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    xb = host_bits(x_host)
+    wq = oracle_setup(cfg, xb, ids_np, w_np, host_bits(w_in), host_bits(w_out), static)
+    n = args.cpu_sample_tokens or 8
+    dt = oracle_time(cfg, xb, ids_np, w_np, wq, static, n)
+    # grow the sample towards ~10 s of CPU work
+    if not args.cpu_sample_tokens and dt < 2.0:
+        n = int(min(cfg.T, max(n, n * 10.0 / max(dt, 1e-3))))
+        dt = oracle_time(cfg, xb, ids_np, w_np, wq, static, n, seed=1)
+    return {"value": n / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} of {cfg.T} tokens through the oracle forward (fp64, OpenMP); weights quantised "
+                      f"beforehand", "seconds": dt}
+
+
+def run_reference(args, cfg, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    x_host, ids_np, w_np = host_inputs(cfg, seed=0)
+    w_in, w_out = synth.expert_weights(cfg, 0)
+    static = synth.calibration_scales(cfg, 0) if cfg.act_mode == synth.PER_TENSOR else None
+
+    def host_bits(t):
+        return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    xb = host_bits(x_host)
+    wq = oracle_setup(cfg, xb, ids_np, w_np, host_bits(w_in), host_bits(w_out), static)
+    n = args.cpu_sample_tokens or 16
+    for _ in range(args.warmup):
+        oracle_time(cfg, xb, ids_np, w_np, wq, static, max(1, n // 4))
+    times = [oracle_time(cfg, xb, ids_np, w_np, wq, static, n, seed=i) for i in range(args.steps)]
+    sec = float(np.sum(times))
+    value = n * args.steps / sec
+    return {
+        "metric": METRIC, "impl": "reference", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": workload_name(cfg)},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{n} tokens per step of {cfg.T}"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    cfg = synth.CONFIGS[args.config]
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, cfg, rank, world)
+    else:
+        res = run_ours(args, cfg, rank, world, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

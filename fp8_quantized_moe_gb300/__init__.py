@@ -1,0 +1,340 @@
+"""GB300 (sm_103a) FP8-quantized MoE expert FFN.
+
+Python binding of libmoefp8.so (C ABI in include/moefp8.h).  Every function
+here only marshals arguments: it allocates outputs with PyTorch, passes raw
+device pointers and the current CUDA stream, and checks the status.  All
+arithmetic runs in the library's CUDA kernels; there is no fallback.
+
+Forward path (the order of "Quantize activations before EP all gather"):
+quantize_rows -> ragged_sort -> gmm (wi_0 | wi_1) -> swiglu_quant ->
+gmm (wo) -> ragged_gather_reduce.  The backward pass of the static scheme
+("Support quantization for tokamax gmm v2": fp8_static_wa) adds
+gather_scale_quant, swiglu_bwd_quant, quantize_group_cols and tgmm.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+from typing import Optional
+
+import torch
+
+from . import _native
+from ._native import MoEError, check
+
+PER_ROW = 0
+PER_ROW_BLOCK128 = 1
+PER_TENSOR = 2
+PER_GROUP_COL = 3
+
+__all__ = [
+    "PER_ROW", "PER_ROW_BLOCK128", "PER_TENSOR", "PER_GROUP_COL", "MoEError", "lib", "device_error",
+    "quantize_rows", "quantize_weights", "ragged_sort", "gmm", "swiglu_quant", "ragged_gather_reduce",
+    "gather_scale_quant", "swiglu_bwd_quant", "quantize_group_cols", "tgmm", "transpose_u8",
+    "ExpertWeights", "prepare_weights", "FFNBuffers", "ffn_forward", "ffn_backward",
+]
+
+
+def lib():
+    return _native.load()
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise MoEError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise MoEError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _s():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _nb(cols: int) -> int:
+    return (cols + 127) // 128
+
+
+def device_error() -> int:
+    """Synchronise the current stream and return (and clear) the device error word."""
+    code = ctypes.c_int(0)
+    st = lib().moe_get_device_error(_s(), ctypes.byref(code))
+    if st not in (0, 4):
+        check(st, "moe_get_device_error")
+    return code.value
+
+
+def _scale_buf(mode: int, rows: int, cols: int, device, out=None):
+    if out is not None:
+        return out
+    if mode == PER_ROW:
+        return torch.empty(rows, dtype=torch.float32, device=device)
+    if mode == PER_ROW_BLOCK128:
+        return torch.empty(rows, _nb(cols), dtype=torch.float32, device=device)
+    return None
+
+
+def quantize_rows(x: torch.Tensor, mode: int, static_scale: Optional[torch.Tensor] = None, q=None, scale=None):
+    """bf16 [rows, cols] -> (e4m3 codes uint8 [rows, cols], fp32 scales or None)."""
+    rows, cols = x.shape
+    q = torch.empty(rows, cols, dtype=torch.uint8, device=x.device) if q is None else q
+    scale = _scale_buf(mode, rows, cols, x.device, scale)
+    check(lib().moe_quantize_rows(_p(x), rows, cols, mode, _p(static_scale), _p(q), _p(scale), _s()),
+          "moe_quantize_rows")
+    return q, scale
+
+
+def quantize_weights(w: torch.Tensor, mode: int, static_scale: Optional[torch.Tensor] = None):
+    """bf16 [E, N, K] -> (codes [E, N, K], scales [E, N] | [E, K/128, N] | None)."""
+    E, N, K = w.shape
+    q = torch.empty(E, N, K, dtype=torch.uint8, device=w.device)
+    if mode == PER_ROW:
+        s = torch.empty(E, N, dtype=torch.float32, device=w.device)
+    elif mode == PER_ROW_BLOCK128:
+        s = torch.empty(E, _nb(K), N, dtype=torch.float32, device=w.device)
+    else:
+        s = None
+    check(lib().moe_quantize_weights(_p(w), E, N, K, mode, _p(static_scale), _p(q), _p(s), _s()),
+          "moe_quantize_weights")
+    return q, s
+
+
+def ragged_sort(topk_ids: torch.Tensor, E: int, x_q: torch.Tensor, x_scale: Optional[torch.Tensor], mode: int,
+                out: Optional[dict] = None):
+    """Returns dict(sorted_src, pos, group_sizes, group_offsets, xs_q, xs_scale)."""
+    T, k = topk_ids.shape
+    D = x_q.shape[1]
+    R = T * k
+    dev = x_q.device
+    o = out if out is not None else {}
+    if "sorted_src" not in o:
+        o["sorted_src"] = torch.empty(R, dtype=torch.int32, device=dev)
+        o["pos"] = torch.empty(R, dtype=torch.int32, device=dev)
+        o["group_sizes"] = torch.empty(E, dtype=torch.int32, device=dev)
+        o["group_offsets"] = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        o["xs_q"] = torch.empty(R, D, dtype=torch.uint8, device=dev)
+        o["xs_scale"] = _scale_buf(mode, R, D, dev)
+    nws = lib().moe_ragged_sort_workspace_bytes(T, k, E)
+    if "sort_ws" not in o or o["sort_ws"].numel() < nws:
+        o["sort_ws"] = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+    xs_scale = o["xs_scale"]
+    check(lib().moe_ragged_sort(_p(topk_ids), T, k, E, _p(x_q), _p(x_scale), D, mode, _p(o["sorted_src"]),
+                                _p(o["pos"]), _p(o["group_sizes"]), _p(o["group_offsets"]), _p(o["xs_q"]),
+                                _p(xs_scale), _p(o["sort_ws"]), o["sort_ws"].numel(), _s()), "moe_ragged_sort")
+    return o
+
+
+def gmm(lhs_q, lhs_scale, lhs_mode, rhs_q, rhs_scale, rhs_mode, group_sizes, group_offset: int = 0,
+        E_local: Optional[int] = None, out=None):
+    """Grouped matmul -> bf16 [M, N]."""
+    M, K = lhs_q.shape
+    El, N, K2 = rhs_q.shape
+    if K2 != K:
+        raise MoEError("lhs/rhs K mismatch")
+    E = group_sizes.numel()
+    E_local = El if E_local is None else E_local
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=lhs_q.device) if out is None else out
+    check(lib().gmm_fp8(_p(lhs_q), _p(lhs_scale), lhs_mode, _p(rhs_q), _p(rhs_scale), rhs_mode, _p(group_sizes),
+                        E, group_offset, E_local, M, K, N, _p(out), _s()), "gmm_fp8")
+    return out
+
+
+def swiglu_quant(a: torch.Tensor, mode: int, static_scale: Optional[torch.Tensor] = None, h_q=None, h_scale=None):
+    R, F2 = a.shape
+    F = F2 // 2
+    h_q = torch.empty(R, F, dtype=torch.uint8, device=a.device) if h_q is None else h_q
+    h_scale = _scale_buf(mode, R, F, a.device, h_scale)
+    check(lib().moe_swiglu_quant(_p(a), R, F, mode, _p(static_scale), _p(h_q), _p(h_scale), _s()),
+          "moe_swiglu_quant")
+    return h_q, h_scale
+
+
+def ragged_gather_reduce(rows: torch.Tensor, pos: torch.Tensor, weights: Optional[torch.Tensor], k: int,
+                         out=None):
+    R, D = rows.shape
+    T = R // k
+    out = torch.empty(T, D, dtype=torch.bfloat16, device=rows.device) if out is None else out
+    check(lib().ragged_gather_reduce(_p(rows), _p(pos), _p(weights), T, k, D, _p(out), _s()),
+          "ragged_gather_reduce")
+    return out
+
+
+def gather_scale_quant(G: torch.Tensor, w: Optional[torch.Tensor], sorted_src: torch.Tensor, k: int):
+    T, D = G.shape
+    R = T * k
+    dev = G.device
+    dO = torch.empty(R, D, dtype=torch.bfloat16, device=dev)
+    dO_q = torch.empty(R, D, dtype=torch.uint8, device=dev)
+    dO_s = torch.empty(R, dtype=torch.float32, device=dev)
+    check(lib().moe_gather_scale_quant(_p(G), _p(w), _p(sorted_src), T, k, D, _p(dO), _p(dO_q), _p(dO_s), _s()),
+          "moe_gather_scale_quant")
+    return dO, dO_q, dO_s
+
+
+def swiglu_bwd_quant(dH: torch.Tensor, a: torch.Tensor):
+    R, F = dH.shape
+    dev = dH.device
+    dA = torch.empty(R, 2 * F, dtype=torch.bfloat16, device=dev)
+    dA_q = torch.empty(R, 2 * F, dtype=torch.uint8, device=dev)
+    dA_s = torch.empty(R, dtype=torch.float32, device=dev)
+    check(lib().moe_swiglu_bwd_quant(_p(dH), _p(a), R, F, _p(dA), _p(dA_q), _p(dA_s), _s()), "moe_swiglu_bwd_quant")
+    return dA, dA_q, dA_s
+
+
+def quantize_group_cols(g: torch.Tensor, group_sizes: torch.Tensor, group_offset: int = 0,
+                        E_local: Optional[int] = None):
+    M, N = g.shape
+    E = group_sizes.numel()
+    E_local = E - group_offset if E_local is None else E_local
+    q = torch.zeros(M, N, dtype=torch.uint8, device=g.device)
+    s = torch.empty(E_local, N, dtype=torch.float32, device=g.device)
+    check(lib().moe_quantize_group_cols(_p(g), M, N, _p(group_sizes), E, group_offset, E_local, _p(q), _p(s), _s()),
+          "moe_quantize_group_cols")
+    return q, s
+
+
+def tgmm(lhs_q, lhs_scale, lhs_mode, rhs_q, rhs_scale, rhs_mode, group_sizes, group_offset: int = 0,
+         E_local: Optional[int] = None, out=None, workspace=None):
+    """Transposed grouped matmul -> fp32 [E_local, K, N]."""
+    M, K = lhs_q.shape
+    M2, N = rhs_q.shape
+    if M2 != M:
+        raise MoEError("lhs/rhs M mismatch")
+    E = group_sizes.numel()
+    E_local = E - group_offset if E_local is None else E_local
+    out = torch.empty(E_local, K, N, dtype=torch.float32, device=lhs_q.device) if out is None else out
+    nws = lib().tgmm_fp8_workspace_bytes(M, K, N, E_local)
+    if workspace is None or workspace.numel() < nws:
+        workspace = torch.empty(nws, dtype=torch.uint8, device=lhs_q.device)
+    check(lib().tgmm_fp8(_p(lhs_q), _p(lhs_scale), lhs_mode, _p(rhs_q), _p(rhs_scale), rhs_mode, _p(group_sizes), E,
+                         group_offset, E_local, M, K, N, _p(out), _p(workspace), workspace.numel(), _s()), "tgmm_fp8")
+    return out
+
+
+def transpose_u8(x: torch.Tensor) -> torch.Tensor:
+    """Batched byte transpose [B, R, C] -> [B, C, R] (weight layout preparation)."""
+    B, R, C = x.shape
+    out = torch.empty(B, C, R, dtype=torch.uint8, device=x.device)
+    check(lib().moe_transpose_u8(_p(x), B, R, C, _p(out), _s()), "moe_transpose_u8")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# The expert FFN
+# ---------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class ExpertWeights:
+    """Pre-quantised expert weights in the device layout.
+
+    w_in  [E, 2F, D] codes (wi_0 rows, then wi_1 rows), scales per in_mode;
+    w_out [E, D, F] codes, scales per out_mode.  For the backward pass the
+    transposed codes w_in_t [E, D, 2F] and w_out_t [E, F, D] are kept too."""
+    w_in: torch.Tensor
+    s_in: torch.Tensor
+    in_mode: int
+    w_out: torch.Tensor
+    s_out: torch.Tensor
+    out_mode: int
+    w_in_t: Optional[torch.Tensor] = None
+    s_in_t: Optional[torch.Tensor] = None
+    w_out_t: Optional[torch.Tensor] = None
+
+
+def prepare_weights(w_in: torch.Tensor, w_out: torch.Tensor, w_mode: int, static: Optional[dict] = None,
+                    for_backward: bool = False) -> ExpertWeights:
+    """Quantise the bf16 expert weights once (outside the timed FFN).
+
+    Static scheme: wi_0, wi_1 and wo each carry one fixed scale; the wi_0 |
+    wi_1 concatenation then has a per-channel scale vector."""
+    dev = w_in.device
+    E, F2, D = w_in.shape
+    F = F2 // 2
+    if w_mode == PER_TENSOR:
+        s0 = torch.tensor([static["w0"]], dtype=torch.float32, device=dev)
+        s1 = torch.tensor([static["w1"]], dtype=torch.float32, device=dev)
+        so = torch.tensor([static["wo"]], dtype=torch.float32, device=dev)
+        q0, _ = quantize_weights(w_in[:, :F].contiguous(), PER_TENSOR, s0)
+        q1, _ = quantize_weights(w_in[:, F:].contiguous(), PER_TENSOR, s1)
+        qin = torch.cat([q0, q1], dim=1).contiguous()
+        sin = torch.empty(E, F2, dtype=torch.float32, device=dev)
+        sin[:, :F] = static["w0"]
+        sin[:, F:] = static["w1"]
+        qo, _ = quantize_weights(w_out, PER_TENSOR, so)
+        W = ExpertWeights(qin, sin, PER_ROW, qo, so, PER_TENSOR)
+        if for_backward:
+            if F2 % 128 != 0 or F % 128 != 0:
+                raise MoEError("the backward pass needs F % 128 == 0")
+            W.w_in_t = transpose_u8(qin)
+            nb = F2 // 128
+            st = torch.empty(E, nb, D, dtype=torch.float32, device=dev)
+            st[:, : F // 128] = static["w0"]
+            st[:, F // 128:] = static["w1"]
+            W.s_in_t = st
+            W.w_out_t = transpose_u8(qo)
+        return W
+    qin, sin = quantize_weights(w_in, w_mode)
+    qo, so = quantize_weights(w_out, w_mode)
+    return ExpertWeights(qin, sin, w_mode, qo, so, w_mode)
+
+
+class FFNBuffers:
+    """Every intermediate of one forward (and backward) pass, allocated once."""
+
+    def __init__(self, T, D, E, k, F, act_mode, device, backward=False):
+        R = T * k
+        f = lambda *s, dt=torch.uint8: torch.empty(*s, dtype=dt, device=device)
+        self.T, self.D, self.E, self.k, self.F, self.act_mode = T, D, E, k, F, act_mode
+        self.x_q = f(T, D)
+        self.x_s = _scale_buf(act_mode, T, D, device)
+        self.sort = {}
+        self.a = f(R, 2 * F, dt=torch.bfloat16)
+        self.h_q = f(R, F)
+        self.h_s = _scale_buf(act_mode, R, F, device)
+        self.o = f(R, D, dt=torch.bfloat16)
+        self.y = f(T, D, dt=torch.bfloat16)
+        if backward:
+            self.dH = f(R, F, dt=torch.bfloat16)
+            self.dXs = f(R, D, dt=torch.bfloat16)
+            self.dX = f(T, D, dt=torch.bfloat16)
+
+
+def ffn_forward(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, W: ExpertWeights, act_mode: int,
+                buf: FFNBuffers, static_x: Optional[torch.Tensor] = None,
+                static_h: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One forward pass of the expert FFN; returns buf.y (bf16 [T, D])."""
+    E = W.w_in.shape[0]
+    k = topk_ids.shape[1]
+    quantize_rows(x, act_mode, static_x, q=buf.x_q, scale=buf.x_s)
+    s = ragged_sort(topk_ids, E, buf.x_q, buf.x_s if act_mode != PER_TENSOR else static_x, act_mode, out=buf.sort)
+    xs_s = s["xs_scale"] if act_mode != PER_TENSOR else static_x
+    gmm(s["xs_q"], xs_s, act_mode, W.w_in, W.s_in, W.in_mode, s["group_sizes"], out=buf.a)
+    swiglu_quant(buf.a, act_mode, static_h, h_q=buf.h_q, h_scale=buf.h_s)
+    h_s = buf.h_s if act_mode != PER_TENSOR else static_h
+    gmm(buf.h_q, h_s, act_mode, W.w_out, W.s_out, W.out_mode, s["group_sizes"], out=buf.o)
+    ragged_gather_reduce(buf.o, s["pos"], topk_w, k, out=buf.y)
+    return buf.y
+
+
+def ffn_backward(dY: torch.Tensor, topk_w: torch.Tensor, W: ExpertWeights, buf: FFNBuffers,
+                 static_x: torch.Tensor, static_h: torch.Tensor):
+    """Backward pass of the static scheme after ffn_forward on `buf`.
+
+    Returns (dX bf16 [T, D], dW_in fp32 [E, D, 2F], dW_out fp32 [E, F, D]):
+    dW_in holds grad_wi_0 | grad_wi_1 and dW_out grad_wo, in the pages'
+    [E, in, out] layouts."""
+    s = buf.sort
+    k = buf.k
+    dO, dO_q, dO_s = gather_scale_quant(dY, topk_w, s["sorted_src"], k)
+    gmm(dO_q, dO_s, PER_ROW, W.w_out_t, W.s_out, PER_TENSOR, s["group_sizes"], out=buf.dH)
+    dA, dA_q, dA_s = swiglu_bwd_quant(buf.dH, buf.a)
+    gmm(dA_q, dA_s, PER_ROW, W.w_in_t, W.s_in_t, PER_ROW_BLOCK128, s["group_sizes"], out=buf.dXs)
+    ragged_gather_reduce(buf.dXs, s["pos"], None, k, out=buf.dX)
+    dAg_q, dAg_s = quantize_group_cols(dA, s["group_sizes"])
+    dOg_q, dOg_s = quantize_group_cols(dO, s["group_sizes"])
+    dW_in = tgmm(s["xs_q"], static_x, PER_TENSOR, dAg_q, dAg_s, PER_GROUP_COL, s["group_sizes"])
+    dW_out = tgmm(buf.h_q, static_h, PER_TENSOR, dOg_q, dOg_s, PER_GROUP_COL, s["group_sizes"])
+    return buf.dX, dW_in, dW_out

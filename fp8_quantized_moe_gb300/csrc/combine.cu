@@ -1,0 +1,97 @@
+// Ragged gather-reduce ("Quantize activations before EP all gather":
+// ragged_gather_reduce un-permutes the expert outputs and sums the top-k rows
+// of every token weighted by its router probabilities).
+//
+//   out[t, :] = bf16( sum_{j < k} w[t, j] * rows[pos[t*k + j], :] )
+//
+// HBM-bound: one warp per token; per pass each lane loads one 16-byte vector
+// (8 bf16) from each of the k source rows (k independent loads in flight),
+// accumulates in fp32 in ascending j, and writes 8 bf16.  Two passes are
+// unrolled so that small k still keeps enough loads in flight.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+__device__ unsigned int g_err;
+
+constexpr int kMaxK = 32;
+
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* rows, const int32_t* pos,
+                                                      const float* weights, int64_t T, int k, int64_t D,
+                                                      uint16_t* out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int64_t R = T * k;
+  int my_pos = 0;
+  float my_w = 0.0f;
+  if (lane < k) {
+    const int p = __ldg(pos + t * k + lane);
+    my_pos = (p >= 0 && p < R) ? p : -1;
+    my_w = weights ? __ldg(weights + t * k + lane) : 1.0f;
+  }
+  const int64_t nvec = D / 8;
+  for (int64_t v0 = lane; v0 < nvec; v0 += 64) {
+    float acc[2][8];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[u][c] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const int p = __shfl_sync(0xffffffffu, my_pos, j);
+      const float w = __shfl_sync(0xffffffffu, my_w, j);
+      if (p < 0) continue;
+      const uint16_t* src = rows + static_cast<int64_t>(p) * D;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int64_t v = v0 + 32 * u;
+        if (v < nvec) {
+          const uint4 d = __ldg(reinterpret_cast<const uint4*>(src + 8 * v));
+          const uint32_t wd[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            acc[u][2 * c] = __fmaf_rn(w, bf16lo(wd[c]), acc[u][2 * c]);
+            acc[u][2 * c + 1] = __fmaf_rn(w, bf16hi(wd[c]), acc[u][2 * c + 1]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int64_t v = v0 + 32 * u;
+      if (v < nvec) {
+        uint4 o;
+        o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+        o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+        o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+        o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+        *reinterpret_cast<uint4*>(out + t * D + 8 * v) = o;
+      }
+    }
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" __attribute__((visibility("hidden"))) cudaError_t moe_detail_take_error_combine(unsigned int* out) {
+  unsigned int v = 0, z = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_err, sizeof(v));
+  if (e == cudaSuccess && v) e = cudaMemcpyToSymbol(g_err, &z, sizeof(z));
+  *out = v;
+  return e;
+}
+
+extern "C" moe_status ragged_gather_reduce(const uint16_t* rows, const int32_t* pos, const float* weights, int64_t T,
+                                           int k, int64_t D, uint16_t* out, moe_stream_t stream) {
+  MOE_HOST_CHECK(rows && pos && out && T >= 0 && k > 0 && k <= kMaxK && D > 0 && D % 8 == 0, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(T * k < (1ll << 31) && aligned16(rows) && aligned16(out), MOE_ERR_INVALID_ARG);
+  if (T == 0) return MOE_OK;
+  combine_kernel<<<static_cast<unsigned>((T + 7) / 8), 256, 0, as_stream(stream)>>>(rows, pos, weights, T, k, D,
+                                                                                     out);
+  MOE_CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}

@@ -1,0 +1,839 @@
+// Grouped FP8 matmuls on the 5th-generation tensor cores (tcgen05, sm_103a):
+//   gmm_fp8   out[m, n] = sum_k deq(lhs)[m, k] deq(rhs)[g(m), n, k]   (bf16 out)
+//   tgmm_fp8  out[e, k, n] = sum_{m in e} deq(lhs)[m, k] deq(rhs)[m, n] (fp32 out)
+// following "Quantize activations before EP all gather" (gmm_v2 on
+// pre-quantised lhs with rhs_scale and group_offset, lhs scale on the
+// output, bf16 output), "Support quantization for tokamax gmm v2" (gmm and
+// tgmm with absmax scales) and "Keep qwix out of tpu-inference's fused MoE
+// kernel and pre-quantize weights" (fp8 weights with [E, blocks, 1, N]
+// scales; 32-bit accumulation).
+//
+// Design (one persistent CTA per SM, 1 CTA/SM by shared memory):
+//   warp 0      TMA producer: 128x128 A tile + 256x128 B tile per stage into a
+//               4-stage ring of 48 KB stages (128-byte swizzle).
+//   warp 1      MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (M=128, N=256, K=32)
+//               per stage into a TMEM accumulator; commits free the stage.
+//               Also allocates / frees the 512 TMEM columns (2 accumulators).
+//   warps 2..   epilogue: tcgen05.ld the accumulator, apply the scales, store.
+// Accumulators are double-buffered, so the epilogue of tile i overlaps the
+// mainloop of tile i+1.  With a blockwise (128-wide K block) scale on either
+// operand the scale cannot leave the sum, so every K block gets a fresh TMEM
+// accumulator and eight epilogue warps fold it into fp32 registers
+// ("promotion", packed f32x2 FMAs).
+//
+// Tile scheduler: tiles are ordered expert-major, then N tile, then M tile,
+// so that the CTAs running at the same time share the same expert's weights
+// (weights stream from HBM about once).  A group's M tiles start at its first
+// row; rows past the group end are computed and masked at the store.  tgmm
+// contracts over a group's rows: its operands are first transposed into the
+// workspace with every group padded (with zeros) to a multiple of 128 rows, so
+// that the contraction dimension is contiguous (K-major) and every TMA box
+// starts 16-byte aligned.
+//
+// Every wait is bounded (mbarrier try_wait + %globaltimer); on expiry the
+// kernel raises MOE_DEVERR_TIMEOUT, drains what it issued and returns.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+__device__ unsigned int g_err;
+
+constexpr int BM = 128;
+constexpr int BK = 128;
+constexpr int BN = 256;
+constexpr int NSTAGE = 4;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int UMMA_K = 32;
+constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
+constexpr int kMaxGroups = 1024;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+constexpr uint32_t kTmemCols = 512;
+
+enum Mode { kFinal = 0, kPromote = 1, kTgmm = 2 };
+
+template <int MODE>
+struct Cfg {
+  static constexpr int EPI_WARPS = MODE == kPromote ? 8 : 4;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+};
+
+struct Params {
+  const int32_t* group_sizes;
+  int E, g0, El;
+  int64_t M;
+  int K, N;
+  int kblocks;  // gmm: K blocks per tile
+  int ntiles;   // N tiles
+  int ktiles;   // tgmm: output-row tiles (K / 128)
+  const float* lhs_scale;
+  int lhs_mode;
+  const float* rhs_scale;
+  int rhs_mode;
+  void* out;
+};
+
+struct SmemCtl {
+  uint64_t full[NSTAGE];
+  uint64_t empty[NSTAGE];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int err;
+  int total_tiles;
+  int gstart[kMaxGroups + 1];       // gmm: first row of local group; tgmm: padded first row
+  int tile_prefix[kMaxGroups + 1];  // gmm: first tile of local group
+  int gsize[kMaxGroups];
+  float sw_stage[8][128];           // promotion: weight scales of the current K block, per warp
+};
+
+constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(NSTAGE) * STAGE_BYTES + sizeof(SmemCtl);
+
+// ---- group tables --------------------------------------------------------
+// Warp 0 reads all E sizes at once (<= 32 per lane), scans them, and fills
+// the tables for the local groups [g0, g0 + El).  Returns (in ctl->err) 1 if a
+// size is negative or the sizes do not add up to M.
+template <bool TGMM>
+__device__ void build_group_tables(const Params& p, SmemCtl* ctl) {
+  const int lane = threadIdx.x & 31;
+  int v[kMaxGroups / 32];
+#pragma unroll
+  for (int c = 0; c < kMaxGroups / 32; ++c) {
+    const int g = c * 32 + lane;
+    v[c] = g < p.E ? __ldg(p.group_sizes + g) : 0;
+  }
+  int64_t carry_rows = 0;
+  int carry_aux = 0;
+  bool bad = false;
+#pragma unroll
+  for (int c = 0; c < kMaxGroups / 32; ++c) {
+    if (c * 32 >= p.E) break;
+    const int g = c * 32 + lane;
+    const int sz = v[c];
+    if (sz < 0) bad = true;
+    const int local = g - p.g0;
+    const bool mine = g < p.E && local >= 0 && local < p.El;
+    int64_t incl = sz;
+    // aux: gmm -> tiles of the group; tgmm -> padded rows of the group
+    int aux = 0;
+    if (mine && sz > 0) aux = TGMM ? ((sz + BM - 1) / BM) * BM : ((sz + BM - 1) / BM) * p.ntiles;
+    int incl_aux = aux;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+      const int ta = __shfl_up_sync(0xffffffffu, incl_aux, o);
+      if (lane >= o) {
+        incl += t;
+        incl_aux += ta;
+      }
+    }
+    if (mine) {
+      ctl->gsize[local] = sz;
+      if (TGMM) {
+        ctl->gstart[local] = carry_aux + incl_aux - aux;  // padded start
+      } else {
+        ctl->gstart[local] = static_cast<int>(carry_rows + incl - sz);
+        ctl->tile_prefix[local] = carry_aux + incl_aux - aux;
+      }
+    }
+    carry_rows += __shfl_sync(0xffffffffu, incl, 31);
+    carry_aux += __shfl_sync(0xffffffffu, incl_aux, 31);
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  if (lane == 0) {
+    if (TGMM) {
+      ctl->gstart[p.El] = carry_aux;
+      ctl->total_tiles = p.El * p.ktiles * p.ntiles;
+    } else {
+      ctl->tile_prefix[p.El] = carry_aux;
+      ctl->total_tiles = carry_aux;
+    }
+    ctl->err = (bad || carry_rows != p.M) ? 1 : 0;
+  }
+}
+
+struct Tile {
+  int el;       // local group
+  int nkb;      // K blocks to accumulate (0: empty tgmm group)
+  int ax, ay;   // A box coordinates of K block 0 (x advances by BK per block)
+  int bx, by;   // B box coordinates of K block 0
+  int row0;     // gmm: first output row; tgmm: first output row (k) of the tile
+  int rows;     // valid output rows in the tile
+  int n0;       // first output column
+};
+
+template <int MODE>
+__device__ __forceinline__ Tile get_tile(const Params& p, const SmemCtl* ctl, int t) {
+  Tile tl;
+  if (MODE == kTgmm) {
+    const int per = p.ktiles * p.ntiles;
+    tl.el = t / per;
+    const int r = t - tl.el * per;
+    const int kt = r / p.ntiles, nt = r - kt * p.ntiles;
+    const int sz = ctl->gsize[tl.el];
+    const int pst = ctl->gstart[tl.el];
+    tl.nkb = (sz + BK - 1) / BK;
+    tl.ax = pst;
+    tl.ay = kt * BM;
+    tl.bx = pst;
+    tl.by = nt * BN;
+    tl.row0 = kt * BM;
+    tl.rows = min(BM, p.K - kt * BM);
+    tl.n0 = nt * BN;
+  } else {
+    int lo = 0, hi = p.El;  // tile_prefix[lo] <= t < tile_prefix[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (ctl->tile_prefix[mid] <= t) lo = mid; else hi = mid;
+    }
+    // skip empty groups that share the same prefix value
+    while (lo + 1 < p.El && ctl->tile_prefix[lo + 1] <= t) ++lo;
+    tl.el = lo;
+    const int sz = ctl->gsize[lo];
+    const int mt = (sz + BM - 1) / BM;
+    const int local = t - ctl->tile_prefix[lo];
+    const int nt = local / mt, mi = local - nt * mt;
+    tl.nkb = p.kblocks;
+    tl.row0 = ctl->gstart[lo] + mi * BM;
+    tl.rows = min(BM, sz - mi * BM);
+    tl.ax = 0;
+    tl.ay = tl.row0;
+    tl.bx = 0;
+    tl.by = lo * p.N + nt * BN;
+    tl.n0 = nt * BN;
+  }
+  return tl;
+}
+
+__device__ __forceinline__ float lhs_scale_at(const Params& p, int64_t row, int kb) {
+  if (p.lhs_mode == MOE_SCALE_PER_ROW) return __ldg(p.lhs_scale + row);
+  if (p.lhs_mode == MOE_SCALE_PER_ROW_BLOCK128) return __ldg(p.lhs_scale + row * p.kblocks + kb);
+  return __ldg(p.lhs_scale);
+}
+
+__device__ __forceinline__ float rhs_scale_at(const Params& p, int el, int n, int kb) {
+  if (p.rhs_mode == MOE_SCALE_PER_ROW) return __ldg(p.rhs_scale + static_cast<int64_t>(el) * p.N + n);
+  if (p.rhs_mode == MOE_SCALE_PER_ROW_BLOCK128)
+    return __ldg(p.rhs_scale + (static_cast<int64_t>(el) * p.kblocks + kb) * p.N + n);
+  return __ldg(p.rhs_scale);
+}
+
+// tgmm operand scale: per tensor or per (local group, column).
+__device__ __forceinline__ float group_col_scale(const float* s, int mode, int el, int c, int C) {
+  return mode == MOE_SCALE_PER_GROUP_COL ? __ldg(s + static_cast<int64_t>(el) * C + c) : __ldg(s);
+}
+
+__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float* v, int ncols_valid) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    if (g * 8 < ncols_valid) {
+      uint4 o;
+      o.x = pack_bf16x2(v[g * 8 + 0], v[g * 8 + 1]);
+      o.y = pack_bf16x2(v[g * 8 + 2], v[g * 8 + 3]);
+      o.z = pack_bf16x2(v[g * 8 + 4], v[g * 8 + 5]);
+      o.w = pack_bf16x2(v[g * 8 + 6], v[g * 8 + 7]);
+      *reinterpret_cast<uint4*>(dst + g * 8) = o;
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
+    mma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+  constexpr int EPI_WARPS = Cfg<MODE>::EPI_WARPS;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_addr);
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(base_ptr + NSTAGE * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (warp == 0) build_group_tables<MODE == kTgmm>(p, ctl);
+  if (threadIdx.x == 32) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&ctl->tfull[a]), 1);
+      mbar_init(smem_u32(&ctl->tempty[a]), EPI_WARPS);
+    }
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (ctl->err) {
+    if (threadIdx.x == 0) raise_error(&g_err, MOE_DEVERR_GROUP_SIZES);
+    return;
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+  const int total = ctl->total_tiles;
+  volatile int* abort_flag = &ctl->abort_flag;
+  bool timed_out = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
+        const Tile tl = get_tile<MODE>(p, ctl, t);
+        for (int kb = 0; kb < tl.nkb; ++kb) {
+          const int s = it % NSTAGE;
+          const uint32_t ph = (it / NSTAGE) & 1;
+          if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1, abort_flag, kWaitLimitNs)) {
+            timed_out = true;
+            break;
+          }
+          const uint32_t fb = smem_u32(&ctl->full[s]);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t sa = base + s * STAGE_BYTES;
+          tma_load_2d(sa, &tmA, tl.ax + kb * BK, tl.ay, fb);
+          tma_load_2d(sa + A_BYTES, &tmB, tl.bx + kb * BK, tl.by, fb);
+          ++it;
+        }
+      }
+      if (timed_out) {
+        *abort_flag = 1;
+        ctl->err = 2;
+        // let the loads already issued land before the CTA can exit
+        for (uint32_t j = (it > NSTAGE ? it - NSTAGE : 0); j < it; ++j)
+          mbar_wait_bounded(smem_u32(&ctl->full[j % NSTAGE]), (j / NSTAGE) & 1, abort_flag + 1, kWaitLimitNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, acc = 0;
+      for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
+        const Tile tl = get_tile<MODE>(p, ctl, t);
+        if (tl.nkb == 0) continue;
+        uint32_t a = acc & 1;
+        if (MODE != kPromote) {
+          if (!mbar_wait_bounded(smem_u32(&ctl->tempty[a]), ((acc >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+            timed_out = true;
+            break;
+          }
+          tc_fence_after();
+        }
+        for (int kb = 0; kb < tl.nkb; ++kb) {
+          if (MODE == kPromote) {
+            a = acc & 1;
+            if (!mbar_wait_bounded(smem_u32(&ctl->tempty[a]), ((acc >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+              timed_out = true;
+              break;
+            }
+            tc_fence_after();
+          }
+          const int s = it % NSTAGE;
+          const uint32_t ph = (it / NSTAGE) & 1;
+          if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, kWaitLimitNs)) {
+            timed_out = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = base + s * STAGE_BYTES;
+          const uint64_t da = smem_desc_sw128(sa);
+          const uint64_t db = smem_desc_sw128(sa + A_BYTES);
+          const uint32_t d_tmem = tmem_base + a * BN;
+#pragma unroll
+          for (int k4 = 0; k4 < BK / UMMA_K; ++k4) {
+            const uint32_t accumulate = (MODE == kPromote) ? (k4 > 0) : (kb > 0 || k4 > 0);
+            // +32 bytes along K inside the 128-byte swizzled row = +2 in the
+            // descriptor's address field (16-byte units)
+            mma_f8(d_tmem, da + 2 * k4, db + 2 * k4, IDESC, accumulate);
+          }
+          mma_commit(smem_u32(&ctl->empty[s]));
+          if (MODE == kPromote) {
+            mma_commit(smem_u32(&ctl->tfull[a]));
+            ++acc;
+          }
+          ++it;
+        }
+        if (timed_out) break;
+        if (MODE != kPromote) {
+          mma_commit(smem_u32(&ctl->tfull[a]));
+          ++acc;
+        }
+      }
+      // drain: every MMA this thread issued has completed once `drain` flips
+      mma_commit(smem_u32(&ctl->drain));
+      if (!mbar_wait_bounded(smem_u32(&ctl->drain), 0, abort_flag + 1, kWaitLimitNs)) timed_out = true;
+      if (timed_out) {
+        *abort_flag = 1;
+        ctl->err = 2;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q4 = warp & 3;                            // TMEM lane quarter of this warp
+    const int half = (MODE == kPromote) ? (warp - 2) >> 2 : 0;  // column half (promotion only)
+    const int r = q4 * 32 + lane;                       // row of the tile = TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
+    uint32_t acc = 0;
+    for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
+      const Tile tl = get_tile<MODE>(p, ctl, t);
+      const bool row_ok = r < tl.rows;
+      if (MODE == kTgmm) {
+        float* out = static_cast<float*>(p.out);
+        const int64_t krow = tl.row0 + r;
+        float* orow = out + (static_cast<int64_t>(tl.el) * p.K + krow) * p.N;
+        if (tl.nkb == 0) {
+          if (row_ok) {
+            for (int c = 0; c < BN; c += 4)
+              if (tl.n0 + c < p.N) *reinterpret_cast<float4*>(orow + tl.n0 + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          continue;
+        }
+        const uint32_t a = acc & 1;
+        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc >> 1) & 1, abort_flag, kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+        const float sx = row_ok ? group_col_scale(p.lhs_scale, p.lhs_mode, tl.el, static_cast<int>(krow), p.K) : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + c * 32, v);
+          tmem_wait_ld();
+          const int nb = tl.n0 + c * 32;
+          if (row_ok) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              const int n = nb + g * 4;
+              if (n < p.N) {
+                float4 o;
+                o.x = __uint_as_float(v[g * 4 + 0]) * sx * group_col_scale(p.rhs_scale, p.rhs_mode, tl.el, n + 0, p.N);
+                o.y = __uint_as_float(v[g * 4 + 1]) * sx * group_col_scale(p.rhs_scale, p.rhs_mode, tl.el, n + 1, p.N);
+                o.z = __uint_as_float(v[g * 4 + 2]) * sx * group_col_scale(p.rhs_scale, p.rhs_mode, tl.el, n + 2, p.N);
+                o.w = __uint_as_float(v[g * 4 + 3]) * sx * group_col_scale(p.rhs_scale, p.rhs_mode, tl.el, n + 3, p.N);
+                *reinterpret_cast<float4*>(orow + n) = o;
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
+        ++acc;
+      } else if (MODE == kFinal) {
+        uint16_t* out = static_cast<uint16_t*>(p.out);
+        const int64_t row = static_cast<int64_t>(tl.row0) + r;
+        const uint32_t a = acc & 1;
+        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc >> 1) & 1, abort_flag, kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+        const float sa = row_ok ? lhs_scale_at(p, row, 0) : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + c * 32, v);
+          tmem_wait_ld();
+          const int nb = tl.n0 + c * 32;
+          if (row_ok && nb < p.N) {
+            float f[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int n = min(nb + j, p.N - 1);
+              f[j] = __fmul_rn(__fmul_rn(__uint_as_float(v[j]), sa), rhs_scale_at(p, tl.el, n, 0));
+            }
+            store_bf16x32(out + row * p.N + nb, f, p.N - nb);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
+        ++acc;
+      } else {
+        // promotion: one fresh accumulator per K block, folded into registers
+        uint16_t* out = static_cast<uint16_t*>(p.out);
+        const int64_t row = static_cast<int64_t>(tl.row0) + r;
+        const int cbase = tl.n0 + half * 128;
+        float* stage = ctl->sw_stage[warp - 2];
+        uint64_t acc2[64];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) acc2[j] = 0ull;
+        for (int kb = 0; kb < tl.nkb; ++kb) {
+          // weight scales of this warp's 128 columns for K block kb
+          {
+            float4 w4;
+            const int n = cbase + 4 * lane;
+            w4.x = n + 0 < p.N ? rhs_scale_at(p, tl.el, n + 0, kb) : 0.f;
+            w4.y = n + 1 < p.N ? rhs_scale_at(p, tl.el, n + 1, kb) : 0.f;
+            w4.z = n + 2 < p.N ? rhs_scale_at(p, tl.el, n + 2, kb) : 0.f;
+            w4.w = n + 3 < p.N ? rhs_scale_at(p, tl.el, n + 3, kb) : 0.f;
+            *reinterpret_cast<float4*>(stage + 4 * lane) = w4;
+          }
+          const float sa = row_ok ? lhs_scale_at(p, row, kb) : 0.f;
+          const uint64_t sa2 = f2_pack(sa, sa);
+          __syncwarp();
+          const uint32_t a = acc & 1;
+          if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc >> 1) & 1, abort_flag, kWaitLimitNs)) {
+            timed_out = true;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + half * 128 + c * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float2 sw = *reinterpret_cast<const float2*>(stage + c * 32 + 2 * j);
+              const uint64_t pr = f2_mul(f2_pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])),
+                                         f2_pack(sw.x, sw.y));
+              acc2[c * 16 + j] = f2_fma(pr, sa2, acc2[c * 16 + j]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
+          ++acc;
+        }
+        if (timed_out) break;
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int nb = cbase + c * 32;
+            if (nb < p.N) {
+              float f[32];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) f2_unpack(acc2[c * 16 + j], f[2 * j], f[2 * j + 1]);
+              store_bf16x32(out + row * p.N + nb, f, p.N - nb);
+            }
+          }
+        }
+      }
+    }
+    if (timed_out) {
+      *abort_flag = 1;
+      ctl->err = 2;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+  if (threadIdx.x == 0 && ctl->err) raise_error(&g_err, MOE_DEVERR_TIMEOUT);
+}
+
+// ---- helpers for the padded / sharded layouts ----------------------------
+
+// Global first row of every group [0, E] into shared memory (warp 0).
+__device__ void group_starts_smem(const int32_t* sizes, int E, int* starts) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    for (int c = 0; c < E; c += 32) {
+      const int g = c + lane;
+      const int v = g < E ? __ldg(sizes + g) : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (g < E) starts[g] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) starts[E] = carry;
+  }
+  __syncthreads();
+}
+
+// Zero the rows of a gmm output that lie outside groups [g0, g0 + El).
+__global__ void zero_outside_kernel(uint16_t* out, int64_t M, int64_t N, const int32_t* sizes, int E, int g0,
+                                    int El) {
+  __shared__ int starts[kMaxGroups + 1];
+  group_starts_smem(sizes, E, starts);
+  const int64_t lo = starts[g0], hi = starts[g0 + El];
+  const int64_t nvec = N / 8;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < M * nvec;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = i / nvec;
+    if (row < lo || row >= hi) reinterpret_cast<uint4*>(out)[i] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+// src [M, C] e4m3 -> dst [C, Mp]: local group el's rows land at columns
+// [pst(el), pst(el) + size), zero-filled up to the next multiple of 128.
+// 64 x 64 byte tiles through shared memory.
+__global__ void __launch_bounds__(256) transpose_pad_kernel(const uint8_t* src, int64_t M, int64_t C, uint8_t* dst,
+                                                            int64_t Mp, const int32_t* sizes, int E, int g0,
+                                                            int El) {
+  __shared__ int starts[kMaxGroups + 1];
+  __shared__ int pst[kMaxGroups + 1];
+  __shared__ __align__(16) uint8_t tile[64][80];
+  group_starts_smem(sizes, E, starts);
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    for (int c = 0; c < El; c += 32) {
+      const int el = c + lane;
+      const int sz = el < El ? starts[g0 + el + 1] - starts[g0 + el] : 0;
+      const int v = ((sz + 127) / 128) * 128;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (el < El) pst[el] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) pst[El] = carry;
+  }
+  __syncthreads();
+  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * 64;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.y) * 64;
+  if (j0 >= pst[El] || j0 >= Mp) return;
+  {
+    const int jj = threadIdx.x >> 2, part = threadIdx.x & 3;
+    const int64_t j = j0 + jj;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (j < pst[El]) {
+      int lo = 0, hi = El;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pst[mid] <= j) lo = mid; else hi = mid;
+      }
+      while (lo + 1 < El && pst[lo + 1] <= j) ++lo;
+      const int64_t off = j - pst[lo];
+      const int64_t sz = starts[g0 + lo + 1] - starts[g0 + lo];
+      const int64_t c = c0 + part * 16;
+      if (off < sz && c < C) {
+        const int64_t m = starts[g0 + lo] + off;
+        if (m < M) v = __ldg(reinterpret_cast<const uint4*>(src + m * C + c));
+      }
+    }
+    *reinterpret_cast<uint4*>(&tile[jj][part * 16]) = v;
+  }
+  __syncthreads();
+  {
+    const int cc = threadIdx.x >> 2, part = threadIdx.x & 3;
+    const int64_t c = c0 + cc;
+    if (c < C) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int jb = part * 16 + q * 4;
+        w[q] = static_cast<uint32_t>(tile[jb][cc]) | (static_cast<uint32_t>(tile[jb + 1][cc]) << 8) |
+               (static_cast<uint32_t>(tile[jb + 2][cc]) << 16) | (static_cast<uint32_t>(tile[jb + 3][cc]) << 24);
+      }
+      *reinterpret_cast<uint4*>(dst + c * Mp + j0 + part * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+// ---- host side -----------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D uint8 tensor map: rows x inner bytes, box rows_box x 128, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint64_t pitch, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+bool device_is_sm103() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  return major == 10 && minor == 3;
+}
+
+template <int MODE>
+moe_status launch_mma(const CUtensorMap& A, const CUtensorMap& B, const Params& p, int max_tiles,
+                      cudaStream_t st) {
+  MOE_CUDA_TRY(cudaFuncSetAttribute(mma_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(kSmemBytes)));
+  const int sms = sm_count();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const int grid = max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms;
+  mma_kernel<MODE><<<grid, Cfg<MODE>::THREADS, kSmemBytes, st>>>(A, B, p);
+  MOE_CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
+bool valid_lhs_mode(int m) {
+  return m == MOE_SCALE_PER_ROW || m == MOE_SCALE_PER_ROW_BLOCK128 || m == MOE_SCALE_PER_TENSOR;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" __attribute__((visibility("hidden"))) cudaError_t moe_detail_take_error_gmm(unsigned int* out) {
+  unsigned int v = 0, z = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_err, sizeof(v));
+  if (e == cudaSuccess && v) e = cudaMemcpyToSymbol(g_err, &z, sizeof(z));
+  *out = v;
+  return e;
+}
+
+extern "C" int moe_num_sms(void) { return sm_count(); }
+
+extern "C" moe_status gmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode,
+                              const uint8_t* rhs_q, const float* rhs_scale, moe_scale_mode rhs_mode,
+                              const int32_t* group_sizes, int E, int group_offset, int E_local, int64_t M, int64_t K,
+                              int64_t N, uint16_t* out, moe_stream_t stream) {
+  MOE_HOST_CHECK(lhs_q && lhs_scale && rhs_q && rhs_scale && group_sizes && out, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(valid_lhs_mode(lhs_mode) && valid_lhs_mode(rhs_mode), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(E > 0 && E <= kMaxGroups && group_offset >= 0 && E_local > 0 && group_offset + E_local <= E,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(M >= 0 && M < (1ll << 31) && K > 0 && K % 16 == 0 && K < (1 << 30) && N > 0 && N % 16 == 0,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(static_cast<int64_t>(E_local) * N < (1ll << 31), MOE_ERR_INVALID_ARG);
+  const bool blockwise = lhs_mode == MOE_SCALE_PER_ROW_BLOCK128 || rhs_mode == MOE_SCALE_PER_ROW_BLOCK128;
+  MOE_HOST_CHECK(!blockwise || K % 128 == 0, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(aligned16(lhs_q) && aligned16(rhs_q) && aligned16(out), MOE_ERR_INVALID_ARG);
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = as_stream(stream);
+  if (M == 0) return MOE_OK;
+  if (group_offset > 0 || E_local < E) {
+    zero_outside_kernel<<<sm_count() * 4, 256, 0, st>>>(out, M, N, group_sizes, E, group_offset, E_local);
+    MOE_CUDA_TRY(cudaGetLastError());
+  }
+  CUtensorMap A, B;
+  if (!make_map(&A, lhs_q, K, M, K, BM)) return MOE_ERR_CUDA;
+  if (!make_map(&B, rhs_q, K, static_cast<uint64_t>(E_local) * N, K, BN)) return MOE_ERR_CUDA;
+  Params p{};
+  p.group_sizes = group_sizes;
+  p.E = E;
+  p.g0 = group_offset;
+  p.El = E_local;
+  p.M = M;
+  p.K = static_cast<int>(K);
+  p.N = static_cast<int>(N);
+  p.kblocks = static_cast<int>((K + BK - 1) / BK);
+  p.ntiles = static_cast<int>((N + BN - 1) / BN);
+  p.ktiles = 0;
+  p.lhs_scale = lhs_scale;
+  p.lhs_mode = lhs_mode;
+  p.rhs_scale = rhs_scale;
+  p.rhs_mode = rhs_mode;
+  p.out = out;
+  const int64_t max_tiles64 = ((M + BM - 1) / BM + E_local) * p.ntiles;
+  const int max_tiles = static_cast<int>(max_tiles64 > (1 << 30) ? (1 << 30) : max_tiles64);
+  return blockwise ? launch_mma<kPromote>(A, B, p, max_tiles, st) : launch_mma<kFinal>(A, B, p, max_tiles, st);
+}
+
+namespace {
+int64_t padded_rows(int64_t M, int E_local) { return ((M + 127) / 128) * 128 + 128ll * E_local; }
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+}  // namespace
+
+extern "C" size_t tgmm_fp8_workspace_bytes(int64_t M, int64_t K, int64_t N, int E_local) {
+  if (M < 0 || K <= 0 || N <= 0 || E_local <= 0) return 0;
+  const int64_t Mp = padded_rows(M, E_local);
+  return align256(static_cast<size_t>(K * Mp)) + align256(static_cast<size_t>(N * Mp));
+}
+
+extern "C" moe_status tgmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode,
+                               const uint8_t* rhs_q, const float* rhs_scale, moe_scale_mode rhs_mode,
+                               const int32_t* group_sizes, int E, int group_offset, int E_local, int64_t M,
+                               int64_t K, int64_t N, float* out, void* workspace, size_t workspace_bytes,
+                               moe_stream_t stream) {
+  MOE_HOST_CHECK(lhs_q && lhs_scale && rhs_q && rhs_scale && group_sizes && out && workspace, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK((lhs_mode == MOE_SCALE_PER_TENSOR || lhs_mode == MOE_SCALE_PER_GROUP_COL) &&
+                     (rhs_mode == MOE_SCALE_PER_TENSOR || rhs_mode == MOE_SCALE_PER_GROUP_COL),
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(E > 0 && E <= kMaxGroups && group_offset >= 0 && E_local > 0 && group_offset + E_local <= E,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(M >= 0 && M < (1ll << 30) && K > 0 && K % 16 == 0 && K < (1 << 30) && N > 0 && N % 16 == 0 &&
+                     N < (1 << 30),
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(aligned16(lhs_q) && aligned16(rhs_q) && aligned16(out) && aligned16(workspace),
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(workspace_bytes >= tgmm_fp8_workspace_bytes(M, K, N, E_local), MOE_ERR_INVALID_ARG);
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = as_stream(stream);
+  const int64_t Mp = padded_rows(M, E_local);
+  uint8_t* lhsT = static_cast<uint8_t*>(workspace);
+  uint8_t* rhsT = lhsT + align256(static_cast<size_t>(K * Mp));
+  if (M > 0) {
+    dim3 gk(static_cast<unsigned>(Mp / 64), static_cast<unsigned>((K + 63) / 64));
+    transpose_pad_kernel<<<gk, 256, 0, st>>>(lhs_q, M, K, lhsT, Mp, group_sizes, E, group_offset, E_local);
+    MOE_CUDA_TRY(cudaGetLastError());
+    dim3 gn(static_cast<unsigned>(Mp / 64), static_cast<unsigned>((N + 63) / 64));
+    transpose_pad_kernel<<<gn, 256, 0, st>>>(rhs_q, M, N, rhsT, Mp, group_sizes, E, group_offset, E_local);
+    MOE_CUDA_TRY(cudaGetLastError());
+  }
+  CUtensorMap A, B;
+  if (!make_map(&A, lhsT, Mp, K, Mp, BM)) return MOE_ERR_CUDA;
+  if (!make_map(&B, rhsT, Mp, N, Mp, BN)) return MOE_ERR_CUDA;
+  Params p{};
+  p.group_sizes = group_sizes;
+  p.E = E;
+  p.g0 = group_offset;
+  p.El = E_local;
+  p.M = M;
+  p.K = static_cast<int>(K);
+  p.N = static_cast<int>(N);
+  p.kblocks = 0;
+  p.ntiles = static_cast<int>((N + BN - 1) / BN);
+  p.ktiles = static_cast<int>((K + BM - 1) / BM);
+  p.lhs_scale = lhs_scale;
+  p.lhs_mode = lhs_mode;
+  p.rhs_scale = rhs_scale;
+  p.rhs_mode = rhs_mode;
+  p.out = out;
+  const int64_t tiles = static_cast<int64_t>(E_local) * p.ktiles * p.ntiles;
+  return launch_mma<kTgmm>(A, B, p, static_cast<int>(tiles > (1 << 30) ? (1 << 30) : tiles), st);
+}

@@ -1,0 +1,467 @@
+// Row-wise absmax quantisation to e4m3 and the fused producers that feed it:
+//   moe_quantize_rows, moe_quantize_weights        (plain bf16 rows)
+//   moe_swiglu_quant                               (h = bf16(silu(a0) a1))
+//   moe_gather_scale_quant                         (dO = bf16(w G[src]))
+//   moe_swiglu_bwd_quant                           (dA0 | dA1)
+//   moe_quantize_group_cols                        (per-(expert, column) scales)
+//
+// All of these are HBM-bound.  One CTA handles one row: each thread loads
+// 16-byte vectors (8 bf16), applies the producer, keeps the bf16 results in
+// registers, the CTA reduces the absolute maximum (warp shuffles, then shared
+// memory; or 16-lane shuffles for 128-column blocks), and the codes are
+// written with 8-byte stores.  Scales follow "Support quantization for
+// tokamax gmm v2" (absmax for activations and gradients) and "Quantize
+// activations before EP all gather" (quantise before the sort); weights are
+// pre-quantised as in "Keep qwix out of tpu-inference's fused MoE kernel and
+// pre-quantize weights" ([E, blocks, 1, N] scales).
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+__device__ unsigned int g_err;
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ uint4 ldg16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+
+__device__ __forceinline__ void unpack8(const uint4& d, float* v) {
+  v[0] = bf16lo(d.x);
+  v[1] = bf16hi(d.x);
+  v[2] = bf16lo(d.y);
+  v[3] = bf16hi(d.y);
+  v[4] = bf16lo(d.z);
+  v[5] = bf16hi(d.z);
+  v[6] = bf16lo(d.w);
+  v[7] = bf16hi(d.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float* v) {
+  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                    pack_bf16x2(v[6], v[7]));
+}
+
+__device__ __forceinline__ float silu_f32(float z) { return __fdiv_rn(z, __fadd_rn(1.0f, exp_f32(-z))); }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Where the scale of (row, 128-column block b) goes.
+struct ScaleOut {
+  float* scale;
+  int64_t group_n;  // > 0: weights [E, KB, N] with row = e * N + n; 0: [rows, KB]
+  int kb;
+  __device__ __forceinline__ int64_t blk(int64_t row, int b) const {
+    if (group_n > 0) {
+      const int64_t e = row / group_n, n = row - e * group_n;
+      return (e * kb + b) * group_n + n;
+    }
+    return row * kb + b;
+  }
+};
+
+// ---- producers: each "unit" yields U vectors of 8 bf16-exact values ------
+
+struct RowsOp {  // plain bf16 rows
+  static constexpr int U = 1;
+  const uint16_t* x;
+  int64_t cols;
+  __device__ __forceinline__ void operator()(int64_t row, int u, float (&v)[1][8]) const {
+    unpack8(ldg16(x + row * cols + 8 * u), v[0]);
+  }
+  __device__ __forceinline__ int64_t col(int u, int) const { return 8 * static_cast<int64_t>(u); }
+};
+
+struct SwigluOp {  // h = bf16(silu(a0) * a1), a = [a0 | a1] of width 2F
+  static constexpr int U = 1;
+  const uint16_t* a;
+  int64_t F;
+  __device__ __forceinline__ void operator()(int64_t row, int u, float (&v)[1][8]) const {
+    float a0[8], a1[8];
+    const uint16_t* r = a + row * 2 * F + 8 * static_cast<int64_t>(u);
+    unpack8(ldg16(r), a0);
+    unpack8(ldg16(r + F), a1);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[0][j] = round_bf16(__fmul_rn(silu_f32(a0[j]), a1[j]));
+  }
+  __device__ __forceinline__ int64_t col(int u, int) const { return 8 * static_cast<int64_t>(u); }
+};
+
+struct GatherScaleOp {  // dO[r] = bf16(w[i] * G[i / k]), i = sorted_src[r]; also stores dO
+  static constexpr int U = 1;
+  const uint16_t* G;
+  const float* w;
+  const int32_t* sorted_src;
+  int64_t R;
+  int k;
+  int64_t D;
+  uint16_t* dO;
+  __device__ __forceinline__ void operator()(int64_t row, int u, float (&v)[1][8]) const {
+    const int64_t i = __ldg(sorted_src + row);
+    if (i < 0 || i >= R) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[0][j] = 0.0f;
+    } else {
+      const float wi = w ? __ldg(w + i) : 1.0f;
+      float g[8];
+      unpack8(ldg16(G + (i / k) * D + 8 * static_cast<int64_t>(u)), g);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[0][j] = round_bf16(__fmul_rn(wi, g[j]));
+    }
+    *reinterpret_cast<uint4*>(dO + row * D + 8 * static_cast<int64_t>(u)) = pack8(v[0]);
+  }
+  __device__ __forceinline__ int64_t col(int u, int) const { return 8 * static_cast<int64_t>(u); }
+};
+
+struct SwigluBwdOp {  // dA0 = (dH a1) silu'(a0), dA1 = dH silu(a0); also stores dA
+  static constexpr int U = 2;
+  const uint16_t* dH;
+  const uint16_t* a;
+  int64_t F;
+  uint16_t* dA;
+  __device__ __forceinline__ void operator()(int64_t row, int u, float (&v)[2][8]) const {
+    float z[8], a1[8], dh[8];
+    const int64_t c = 8 * static_cast<int64_t>(u);
+    unpack8(ldg16(a + row * 2 * F + c), z);
+    unpack8(ldg16(a + row * 2 * F + F + c), a1);
+    unpack8(ldg16(dH + row * F + c), dh);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float e = exp_f32(-z[j]);
+      const float d = __fadd_rn(1.0f, e);
+      const float sig = __fdiv_rn(1.0f, d);
+      const float silu = __fdiv_rn(z[j], d);
+      const float t1 = __fsub_rn(1.0f, sig);
+      const float t2 = __fmul_rn(z[j], t1);
+      const float t3 = __fadd_rn(1.0f, t2);
+      const float ds = __fmul_rn(sig, t3);
+      const float p = __fmul_rn(dh[j], a1[j]);
+      v[0][j] = round_bf16(__fmul_rn(p, ds));
+      v[1][j] = round_bf16(__fmul_rn(dh[j], silu));
+    }
+    *reinterpret_cast<uint4*>(dA + row * 2 * F + c) = pack8(v[0]);
+    *reinterpret_cast<uint4*>(dA + row * 2 * F + F + c) = pack8(v[1]);
+  }
+  __device__ __forceinline__ int64_t col(int u, int uu) const { return 8 * static_cast<int64_t>(u) + uu * F; }
+};
+
+// ---- the row kernel ------------------------------------------------------
+// MODE: MOE_SCALE_PER_ROW, MOE_SCALE_PER_ROW_BLOCK128 or MOE_SCALE_PER_TENSOR.
+// MAXI: units per thread (ceil(nunits / blockDim.x) <= MAXI).
+template <int MODE, int MAXI, class Op>
+__global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, int64_t qcols,
+                                                            const float* static_scale, uint8_t* q, ScaleOut so) {
+  constexpr int U = Op::U;
+  const int64_t row = blockIdx.x;
+  const int tid = threadIdx.x;
+  uint32_t pk[MAXI][U][4];
+  float amax_i[MAXI];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < MAXI; ++i) {
+    const int u = i * blockDim.x + tid;
+    float m = 0.0f;
+    if (u < nunits) {
+      float v[U][8];
+      op(row, u, v);
+#pragma unroll
+      for (int uu = 0; uu < U; ++uu) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[uu][j]));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) pk[i][uu][j] = pack_bf16x2(v[uu][2 * j], v[uu][2 * j + 1]);
+      }
+    }
+    amax_i[i] = m;
+    amax = fmaxf(amax, m);
+  }
+
+  float s_row = 1.0f;
+  if (MODE == MOE_SCALE_PER_ROW) {
+    __shared__ float red[kThreads / 32];
+    amax = warp_max(amax);
+    if ((tid & 31) == 0) red[tid >> 5] = amax;
+    __syncthreads();
+    if (tid < 32) {
+      float t = tid < static_cast<int>(blockDim.x >> 5) ? red[tid] : 0.0f;
+      t = warp_max(t);
+      if (tid == 0) red[0] = t;
+    }
+    __syncthreads();
+    s_row = absmax_scale(red[0]);
+    if (tid == 0) so.scale[row] = s_row;
+  } else if (MODE == MOE_SCALE_PER_TENSOR) {
+    s_row = __ldg(static_scale);
+  }
+
+#pragma unroll
+  for (int i = 0; i < MAXI; ++i) {
+    const int u = i * blockDim.x + tid;
+    float s = s_row;
+    if (MODE == MOE_SCALE_PER_ROW_BLOCK128) {
+      // 16 consecutive units (one 128-column block) sit on 16 consecutive lanes
+      float m = amax_i[i];
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      s = absmax_scale(m);
+      if (u < nunits && (u & 15) == 0) so.scale[so.blk(row, u >> 4)] = s;
+    }
+    if (u < nunits) {
+#pragma unroll
+      for (int uu = 0; uu < U; ++uu) {
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[2 * j] = __fdiv_rn(bf16lo(pk[i][uu][j]), s);
+          v[2 * j + 1] = __fdiv_rn(bf16hi(pk[i][uu][j]), s);
+        }
+        *reinterpret_cast<uint2*>(q + row * qcols + op.col(u, uu)) = pack_e4m3x8(v);
+      }
+    }
+  }
+}
+
+template <int MODE, int MAXI, class Op>
+cudaError_t launch_rows_t(const Op& op, int64_t rows, int nunits, int threads, int64_t qcols, const float* ss,
+                          uint8_t* q, ScaleOut so, cudaStream_t st) {
+  rowquant_kernel<MODE, MAXI, Op><<<static_cast<unsigned>(rows), threads, 0, st>>>(op, nunits, qcols, ss, q, so);
+  return cudaGetLastError();
+}
+
+template <int MODE, class Op>
+cudaError_t launch_rows_m(const Op& op, int64_t rows, int nunits, int64_t qcols, const float* ss, uint8_t* q,
+                          ScaleOut so, cudaStream_t st) {
+  int threads = nunits >= kThreads ? kThreads : ((nunits + 31) / 32) * 32;
+  const int per = (nunits + threads - 1) / threads;
+  if (per <= 1) return launch_rows_t<MODE, 1>(op, rows, nunits, threads, qcols, ss, q, so, st);
+  if (per <= 2) return launch_rows_t<MODE, 2>(op, rows, nunits, threads, qcols, ss, q, so, st);
+  if (per <= 4) return launch_rows_t<MODE, 4>(op, rows, nunits, threads, qcols, ss, q, so, st);
+  if (per <= 8) return launch_rows_t<MODE, 8>(op, rows, nunits, threads, qcols, ss, q, so, st);
+  return launch_rows_t<MODE, 16>(op, rows, nunits, threads, qcols, ss, q, so, st);
+}
+
+template <class Op>
+moe_status launch_rows(const Op& op, int64_t rows, int nunits, int64_t qcols, moe_scale_mode mode, const float* ss,
+                       uint8_t* q, ScaleOut so, cudaStream_t st) {
+  if (rows == 0) return MOE_OK;
+  cudaError_t e;
+  if (mode == MOE_SCALE_PER_ROW)
+    e = launch_rows_m<MOE_SCALE_PER_ROW>(op, rows, nunits, qcols, ss, q, so, st);
+  else if (mode == MOE_SCALE_PER_ROW_BLOCK128)
+    e = launch_rows_m<MOE_SCALE_PER_ROW_BLOCK128>(op, rows, nunits, qcols, ss, q, so, st);
+  else
+    e = launch_rows_m<MOE_SCALE_PER_TENSOR>(op, rows, nunits, qcols, ss, q, so, st);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+constexpr int64_t kMaxCols = 16 * kThreads * 8;  // 32768 values per quantised row
+
+moe_status check_mode_ptrs(moe_scale_mode mode, const float* static_scale, const float* scale) {
+  if (mode == MOE_SCALE_PER_TENSOR) return static_scale ? MOE_OK : MOE_ERR_INVALID_ARG;
+  if (mode == MOE_SCALE_PER_ROW || mode == MOE_SCALE_PER_ROW_BLOCK128)
+    return (scale && aligned16(scale)) ? MOE_OK : MOE_ERR_INVALID_ARG;
+  return MOE_ERR_INVALID_ARG;
+}
+
+// ---- per-(expert, column) gradient quantisation -------------------------
+// Tiles of 64 rows x 256 columns: 8 warps, each warp owns 8 rows, each lane
+// 8 consecutive columns.  Rows walk through the groups in order, so a lane
+// keeps one running maximum per column and flushes it with atomicMax (the bit
+// pattern of a non-negative float orders like an unsigned integer) whenever
+// the group changes.  The scale array holds the maxima until a second kernel
+// turns them into amax / 448.
+constexpr int kGcRows = 64;
+constexpr int kMaxGroups = 1024;
+
+// Global start row of every group, for groups [0, E]; computed by warp 0.
+__device__ __forceinline__ void group_starts_smem(const int32_t* sizes, int E, int64_t* starts) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int64_t carry = 0;
+    for (int c = 0; c < E; c += 32) {
+      const int g = c + lane;
+      int64_t v = g < E ? __ldg(sizes + g) : 0;
+      int64_t incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (g < E) starts[g] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) starts[E] = carry;
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ int find_group(const int64_t* starts, int E, int64_t m) {
+  int lo = 0, hi = E;  // starts[lo] <= m < starts[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (starts[mid] <= m) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+template <bool QUANT>
+__global__ void __launch_bounds__(256) group_cols_kernel(const uint16_t* g, int64_t M, int64_t N,
+                                                         const int32_t* sizes, int E, int g0, int El, uint8_t* q,
+                                                         float* scale) {
+  __shared__ int64_t starts[kMaxGroups + 1];
+  group_starts_smem(sizes, E, starts);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * 32 + lane) * 8;
+  if (c0 >= N) return;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kGcRows + warp * 8;
+  const int64_t lo = starts[g0], hi = starts[g0 + El];
+  float m[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m[j] = 0.0f;
+  int cur = -1;
+  float sc[8];
+  for (int rr = 0; rr < 8; ++rr) {
+    const int64_t row = r0 + rr;
+    if (row >= M) break;
+    if (row < lo || row >= hi) continue;
+    const int grp = find_group(starts, E, row) - g0;
+    if (grp != cur) {
+      if (!QUANT && cur >= 0) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          atomicMax(reinterpret_cast<unsigned int*>(scale) + static_cast<int64_t>(cur) * N + c0 + j,
+                    __float_as_uint(m[j]));
+      }
+      if (QUANT) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sc[j] = scale[static_cast<int64_t>(grp) * N + c0 + j];
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m[j] = 0.0f;
+      cur = grp;
+    }
+    float v[8];
+    unpack8(ldg16(g + row * N + c0), v);
+    if (QUANT) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = __fdiv_rn(v[j], sc[j]);
+      *reinterpret_cast<uint2*>(q + row * N + c0) = pack_e4m3x8(v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m[j] = fmaxf(m[j], fabsf(v[j]));
+    }
+  }
+  if (!QUANT && cur >= 0) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      atomicMax(reinterpret_cast<unsigned int*>(scale) + static_cast<int64_t>(cur) * N + c0 + j,
+                __float_as_uint(m[j]));
+  }
+}
+
+__global__ void finalize_scales_kernel(float* scale, int64_t n) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) scale[i] = absmax_scale(scale[i]);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+// Device error word of this translation unit (read by moe_get_device_error).
+extern "C" __attribute__((visibility("hidden"))) cudaError_t moe_detail_take_error_quantize(unsigned int* out) {
+  unsigned int v = 0, z = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_err, sizeof(v));
+  if (e == cudaSuccess && v) e = cudaMemcpyToSymbol(g_err, &z, sizeof(z));
+  *out = v;
+  return e;
+}
+
+extern "C" moe_status moe_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, moe_scale_mode mode,
+                                        const float* static_scale, uint8_t* q, float* scale, moe_stream_t stream) {
+  MOE_HOST_CHECK(x && q && rows >= 0 && cols > 0 && cols % 16 == 0 && cols <= kMaxCols, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(rows < (1ll << 31) && aligned16(x) && aligned16(q), MOE_ERR_INVALID_ARG);
+  moe_status st = check_mode_ptrs(mode, static_scale, scale);
+  if (st != MOE_OK) return st;
+  RowsOp op{x, cols};
+  ScaleOut so{scale, 0, static_cast<int>((cols + 127) / 128)};
+  return launch_rows(op, rows, static_cast<int>(cols / 8), cols, mode, static_scale, q, so, as_stream(stream));
+}
+
+extern "C" moe_status moe_quantize_weights(const uint16_t* w, int64_t E, int64_t N, int64_t K, moe_scale_mode mode,
+                                           const float* static_scale, uint8_t* q, float* scale,
+                                           moe_stream_t stream) {
+  MOE_HOST_CHECK(w && q && E > 0 && N > 0 && K > 0 && K % 16 == 0 && K <= kMaxCols, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(E * N < (1ll << 31) && aligned16(w) && aligned16(q), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(mode != MOE_SCALE_PER_ROW_BLOCK128 || K % 128 == 0, MOE_ERR_INVALID_ARG);
+  moe_status st = check_mode_ptrs(mode, static_scale, scale);
+  if (st != MOE_OK) return st;
+  RowsOp op{w, K};
+  ScaleOut so{scale, N, static_cast<int>(K / 128)};
+  return launch_rows(op, E * N, static_cast<int>(K / 8), K, mode, static_scale, q, so, as_stream(stream));
+}
+
+extern "C" moe_status moe_swiglu_quant(const uint16_t* a, int64_t R, int64_t F, moe_scale_mode mode,
+                                       const float* static_scale, uint8_t* h_q, float* h_scale,
+                                       moe_stream_t stream) {
+  MOE_HOST_CHECK(a && h_q && R >= 0 && F > 0 && F % 16 == 0 && F <= kMaxCols, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(R < (1ll << 31) && aligned16(a) && aligned16(h_q), MOE_ERR_INVALID_ARG);
+  moe_status st = check_mode_ptrs(mode, static_scale, h_scale);
+  if (st != MOE_OK) return st;
+  SwigluOp op{a, F};
+  ScaleOut so{h_scale, 0, static_cast<int>((F + 127) / 128)};
+  return launch_rows(op, R, static_cast<int>(F / 8), F, mode, static_scale, h_q, so, as_stream(stream));
+}
+
+extern "C" moe_status moe_gather_scale_quant(const uint16_t* G, const float* w, const int32_t* sorted_src,
+                                             int64_t T, int k, int64_t D, uint16_t* dO, uint8_t* dO_q,
+                                             float* dO_scale, moe_stream_t stream) {
+  MOE_HOST_CHECK(G && sorted_src && dO && dO_q && dO_scale && T >= 0 && k > 0 && D > 0, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(D % 16 == 0 && D <= kMaxCols && T * k < (1ll << 31), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(aligned16(G) && aligned16(dO) && aligned16(dO_q) && aligned16(dO_scale), MOE_ERR_INVALID_ARG);
+  GatherScaleOp op{G, w, sorted_src, T * k, k, D, dO};
+  ScaleOut so{dO_scale, 0, 0};
+  return launch_rows(op, T * k, static_cast<int>(D / 8), D, MOE_SCALE_PER_ROW, nullptr, dO_q, so,
+                     as_stream(stream));
+}
+
+extern "C" moe_status moe_swiglu_bwd_quant(const uint16_t* dH, const uint16_t* a, int64_t R, int64_t F,
+                                           uint16_t* dA, uint8_t* dA_q, float* dA_scale, moe_stream_t stream) {
+  MOE_HOST_CHECK(dH && a && dA && dA_q && dA_scale && R >= 0 && F > 0, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(F % 16 == 0 && 2 * F <= kMaxCols && R < (1ll << 31), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(aligned16(dH) && aligned16(a) && aligned16(dA) && aligned16(dA_q) && aligned16(dA_scale),
+                 MOE_ERR_INVALID_ARG);
+  SwigluBwdOp op{dH, a, F, dA};
+  ScaleOut so{dA_scale, 0, 0};
+  return launch_rows(op, R, static_cast<int>(F / 8), 2 * F, MOE_SCALE_PER_ROW, nullptr, dA_q, so,
+                     as_stream(stream));
+}
+
+extern "C" moe_status moe_quantize_group_cols(const uint16_t* g, int64_t M, int64_t N, const int32_t* group_sizes,
+                                              int E, int group_offset, int E_local, uint8_t* q, float* scale,
+                                              moe_stream_t stream) {
+  MOE_HOST_CHECK(g && group_sizes && q && scale && M >= 0 && N > 0 && N % 16 == 0, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(E > 0 && E <= kMaxGroups && group_offset >= 0 && E_local > 0 && group_offset + E_local <= E,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(aligned16(g) && aligned16(q) && aligned16(scale), MOE_ERR_INVALID_ARG);
+  cudaStream_t st = as_stream(stream);
+  const int64_t ns = static_cast<int64_t>(E_local) * N;
+  MOE_CUDA_TRY(cudaMemsetAsync(scale, 0, sizeof(float) * ns, st));
+  if (M > 0) {
+    dim3 grid(static_cast<unsigned>((N / 8 + 31) / 32), static_cast<unsigned>((M + kGcRows - 1) / kGcRows));
+    group_cols_kernel<false><<<grid, 256, 0, st>>>(g, M, N, group_sizes, E, group_offset, E_local, q, scale);
+    MOE_CUDA_TRY(cudaGetLastError());
+  }
+  finalize_scales_kernel<<<static_cast<unsigned>((ns + 255) / 256), 256, 0, st>>>(scale, ns);
+  MOE_CUDA_TRY(cudaGetLastError());
+  if (M > 0) {
+    dim3 grid(static_cast<unsigned>((N / 8 + 31) / 32), static_cast<unsigned>((M + kGcRows - 1) / kGcRows));
+    group_cols_kernel<true><<<grid, 256, 0, st>>>(g, M, N, group_sizes, E, group_offset, E_local, q, scale);
+    MOE_CUDA_TRY(cudaGetLastError());
+  }
+  return MOE_OK;
+}

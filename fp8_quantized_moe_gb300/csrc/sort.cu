@@ -1,0 +1,260 @@
+// Ragged sort of the (token, expert) pairs by routed expert, plus the gather
+// of the quantised rows and (per-token) scales -- "Quantize activations
+// before EP all gather": the activations are quantised first, so the sort
+// moves fp8 rows, and the scale rows are gathered only when the scale is per
+// token.
+//
+// Stable counting sort over the flat pairs i = t*k + j, keyed by expert id:
+//   1. hist:    each CTA owns a chunk of 2048 pairs (8 warps x 256); per-warp
+//               histograms in shared memory, chunk totals to the workspace.
+//   2. scan:    one CTA: per expert, prefix over chunks; across experts, a
+//               block-wide exclusive scan -> group_sizes, group_offsets and
+//               the first output slot of every (chunk, expert).
+//   3. scatter: each warp walks its 256 pairs in index order, 32 at a time;
+//               __match_any_sync ranks equal ids inside a round, per-warp
+//               running counters carry the rank across rounds -> stable.
+//   4. gather:  one warp per token reads its fp8 row once (16-byte loads) and
+//               writes it to the k sorted positions; scales alongside.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+__device__ unsigned int g_err;
+
+constexpr int kWarps = 8;
+constexpr int kPerWarp = 256;
+constexpr int kChunk = kWarps * kPerWarp;  // 2048 pairs per CTA
+constexpr int kMaxE = 1024;
+
+__device__ __forceinline__ int load_id(const int32_t* ids, int64_t i, int64_t R, int E, bool& bad) {
+  if (i >= R) return -1;
+  const int e = __ldg(ids + i);
+  if (e < 0 || e >= E) {
+    bad = true;
+    return -1;
+  }
+  return e;
+}
+
+// Per-warp histograms of the chunk; hist is [kWarps][E] in shared memory.
+__device__ __forceinline__ void chunk_hist(const int32_t* ids, int64_t R, int E, int* hist) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kChunk + warp * kPerWarp;
+  bool bad = false;
+  for (int r = 0; r < kPerWarp / 32; ++r) {
+    const int e = load_id(ids, base + r * 32 + lane, R, E, bad);
+    if (e >= 0) atomicAdd(&hist[warp * E + e], 1);
+  }
+  if (bad) raise_error(&g_err, MOE_DEVERR_BAD_EXPERT_ID);
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(256) sort_hist_kernel(const int32_t* ids, int64_t R, int E, int* chunk_counts) {
+  extern __shared__ int hist[];
+  chunk_hist(ids, R, E, hist);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int s = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s += hist[w * E + e];
+    chunk_counts[static_cast<int64_t>(blockIdx.x) * E + e] = s;
+  }
+}
+
+// One CTA of 1024 threads; thread e owns expert e.
+__global__ void __launch_bounds__(1024) sort_scan_kernel(int* chunk_counts, int nchunks, int E,
+                                                         int32_t* group_sizes, int32_t* group_offsets) {
+  __shared__ int warp_sums[32];
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = chunk_counts[static_cast<int64_t>(c) * E + e];
+      chunk_counts[static_cast<int64_t>(c) * E + e] = total;  // exclusive within the expert
+      total += v;
+    }
+  }
+  // block-wide exclusive scan of total over experts
+  const int lane = e & 31, warp = e >> 5;
+  int incl = total;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = warp_sums[lane];
+    int inc2 = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, inc2, o);
+      if (lane >= o) inc2 += t;
+    }
+    warp_sums[lane] = inc2 - v;
+  }
+  __syncthreads();
+  const int excl = incl - total + warp_sums[warp];
+  if (e < E) {
+    group_sizes[e] = total;
+    group_offsets[e] = excl;
+    if (e == E - 1) group_offsets[E] = excl + total;
+    for (int c = 0; c < nchunks; ++c) chunk_counts[static_cast<int64_t>(c) * E + e] += excl;
+  }
+}
+
+__global__ void __launch_bounds__(256) sort_scatter_kernel(const int32_t* ids, int64_t R, int E,
+                                                           const int* chunk_counts, int32_t* sorted_src,
+                                                           int32_t* pos) {
+  extern __shared__ int hist[];  // [kWarps][E] counts, then running slots
+  chunk_hist(ids, R, E, hist);
+  // hist[w][e] <- first slot of warp w's pairs of expert e
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = chunk_counts[static_cast<int64_t>(blockIdx.x) * E + e];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = hist[w * E + e];
+      hist[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* slot = hist + warp * E;
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kChunk + warp * kPerWarp;
+  bool bad = false;
+  for (int r = 0; r < kPerWarp / 32; ++r) {
+    const int64_t i = base + r * 32 + lane;
+    const int e = load_id(ids, i, R, E, bad);
+    const unsigned valid = __ballot_sync(0xffffffffu, e >= 0);
+    if (e >= 0) {
+      const unsigned peers = __match_any_sync(valid, e);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int p = slot[e] + rank;
+      sorted_src[p] = static_cast<int32_t>(i);
+      pos[i] = p;
+      __syncwarp(valid);
+      if (rank == 0) slot[e] += __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
+// One warp per token: read the fp8 row once, write it to its k slots.
+template <int MODE>
+__global__ void __launch_bounds__(256) sort_gather_kernel(const uint8_t* x_q, const float* x_scale, int64_t T,
+                                                          int k, int64_t D, const int32_t* pos, uint8_t* xs_q,
+                                                          float* xs_scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int64_t R = T * k;
+  int my_pos = -1;
+  if (lane < k) {
+    my_pos = pos[t * k + lane];
+    if (my_pos < 0 || my_pos >= R) my_pos = -1;
+  }
+  const uint8_t* src = x_q + t * D;
+  constexpr int CH = 8;  // 16-byte vectors per lane per pass (4 KB per warp)
+  for (int64_t b0 = 0; b0 < D; b0 += 32 * 16 * CH) {
+    uint4 v[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int64_t off = b0 + (static_cast<int64_t>(c) * 32 + lane) * 16;
+      if (off < D) v[c] = __ldg(reinterpret_cast<const uint4*>(src + off));
+    }
+    for (int j = 0; j < k; ++j) {
+      const int p = __shfl_sync(0xffffffffu, my_pos, j);
+      if (p < 0) continue;
+      uint8_t* dst = xs_q + static_cast<int64_t>(p) * D;
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int64_t off = b0 + (static_cast<int64_t>(c) * 32 + lane) * 16;
+        if (off < D) *reinterpret_cast<uint4*>(dst + off) = v[c];
+      }
+    }
+  }
+  if (MODE == MOE_SCALE_PER_ROW) {
+    if (my_pos >= 0) xs_scale[my_pos] = __ldg(x_scale + t);
+  } else if (MODE == MOE_SCALE_PER_ROW_BLOCK128) {
+    const int64_t nb = (D + 127) / 128;
+    for (int j = 0; j < k; ++j) {
+      const int p = __shfl_sync(0xffffffffu, my_pos, j);
+      if (p < 0) continue;
+      for (int64_t b = lane; b < nb; b += 32) xs_scale[static_cast<int64_t>(p) * nb + b] = __ldg(x_scale + t * nb + b);
+    }
+  }
+}
+
+int64_t num_chunks(int64_t R) { return (R + kChunk - 1) / kChunk; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" __attribute__((visibility("hidden"))) cudaError_t moe_detail_take_error_sort(unsigned int* out) {
+  unsigned int v = 0, z = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_err, sizeof(v));
+  if (e == cudaSuccess && v) e = cudaMemcpyToSymbol(g_err, &z, sizeof(z));
+  *out = v;
+  return e;
+}
+
+extern "C" size_t moe_ragged_sort_workspace_bytes(int64_t T, int k, int E) {
+  if (T < 0 || k <= 0 || E <= 0) return 0;
+  const int64_t nc = num_chunks(T * k);
+  return static_cast<size_t>((nc > 0 ? nc : 1) * E) * sizeof(int);
+}
+
+extern "C" moe_status moe_ragged_sort(const int32_t* topk_ids, int64_t T, int k, int E, const uint8_t* x_q,
+                                      const float* x_scale, int64_t D, moe_scale_mode mode, int32_t* sorted_src,
+                                      int32_t* pos, int32_t* group_sizes, int32_t* group_offsets, uint8_t* xs_q,
+                                      float* xs_scale, void* workspace, size_t workspace_bytes,
+                                      moe_stream_t stream) {
+  MOE_HOST_CHECK(topk_ids && x_q && sorted_src && pos && group_sizes && group_offsets && xs_q && workspace,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(T >= 0 && k > 0 && k <= 32 && E > 0 && E <= kMaxE && D > 0 && D % 16 == 0, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(T * k < (1ll << 31), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(aligned16(x_q) && aligned16(xs_q) && (reinterpret_cast<uintptr_t>(workspace) & 3) == 0,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(workspace_bytes >= moe_ragged_sort_workspace_bytes(T, k, E), MOE_ERR_INVALID_ARG);
+  if (mode == MOE_SCALE_PER_ROW || mode == MOE_SCALE_PER_ROW_BLOCK128) {
+    MOE_HOST_CHECK(x_scale && xs_scale, MOE_ERR_INVALID_ARG);
+  } else {
+    MOE_HOST_CHECK(mode == MOE_SCALE_PER_TENSOR, MOE_ERR_INVALID_ARG);
+  }
+  cudaStream_t st = as_stream(stream);
+  const int64_t R = T * k;
+  const int64_t nc = num_chunks(R);
+  int* counts = static_cast<int*>(workspace);
+  const size_t hist_smem = sizeof(int) * kWarps * E;
+  if (nc > 0) {
+    if (hist_smem > 48 * 1024) {
+      MOE_CUDA_TRY(cudaFuncSetAttribute(sort_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(hist_smem)));
+      MOE_CUDA_TRY(cudaFuncSetAttribute(sort_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(hist_smem)));
+    }
+    sort_hist_kernel<<<static_cast<unsigned>(nc), 256, hist_smem, st>>>(topk_ids, R, E, counts);
+    MOE_CUDA_TRY(cudaGetLastError());
+  }
+  sort_scan_kernel<<<1, 1024, 0, st>>>(counts, static_cast<int>(nc), E, group_sizes, group_offsets);
+  MOE_CUDA_TRY(cudaGetLastError());
+  if (nc == 0) return MOE_OK;
+  sort_scatter_kernel<<<static_cast<unsigned>(nc), 256, hist_smem, st>>>(topk_ids, R, E, counts, sorted_src, pos);
+  MOE_CUDA_TRY(cudaGetLastError());
+  const unsigned gblocks = static_cast<unsigned>((T + 7) / 8);
+  if (mode == MOE_SCALE_PER_ROW)
+    sort_gather_kernel<MOE_SCALE_PER_ROW><<<gblocks, 256, 0, st>>>(x_q, x_scale, T, k, D, pos, xs_q, xs_scale);
+  else if (mode == MOE_SCALE_PER_ROW_BLOCK128)
+    sort_gather_kernel<MOE_SCALE_PER_ROW_BLOCK128>
+        <<<gblocks, 256, 0, st>>>(x_q, x_scale, T, k, D, pos, xs_q, xs_scale);
+  else
+    sort_gather_kernel<MOE_SCALE_PER_TENSOR><<<gblocks, 256, 0, st>>>(x_q, x_scale, T, k, D, pos, xs_q, xs_scale);
+  MOE_CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}

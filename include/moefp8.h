@@ -1,0 +1,255 @@
+/*
+ * moefp8.h -- C ABI of libmoefp8.so, the FP8-quantized MoE expert FFN on
+ * GB300 (sm_103a).
+ *
+ * The path, in order (forward):
+ *   1. moe_quantize_rows      bf16 activations -> e4m3 codes + fp32 scales
+ *   2. moe_ragged_sort        stable sort of the (token, expert) pairs by
+ *                             expert; gathers the quantised rows and scales
+ *   3. gmm_fp8                grouped matmul with [wi_0 | wi_1]
+ *   4. moe_swiglu_quant       h = silu(a0) * a1, requantised like step 1
+ *   5. gmm_fp8                grouped matmul with wo
+ *   6. ragged_gather_reduce   undo the sort, sum the top-k rows weighted by
+ *                             the router probabilities
+ * and, for the weight-gradient pass, tgmm_fp8 plus the helpers
+ * moe_gather_scale_quant, moe_swiglu_bwd_quant and moe_quantize_group_cols.
+ *
+ * Sources (MaxText pull-request pages):
+ *   [Q-EP]   "Quantize activations before EP all gather" (PR #4812).
+ *   [Q-GMM]  "Support quantization for tokamax gmm v2" (PR #4451).
+ *   [Q-FUSE] "Keep qwix out of tpu-inference's fused MoE kernel and
+ *            pre-quantize weights" (PR #5136).
+ *
+ * Conventions, for every entry point unless stated otherwise:
+ *   - Every pointer is a DEVICE pointer owned by the caller; the library
+ *     never frees or retains it.  Pointers must be 16-byte aligned.
+ *   - bf16 tensors are passed as uint16_t bit patterns; e4m3 tensors
+ *     ("float8_e4m3fn") as uint8_t codes; scales are IEEE fp32.
+ *   - Matrices are row-major and dense (row pitch = columns).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and returns before the GPU work finishes.
+ *   - The library allocates no device memory.  Kernels that need scratch
+ *     memory take a caller-provided workspace whose size a *_workspace_bytes
+ *     function reports.
+ *   - On a non-OK status nothing was launched, unless the status is
+ *     MOE_ERR_CUDA (a launch failed part way).  Outputs are undefined after
+ *     any error.
+ *   - Data-dependent problems found on the GPU (an expert id outside [0, E),
+ *     group sizes that do not add up, a bounded wait that ran out) set a
+ *     sticky device error word instead of faulting; the affected kernel
+ *     stops early.  Read and clear it with moe_get_device_error.
+ */
+#ifndef MOEFP8_H_
+#define MOEFP8_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* moe_stream_t; /* a cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, bad mode */
+  MOE_ERR_UNSUPPORTED = 2, /* shape or mode not built, or device is not sm_103 */
+  MOE_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+  MOE_ERR_DEVICE = 4       /* the device error word was non-zero */
+} moe_status;
+
+/* Scale modes.  The shape of a scale tensor follows from the mode:
+ *   MOE_SCALE_PER_ROW           [rows]            one scale per row (per token;
+ *                                                 for weights: per output channel)
+ *   MOE_SCALE_PER_ROW_BLOCK128  [rows, cols/128]  per row and per 128 columns
+ *                                                 (weights: see gmm_fp8)
+ *   MOE_SCALE_PER_TENSOR        [1]               one fixed scale (static scheme)
+ *   MOE_SCALE_PER_GROUP_COL     [E_local, cols]   one scale per (expert, column),
+ *                                                 for tgmm operands only */
+typedef enum {
+  MOE_SCALE_PER_ROW = 0,
+  MOE_SCALE_PER_ROW_BLOCK128 = 1,
+  MOE_SCALE_PER_TENSOR = 2,
+  MOE_SCALE_PER_GROUP_COL = 3
+} moe_scale_mode;
+
+/* Device error word bits. */
+#define MOE_DEVERR_BAD_EXPERT_ID 0x1u /* moe_ragged_sort: id outside [0, E) */
+#define MOE_DEVERR_GROUP_SIZES 0x2u   /* gmm/tgmm: negative size or sum != M */
+#define MOE_DEVERR_TIMEOUT 0x4u       /* a bounded wait in a tcgen05 kernel ran out */
+#define MOE_DEVERR_TMEM 0x8u          /* tensor-memory allocation returned no columns */
+
+const char* moe_status_string(moe_status s);
+
+/* Synchronises `stream`, stores the device error word of the current device
+ * in *code (0 = none) and clears it.  Returns MOE_ERR_DEVICE when *code != 0,
+ * MOE_ERR_CUDA when synchronisation failed, else MOE_OK. */
+moe_status moe_get_device_error(moe_stream_t stream, int* code);
+
+/* Number of streaming multiprocessors the persistent kernels size their grid
+ * by (the current device's SM count); 0 on error. */
+int moe_num_sms(void);
+
+/* ------------------------------------------------------------------------
+ * Step 1 -- activation quantisation ([Q-EP] description: quantise before the
+ * all-gather and the activation sort; [Q-GMM] review reply: fp8_dynamic uses
+ * absmax scales, fp8_static_wa fixed activation scales).
+ *
+ *   s = fp32(amax / 448)   (s = 1 when amax = 0)
+ *   q = e4m3(fp32(x / s))  round to nearest even, |v| > 448 saturates, the
+ *                          sign of zero is kept.
+ * x: bf16 [rows, cols].  q: e4m3 [rows, cols].
+ * mode PER_ROW: scale [rows]; PER_ROW_BLOCK128: scale [rows, cols/128];
+ * PER_TENSOR: static_scale (device, [1]) is used and `scale` is not written
+ * (may be NULL).  cols % 16 == 0 (a last block narrower than 128 columns
+ * takes its own scale); cols <= 32768; rows < 2^31.
+ */
+moe_status moe_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, moe_scale_mode mode,
+                             const float* static_scale, uint8_t* q, float* scale, moe_stream_t stream);
+
+/* Weight pre-quantisation ([Q-FUSE]: weights pre-quantised to float8_e4m3fn
+ * with [E, blocks, 1, N] scales).  w: bf16 [E, N, K] (output channel major,
+ * the contracted dimension K contiguous).  Each (e, n) row is quantised as in
+ * moe_quantize_rows.  Scale layouts: PER_ROW (per channel) [E, N];
+ * PER_ROW_BLOCK128 (blockwise) [E, K/128, N], the pages' [E, blocks, 1, N];
+ * PER_TENSOR uses static_scale.  K % 16 == 0 (% 128 for blockwise). */
+moe_status moe_quantize_weights(const uint16_t* w, int64_t E, int64_t N, int64_t K, moe_scale_mode mode,
+                                const float* static_scale, uint8_t* q, float* scale, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Step 2 -- ragged sort by routed expert, plus the gather of quantised rows
+ * and row scales ([Q-EP] review threads on ragged_sort / ragged_gather: the
+ * scale rows are gathered only when the scale's leading dimension is the
+ * token dimension).
+ *
+ * topk_ids: int32 [T, k]; flat pair i = t*k + j.  Stable counting sort by
+ * expert id, then by i.  Outputs:
+ *   sorted_src    int32 [T*k]   flat pair index at sorted position r
+ *   pos           int32 [T*k]   inverse: sorted position of pair i
+ *   group_sizes   int32 [E]
+ *   group_offsets int32 [E+1]   exclusive prefix sum of group_sizes
+ *   xs_q          e4m3 [T*k, D] xs_q[r] = x_q[sorted_src[r] / k]
+ *   xs_scale      PER_ROW: [T*k]; PER_ROW_BLOCK128: [T*k, D/128];
+ *                 PER_TENSOR: not written (may be NULL)
+ * workspace: device scratch of moe_ragged_sort_workspace_bytes(T, k, E)
+ * bytes (its contents need not be initialised).  An id outside [0, E) sets
+ * MOE_DEVERR_BAD_EXPERT_ID.  D % 16 == 0; 1 <= k <= 32; E <= 1024;
+ * T*k < 2^31.
+ */
+size_t moe_ragged_sort_workspace_bytes(int64_t T, int k, int E);
+moe_status moe_ragged_sort(const int32_t* topk_ids, int64_t T, int k, int E, const uint8_t* x_q,
+                           const float* x_scale, int64_t D, moe_scale_mode mode, int32_t* sorted_src, int32_t* pos,
+                           int32_t* group_sizes, int32_t* group_offsets, uint8_t* xs_q, float* xs_scale,
+                           void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Steps 3 and 5 -- grouped matmul ([Q-EP] review on gmm_v2: gmm(lhs_q,
+ * rhs_q, group_sizes, rhs_scale, group_offset) on already-quantised lhs, the
+ * lhs scale multiplying the output; bf16 output for fp8 operands; [Q-FUSE]:
+ * fp32 accumulation).
+ *
+ *   out[m, n] = sum_k deq(lhs)[m, k] * deq(rhs)[g(m) - group_offset, n, k]
+ *
+ * g(m) is the group holding row m (groups are consecutive row ranges of
+ * sizes group_sizes[0..E)).  Only groups [group_offset, group_offset +
+ * E_local) are computed; all other rows of out are written as zero.
+ *   lhs_q     e4m3 [M, K];  lhs_scale: PER_ROW [M], PER_ROW_BLOCK128
+ *             [M, K/128] or PER_TENSOR [1]
+ *   rhs_q     e4m3 [E_local, N, K] (K contiguous);  rhs_scale: PER_ROW (per
+ *             channel) [E_local, N], PER_ROW_BLOCK128 (blockwise)
+ *             [E_local, K/128, N], or PER_TENSOR [1]
+ *   out       bf16 [M, N], fp32 accumulation on the tensor cores; with a
+ *             blockwise operand each 128-wide K block is scaled and summed in
+ *             fp32 registers.
+ * Requires K % 16 == 0 (K % 128 == 0 when either side is blockwise),
+ * N % 16 == 0, sum(group_sizes) == M (else MOE_DEVERR_GROUP_SIZES), E <= 1024.
+ * Returns MOE_ERR_UNSUPPORTED on a device other than sm_103.
+ */
+moe_status gmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode, const uint8_t* rhs_q,
+                   const float* rhs_scale, moe_scale_mode rhs_mode, const int32_t* group_sizes, int E,
+                   int group_offset, int E_local, int64_t M, int64_t K, int64_t N, uint16_t* out,
+                   moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Step 4 -- SwiGLU and requantisation.  a = [a0 | a1], bf16 [R, 2F] (the
+ * wi_0 | wi_1 gmm output).  h = bf16(silu(a0) * a1) in fp32 with
+ * silu(z) = z / (1 + e^-z); h is quantised exactly as moe_quantize_rows does
+ * (same modes and scale shapes, cols = F).  F % 16 == 0, F <= 32768.
+ */
+moe_status moe_swiglu_quant(const uint16_t* a, int64_t R, int64_t F, moe_scale_mode mode,
+                            const float* static_scale, uint8_t* h_q, float* h_scale, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Step 6 -- ragged gather-reduce ([Q-EP]: ragged_gather_reduce un-permutes
+ * the expert outputs and sums the top-k rows of each token):
+ *   out[t, :] = bf16( sum_{j<k} weights[t, j] * rows[pos[t*k + j], :] )
+ * fp32 accumulation in ascending j.  rows bf16 [T*k, D]; pos int32 [T*k];
+ * weights fp32 [T, k] or NULL (all ones); out bf16 [T, D].  D % 8 == 0;
+ * 1 <= k <= 32.  A pos entry outside [0, T*k) contributes nothing.
+ */
+moe_status ragged_gather_reduce(const uint16_t* rows, const int32_t* pos, const float* weights, int64_t T, int k,
+                                int64_t D, uint16_t* out, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Backward helpers ([Q-GMM]: gmm and tgmm gradients, "absmax grad").
+ *
+ * moe_gather_scale_quant -- adjoint of the combine, fused with per-row
+ * quantisation:  dO[r] = bf16(fp32(w[i] * G[i / k])), i = sorted_src[r];
+ * then dO_q, dO_scale = per-row quantisation of dO as in moe_quantize_rows.
+ * G bf16 [T, D]; w fp32 [T*k] (NULL: ones); dO bf16 [T*k, D]; dO_q e4m3
+ * [T*k, D]; dO_scale [T*k].  D % 16 == 0.
+ */
+moe_status moe_gather_scale_quant(const uint16_t* G, const float* w, const int32_t* sorted_src, int64_t T, int k,
+                                  int64_t D, uint16_t* dO, uint8_t* dO_q, float* dO_scale, moe_stream_t stream);
+
+/* moe_swiglu_bwd_quant -- SwiGLU backward in fp32, rounded to bf16, fused
+ * with per-row quantisation of the concatenated [dA0 | dA1] row:
+ *   sigma = 1/(1 + e^-a0), silu = a0/(1 + e^-a0),
+ *   dA0 = (dH * a1) * sigma (1 + a0 (1 - sigma)),   dA1 = dH * silu.
+ * dH bf16 [R, F]; a bf16 [R, 2F]; dA bf16 [R, 2F]; dA_q e4m3 [R, 2F];
+ * dA_scale [R].  F % 16 == 0, 2F <= 32768. */
+moe_status moe_swiglu_bwd_quant(const uint16_t* dH, const uint16_t* a, int64_t R, int64_t F, uint16_t* dA,
+                                uint8_t* dA_q, float* dA_scale, moe_stream_t stream);
+
+/* moe_quantize_group_cols -- requantise a gradient with one absmax scale per
+ * (expert, column) over that expert's rows, so that both scales of the
+ * weight-gradient contraction factor out of the sum over rows.
+ * g bf16 [M, N]; q e4m3 [M, N] (rows outside the local groups are not
+ * written); scale fp32 [E_local, N] (an expert without rows, or an all-zero
+ * column, gets 1).  N % 16 == 0, E <= 1024.  `scale` is also used as the
+ * running maximum while the kernel runs. */
+moe_status moe_quantize_group_cols(const uint16_t* g, int64_t M, int64_t N, const int32_t* group_sizes, int E,
+                                   int group_offset, int E_local, uint8_t* q, float* scale, moe_stream_t stream);
+
+/* tgmm_fp8 -- transposed grouped matmul for weight gradients ([Q-GMM]:
+ * tgmm for grad_wi_0, grad_wi_1 and grad_wo):
+ *   out[e, k, n] = sum_{m in group e} deq(lhs)[m, k] * deq(rhs)[m, n]
+ * for local groups e in [0, E_local) (global group group_offset + e).
+ *   lhs_q e4m3 [M, K], lhs_scale PER_TENSOR [1] or PER_GROUP_COL [E_local, K]
+ *   rhs_q e4m3 [M, N], rhs_scale PER_TENSOR [1] or PER_GROUP_COL [E_local, N]
+ *   out   fp32 [E_local, K, N]; an expert without rows gets zeros.
+ * workspace: tgmm_fp8_workspace_bytes(M, K, N, E_local) bytes of device
+ * scratch (no initialisation needed); it holds both operands transposed, each
+ * group padded to 128 rows.  K % 16 == 0, N % 16 == 0, E <= 1024.
+ * Returns MOE_ERR_UNSUPPORTED on a device other than sm_103.
+ */
+size_t tgmm_fp8_workspace_bytes(int64_t M, int64_t K, int64_t N, int E_local);
+moe_status tgmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode, const uint8_t* rhs_q,
+                    const float* rhs_scale, moe_scale_mode rhs_mode, const int32_t* group_sizes, int E,
+                    int group_offset, int E_local, int64_t M, int64_t K, int64_t N, float* out, void* workspace,
+                    size_t workspace_bytes, moe_stream_t stream);
+
+/* moe_transpose_u8 -- weight layout preparation for the backward pass (run
+ * once, outside the FFN): batched byte transpose src [B, R, C] -> dst
+ * [B, C, R] of e4m3 codes.  The input-gradient gmm contracts over the
+ * weights' output channels, so it reads the weights transposed.  With a
+ * per-tensor weight scale the transposed codes are exactly the codes of the
+ * transposed weights.  R % 16 == 0, C % 16 == 0. */
+moe_status moe_transpose_u8(const uint8_t* src, int64_t B, int64_t R, int64_t C, uint8_t* dst, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEFP8_H_ */

@@ -26,6 +26,7 @@ import torch
 PER_ROW = 0           # one fp32 scale per row
 PER_ROW_BLOCK128 = 1  # one fp32 scale per row and per 128 columns
 PER_TENSOR = 2        # one fixed fp32 scale for the whole tensor
+PER_GROUP_COL = 3     # one fp32 scale per (expert, column) (weight-gradient operands)
 
 
 @dataclasses.dataclass(frozen=True)

@@ -1,0 +1,109 @@
+"""GPU parity of the tcgen05 grouped matmuls (gmm_fp8, tgmm_fp8) against the
+oracle: relative Frobenius <= 2e-3 and max |delta| <= 1e-2 max|ref| after
+bf16 rounding, over several tiles, ragged group tails, empty groups, partial
+N tiles, K tails and expert-parallel shards."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.gpu_helpers import assert_close, dev, host, rand_codes, ragged_sizes
+
+pytestmark = pytest.mark.gpu
+
+moe = pytest.importorskip("fp8_quantized_moe_gb300")
+
+R0, RB, RT, GC = synth.PER_ROW, synth.PER_ROW_BLOCK128, synth.PER_TENSOR, synth.PER_GROUP_COL
+
+
+def make_case(seed, M, K, N, E, amode, wmode, zero_frac=0.25):
+    rng = np.random.default_rng(seed)
+    sizes = ragged_sizes(rng, E, M, zero_frac)
+    a = rand_codes(rng, (M, K))
+    w = rand_codes(rng, (E, N, K))
+    nb = oracle.nblocks(K)
+    sa = {R0: rng.uniform(0.5, 2, M), RB: rng.uniform(0.5, 2, (M, nb)), RT: [0.7]}[amode]
+    sw = {R0: rng.uniform(0.5, 2, (E, N)), RB: rng.uniform(0.5, 2, (E, nb, N)), RT: [1.3]}[wmode]
+    # scale the scales so that outputs are O(1): e4m3 codes reach 448
+    sa = (np.asarray(sa) / 448.0).astype(np.float32)
+    sw = (np.asarray(sw) / (448.0 * np.sqrt(K))).astype(np.float32)
+    return sizes, a, w, sa, sw
+
+
+@pytest.mark.parametrize("M,K,N,E,amode,wmode", [
+    (128, 128, 256, 1, R0, R0),      # one tile
+    (1, 128, 256, 1, R0, R0),        # a single row
+    (200, 256, 512, 3, R0, R0),      # ragged groups, several tiles
+    (300, 128, 144, 4, R0, R0),      # N not a multiple of the tile
+    (257, 48, 256, 2, R0, R0),       # K tail (48 < 128)
+    (640, 512, 256, 8, RT, R0),      # static lhs, per-channel rhs
+    (640, 512, 256, 8, RT, RT),
+    (384, 384, 256, 3, RB, RB),      # blockwise both sides (promotion)
+    (384, 384, 512, 5, R0, RB),      # per-row lhs, blockwise rhs
+    (256, 256, 128, 2, RB, R0),
+    (1500, 1024, 768, 16, R0, R0),
+    (2048, 2048, 1536, 128, R0, RB),  # prefill-chunk shaped, E = 128
+])
+def test_gmm_matches_oracle(M, K, N, E, amode, wmode):
+    sizes, a, w, sa, sw = make_case(M * 31 + K + N + E, M, K, N, E, amode, wmode)
+    ref = oracle.gmm(a, sa, amode, w, sw, wmode, sizes)
+    out = moe.gmm(dev(a), dev(sa), amode, dev(w), dev(sw), wmode, dev(sizes))
+    assert moe.device_error() == 0
+    assert_close(host(out), ref, f"gmm M={M} K={K} N={N} E={E}")
+
+
+def test_gmm_expert_parallel_shard_zeroes_other_rows():
+    M, K, N, E = 700, 256, 256, 8
+    sizes, a, w, sa, sw = make_case(5, M, K, N, E, R0, R0, zero_frac=0.0)
+    g0, El = 2, 3
+    ref = oracle.gmm(a, sa, R0, w[g0:g0 + El], sw[g0:g0 + El], R0, sizes, group_offset=g0, E_local=El)
+    out = moe.gmm(dev(a), dev(sa), R0, dev(w[g0:g0 + El].copy()), dev(sw[g0:g0 + El].copy()), R0, dev(sizes),
+                  group_offset=g0, E_local=El)
+    o = host(out)
+    starts = np.concatenate([[0], np.cumsum(sizes)])
+    lo, hi = starts[g0], starts[g0 + El]
+    assert np.all(o[:lo] == 0) and np.all(o[hi:] == 0)
+    assert_close(o, ref, "gmm shard")
+
+
+def test_gmm_bad_group_sizes_sets_device_error():
+    M, K, N = 64, 128, 256
+    a = np.zeros((M, K), np.uint8)
+    w = np.zeros((2, N, K), np.uint8)
+    sizes = np.array([10, 20], np.int32)  # sums to 30 != 64
+    moe.gmm(dev(a), dev(np.ones(M, np.float32)), R0, dev(w), dev(np.ones((2, N), np.float32)), R0, dev(sizes))
+    assert moe.device_error() & 0x2
+
+
+def test_gmm_accumulation_over_long_k():
+    """K = 14336 (the wo projection of the Mixtral-shaped layer): fp32
+    accumulation on the tensor cores must stay within the tolerance."""
+    M, K, N, E = 256, 14336, 256, 2
+    sizes, a, w, sa, sw = make_case(11, M, K, N, E, R0, R0, zero_frac=0.0)
+    ref = oracle.gmm(a, sa, R0, w, sw, R0, sizes)
+    out = moe.gmm(dev(a), dev(sa), R0, dev(w), dev(sw), R0, dev(sizes))
+    assert_close(host(out), ref, "gmm long K")
+
+
+@pytest.mark.parametrize("M,K,N,E,lmode,rmode", [
+    (128, 128, 256, 1, RT, RT),
+    (300, 256, 512, 4, RT, GC),
+    (1000, 384, 256, 9, GC, GC),
+    (2000, 128, 2816, 16, RT, GC),
+])
+def test_tgmm_matches_oracle(M, K, N, E, lmode, rmode):
+    rng = np.random.default_rng(M + K + N)
+    sizes = ragged_sizes(rng, E, M)
+    x = rand_codes(rng, (M, K))
+    g = rand_codes(rng, (M, N))
+    sx = np.array([0.01], np.float32) if lmode == RT else rng.uniform(0.5, 2, (E, K)).astype(np.float32) / 448
+    sg = np.array([0.02], np.float32) if rmode == RT else rng.uniform(0.5, 2, (E, N)).astype(np.float32) / 448
+    ref = oracle.tgmm(x, sx, lmode, g, sg, rmode, sizes)
+    out = moe.tgmm(dev(x), dev(sx), lmode, dev(g), dev(sg), rmode, dev(sizes))
+    assert moe.device_error() == 0
+    o = host(out)
+    for e in np.flatnonzero(sizes == 0):
+        assert np.all(o[e] == 0)
+    assert_close(o, ref, f"tgmm M={M} K={K} N={N} E={E}")
