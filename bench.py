@@ -37,10 +37,11 @@ L2_BYTES = 129 * 1024 * 1024
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="mixtral", choices=list(synth.CONFIGS))
+    ap.add_argument("--tokens", type=int, default=0, help="override T (small cases for profiling)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0, help="oracle sample size (0 = auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -169,6 +170,11 @@ def run_ours(args, cfg, rank, world, local):
     x_host, ids_np, w_np = host_inputs(cfg, seed=rank)
     w_in, w_out = synth.expert_weights(cfg, 0, device=dev)
     W = moe.prepare_weights(w_in, w_out, cfg.w_mode, static)
+    torch.cuda.synchronize()
+    if rank != 0 or args.no_cpu_baseline:
+        # only the fp8 copies stay resident; the oracle leg needs the bf16 weights
+        w_in = w_out = None
+        torch.cuda.empty_cache()
     x = x_host.to(dev)
     ids = torch.from_numpy(ids_np).to(dev)
     w = torch.from_numpy(w_np).to(dev)
@@ -349,6 +355,8 @@ def run_reference(args, cfg, rank, world):
 def main():
     args = parse()
     cfg = synth.CONFIGS[args.config]
+    if args.tokens:
+        cfg = synth.scaled(cfg, T=args.tokens)
     rank, world, local = dist_env()
     if args.impl == "reference":
         res = run_reference(args, cfg, rank, world)
