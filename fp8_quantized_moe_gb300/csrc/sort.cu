@@ -258,3 +258,53 @@ extern "C" moe_status moe_ragged_sort(const int32_t* topk_ids, int64_t T, int k,
   MOE_CUDA_TRY(cudaGetLastError());
   return MOE_OK;
 }
+
+// ---------------------------------------------------------------------------
+// moe_ragged_sort_noalloc: the same sort for callers that cannot allocate
+// device memory.  Its scratch (the per-(chunk, expert) counts) lives in a
+// fixed file-scope device array; every GPU that loads this library holds it
+// until the process exits.  Host code cannot pass `g_sort_scratch` itself to
+// a kernel (in host code the name denotes a host-side shadow, not a device
+// address), so the device address is looked up once per device with
+// cudaGetSymbolAddress, with that device current, on the first call.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = MOE_RAGGED_SORT_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) int g_sort_scratch[kNoAllocScratchBytes / sizeof(int)];
+
+constexpr int kMaxDevices = 256;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_ragged_sort_noalloc(const int32_t* topk_ids, int64_t T, int k, int E, const uint8_t* x_q,
+                                              const float* x_scale, int64_t D, moe_scale_mode mode,
+                                              int32_t* sorted_src, int32_t* pos, int32_t* group_sizes,
+                                              int32_t* group_offsets, uint8_t* xs_q, float* xs_scale,
+                                              moe_stream_t stream) {
+  if (T < 0 || k <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+  // the counts need nchunks * E ints; larger problems do not fit the array
+  if (moe_ragged_sort_workspace_bytes(T, k, E) > moe::kNoAllocScratchBytes) return MOE_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= moe::kMaxDevices) return MOE_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(moe::g_scratch_mu);
+    if (!moe::g_scratch_addr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, moe::g_sort_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+      moe::g_scratch_addr[dev] = p;
+    }
+    scratch = moe::g_scratch_addr[dev];
+  }
+  // every count the sort reads is written by its histogram kernel first, so
+  // the array needs no clearing between calls
+  return moe_ragged_sort(topk_ids, T, k, E, x_q, x_scale, D, mode, sorted_src, pos, group_sizes, group_offsets,
+                         xs_q, xs_scale, scratch, moe::kNoAllocScratchBytes, stream);
+}

@@ -143,6 +143,32 @@ moe_status moe_ragged_sort(const int32_t* topk_ids, int64_t T, int k, int E, con
                            int32_t* group_sizes, int32_t* group_offsets, uint8_t* xs_q, float* xs_scale,
                            void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* moe_ragged_sort_noalloc -- moe_ragged_sort for callers that cannot
+ * allocate device memory.  The pages have no counterpart: it exists for
+ * hosts that own every byte of device memory themselves (an inference engine
+ * whose pool has already claimed the free HBM, a plugin interface that hands
+ * out no allocator) and for latency-critical loops where cudaMalloc, which
+ * may synchronise the device, is not allowed.  Arguments and results are
+ * those of moe_ragged_sort without the workspace.
+ *
+ * The scratch is a fixed device array of MOE_RAGGED_SORT_NOALLOC_SCRATCH_BYTES
+ * (1 MiB) inside the library; every GPU that loads the library holds it
+ * until the process exits.  Problems for which
+ * moe_ragged_sort_workspace_bytes(T, k, E) exceeds it -- with E = 256, more
+ * than 2^21 (token, expert) pairs -- are rejected with MOE_ERR_INVALID_ARG
+ * before anything is launched.  The first call on a device looks up the
+ * array's device address (once per device, with that device current); make
+ * that first call before any stream capture.  All calls on a device share
+ * the one array: calls that overlap on the GPU (on different streams, or from
+ * different host threads) race and corrupt each other's results.  Each call
+ * writes every count it reads, so nothing carries over between calls.  No
+ * device memory is allocated or freed. */
+#define MOE_RAGGED_SORT_NOALLOC_SCRATCH_BYTES (1u << 20)
+moe_status moe_ragged_sort_noalloc(const int32_t* topk_ids, int64_t T, int k, int E, const uint8_t* x_q,
+                                   const float* x_scale, int64_t D, moe_scale_mode mode, int32_t* sorted_src,
+                                   int32_t* pos, int32_t* group_sizes, int32_t* group_offsets, uint8_t* xs_q,
+                                   float* xs_scale, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Steps 3 and 5 -- grouped matmul ([Q-EP] review on gmm_v2: gmm(lhs_q,
  * rhs_q, group_sizes, rhs_scale, group_offset) on already-quantised lhs, the
