@@ -30,7 +30,7 @@ PER_GROUP_COL = 3
 
 __all__ = [
     "PER_ROW", "PER_ROW_BLOCK128", "PER_TENSOR", "PER_GROUP_COL", "MoEError", "lib", "device_error",
-    "quantize_rows", "quantize_weights", "ragged_sort", "gmm", "swiglu_quant", "ragged_gather_reduce",
+    "quantize_rows", "quantize_weights", "ragged_sort", "gmm", "gmm_swiglu", "swiglu_fusable", "swiglu_quant", "ragged_gather_reduce",
     "gather_scale_quant", "swiglu_bwd_quant", "quantize_group_cols", "tgmm", "transpose_u8",
     "ExpertWeights", "prepare_weights", "FFNBuffers", "ffn_forward", "ffn_backward",
 ]
@@ -140,6 +140,37 @@ def gmm(lhs_q, lhs_scale, lhs_mode, rhs_q, rhs_scale, rhs_mode, group_sizes, gro
     check(lib().gmm_fp8(_p(lhs_q), _p(lhs_scale), lhs_mode, _p(rhs_q), _p(rhs_scale), rhs_mode, _p(group_sizes),
                         E, group_offset, E_local, M, K, N, _p(out), _s()), "gmm_fp8")
     return out
+
+
+def gmm_swiglu(lhs_q, lhs_scale, lhs_mode, rhs_q, rhs_scale, rhs_mode, group_sizes, h_mode: int,
+               h_static: Optional[torch.Tensor] = None, group_offset: int = 0, E_local: Optional[int] = None,
+               keep_a: bool = False, a_out=None, h=None, h_q=None, h_scale=None):
+    """gmm with [wi_0 | wi_1] fused with SwiGLU and the requantisation of h.
+
+    Returns (h_q uint8 [M, F], h_scale or None, a [M, 2F] bf16 or None)."""
+    M, K = lhs_q.shape
+    El, F2, K2 = rhs_q.shape
+    if K2 != K:
+        raise MoEError("lhs/rhs K mismatch")
+    F = F2 // 2
+    dev = lhs_q.device
+    E = group_sizes.numel()
+    E_local = El if E_local is None else E_local
+    h_q = torch.empty(M, F, dtype=torch.uint8, device=dev) if h_q is None else h_q
+    h_scale = _scale_buf(h_mode, M, F, dev, h_scale)
+    if h_mode == PER_ROW and h is None:
+        h = torch.empty(M, F, dtype=torch.bfloat16, device=dev)
+    if keep_a and a_out is None:
+        a_out = torch.empty(M, F2, dtype=torch.bfloat16, device=dev)
+    check(lib().gmm_fp8_swiglu(_p(lhs_q), _p(lhs_scale), lhs_mode, _p(rhs_q), _p(rhs_scale), rhs_mode,
+                               _p(group_sizes), E, group_offset, E_local, M, K, F, h_mode, _p(h_static), _p(a_out),
+                               _p(h), _p(h_q), _p(h_scale), _s()), "gmm_fp8_swiglu")
+    return h_q, h_scale, a_out
+
+
+def swiglu_fusable(act_mode: int, w_mode: int, F: int) -> bool:
+    """gmm_fp8_swiglu covers per-row / per-tensor operand scales and F % 128 == 0."""
+    return act_mode in (PER_ROW, PER_TENSOR) and w_mode in (PER_ROW, PER_TENSOR) and F % 128 == 0
 
 
 def swiglu_quant(a: torch.Tensor, mode: int, static_scale: Optional[torch.Tensor] = None, h_q=None, h_scale=None):
@@ -292,6 +323,8 @@ class FFNBuffers:
         self.x_s = _scale_buf(act_mode, T, D, device)
         self.sort = {}
         self.a = f(R, 2 * F, dt=torch.bfloat16)
+        self.h = f(R, F, dt=torch.bfloat16)  # scratch of the fused per-row path
+        self.keep_a = backward
         self.h_q = f(R, F)
         self.h_s = _scale_buf(act_mode, R, F, device)
         self.o = f(R, D, dt=torch.bfloat16)
@@ -304,15 +337,23 @@ class FFNBuffers:
 
 def ffn_forward(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, W: ExpertWeights, act_mode: int,
                 buf: FFNBuffers, static_x: Optional[torch.Tensor] = None,
-                static_h: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """One forward pass of the expert FFN; returns buf.y (bf16 [T, D])."""
+                static_h: Optional[torch.Tensor] = None, fuse_swiglu: bool = True) -> torch.Tensor:
+    """One forward pass of the expert FFN; returns buf.y (bf16 [T, D]).
+
+    Where the scale modes allow it, steps 3 and 4 run as one fused kernel
+    (gmm_fp8_swiglu, bit-identical to gmm_fp8 + moe_swiglu_quant); buf.a then
+    holds a only when the buffers were made for a backward pass."""
     E = W.w_in.shape[0]
     k = topk_ids.shape[1]
     quantize_rows(x, act_mode, static_x, q=buf.x_q, scale=buf.x_s)
     s = ragged_sort(topk_ids, E, buf.x_q, buf.x_s if act_mode != PER_TENSOR else static_x, act_mode, out=buf.sort)
     xs_s = s["xs_scale"] if act_mode != PER_TENSOR else static_x
-    gmm(s["xs_q"], xs_s, act_mode, W.w_in, W.s_in, W.in_mode, s["group_sizes"], out=buf.a)
-    swiglu_quant(buf.a, act_mode, static_h, h_q=buf.h_q, h_scale=buf.h_s)
+    if fuse_swiglu and swiglu_fusable(act_mode, W.in_mode, buf.F):
+        gmm_swiglu(s["xs_q"], xs_s, act_mode, W.w_in, W.s_in, W.in_mode, s["group_sizes"], act_mode, static_h,
+                   a_out=buf.a if buf.keep_a else None, h=buf.h, h_q=buf.h_q, h_scale=buf.h_s)
+    else:
+        gmm(s["xs_q"], xs_s, act_mode, W.w_in, W.s_in, W.in_mode, s["group_sizes"], out=buf.a)
+        swiglu_quant(buf.a, act_mode, static_h, h_q=buf.h_q, h_scale=buf.h_s)
     h_s = buf.h_s if act_mode != PER_TENSOR else static_h
     gmm(buf.h_q, h_s, act_mode, W.w_out, W.s_out, W.out_mode, s["group_sizes"], out=buf.o)
     ragged_gather_reduce(buf.o, s["pos"], topk_w, k, out=buf.y)

@@ -83,11 +83,8 @@ __device__ __forceinline__ float absmax_scale(float amax) { return amax > 0.0f ?
 // ------------------------------------------------------------------------
 __device__ __forceinline__ float pow2i(int i) { return __int_as_float((i + 127) << 23); }
 
-__device__ __forceinline__ float exp_f32(float x) {
-  if (x != x) return x;
-  if (x > 88.72283935546875f) return __int_as_float(0x7f800000);
-  if (x < -103.972076416015625f) return 0.0f;
-  const float n = rintf(__fmul_rn(x, 1.44269502162933349609375f));
+__device__ __forceinline__ float exp_poly(float x, float& n) {
+  n = rintf(__fmul_rn(x, 1.44269502162933349609375f));
   float r = __fmaf_rn(-n, 0.693145751953125f, x);
   r = __fmaf_rn(-n, 1.428606765330187045e-6f, r);
   float p = 1.0f / 5040.0f;
@@ -98,11 +95,138 @@ __device__ __forceinline__ float exp_f32(float x) {
   p = __fmaf_rn(p, r, 0.5f);
   p = __fmaf_rn(p, r, 1.0f);
   p = __fmaf_rn(p, r, 1.0f);
+  return p;
+}
+
+__device__ __forceinline__ float exp_f32(float x) {
+  float n;
+  if (fabsf(x) <= 87.0f) {
+    // n lies in [-126, 126], so 2^n is a normal float and the single product
+    // rounds once -- the same value as the two-step scaling below, whose
+    // first step is exact.
+    const float p = exp_poly(x, n);
+    return __fmul_rn(p, pow2i(static_cast<int>(n)));
+  }
+  if (x != x) return x;
+  if (x > 88.72283935546875f) return __int_as_float(0x7f800000);
+  if (x < -103.972076416015625f) return 0.0f;
+  float p = exp_poly(x, n);
   const int ni = static_cast<int>(n);
   const int n1 = ni / 2, n2 = ni - n1;
   p = __fmul_rn(p, pow2i(n1));
   p = __fmul_rn(p, pow2i(n2));
   return p;
+}
+
+__device__ __forceinline__ float silu_f32(float z) { return __fdiv_rn(z, __fadd_rn(1.0f, exp_f32(-z))); }
+
+// ---- branch-free forms of the same arithmetic ----------------------------
+// The per-element code below has no data-dependent branch in its common
+// range, so that a thread's elements form one basic block the compiler can
+// interleave.  Each helper flags the rare inputs it does not cover and the
+// caller recomputes those with the exact per-element path, so the values are
+// bit-identical to exp_f32 / __fdiv_rn / quant_quotient.
+
+__device__ __forceinline__ float rcp_approx(float b) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(b));
+  return y;
+}
+
+// exp_f32 for |x| <= 87 (no range checks; same value).
+__device__ __forceinline__ float exp_fast(float x) {
+  float n;
+  const float p = exp_poly(x, n);
+  return __fmul_rn(p, pow2i(static_cast<int>(n)));
+}
+
+// fp32(a / b), correctly rounded, for b in [1, 2^30] and a = 0 or
+// 2^-60 <= |a| <= 2^20.  A reciprocal estimate y and one correction step
+// (Markstein's method, q1 = q0 + (a - b q0) y) give a candidate q1; q1 is the
+// correctly rounded quotient iff |a/b - q1| < ulp(q1)/2, i.e. iff
+// |a - b q1| * 2^(24 - E(q1)) < b.  The residual is computed with one fused
+// multiply-add and the scaling by a power of two is exact, so the test is
+// rounding-monotone and never accepts a wrong q1 (a quotient of two fp32
+// values is never exactly halfway between two floats).  `ok` is cleared when
+// the test fails.
+__device__ __forceinline__ float div_checked(float a, float b, bool& ok) {
+  const float y = rcp_approx(b);
+  const float q0 = __fmul_rn(a, y);
+  const float r0 = __fmaf_rn(-b, q0, a);
+  const float q1 = __fmaf_rn(r0, y, q0);
+  const float r1 = __fmaf_rn(-b, q1, a);
+  const uint32_t eb = (__float_as_uint(q1) >> 23) & 0xFFu;
+  const float sc = __uint_as_float((278u - eb) << 23);  // 2^(24 - E(q1))
+  ok = ok && (a == 0.0f || __fmul_rn(fabsf(r1), sc) < b);
+  return a == 0.0f ? a : q1;  // keeps the sign of a zero numerator
+}
+
+// Range in which the SwiGLU fast path applies: |z| <= 20 keeps e^-z in
+// [2^-29, 2^29] and the quotients normal.
+__device__ __forceinline__ bool swiglu_fast_range(float z) {
+  const float a = fabsf(z);
+  return a <= 20.0f && (a >= 0x1p-60f || a == 0.0f);
+}
+
+// h[j] = bf16(silu(a0[j]) * a1[j]) for N elements.
+template <int N>
+__device__ __forceinline__ void swiglu_h(const float* a0, const float* a1, float* h) {
+  bool fast = true;
+#pragma unroll
+  for (int j = 0; j < N; ++j) fast = fast && swiglu_fast_range(a0[j]);
+  if (fast) {
+    bool ok = true;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      const float d = __fadd_rn(1.0f, exp_fast(-a0[j]));
+      h[j] = round_bf16(__fmul_rn(div_checked(a0[j], d, ok), a1[j]));
+    }
+    if (ok) return;
+  }
+#pragma unroll
+  for (int j = 0; j < N; ++j) h[j] = round_bf16(__fmul_rn(silu_f32(a0[j]), a1[j]));
+}
+
+// True when e4m3(x * inv_s) may differ from e4m3(fp32(x / s)) (see below).
+__device__ __forceinline__ bool quant_needs_division(float y) {
+  const uint32_t u = __float_as_uint(y);
+  const bool near_mid = ((u & 0xFFFFFu) - 0x80000u + 8u) <= 16u;
+  const bool small = ((u & 0x7FFFFFFFu) - 1u) < (0x3C800000u - 1u);  // 0 < |y| < 2^-6
+  return near_mid || small;
+}
+
+// out[j] = fp32(x[j] / s) as far as e4m3 rounding can tell, for N elements.
+template <int N>
+__device__ __forceinline__ void quant_n(const float* x, float s, float inv, float* out) {
+  bool slow = false;
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    out[j] = __fmul_rn(x[j], inv);
+    slow = slow || quant_needs_division(out[j]);
+  }
+  if (slow) {
+#pragma unroll
+    for (int j = 0; j < N; ++j)
+      if (quant_needs_division(out[j])) out[j] = __fdiv_rn(x[j], s);
+  }
+}
+
+// The quotient that e4m3 quantisation rounds, fp32(x / s), without a division
+// per element.  y = x * inv_s with inv_s = 1/s rounded to nearest lies within
+// 2 ulp of x / s (two roundings of relative size 2^-24).  Rounding to e4m3
+// keeps 3 mantissa bits, so y and fp32(x / s) can only round to different
+// e4m3 values when a midpoint between two e4m3 values (low 20 mantissa bits
+// 0x80000) lies within those ulp, or in the e4m3 subnormal range |y| < 2^-6
+// where the rounding position moves.  Those rare values take the exact
+// division; everywhere else e4m3(y) == e4m3(fp32(x / s)).  Above 448 every
+// value saturates to 448 either way.
+__device__ __forceinline__ float quant_quotient(float x, float s, float inv_s) {
+  const float y = __fmul_rn(x, inv_s);
+  const uint32_t u = __float_as_uint(y);
+  const bool near_mid = ((u & 0xFFFFFu) - 0x80000u + 8u) <= 16u;
+  const bool small = (u & 0x7FFFFFFFu) < 0x3C800000u;
+  if (near_mid || small) return __fdiv_rn(x, s);
+  return y;
 }
 
 // ------------------------------------------------------------------------
@@ -189,6 +313,12 @@ __device__ __forceinline__ void tmem_relinquish() {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
+// Barrier among `count` threads (a multiple of 32) on hardware barrier `id`
+// (1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }

@@ -56,11 +56,11 @@ constexpr int kMaxGroups = 1024;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint32_t kTmemCols = 512;
 
-enum Mode { kFinal = 0, kPromote = 1, kTgmm = 2 };
+enum Mode { kFinal = 0, kPromote = 1, kTgmm = 2, kSwiglu = 3 };
 
 template <int MODE>
 struct Cfg {
-  static constexpr int EPI_WARPS = MODE == kPromote ? 8 : 4;
+  static constexpr int EPI_WARPS = (MODE == kPromote || MODE == kSwiglu) ? 8 : 4;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
 };
 
@@ -77,6 +77,14 @@ struct Params {
   const float* rhs_scale;
   int rhs_mode;
   void* out;
+  // kSwiglu: h = bf16(silu(a0) a1) requantised; a = [a0 | a1] optionally kept
+  int F;
+  int h_mode;
+  const float* h_static;
+  uint16_t* a_out;     // [M, 2F] bf16 or null
+  uint16_t* h_out;     // [M, F] bf16 (per-row h scales)
+  uint8_t* h_q;        // [M, F] e4m3 (per-tensor / per-128 h scales)
+  float* h_scale;      // per-row: running amax [M]; per-128: [M, F/128]
 };
 
 struct SmemCtl {
@@ -93,6 +101,7 @@ struct SmemCtl {
   int tile_prefix[kMaxGroups + 1];  // gmm: first tile of local group
   int gsize[kMaxGroups];
   float sw_stage[8][128];           // promotion: weight scales of the current K block, per warp
+  float pamax[2][4][2][32];          // fused SwiGLU, per-128 h scales: row maxima of the two column halves
 };
 
 constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(NSTAGE) * STAGE_BYTES + sizeof(SmemCtl);
@@ -207,8 +216,14 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const SmemCtl* ctl, in
     tl.ax = 0;
     tl.ay = tl.row0;
     tl.bx = 0;
-    tl.by = lo * p.N + nt * BN;
-    tl.n0 = nt * BN;
+    if (MODE == kSwiglu) {
+      // 128 h columns: wi_0 channels nt*128.. and the matching wi_1 channels
+      tl.by = lo * 2 * p.F + nt * 128;
+      tl.n0 = nt * 128;
+    } else {
+      tl.by = lo * p.N + nt * BN;
+      tl.n0 = nt * BN;
+    }
   }
   return tl;
 }
@@ -308,7 +323,13 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
           const uint32_t sa = base + s * STAGE_BYTES;
           tma_load_2d(sa, &tmA, tl.ax + kb * BK, tl.ay, fb);
-          tma_load_2d(sa + A_BYTES, &tmB, tl.bx + kb * BK, tl.by, fb);
+          if (MODE == kSwiglu) {
+            // B rows 0..127: wi_0 channels; rows 128..255: the matching wi_1 channels
+            tma_load_2d(sa + A_BYTES, &tmB, tl.bx + kb * BK, tl.by, fb);
+            tma_load_2d(sa + 2 * A_BYTES, &tmB, tl.bx + kb * BK, tl.by + p.F, fb);
+          } else {
+            tma_load_2d(sa + A_BYTES, &tmB, tl.bx + kb * BK, tl.by, fb);
+          }
           ++it;
         }
       }
@@ -388,7 +409,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q4 = warp & 3;                            // TMEM lane quarter of this warp
-    const int half = (MODE == kPromote) ? (warp - 2) >> 2 : 0;  // column half (promotion only)
+    const int half = (MODE == kPromote || MODE == kSwiglu) ? (warp - 2) >> 2 : 0;  // column half
     const int r = q4 * 32 + lane;                       // row of the tile = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
     uint32_t acc = 0;
@@ -438,6 +459,114 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
         ++acc;
+      } else if (MODE == kSwiglu) {
+        // 8 warps: TMEM lane quarter q4, h columns [half*64, half*64 + 64) of
+        // the tile; accumulator columns c*32.. hold a0, 128 + c*32.. hold a1.
+        const int64_t row = static_cast<int64_t>(tl.row0) + r;
+        const uint32_t a = acc & 1;
+        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc >> 1) & 1, abort_flag, kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+        const float sa = row_ok ? lhs_scale_at(p, row, 0) : 0.f;
+        const bool per_chan = p.rhs_mode == MOE_SCALE_PER_ROW;
+        const float* swb = p.rhs_scale + (per_chan ? static_cast<int64_t>(tl.el) * 2 * p.F : 0);
+        float hs = 1.0f, hinv = 1.0f;
+        if (p.h_mode == MOE_SCALE_PER_TENSOR) {
+          hs = __ldg(p.h_static);
+          hinv = __frcp_rn(hs);
+        }
+        float amax = 0.0f;
+        uint32_t hp[32];  // this warp's 64 h values of the row, bf16 pairs (per-128 h scales)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = half * 2 + cc;
+          uint32_t v0[32], v1[32];
+          tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + c * 32, v0);
+          tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + 128 + c * 32, v1);
+          tmem_wait_ld();
+          if (cc == 1) {  // the accumulator is no longer needed: release it early
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
+          }
+          const int hc = tl.n0 + c * 32;  // first h column of the chunk
+          float f0[32], f1[32], h[32];
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            float4 s0, s1;
+            if (per_chan) {
+              s0 = __ldg(reinterpret_cast<const float4*>(swb + hc) + g);
+              s1 = __ldg(reinterpret_cast<const float4*>(swb + p.F + hc) + g);
+            } else {
+              s0.x = s0.y = s0.z = s0.w = __ldg(swb);
+              s1 = s0;
+            }
+            const float w0[4] = {s0.x, s0.y, s0.z, s0.w}, w1[4] = {s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              // a0, a1 rounded to bf16 exactly as gmm_fp8 stores them
+              f0[g * 4 + j] = round_bf16(__fmul_rn(__fmul_rn(__uint_as_float(v0[g * 4 + j]), sa), w0[j]));
+              f1[g * 4 + j] = round_bf16(__fmul_rn(__fmul_rn(__uint_as_float(v1[g * 4 + j]), sa), w1[j]));
+            }
+          }
+          swiglu_h<32>(f0, f1, h);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(h[j]));
+          if (row_ok) {
+            if (p.a_out) {
+              store_bf16x32(p.a_out + row * 2 * p.F + hc, f0, 32);
+              store_bf16x32(p.a_out + row * 2 * p.F + p.F + hc, f1, 32);
+            }
+            if (p.h_mode == MOE_SCALE_PER_ROW) {
+              store_bf16x32(p.h_out + row * p.F + hc, h, 32);
+            } else if (p.h_mode == MOE_SCALE_PER_TENSOR) {
+              float qv[32];
+              quant_n<32>(h, hs, hinv, qv);
+              uint4* dst = reinterpret_cast<uint4*>(p.h_q + row * p.F + hc);
+#pragma unroll
+              for (int g = 0; g < 2; ++g) {
+                const uint2 lo8 = pack_e4m3x8(qv + 16 * g), hi8 = pack_e4m3x8(qv + 16 * g + 8);
+                dst[g] = make_uint4(lo8.x, lo8.y, hi8.x, hi8.y);
+              }
+            }
+          }
+          if (p.h_mode == MOE_SCALE_PER_ROW_BLOCK128) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) hp[cc * 16 + j] = pack_bf16x2(h[2 * j], h[2 * j + 1]);
+          }
+        }
+        const int par = acc & 1;
+        ++acc;
+        if (p.h_mode == MOE_SCALE_PER_ROW) {
+          // non-negative floats order like their bit patterns
+          if (row_ok) atomicMax(reinterpret_cast<unsigned int*>(p.h_scale) + row, __float_as_uint(amax));
+        } else if (p.h_mode == MOE_SCALE_PER_ROW_BLOCK128) {
+          // the tile's 128 h columns are one 128-column scale block, split
+          // over the two warps of this lane quarter: exchange their maxima
+          ctl->pamax[par][q4][half][lane] = amax;
+          named_barrier_sync(1 + q4, 64);
+          const float m = fmaxf(amax, ctl->pamax[par][q4][half ^ 1][lane]);
+          if (row_ok) {
+            const float sblk = absmax_scale(m);
+            const float inv = __frcp_rn(sblk);
+            if (half == 0) p.h_scale[row * (p.F / 128) + tl.n0 / 128] = sblk;
+            float x16[16], qv[16];
+            uint4* dst = reinterpret_cast<uint4*>(p.h_q + row * p.F + tl.n0 + half * 64);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                x16[2 * j] = bf16lo(hp[g * 8 + j]);
+                x16[2 * j + 1] = bf16hi(hp[g * 8 + j]);
+              }
+              quant_n<16>(x16, sblk, inv, qv);
+              const uint2 lo8 = pack_e4m3x8(qv), hi8 = pack_e4m3x8(qv + 8);
+              dst[g] = make_uint4(lo8.x, lo8.y, hi8.x, hi8.y);
+            }
+          }
+        }
       } else if (MODE == kFinal) {
         uint16_t* out = static_cast<uint16_t*>(p.out);
         const int64_t row = static_cast<int64_t>(tl.row0) + r;
@@ -652,6 +781,62 @@ __global__ void __launch_bounds__(256) transpose_pad_kernel(const uint8_t* src, 
   }
 }
 
+// ---- fused SwiGLU: rows outside the local groups, per-row second phase ----
+
+// Rows outside groups [g0, g0 + El) of a fused SwiGLU call get zero codes and
+// scale 1, as the unfused path gives for its zero rows.  In the per-row mode
+// their running maximum is set to -1 so that the quantise pass skips them and
+// the scale pass turns them into 1.
+__global__ void swiglu_outside_kernel(uint8_t* h_q, float* h_scale, int64_t M, int64_t F, int h_mode,
+                                      const int32_t* sizes, int E, int g0, int El) {
+  __shared__ int starts[kMaxGroups + 1];
+  group_starts_smem(sizes, E, starts);
+  const int64_t lo = starts[g0], hi = starts[g0 + El];
+  const int64_t nvec = F / 16, nb = F / 128;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < M * nvec; i += stride) {
+    const int64_t row = i / nvec;
+    if (row < lo || row >= hi) reinterpret_cast<uint4*>(h_q)[i] = make_uint4(0, 0, 0, 0);
+  }
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; row < M; row += stride) {
+    if (row >= lo && row < hi) continue;
+    if (h_mode == MOE_SCALE_PER_ROW) {
+      h_scale[row] = -1.0f;
+    } else if (h_mode == MOE_SCALE_PER_ROW_BLOCK128) {
+      for (int64_t b = 0; b < nb; ++b) h_scale[row * nb + b] = 1.0f;
+    }
+  }
+}
+
+// Per-row h scales, second phase: the epilogue left max|h| of every row in
+// `amax`; quantise the row's bf16 h against s = amax / 448.
+__global__ void __launch_bounds__(256) h_quant_rows_kernel(const uint16_t* h, const float* amax, int64_t F,
+                                                           uint8_t* q) {
+  const int64_t row = blockIdx.x;
+  const float m = amax[row];
+  if (m < 0.0f) return;  // outside the local groups
+  const float s = absmax_scale(m), inv = __frcp_rn(s);
+  const uint16_t* hr = h + row * F;
+  uint8_t* qr = q + row * F;
+  for (int64_t v = threadIdx.x; v < F / 8; v += blockDim.x) {
+    const uint4 d = __ldg(reinterpret_cast<const uint4*>(hr + 8 * v));
+    const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+    float x8[8], qv[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x8[2 * j] = bf16lo(w[j]);
+      x8[2 * j + 1] = bf16hi(w[j]);
+    }
+    quant_n<8>(x8, s, inv, qv);
+    *reinterpret_cast<uint2*>(qr + 8 * v) = pack_e4m3x8(qv);
+  }
+}
+
+__global__ void h_scale_finalize_kernel(float* h_scale, int64_t M) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < M) h_scale[i] = absmax_scale(h_scale[i]);  // a negative mark or 0 gives 1
+}
+
 // ---- host side -----------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -772,6 +957,77 @@ extern "C" moe_status gmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_
   const int64_t max_tiles64 = ((M + BM - 1) / BM + E_local) * p.ntiles;
   const int max_tiles = static_cast<int>(max_tiles64 > (1 << 30) ? (1 << 30) : max_tiles64);
   return blockwise ? launch_mma<kPromote>(A, B, p, max_tiles, st) : launch_mma<kFinal>(A, B, p, max_tiles, st);
+}
+
+extern "C" moe_status gmm_fp8_swiglu(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode,
+                                     const uint8_t* rhs_q, const float* rhs_scale, moe_scale_mode rhs_mode,
+                                     const int32_t* group_sizes, int E, int group_offset, int E_local, int64_t M,
+                                     int64_t K, int64_t F, moe_scale_mode h_mode, const float* h_static_scale,
+                                     uint16_t* a_out, uint16_t* h, uint8_t* h_q, float* h_scale,
+                                     moe_stream_t stream) {
+  MOE_HOST_CHECK(lhs_q && lhs_scale && rhs_q && rhs_scale && group_sizes && h_q, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK((lhs_mode == MOE_SCALE_PER_ROW || lhs_mode == MOE_SCALE_PER_TENSOR) &&
+                     (rhs_mode == MOE_SCALE_PER_ROW || rhs_mode == MOE_SCALE_PER_TENSOR),
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(E > 0 && E <= kMaxGroups && group_offset >= 0 && E_local > 0 && group_offset + E_local <= E,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(M >= 0 && M < (1ll << 31) && K > 0 && K % 16 == 0 && K < (1 << 30) && F > 0 && F % 128 == 0 &&
+                     2 * static_cast<int64_t>(E_local) * F < (1ll << 31),
+                 MOE_ERR_INVALID_ARG);
+  if (h_mode == MOE_SCALE_PER_ROW) {
+    MOE_HOST_CHECK(h && h_scale && aligned16(h), MOE_ERR_INVALID_ARG);
+  } else if (h_mode == MOE_SCALE_PER_ROW_BLOCK128) {
+    MOE_HOST_CHECK(h_scale != nullptr, MOE_ERR_INVALID_ARG);
+  } else {
+    MOE_HOST_CHECK(h_mode == MOE_SCALE_PER_TENSOR && h_static_scale, MOE_ERR_INVALID_ARG);
+  }
+  MOE_HOST_CHECK(aligned16(lhs_q) && aligned16(rhs_q) && aligned16(h_q) && (!a_out || aligned16(a_out)) &&
+                     (rhs_mode != MOE_SCALE_PER_ROW || aligned16(rhs_scale)),
+                 MOE_ERR_INVALID_ARG);
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = as_stream(stream);
+  if (M == 0) return MOE_OK;
+  if (h_mode == MOE_SCALE_PER_ROW) MOE_CUDA_TRY(cudaMemsetAsync(h_scale, 0, sizeof(float) * M, st));
+  if (group_offset > 0 || E_local < E) {
+    swiglu_outside_kernel<<<sm_count() * 4, 256, 0, st>>>(h_q, h_scale, M, F, h_mode, group_sizes, E, group_offset,
+                                                            E_local);
+    MOE_CUDA_TRY(cudaGetLastError());
+  }
+  CUtensorMap A, B;
+  if (!make_map(&A, lhs_q, K, M, K, BM)) return MOE_ERR_CUDA;
+  if (!make_map(&B, rhs_q, K, static_cast<uint64_t>(E_local) * 2 * F, K, 128)) return MOE_ERR_CUDA;
+  Params p{};
+  p.group_sizes = group_sizes;
+  p.E = E;
+  p.g0 = group_offset;
+  p.El = E_local;
+  p.M = M;
+  p.K = static_cast<int>(K);
+  p.N = static_cast<int>(2 * F);
+  p.kblocks = static_cast<int>((K + BK - 1) / BK);
+  p.ntiles = static_cast<int>(F / 128);
+  p.lhs_scale = lhs_scale;
+  p.lhs_mode = lhs_mode;
+  p.rhs_scale = rhs_scale;
+  p.rhs_mode = rhs_mode;
+  p.F = static_cast<int>(F);
+  p.h_mode = h_mode;
+  p.h_static = h_static_scale;
+  p.a_out = a_out;
+  p.h_out = h;
+  p.h_q = h_q;
+  p.h_scale = h_scale;
+  const int64_t max_tiles64 = ((M + BM - 1) / BM + E_local) * p.ntiles;
+  moe_status stt = launch_mma<kSwiglu>(A, B, p, static_cast<int>(max_tiles64 > (1 << 30) ? (1 << 30) : max_tiles64),
+                                       st);
+  if (stt != MOE_OK) return stt;
+  if (h_mode == MOE_SCALE_PER_ROW) {
+    h_quant_rows_kernel<<<static_cast<unsigned>(M), 256, 0, st>>>(h, h_scale, F, h_q);
+    MOE_CUDA_TRY(cudaGetLastError());
+    h_scale_finalize_kernel<<<static_cast<unsigned>((M + 255) / 256), 256, 0, st>>>(h_scale, M);
+    MOE_CUDA_TRY(cudaGetLastError());
+  }
+  return MOE_OK;
 }
 
 namespace {

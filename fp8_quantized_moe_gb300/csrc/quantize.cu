@@ -41,7 +41,6 @@ __device__ __forceinline__ uint4 pack8(const float* v) {
                     pack_bf16x2(v[6], v[7]));
 }
 
-__device__ __forceinline__ float silu_f32(float z) { return __fdiv_rn(z, __fadd_rn(1.0f, exp_f32(-z))); }
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -84,8 +83,7 @@ struct SwigluOp {  // h = bf16(silu(a0) * a1), a = [a0 | a1] of width 2F
     const uint16_t* r = a + row * 2 * F + 8 * static_cast<int64_t>(u);
     unpack8(ldg16(r), a0);
     unpack8(ldg16(r + F), a1);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[0][j] = round_bf16(__fmul_rn(silu_f32(a0[j]), a1[j]));
+    swiglu_h<8>(a0, a1, v[0]);
   }
   __device__ __forceinline__ int64_t col(int u, int) const { return 8 * static_cast<int64_t>(u); }
 };
@@ -116,6 +114,18 @@ struct GatherScaleOp {  // dO[r] = bf16(w[i] * G[i / k]), i = sorted_src[r]; als
   __device__ __forceinline__ int64_t col(int u, int) const { return 8 * static_cast<int64_t>(u); }
 };
 
+// sigma' chain of the SwiGLU backward, in a fixed order of fp32 operations:
+// silu' = sigma (1 + z (1 - sigma)), dA0 = (dH a1) silu', dA1 = dH silu.
+__device__ __forceinline__ void bwd_elem(float z, float a1, float dh, float sig, float silu, float& da0, float& da1) {
+  const float t1 = __fsub_rn(1.0f, sig);
+  const float t2 = __fmul_rn(z, t1);
+  const float t3 = __fadd_rn(1.0f, t2);
+  const float ds = __fmul_rn(sig, t3);
+  const float p = __fmul_rn(dh, a1);
+  da0 = round_bf16(__fmul_rn(p, ds));
+  da1 = round_bf16(__fmul_rn(dh, silu));
+}
+
 struct SwigluBwdOp {  // dA0 = (dH a1) silu'(a0), dA1 = dH silu(a0); also stores dA
   static constexpr int U = 2;
   const uint16_t* dH;
@@ -128,19 +138,25 @@ struct SwigluBwdOp {  // dA0 = (dH a1) silu'(a0), dA1 = dH silu(a0); also stores
     unpack8(ldg16(a + row * 2 * F + c), z);
     unpack8(ldg16(a + row * 2 * F + F + c), a1);
     unpack8(ldg16(dH + row * F + c), dh);
+    bool fast = true;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float e = exp_f32(-z[j]);
-      const float d = __fadd_rn(1.0f, e);
-      const float sig = __fdiv_rn(1.0f, d);
-      const float silu = __fdiv_rn(z[j], d);
-      const float t1 = __fsub_rn(1.0f, sig);
-      const float t2 = __fmul_rn(z[j], t1);
-      const float t3 = __fadd_rn(1.0f, t2);
-      const float ds = __fmul_rn(sig, t3);
-      const float p = __fmul_rn(dh[j], a1[j]);
-      v[0][j] = round_bf16(__fmul_rn(p, ds));
-      v[1][j] = round_bf16(__fmul_rn(dh[j], silu));
+    for (int j = 0; j < 8; ++j) fast = fast && swiglu_fast_range(z[j]);
+    bool ok = fast;
+    if (fast) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float d = __fadd_rn(1.0f, exp_fast(-z[j]));
+        const float sig = div_checked(1.0f, d, ok);
+        const float silu = div_checked(z[j], d, ok);
+        bwd_elem(z[j], a1[j], dh[j], sig, silu, v[0][j], v[1][j]);
+      }
+    }
+    if (!ok) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float d = __fadd_rn(1.0f, exp_f32(-z[j]));
+        bwd_elem(z[j], a1[j], dh[j], __fdiv_rn(1.0f, d), __fdiv_rn(z[j], d), v[0][j], v[1][j]);
+      }
     }
     *reinterpret_cast<uint4*>(dA + row * 2 * F + c) = pack8(v[0]);
     *reinterpret_cast<uint4*>(dA + row * 2 * F + F + c) = pack8(v[1]);
@@ -197,27 +213,30 @@ __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, i
     s_row = __ldg(static_scale);
   }
 
+  const float inv_row = __frcp_rn(s_row);
 #pragma unroll
   for (int i = 0; i < MAXI; ++i) {
     const int u = i * blockDim.x + tid;
-    float s = s_row;
+    float s = s_row, inv = inv_row;
     if (MODE == MOE_SCALE_PER_ROW_BLOCK128) {
       // 16 consecutive units (one 128-column block) sit on 16 consecutive lanes
       float m = amax_i[i];
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
       s = absmax_scale(m);
+      inv = __frcp_rn(s);
       if (u < nunits && (u & 15) == 0) so.scale[so.blk(row, u >> 4)] = s;
     }
     if (u < nunits) {
 #pragma unroll
       for (int uu = 0; uu < U; ++uu) {
-        float v[8];
+        float x8[8], v[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          v[2 * j] = __fdiv_rn(bf16lo(pk[i][uu][j]), s);
-          v[2 * j + 1] = __fdiv_rn(bf16hi(pk[i][uu][j]), s);
+          x8[2 * j] = bf16lo(pk[i][uu][j]);
+          x8[2 * j + 1] = bf16hi(pk[i][uu][j]);
         }
+        quant_n<8>(x8, s, inv, v);
         *reinterpret_cast<uint2*>(q + row * qcols + op.col(u, uu)) = pack_e4m3x8(v);
       }
     }
@@ -322,7 +341,7 @@ __global__ void __launch_bounds__(256) group_cols_kernel(const uint16_t* g, int6
 #pragma unroll
   for (int j = 0; j < 8; ++j) m[j] = 0.0f;
   int cur = -1;
-  float sc[8];
+  float sc[8], inv[8];
   for (int rr = 0; rr < 8; ++rr) {
     const int64_t row = r0 + rr;
     if (row >= M) break;
@@ -337,7 +356,10 @@ __global__ void __launch_bounds__(256) group_cols_kernel(const uint16_t* g, int6
       }
       if (QUANT) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) sc[j] = scale[static_cast<int64_t>(grp) * N + c0 + j];
+        for (int j = 0; j < 8; ++j) {
+          sc[j] = scale[static_cast<int64_t>(grp) * N + c0 + j];
+          inv[j] = __frcp_rn(sc[j]);
+        }
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) m[j] = 0.0f;
@@ -346,8 +368,20 @@ __global__ void __launch_bounds__(256) group_cols_kernel(const uint16_t* g, int6
     float v[8];
     unpack8(ldg16(g + row * N + c0), v);
     if (QUANT) {
+      float y[8];
+      bool slow = false;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = __fdiv_rn(v[j], sc[j]);
+      for (int j = 0; j < 8; ++j) {
+        y[j] = __fmul_rn(v[j], inv[j]);
+        slow = slow || quant_needs_division(y[j]);
+      }
+      if (slow) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (quant_needs_division(y[j])) y[j] = __fdiv_rn(v[j], sc[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = y[j];
       *reinterpret_cast<uint2*>(q + row * N + c0) = pack_e4m3x8(v);
     } else {
 #pragma unroll

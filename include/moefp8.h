@@ -197,6 +197,31 @@ moe_status gmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode 
                    int group_offset, int E_local, int64_t M, int64_t K, int64_t N, uint16_t* out,
                    moe_stream_t stream);
 
+/* gmm_fp8_swiglu -- steps 3 and 4 in one pass: the [wi_0 | wi_1] grouped
+ * matmul with SwiGLU and the requantisation of h in its epilogue, so the
+ * [M, 2F] bf16 product a never goes to memory.  Bit-identical to gmm_fp8
+ * (rhs = [wi_0 | wi_1], N = 2F) followed by moe_swiglu_quant: every output tile
+ * holds matching wi_0 and wi_1 channels, a0 and a1 are rounded to bf16 exactly
+ * as gmm_fp8 stores them, and h = bf16(silu(a0) a1) is computed the same way.
+ *   lhs_q e4m3 [M, K], lhs_scale PER_ROW [M] or PER_TENSOR [1]
+ *   rhs_q e4m3 [E_local, 2F, K] (wi_0 channels, then wi_1 channels),
+ *         rhs_scale PER_ROW (per channel) [E_local, 2F] or PER_TENSOR [1]
+ *   h_mode PER_ROW: h_scale [M]; `h` is bf16 [M, F] scratch that receives h
+ *          (the row's scale needs all of its F columns first)
+ *   h_mode PER_ROW_BLOCK128: h_scale [M, F/128], fully fused (h may be NULL)
+ *   h_mode PER_TENSOR: h_static_scale [1], fully fused (h may be NULL)
+ *   h_q   e4m3 [M, F]
+ *   a_out optional bf16 [M, 2F]: also store a = [a0 | a1] (for a backward pass)
+ * Rows outside groups [group_offset, group_offset + E_local) get zero codes
+ * and scale 1; a_out and h are not written there.  F % 128 == 0, K % 16 == 0,
+ * sum(group_sizes) == M, E <= 1024; blockwise operand scales are not fused
+ * (use gmm_fp8 + moe_swiglu_quant).  MOE_ERR_UNSUPPORTED off sm_103. */
+moe_status gmm_fp8_swiglu(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode,
+                          const uint8_t* rhs_q, const float* rhs_scale, moe_scale_mode rhs_mode,
+                          const int32_t* group_sizes, int E, int group_offset, int E_local, int64_t M, int64_t K,
+                          int64_t F, moe_scale_mode h_mode, const float* h_static_scale, uint16_t* a_out,
+                          uint16_t* h, uint8_t* h_q, float* h_scale, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Step 4 -- SwiGLU and requantisation.  a = [a0 | a1], bf16 [R, 2F] (the
  * wi_0 | wi_1 gmm output).  h = bf16(silu(a0) * a1) in fp32 with

@@ -25,6 +25,7 @@ def run_gpu_forward(cfg, x, ids, w, W, static):
         sx = torch.tensor([static["x"]], dtype=torch.float32, device="cuda")
         sh = torch.tensor([static["h"]], dtype=torch.float32, device="cuda")
     buf = moe.FFNBuffers(cfg.T, cfg.D, cfg.E, cfg.k, cfg.F, cfg.act_mode, "cuda", backward=cfg.backward)
+    buf.keep_a = True  # the tests compare the wi_0 | wi_1 product too
     y = moe.ffn_forward(x, ids, w, W, cfg.act_mode, buf, sx, sh)
     assert moe.device_error() == 0
     return y, buf, sx, sh
@@ -131,3 +132,26 @@ def test_ffn_full_size_sampled_tokens(name):
         ys.append(oracle.f64_to_bf16(acc))
     assert_close(yh[tokens], np.stack(ys), f"{name}: y sampled", rel_fro=5e-3)
     del F
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "fwdbwd"])
+def test_fused_and_unfused_forward_are_identical(name):
+    cfg = SMALL[name]
+    x_t = synth.activations(cfg, 0).cuda()
+    ids, w = synth.routing(cfg, 0)
+    w_in, w_out = synth.expert_weights(cfg, 0)
+    static = synth.calibration_scales(cfg, 0) if cfg.act_mode == synth.PER_TENSOR else None
+    W = moe.prepare_weights(w_in.cuda(), w_out.cuda(), cfg.w_mode, static)
+    assert moe.swiglu_fusable(cfg.act_mode, W.in_mode, cfg.F)
+    sx = sh = None
+    if static:
+        sx = torch.tensor([static["x"]], dtype=torch.float32, device="cuda")
+        sh = torch.tensor([static["h"]], dtype=torch.float32, device="cuda")
+    outs = []
+    for fuse in (True, False):
+        buf = moe.FFNBuffers(cfg.T, cfg.D, cfg.E, cfg.k, cfg.F, cfg.act_mode, "cuda")
+        y = moe.ffn_forward(x_t, dev(ids), dev(w), W, cfg.act_mode, buf, sx, sh, fuse_swiglu=fuse)
+        outs.append((host(y), host(buf.h_q)))
+    assert moe.device_error() == 0
+    assert np.array_equal(outs[0][1], outs[1][1])
+    assert np.array_equal(outs[0][0], outs[1][0])

@@ -107,3 +107,40 @@ def test_tgmm_matches_oracle(M, K, N, E, lmode, rmode):
     for e in np.flatnonzero(sizes == 0):
         assert np.all(o[e] == 0)
     assert_close(o, ref, f"tgmm M={M} K={K} N={N} E={E}")
+
+
+# ---- gmm_fp8_swiglu: steps 3 + 4 fused, bit-identical to gmm_fp8 + moe_swiglu_quant
+
+@pytest.mark.parametrize("M,K,F,E,amode,wmode,hmode,shard", [
+    (300, 256, 256, 4, R0, R0, R0, None),
+    (300, 256, 256, 4, R0, R0, RB, None),
+    (640, 512, 384, 8, RT, RT, RT, None),
+    (640, 512, 384, 8, RT, R0, RT, None),
+    (1, 128, 128, 1, R0, R0, R0, None),
+    (1000, 512, 384, 9, R0, R0, R0, (2, 4)),
+    (1000, 512, 384, 9, R0, RT, RB, (3, 5)),
+])
+def test_gmm_swiglu_equals_gmm_then_swiglu(M, K, F, E, amode, wmode, hmode, shard):
+    sizes, a, w, sa, sw = make_case(M + K + F + E + hmode, M, K, 2 * F, E, amode, wmode, zero_frac=0.2)
+    g0, El = shard if shard else (0, E)
+    w = np.ascontiguousarray(w[g0:g0 + El])
+    if wmode == R0:
+        sw = np.ascontiguousarray(sw[g0:g0 + El])
+    # give a0/a1 a realistic O(1..5) spread so that silu and the scales are exercised
+    sa = (sa * 4).astype(np.float32)
+    hs = torch.tensor([0.01], dtype=torch.float32, device="cuda")
+    sz = dev(sizes)
+    a_ref = moe.gmm(dev(a), dev(sa), amode, dev(w), dev(sw), wmode, sz, group_offset=g0, E_local=El)
+    hq_ref, hs_ref = moe.swiglu_quant(a_ref, hmode, hs)
+    hq, hsc, a_out = moe.gmm_swiglu(dev(a), dev(sa), amode, dev(w), dev(sw), wmode, sz, hmode, hs,
+                                    group_offset=g0, E_local=El, keep_a=True)
+    assert moe.device_error() == 0
+    starts = np.concatenate([[0], np.cumsum(sizes)])
+    lo, hi = starts[g0], starts[g0 + El]
+    assert np.array_equal(host(a_out)[lo:hi], host(a_ref)[lo:hi])
+    assert np.array_equal(host(hq), host(hq_ref))
+    if hmode != RT:
+        assert np.array_equal(host(hsc), host(hs_ref))
+    # and against the oracle, from the oracle's own a
+    a_or = oracle.gmm(a, sa, amode, w, sw, wmode, sizes, group_offset=g0, E_local=El)
+    assert_close(host(a_out)[lo:hi], a_or[lo:hi], "gmm_swiglu a")
