@@ -46,7 +46,10 @@ __device__ unsigned int g_err;
 constexpr int BM = 128;
 constexpr int BK = 128;
 constexpr int BN = 256;
-constexpr int NSTAGE = 4;
+#ifndef MOE_GMM_NSTAGE
+#define MOE_GMM_NSTAGE 4
+#endif
+constexpr int NSTAGE = MOE_GMM_NSTAGE;  // smem ring depth (48 KB per stage)
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -810,7 +813,7 @@ __global__ void swiglu_outside_kernel(uint8_t* h_q, float* h_scale, int64_t M, i
 
 // Per-row h scales, second phase: the epilogue left max|h| of every row in
 // `amax`; quantise the row's bf16 h against s = amax / 448.
-__global__ void __launch_bounds__(256) h_quant_rows_kernel(const uint16_t* h, const float* amax, int64_t F,
+__global__ void __launch_bounds__(256, 4) h_quant_rows_kernel(const uint16_t* h, const float* amax, int64_t F,
                                                            uint8_t* q) {
   const int64_t row = blockIdx.x;
   const float m = amax[row];
@@ -818,17 +821,30 @@ __global__ void __launch_bounds__(256) h_quant_rows_kernel(const uint16_t* h, co
   const float s = absmax_scale(m), inv = __frcp_rn(s);
   const uint16_t* hr = h + row * F;
   uint8_t* qr = q + row * F;
-  for (int64_t v = threadIdx.x; v < F / 8; v += blockDim.x) {
-    const uint4 d = __ldg(reinterpret_cast<const uint4*>(hr + 8 * v));
-    const uint32_t w[4] = {d.x, d.y, d.z, d.w};
-    float x8[8], qv[8];
+  const int64_t nvec = F / 8;
+  constexpr int V = 4;  // 16-byte loads in flight per thread
+  for (int64_t base = 0; base < nvec; base += V * blockDim.x) {
+    uint4 d[V];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      x8[2 * j] = bf16lo(w[j]);
-      x8[2 * j + 1] = bf16hi(w[j]);
+    for (int i = 0; i < V; ++i) {
+      const int64_t v = base + i * blockDim.x + threadIdx.x;
+      if (v < nvec) d[i] = __ldg(reinterpret_cast<const uint4*>(hr + 8 * v));
     }
-    quant_n<8>(x8, s, inv, qv);
-    *reinterpret_cast<uint2*>(qr + 8 * v) = pack_e4m3x8(qv);
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int64_t v = base + i * blockDim.x + threadIdx.x;
+      if (v < nvec) {
+        const uint32_t w[4] = {d[i].x, d[i].y, d[i].z, d[i].w};
+        float x8[8], qv[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          x8[2 * j] = bf16lo(w[j]);
+          x8[2 * j + 1] = bf16hi(w[j]);
+        }
+        quant_n<8>(x8, s, inv, qv);
+        *reinterpret_cast<uint2*>(qr + 8 * v) = pack_e4m3x8(qv);
+      }
+    }
   }
 }
 
