@@ -45,6 +45,9 @@ def parse():
     ap.add_argument("--cpu-sample-tokens", type=int, default=0, help="oracle sample size (0 = auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--suite", action="store_true",
+                    help="time every call of the path alone, for every config (one JSON line per call)")
+    ap.add_argument("--suite-configs", default="mixtral,dsv3,prefill,fwdbwd,tiny")
     return ap.parse_args()
 
 
@@ -364,8 +367,149 @@ def run_reference(args, cfg, rank, world):
     }
 
 
+# ---------------------------------------------------------------------------
+# Per-call suite: every step of the path timed alone against its roofline
+# ---------------------------------------------------------------------------
+
+def run_suite(args):
+    import fp8_quantized_moe_gb300 as moe
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pk, pk_kind = peaks()
+    hbm = pk["hbm_gbs"]
+    fp8 = 2.0 * pk["bf16_tflops"]  # calls timed alone: burst figure
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    lines = []
+
+    def timed(fn, reps=10):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            flush.fill_(1)  # evict the previous call's data from L2 (512 MB > 129 MB)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+    for name in args.suite_configs.split(","):
+        cfg = synth.CONFIGS[name]
+        T, D, E, k, F = cfg.T, cfg.D, cfg.E, cfg.k, cfg.F
+        R = T * k
+        static = synth.calibration_scales(cfg, 0) if cfg.act_mode == synth.PER_TENSOR else None
+        sx = sh = None
+        if static:
+            sx = torch.tensor([static["x"]], dtype=torch.float32, device=dev)
+            sh = torch.tensor([static["h"]], dtype=torch.float32, device=dev)
+        x_host, ids_np, w_np = host_inputs(cfg, 0)
+        w_in, w_out = synth.expert_weights(cfg, 0, device=dev)
+        W = moe.prepare_weights(w_in, w_out, cfg.w_mode, static, for_backward=cfg.backward)
+        del w_in, w_out
+        torch.cuda.empty_cache()
+        x = x_host.to(dev)
+        ids = torch.from_numpy(ids_np).to(dev)
+        w = torch.from_numpy(w_np).to(dev)
+        buf = moe.FFNBuffers(T, D, E, k, F, cfg.act_mode, dev, backward=cfg.backward)
+        am = cfg.act_mode
+        fused = moe.swiglu_fusable(am, W.in_mode, F)
+        moe.ffn_forward(x, ids, w, W, am, buf, sx, sh)  # fills every intermediate
+        torch.cuda.synchronize()
+        nb = lambda c: (c + 127) // 128
+        sbytes = lambda rows, cols: 0 if am == 2 else 4 * rows * (1 if am == 0 else nb(cols))
+        xs_s = buf.sort["xs_scale"] if am != 2 else sx
+        h_s = buf.h_s if am != 2 else sh
+        calls = [
+            ("quantize_rows x", lambda: moe.quantize_rows(x, am, sx, q=buf.x_q, scale=buf.x_s),
+             "hbm", 3 * T * D + sbytes(T, D)),
+            ("ragged_sort (+ gather)", lambda: moe.ragged_sort(ids, E, buf.x_q, buf.x_s if am != 2 else sx, am,
+                                                               out=buf.sort),
+             "hbm", T * D + R * D + 16 * R + 2 * sbytes(T, D)),
+        ]
+        if fused:
+            calls.append(("gmm_fp8_swiglu (wi_0|wi_1 + SwiGLU + requant)",
+                          lambda: moe.gmm_swiglu(buf.sort["xs_q"], xs_s, am, W.w_in, W.s_in, W.in_mode,
+                                                 buf.sort["group_sizes"], am, sh, h=buf.h, h_q=buf.h_q,
+                                                 h_scale=buf.h_s, a_out=buf.a if buf.keep_a else None),
+                          "tensor", 2.0 * R * D * 2 * F))
+        calls.append(("gmm_fp8 wi_0|wi_1", lambda: moe.gmm(buf.sort["xs_q"], xs_s, am, W.w_in, W.s_in, W.in_mode,
+                                                           buf.sort["group_sizes"], out=buf.a),
+                      "tensor", 2.0 * R * D * 2 * F))
+        calls.append(("moe_swiglu_quant", lambda: moe.swiglu_quant(buf.a, am, sh, h_q=buf.h_q, h_scale=buf.h_s),
+                      "hbm", 5 * R * F + sbytes(R, F)))
+        calls.append(("gmm_fp8 wo", lambda: moe.gmm(buf.h_q, h_s, am, W.w_out, W.s_out, W.out_mode,
+                                                    buf.sort["group_sizes"], out=buf.o),
+                      "tensor", 2.0 * R * F * D))
+        calls.append(("ragged_gather_reduce", lambda: moe.ragged_gather_reduce(buf.o, buf.sort["pos"], w, k,
+                                                                                out=buf.y),
+                      "hbm", 2 * R * D + 2 * T * D + 8 * R))
+        if cfg.backward:
+            G = synth.output_grad(cfg, 0, device=dev)
+            src, sizes = buf.sort["sorted_src"], buf.sort["group_sizes"]
+            wflat = w.reshape(-1)
+            dO, dO_q, dO_s = moe.gather_scale_quant(G, wflat, src, k)
+            dA, dA_q, dA_s = moe.swiglu_bwd_quant(buf.dH, buf.a)
+            calls += [
+                ("bwd moe_gather_scale_quant", lambda: moe.gather_scale_quant(G, wflat, src, k),
+                 "hbm", 2 * T * D + 3 * R * D + 4 * R),
+                ("bwd gmm_fp8 dH = dO wo", lambda: moe.gmm(dO_q, dO_s, 0, W.w_out_t, W.s_out, 2, sizes, out=buf.dH),
+                 "tensor", 2.0 * R * D * F),
+                ("bwd moe_swiglu_bwd_quant", lambda: moe.swiglu_bwd_quant(buf.dH, buf.a),
+                 "hbm", 2 * R * F + 4 * R * F + 6 * R * F + 4 * R),
+                ("bwd gmm_fp8 dXs = dA [wi_0|wi_1]", lambda: moe.gmm(dA_q, dA_s, 0, W.w_in_t, W.s_in_t, 1, sizes,
+                                                                    out=buf.dXs),
+                 "tensor", 2.0 * R * 2 * F * D),
+                ("bwd ragged_gather_reduce dX", lambda: moe.ragged_gather_reduce(buf.dXs, buf.sort["pos"], None, k,
+                                                                                 out=buf.dX),
+                 "hbm", 2 * R * D + 2 * T * D + 4 * R),
+                ("bwd moe_quantize_group_cols dA", lambda: moe.quantize_group_cols(dA, sizes),
+                 "hbm", 3 * R * 2 * F),
+                ("bwd moe_quantize_group_cols dO", lambda: moe.quantize_group_cols(dO, sizes),
+                 "hbm", 3 * R * D),
+            ]
+            dAg_q, dAg_s = moe.quantize_group_cols(dA, sizes)
+            dOg_q, dOg_s = moe.quantize_group_cols(dO, sizes)
+            ws = torch.empty(moe.lib().tgmm_fp8_workspace_bytes(R, D, 2 * F, E), dtype=torch.uint8, device=dev)
+            calls += [
+                ("bwd tgmm_fp8 dW_in (incl. operand transposes)",
+                 lambda: moe.tgmm(buf.sort["xs_q"], sx, 2, dAg_q, dAg_s, 3, sizes, workspace=ws),
+                 "tensor", 2.0 * R * D * 2 * F),
+                ("bwd tgmm_fp8 dW_out (incl. operand transposes)",
+                 lambda: moe.tgmm(buf.h_q, sh, 2, dOg_q, dOg_s, 3, sizes, workspace=ws),
+                 "tensor", 2.0 * R * F * D),
+            ]
+        total = 0.0
+        for label, fn, bound, work in calls:
+            ms = timed(fn)
+            if bound == "hbm":
+                ach, peak, unit = work / (ms / 1e3) / 1e9, hbm, "GB/s"
+            else:
+                ach, peak, unit = work / (ms / 1e3) / 1e12, fp8, "TFLOP/s"
+            on_path = not (fused and label in ("gmm_fp8 wi_0|wi_1", "moe_swiglu_quant"))
+            if on_path:
+                total += ms
+            line = {"suite": cfg.name, "call": label, "ms": round(ms, 4), "bound": bound,
+                    "achieved": round(ach, 1), "peak": peak, "unit": unit, "frac": round(ach / peak, 3),
+                    "on_step": on_path, "peak_kind": pk_kind}
+            print(json.dumps(line), flush=True)
+        step = {"suite": cfg.name, "call": "sum of the step's calls (timed alone, L2 flushed)",
+                "ms": round(total, 4), "tokens_per_s": round(T / (total / 1e3), 1),
+                "workload": workload_name(cfg) + (" + backward" if cfg.backward else "")}
+        print(json.dumps(step), flush=True)
+        assert moe.device_error() == 0
+        del buf, W, x
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
+    if args.suite:
+        run_suite(args)
+        return
     cfg = synth.CONFIGS[args.config]
     if args.tokens:
         cfg = synth.scaled(cfg, T=args.tokens)

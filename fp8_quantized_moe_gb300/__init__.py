@@ -220,7 +220,7 @@ def quantize_group_cols(g: torch.Tensor, group_sizes: torch.Tensor, group_offset
     M, N = g.shape
     E = group_sizes.numel()
     E_local = E - group_offset if E_local is None else E_local
-    q = torch.zeros(M, N, dtype=torch.uint8, device=g.device)
+    q = torch.empty(M, N, dtype=torch.uint8, device=g.device)  # rows of other experts stay unwritten
     s = torch.empty(E_local, N, dtype=torch.float32, device=g.device)
     check(lib().moe_quantize_group_cols(_p(g), M, N, _p(group_sizes), E, group_offset, E_local, _p(q), _p(s), _s()),
           "moe_quantize_group_cols")

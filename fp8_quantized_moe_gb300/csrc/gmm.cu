@@ -35,6 +35,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -45,27 +46,18 @@ __device__ unsigned int g_err;
 
 constexpr int BM = 128;
 constexpr int BK = 128;
-constexpr int BN = 256;
 #ifndef MOE_GMM_NSTAGE
 #define MOE_GMM_NSTAGE 4
 #endif
-constexpr int NSTAGE = MOE_GMM_NSTAGE;  // smem ring depth (48 KB per stage)
 constexpr int A_BYTES = BM * BK;
-constexpr int B_BYTES = BN * BK;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int UMMA_K = 32;
-constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
+constexpr int kMaxStages = 8;
+constexpr int kMaxAcc = 4;
 constexpr int kMaxGroups = 1024;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint32_t kTmemCols = 512;
 
 enum Mode { kFinal = 0, kPromote = 1, kTgmm = 2, kSwiglu = 3 };
-
-template <int MODE>
-struct Cfg {
-  static constexpr int EPI_WARPS = (MODE == kPromote || MODE == kSwiglu) ? 8 : 4;
-  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-};
 
 struct Params {
   const int32_t* group_sizes;
@@ -91,10 +83,10 @@ struct Params {
 };
 
 struct SmemCtl {
-  uint64_t full[NSTAGE];
-  uint64_t empty[NSTAGE];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t tfull[kMaxAcc];
+  uint64_t tempty[kMaxAcc];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -103,11 +95,31 @@ struct SmemCtl {
   int gstart[kMaxGroups + 1];       // gmm: first row of local group; tgmm: padded first row
   int tile_prefix[kMaxGroups + 1];  // gmm: first tile of local group
   int gsize[kMaxGroups];
-  float sw_stage[8][128];           // promotion: weight scales of the current K block, per warp
+  float sw_stage[8][64];            // promotion: weight scales of the current K block, per warp
   float pamax[2][4][2][32];          // fused SwiGLU, per-128 h scales: row maxima of the two column halves
 };
 
-constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(NSTAGE) * STAGE_BYTES + sizeof(SmemCtl);
+// Tile configuration per mode.  Promotion (a blockwise operand scale) uses
+// 128x128 tiles with four TMEM accumulators, so the MMA can run up to three K
+// blocks ahead of the epilogue that folds each block's partial sums into
+// registers; the other modes use 128x256 tiles with two accumulators.
+#ifndef MOE_PROMOTE_BN
+#define MOE_PROMOTE_BN 128
+#endif
+template <int MODE>
+struct Cfg {
+  static constexpr bool PROMOTE = MODE == kPromote;
+  static constexpr int BN = PROMOTE ? MOE_PROMOTE_BN : 256;  // output columns per tile
+  static constexpr int NACC = 512 / BN;                      // accumulators; NACC * BN = 512 TMEM columns
+  static constexpr int NSTAGE = BN == 128 ? 6 : MOE_GMM_NSTAGE;
+  static constexpr int B_BYTES = BN * BK;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
+  static constexpr int EPI_WARPS = (MODE == kPromote || MODE == kSwiglu) ? 8 : 4;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr size_t SMEM = 1024 + static_cast<size_t>(NSTAGE) * STAGE_BYTES + sizeof(SmemCtl);
+  static_assert(NSTAGE <= kMaxStages && NACC <= kMaxAcc && NACC * BN == 512, "tile configuration");
+};
 
 // ---- group tables --------------------------------------------------------
 // Warp 0 reads all E sizes at once (<= 32 per lane), scans them, and fills
@@ -185,6 +197,7 @@ struct Tile {
 template <int MODE>
 __device__ __forceinline__ Tile get_tile(const Params& p, const SmemCtl* ctl, int t) {
   Tile tl;
+  constexpr int BN = Cfg<MODE>::BN;
   if (MODE == kTgmm) {
     const int per = p.ktiles * p.ntiles;
     tl.el = t / per;
@@ -237,16 +250,29 @@ __device__ __forceinline__ float lhs_scale_at(const Params& p, int64_t row, int 
   return __ldg(p.lhs_scale);
 }
 
-__device__ __forceinline__ float rhs_scale_at(const Params& p, int el, int n, int kb) {
-  if (p.rhs_mode == MOE_SCALE_PER_ROW) return __ldg(p.rhs_scale + static_cast<int64_t>(el) * p.N + n);
-  if (p.rhs_mode == MOE_SCALE_PER_ROW_BLOCK128)
-    return __ldg(p.rhs_scale + (static_cast<int64_t>(el) * p.kblocks + kb) * p.N + n);
-  return __ldg(p.rhs_scale);
-}
-
 // tgmm operand scale: per tensor or per (local group, column).
 __device__ __forceinline__ float group_col_scale(const float* s, int mode, int el, int c, int C) {
   return mode == MOE_SCALE_PER_GROUP_COL ? __ldg(s + static_cast<int64_t>(el) * C + c) : __ldg(s);
+}
+
+// 32 per-column scales starting at column nb: 16-byte loads from `base` when
+// the span is in range and per-column, else guarded scalar loads or the one
+// per-tensor value.
+__device__ __forceinline__ void load_col_scales32(const float* base, int nb, int N, bool per_col, float uniform,
+                                                  float* sw) {
+  if (per_col && nb + 32 <= N) {
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const float4 t = __ldg(reinterpret_cast<const float4*>(base + nb) + g);
+      sw[4 * g] = t.x;
+      sw[4 * g + 1] = t.y;
+      sw[4 * g + 2] = t.z;
+      sw[4 * g + 3] = t.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) sw[j] = per_col ? (nb + j < N ? __ldg(base + nb + j) : 0.f) : uniform;
+  }
 }
 
 __device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float* v, int ncols_valid) {
@@ -266,7 +292,10 @@ __device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float* v, int
 template <int MODE>
 __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
-  constexpr int EPI_WARPS = Cfg<MODE>::EPI_WARPS;
+  using C = Cfg<MODE>;
+  constexpr int EPI_WARPS = C::EPI_WARPS, BN = C::BN, NSTAGE = C::NSTAGE, NACC = C::NACC;
+  constexpr int STAGE_BYTES = C::STAGE_BYTES;
+  constexpr uint32_t IDESC = C::IDESC;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -280,7 +309,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
       mbar_init(smem_u32(&ctl->full[s]), 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < NACC; ++a) {
       mbar_init(smem_u32(&ctl->tfull[a]), 1);
       mbar_init(smem_u32(&ctl->tempty[a]), EPI_WARPS);
     }
@@ -352,9 +381,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
       for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
         const Tile tl = get_tile<MODE>(p, ctl, t);
         if (tl.nkb == 0) continue;
-        uint32_t a = acc & 1;
+        uint32_t a = acc % NACC;
         if (MODE != kPromote) {
-          if (!mbar_wait_bounded(smem_u32(&ctl->tempty[a]), ((acc >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+          if (!mbar_wait_bounded(smem_u32(&ctl->tempty[a]), ((acc / NACC) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
             timed_out = true;
             break;
           }
@@ -362,8 +391,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
         }
         for (int kb = 0; kb < tl.nkb; ++kb) {
           if (MODE == kPromote) {
-            a = acc & 1;
-            if (!mbar_wait_bounded(smem_u32(&ctl->tempty[a]), ((acc >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+            a = acc % NACC;
+            if (!mbar_wait_bounded(smem_u32(&ctl->tempty[a]), ((acc / NACC) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
               timed_out = true;
               break;
             }
@@ -412,7 +441,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q4 = warp & 3;                            // TMEM lane quarter of this warp
-    const int half = (MODE == kPromote || MODE == kSwiglu) ? (warp - 2) >> 2 : 0;  // column half
+    const int half = (MODE == kPromote || MODE == kSwiglu) ? (warp - 2) >> 2 : 0;  // column part of the warp
     const int r = q4 * 32 + lane;                       // row of the tile = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
     uint32_t acc = 0;
@@ -430,29 +459,34 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
           }
           continue;
         }
-        const uint32_t a = acc & 1;
-        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc >> 1) & 1, abort_flag, kWaitLimitNs)) {
+        const uint32_t a = acc % NACC;
+        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
           timed_out = true;
           break;
         }
         tc_fence_after();
         const float sx = row_ok ? group_col_scale(p.lhs_scale, p.lhs_mode, tl.el, static_cast<int>(krow), p.K) : 0.f;
+        const bool per_col = p.rhs_mode == MOE_SCALE_PER_GROUP_COL;
+        const float* sgb = p.rhs_scale + (per_col ? static_cast<int64_t>(tl.el) * p.N : 0);
+        const float sg_t = per_col ? 0.f : __ldg(p.rhs_scale);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
+          const int nb = tl.n0 + c * 32;
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + c * 32, v);
+          float sg[32];
+          load_col_scales32(sgb, nb, p.N, per_col, sg_t, sg);
           tmem_wait_ld();
-          const int nb = tl.n0 + c * 32;
           if (row_ok) {
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
               const int n = nb + g * 4;
               if (n < p.N) {
                 float4 o;
-                o.x = __uint_as_float(v[g * 4 + 0]) * sx * group_col_scale(p.rhs_scale, p.rhs_mode, tl.el, n + 0, p.N);
-                o.y = __uint_as_float(v[g * 4 + 1]) * sx * group_col_scale(p.rhs_scale, p.rhs_mode, tl.el, n + 1, p.N);
-                o.z = __uint_as_float(v[g * 4 + 2]) * sx * group_col_scale(p.rhs_scale, p.rhs_mode, tl.el, n + 2, p.N);
-                o.w = __uint_as_float(v[g * 4 + 3]) * sx * group_col_scale(p.rhs_scale, p.rhs_mode, tl.el, n + 3, p.N);
+                o.x = __uint_as_float(v[g * 4 + 0]) * sx * sg[g * 4 + 0];
+                o.y = __uint_as_float(v[g * 4 + 1]) * sx * sg[g * 4 + 1];
+                o.z = __uint_as_float(v[g * 4 + 2]) * sx * sg[g * 4 + 2];
+                o.w = __uint_as_float(v[g * 4 + 3]) * sx * sg[g * 4 + 3];
                 *reinterpret_cast<float4*>(orow + n) = o;
               }
             }
@@ -466,8 +500,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
         // 8 warps: TMEM lane quarter q4, h columns [half*64, half*64 + 64) of
         // the tile; accumulator columns c*32.. hold a0, 128 + c*32.. hold a1.
         const int64_t row = static_cast<int64_t>(tl.row0) + r;
-        const uint32_t a = acc & 1;
-        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc >> 1) & 1, abort_flag, kWaitLimitNs)) {
+        const uint32_t a = acc % NACC;
+        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
           timed_out = true;
           break;
         }
@@ -573,26 +607,30 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
       } else if (MODE == kFinal) {
         uint16_t* out = static_cast<uint16_t*>(p.out);
         const int64_t row = static_cast<int64_t>(tl.row0) + r;
-        const uint32_t a = acc & 1;
-        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc >> 1) & 1, abort_flag, kWaitLimitNs)) {
+        const uint32_t a = acc % NACC;
+        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
           timed_out = true;
           break;
         }
         tc_fence_after();
         const float sa = row_ok ? lhs_scale_at(p, row, 0) : 0.f;
+        // channel scales: branch on the mode once per tile, then 16-byte
+        // broadcast loads (every lane reads the same 32 scales)
+        const bool per_chan = p.rhs_mode == MOE_SCALE_PER_ROW;
+        const float* swb = p.rhs_scale + (per_chan ? static_cast<int64_t>(tl.el) * p.N : 0);
+        const float sw_t = per_chan ? 0.f : __ldg(p.rhs_scale);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
+          const int nb = tl.n0 + c * 32;
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + c * 32, v);
+          float sw[32];
+          load_col_scales32(swb, nb, p.N, per_chan, sw_t, sw);
           tmem_wait_ld();
-          const int nb = tl.n0 + c * 32;
           if (row_ok && nb < p.N) {
             float f[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int n = min(nb + j, p.N - 1);
-              f[j] = __fmul_rn(__fmul_rn(__uint_as_float(v[j]), sa), rhs_scale_at(p, tl.el, n, 0));
-            }
+            for (int j = 0; j < 32; ++j) f[j] = __fmul_rn(__fmul_rn(__uint_as_float(v[j]), sa), sw[j]);
             store_bf16x32(out + row * p.N + nb, f, p.N - nb);
           }
         }
@@ -601,62 +639,161 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
         if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
         ++acc;
       } else {
-        // promotion: one fresh accumulator per K block, folded into registers
+        // promotion: one fresh accumulator per K block, folded into registers.
+        // Eight warps: TMEM lane quarter q4, columns [half*64, half*64 + 64)
+        // of the 128-column tile.  Only the blockwise side(s) enter the
+        // per-block update; a scale constant along K is applied at the end.
         uint16_t* out = static_cast<uint16_t*>(p.out);
         const int64_t row = static_cast<int64_t>(tl.row0) + r;
-        const int cbase = tl.n0 + half * 128;
+        constexpr int WC = BN / (EPI_WARPS / 4);  // columns per epilogue warp
+        const int cbase = tl.n0 + half * WC;
         float* stage = ctl->sw_stage[warp - 2];
-        uint64_t acc2[64];
+        const bool a_blk = p.lhs_mode == MOE_SCALE_PER_ROW_BLOCK128;
+        const bool w_blk = p.rhs_mode == MOE_SCALE_PER_ROW_BLOCK128;
+        const int64_t srow = row_ok ? row : 0;
+        const float* sab = p.lhs_scale + (p.lhs_mode == MOE_SCALE_PER_ROW ? srow : (a_blk ? srow * p.kblocks : 0));
+        const float* swb = p.rhs_scale + (p.rhs_mode == MOE_SCALE_PER_ROW
+                                              ? static_cast<int64_t>(tl.el) * p.N
+                                              : (w_blk ? static_cast<int64_t>(tl.el) * p.kblocks * p.N : 0));
+        uint64_t acc2[WC / 2];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) acc2[j] = 0ull;
-        for (int kb = 0; kb < tl.nkb; ++kb) {
-          // weight scales of this warp's 128 columns for K block kb
-          {
-            float4 w4;
-            const int n = cbase + 4 * lane;
-            w4.x = n + 0 < p.N ? rhs_scale_at(p, tl.el, n + 0, kb) : 0.f;
-            w4.y = n + 1 < p.N ? rhs_scale_at(p, tl.el, n + 1, kb) : 0.f;
-            w4.z = n + 2 < p.N ? rhs_scale_at(p, tl.el, n + 2, kb) : 0.f;
-            w4.w = n + 3 < p.N ? rhs_scale_at(p, tl.el, n + 3, kb) : 0.f;
-            *reinterpret_cast<float4*>(stage + 4 * lane) = w4;
+        for (int j = 0; j < WC / 2; ++j) acc2[j] = 0ull;
+        // The scales of a K block are loaded PD blocks ahead (a register
+        // ring), so their memory latency stays off the per-block path.
+        constexpr int PD = 4;
+        constexpr int SPL = WC / 32;        // staged column scales per lane
+        const int nw = cbase + SPL * lane;  // this lane's first staged column
+        using WVec = typename std::conditional<SPL == 1, float, typename std::conditional<SPL == 2, float2, float4>::type>::type;
+        auto load_w = [&](int kb) -> WVec {
+          WVec w{};
+          if (w_blk && kb < tl.nkb) {
+            const float* src = swb + static_cast<int64_t>(kb) * p.N + nw;
+            if (nw + SPL - 1 < p.N) {
+              w = __ldg(reinterpret_cast<const WVec*>(src));
+            } else {
+              float* wf = reinterpret_cast<float*>(&w);
+              for (int i = 0; i < SPL; ++i) wf[i] = nw + i < p.N ? __ldg(src + i) : 0.f;
+            }
           }
-          const float sa = row_ok ? lhs_scale_at(p, row, kb) : 0.f;
+          return w;
+        };
+        auto load_a = [&](int kb) -> float { return (a_blk && kb < tl.nkb) ? __ldg(sab + kb) : 1.0f; };
+        WVec wq[PD];
+        float aq[PD];
+#pragma unroll
+        for (int i = 0; i < PD; ++i) {
+          wq[i] = load_w(i);
+          aq[i] = load_a(i);
+        }
+        // Unrolled by PD so that slot i is consumed and refilled in place
+        // (moving an in-flight load between registers would wait for it).
+        for (int kb0 = 0; kb0 < tl.nkb && !timed_out; kb0 += PD) {
+#pragma unroll
+         for (int i = 0; i < PD; ++i) {
+          const int kb = kb0 + i;
+          if (kb >= tl.nkb || timed_out) break;
+          const WVec w2 = wq[i];
+          const float sa = aq[i];
+          wq[i] = load_w(kb + PD);
+          aq[i] = load_a(kb + PD);
+          if (w_blk) *reinterpret_cast<WVec*>(stage + SPL * lane) = w2;
           const uint64_t sa2 = f2_pack(sa, sa);
           __syncwarp();
-          const uint32_t a = acc & 1;
-          if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc >> 1) & 1, abort_flag, kWaitLimitNs)) {
+          const uint32_t a = acc % NACC;
+          if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
             timed_out = true;
             break;
           }
           tc_fence_after();
+          auto fold16 = [&](const uint32_t* v, int j0) {  // 16 columns from column j0 of this warp's span
+            if (a_blk && w_blk) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+              for (int j = 0; j < 8; ++j) {
+                const float2 sw = *reinterpret_cast<const float2*>(stage + j0 + 2 * j);
+                const uint64_t pr = f2_mul(f2_pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])),
+                                           f2_pack(sw.x, sw.y));
+                acc2[j0 / 2 + j] = f2_fma(pr, sa2, acc2[j0 / 2 + j]);
+              }
+            } else if (w_blk) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float2 sw = *reinterpret_cast<const float2*>(stage + j0 + 2 * j);
+                acc2[j0 / 2 + j] = f2_fma(f2_pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])),
+                                          f2_pack(sw.x, sw.y), acc2[j0 / 2 + j]);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                acc2[j0 / 2 + j] = f2_fma(f2_pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), sa2,
+                                          acc2[j0 / 2 + j]);
+            }
+          };
+          if (WC == 32) {
             uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + half * 128 + c * 32, v);
+            tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + half * WC, v);
             tmem_wait_ld();
+            tc_fence_before();  // the accumulator is in registers: release it
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
+            fold16(v, 0);
+            fold16(v + 16, 16);
+          } else if (WC == 64) {
+            // the whole span fits in registers: load it, release the accumulator, then fold
+            uint32_t v[64];
+            tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + half * WC, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + half * WC + 32,
+                               *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float2 sw = *reinterpret_cast<const float2*>(stage + c * 32 + 2 * j);
-              const uint64_t pr = f2_mul(f2_pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])),
-                                         f2_pack(sw.x, sw.y));
-              acc2[c * 16 + j] = f2_fma(pr, sa2, acc2[c * 16 + j]);
+            for (int c = 0; c < WC / 16; ++c) fold16(v + 16 * c, 16 * c);
+          } else {
+            // 128 columns: fold 16 at a time, release after the last load
+#pragma unroll
+            for (int c = 0; c < WC / 16; ++c) {
+              uint32_t v[16];
+              tmem_ld_32x32b_x16(tmem_base + lane_addr + a * BN + half * WC + 16 * c, v);
+              tmem_wait_ld();
+              if (c == WC / 16 - 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
+              }
+              fold16(v, 16 * c);
             }
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
           ++acc;
+          __syncwarp();  // the staged scales are read before the next block overwrites them
+         }
         }
         if (timed_out) break;
         if (row_ok) {
+          const float sa_end = a_blk ? 1.0f : __ldg(sab);
+          const bool w_col = p.rhs_mode == MOE_SCALE_PER_ROW;
+          const float sw_t = (w_blk || w_col) ? 1.0f : __ldg(p.rhs_scale);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < WC / 32; ++c) {
             const int nb = cbase + c * 32;
             if (nb < p.N) {
-              float f[32];
+              uint32_t pk[16];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) f2_unpack(acc2[c * 16 + j], f[2 * j], f[2 * j + 1]);
-              store_bf16x32(out + row * p.N + nb, f, p.N - nb);
+              for (int g = 0; g < 8; ++g) {  // columns nb + 4g .. nb + 4g + 3
+                float4 w4 = make_float4(sw_t, sw_t, sw_t, sw_t);
+                if (w_col && nb + 4 * g + 3 < p.N) w4 = __ldg(reinterpret_cast<const float4*>(swb + nb) + g);
+                float f0, f1, f2, f3;
+                f2_unpack(acc2[c * 16 + 2 * g], f0, f1);
+                f2_unpack(acc2[c * 16 + 2 * g + 1], f2, f3);
+                pk[2 * g] = pack_bf16x2(__fmul_rn(__fmul_rn(f0, sa_end), w4.x), __fmul_rn(__fmul_rn(f1, sa_end), w4.y));
+                pk[2 * g + 1] =
+                    pack_bf16x2(__fmul_rn(__fmul_rn(f2, sa_end), w4.z), __fmul_rn(__fmul_rn(f3, sa_end), w4.w));
+              }
+              uint16_t* dst = out + row * p.N + nb;
+#pragma unroll
+              for (int g = 0; g < 4; ++g)
+                if (g * 8 < p.N - nb)
+                  *reinterpret_cast<uint4*>(dst + g * 8) = make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
             }
           }
         }
@@ -902,11 +1039,11 @@ template <int MODE>
 moe_status launch_mma(const CUtensorMap& A, const CUtensorMap& B, const Params& p, int max_tiles,
                       cudaStream_t st) {
   MOE_CUDA_TRY(cudaFuncSetAttribute(mma_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(kSmemBytes)));
+                                    static_cast<int>(Cfg<MODE>::SMEM)));
   const int sms = sm_count();
   if (sms <= 0) return MOE_ERR_CUDA;
   const int grid = max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms;
-  mma_kernel<MODE><<<grid, Cfg<MODE>::THREADS, kSmemBytes, st>>>(A, B, p);
+  mma_kernel<MODE><<<grid, Cfg<MODE>::THREADS, Cfg<MODE>::SMEM, st>>>(A, B, p);
   MOE_CUDA_TRY(cudaGetLastError());
   return MOE_OK;
 }
@@ -944,6 +1081,7 @@ extern "C" moe_status gmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_
   const bool blockwise = lhs_mode == MOE_SCALE_PER_ROW_BLOCK128 || rhs_mode == MOE_SCALE_PER_ROW_BLOCK128;
   MOE_HOST_CHECK(!blockwise || K % 128 == 0, MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(aligned16(lhs_q) && aligned16(rhs_q) && aligned16(out), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(rhs_mode == MOE_SCALE_PER_TENSOR || aligned16(rhs_scale), MOE_ERR_INVALID_ARG);
   if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
   cudaStream_t st = as_stream(stream);
   if (M == 0) return MOE_OK;
@@ -953,7 +1091,8 @@ extern "C" moe_status gmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_
   }
   CUtensorMap A, B;
   if (!make_map(&A, lhs_q, K, M, K, BM)) return MOE_ERR_CUDA;
-  if (!make_map(&B, rhs_q, K, static_cast<uint64_t>(E_local) * N, K, BN)) return MOE_ERR_CUDA;
+  const int bn = blockwise ? Cfg<kPromote>::BN : Cfg<kFinal>::BN;
+  if (!make_map(&B, rhs_q, K, static_cast<uint64_t>(E_local) * N, K, bn)) return MOE_ERR_CUDA;
   Params p{};
   p.group_sizes = group_sizes;
   p.E = E;
@@ -963,7 +1102,7 @@ extern "C" moe_status gmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_
   p.K = static_cast<int>(K);
   p.N = static_cast<int>(N);
   p.kblocks = static_cast<int>((K + BK - 1) / BK);
-  p.ntiles = static_cast<int>((N + BN - 1) / BN);
+  p.ntiles = static_cast<int>((N + bn - 1) / bn);
   p.ktiles = 0;
   p.lhs_scale = lhs_scale;
   p.lhs_mode = lhs_mode;
@@ -1073,6 +1212,7 @@ extern "C" moe_status tgmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe
                  MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(aligned16(lhs_q) && aligned16(rhs_q) && aligned16(out) && aligned16(workspace),
                  MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(rhs_mode == MOE_SCALE_PER_TENSOR || aligned16(rhs_scale), MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(workspace_bytes >= tgmm_fp8_workspace_bytes(M, K, N, E_local), MOE_ERR_INVALID_ARG);
   if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
   cudaStream_t st = as_stream(stream);
@@ -1089,7 +1229,8 @@ extern "C" moe_status tgmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe
   }
   CUtensorMap A, B;
   if (!make_map(&A, lhsT, Mp, K, Mp, BM)) return MOE_ERR_CUDA;
-  if (!make_map(&B, rhsT, Mp, N, Mp, BN)) return MOE_ERR_CUDA;
+  constexpr int bn = Cfg<kTgmm>::BN;
+  if (!make_map(&B, rhsT, Mp, N, Mp, bn)) return MOE_ERR_CUDA;
   Params p{};
   p.group_sizes = group_sizes;
   p.E = E;
@@ -1099,7 +1240,7 @@ extern "C" moe_status tgmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe
   p.K = static_cast<int>(K);
   p.N = static_cast<int>(N);
   p.kblocks = 0;
-  p.ntiles = static_cast<int>((N + BN - 1) / BN);
+  p.ntiles = static_cast<int>((N + bn - 1) / bn);
   p.ktiles = static_cast<int>((K + BM - 1) / BM);
   p.lhs_scale = lhs_scale;
   p.lhs_mode = lhs_mode;
