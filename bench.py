@@ -435,15 +435,15 @@ def run_suite(args):
                           lambda: moe.gmm_swiglu(buf.sort["xs_q"], xs_s, am, W.w_in, W.s_in, W.in_mode,
                                                  buf.sort["group_sizes"], am, sh, h=buf.h, h_q=buf.h_q,
                                                  h_scale=buf.h_s, a_out=buf.a if buf.keep_a else None),
-                          "tensor", 2.0 * R * D * 2 * F))
+                          "tensor", (2.0 * R * D * 2 * F, R * D + E * 2 * F * D + (5 if am == 0 else 1) * R * F)))
         calls.append(("gmm_fp8 wi_0|wi_1", lambda: moe.gmm(buf.sort["xs_q"], xs_s, am, W.w_in, W.s_in, W.in_mode,
                                                            buf.sort["group_sizes"], out=buf.a),
-                      "tensor", 2.0 * R * D * 2 * F))
+                      "tensor", (2.0 * R * D * 2 * F, R * D + E * 2 * F * D + 4 * R * F)))
         calls.append(("moe_swiglu_quant", lambda: moe.swiglu_quant(buf.a, am, sh, h_q=buf.h_q, h_scale=buf.h_s),
                       "hbm", 5 * R * F + sbytes(R, F)))
         calls.append(("gmm_fp8 wo", lambda: moe.gmm(buf.h_q, h_s, am, W.w_out, W.s_out, W.out_mode,
                                                     buf.sort["group_sizes"], out=buf.o),
-                      "tensor", 2.0 * R * F * D))
+                      "tensor", (2.0 * R * F * D, R * F + E * D * F + 2 * R * D)))
         calls.append(("ragged_gather_reduce", lambda: moe.ragged_gather_reduce(buf.o, buf.sort["pos"], w, k,
                                                                                 out=buf.y),
                       "hbm", 2 * R * D + 2 * T * D + 8 * R))
@@ -457,12 +457,12 @@ def run_suite(args):
                 ("bwd moe_gather_scale_quant", lambda: moe.gather_scale_quant(G, wflat, src, k),
                  "hbm", 2 * T * D + 3 * R * D + 4 * R),
                 ("bwd gmm_fp8 dH = dO wo", lambda: moe.gmm(dO_q, dO_s, 0, W.w_out_t, W.s_out, 2, sizes, out=buf.dH),
-                 "tensor", 2.0 * R * D * F),
+                 "tensor", (2.0 * R * D * F, R * D + E * D * F + 2 * R * F)),
                 ("bwd moe_swiglu_bwd_quant", lambda: moe.swiglu_bwd_quant(buf.dH, buf.a),
                  "hbm", 2 * R * F + 4 * R * F + 6 * R * F + 4 * R),
                 ("bwd gmm_fp8 dXs = dA [wi_0|wi_1]", lambda: moe.gmm(dA_q, dA_s, 0, W.w_in_t, W.s_in_t, 1, sizes,
                                                                     out=buf.dXs),
-                 "tensor", 2.0 * R * 2 * F * D),
+                 "tensor", (2.0 * R * 2 * F * D, 2 * R * F + E * 2 * F * D + 2 * R * D)),
                 ("bwd ragged_gather_reduce dX", lambda: moe.ragged_gather_reduce(buf.dXs, buf.sort["pos"], None, k,
                                                                                  out=buf.dX),
                  "hbm", 2 * R * D + 2 * T * D + 4 * R),
@@ -477,10 +477,10 @@ def run_suite(args):
             calls += [
                 ("bwd tgmm_fp8 dW_in (incl. operand transposes)",
                  lambda: moe.tgmm(buf.sort["xs_q"], sx, 2, dAg_q, dAg_s, 3, sizes, workspace=ws),
-                 "tensor", 2.0 * R * D * 2 * F),
+                 "tensor", (2.0 * R * D * 2 * F, 4 * E * D * 2 * F + R * D + R * 2 * F)),
                 ("bwd tgmm_fp8 dW_out (incl. operand transposes)",
                  lambda: moe.tgmm(buf.h_q, sh, 2, dOg_q, dOg_s, 3, sizes, workspace=ws),
-                 "tensor", 2.0 * R * F * D),
+                 "tensor", (2.0 * R * F * D, 4 * E * F * D + R * F + R * D)),
             ]
         total = 0.0
         for label, fn, bound, work in calls:
@@ -488,7 +488,12 @@ def run_suite(args):
             if bound == "hbm":
                 ach, peak, unit = work / (ms / 1e3) / 1e9, hbm, "GB/s"
             else:
-                ach, peak, unit = work / (ms / 1e3) / 1e12, fp8, "TFLOP/s"
+                # a contraction is bound by whichever of its flops and its bytes takes longer
+                flops, nbytes = work
+                if nbytes / (hbm * 1e9) > flops / (fp8 * 1e12):
+                    bound, ach, peak, unit = "hbm", nbytes / (ms / 1e3) / 1e9, hbm, "GB/s"
+                else:
+                    ach, peak, unit = flops / (ms / 1e3) / 1e12, fp8, "TFLOP/s"
             on_path = not (fused and label in ("gmm_fp8 wi_0|wi_1", "moe_swiglu_quant"))
             if on_path:
                 total += ms

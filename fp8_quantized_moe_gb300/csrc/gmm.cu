@@ -111,13 +111,18 @@ struct Cfg {
   static constexpr bool PROMOTE = MODE == kPromote;
   static constexpr int BN = PROMOTE ? MOE_PROMOTE_BN : 256;  // output columns per tile
   static constexpr int NACC = 512 / BN;                      // accumulators; NACC * BN = 512 TMEM columns
-  static constexpr int NSTAGE = BN == 128 ? 6 : MOE_GMM_NSTAGE;
+  static constexpr int NSTAGE = BN == 128 ? 6 : (MODE == kTgmm ? 3 : MOE_GMM_NSTAGE);
   static constexpr int B_BYTES = BN * BK;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
   static constexpr int EPI_WARPS = (MODE == kPromote || MODE == kSwiglu) ? 8 : 4;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  static constexpr size_t SMEM = 1024 + static_cast<size_t>(NSTAGE) * STAGE_BYTES + sizeof(SmemCtl);
+  // per-warp staging of 32x32 output blocks for row-contiguous stores:
+  // bf16 rows padded to 80 bytes (kFinal), fp32 rows padded to 144 bytes (kTgmm)
+  static constexpr int STG_PITCH = MODE == kFinal ? 80 : (MODE == kTgmm ? 144 : 0);
+  static constexpr size_t CTL_BYTES = (sizeof(SmemCtl) + 127) / 128 * 128;
+  static constexpr size_t SMEM = 1024 + static_cast<size_t>(NSTAGE) * STAGE_BYTES + CTL_BYTES +
+                                 static_cast<size_t>(EPI_WARPS) * 32 * STG_PITCH;
   static_assert(NSTAGE <= kMaxStages && NACC <= kMaxAcc && NACC * BN == 512, "tile configuration");
 };
 
@@ -301,6 +306,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw_addr);
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(base_ptr + NSTAGE * STAGE_BYTES);
+  uint8_t* stg_base = base_ptr + NSTAGE * STAGE_BYTES + C::CTL_BYTES;  // output staging (kFinal, kTgmm)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (warp == 0) build_group_tables<MODE == kTgmm>(p, ctl);
@@ -477,20 +483,29 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
           float sg[32];
           load_col_scales32(sgb, nb, p.N, per_col, sg_t, sg);
           tmem_wait_ld();
-          if (row_ok) {
+          // stage this warp's 32x32 block, then write 4 rows (128 contiguous bytes each) per instruction
+          float* stg = reinterpret_cast<float*>(stg_base + (warp - 2) * 32 * C::STG_PITCH);
+          constexpr int PF = C::STG_PITCH / 4;  // pitch in floats
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              const int n = nb + g * 4;
-              if (n < p.N) {
-                float4 o;
-                o.x = __uint_as_float(v[g * 4 + 0]) * sx * sg[g * 4 + 0];
-                o.y = __uint_as_float(v[g * 4 + 1]) * sx * sg[g * 4 + 1];
-                o.z = __uint_as_float(v[g * 4 + 2]) * sx * sg[g * 4 + 2];
-                o.w = __uint_as_float(v[g * 4 + 3]) * sx * sg[g * 4 + 3];
-                *reinterpret_cast<float4*>(orow + n) = o;
-              }
-            }
+          for (int g = 0; g < 8; ++g) {
+            float4 o;
+            o.x = __uint_as_float(v[g * 4 + 0]) * sx * sg[g * 4 + 0];
+            o.y = __uint_as_float(v[g * 4 + 1]) * sx * sg[g * 4 + 1];
+            o.z = __uint_as_float(v[g * 4 + 2]) * sx * sg[g * 4 + 2];
+            o.w = __uint_as_float(v[g * 4 + 3]) * sx * sg[g * 4 + 3];
+            *reinterpret_cast<float4*>(stg + lane * PF + 4 * g) = o;
           }
+          __syncwarp();
+          const int cseg = (lane & 7) * 4;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = i * 4 + (lane >> 3);  // row of this warp's block
+            const int64_t k = tl.row0 + q4 * 32 + rr;
+            if (rr < tl.rows - q4 * 32 && nb + cseg < p.N)
+              *reinterpret_cast<float4*>(out + (static_cast<int64_t>(tl.el) * p.K + k) * p.N + nb + cseg) =
+                  *reinterpret_cast<const float4*>(stg + rr * PF + cseg);
+          }
+          __syncwarp();
         }
         tc_fence_before();
         __syncwarp();
@@ -627,12 +642,32 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
           float sw[32];
           load_col_scales32(swb, nb, p.N, per_chan, sw_t, sw);
           tmem_wait_ld();
-          if (row_ok && nb < p.N) {
-            float f[32];
+          // stage this warp's 32x32 bf16 block, then write 8 rows (64 contiguous bytes each) per instruction
+          uint8_t* stg = stg_base + (warp - 2) * 32 * C::STG_PITCH;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) f[j] = __fmul_rn(__fmul_rn(__uint_as_float(v[j]), sa), sw[j]);
-            store_bf16x32(out + row * p.N + nb, f, p.N - nb);
+          for (int g = 0; g < 4; ++g) {
+            uint4 q;
+            q.x = pack_bf16x2(__fmul_rn(__fmul_rn(__uint_as_float(v[8 * g + 0]), sa), sw[8 * g + 0]),
+                              __fmul_rn(__fmul_rn(__uint_as_float(v[8 * g + 1]), sa), sw[8 * g + 1]));
+            q.y = pack_bf16x2(__fmul_rn(__fmul_rn(__uint_as_float(v[8 * g + 2]), sa), sw[8 * g + 2]),
+                              __fmul_rn(__fmul_rn(__uint_as_float(v[8 * g + 3]), sa), sw[8 * g + 3]));
+            q.z = pack_bf16x2(__fmul_rn(__fmul_rn(__uint_as_float(v[8 * g + 4]), sa), sw[8 * g + 4]),
+                              __fmul_rn(__fmul_rn(__uint_as_float(v[8 * g + 5]), sa), sw[8 * g + 5]));
+            q.w = pack_bf16x2(__fmul_rn(__fmul_rn(__uint_as_float(v[8 * g + 6]), sa), sw[8 * g + 6]),
+                              __fmul_rn(__fmul_rn(__uint_as_float(v[8 * g + 7]), sa), sw[8 * g + 7]));
+            *reinterpret_cast<uint4*>(stg + lane * C::STG_PITCH + 16 * g) = q;
           }
+          __syncwarp();
+          const int seg = (lane & 3) * 8;  // bf16 column offset of this lane's 16 bytes
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int rr = i * 8 + (lane >> 2);
+            const int64_t orow = static_cast<int64_t>(tl.row0) + q4 * 32 + rr;
+            if (rr < tl.rows - q4 * 32 && nb + seg < p.N)
+              *reinterpret_cast<uint4*>(out + orow * p.N + nb + seg) =
+                  *reinterpret_cast<const uint4*>(stg + rr * C::STG_PITCH + 2 * seg);
+          }
+          __syncwarp();
         }
         tc_fence_before();
         __syncwarp();

@@ -286,13 +286,16 @@ moe_status check_mode_ptrs(moe_scale_mode mode, const float* static_scale, const
 }
 
 // ---- per-(expert, column) gradient quantisation -------------------------
-// Tiles of 64 rows x 256 columns: 8 warps, each warp owns 8 rows, each lane
-// 8 consecutive columns.  Rows walk through the groups in order, so a lane
-// keeps one running maximum per column and flushes it with atomicMax (the bit
-// pattern of a non-negative float orders like an unsigned integer) whenever
-// the group changes.  The scale array holds the maxima until a second kernel
-// turns them into amax / 448.
-constexpr int kGcRows = 64;
+// CTA tile: 256 columns x 256 rows; each warp owns a strip of 32 consecutive
+// rows, each lane 8 consecutive columns (one 16-byte load per row).  Rows are
+// read 8 at a time (8 loads in flight per thread) and walk through the groups
+// in order, so a lane keeps one running maximum per column and flushes it with
+// atomicMax (the bit pattern of a non-negative float orders like an unsigned
+// integer) only when its strip crosses into the next group.  The scale array
+// holds the maxima until a second kernel turns them into amax / 448; a third
+// pass quantises against them.
+constexpr int kGcRows = 256;
+constexpr int kGcStrip = 32;
 constexpr int kMaxGroups = 1024;
 
 // Global start row of every group, for groups [0, E]; computed by warp 0.
@@ -335,65 +338,76 @@ __global__ void __launch_bounds__(256) group_cols_kernel(const uint16_t* g, int6
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * 32 + lane) * 8;
   if (c0 >= N) return;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kGcRows + warp * 8;
   const int64_t lo = starts[g0], hi = starts[g0 + El];
-  float m[8];
+  int64_t r0 = static_cast<int64_t>(blockIdx.y) * kGcRows + warp * kGcStrip;
+  int64_t r1 = min(r0 + kGcStrip, M);
+  r0 = max(r0, lo);
+  r1 = min(r1, hi);
+  if (r0 >= r1) return;
+  int grp = find_group(starts, E, r0);  // global group of row r0
+  int64_t gend = starts[grp + 1];
+  float m[8], sc[8], inv[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) m[j] = 0.0f;
-  int cur = -1;
-  float sc[8], inv[8];
-  for (int rr = 0; rr < 8; ++rr) {
-    const int64_t row = r0 + rr;
-    if (row >= M) break;
-    if (row < lo || row >= hi) continue;
-    const int grp = find_group(starts, E, row) - g0;
-    if (grp != cur) {
-      if (!QUANT && cur >= 0) {
+  auto load_scales = [&](int gg) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          atomicMax(reinterpret_cast<unsigned int*>(scale) + static_cast<int64_t>(cur) * N + c0 + j,
-                    __float_as_uint(m[j]));
-      }
-      if (QUANT) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          sc[j] = scale[static_cast<int64_t>(grp) * N + c0 + j];
-          inv[j] = __frcp_rn(sc[j]);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) m[j] = 0.0f;
-      cur = grp;
+    for (int j = 0; j < 8; ++j) {
+      sc[j] = scale[static_cast<int64_t>(gg - g0) * N + c0 + j];
+      inv[j] = __frcp_rn(sc[j]);
     }
-    float v[8];
-    unpack8(ldg16(g + row * N + c0), v);
-    if (QUANT) {
-      float y[8];
-      bool slow = false;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        y[j] = __fmul_rn(v[j], inv[j]);
-        slow = slow || quant_needs_division(y[j]);
-      }
-      if (slow) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (quant_needs_division(y[j])) y[j] = __fdiv_rn(v[j], sc[j]);
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = y[j];
-      *reinterpret_cast<uint2*>(q + row * N + c0) = pack_e4m3x8(v);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) m[j] = fmaxf(m[j], fabsf(v[j]));
-    }
-  }
-  if (!QUANT && cur >= 0) {
+  };
+  auto flush = [&](int gg) {
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      atomicMax(reinterpret_cast<unsigned int*>(scale) + static_cast<int64_t>(cur) * N + c0 + j,
+      atomicMax(reinterpret_cast<unsigned int*>(scale) + static_cast<int64_t>(gg - g0) * N + c0 + j,
                 __float_as_uint(m[j]));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m[j] = 0.0f;
+  };
+  if (QUANT) load_scales(grp);
+  for (int64_t rb = r0; rb < r1; rb += 8) {
+    uint4 d[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (rb + i < r1) d[i] = __ldg(reinterpret_cast<const uint4*>(g + (rb + i) * N + c0));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int64_t row = rb + i;
+      if (row >= r1) break;
+      while (row >= gend) {  // next group (rows walk forward through the groups)
+        if (!QUANT) flush(grp);
+        ++grp;
+        gend = starts[grp + 1];
+        if (QUANT) load_scales(grp);
+      }
+      const uint32_t w[4] = {d[i].x, d[i].y, d[i].z, d[i].w};
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[2 * j] = bf16lo(w[j]);
+        v[2 * j + 1] = bf16hi(w[j]);
+      }
+      if (QUANT) {
+        float y[8];
+        bool slow = false;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          y[j] = __fmul_rn(v[j], inv[j]);
+          slow = slow || quant_needs_division(y[j]);
+        }
+        if (slow) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (quant_needs_division(y[j])) y[j] = __fdiv_rn(v[j], sc[j]);
+        }
+        *reinterpret_cast<uint2*>(q + row * N + c0) = pack_e4m3x8(y);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m[j] = fmaxf(m[j], fabsf(v[j]));
+      }
+    }
   }
+  if (!QUANT) flush(grp);
 }
 
 __global__ void finalize_scales_kernel(float* scale, int64_t n) {
