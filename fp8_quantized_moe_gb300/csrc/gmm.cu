@@ -90,14 +90,18 @@ struct SmemCtl {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  int no_abort;  // always 0: for waits that must run to completion or to their time limit
   int err;
   int total_tiles;
   int gstart[kMaxGroups + 1];       // gmm: first row of local group; tgmm: padded first row
   int tile_prefix[kMaxGroups + 1];  // gmm: first tile of local group
   int gsize[kMaxGroups];
-  float sw_stage[8][64];            // promotion: weight scales of the current K block, per warp
-  float pamax[2][4][2][32];          // fused SwiGLU, per-128 h scales: row maxima of the two column halves
+  alignas(16) float sw_stage[8][64];    // promotion: weight scales of the current K block, per warp
+  alignas(16) float pamax[2][4][2][32];  // fused SwiGLU, per-128 h scales: row maxima of the two column halves
 };
+// sw_stage is read and written with float2 / float4 accesses
+static_assert(offsetof(SmemCtl, sw_stage) % 16 == 0 && offsetof(SmemCtl, pamax) % 16 == 0, "SmemCtl alignment");
+static_assert(sizeof(SmemCtl) % 16 == 0, "SmemCtl size");
 
 // Tile configuration per mode.  Promotion (a blockwise operand scale) uses
 // 128x128 tiles with four TMEM accumulators, so the MMA can run up to three K
@@ -321,6 +325,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort_flag = 0;
+    ctl->no_abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -376,7 +381,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
         ctl->err = 2;
         // let the loads already issued land before the CTA can exit
         for (uint32_t j = (it > NSTAGE ? it - NSTAGE : 0); j < it; ++j)
-          mbar_wait_bounded(smem_u32(&ctl->full[j % NSTAGE]), (j / NSTAGE) & 1, abort_flag + 1, kWaitLimitNs);
+          mbar_wait_bounded(smem_u32(&ctl->full[j % NSTAGE]), (j / NSTAGE) & 1, &ctl->no_abort, kWaitLimitNs);
       }
     }
     __syncwarp();
@@ -437,7 +442,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
       }
       // drain: every MMA this thread issued has completed once `drain` flips
       mma_commit(smem_u32(&ctl->drain));
-      if (!mbar_wait_bounded(smem_u32(&ctl->drain), 0, abort_flag + 1, kWaitLimitNs)) timed_out = true;
+      if (!mbar_wait_bounded(smem_u32(&ctl->drain), 0, &ctl->no_abort, kWaitLimitNs)) timed_out = true;
       if (timed_out) {
         *abort_flag = 1;
         ctl->err = 2;
