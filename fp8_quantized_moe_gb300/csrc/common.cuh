@@ -187,12 +187,24 @@ __device__ __forceinline__ void swiglu_h(const float* a0, const float* a1, float
   for (int j = 0; j < N; ++j) h[j] = round_bf16(__fmul_rn(silu_f32(a0[j]), a1[j]));
 }
 
-// True when e4m3(x * inv_s) may differ from e4m3(fp32(x / s)) (see below).
+// Fast e4m3 quotient.  y = x * inv_s with inv_s = 1/s rounded to nearest lies
+// within 2 ulp of x / s (two roundings of relative size 2^-24).  Rounding to
+// e4m3 keeps 3 mantissa bits, so y and fp32(x / s) can only round to
+// different e4m3 values when a midpoint between two neighbouring e4m3 values
+// lies within those ulp.  For |y| >= 2^-6 (normal e4m3) the midpoints are the
+// fp32 values whose low 20 mantissa bits are 0x80000.  Below 2^-6 the e4m3
+// grid is uniform with step 2^-9, the same step as the normal binade
+// [2^-6, 2^-5); adding 2^-6 maps that grid and its midpoints onto the
+// binade's, and the addition rounds by at most 2^-30, far inside the +-8 ulp
+// (8 * 2^-29) window tested.  So one test on the low mantissa bits of
+// |y| (+ 2^-6 when small) finds every value that may round differently; those
+// rare values take the exact division, everywhere else
+// e4m3(y) == e4m3(fp32(x / s)).  Above 448 every value saturates to 448 either
+// way.
 __device__ __forceinline__ bool quant_needs_division(float y) {
-  const uint32_t u = __float_as_uint(y);
-  const bool near_mid = ((u & 0xFFFFFu) - 0x80000u + 8u) <= 16u;
-  const bool small = ((u & 0x7FFFFFFFu) - 1u) < (0x3C800000u - 1u);  // 0 < |y| < 2^-6
-  return near_mid || small;
+  const float a = fabsf(y);
+  const float v = a < 0x1p-6f ? __fadd_rn(a, 0x1p-6f) : a;
+  return ((__float_as_uint(v) & 0xFFFFFu) - 0x80000u + 8u) <= 16u;
 }
 
 // out[j] = fp32(x[j] / s) as far as e4m3 rounding can tell, for N elements.
@@ -211,22 +223,10 @@ __device__ __forceinline__ void quant_n(const float* x, float s, float inv, floa
   }
 }
 
-// The quotient that e4m3 quantisation rounds, fp32(x / s), without a division
-// per element.  y = x * inv_s with inv_s = 1/s rounded to nearest lies within
-// 2 ulp of x / s (two roundings of relative size 2^-24).  Rounding to e4m3
-// keeps 3 mantissa bits, so y and fp32(x / s) can only round to different
-// e4m3 values when a midpoint between two e4m3 values (low 20 mantissa bits
-// 0x80000) lies within those ulp, or in the e4m3 subnormal range |y| < 2^-6
-// where the rounding position moves.  Those rare values take the exact
-// division; everywhere else e4m3(y) == e4m3(fp32(x / s)).  Above 448 every
-// value saturates to 448 either way.
+// The quotient that e4m3 quantisation rounds, fp32(x / s), for one element.
 __device__ __forceinline__ float quant_quotient(float x, float s, float inv_s) {
   const float y = __fmul_rn(x, inv_s);
-  const uint32_t u = __float_as_uint(y);
-  const bool near_mid = ((u & 0xFFFFFu) - 0x80000u + 8u) <= 16u;
-  const bool small = (u & 0x7FFFFFFFu) < 0x3C800000u;
-  if (near_mid || small) return __fdiv_rn(x, s);
-  return y;
+  return quant_needs_division(y) ? __fdiv_rn(x, s) : y;
 }
 
 // ------------------------------------------------------------------------
