@@ -412,7 +412,9 @@ def run_suite(args):
     pk, pk_kind = peaks()
     hbm = pk["hbm_gbs"]
     fp8 = 2.0 * pk["bf16_tflops"]  # calls timed alone: burst figure
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    # L2 flush by reading 512 MB (> 129 MB of L2): the lines left behind are
+    # clean, so the timed call pays no write-back of someone else's data
+    flush = torch.ones(64 * 1024 * 1024, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream()
     lines = []
 
@@ -421,7 +423,7 @@ def run_suite(args):
         torch.cuda.synchronize()
         ts = []
         for _ in range(reps):
-            flush.fill_(1)  # evict the previous call's data from L2 (512 MB > 129 MB)
+            flush.sum()  # evict the previous call's data from L2
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             fn()

@@ -55,7 +55,6 @@ constexpr int kMaxStages = 8;
 constexpr int kMaxAcc = 4;
 constexpr int kMaxGroups = 1024;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
-constexpr uint32_t kTmemCols = 512;
 
 enum Mode { kFinal = 0, kPromote = 1, kTgmm = 2, kSwiglu = 3 };
 
@@ -106,19 +105,32 @@ static_assert(sizeof(SmemCtl) % 16 == 0, "SmemCtl size");
 // Tile configuration per mode.  Promotion (a blockwise operand scale) uses
 // 128x128 tiles with four TMEM accumulators, so the MMA can run up to three K
 // blocks ahead of the epilogue that folds each block's partial sums into
-// registers; the other modes use 128x256 tiles with two accumulators.
+// registers; tgmm uses 128x256 tiles with two accumulators.  The plain and
+// SwiGLU gmm run on CTA pairs (a 2-CTA cluster): one 256x256 MMA per K step
+// over both CTAs, each CTA holding 128 rows of A and half of the B tile, so a
+// stage is 32 KB per CTA instead of 48 and the operand traffic through each
+// SM's shared memory drops by a third.
 #ifndef MOE_PROMOTE_BN
 #define MOE_PROMOTE_BN 128
+#endif
+#ifndef MOE_GMM_PAIR
+#define MOE_GMM_PAIR 1
+#endif
+#ifndef MOE_PAIR_TMEM_COLS
+#define MOE_PAIR_TMEM_COLS 512
 #endif
 template <int MODE>
 struct Cfg {
   static constexpr bool PROMOTE = MODE == kPromote;
+  static constexpr bool PAIR = MOE_GMM_PAIR && (MODE == kFinal || MODE == kSwiglu);
   static constexpr int BN = PROMOTE ? MOE_PROMOTE_BN : 256;  // output columns per tile
-  static constexpr int NACC = 512 / BN;                      // accumulators; NACC * BN = 512 TMEM columns
-  static constexpr int NSTAGE = BN == 128 ? 6 : (MODE == kTgmm ? 3 : MOE_GMM_NSTAGE);
-  static constexpr int B_BYTES = BN * BK;
+  static constexpr int TMEM_COLS = PAIR ? MOE_PAIR_TMEM_COLS : 512;
+  static constexpr int NACC = TMEM_COLS / BN;                // accumulators of BN columns
+  static constexpr int NSTAGE = PAIR ? 6 : (BN == 128 ? 6 : (MODE == kTgmm ? 3 : MOE_GMM_NSTAGE));
+  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK;  // this CTA's part of the B tile
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
+  static constexpr uint32_t TX_BYTES = (PAIR ? 2 : 1) * STAGE_BYTES;  // what one full barrier waits for
+  static constexpr uint32_t IDESC = idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN);
   static constexpr int EPI_WARPS = (MODE == kPromote || MODE == kSwiglu) ? 8 : 4;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   // per-warp staging of 32x32 output blocks for row-contiguous stores:
@@ -127,14 +139,17 @@ struct Cfg {
   static constexpr size_t CTL_BYTES = (sizeof(SmemCtl) + 127) / 128 * 128;
   static constexpr size_t SMEM = 1024 + static_cast<size_t>(NSTAGE) * STAGE_BYTES + CTL_BYTES +
                                  static_cast<size_t>(EPI_WARPS) * 32 * STG_PITCH;
-  static_assert(NSTAGE <= kMaxStages && NACC <= kMaxAcc && NACC * BN == 512, "tile configuration");
+  static_assert(NSTAGE <= kMaxStages && NACC >= 1 && NACC <= kMaxAcc && NACC * BN == TMEM_COLS,
+                "tile configuration");
+  static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
 // ---- group tables --------------------------------------------------------
 // Warp 0 reads all E sizes at once (<= 32 per lane), scans them, and fills
 // the tables for the local groups [g0, g0 + El).  Returns (in ctl->err) 1 if a
-// size is negative or the sizes do not add up to M.
-template <bool TGMM>
+// size is negative or the sizes do not add up to M.  With PAIR a unit of work
+// is a pair of M tiles (one per CTA of the pair).
+template <bool TGMM, bool PAIR>
 __device__ void build_group_tables(const Params& p, SmemCtl* ctl) {
   const int lane = threadIdx.x & 31;
   int v[kMaxGroups / 32];
@@ -157,7 +172,9 @@ __device__ void build_group_tables(const Params& p, SmemCtl* ctl) {
     int64_t incl = sz;
     // aux: gmm -> tiles of the group; tgmm -> padded rows of the group
     int aux = 0;
-    if (mine && sz > 0) aux = TGMM ? ((sz + BM - 1) / BM) * BM : ((sz + BM - 1) / BM) * p.ntiles;
+    if (mine && sz > 0)
+      aux = TGMM ? ((sz + BM - 1) / BM) * BM
+                 : (PAIR ? (sz + 2 * BM - 1) / (2 * BM) : (sz + BM - 1) / BM) * p.ntiles;
     int incl_aux = aux;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -204,9 +221,10 @@ struct Tile {
 };
 
 template <int MODE>
-__device__ __forceinline__ Tile get_tile(const Params& p, const SmemCtl* ctl, int t) {
+__device__ __forceinline__ Tile get_tile(const Params& p, const SmemCtl* ctl, int t, int rank) {
   Tile tl;
   constexpr int BN = Cfg<MODE>::BN;
+  constexpr bool PAIR = Cfg<MODE>::PAIR;
   if (MODE == kTgmm) {
     const int per = p.ktiles * p.ntiles;
     tl.el = t / per;
@@ -232,21 +250,24 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const SmemCtl* ctl, in
     while (lo + 1 < p.El && ctl->tile_prefix[lo + 1] <= t) ++lo;
     tl.el = lo;
     const int sz = ctl->gsize[lo];
-    const int mt = (sz + BM - 1) / BM;
+    // M tiles of the group, counted in units (pairs of tiles for a CTA pair)
+    const int mt = PAIR ? (sz + 2 * BM - 1) / (2 * BM) : (sz + BM - 1) / BM;
     const int local = t - ctl->tile_prefix[lo];
-    const int nt = local / mt, mi = local - nt * mt;
+    const int nt = local / mt;
+    const int mi = PAIR ? 2 * (local - nt * mt) + rank : local - nt * mt;
     tl.nkb = p.kblocks;
     tl.row0 = ctl->gstart[lo] + mi * BM;
-    tl.rows = min(BM, sz - mi * BM);
+    tl.rows = min(BM, sz - mi * BM);  // <= 0: the odd CTA of a pair past the group's end
     tl.ax = 0;
     tl.ay = tl.row0;
     tl.bx = 0;
     if (MODE == kSwiglu) {
       // 128 h columns: wi_0 channels nt*128.. and the matching wi_1 channels
-      tl.by = lo * 2 * p.F + nt * 128;
+      // (a CTA pair: the even CTA holds the wi_0 rows, the odd one the wi_1 rows)
+      tl.by = lo * 2 * p.F + nt * 128 + (PAIR ? rank * p.F : 0);
       tl.n0 = nt * 128;
     } else {
-      tl.by = lo * p.N + nt * BN;
+      tl.by = lo * p.N + nt * BN + (PAIR ? rank * (BN / 2) : 0);
       tl.n0 = nt * BN;
     }
   }
@@ -305,6 +326,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
   constexpr int EPI_WARPS = C::EPI_WARPS, BN = C::BN, NSTAGE = C::NSTAGE, NACC = C::NACC;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
   constexpr uint32_t IDESC = C::IDESC;
+  constexpr bool PAIR = C::PAIR;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -312,8 +334,13 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(base_ptr + NSTAGE * STAGE_BYTES);
   uint8_t* stg_base = base_ptr + NSTAGE * STAGE_BYTES + C::CTL_BYTES;  // output staging (kFinal, kTgmm)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // A CTA pair works on the same sequence of units; its even CTA (rank 0)
+  // issues the MMAs and owns the full and accumulator-empty barriers.
+  const int rank = PAIR ? static_cast<int>(__clusterRelativeBlockRank()) : 0;
+  const int unit0 = PAIR ? static_cast<int>(__clusterIdx().x) : static_cast<int>(blockIdx.x);
+  const int units = PAIR ? static_cast<int>(__clusterGridDimInClusters().x) : static_cast<int>(gridDim.x);
 
-  if (warp == 0) build_group_tables<MODE == kTgmm>(p, ctl);
+  if (warp == 0) build_group_tables<MODE == kTgmm, PAIR>(p, ctl);
   if (threadIdx.x == 32) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
@@ -321,7 +348,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
     }
     for (int a = 0; a < NACC; ++a) {
       mbar_init(smem_u32(&ctl->tfull[a]), 1);
-      mbar_init(smem_u32(&ctl->tempty[a]), EPI_WARPS);
+      mbar_init(smem_u32(&ctl->tempty[a]), (PAIR ? 2 : 1) * EPI_WARPS);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort_flag = 0;
@@ -329,32 +356,50 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
     fence_mbar_init();
   }
   __syncthreads();
+  // both CTAs of a pair read the same group sizes, so they leave here together
   if (ctl->err) {
     if (threadIdx.x == 0) raise_error(&g_err, MOE_DEVERR_GROUP_SIZES);
     return;
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(&ctl->tmem_base), C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&ctl->tmem_base), C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
   tc_fence_before();
-  __syncthreads();
+  // a pair: the peer's barriers are initialised and its columns allocated
+  // before any operand, commit or release crosses between the two CTAs
+  if (PAIR) cluster_sync_all(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
+  if (PAIR && rank == 1 && threadIdx.x == 0 &&
+      ld_shared_cluster_u32(mapa_shared(smem_u32(&ctl->tmem_base), 0)) != tmem_base)
+    raise_error(&g_err, MOE_DEVERR_TMEM);  // the pair's accumulators would not line up
   const int total = ctl->total_tiles;
   volatile int* abort_flag = &ctl->abort_flag;
   bool timed_out = false;
+  // release of accumulator `a` by one epilogue warp (to the pair's even CTA)
+  auto release_acc = [&](uint32_t a) {
+    if (PAIR)
+      mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[a]), 0));
+    else
+      mbar_arrive(smem_u32(&ctl->tempty[a]));
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t it = 0;
-      for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
-        const Tile tl = get_tile<MODE>(p, ctl, t);
+      for (int t = unit0; t < total && !timed_out; t += units) {
+        const Tile tl = get_tile<MODE>(p, ctl, t, rank);
         for (int kb = 0; kb < tl.nkb; ++kb) {
           const int s = it % NSTAGE;
           const uint32_t ph = (it / NSTAGE) & 1;
@@ -362,16 +407,24 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
             timed_out = true;
             break;
           }
-          const uint32_t fb = smem_u32(&ctl->full[s]);
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
           const uint32_t sa = base + s * STAGE_BYTES;
-          tma_load_2d(sa, &tmA, tl.ax + kb * BK, tl.ay, fb);
-          if (MODE == kSwiglu) {
-            // B rows 0..127: wi_0 channels; rows 128..255: the matching wi_1 channels
-            tma_load_2d(sa + A_BYTES, &tmB, tl.bx + kb * BK, tl.by, fb);
-            tma_load_2d(sa + 2 * A_BYTES, &tmB, tl.bx + kb * BK, tl.by + p.F, fb);
+          if (PAIR) {
+            // both CTAs' boxes complete on the even CTA's full barrier
+            const uint32_t fb = mapa_shared(smem_u32(&ctl->full[s]), 0);
+            if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), C::TX_BYTES);
+            tma_load_2d_pair(sa, &tmA, tl.ax + kb * BK, tl.ay, fb);
+            tma_load_2d_pair(sa + A_BYTES, &tmB, tl.bx + kb * BK, tl.by, fb);
           } else {
-            tma_load_2d(sa + A_BYTES, &tmB, tl.bx + kb * BK, tl.by, fb);
+            const uint32_t fb = smem_u32(&ctl->full[s]);
+            mbar_arrive_expect_tx(fb, C::TX_BYTES);
+            tma_load_2d(sa, &tmA, tl.ax + kb * BK, tl.ay, fb);
+            if (MODE == kSwiglu) {
+              // B rows 0..127: wi_0 channels; rows 128..255: the matching wi_1 channels
+              tma_load_2d(sa + A_BYTES, &tmB, tl.bx + kb * BK, tl.by, fb);
+              tma_load_2d(sa + 2 * A_BYTES, &tmB, tl.bx + kb * BK, tl.by + p.F, fb);
+            } else {
+              tma_load_2d(sa + A_BYTES, &tmB, tl.bx + kb * BK, tl.by, fb);
+            }
           }
           ++it;
         }
@@ -379,18 +432,21 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
       if (timed_out) {
         *abort_flag = 1;
         ctl->err = 2;
-        // let the loads already issued land before the CTA can exit
-        for (uint32_t j = (it > NSTAGE ? it - NSTAGE : 0); j < it; ++j)
-          mbar_wait_bounded(smem_u32(&ctl->full[j % NSTAGE]), (j / NSTAGE) & 1, &ctl->no_abort, kWaitLimitNs);
+        // let the loads already issued land before the CTA can exit (the
+        // full barriers that count them are this CTA's unless it is the
+        // odd CTA of a pair)
+        if (!PAIR || rank == 0)
+          for (uint32_t j = (it > NSTAGE ? it - NSTAGE : 0); j < it; ++j)
+            mbar_wait_bounded(smem_u32(&ctl->full[j % NSTAGE]), (j / NSTAGE) & 1, &ctl->no_abort, kWaitLimitNs);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && (!PAIR || rank == 0)) {
       uint32_t it = 0, acc = 0;
-      for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
-        const Tile tl = get_tile<MODE>(p, ctl, t);
+      for (int t = unit0; t < total && !timed_out; t += units) {
+        const Tile tl = get_tile<MODE>(p, ctl, t, rank);
         if (tl.nkb == 0) continue;
         uint32_t a = acc % NACC;
         if (MODE != kPromote) {
@@ -425,9 +481,15 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
             const uint32_t accumulate = (MODE == kPromote) ? (k4 > 0) : (kb > 0 || k4 > 0);
             // +32 bytes along K inside the 128-byte swizzled row = +2 in the
             // descriptor's address field (16-byte units)
-            mma_f8(d_tmem, da + 2 * k4, db + 2 * k4, IDESC, accumulate);
+            if (PAIR)
+              mma_f8_pair(d_tmem, da + 2 * k4, db + 2 * k4, IDESC, accumulate);
+            else
+              mma_f8(d_tmem, da + 2 * k4, db + 2 * k4, IDESC, accumulate);
           }
-          mma_commit(smem_u32(&ctl->empty[s]));
+          if (PAIR)
+            mma_commit_pair_mc(smem_u32(&ctl->empty[s]), 0x3);  // frees the stage in both CTAs
+          else
+            mma_commit(smem_u32(&ctl->empty[s]));
           if (MODE == kPromote) {
             mma_commit(smem_u32(&ctl->tfull[a]));
             ++acc;
@@ -436,12 +498,18 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
         }
         if (timed_out) break;
         if (MODE != kPromote) {
-          mma_commit(smem_u32(&ctl->tfull[a]));
+          if (PAIR)
+            mma_commit_pair_mc(smem_u32(&ctl->tfull[a]), 0x3);
+          else
+            mma_commit(smem_u32(&ctl->tfull[a]));
           ++acc;
         }
       }
       // drain: every MMA this thread issued has completed once `drain` flips
-      mma_commit(smem_u32(&ctl->drain));
+      if (PAIR)
+        mma_commit_pair(smem_u32(&ctl->drain));
+      else
+        mma_commit(smem_u32(&ctl->drain));
       if (!mbar_wait_bounded(smem_u32(&ctl->drain), 0, &ctl->no_abort, kWaitLimitNs)) timed_out = true;
       if (timed_out) {
         *abort_flag = 1;
@@ -456,8 +524,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
     const int r = q4 * 32 + lane;                       // row of the tile = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
     uint32_t acc = 0;
-    for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
-      const Tile tl = get_tile<MODE>(p, ctl, t);
+    for (int t = unit0; t < total && !timed_out; t += units) {
+      const Tile tl = get_tile<MODE>(p, ctl, t, rank);
       const bool row_ok = r < tl.rows;
       if (MODE == kTgmm) {
         float* out = static_cast<float*>(p.out);
@@ -514,7 +582,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
+        if (lane == 0) release_acc(a);
         ++acc;
       } else if (MODE == kSwiglu) {
         // 8 warps: TMEM lane quarter q4, h columns [half*64, half*64 + 64) of
@@ -546,7 +614,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
           if (cc == 1) {  // the accumulator is no longer needed: release it early
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
+            if (lane == 0) release_acc(a);
           }
           const int hc = tl.n0 + c * 32;  // first h column of the chunk
           float f0[32], f1[32], h[32];
@@ -676,7 +744,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
+        if (lane == 0) release_acc(a);
         ++acc;
       } else {
         // promotion: one fresh accumulator per K block, folded into registers.
@@ -774,7 +842,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
             tmem_wait_ld();
             tc_fence_before();  // the accumulator is in registers: release it
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
+            if (lane == 0) release_acc(a);
             fold16(v, 0);
             fold16(v + 16, 16);
           } else if (WC == 64) {
@@ -786,7 +854,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
+            if (lane == 0) release_acc(a);
 #pragma unroll
             for (int c = 0; c < WC / 16; ++c) fold16(v + 16 * c, 16 * c);
           } else {
@@ -799,7 +867,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
               if (c == WC / 16 - 1) {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
+                if (lane == 0) release_acc(a);
               }
               fold16(v, 16 * c);
             }
@@ -845,10 +913,16 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
     }
   }
 
-  __syncthreads();
+  tc_fence_before();
+  // a pair: neither CTA leaves (or frees its columns) while the other may
+  // still write its tensor memory or arrive on its barriers
+  if (PAIR) cluster_sync_all(); else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
   if (threadIdx.x == 0 && ctl->err) raise_error(&g_err, MOE_DEVERR_TIMEOUT);
 }
@@ -1075,16 +1149,54 @@ bool device_is_sm103() {
   return major == 10 && minor == 3;
 }
 
+// Units of work for a gmm launch: M tiles (pairs of M tiles on CTA pairs)
+// times N tiles, bounded by the ragged-group worst case.
 template <int MODE>
-moe_status launch_mma(const CUtensorMap& A, const CUtensorMap& B, const Params& p, int max_tiles,
+int gmm_max_units(int64_t M, int E_local, int ntiles) {
+  const int64_t rows_per_unit = (Cfg<MODE>::PAIR ? 2 : 1) * BM;
+  const int64_t u = ((M + rows_per_unit - 1) / rows_per_unit + E_local) * ntiles;
+  return static_cast<int>(u > (1 << 30) ? (1 << 30) : u);
+}
+
+template <int MODE>
+moe_status launch_mma(const CUtensorMap& A, const CUtensorMap& B, const Params& p, int max_units,
                       cudaStream_t st) {
+  using C = Cfg<MODE>;
   MOE_CUDA_TRY(cudaFuncSetAttribute(mma_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(Cfg<MODE>::SMEM)));
+                                    static_cast<int>(C::SMEM)));
   const int sms = sm_count();
   if (sms <= 0) return MOE_ERR_CUDA;
-  const int grid = max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms;
-  mma_kernel<MODE><<<grid, Cfg<MODE>::THREADS, Cfg<MODE>::SMEM, st>>>(A, B, p);
-  MOE_CUDA_TRY(cudaGetLastError());
+  if (max_units <= 0) max_units = 1;
+  if (!C::PAIR) {
+    const int grid = max_units < sms ? max_units : sms;
+    mma_kernel<MODE><<<grid, C::THREADS, C::SMEM, st>>>(A, B, p);
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+  }
+  // persistent CTA pairs: as many 2-CTA clusters as fit at once
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_clusters[4] = {0, 0, 0, 0};
+  int& mc = max_clusters[MODE & 3];
+  if (mc == 0) {
+    cfg.gridDim = dim3(2 * (sms / 2));
+    int n = 0;
+    MOE_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, mma_kernel<MODE>, &cfg));
+    if (n <= 0) return MOE_ERR_UNSUPPORTED;
+    mc = n;
+  }
+  const int clusters = max_units < mc ? max_units : mc;
+  cfg.gridDim = dim3(2 * clusters);
+  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, mma_kernel<MODE>, A, B, p));
   return MOE_OK;
 }
 
@@ -1132,7 +1244,9 @@ extern "C" moe_status gmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_
   CUtensorMap A, B;
   if (!make_map(&A, lhs_q, K, M, K, BM)) return MOE_ERR_CUDA;
   const int bn = blockwise ? Cfg<kPromote>::BN : Cfg<kFinal>::BN;
-  if (!make_map(&B, rhs_q, K, static_cast<uint64_t>(E_local) * N, K, bn)) return MOE_ERR_CUDA;
+  // B box: one tile of N rows, or this CTA's half of it on a CTA pair
+  const uint32_t b_box = blockwise ? Cfg<kPromote>::BN : (Cfg<kFinal>::PAIR ? Cfg<kFinal>::BN / 2 : Cfg<kFinal>::BN);
+  if (!make_map(&B, rhs_q, K, static_cast<uint64_t>(E_local) * N, K, b_box)) return MOE_ERR_CUDA;
   Params p{};
   p.group_sizes = group_sizes;
   p.E = E;
@@ -1149,9 +1263,8 @@ extern "C" moe_status gmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_
   p.rhs_scale = rhs_scale;
   p.rhs_mode = rhs_mode;
   p.out = out;
-  const int64_t max_tiles64 = ((M + BM - 1) / BM + E_local) * p.ntiles;
-  const int max_tiles = static_cast<int>(max_tiles64 > (1 << 30) ? (1 << 30) : max_tiles64);
-  return blockwise ? launch_mma<kPromote>(A, B, p, max_tiles, st) : launch_mma<kFinal>(A, B, p, max_tiles, st);
+  return blockwise ? launch_mma<kPromote>(A, B, p, gmm_max_units<kPromote>(M, E_local, p.ntiles), st)
+                   : launch_mma<kFinal>(A, B, p, gmm_max_units<kFinal>(M, E_local, p.ntiles), st);
 }
 
 extern "C" moe_status gmm_fp8_swiglu(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode,
@@ -1212,9 +1325,7 @@ extern "C" moe_status gmm_fp8_swiglu(const uint8_t* lhs_q, const float* lhs_scal
   p.h_out = h;
   p.h_q = h_q;
   p.h_scale = h_scale;
-  const int64_t max_tiles64 = ((M + BM - 1) / BM + E_local) * p.ntiles;
-  moe_status stt = launch_mma<kSwiglu>(A, B, p, static_cast<int>(max_tiles64 > (1 << 30) ? (1 << 30) : max_tiles64),
-                                       st);
+  moe_status stt = launch_mma<kSwiglu>(A, B, p, gmm_max_units<kSwiglu>(M, E_local, p.ntiles), st);
   if (stt != MOE_OK) return stt;
   if (h_mode == MOE_SCALE_PER_ROW) {
     h_quant_rows_kernel<<<static_cast<unsigned>(M), 256, 0, st>>>(h, h_scale, F, h_q);
