@@ -42,6 +42,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="mixtral", choices=list(synth.CONFIGS))
     ap.add_argument("--tokens", type=int, default=0, help="override T (small cases for profiling)")
+    ap.add_argument("--experts", type=int, default=0, help="override E (small cases for profiling)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0, help="oracle sample size (0 = auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -329,7 +330,7 @@ def run_ours(args, cfg, rank, world, local):
                          % ((2 * cfg.F * cfg.D + cfg.D * cfg.F) * cfg.E / 1e9)},
         "roofline": {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": fp8_peak,
                      "unit": "TFLOP/s", "frac": achieved / fp8_peak,
-                     "traffic": recorded_traffic(kname, cfg) if args.tokens == 0 else None,
+                     "traffic": recorded_traffic(kname, cfg) if not (args.tokens or args.experts) else None,
                      "peak_note": f"of {pk_kind}: fp8 = 2 x sustained bf16 cuBLAS "
                                   f"({pk['bf16_tflops_sustained']} TFLOP/s)",
                      "flops_per_call": fl["gmm_in"], "ms_per_call": g_in,
@@ -553,6 +554,8 @@ def main():
     cfg = synth.CONFIGS[args.config]
     if args.tokens:
         cfg = synth.scaled(cfg, T=args.tokens)
+    if args.experts:
+        cfg = synth.scaled(cfg, E=args.experts)
     rank, world, local = dist_env()
     if args.impl == "reference":
         res = run_reference(args, cfg, rank, world)

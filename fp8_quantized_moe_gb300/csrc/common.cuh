@@ -53,6 +53,36 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // Round an fp32 value to the nearest bf16 and return it as fp32 (exact).
 __device__ __forceinline__ float round_bf16(float v) { return bf16lo(pack_bf16x2(v, 0.0f)); }
 
+// Packed fp32 pair arithmetic (two lanes of work per instruction).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // Two fp32 -> e4m3x2 (float8_e4m3fn), round to nearest even, saturating to
 // +-448; `lo` lands in the low byte.
 __device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
@@ -168,23 +198,78 @@ __device__ __forceinline__ bool swiglu_fast_range(float z) {
   return a <= 20.0f && (a >= 0x1p-60f || a == 0.0f);
 }
 
-// h[j] = bf16(silu(a0[j]) * a1[j]) for N elements.
+// h[j] = bf16(silu(a0[j]) * a1[j]) for N elements (N even), on pairs of
+// elements with packed fp32 arithmetic.  The fast path takes the steps of
+// exp_fast, div_checked and round_bf16 lane by lane, so its values are those
+// of the exact per-element path that takes over when a check fails.  rint(t)
+// is (t + 1.5 * 2^23) - 1.5 * 2^23 (exact round-to-nearest-even for
+// |t| < 2^22), whose bit pattern also gives 2^n; negations are exact sign
+// flips folded into products.  hb receives the h pairs as packed bf16 (the
+// storage format).
 template <int N>
-__device__ __forceinline__ void swiglu_h(const float* a0, const float* a1, float* h) {
+__device__ __forceinline__ void swiglu_h_x2(const float* a0, const float* a1, float* h, uint32_t* hb) {
   bool fast = true;
 #pragma unroll
   for (int j = 0; j < N; ++j) fast = fast && swiglu_fast_range(a0[j]);
   if (fast) {
     bool ok = true;
+    const uint64_t kMagic = f2_pack(12582912.0f, 12582912.0f);
+    const uint64_t kNegOne = f2_pack(-1.0f, -1.0f);
 #pragma unroll
-    for (int j = 0; j < N; ++j) {
-      const float d = __fadd_rn(1.0f, exp_fast(-a0[j]));
-      h[j] = round_bf16(__fmul_rn(div_checked(a0[j], d, ok), a1[j]));
+    for (int j = 0; j < N; j += 2) {
+      const uint64_t z = f2_pack(a0[j], a0[j + 1]);
+      const uint64_t x = f2_mul(z, kNegOne);  // -z
+      const uint64_t t = f2_mul(x, f2_pack(1.44269502162933349609375f, 1.44269502162933349609375f));
+      const uint64_t m = f2_add(t, kMagic);
+      const uint64_t n = f2_sub(m, kMagic);  // rint(t)
+      uint64_t r = f2_fma(n, f2_pack(-0.693145751953125f, -0.693145751953125f), x);
+      r = f2_fma(n, f2_pack(-1.428606765330187045e-6f, -1.428606765330187045e-6f), r);
+      uint64_t p = f2_pack(1.0f / 5040.0f, 1.0f / 5040.0f);
+      p = f2_fma(p, r, f2_pack(1.0f / 720.0f, 1.0f / 720.0f));
+      p = f2_fma(p, r, f2_pack(1.0f / 120.0f, 1.0f / 120.0f));
+      p = f2_fma(p, r, f2_pack(1.0f / 24.0f, 1.0f / 24.0f));
+      p = f2_fma(p, r, f2_pack(1.0f / 6.0f, 1.0f / 6.0f));
+      p = f2_fma(p, r, f2_pack(0.5f, 0.5f));
+      p = f2_fma(p, r, f2_pack(1.0f, 1.0f));
+      p = f2_fma(p, r, f2_pack(1.0f, 1.0f));
+      float m0, m1;
+      f2_unpack(m, m0, m1);
+      // bits(m) = 0x4B400000 + n, so (bits(m) << 23) + (127 << 23) = (n + 127) << 23 = 2^n
+      const float s0 = __uint_as_float((__float_as_uint(m0) << 23) + (127u << 23));
+      const float s1 = __uint_as_float((__float_as_uint(m1) << 23) + (127u << 23));
+      const uint64_t d = f2_add(f2_mul(p, f2_pack(s0, s1)), f2_pack(1.0f, 1.0f));  // 1 + e^-z
+      // silu = z / d (div_checked, lane by lane)
+      float d0, d1;
+      f2_unpack(d, d0, d1);
+      const uint64_t y = f2_pack(rcp_approx(d0), rcp_approx(d1));
+      const uint64_t q0 = f2_mul(z, y);
+      const uint64_t nd = f2_mul(d, kNegOne);
+      const uint64_t r0 = f2_fma(nd, q0, z);
+      const uint64_t q1 = f2_fma(r0, y, q0);
+      const uint64_t r1 = f2_fma(nd, q1, z);
+      float q10, q11, r10, r11;
+      f2_unpack(q1, q10, q11);
+      f2_unpack(r1, r10, r11);
+      const float sc0 = __uint_as_float((278u - ((__float_as_uint(q10) >> 23) & 0xFFu)) << 23);
+      const float sc1 = __uint_as_float((278u - ((__float_as_uint(q11) >> 23) & 0xFFu)) << 23);
+      ok = ok && (a0[j] == 0.0f || __fmul_rn(fabsf(r10), sc0) < d0);
+      ok = ok && (a0[j + 1] == 0.0f || __fmul_rn(fabsf(r11), sc1) < d1);
+      const float si0 = a0[j] == 0.0f ? a0[j] : q10, si1 = a0[j + 1] == 0.0f ? a0[j + 1] : q11;
+      float h0, h1;
+      f2_unpack(f2_mul(f2_pack(si0, si1), f2_pack(a1[j], a1[j + 1])), h0, h1);
+      const uint32_t pk = pack_bf16x2(h0, h1);
+      hb[j / 2] = pk;
+      h[j] = bf16lo(pk);
+      h[j + 1] = bf16hi(pk);
     }
     if (ok) return;
   }
 #pragma unroll
-  for (int j = 0; j < N; ++j) h[j] = round_bf16(__fmul_rn(silu_f32(a0[j]), a1[j]));
+  for (int j = 0; j < N; j += 2) {
+    h[j] = round_bf16(__fmul_rn(silu_f32(a0[j]), a1[j]));
+    h[j + 1] = round_bf16(__fmul_rn(silu_f32(a0[j + 1]), a1[j + 1]));
+    hb[j / 2] = pack_bf16x2(h[j], h[j + 1]);
+  }
 }
 
 // Fast e4m3 quotient.  y = x * inv_s with inv_s = 1/s rounded to nearest lies
@@ -269,6 +354,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+
+// Time limit of every bounded mbarrier wait.
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 // Bounded wait: true once the phase with `parity` has completed; false if
 // `abort_flag` becomes non-zero or `limit_ns` of wall time pass first.
@@ -458,24 +546,5 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-// Packed fp32 pair arithmetic (two lanes of work per instruction).
-__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 
 }  // namespace moe

@@ -83,7 +83,8 @@ struct SwigluOp {  // h = bf16(silu(a0) * a1), a = [a0 | a1] of width 2F
     const uint16_t* r = a + row * 2 * F + 8 * static_cast<int64_t>(u);
     unpack8(ldg16(r), a0);
     unpack8(ldg16(r + F), a1);
-    swiglu_h<8>(a0, a1, v[0]);
+    uint32_t hb[4];
+    swiglu_h_x2<8>(a0, a1, v[0], hb);
   }
   __device__ __forceinline__ int64_t col(int u, int) const { return 8 * static_cast<int64_t>(u); }
 };

@@ -45,6 +45,10 @@ def make_case(seed, M, K, N, E, amode, wmode, zero_frac=0.25):
     (256, 256, 128, 2, RB, R0),
     (1500, 1024, 768, 16, R0, R0),
     (2048, 2048, 1536, 128, R0, RB),  # prefill-chunk shaped, E = 128
+    # K >= 3072 runs on CTA pairs: odd M-tile counts leave the odd CTA past its group
+    (700, 4096, 512, 5, R0, R0),
+    (129, 3072, 272, 2, RT, R0),     # one pair per group, N tail inside the pair's B halves
+    (1, 4096, 256, 1, R0, R0),
 ])
 def test_gmm_matches_oracle(M, K, N, E, amode, wmode):
     sizes, a, w, sa, sw = make_case(M * 31 + K + N + E, M, K, N, E, amode, wmode)
@@ -66,6 +70,17 @@ def test_gmm_expert_parallel_shard_zeroes_other_rows():
     lo, hi = starts[g0], starts[g0 + El]
     assert np.all(o[:lo] == 0) and np.all(o[hi:] == 0)
     assert_close(o, ref, "gmm shard")
+
+
+def test_gmm_pair_expert_parallel_shard():
+    M, K, N, E = 900, 4096, 256, 6
+    sizes, a, w, sa, sw = make_case(6, M, K, N, E, R0, R0, zero_frac=0.2)
+    g0, El = 1, 4
+    ref = oracle.gmm(a, sa, R0, w[g0:g0 + El], sw[g0:g0 + El], R0, sizes, group_offset=g0, E_local=El)
+    out = moe.gmm(dev(a), dev(sa), R0, dev(w[g0:g0 + El].copy()), dev(sw[g0:g0 + El].copy()), R0, dev(sizes),
+                  group_offset=g0, E_local=El)
+    assert moe.device_error() == 0
+    assert_close(host(out), ref, "gmm pair shard")
 
 
 def test_gmm_bad_group_sizes_sets_device_error():
@@ -119,6 +134,10 @@ def test_tgmm_matches_oracle(M, K, N, E, lmode, rmode):
     (1, 128, 128, 1, R0, R0, R0, None),
     (1000, 512, 384, 9, R0, R0, R0, (2, 4)),
     (1000, 512, 384, 9, R0, RT, RB, (3, 5)),
+    # K >= 3072: CTA pairs
+    (700, 4096, 256, 5, R0, R0, R0, None),
+    (700, 4096, 256, 5, RT, RT, RT, (1, 3)),
+    (450, 3072, 384, 3, R0, R0, RB, None),
 ])
 def test_gmm_swiglu_equals_gmm_then_swiglu(M, K, F, E, amode, wmode, hmode, shard):
     sizes, a, w, sa, sw = make_case(M + K + F + E + hmode, M, K, 2 * F, E, amode, wmode, zero_frac=0.2)
