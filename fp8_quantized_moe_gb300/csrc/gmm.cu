@@ -1073,13 +1073,15 @@ __global__ void swiglu_outside_kernel(uint8_t* h_q, float* h_scale, int64_t M, i
 
 // Second phase of the per-token h scales: the codes of one row against its
 // finished amax (one CTA per row, V 16-byte loads in flight per thread, all
-// issued before any is used, and before the row's scale is read).
+// issued before any is used, and before the row's amax is read), and the
+// row's final scale amax / 448 written over the amax (1 for a row outside the
+// local groups, whose amax slot holds a negative mark).
 template <int V>
-__global__ void __launch_bounds__(256) h_quant_rows_kernel(const uint16_t* h, const float* amax, int nvec,
-                                                           uint8_t* q) {
+__global__ void __launch_bounds__(256) h_quant_rows_kernel(const uint16_t* h, float* h_scale, int nvec, uint8_t* q) {
   const int64_t row = blockIdx.x;
   const uint4* hr = reinterpret_cast<const uint4*>(h) + row * nvec;
   uint2* qr = reinterpret_cast<uint2*>(q) + row * nvec;
+  float m = 0.0f, s = 1.0f, inv = 1.0f;
   for (int base = 0; base < nvec; base += V * blockDim.x) {
     uint4 d[V];
 #pragma unroll
@@ -1087,9 +1089,14 @@ __global__ void __launch_bounds__(256) h_quant_rows_kernel(const uint16_t* h, co
       const int v = base + i * blockDim.x + threadIdx.x;
       if (v < nvec) d[i] = __ldg(hr + v);
     }
-    const float m = __ldg(amax + row);
+    if (base == 0) {
+      m = h_scale[row];
+      s = absmax_scale(m);  // 1 for a negative mark
+      inv = __frcp_rn(s);
+      __syncthreads();  // every thread has read the amax before it is replaced
+      if (threadIdx.x == 0) h_scale[row] = s;
+    }
     if (m < 0.0f) return;  // outside the local groups
-    const float s = absmax_scale(m), inv = __frcp_rn(s);
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const int v = base + i * blockDim.x + threadIdx.x;
@@ -1108,10 +1115,6 @@ __global__ void __launch_bounds__(256) h_quant_rows_kernel(const uint16_t* h, co
   }
 }
 
-__global__ void h_scale_finalize_kernel(float* h_scale, int64_t M) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i < M) h_scale[i] = absmax_scale(h_scale[i]);  // a negative mark or 0 gives 1
-}
 
 // ---- host side -----------------------------------------------------------
 
@@ -1348,8 +1351,6 @@ extern "C" moe_status gmm_fp8_swiglu(const uint8_t* lhs_q, const float* lhs_scal
     const int nvec = static_cast<int>(F / 8);
     const int threads = std::min(256, ((nvec + 8 * 32 - 1) / (8 * 32)) * 32);
     h_quant_rows_kernel<8><<<static_cast<unsigned>(M), threads, 0, st>>>(h, h_scale, nvec, h_q);
-    MOE_CUDA_TRY(cudaGetLastError());
-    h_scale_finalize_kernel<<<static_cast<unsigned>((M + 255) / 256), 256, 0, st>>>(h_scale, M);
     MOE_CUDA_TRY(cudaGetLastError());
   }
   return MOE_OK;
