@@ -391,10 +391,13 @@ def cpu_baseline(args, cfg, x_host, ids_np, w_np, w_in, w_out, static):
     wq = oracle_setup(cfg, xb, ids_np, w_np, host_bits(w_in), host_bits(w_out), static)
     n = args.cpu_sample_tokens or 8
     dt = oracle_time(cfg, xb, ids_np, w_np, wq, static, n)
-    # grow the sample towards ~10 s of CPU work
-    if not args.cpu_sample_tokens and dt < 2.0:
-        n = int(min(cfg.T, max(n, n * 10.0 / max(dt, 1e-3))))
-        dt = oracle_time(cfg, xb, ids_np, w_np, wq, static, n, seed=1)
+    # grow the sample towards ~15 s of CPU work (the whole-batch sort and
+    # quantisation make small samples look slower per token, so re-aim once)
+    for seed, target in ((1, 10.0), (2, 15.0)):
+        if args.cpu_sample_tokens or dt >= 0.6 * target or n >= cfg.T:
+            break
+        n = int(min(cfg.T, max(n + 1, n * target / max(dt, 1e-3))))
+        dt = oracle_time(cfg, xb, ids_np, w_np, wq, static, n, seed=seed)
     return {"value": n / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{n} of {cfg.T} tokens through the oracle forward (fp64, OpenMP); weights quantised "
                       f"beforehand", "seconds": dt}

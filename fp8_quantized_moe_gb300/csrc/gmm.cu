@@ -117,6 +117,9 @@ static_assert(sizeof(SmemCtl) % 16 == 0, "SmemCtl size");
 #ifndef MOE_PROMOTE_EPI_WARPS
 #define MOE_PROMOTE_EPI_WARPS 8
 #endif
+#ifndef MOE_TGMM_EPI_WARPS
+#define MOE_TGMM_EPI_WARPS 8
+#endif
 #ifndef MOE_GMM_PAIR
 #define MOE_GMM_PAIR 1
 #endif
@@ -135,14 +138,17 @@ struct Cfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TX_BYTES = (PAIR ? 2 : 1) * STAGE_BYTES;  // what one full barrier waits for
   static constexpr uint32_t IDESC = idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN);
-  static constexpr int EPI_WARPS = MODE == kPromote ? MOE_PROMOTE_EPI_WARPS : (MODE == kSwiglu ? 8 : 4);
+  static constexpr int EPI_WARPS =
+      MODE == kPromote ? MOE_PROMOTE_EPI_WARPS : (MODE == kSwiglu ? 8 : (MODE == kTgmm ? MOE_TGMM_EPI_WARPS : 4));
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  // per-warp staging of 32x32 output blocks for row-contiguous stores:
-  // bf16 rows padded to 80 bytes (kFinal), fp32 rows padded to 144 bytes (kTgmm)
-  static constexpr int STG_PITCH = MODE == kFinal ? 80 : (MODE == kTgmm ? 144 : 0);
-  static constexpr size_t CTL_BYTES = (sizeof(SmemCtl) + 127) / 128 * 128;
+  // per-warp staging of 32x32 output blocks: kFinal, bf16 rows padded to 80
+  // bytes for row-contiguous stores; kTgmm, two 4 KB fp32 blocks in the
+  // 128-byte-swizzled layout of a TMA store box
+  static constexpr int STG_PITCH = MODE == kFinal ? 80 : 0;
+  static constexpr int STG_WARP_BYTES = MODE == kFinal ? 32 * STG_PITCH : (MODE == kTgmm ? 2 * 4096 : 0);
+  static constexpr size_t CTL_BYTES = (sizeof(SmemCtl) + 1023) / 1024 * 1024;  // keeps the staging 1 KB aligned
   static constexpr size_t SMEM = 1024 + static_cast<size_t>(NSTAGE) * STAGE_BYTES + CTL_BYTES +
-                                 static_cast<size_t>(EPI_WARPS) * 32 * STG_PITCH;
+                                 static_cast<size_t>(EPI_WARPS) * STG_WARP_BYTES;
   static_assert(NSTAGE <= kMaxStages && NACC >= 1 && NACC <= kMaxAcc && NACC * BN == TMEM_COLS,
                 "tile configuration");
   static_assert(SMEM <= 232448, "shared memory per CTA");
@@ -310,7 +316,8 @@ __device__ __forceinline__ void load_col_scales32(const float* base, int nb, int
 
 template <int MODE, bool PAIR_REQ>
 __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
-    mma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+    mma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmO, const Params p) {
   using C = Cfg<MODE, PAIR_REQ>;
   constexpr int EPI_WARPS = C::EPI_WARPS, BN = C::BN, NSTAGE = C::NSTAGE, NACC = C::NACC;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
@@ -509,10 +516,11 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q4 = warp & 3;                            // TMEM lane quarter of this warp
-    const int half = (MODE == kPromote || MODE == kSwiglu) ? (warp - 2) >> 2 : 0;  // column part of the warp
+    const int half = (warp - 2) >> 2;  // column part of the warp (0 with 4 epilogue warps)
     const int r = q4 * 32 + lane;                       // row of the tile = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
     uint32_t acc = 0;
+    int stg_sel = 0;  // kTgmm: staging buffer of this warp's next block
     for (int t = unit0; t < total && !timed_out; t += units) {
       const Tile tl = get_tile<MODE, PAIR>(p, ctl, t, rank);
       const bool row_ok = r < tl.rows;
@@ -520,9 +528,10 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         float* out = static_cast<float*>(p.out);
         const int64_t krow = tl.row0 + r;
         float* orow = out + (static_cast<int64_t>(tl.el) * p.K + krow) * p.N;
+        constexpr int WCOLS = BN / (EPI_WARPS / 4);  // columns of the tile this warp writes
         if (tl.nkb == 0) {
           if (row_ok) {
-            for (int c = 0; c < BN; c += 4)
+            for (int c = half * WCOLS; c < (half + 1) * WCOLS; c += 4)
               if (tl.n0 + c < p.N) *reinterpret_cast<float4*>(orow + tl.n0 + c) = make_float4(0.f, 0.f, 0.f, 0.f);
           }
           continue;
@@ -537,17 +546,20 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         const bool per_col = p.rhs_mode == MOE_SCALE_PER_GROUP_COL;
         const float* sgb = p.rhs_scale + (per_col ? static_cast<int64_t>(tl.el) * p.N : 0);
         const float sg_t = per_col ? 0.f : __ldg(p.rhs_scale);
+        const bool block_rows = tl.rows - q4 * 32 > 0;  // rows >= K are clipped by the store
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = half * (WCOLS / 32); c < (half + 1) * (WCOLS / 32); ++c) {
           const int nb = tl.n0 + c * 32;
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + c * 32, v);
           float sg[32];
           load_col_scales32(sgb, nb, p.N, per_col, sg_t, sg);
           tmem_wait_ld();
-          // stage this warp's 32x32 block, then write 4 rows (128 contiguous bytes each) per instruction
-          float* stg = reinterpret_cast<float*>(stg_base + (warp - 2) * 32 * C::STG_PITCH);
-          constexpr int PF = C::STG_PITCH / 4;  // pitch in floats
+          // this warp's 32x32 block, staged in the swizzled box layout and
+          // written by one TMA store; two staging buffers alternate
+          uint8_t* buf = stg_base + (warp - 2) * C::STG_WARP_BYTES + stg_sel * 4096;
+          if (lane == 0) bulk_wait_read<1>();  // the store issued from `buf` two blocks ago has read it
+          __syncwarp();
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
             float4 o;
@@ -555,19 +567,15 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
             o.y = __uint_as_float(v[g * 4 + 1]) * sx * sg[g * 4 + 1];
             o.z = __uint_as_float(v[g * 4 + 2]) * sx * sg[g * 4 + 2];
             o.w = __uint_as_float(v[g * 4 + 3]) * sx * sg[g * 4 + 3];
-            *reinterpret_cast<float4*>(stg + lane * PF + 4 * g) = o;
+            *reinterpret_cast<float4*>(buf + lane * 128 + ((g ^ (lane & 7)) << 4)) = o;
           }
+          fence_proxy_async_smem();
           __syncwarp();
-          const int cseg = (lane & 7) * 4;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rr = i * 4 + (lane >> 3);  // row of this warp's block
-            const int64_t k = tl.row0 + q4 * 32 + rr;
-            if (rr < tl.rows - q4 * 32 && nb + cseg < p.N)
-              *reinterpret_cast<float4*>(out + (static_cast<int64_t>(tl.el) * p.K + k) * p.N + nb + cseg) =
-                  *reinterpret_cast<const float4*>(stg + rr * PF + cseg);
+          if (lane == 0 && block_rows && nb < p.N) {
+            tma_store_3d(&tmO, smem_u32(buf), nb, tl.row0 + q4 * 32, tl.el);
+            bulk_commit();
           }
-          __syncwarp();
+          stg_sel ^= 1;
         }
         tc_fence_before();
         __syncwarp();
@@ -726,7 +734,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
           load_col_scales32(swb, nb, p.N, per_chan, sw_t, sw);
           tmem_wait_ld();
           // stage this warp's 32x32 bf16 block, then write 8 rows (64 contiguous bytes each) per instruction
-          uint8_t* stg = stg_base + (warp - 2) * 32 * C::STG_PITCH;
+          uint8_t* stg = stg_base + (warp - 2) * C::STG_WARP_BYTES;
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             uint4 q;
@@ -920,6 +928,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
       *abort_flag = 1;
       ctl->err = 2;
     }
+    if (MODE == kTgmm && lane == 0) bulk_wait_all();  // the output stores have landed
   }
 
   tc_fence_before();
@@ -976,13 +985,19 @@ __global__ void zero_outside_kernel(uint16_t* out, int64_t M, int64_t N, const i
 
 // src [M, C] e4m3 -> dst [C, Mp]: local group el's rows land at columns
 // [pst(el), pst(el) + size), zero-filled up to the next multiple of 128.
-// 64 x 64 byte tiles through shared memory.
+// Persistent CTAs build the group tables once and walk 64-row x 256-byte
+// tiles (column tiles fastest).  A tile comes in with four 16-byte loads per
+// thread (the next tile's loads are issued before the current one is written
+// out) and is staged in shared memory; each thread then reads a 16-row x
+// 4-byte column strip as sixteen words, transposes its 4 x 4 byte blocks with
+// byte permutes, and writes four 16-byte runs of output rows.
+constexpr int kTpRows = 64, kTpCols = 256, kTpPitch = kTpCols + 16;
 __global__ void __launch_bounds__(256) transpose_pad_kernel(const uint8_t* src, int64_t M, int64_t C, uint8_t* dst,
                                                             int64_t Mp, const int32_t* sizes, int E, int g0,
                                                             int El) {
   __shared__ int starts[kMaxGroups + 1];
   __shared__ int pst[kMaxGroups + 1];
-  __shared__ __align__(16) uint8_t tile[64][80];
+  __shared__ __align__(16) uint8_t tile[2][kTpRows][kTpPitch];
   group_starts_smem(sizes, E, starts);
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
@@ -1003,43 +1018,67 @@ __global__ void __launch_bounds__(256) transpose_pad_kernel(const uint8_t* src, 
     if (lane == 0) pst[El] = carry;
   }
   __syncthreads();
-  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * 64;
-  const int64_t c0 = static_cast<int64_t>(blockIdx.y) * 64;
-  if (j0 >= pst[El] || j0 >= Mp) return;
-  {
-    const int jj = threadIdx.x >> 2, part = threadIdx.x & 3;
-    const int64_t j = j0 + jj;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (j < pst[El]) {
-      int lo = 0, hi = El;
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (pst[mid] <= j) lo = mid; else hi = mid;
-      }
-      while (lo + 1 < El && pst[lo + 1] <= j) ++lo;
-      const int64_t off = j - pst[lo];
-      const int64_t sz = starts[g0 + lo + 1] - starts[g0 + lo];
-      const int64_t c = c0 + part * 16;
-      if (off < sz && c < C) {
-        const int64_t m = starts[g0 + lo] + off;
-        if (m < M) v = __ldg(reinterpret_cast<const uint4*>(src + m * C + c));
+  const int64_t rows_out = min(static_cast<int64_t>(pst[El]), Mp);  // padded columns of dst to fill
+  const int64_t ntc = (C + kTpCols - 1) / kTpCols;
+  const int64_t ntiles = ((rows_out + kTpRows - 1) / kTpRows) * ntc;
+  const int tid = threadIdx.x;
+  // thread tid loads 16-byte unit (row (tid >> 4) + 16 i, column 16 (tid & 15)) of a tile
+  auto load = [&](int64_t t, uint4 (&v)[4]) {
+    const int64_t jb = (t / ntc) * kTpRows, cb = (t % ntc) * kTpCols;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t j = jb + (tid >> 4) + 16 * i;
+      const int64_t c = cb + 16 * (tid & 15);
+      v[i] = make_uint4(0, 0, 0, 0);
+      if (j < rows_out && c < C) {
+        int lo = 0, hi = El;
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (pst[mid] <= j) lo = mid; else hi = mid;
+        }
+        while (lo + 1 < El && pst[lo + 1] <= j) ++lo;
+        const int64_t off = j - pst[lo];
+        const int64_t sz = starts[g0 + lo + 1] - starts[g0 + lo];
+        if (off < sz) {
+          const int64_t m = starts[g0 + lo] + off;
+          if (m < M) v[i] = __ldg(reinterpret_cast<const uint4*>(src + m * C + c));
+        }
       }
     }
-    *reinterpret_cast<uint4*>(&tile[jj][part * 16]) = v;
-  }
-  __syncthreads();
-  {
-    const int cc = threadIdx.x >> 2, part = threadIdx.x & 3;
-    const int64_t c = c0 + cc;
-    if (c < C) {
-      uint32_t w[4];
+  };
+  int64_t t = blockIdx.x;
+  uint4 nxt[4];
+  if (t < ntiles) load(t, nxt);
+  const int cw = tid & 63, rg = tid >> 6;  // output: columns 4 cw .. 4 cw + 3, source rows 16 rg .. 16 rg + 15
+  for (int b = 0; t < ntiles; t += gridDim.x, b ^= 1) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int jb = part * 16 + q * 4;
-        w[q] = static_cast<uint32_t>(tile[jb][cc]) | (static_cast<uint32_t>(tile[jb + 1][cc]) << 8) |
-               (static_cast<uint32_t>(tile[jb + 2][cc]) << 16) | (static_cast<uint32_t>(tile[jb + 3][cc]) << 24);
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<uint4*>(&tile[b][(tid >> 4) + 16 * i][16 * (tid & 15)]) = nxt[i];
+    if (t + gridDim.x < ntiles) load(t + gridDim.x, nxt);
+    __syncthreads();  // the two buffers alternate, so one barrier per tile suffices
+    const int64_t jb = (t / ntc) * kTpRows, cb = (t % ntc) * kTpCols;
+    uint32_t o[4][4];  // o[k][q]: column 4 cw + k, source rows 16 rg + 4 q .. + 3
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = 16 * rg + 4 * q;
+      const uint32_t r0 = *reinterpret_cast<const uint32_t*>(&tile[b][r][4 * cw]);
+      const uint32_t r1 = *reinterpret_cast<const uint32_t*>(&tile[b][r + 1][4 * cw]);
+      const uint32_t r2 = *reinterpret_cast<const uint32_t*>(&tile[b][r + 2][4 * cw]);
+      const uint32_t r3 = *reinterpret_cast<const uint32_t*>(&tile[b][r + 3][4 * cw]);
+      const uint32_t t0 = __byte_perm(r0, r1, 0x5140), t1 = __byte_perm(r2, r3, 0x5140);
+      const uint32_t t2 = __byte_perm(r0, r1, 0x7362), t3 = __byte_perm(r2, r3, 0x7362);
+      o[0][q] = __byte_perm(t0, t1, 0x5410);
+      o[1][q] = __byte_perm(t0, t1, 0x7632);
+      o[2][q] = __byte_perm(t2, t3, 0x5410);
+      o[3][q] = __byte_perm(t2, t3, 0x7632);
+    }
+    if (jb + 16 * rg < rows_out) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int64_t c = cb + 4 * cw + k;
+        if (c < C)
+          *reinterpret_cast<uint4*>(dst + c * Mp + jb + 16 * rg) = make_uint4(o[k][0], o[k][1], o[k][2], o[k][3]);
       }
-      *reinterpret_cast<uint4*>(dst + c * Mp + j0 + part * 16) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
 }
@@ -1048,8 +1087,8 @@ __global__ void __launch_bounds__(256) transpose_pad_kernel(const uint8_t* src, 
 
 // Rows outside groups [g0, g0 + El) of a fused SwiGLU call get zero codes and
 // scale 1, as the unfused path gives for its zero rows.  In the per-row mode
-// their running maximum is set to -1 so that the quantise pass skips them and
-// the scale pass turns them into 1.
+// their running maximum is set to -1 so that the code pass skips them and
+// writes scale 1.
 __global__ void swiglu_outside_kernel(uint8_t* h_q, float* h_scale, int64_t M, int64_t F, int h_mode,
                                       const int32_t* sizes, int E, int g0, int El) {
   __shared__ int starts[kMaxGroups + 1];
@@ -1146,6 +1185,20 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, ui
   return r == CUDA_SUCCESS;
 }
 
+// 3-D fp32 tensor map of the tgmm output [E_local, K, N] for 32 x 32 stores
+// with the 128-byte swizzle (rows >= K or columns >= N are clipped).
+bool make_map_out_f32(CUtensorMap* m, void* ptr, uint64_t N, uint64_t K, uint64_t El) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {N, K, El};
+  cuuint64_t strides[2] = {N * 4, K * N * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -1171,8 +1224,8 @@ int gmm_max_units(int64_t M, int E_local, int ntiles) {
 }
 
 template <int MODE, bool PAIR_REQ>
-moe_status launch_mma(const CUtensorMap& A, const CUtensorMap& B, const Params& p, int max_units,
-                      cudaStream_t st) {
+moe_status launch_mma(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& O, const Params& p,
+                      int max_units, cudaStream_t st) {
   using C = Cfg<MODE, PAIR_REQ>;
   auto kernel = mma_kernel<MODE, PAIR_REQ>;
   MOE_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1182,7 +1235,7 @@ moe_status launch_mma(const CUtensorMap& A, const CUtensorMap& B, const Params& 
   if (max_units <= 0) max_units = 1;
   if (!C::PAIR) {
     const int grid = max_units < sms ? max_units : sms;
-    kernel<<<grid, C::THREADS, C::SMEM, st>>>(A, B, p);
+    kernel<<<grid, C::THREADS, C::SMEM, st>>>(A, B, O, p);
     MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;
   }
@@ -1209,7 +1262,7 @@ moe_status launch_mma(const CUtensorMap& A, const CUtensorMap& B, const Params& 
   }
   const int clusters = max_units < mc ? max_units : mc;
   cfg.gridDim = dim3(2 * clusters);
-  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, kernel, A, B, p));
+  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, kernel, A, B, O, p));
   return MOE_OK;
 }
 
@@ -1280,9 +1333,9 @@ extern "C" moe_status gmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_
   p.rhs_scale = rhs_scale;
   p.rhs_mode = rhs_mode;
   p.out = out;
-  if (blockwise) return launch_mma<kPromote, false>(A, B, p, gmm_max_units<kPromote, false>(M, E_local, p.ntiles), st);
-  if (pair) return launch_mma<kFinal, true>(A, B, p, gmm_max_units<kFinal, true>(M, E_local, p.ntiles), st);
-  return launch_mma<kFinal, false>(A, B, p, gmm_max_units<kFinal, false>(M, E_local, p.ntiles), st);
+  if (blockwise) return launch_mma<kPromote, false>(A, B, A, p, gmm_max_units<kPromote, false>(M, E_local, p.ntiles), st);
+  if (pair) return launch_mma<kFinal, true>(A, B, A, p, gmm_max_units<kFinal, true>(M, E_local, p.ntiles), st);
+  return launch_mma<kFinal, false>(A, B, A, p, gmm_max_units<kFinal, false>(M, E_local, p.ntiles), st);
 }
 
 extern "C" moe_status gmm_fp8_swiglu(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode,
@@ -1344,8 +1397,8 @@ extern "C" moe_status gmm_fp8_swiglu(const uint8_t* lhs_q, const float* lhs_scal
   p.h_q = h_q;
   p.h_scale = h_scale;
   moe_status stt = K >= kPairMinK
-                       ? launch_mma<kSwiglu, true>(A, B, p, gmm_max_units<kSwiglu, true>(M, E_local, p.ntiles), st)
-                       : launch_mma<kSwiglu, false>(A, B, p, gmm_max_units<kSwiglu, false>(M, E_local, p.ntiles), st);
+                       ? launch_mma<kSwiglu, true>(A, B, A, p, gmm_max_units<kSwiglu, true>(M, E_local, p.ntiles), st)
+                       : launch_mma<kSwiglu, false>(A, B, A, p, gmm_max_units<kSwiglu, false>(M, E_local, p.ntiles), st);
   if (stt != MOE_OK) return stt;
   if (h_mode == MOE_SCALE_PER_ROW) {
     const int nvec = static_cast<int>(F / 8);
@@ -1391,11 +1444,10 @@ extern "C" moe_status tgmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe
   uint8_t* lhsT = static_cast<uint8_t*>(workspace);
   uint8_t* rhsT = lhsT + align256(static_cast<size_t>(K * Mp));
   if (M > 0) {
-    dim3 gk(static_cast<unsigned>(Mp / 64), static_cast<unsigned>((K + 63) / 64));
-    transpose_pad_kernel<<<gk, 256, 0, st>>>(lhs_q, M, K, lhsT, Mp, group_sizes, E, group_offset, E_local);
+    const int grid = sm_count() * 8;
+    transpose_pad_kernel<<<grid, 256, 0, st>>>(lhs_q, M, K, lhsT, Mp, group_sizes, E, group_offset, E_local);
     MOE_CUDA_TRY(cudaGetLastError());
-    dim3 gn(static_cast<unsigned>(Mp / 64), static_cast<unsigned>((N + 63) / 64));
-    transpose_pad_kernel<<<gn, 256, 0, st>>>(rhs_q, M, N, rhsT, Mp, group_sizes, E, group_offset, E_local);
+    transpose_pad_kernel<<<grid, 256, 0, st>>>(rhs_q, M, N, rhsT, Mp, group_sizes, E, group_offset, E_local);
     MOE_CUDA_TRY(cudaGetLastError());
   }
   CUtensorMap A, B;
@@ -1419,5 +1471,7 @@ extern "C" moe_status tgmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe
   p.rhs_mode = rhs_mode;
   p.out = out;
   const int64_t tiles = static_cast<int64_t>(E_local) * p.ktiles * p.ntiles;
-  return launch_mma<kTgmm, false>(A, B, p, static_cast<int>(tiles > (1 << 30) ? (1 << 30) : tiles), st);
+  CUtensorMap O;
+  if (!make_map_out_f32(&O, out, N, K, E_local)) return MOE_ERR_CUDA;
+  return launch_mma<kTgmm, false>(A, B, O, p, static_cast<int>(tiles > (1 << 30) ? (1 << 30) : tiles), st);
 }
