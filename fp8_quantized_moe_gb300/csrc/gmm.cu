@@ -120,6 +120,12 @@ static_assert(sizeof(SmemCtl) % 16 == 0, "SmemCtl size");
 #ifndef MOE_TGMM_EPI_WARPS
 #define MOE_TGMM_EPI_WARPS 8
 #endif
+#ifndef MOE_TGMM_NSTAGE
+#define MOE_TGMM_NSTAGE 3
+#endif
+#ifndef MOE_TGMM_STG_BUFS
+#define MOE_TGMM_STG_BUFS 2
+#endif
 #ifndef MOE_GMM_PAIR
 #define MOE_GMM_PAIR 1
 #endif
@@ -133,7 +139,7 @@ struct Cfg {
   static constexpr int BN = PROMOTE ? MOE_PROMOTE_BN : 256;  // output columns per tile
   static constexpr int TMEM_COLS = PAIR ? MOE_PAIR_TMEM_COLS : 512;
   static constexpr int NACC = TMEM_COLS / BN;                // accumulators of BN columns
-  static constexpr int NSTAGE = PAIR ? 6 : (BN == 128 ? 6 : (BN == 64 ? 8 : (MODE == kTgmm ? 3 : MOE_GMM_NSTAGE)));
+  static constexpr int NSTAGE = PAIR ? 6 : (BN == 128 ? 6 : (BN == 64 ? 8 : (MODE == kTgmm ? MOE_TGMM_NSTAGE : MOE_GMM_NSTAGE)));
   static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK;  // this CTA's part of the B tile
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TX_BYTES = (PAIR ? 2 : 1) * STAGE_BYTES;  // what one full barrier waits for
@@ -145,7 +151,8 @@ struct Cfg {
   // bytes for row-contiguous stores; kTgmm, two 4 KB fp32 blocks in the
   // 128-byte-swizzled layout of a TMA store box
   static constexpr int STG_PITCH = MODE == kFinal ? 80 : 0;
-  static constexpr int STG_WARP_BYTES = MODE == kFinal ? 32 * STG_PITCH : (MODE == kTgmm ? 2 * 4096 : 0);
+  static constexpr int STG_BUFS = MODE == kTgmm ? MOE_TGMM_STG_BUFS : 1;
+  static constexpr int STG_WARP_BYTES = MODE == kFinal ? 32 * STG_PITCH : (MODE == kTgmm ? STG_BUFS * 4096 : 0);
   static constexpr size_t CTL_BYTES = (sizeof(SmemCtl) + 1023) / 1024 * 1024;  // keeps the staging 1 KB aligned
   static constexpr size_t SMEM = 1024 + static_cast<size_t>(NSTAGE) * STAGE_BYTES + CTL_BYTES +
                                  static_cast<size_t>(EPI_WARPS) * STG_WARP_BYTES;
@@ -556,9 +563,9 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
           load_col_scales32(sgb, nb, p.N, per_col, sg_t, sg);
           tmem_wait_ld();
           // this warp's 32x32 block, staged in the swizzled box layout and
-          // written by one TMA store; two staging buffers alternate
+          // written by one TMA store; the staging buffers rotate
           uint8_t* buf = stg_base + (warp - 2) * C::STG_WARP_BYTES + stg_sel * 4096;
-          if (lane == 0) bulk_wait_read<1>();  // the store issued from `buf` two blocks ago has read it
+          if (lane == 0) bulk_wait_read<C::STG_BUFS - 1>();  // the store last issued from `buf` has read it
           __syncwarp();
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
@@ -575,7 +582,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
             tma_store_3d(&tmO, smem_u32(buf), nb, tl.row0 + q4 * 32, tl.el);
             bulk_commit();
           }
-          stg_sel ^= 1;
+          stg_sel = stg_sel + 1 == C::STG_BUFS ? 0 : stg_sel + 1;
         }
         tc_fence_before();
         __syncwarp();
@@ -985,19 +992,22 @@ __global__ void zero_outside_kernel(uint16_t* out, int64_t M, int64_t N, const i
 
 // src [M, C] e4m3 -> dst [C, Mp]: local group el's rows land at columns
 // [pst(el), pst(el) + size), zero-filled up to the next multiple of 128.
-// Persistent CTAs build the group tables once and walk 64-row x 256-byte
-// tiles (column tiles fastest).  A tile comes in with four 16-byte loads per
-// thread (the next tile's loads are issued before the current one is written
-// out) and is staged in shared memory; each thread then reads a 16-row x
-// 4-byte column strip as sixteen words, transposes its 4 x 4 byte blocks with
-// byte permutes, and writes four 16-byte runs of output rows.
-constexpr int kTpRows = 64, kTpCols = 256, kTpPitch = kTpCols + 16;
+// Persistent CTAs build the group tables once and walk 128 x 128 byte tiles
+// (column tiles fastest).  A tile comes in with four 16-byte loads per thread
+// (each source row segment read whole by eight lanes; the next tile's loads
+// are issued before the current one is written out) and is staged in shared
+// memory with its 16-byte units XOR-swizzled by 16-row group, so that both
+// the stores and the transposing reads are free of bank conflicts.  Each
+// thread then reads a 16-row x 4-byte strip as sixteen words, transposes its
+// 4 x 4 byte blocks with byte permutes, and writes four 16-byte pieces; eight
+// consecutive lanes cover one 128-byte run of an output row.
+constexpr int kTpTile = 128;
 __global__ void __launch_bounds__(256) transpose_pad_kernel(const uint8_t* src, int64_t M, int64_t C, uint8_t* dst,
                                                             int64_t Mp, const int32_t* sizes, int E, int g0,
                                                             int El) {
   __shared__ int starts[kMaxGroups + 1];
   __shared__ int pst[kMaxGroups + 1];
-  __shared__ __align__(16) uint8_t tile[2][kTpRows][kTpPitch];
+  __shared__ __align__(16) uint32_t tile[2][kTpTile][kTpTile / 4];
   group_starts_smem(sizes, E, starts);
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
@@ -1018,19 +1028,19 @@ __global__ void __launch_bounds__(256) transpose_pad_kernel(const uint8_t* src, 
     if (lane == 0) pst[El] = carry;
   }
   __syncthreads();
-  const int64_t rows_out = min(static_cast<int64_t>(pst[El]), Mp);  // padded columns of dst to fill
-  const int64_t ntc = (C + kTpCols - 1) / kTpCols;
-  const int64_t ntiles = ((rows_out + kTpRows - 1) / kTpRows) * ntc;
+  const int64_t rows_out = min(static_cast<int64_t>(pst[El]), Mp);  // padded columns of dst (a multiple of 128)
+  const int64_t ntc = (C + kTpTile - 1) / kTpTile;
+  const int64_t ntiles = (rows_out / kTpTile) * ntc;
   const int tid = threadIdx.x;
-  // thread tid loads 16-byte unit (row (tid >> 4) + 16 i, column 16 (tid & 15)) of a tile
+  const int lrow = tid >> 3, unit = tid & 7;  // load: rows lrow + 32 i, 16-byte unit `unit`
   auto load = [&](int64_t t, uint4 (&v)[4]) {
-    const int64_t jb = (t / ntc) * kTpRows, cb = (t % ntc) * kTpCols;
+    const int64_t jb = (t / ntc) * kTpTile, cb = (t % ntc) * kTpTile;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int64_t j = jb + (tid >> 4) + 16 * i;
-      const int64_t c = cb + 16 * (tid & 15);
+      const int64_t j = jb + lrow + 32 * i;
+      const int64_t c = cb + 16 * unit;
       v[i] = make_uint4(0, 0, 0, 0);
-      if (j < rows_out && c < C) {
+      if (c < C) {
         int lo = 0, hi = El;
         while (hi - lo > 1) {
           const int mid = (lo + hi) >> 1;
@@ -1049,22 +1059,23 @@ __global__ void __launch_bounds__(256) transpose_pad_kernel(const uint8_t* src, 
   int64_t t = blockIdx.x;
   uint4 nxt[4];
   if (t < ntiles) load(t, nxt);
-  const int cw = tid & 63, rg = tid >> 6;  // output: columns 4 cw .. 4 cw + 3, source rows 16 rg .. 16 rg + 15
+  const int rg = tid & 7, cw = tid >> 3;  // transpose: source rows 16 rg .. + 15, output rows 4 cw .. 4 cw + 3
   for (int b = 0; t < ntiles; t += gridDim.x, b ^= 1) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      *reinterpret_cast<uint4*>(&tile[b][(tid >> 4) + 16 * i][16 * (tid & 15)]) = nxt[i];
+    for (int i = 0; i < 4; ++i) {
+      const int r = lrow + 32 * i;
+      *reinterpret_cast<uint4*>(&tile[b][r][4 * (unit ^ ((r >> 4) & 7))]) = nxt[i];
+    }
     if (t + gridDim.x < ntiles) load(t + gridDim.x, nxt);
     __syncthreads();  // the two buffers alternate, so one barrier per tile suffices
-    const int64_t jb = (t / ntc) * kTpRows, cb = (t % ntc) * kTpCols;
-    uint32_t o[4][4];  // o[k][q]: column 4 cw + k, source rows 16 rg + 4 q .. + 3
+    const int64_t jb = (t / ntc) * kTpTile, cb = (t % ntc) * kTpTile;
+    const int wsw = (cw & 3) | (((cw >> 2) ^ rg) << 2);  // word column cw after the swizzle of group rg
+    uint32_t o[4][4];  // o[k][q]: output row 4 cw + k, source rows 16 rg + 4 q .. + 3
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int r = 16 * rg + 4 * q;
-      const uint32_t r0 = *reinterpret_cast<const uint32_t*>(&tile[b][r][4 * cw]);
-      const uint32_t r1 = *reinterpret_cast<const uint32_t*>(&tile[b][r + 1][4 * cw]);
-      const uint32_t r2 = *reinterpret_cast<const uint32_t*>(&tile[b][r + 2][4 * cw]);
-      const uint32_t r3 = *reinterpret_cast<const uint32_t*>(&tile[b][r + 3][4 * cw]);
+      const uint32_t r0 = tile[b][r][wsw], r1 = tile[b][r + 1][wsw];
+      const uint32_t r2 = tile[b][r + 2][wsw], r3 = tile[b][r + 3][wsw];
       const uint32_t t0 = __byte_perm(r0, r1, 0x5140), t1 = __byte_perm(r2, r3, 0x5140);
       const uint32_t t2 = __byte_perm(r0, r1, 0x7362), t3 = __byte_perm(r2, r3, 0x7362);
       o[0][q] = __byte_perm(t0, t1, 0x5410);
@@ -1072,13 +1083,11 @@ __global__ void __launch_bounds__(256) transpose_pad_kernel(const uint8_t* src, 
       o[2][q] = __byte_perm(t2, t3, 0x5410);
       o[3][q] = __byte_perm(t2, t3, 0x7632);
     }
-    if (jb + 16 * rg < rows_out) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int64_t c = cb + 4 * cw + k;
-        if (c < C)
-          *reinterpret_cast<uint4*>(dst + c * Mp + jb + 16 * rg) = make_uint4(o[k][0], o[k][1], o[k][2], o[k][3]);
-      }
+    for (int k = 0; k < 4; ++k) {
+      const int64_t c = cb + 4 * cw + k;
+      if (c < C)
+        *reinterpret_cast<uint4*>(dst + c * Mp + jb + 16 * rg) = make_uint4(o[k][0], o[k][1], o[k][2], o[k][3]);
     }
   }
 }
