@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--suite", action="store_true",
                     help="time every call of the path alone, for every config (one JSON line per call)")
     ap.add_argument("--suite-configs", default="mixtral,dsv3,prefill,fwdbwd,tiny")
+    ap.add_argument("--train-passes", type=int, default=0,
+                    help="run this many forward + backward passes of --config (for profiling the backward "
+                         "kernels; prints one timing line instead of the benchmark line)")
     return ap.parse_args()
 
 
@@ -579,10 +582,52 @@ def run_suite(args):
         torch.cuda.empty_cache()
 
 
+def run_train_passes(args):
+    """Forward + backward passes of one config (the static-scale training layer by
+    default); a profiling aid for the backward kernels, timed with CUDA events."""
+    import fp8_quantized_moe_gb300 as moe
+
+    cfg = synth.CONFIGS[args.config if args.config != "mixtral" else "fwdbwd"]
+    if args.tokens:
+        cfg = synth.scaled(cfg, T=args.tokens)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    static = synth.calibration_scales(cfg, 0) if cfg.act_mode == synth.PER_TENSOR else None
+    sx = sh = None
+    if static:
+        sx = torch.tensor([static["x"]], dtype=torch.float32, device=dev)
+        sh = torch.tensor([static["h"]], dtype=torch.float32, device=dev)
+    x = synth.activations(cfg, 0).to(dev)
+    ids, w = synth.routing(cfg, 0)
+    w_in, w_out = synth.expert_weights(cfg, 0, device=dev)
+    W = moe.prepare_weights(w_in, w_out, cfg.w_mode, static, for_backward=True)
+    del w_in, w_out
+    torch.cuda.empty_cache()
+    G = synth.output_grad(cfg, 0).to(dev)
+    buf = moe.FFNBuffers(cfg.T, cfg.D, cfg.E, cfg.k, cfg.F, cfg.act_mode, dev, backward=True)
+    idd, wd = torch.from_numpy(ids).to(dev), torch.from_numpy(w).to(dev)
+    ms = []
+    for _ in range(args.train_passes):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        moe.ffn_forward(x, idd, wd, W, cfg.act_mode, buf, sx, sh)
+        moe.ffn_backward(G, wd.reshape(-1), W, buf, sx, sh)
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    if moe.device_error():
+        raise RuntimeError("device error during the training passes")
+    print(json.dumps({"train_passes": args.train_passes, "config": workload_name(cfg),
+                      "ms_per_pass": ms, "tokens_per_s_last": cfg.T / (ms[-1] / 1e3)}), flush=True)
+
+
 def main():
     args = parse()
     if args.suite:
         run_suite(args)
+        return
+    if args.train_passes:
+        run_train_passes(args)
         return
     cfg = synth.CONFIGS[args.config]
     if args.tokens:

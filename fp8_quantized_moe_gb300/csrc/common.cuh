@@ -296,10 +296,11 @@ __device__ __forceinline__ bool quant_needs_division(float y) {
 template <int N>
 __device__ __forceinline__ void quant_n(const float* x, float s, float inv, float* out) {
   bool slow = false;
+  const uint64_t inv2 = f2_pack(inv, inv);
 #pragma unroll
-  for (int j = 0; j < N; ++j) {
-    out[j] = __fmul_rn(x[j], inv);
-    slow = slow || quant_needs_division(out[j]);
+  for (int j = 0; j < N; j += 2) {  // the products in pairs (packed fp32, one rounding each)
+    f2_unpack(f2_mul(f2_pack(x[j], x[j + 1]), inv2), out[j], out[j + 1]);
+    slow = slow || quant_needs_division(out[j]) || quant_needs_division(out[j + 1]);
   }
   if (slow) {
 #pragma unroll

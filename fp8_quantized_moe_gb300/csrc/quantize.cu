@@ -392,9 +392,9 @@ __global__ void __launch_bounds__(256) group_cols_kernel(const uint16_t* g, int6
         float y[8];
         bool slow = false;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          y[j] = __fmul_rn(v[j], inv[j]);
-          slow = slow || quant_needs_division(y[j]);
+        for (int j = 0; j < 8; j += 2) {  // products in pairs (packed fp32, one rounding each)
+          f2_unpack(f2_mul(f2_pack(v[j], v[j + 1]), f2_pack(inv[j], inv[j + 1])), y[j], y[j + 1]);
+          slow = slow || quant_needs_division(y[j]) || quant_needs_division(y[j + 1]);
         }
         if (slow) {
 #pragma unroll
