@@ -608,24 +608,27 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         }
         float amax = 0.0f;
         uint32_t hp[32];  // this warp's 64 h values of the row, bf16 pairs (per-128 h scales)
+        // four chunks of 16 h columns (16-column TMEM loads keep the live
+        // arrays small enough to stay in registers)
+        constexpr int CW = 16, NCH = 64 / CW;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = half * 2 + cc;
-          uint32_t v0[32], v1[32];
-          tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + c * 32, v0);
-          tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + 128 + c * 32, v1);
+        for (int cc = 0; cc < NCH; ++cc) {
+          const int c = half * NCH + cc;  // chunk of the tile's 128 h columns
+          uint32_t v0[CW], v1[CW];
+          tmem_ld_32x32b_x16(tmem_base + lane_addr + a * BN + c * CW, v0);
+          tmem_ld_32x32b_x16(tmem_base + lane_addr + a * BN + 128 + c * CW, v1);
           tmem_wait_ld();
-          if (cc == 1) {  // the accumulator is no longer needed: release it early
+          if (cc == NCH - 1) {  // the accumulator is no longer needed: release it early
             tc_fence_before();
             __syncwarp();
             if (lane == 0) release_acc(a);
           }
-          const int hc = tl.n0 + c * 32;  // first h column of the chunk
-          float f0[32], f1[32], h[32];
-          uint32_t a0b[16], a1b[16], hb[16];  // the same values as packed bf16 pairs
+          const int hc = tl.n0 + c * CW;  // first h column of the chunk
+          float f0[CW], f1[CW], h[CW];
+          uint32_t a0b[CW / 2], a1b[CW / 2], hb[CW / 2];  // the same values as packed bf16 pairs
           const uint64_t sa2 = f2_pack(sa, sa);
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
+          for (int g = 0; g < CW / 4; ++g) {
             float4 s0, s1;
             if (per_chan) {
               s0 = __ldg(reinterpret_cast<const float4*>(swb + hc) + g);
@@ -654,15 +657,15 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
               f1[j + 1] = bf16hi(a1b[j / 2]);
             }
           }
-          swiglu_h_x2<32>(f0, f1, h, hb);
+          swiglu_h_x2<CW>(f0, f1, h, hb);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(h[j]));
+          for (int j = 0; j < CW; ++j) amax = fmaxf(amax, fabsf(h[j]));
           if (row_ok) {
             if (p.a_out) {
               uint4* d0 = reinterpret_cast<uint4*>(p.a_out + row * 2 * p.F + hc);
               uint4* d1 = reinterpret_cast<uint4*>(p.a_out + row * 2 * p.F + p.F + hc);
 #pragma unroll
-              for (int g = 0; g < 4; ++g) {
+              for (int g = 0; g < CW / 8; ++g) {
                 d0[g] = make_uint4(a0b[4 * g], a0b[4 * g + 1], a0b[4 * g + 2], a0b[4 * g + 3]);
                 d1[g] = make_uint4(a1b[4 * g], a1b[4 * g + 1], a1b[4 * g + 2], a1b[4 * g + 3]);
               }
@@ -670,13 +673,14 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
             if (p.h_mode == MOE_SCALE_PER_ROW) {
               uint4* dh = reinterpret_cast<uint4*>(p.h_out + row * p.F + hc);
 #pragma unroll
-              for (int g = 0; g < 4; ++g) dh[g] = make_uint4(hb[4 * g], hb[4 * g + 1], hb[4 * g + 2], hb[4 * g + 3]);
+              for (int g = 0; g < CW / 8; ++g)
+                dh[g] = make_uint4(hb[4 * g], hb[4 * g + 1], hb[4 * g + 2], hb[4 * g + 3]);
             } else if (p.h_mode == MOE_SCALE_PER_TENSOR) {
-              float qv[32];
-              quant_n<32>(h, hs, hinv, qv);
+              float qv[CW];
+              quant_n<CW>(h, hs, hinv, qv);
               uint4* dst = reinterpret_cast<uint4*>(p.h_q + row * p.F + hc);
 #pragma unroll
-              for (int g = 0; g < 2; ++g) {
+              for (int g = 0; g < CW / 16; ++g) {
                 const uint2 lo8 = pack_e4m3x8(qv + 16 * g), hi8 = pack_e4m3x8(qv + 16 * g + 8);
                 dst[g] = make_uint4(lo8.x, lo8.y, hi8.x, hi8.y);
               }
@@ -684,7 +688,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
           }
           if (p.h_mode == MOE_SCALE_PER_ROW_BLOCK128) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) hp[cc * 16 + j] = hb[j];
+            for (int j = 0; j < CW / 2; ++j) hp[cc * (CW / 2) + j] = hb[j];
           }
         }
         const int par = acc & 1;
