@@ -220,8 +220,7 @@ def run_ours(args, cfg, rank, world, local):
             return moe.ffn_forward(x, ids, w, W, cfg.act_mode, buf, sx, sh)
         # the same calls as ffn_forward, with events around the two gmms
         E = W.w_in.shape[0]
-        moe.quantize_rows(x, cfg.act_mode, sx, q=buf.x_q, scale=buf.x_s)
-        s = moe.ragged_sort(ids, E, buf.x_q, buf.x_s if cfg.act_mode != 2 else sx, cfg.act_mode, out=buf.sort)
+        s = moe.quantize_sort(x, ids, E, cfg.act_mode, sx, out=buf.sort)
         xs_s = s["xs_scale"] if cfg.act_mode != 2 else sx
         ev[0].record(stream)
         if moe.swiglu_fusable(cfg.act_mode, W.in_mode, cfg.F):
@@ -333,9 +332,9 @@ def run_ours(args, cfg, rank, world, local):
                        "every step, on their own streams, double-buffered across steps"}
 
     fused = moe.swiglu_fusable(cfg.act_mode, W.in_mode, cfg.F)
-    # quantise 1 + sort 4 + (fused gmm+SwiGLU 1, +1 code pass for per-row h scales
-    # | gmm 1 + SwiGLU 1) + gmm 1 + combine 1
-    launches_per_step = 1 + 4 + ((1 + (1 if cfg.act_mode == 0 else 0)) if fused else 2) + 1 + 1
+    # quantise + sort 4 (histogram, scan, scatter, quantise-gather) + (fused gmm+SwiGLU 1, +1 code
+    # pass for per-row h scales | gmm 1 + SwiGLU 1) + gmm 1 + combine 1
+    launches_per_step = 4 + ((1 + (1 if cfg.act_mode == 0 else 0)) if fused else 2) + 1 + 1
     fl = fwd_flops(cfg)
     g_in = float(np.mean([a for a, _ in gmm_ms]))
     g_out = float(np.mean([b for _, b in gmm_ms]))
@@ -496,6 +495,8 @@ def run_suite(args):
         xs_s = buf.sort["xs_scale"] if am != 2 else sx
         h_s = buf.h_s if am != 2 else sh
         calls = [
+            ("quantize_sort (steps 1 + 2 fused)", lambda: moe.quantize_sort(x, ids, E, am, sx, out=buf.sort),
+             "hbm", 2 * T * D + R * D + 16 * R + sbytes(R, D)),
             ("quantize_rows x", lambda: moe.quantize_rows(x, am, sx, q=buf.x_q, scale=buf.x_s),
              "hbm", 3 * T * D + sbytes(T, D)),
             ("ragged_sort (+ gather)", lambda: moe.ragged_sort(ids, E, buf.x_q, buf.x_s if am != 2 else sx, am,
@@ -566,7 +567,8 @@ def run_suite(args):
                     bound, ach, peak, unit = "hbm", nbytes / (ms / 1e3) / 1e9, hbm, "GB/s"
                 else:
                     ach, peak, unit = flops / (ms / 1e3) / 1e12, fp8, "TFLOP/s"
-            on_path = not (fused and label in ("gmm_fp8 wi_0|wi_1", "moe_swiglu_quant"))
+            on_path = not ((fused and label in ("gmm_fp8 wi_0|wi_1", "moe_swiglu_quant")) or
+                           label in ("quantize_rows x", "ragged_sort (+ gather)"))
             if on_path:
                 total += ms
             line = {"suite": cfg.name, "call": label, "ms": round(ms, 4), "bound": bound,

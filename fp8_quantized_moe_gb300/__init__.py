@@ -127,6 +127,32 @@ def ragged_sort(topk_ids: torch.Tensor, E: int, x_q: torch.Tensor, x_scale: Opti
     return o
 
 
+def quantize_sort(x: torch.Tensor, topk_ids: torch.Tensor, E: int, mode: int,
+                  static_scale: Optional[torch.Tensor] = None, out: Optional[dict] = None):
+    """Steps 1 + 2 fused: sort indices and the gathered codes/scales of x.
+    Returns the same dict as ragged_sort (bit-identical xs_q / xs_scale)."""
+    T, k = topk_ids.shape
+    D = x.shape[1]
+    R = T * k
+    dev = x.device
+    o = out if out is not None else {}
+    if "sorted_src" not in o:
+        o["sorted_src"] = torch.empty(R, dtype=torch.int32, device=dev)
+        o["pos"] = torch.empty(R, dtype=torch.int32, device=dev)
+        o["group_sizes"] = torch.empty(E, dtype=torch.int32, device=dev)
+        o["group_offsets"] = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        o["xs_q"] = torch.empty(R, D, dtype=torch.uint8, device=dev)
+        o["xs_scale"] = _scale_buf(mode, R, D, dev)
+    nws = lib().moe_ragged_sort_workspace_bytes(T, k, E)
+    if "sort_ws" not in o or o["sort_ws"].numel() < nws:
+        o["sort_ws"] = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+    xs_scale = o["xs_scale"] if mode != PER_TENSOR else None
+    check(lib().moe_quantize_sort(_p(x), _p(topk_ids), T, k, E, D, mode, _p(static_scale), _p(o["sorted_src"]),
+                                  _p(o["pos"]), _p(o["group_sizes"]), _p(o["group_offsets"]), _p(o["xs_q"]),
+                                  _p(xs_scale), _p(o["sort_ws"]), o["sort_ws"].numel(), _s()), "moe_quantize_sort")
+    return o
+
+
 def gmm(lhs_q, lhs_scale, lhs_mode, rhs_q, rhs_scale, rhs_mode, group_sizes, group_offset: int = 0,
         E_local: Optional[int] = None, out=None):
     """Grouped matmul -> bf16 [M, N]."""
@@ -337,16 +363,23 @@ class FFNBuffers:
 
 def ffn_forward(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, W: ExpertWeights, act_mode: int,
                 buf: FFNBuffers, static_x: Optional[torch.Tensor] = None,
-                static_h: Optional[torch.Tensor] = None, fuse_swiglu: bool = True) -> torch.Tensor:
+                static_h: Optional[torch.Tensor] = None, fuse_swiglu: bool = True,
+                fuse_quant_sort: bool = True) -> torch.Tensor:
     """One forward pass of the expert FFN; returns buf.y (bf16 [T, D]).
 
-    Where the scale modes allow it, steps 3 and 4 run as one fused kernel
-    (gmm_fp8_swiglu, bit-identical to gmm_fp8 + moe_swiglu_quant); buf.a then
-    holds a only when the buffers were made for a backward pass."""
+    Steps 1 and 2 run as one call (moe_quantize_sort; buf.x_q / buf.x_s are
+    then not written), and where the scale modes allow it steps 3 and 4 run as
+    one fused kernel (gmm_fp8_swiglu, bit-identical to gmm_fp8 +
+    moe_swiglu_quant); buf.a then holds a only when the buffers were made for
+    a backward pass."""
     E = W.w_in.shape[0]
     k = topk_ids.shape[1]
-    quantize_rows(x, act_mode, static_x, q=buf.x_q, scale=buf.x_s)
-    s = ragged_sort(topk_ids, E, buf.x_q, buf.x_s if act_mode != PER_TENSOR else static_x, act_mode, out=buf.sort)
+    if fuse_quant_sort:
+        s = quantize_sort(x, topk_ids, E, act_mode, static_x, out=buf.sort)
+    else:
+        quantize_rows(x, act_mode, static_x, q=buf.x_q, scale=buf.x_s)
+        s = ragged_sort(topk_ids, E, buf.x_q, buf.x_s if act_mode != PER_TENSOR else static_x, act_mode,
+                        out=buf.sort)
     xs_s = s["xs_scale"] if act_mode != PER_TENSOR else static_x
     if fuse_swiglu and swiglu_fusable(act_mode, W.in_mode, buf.F):
         gmm_swiglu(s["xs_q"], xs_s, act_mode, W.w_in, W.s_in, W.in_mode, s["group_sizes"], act_mode, static_h,

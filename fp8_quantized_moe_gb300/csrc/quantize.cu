@@ -65,6 +65,8 @@ struct ScaleOut {
 // ---- producers: each "unit" yields U vectors of 8 bf16-exact values ------
 
 struct RowsOp {  // plain bf16 rows
+  __device__ __forceinline__ int ndst() const { return 1; }
+  __device__ __forceinline__ int64_t dst(int64_t row, int) const { return row; }
   static constexpr int U = 1;
   const uint16_t* x;
   int64_t cols;
@@ -75,6 +77,8 @@ struct RowsOp {  // plain bf16 rows
 };
 
 struct SwigluOp {  // h = bf16(silu(a0) * a1), a = [a0 | a1] of width 2F
+  __device__ __forceinline__ int ndst() const { return 1; }
+  __device__ __forceinline__ int64_t dst(int64_t row, int) const { return row; }
   static constexpr int U = 1;
   const uint16_t* a;
   int64_t F;
@@ -90,6 +94,8 @@ struct SwigluOp {  // h = bf16(silu(a0) * a1), a = [a0 | a1] of width 2F
 };
 
 struct GatherScaleOp {  // dO[r] = bf16(w[i] * G[i / k]), i = sorted_src[r]; also stores dO
+  __device__ __forceinline__ int ndst() const { return 1; }
+  __device__ __forceinline__ int64_t dst(int64_t row, int) const { return row; }
   static constexpr int U = 1;
   const uint16_t* G;
   const float* w;
@@ -115,6 +121,27 @@ struct GatherScaleOp {  // dO[r] = bf16(w[i] * G[i / k]), i = sorted_src[r]; als
   __device__ __forceinline__ int64_t col(int u, int) const { return 8 * static_cast<int64_t>(u); }
 };
 
+// plain bf16 token rows whose codes and scales go to the k sorted rows of the
+// token (pos[t * k + j]): the quantisation of step 1 fused into the gather of
+// step 2 (gather(quantize(x)) == quantize(gather(x)) row by row)
+struct RowsGatherOp {
+  static constexpr int U = 1;
+  const uint16_t* x;
+  int64_t cols;
+  const int32_t* pos;
+  int k;
+  int64_t R;
+  __device__ __forceinline__ int ndst() const { return k; }
+  __device__ __forceinline__ int64_t dst(int64_t row, int j) const {
+    const int64_t p = __ldg(pos + row * k + j);
+    return (p >= 0 && p < R) ? p : -1;
+  }
+  __device__ __forceinline__ void operator()(int64_t row, int u, float (&v)[1][8]) const {
+    unpack8(ldg16(x + row * cols + 8 * u), v[0]);
+  }
+  __device__ __forceinline__ int64_t col(int u, int) const { return 8 * static_cast<int64_t>(u); }
+};
+
 // sigma' chain of the SwiGLU backward, in a fixed order of fp32 operations:
 // silu' = sigma (1 + z (1 - sigma)), dA0 = (dH a1) silu', dA1 = dH silu.
 __device__ __forceinline__ void bwd_elem(float z, float a1, float dh, float sig, float silu, float& da0, float& da1) {
@@ -128,6 +155,8 @@ __device__ __forceinline__ void bwd_elem(float z, float a1, float dh, float sig,
 }
 
 struct SwigluBwdOp {  // dA0 = (dH a1) silu'(a0), dA1 = dH silu(a0); also stores dA
+  __device__ __forceinline__ int ndst() const { return 1; }
+  __device__ __forceinline__ int64_t dst(int64_t row, int) const { return row; }
   static constexpr int U = 2;
   const uint16_t* dH;
   const uint16_t* a;
@@ -209,12 +238,14 @@ __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, i
     }
     __syncthreads();
     s_row = absmax_scale(red[0]);
-    if (tid == 0) so.scale[row] = s_row;
   } else if (MODE == MOE_SCALE_PER_TENSOR) {
     s_row = __ldg(static_scale);
   }
 
+  // codes (and 128-column block scales) once; then written to every destination row
   const float inv_row = __frcp_rn(s_row);
+  uint2 codes[MAXI][U];
+  float s_blk[MAXI];
 #pragma unroll
   for (int i = 0; i < MAXI; ++i) {
     const int u = i * blockDim.x + tid;
@@ -226,8 +257,8 @@ __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, i
       for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
       s = absmax_scale(m);
       inv = __frcp_rn(s);
-      if (u < nunits && (u & 15) == 0) so.scale[so.blk(row, u >> 4)] = s;
     }
+    s_blk[i] = s;
     if (u < nunits) {
 #pragma unroll
       for (int uu = 0; uu < U; ++uu) {
@@ -238,7 +269,22 @@ __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, i
           x8[2 * j + 1] = bf16hi(pk[i][uu][j]);
         }
         quant_n<8>(x8, s, inv, v);
-        *reinterpret_cast<uint2*>(q + row * qcols + op.col(u, uu)) = pack_e4m3x8(v);
+        codes[i][uu] = pack_e4m3x8(v);
+      }
+    }
+  }
+  for (int d = 0; d < op.ndst(); ++d) {
+    const int64_t drow = op.dst(row, d);
+    if (drow < 0) continue;
+    if (MODE == MOE_SCALE_PER_ROW && tid == 0) so.scale[drow] = s_row;
+#pragma unroll
+    for (int i = 0; i < MAXI; ++i) {
+      const int u = i * blockDim.x + tid;
+      if (u < nunits) {
+        if (MODE == MOE_SCALE_PER_ROW_BLOCK128 && (u & 15) == 0) so.scale[so.blk(drow, u >> 4)] = s_blk[i];
+#pragma unroll
+        for (int uu = 0; uu < U; ++uu)
+          *reinterpret_cast<uint2*>(q + drow * qcols + op.col(u, uu)) = codes[i][uu];
       }
     }
   }
@@ -428,6 +474,20 @@ extern "C" __attribute__((visibility("hidden"))) cudaError_t moe_detail_take_err
   if (e == cudaSuccess && v) e = cudaMemcpyToSymbol(g_err, &z, sizeof(z));
   *out = v;
   return e;
+}
+
+// Step 1 fused into the gather of step 2 (moe_quantize_sort): token rows of
+// x are quantised once and their codes and scales written to the k sorted
+// rows pos[t * k + j]; called by sort.cu once the sort indices exist.
+extern "C" __attribute__((visibility("hidden"))) moe_status moe_detail_quantize_gather(
+    const uint16_t* x, const int32_t* pos, int64_t T, int k, int64_t D, moe_scale_mode mode, const float* static_scale,
+    uint8_t* xs_q, float* xs_scale, cudaStream_t st) {
+  MOE_HOST_CHECK(D <= kMaxCols, MOE_ERR_INVALID_ARG);
+  moe_status stt = check_mode_ptrs(mode, static_scale, xs_scale);
+  if (stt != MOE_OK) return stt;
+  RowsGatherOp op{x, D, pos, k, T * k};
+  ScaleOut so{xs_scale, 0, static_cast<int>((D + 127) / 128)};
+  return launch_rows(op, T, static_cast<int>(D / 8), D, mode, static_scale, xs_q, so, st);
 }
 
 extern "C" moe_status moe_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, moe_scale_mode mode,

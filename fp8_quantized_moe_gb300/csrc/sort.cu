@@ -210,6 +210,35 @@ extern "C" size_t moe_ragged_sort_workspace_bytes(int64_t T, int k, int E) {
   return static_cast<size_t>((nc > 0 ? nc : 1) * E) * sizeof(int);
 }
 
+namespace moe {
+namespace {
+// Steps of the sort that produce the indices: histogram, scan, stable
+// scatter.  `counts` is the caller's workspace.
+moe_status sort_indices(const int32_t* topk_ids, int64_t T, int k, int E, int32_t* sorted_src, int32_t* pos,
+                        int32_t* group_sizes, int32_t* group_offsets, int* counts, cudaStream_t st) {
+  const int64_t R = T * k;
+  const int64_t nc = num_chunks(R);
+  const size_t hist_smem = sizeof(int) * kWarps * E;
+  if (nc > 0) {
+    if (hist_smem > 48 * 1024) {
+      MOE_CUDA_TRY(cudaFuncSetAttribute(sort_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(hist_smem)));
+      MOE_CUDA_TRY(cudaFuncSetAttribute(sort_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(hist_smem)));
+    }
+    sort_hist_kernel<<<static_cast<unsigned>(nc), 256, hist_smem, st>>>(topk_ids, R, E, counts);
+    MOE_CUDA_TRY(cudaGetLastError());
+  }
+  sort_scan_kernel<<<1, 1024, 0, st>>>(counts, static_cast<int>(nc), E, group_sizes, group_offsets);
+  MOE_CUDA_TRY(cudaGetLastError());
+  if (nc == 0) return MOE_OK;
+  sort_scatter_kernel<<<static_cast<unsigned>(nc), 256, hist_smem, st>>>(topk_ids, R, E, counts, sorted_src, pos);
+  MOE_CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+}  // namespace
+}  // namespace moe
+
 extern "C" moe_status moe_ragged_sort(const int32_t* topk_ids, int64_t T, int k, int E, const uint8_t* x_q,
                                       const float* x_scale, int64_t D, moe_scale_mode mode, int32_t* sorted_src,
                                       int32_t* pos, int32_t* group_sizes, int32_t* group_offsets, uint8_t* xs_q,
@@ -228,25 +257,9 @@ extern "C" moe_status moe_ragged_sort(const int32_t* topk_ids, int64_t T, int k,
     MOE_HOST_CHECK(mode == MOE_SCALE_PER_TENSOR, MOE_ERR_INVALID_ARG);
   }
   cudaStream_t st = as_stream(stream);
-  const int64_t R = T * k;
-  const int64_t nc = num_chunks(R);
-  int* counts = static_cast<int*>(workspace);
-  const size_t hist_smem = sizeof(int) * kWarps * E;
-  if (nc > 0) {
-    if (hist_smem > 48 * 1024) {
-      MOE_CUDA_TRY(cudaFuncSetAttribute(sort_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(hist_smem)));
-      MOE_CUDA_TRY(cudaFuncSetAttribute(sort_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(hist_smem)));
-    }
-    sort_hist_kernel<<<static_cast<unsigned>(nc), 256, hist_smem, st>>>(topk_ids, R, E, counts);
-    MOE_CUDA_TRY(cudaGetLastError());
-  }
-  sort_scan_kernel<<<1, 1024, 0, st>>>(counts, static_cast<int>(nc), E, group_sizes, group_offsets);
-  MOE_CUDA_TRY(cudaGetLastError());
-  if (nc == 0) return MOE_OK;
-  sort_scatter_kernel<<<static_cast<unsigned>(nc), 256, hist_smem, st>>>(topk_ids, R, E, counts, sorted_src, pos);
-  MOE_CUDA_TRY(cudaGetLastError());
+  moe_status stt = sort_indices(topk_ids, T, k, E, sorted_src, pos, group_sizes, group_offsets,
+                                static_cast<int*>(workspace), st);
+  if (stt != MOE_OK || T * k == 0) return stt;
   const unsigned gblocks = static_cast<unsigned>((T + 7) / 8);
   if (mode == MOE_SCALE_PER_ROW)
     sort_gather_kernel<MOE_SCALE_PER_ROW><<<gblocks, 256, 0, st>>>(x_q, x_scale, T, k, D, pos, xs_q, xs_scale);
@@ -257,6 +270,34 @@ extern "C" moe_status moe_ragged_sort(const int32_t* topk_ids, int64_t T, int k,
     sort_gather_kernel<MOE_SCALE_PER_TENSOR><<<gblocks, 256, 0, st>>>(x_q, x_scale, T, k, D, pos, xs_q, xs_scale);
   MOE_CUDA_TRY(cudaGetLastError());
   return MOE_OK;
+}
+
+extern "C" __attribute__((visibility("hidden"))) moe_status moe_detail_quantize_gather(
+    const uint16_t* x, const int32_t* pos, int64_t T, int k, int64_t D, moe_scale_mode mode, const float* static_scale,
+    uint8_t* xs_q, float* xs_scale, cudaStream_t st);
+
+extern "C" moe_status moe_quantize_sort(const uint16_t* x, const int32_t* topk_ids, int64_t T, int k, int E, int64_t D,
+                                        moe_scale_mode mode, const float* static_scale, int32_t* sorted_src,
+                                        int32_t* pos, int32_t* group_sizes, int32_t* group_offsets, uint8_t* xs_q,
+                                        float* xs_scale, void* workspace, size_t workspace_bytes,
+                                        moe_stream_t stream) {
+  MOE_HOST_CHECK(x && topk_ids && sorted_src && pos && group_sizes && group_offsets && xs_q && workspace,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(T >= 0 && k > 0 && k <= 32 && E > 0 && E <= kMaxE && D > 0 && D % 16 == 0, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(T * k < (1ll << 31), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(aligned16(x) && aligned16(xs_q) && (reinterpret_cast<uintptr_t>(workspace) & 3) == 0,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(workspace_bytes >= moe_ragged_sort_workspace_bytes(T, k, E), MOE_ERR_INVALID_ARG);
+  if (mode == MOE_SCALE_PER_ROW || mode == MOE_SCALE_PER_ROW_BLOCK128) {
+    MOE_HOST_CHECK(xs_scale != nullptr && aligned16(xs_scale), MOE_ERR_INVALID_ARG);
+  } else {
+    MOE_HOST_CHECK(mode == MOE_SCALE_PER_TENSOR && static_scale, MOE_ERR_INVALID_ARG);
+  }
+  cudaStream_t st = as_stream(stream);
+  moe_status stt = sort_indices(topk_ids, T, k, E, sorted_src, pos, group_sizes, group_offsets,
+                                static_cast<int*>(workspace), st);
+  if (stt != MOE_OK || T * k == 0) return stt;
+  return moe_detail_quantize_gather(x, pos, T, k, D, mode, static_scale, xs_q, xs_scale, st);
 }
 
 // ---------------------------------------------------------------------------

@@ -143,6 +143,23 @@ moe_status moe_ragged_sort(const int32_t* topk_ids, int64_t T, int k, int E, con
                            int32_t* group_sizes, int32_t* group_offsets, uint8_t* xs_q, float* xs_scale,
                            void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* moe_quantize_sort -- steps 1 and 2 in one call: the sort indices as in
+ * moe_ragged_sort, and the activation quantisation of moe_quantize_rows
+ * (same scale rule and modes) fused into the gather, so the token-order codes
+ * never go to memory: each token row of x is quantised once and its codes and
+ * scales are written to its k sorted rows.  Row by row, gather(quantize(x)) is
+ * quantize(gather(x)) ("Quantize activations before EP all gather": the
+ * quantisation moves ahead of the gather at no cost), so xs_q and xs_scale are
+ * bit-identical to moe_quantize_rows followed by moe_ragged_sort.
+ *   x bf16 [T, D]; static_scale [1] for PER_TENSOR (else unused);
+ *   xs_scale [T*k] (PER_ROW) or [T*k, D/128] (PER_ROW_BLOCK128), 16-byte
+ *   aligned; every other argument as moe_ragged_sort (same workspace size).
+ * D % 16 == 0, D <= 32768.  Invalid ids raise MOE_DEVERR_BAD_EXPERT_ID. */
+moe_status moe_quantize_sort(const uint16_t* x, const int32_t* topk_ids, int64_t T, int k, int E, int64_t D,
+                             moe_scale_mode mode, const float* static_scale, int32_t* sorted_src, int32_t* pos,
+                             int32_t* group_sizes, int32_t* group_offsets, uint8_t* xs_q, float* xs_scale,
+                             void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
 /* moe_ragged_sort_noalloc -- moe_ragged_sort for callers that cannot
  * allocate device memory.  The pages have no counterpart: it exists for
  * hosts that own every byte of device memory themselves (an inference engine

@@ -58,12 +58,12 @@ def test_ffn_small_matches_oracle(name):
     if cfg.w_mode != synth.PER_TENSOR:
         assert np.array_equal(host(W.s_out), wq[4])
     y, buf, sx, sh = run_gpu_forward(cfg, x_t.cuda(), dev(ids), dev(w), W, static)
-    # steps computed from the inputs directly: bit-exact
-    assert np.array_equal(host(buf.x_q), ref["x_q"])
-    if cfg.act_mode != synth.PER_TENSOR:
-        assert np.array_equal(host(buf.x_s), ref["x_s"])
+    # steps computed from the inputs directly (quantise + sort + gather, fused): bit-exact
     for key in ("sorted_src", "pos", "group_sizes", "group_offsets", "xs_q"):
         assert np.array_equal(host(buf.sort[key]), ref[{"group_sizes": "sizes", "group_offsets": "offsets"}.get(key, key)]), key
+    if cfg.act_mode != synth.PER_TENSOR:
+        _, xss_ref = oracle.gather_rows(ref["x_q"], ref["x_s"], cfg.act_mode, ref["sorted_src"], cfg.k)
+        assert np.array_equal(host(buf.sort["xs_scale"]).view(np.uint32), xss_ref.view(np.uint32))
     # downstream of the contractions: tolerance
     assert_close(host(buf.a), ref["a"], f"{name}: a")
     assert_close(host(buf.o), ref["o"], f"{name}: o", rel_fro=5e-3)
@@ -150,8 +150,9 @@ def test_fused_and_unfused_forward_are_identical(name):
     outs = []
     for fuse in (True, False):
         buf = moe.FFNBuffers(cfg.T, cfg.D, cfg.E, cfg.k, cfg.F, cfg.act_mode, "cuda")
-        y = moe.ffn_forward(x_t, dev(ids), dev(w), W, cfg.act_mode, buf, sx, sh, fuse_swiglu=fuse)
-        outs.append((host(y), host(buf.h_q)))
+        y = moe.ffn_forward(x_t, dev(ids), dev(w), W, cfg.act_mode, buf, sx, sh, fuse_swiglu=fuse,
+                            fuse_quant_sort=fuse)
+        outs.append((host(y), host(buf.h_q), host(buf.sort["xs_q"])))
     assert moe.device_error() == 0
-    assert np.array_equal(outs[0][1], outs[1][1])
-    assert np.array_equal(outs[0][0], outs[1][0])
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(a, b)

@@ -87,6 +87,36 @@ def test_ragged_sort_bit_exact(T, k, E, D, mode):
         assert np.array_equal(host(out["xs_scale"]), xss_ref)
 
 
+@pytest.mark.parametrize("T,k,E,D,mode", [
+    (1, 1, 1, 16, synth.PER_ROW),
+    (7, 2, 16, 128, synth.PER_ROW),           # zero-token experts
+    (333, 6, 64, 272, synth.PER_TENSOR),      # D not a multiple of 128
+    (1000, 8, 256, 384, synth.PER_ROW_BLOCK128),
+    (2500, 2, 8, 4096, synth.PER_ROW),
+    (600, 8, 256, 7168, synth.PER_ROW_BLOCK128),
+])
+def test_quantize_sort_bit_exact(T, k, E, D, mode):
+    """Steps 1 + 2 fused: sort indices, gathered codes and scales all match the
+    oracle's quantise-then-sort-then-gather."""
+    rng = np.random.default_rng(T * 3 + D + mode)
+    ids = rng.integers(0, E, (T, k)).astype(np.int32)
+    x = bf16_rows(rng, T, D)
+    static = 0.0211
+    q_ref, s_ref = oracle.quantize_rows(x, mode, static)
+    src, pos, sizes, offs = oracle.ragged_sort(ids, E)
+    xs_ref, xss_ref = oracle.gather_rows(q_ref, s_ref, mode, src, k)
+    ss = torch.tensor([static], dtype=torch.float32, device="cuda")
+    out = moe.quantize_sort(dev(x), dev(ids), E, mode, ss)
+    assert moe.device_error() == 0
+    assert np.array_equal(host(out["sorted_src"]), src)
+    assert np.array_equal(host(out["pos"]), pos)
+    assert np.array_equal(host(out["group_sizes"]), sizes)
+    assert np.array_equal(host(out["group_offsets"]), offs)
+    assert np.array_equal(host(out["xs_q"]), xs_ref)
+    if mode != synth.PER_TENSOR:
+        assert np.array_equal(host(out["xs_scale"]).view(np.uint32), xss_ref.view(np.uint32))
+
+
 def test_ragged_sort_bad_id_sets_device_error():
     ids = np.array([[0, 1], [2, 7]], np.int32)  # 7 >= E
     x_q = np.zeros((2, 16), np.uint8)
