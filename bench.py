@@ -533,8 +533,8 @@ def run_suite(args):
                  "tensor", (2.0 * R * D * F, R * D + E * D * F + 2 * R * F)),
                 ("bwd moe_swiglu_bwd_quant", lambda: moe.swiglu_bwd_quant(buf.dH, buf.a),
                  "hbm", 2 * R * F + 4 * R * F + 6 * R * F + 4 * R),
-                ("bwd gmm_fp8 dXs = dA [wi_0|wi_1]", lambda: moe.gmm(dA_q, dA_s, 0, W.w_in_t, W.s_in_t, 1, sizes,
-                                                                    out=buf.dXs),
+                ("bwd gmm_fp8_ksplit dXs = dA [wi_0|wi_1]",
+                 lambda: moe.gmm_ksplit(dA_q, dA_s, 0, W.w_in_t, W.s_in_split, F, sizes, out=buf.dXs),
                  "tensor", (2.0 * R * 2 * F * D, 2 * R * F + E * 2 * F * D + 2 * R * D)),
                 ("bwd ragged_gather_reduce dX", lambda: moe.ragged_gather_reduce(buf.dXs, buf.sort["pos"], None, k,
                                                                                  out=buf.dX),

@@ -168,6 +168,22 @@ def gmm(lhs_q, lhs_scale, lhs_mode, rhs_q, rhs_scale, rhs_mode, group_sizes, gro
     return out
 
 
+def gmm_ksplit(lhs_q, lhs_scale, lhs_mode, rhs_q, rhs_scale2, K_split: int, group_sizes, group_offset: int = 0,
+               E_local: Optional[int] = None, out=None):
+    """Grouped matmul over two K segments with one static weight scale each
+    (rhs_scale2 = [s0, s1]) -> bf16 [M, N]."""
+    M, K = lhs_q.shape
+    El, N, K2 = rhs_q.shape
+    if K2 != K:
+        raise MoEError("lhs/rhs K mismatch")
+    E = group_sizes.numel()
+    E_local = El if E_local is None else E_local
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=lhs_q.device) if out is None else out
+    check(lib().gmm_fp8_ksplit(_p(lhs_q), _p(lhs_scale), lhs_mode, _p(rhs_q), _p(rhs_scale2), K_split,
+                               _p(group_sizes), E, group_offset, E_local, M, K, N, _p(out), _s()), "gmm_fp8_ksplit")
+    return out
+
+
 def gmm_swiglu(lhs_q, lhs_scale, lhs_mode, rhs_q, rhs_scale, rhs_mode, group_sizes, h_mode: int,
                h_static: Optional[torch.Tensor] = None, group_offset: int = 0, E_local: Optional[int] = None,
                keep_a: bool = False, a_out=None, h=None, h_q=None, h_scale=None):
@@ -299,6 +315,7 @@ class ExpertWeights:
     w_in_t: Optional[torch.Tensor] = None
     s_in_t: Optional[torch.Tensor] = None
     w_out_t: Optional[torch.Tensor] = None
+    s_in_split: Optional[torch.Tensor] = None  # [s_w0, s_w1]: the two K halves of w_in_t
 
 
 def prepare_weights(w_in: torch.Tensor, w_out: torch.Tensor, w_mode: int, static: Optional[dict] = None,
@@ -331,6 +348,7 @@ def prepare_weights(w_in: torch.Tensor, w_out: torch.Tensor, w_mode: int, static
             st[:, : F // 128] = static["w0"]
             st[:, F // 128:] = static["w1"]
             W.s_in_t = st
+            W.s_in_split = torch.tensor([static["w0"], static["w1"]], dtype=torch.float32, device=dev)
             W.w_out_t = transpose_u8(qo)
         return W
     qin, sin = quantize_weights(w_in, w_mode)
@@ -405,7 +423,8 @@ def ffn_backward(dY: torch.Tensor, topk_w: torch.Tensor, W: ExpertWeights, buf: 
     dO, dO_q, dO_s = gather_scale_quant(dY, topk_w, s["sorted_src"], k)
     gmm(dO_q, dO_s, PER_ROW, W.w_out_t, W.s_out, PER_TENSOR, s["group_sizes"], out=buf.dH)
     dA, dA_q, dA_s = swiglu_bwd_quant(buf.dH, buf.a)
-    gmm(dA_q, dA_s, PER_ROW, W.w_in_t, W.s_in_t, PER_ROW_BLOCK128, s["group_sizes"], out=buf.dXs)
+    # dXs = dA0 W0^T + dA1 W1^T: one contraction over [dA0 | dA1], one static scale per K half
+    gmm_ksplit(dA_q, dA_s, PER_ROW, W.w_in_t, W.s_in_split, buf.F, s["group_sizes"], out=buf.dXs)
     ragged_gather_reduce(buf.dXs, s["pos"], None, k, out=buf.dX)
     dAg_q, dAg_s = quantize_group_cols(dA, s["group_sizes"])
     dOg_q, dOg_s = quantize_group_cols(dO, s["group_sizes"])

@@ -28,6 +28,7 @@ SIGNATURES = {
     "moe_ragged_sort_workspace_bytes": ([i64, i32, i32], sz),
     "moe_ragged_sort": ([P, i64, i32, i32, P, P, i64, i32, P, P, P, P, P, P, P, sz, P], i32),
     "moe_quantize_sort": ([P, P, i64, i32, i32, i64, i32, P, P, P, P, P, P, P, P, sz, P], i32),
+    "gmm_fp8_ksplit": ([P, P, i32, P, P, i64, P, i32, i32, i32, i64, i64, i64, P, P], i32),
     "gmm_fp8": ([P, P, i32, P, P, i32, P, i32, i32, i32, i64, i64, i64, P, P], i32),
     "moe_swiglu_quant": ([P, i64, i64, i32, P, P, P, P], i32),
     "ragged_gather_reduce": ([P, P, P, i64, i32, i64, P, P], i32),

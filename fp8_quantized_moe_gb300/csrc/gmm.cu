@@ -57,7 +57,7 @@ constexpr int kMaxAcc = 8;
 constexpr int kMaxGroups = 1024;
 constexpr int64_t kPairMinK = 3072;  // gmm K from which the plain and SwiGLU gmm run on CTA pairs
 
-enum Mode { kFinal = 0, kPromote = 1, kTgmm = 2, kSwiglu = 3 };
+enum Mode { kFinal = 0, kPromote = 1, kTgmm = 2, kSwiglu = 3, kSplit = 4 };
 
 struct Params {
   const int32_t* group_sizes;
@@ -65,6 +65,7 @@ struct Params {
   int64_t M;
   int K, N;
   int kblocks;  // gmm: K blocks per tile
+  int kb_split;  // kSplit: K blocks of the first scale segment
   int ntiles;   // N tiles
   int ktiles;   // tgmm: output-row tiles (K / 128)
   const float* lhs_scale;
@@ -138,7 +139,8 @@ struct Cfg {
   static constexpr bool PAIR = PAIR_REQ && MOE_GMM_PAIR && (MODE == kFinal || MODE == kSwiglu);
   static constexpr int BN = PROMOTE ? MOE_PROMOTE_BN : 256;  // output columns per tile
   static constexpr int TMEM_COLS = PAIR ? MOE_PAIR_TMEM_COLS : 512;
-  static constexpr int NACC = TMEM_COLS / BN;                // accumulators of BN columns
+  static constexpr int SEGS = MODE == kSplit ? 2 : 1;        // accumulators per tile (one per K segment)
+  static constexpr int NACC = TMEM_COLS / (BN * SEGS);       // tiles in flight in tensor memory
   static constexpr int NSTAGE = PAIR ? 6 : (BN == 128 ? 6 : (BN == 64 ? 8 : (MODE == kTgmm ? MOE_TGMM_NSTAGE : MOE_GMM_NSTAGE)));
   static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK;  // this CTA's part of the B tile
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -150,13 +152,14 @@ struct Cfg {
   // per-warp staging of 32x32 output blocks: kFinal, bf16 rows padded to 80
   // bytes for row-contiguous stores; kTgmm, two 4 KB fp32 blocks in the
   // 128-byte-swizzled layout of a TMA store box
-  static constexpr int STG_PITCH = MODE == kFinal ? 80 : 0;
+  static constexpr int STG_PITCH = (MODE == kFinal || MODE == kSplit) ? 80 : 0;
   static constexpr int STG_BUFS = MODE == kTgmm ? MOE_TGMM_STG_BUFS : 1;
-  static constexpr int STG_WARP_BYTES = MODE == kFinal ? 32 * STG_PITCH : (MODE == kTgmm ? STG_BUFS * 4096 : 0);
+  static constexpr int STG_WARP_BYTES =
+      (MODE == kFinal || MODE == kSplit) ? 32 * STG_PITCH : (MODE == kTgmm ? STG_BUFS * 4096 : 0);
   static constexpr size_t CTL_BYTES = (sizeof(SmemCtl) + 1023) / 1024 * 1024;  // keeps the staging 1 KB aligned
   static constexpr size_t SMEM = 1024 + static_cast<size_t>(NSTAGE) * STAGE_BYTES + CTL_BYTES +
                                  static_cast<size_t>(EPI_WARPS) * STG_WARP_BYTES;
-  static_assert(NSTAGE <= kMaxStages && NACC >= 1 && NACC <= kMaxAcc && NACC * BN == TMEM_COLS,
+  static_assert(NSTAGE <= kMaxStages && NACC >= 1 && NACC <= kMaxAcc && NACC * BN * SEGS == TMEM_COLS,
                 "tile configuration");
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
@@ -478,10 +481,14 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
           const uint32_t sa = base + s * STAGE_BYTES;
           const uint64_t da = smem_desc_sw128(sa);
           const uint64_t db = smem_desc_sw128(sa + A_BYTES);
-          const uint32_t d_tmem = tmem_base + a * BN;
+          // kSplit: K blocks [0, kb_split) accumulate into the tile's first
+          // accumulator, the rest into its second (each segment starts fresh)
+          const bool seg1 = MODE == kSplit && kb >= p.kb_split;
+          const uint32_t d_tmem = tmem_base + a * BN * C::SEGS + (seg1 ? BN : 0);
+          const int seg_kb0 = seg1 ? p.kb_split : 0;
 #pragma unroll
           for (int k4 = 0; k4 < BK / UMMA_K; ++k4) {
-            const uint32_t accumulate = (MODE == kPromote) ? (k4 > 0) : (kb > 0 || k4 > 0);
+            const uint32_t accumulate = (MODE == kPromote) ? (k4 > 0) : (kb > seg_kb0 || k4 > 0);
             // +32 bytes along K inside the 128-byte swizzled row = +2 in the
             // descriptor's address field (16-byte units)
             if (PAIR)
@@ -721,6 +728,57 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
             }
           }
         }
+      } else if (MODE == kSplit) {
+        // out = bf16((s0 * acc0 + s1 * acc1) * s_a): the two K segments'
+        // fp32 sums meet in the epilogue, each with its static weight scale
+        uint16_t* out = static_cast<uint16_t*>(p.out);
+        const int64_t row = static_cast<int64_t>(tl.row0) + r;
+        const uint32_t a = acc % NACC;
+        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+        const float sa = row_ok ? lhs_scale_at(p, row, 0) : 0.f;
+        const float s0 = __ldg(p.rhs_scale), s1 = __ldg(p.rhs_scale + 1);
+        const bool has0 = p.kb_split > 0, has1 = p.kb_split < p.kblocks;
+        const uint32_t t0 = tmem_base + lane_addr + a * BN * C::SEGS;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          const int nb = tl.n0 + c * 32;
+          uint32_t v0[32], v1[32];
+          if (has0) tmem_ld_32x32b_x32(t0 + c * 32, v0);
+          if (has1) tmem_ld_32x32b_x32(t0 + BN + c * 32, v1);
+          tmem_wait_ld();
+          float f[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float p0 = has0 ? __fmul_rn(__uint_as_float(v0[j]), s0) : 0.0f;
+            f[j] = __fmul_rn(has1 ? __fmaf_rn(__uint_as_float(v1[j]), s1, p0) : p0, sa);
+          }
+          // stage this warp's 32x32 bf16 block, then write 8 rows (64 contiguous bytes each) per instruction
+          uint8_t* stg = stg_base + (warp - 2) * C::STG_WARP_BYTES;
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            *reinterpret_cast<uint4*>(stg + lane * C::STG_PITCH + 16 * g) =
+                make_uint4(pack_bf16x2(f[8 * g], f[8 * g + 1]), pack_bf16x2(f[8 * g + 2], f[8 * g + 3]),
+                           pack_bf16x2(f[8 * g + 4], f[8 * g + 5]), pack_bf16x2(f[8 * g + 6], f[8 * g + 7]));
+          __syncwarp();
+          const int seg = (lane & 3) * 8;  // bf16 column offset of this lane's 16 bytes
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int rr = i * 8 + (lane >> 2);
+            const int64_t orow = static_cast<int64_t>(tl.row0) + q4 * 32 + rr;
+            if (rr < tl.rows - q4 * 32 && nb + seg < p.N)
+              *reinterpret_cast<uint4*>(out + orow * p.N + nb + seg) =
+                  *reinterpret_cast<const uint4*>(stg + rr * C::STG_PITCH + 2 * seg);
+          }
+          __syncwarp();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) release_acc(a);
+        ++acc;
       } else if (MODE == kFinal) {
         uint16_t* out = static_cast<uint16_t*>(p.out);
         const int64_t row = static_cast<int64_t>(tl.row0) + r;
@@ -1349,6 +1407,49 @@ extern "C" moe_status gmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_
   if (blockwise) return launch_mma<kPromote, false>(A, B, A, p, gmm_max_units<kPromote, false>(M, E_local, p.ntiles), st);
   if (pair) return launch_mma<kFinal, true>(A, B, A, p, gmm_max_units<kFinal, true>(M, E_local, p.ntiles), st);
   return launch_mma<kFinal, false>(A, B, A, p, gmm_max_units<kFinal, false>(M, E_local, p.ntiles), st);
+}
+
+extern "C" moe_status gmm_fp8_ksplit(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode,
+                                     const uint8_t* rhs_q, const float* rhs_scale2, int64_t K_split,
+                                     const int32_t* group_sizes, int E, int group_offset, int E_local, int64_t M,
+                                     int64_t K, int64_t N, uint16_t* out, moe_stream_t stream) {
+  MOE_HOST_CHECK(lhs_q && lhs_scale && rhs_q && rhs_scale2 && group_sizes && out, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(lhs_mode == MOE_SCALE_PER_ROW || lhs_mode == MOE_SCALE_PER_TENSOR, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(E > 0 && E <= kMaxGroups && group_offset >= 0 && E_local > 0 && group_offset + E_local <= E,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(M >= 0 && M < (1ll << 31) && K > 0 && K % 16 == 0 && K < (1 << 30) && N > 0 && N % 16 == 0,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(K_split >= 0 && K_split <= K && K_split % BK == 0, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(static_cast<int64_t>(E_local) * N < (1ll << 31), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(aligned16(lhs_q) && aligned16(rhs_q) && aligned16(out), MOE_ERR_INVALID_ARG);
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = as_stream(stream);
+  if (M == 0) return MOE_OK;
+  if (group_offset > 0 || E_local < E) {
+    zero_outside_kernel<<<sm_count() * 4, 256, 0, st>>>(out, M, N, group_sizes, E, group_offset, E_local);
+    MOE_CUDA_TRY(cudaGetLastError());
+  }
+  CUtensorMap A, B;
+  if (!make_map(&A, lhs_q, K, M, K, BM)) return MOE_ERR_CUDA;
+  if (!make_map(&B, rhs_q, K, static_cast<uint64_t>(E_local) * N, K, Cfg<kSplit>::BN)) return MOE_ERR_CUDA;
+  Params p{};
+  p.group_sizes = group_sizes;
+  p.E = E;
+  p.g0 = group_offset;
+  p.El = E_local;
+  p.M = M;
+  p.K = static_cast<int>(K);
+  p.N = static_cast<int>(N);
+  p.kblocks = static_cast<int>((K + BK - 1) / BK);
+  p.kb_split = static_cast<int>(K_split / BK);
+  p.ntiles = static_cast<int>((N + Cfg<kSplit>::BN - 1) / Cfg<kSplit>::BN);
+  p.ktiles = 0;
+  p.lhs_scale = lhs_scale;
+  p.lhs_mode = lhs_mode;
+  p.rhs_scale = rhs_scale2;
+  p.rhs_mode = MOE_SCALE_PER_TENSOR;
+  p.out = out;
+  return launch_mma<kSplit, false>(A, B, A, p, gmm_max_units<kSplit, false>(M, E_local, p.ntiles), st);
 }
 
 extern "C" moe_status gmm_fp8_swiglu(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode,

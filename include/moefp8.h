@@ -214,6 +214,22 @@ moe_status gmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode 
                    int group_offset, int E_local, int64_t M, int64_t K, int64_t N, uint16_t* out,
                    moe_stream_t stream);
 
+/* gmm_fp8_ksplit -- grouped matmul whose K range is two segments, each with
+ * one static weight scale: the backward's input gradient
+ * dXs = dA0 W0^T + dA1 W1^T as one contraction over [dA0 | dA1] (K = 2F,
+ * K_split = F) with rhs = [W0 | W1]^T, the static scales s0 of wi_0 and s1 of
+ * wi_1 ("Support quantization for tokamax gmm v2": fp8_static_wa):
+ *   out[m, n] = bf16( (s0 * sum_{k < K_split} a[m,k] w[g,n,k]
+ *                    + s1 * sum_{k >= K_split} a[m,k] w[g,n,k]) * s_a[m] )
+ * Both sums are fp32 on the tensor cores, in two accumulators that meet in the
+ * epilogue (no per-128 promotion).  lhs_mode PER_ROW [M] or PER_TENSOR [1];
+ * rhs_scale2 = {s0, s1} (device, 2 floats); rhs_q [E_local, N, K].
+ * K_split % 128 == 0, 0 <= K_split <= K; otherwise as gmm_fp8. */
+moe_status gmm_fp8_ksplit(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode,
+                          const uint8_t* rhs_q, const float* rhs_scale2, int64_t K_split,
+                          const int32_t* group_sizes, int E, int group_offset, int E_local, int64_t M, int64_t K,
+                          int64_t N, uint16_t* out, moe_stream_t stream);
+
 /* gmm_fp8_swiglu -- steps 3 and 4 in one pass: the [wi_0 | wi_1] grouped
  * matmul with SwiGLU and the requantisation of h in its epilogue, so the
  * [M, 2F] bf16 product a never goes to memory.  Bit-identical to gmm_fp8

@@ -83,6 +83,36 @@ def test_gmm_pair_expert_parallel_shard():
     assert_close(host(out), ref, "gmm pair shard")
 
 
+@pytest.mark.parametrize("M,K,N,E,K_split,amode,shard", [
+    (700, 768, 512, 5, 384, R0, None),
+    (640, 2816, 272, 8, 1408, R0, None),      # the backward's K = 2F, K_split = F; N tail
+    (300, 512, 256, 3, 0, RT, None),          # one segment only (the second)
+    (300, 512, 256, 3, 512, R0, None),        # one segment only (the first)
+    (900, 1024, 256, 6, 512, R0, (1, 4)),     # expert-parallel shard
+])
+def test_gmm_ksplit_matches_oracle(M, K, N, E, K_split, amode, shard):
+    """Two K segments with one static weight scale each equal the blockwise-scaled
+    gmm whose K blocks carry s0 before K_split and s1 after."""
+    sizes, a, w, sa, _ = make_case(M + K + N + K_split, M, K, N, E, amode, RT, zero_frac=0.2)
+    g0, El = shard if shard else (0, E)
+    w = np.ascontiguousarray(w[g0:g0 + El])
+    s0, s1 = np.float32(0.7 / (448 * np.sqrt(K))), np.float32(1.9 / (448 * np.sqrt(K)))
+    nb = K // 128
+    sw_blk = np.empty((El, nb, N), np.float32)
+    sw_blk[:, :K_split // 128] = s0
+    sw_blk[:, K_split // 128:] = s1
+    ref = oracle.gmm(a, sa, amode, w, sw_blk, RB, sizes, group_offset=g0, E_local=El)
+    out = moe.gmm_ksplit(dev(a), dev(sa), amode, dev(w), dev(np.array([s0, s1], np.float32)), K_split, dev(sizes),
+                         group_offset=g0, E_local=El)
+    assert moe.device_error() == 0
+    o = host(out)
+    if shard:
+        starts = np.concatenate([[0], np.cumsum(sizes)])
+        lo, hi = starts[g0], starts[g0 + El]
+        assert np.all(o[:lo] == 0) and np.all(o[hi:] == 0)
+    assert_close(o, ref, f"gmm_ksplit M={M} K={K} N={N} K_split={K_split}")
+
+
 def test_gmm_bad_group_sizes_sets_device_error():
     M, K, N = 64, 128, 256
     a = np.zeros((M, K), np.uint8)
