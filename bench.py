@@ -539,21 +539,21 @@ def run_suite(args):
                 ("bwd ragged_gather_reduce dX", lambda: moe.ragged_gather_reduce(buf.dXs, buf.sort["pos"], None, k,
                                                                                  out=buf.dX),
                  "hbm", 2 * R * D + 2 * T * D + 4 * R),
-                ("bwd moe_quantize_group_cols dA", lambda: moe.quantize_group_cols(dA, sizes),
-                 "hbm", 3 * R * 2 * F),
-                ("bwd moe_quantize_group_cols dO", lambda: moe.quantize_group_cols(dO, sizes),
-                 "hbm", 3 * R * D),
+                ("bwd moe_quantize_group_cols dA (scales)",
+                 lambda: moe.quantize_group_cols(dA, sizes, scales_only=True), "hbm", 2 * R * 2 * F),
+                ("bwd moe_quantize_group_cols dO (scales)",
+                 lambda: moe.quantize_group_cols(dO, sizes, scales_only=True), "hbm", 2 * R * D),
             ]
-            dAg_q, dAg_s = moe.quantize_group_cols(dA, sizes)
-            dOg_q, dOg_s = moe.quantize_group_cols(dO, sizes)
+            _, dAg_s = moe.quantize_group_cols(dA, sizes, scales_only=True)
+            _, dOg_s = moe.quantize_group_cols(dO, sizes, scales_only=True)
             ws = torch.empty(moe.lib().tgmm_fp8_workspace_bytes(R, D, 2 * F, E), dtype=torch.uint8, device=dev)
             calls += [
-                ("bwd tgmm_fp8 dW_in (incl. operand transposes)",
-                 lambda: moe.tgmm(buf.sort["xs_q"], sx, 2, dAg_q, dAg_s, 3, sizes, workspace=ws),
-                 "tensor", (2.0 * R * D * 2 * F, 4 * E * D * 2 * F + R * D + R * 2 * F)),
-                ("bwd tgmm_fp8 dW_out (incl. operand transposes)",
-                 lambda: moe.tgmm(buf.h_q, sh, 2, dOg_q, dOg_s, 3, sizes, workspace=ws),
-                 "tensor", (2.0 * R * F * D, 4 * E * F * D + R * F + R * D)),
+                ("bwd tgmm_fp8_gcq dW_in (with the operand layouts)",
+                 lambda: moe.tgmm_gcq(buf.sort["xs_q"], sx, 2, dA, dAg_s, sizes, workspace=ws),
+                 "tensor", (2.0 * R * D * 2 * F, 4 * E * D * 2 * F + R * D + 2 * R * 2 * F)),
+                ("bwd tgmm_fp8_gcq dW_out (with the operand layouts)",
+                 lambda: moe.tgmm_gcq(buf.h_q, sh, 2, dO, dOg_s, sizes, workspace=ws),
+                 "tensor", (2.0 * R * F * D, 4 * E * F * D + R * F + 2 * R * D)),
             ]
         total = 0.0
         for label, fn, bound, work in calls:

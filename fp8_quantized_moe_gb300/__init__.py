@@ -258,11 +258,13 @@ def swiglu_bwd_quant(dH: torch.Tensor, a: torch.Tensor):
 
 
 def quantize_group_cols(g: torch.Tensor, group_sizes: torch.Tensor, group_offset: int = 0,
-                        E_local: Optional[int] = None):
+                        E_local: Optional[int] = None, scales_only: bool = False):
+    """Per-(expert, column) e4m3 codes and scales of g; (None, scales) with scales_only."""
     M, N = g.shape
     E = group_sizes.numel()
     E_local = E - group_offset if E_local is None else E_local
-    q = torch.empty(M, N, dtype=torch.uint8, device=g.device)  # rows of other experts stay unwritten
+    # rows of other experts stay unwritten
+    q = None if scales_only else torch.empty(M, N, dtype=torch.uint8, device=g.device)
     s = torch.empty(E_local, N, dtype=torch.float32, device=g.device)
     check(lib().moe_quantize_group_cols(_p(g), M, N, _p(group_sizes), E, group_offset, E_local, _p(q), _p(s), _s()),
           "moe_quantize_group_cols")
@@ -284,6 +286,26 @@ def tgmm(lhs_q, lhs_scale, lhs_mode, rhs_q, rhs_scale, rhs_mode, group_sizes, gr
         workspace = torch.empty(nws, dtype=torch.uint8, device=lhs_q.device)
     check(lib().tgmm_fp8(_p(lhs_q), _p(lhs_scale), lhs_mode, _p(rhs_q), _p(rhs_scale), rhs_mode, _p(group_sizes), E,
                          group_offset, E_local, M, K, N, _p(out), _p(workspace), workspace.numel(), _s()), "tgmm_fp8")
+    return out
+
+
+def tgmm_gcq(lhs_q, lhs_scale, lhs_mode, rhs_g, rhs_scale, group_sizes, group_offset: int = 0,
+             E_local: Optional[int] = None, out=None, workspace=None):
+    """tgmm with the rhs as a bf16 gradient and its per-(expert, column) scales
+    -> fp32 [E_local, K, N] (the codes are made in the contraction's layout)."""
+    M, K = lhs_q.shape
+    M2, N = rhs_g.shape
+    if M2 != M:
+        raise MoEError("lhs/rhs M mismatch")
+    E = group_sizes.numel()
+    E_local = E - group_offset if E_local is None else E_local
+    out = torch.empty(E_local, K, N, dtype=torch.float32, device=lhs_q.device) if out is None else out
+    nws = lib().tgmm_fp8_workspace_bytes(M, K, N, E_local)
+    if workspace is None or workspace.numel() < nws:
+        workspace = torch.empty(nws, dtype=torch.uint8, device=lhs_q.device)
+    check(lib().tgmm_fp8_gcq(_p(lhs_q), _p(lhs_scale), lhs_mode, _p(rhs_g), _p(rhs_scale), _p(group_sizes), E,
+                             group_offset, E_local, M, K, N, _p(out), _p(workspace), workspace.numel(), _s()),
+          "tgmm_fp8_gcq")
     return out
 
 
@@ -426,8 +448,9 @@ def ffn_backward(dY: torch.Tensor, topk_w: torch.Tensor, W: ExpertWeights, buf: 
     # dXs = dA0 W0^T + dA1 W1^T: one contraction over [dA0 | dA1], one static scale per K half
     gmm_ksplit(dA_q, dA_s, PER_ROW, W.w_in_t, W.s_in_split, buf.F, s["group_sizes"], out=buf.dXs)
     ragged_gather_reduce(buf.dXs, s["pos"], None, k, out=buf.dX)
-    dAg_q, dAg_s = quantize_group_cols(dA, s["group_sizes"])
-    dOg_q, dOg_s = quantize_group_cols(dO, s["group_sizes"])
-    dW_in = tgmm(s["xs_q"], static_x, PER_TENSOR, dAg_q, dAg_s, PER_GROUP_COL, s["group_sizes"])
-    dW_out = tgmm(buf.h_q, static_h, PER_TENSOR, dOg_q, dOg_s, PER_GROUP_COL, s["group_sizes"])
+    # per-(expert, column) gradient scales; their codes are made inside the weight-gradient contractions
+    _, dAg_s = quantize_group_cols(dA, s["group_sizes"], scales_only=True)
+    _, dOg_s = quantize_group_cols(dO, s["group_sizes"], scales_only=True)
+    dW_in = tgmm_gcq(s["xs_q"], static_x, PER_TENSOR, dA, dAg_s, s["group_sizes"])
+    dW_out = tgmm_gcq(buf.h_q, static_h, PER_TENSOR, dO, dOg_s, s["group_sizes"])
     return buf.dX, dW_in, dW_out

@@ -37,6 +37,7 @@ SIGNATURES = {
     "moe_quantize_group_cols": ([P, i64, i64, P, i32, i32, i32, P, P, P], i32),
     "tgmm_fp8_workspace_bytes": ([i64, i64, i64, i32], sz),
     "tgmm_fp8": ([P, P, i32, P, P, i32, P, i32, i32, i32, i64, i64, i64, P, P, sz, P], i32),
+    "tgmm_fp8_gcq": ([P, P, i32, P, P, P, i32, i32, i32, i64, i64, i64, P, P, sz, P], i32),
     "moe_transpose_u8": ([P, i64, i64, i64, P, P], i32),
     "gmm_fp8_swiglu": ([P, P, i32, P, P, i32, P, i32, i32, i32, i64, i64, i64, i32, P, P, P, P, P, P], i32),
     "moe_ragged_sort_noalloc": ([P, i64, i32, i32, P, P, i64, i32, P, P, P, P, P, P, P], i32),

@@ -1154,6 +1154,122 @@ __global__ void __launch_bounds__(256) transpose_pad_kernel(const uint8_t* src, 
   }
 }
 
+// g bf16 [M, C] -> dst [C, Mp]: the per-(group, column) e4m3 codes of g
+// (finished scales `scale` [El, C]) written straight into the transposed,
+// group-padded layout that the tgmm contraction reads; the same tiles,
+// swizzle and byte-permute transpose as transpose_pad_kernel, with the
+// quantisation of moe_quantize_group_cols in between (bit-identical codes).
+// A 128-row tile of the padded layout lies inside one group, so a thread's
+// eight column scales are loaded once per tile.
+__global__ void __launch_bounds__(256) quant_transpose_pad_kernel(const uint16_t* g, int64_t M, int64_t C,
+                                                                  const float* scale, uint8_t* dst, int64_t Mp,
+                                                                  const int32_t* sizes, int E, int g0, int El) {
+  __shared__ int starts[kMaxGroups + 1];
+  __shared__ int pst[kMaxGroups + 1];
+  __shared__ __align__(16) uint32_t tile[kTpTile][kTpTile / 4];
+  group_starts_smem(sizes, E, starts);
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    for (int c = 0; c < El; c += 32) {
+      const int el = c + lane;
+      const int sz = el < El ? starts[g0 + el + 1] - starts[g0 + el] : 0;
+      const int v = ((sz + 127) / 128) * 128;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (el < El) pst[el] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) pst[El] = carry;
+  }
+  __syncthreads();
+  const int64_t rows_out = min(static_cast<int64_t>(pst[El]), Mp);
+  const int64_t ntc = (C + kTpTile - 1) / kTpTile;
+  const int64_t ntiles = (rows_out / kTpTile) * ntc;
+  const int tid = threadIdx.x;
+  const int lrow = tid >> 4, unit = tid & 15;  // load: rows lrow + 16 i, 8 columns 8 unit .. 8 unit + 7
+  const int rg = tid & 7, cw = tid >> 3;       // transpose: as transpose_pad_kernel
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t jb = (t / ntc) * kTpTile, cb = (t % ntc) * kTpTile;
+    // the tile's group (every row of a 128-row padded tile belongs to it)
+    int lo = 0, hi = El;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (pst[mid] <= jb) lo = mid; else hi = mid;
+    }
+    while (lo + 1 < El && pst[lo + 1] <= jb) ++lo;
+    const int64_t sz = starts[g0 + lo + 1] - starts[g0 + lo];
+    const int64_t c0 = cb + 8 * unit;
+    float sc[8], inv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      sc[j] = (c0 + j < C) ? __ldg(scale + static_cast<int64_t>(lo) * C + c0 + j) : 1.0f;
+      inv[j] = __frcp_rn(sc[j]);
+    }
+    uint4 d[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int64_t off = jb + lrow + 16 * i - pst[lo];
+      d[i] = make_uint4(0, 0, 0, 0);
+      if (off < sz && c0 < C) {
+        const int64_t m = starts[g0 + lo] + off;
+        if (m < M) d[i] = __ldg(reinterpret_cast<const uint4*>(g + m * C + c0));
+      }
+    }
+    __syncthreads();  // the previous tile's transposing reads are done
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = lrow + 16 * i;
+      const uint32_t w[4] = {d[i].x, d[i].y, d[i].z, d[i].w};
+      float v[8], y[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[2 * j] = bf16lo(w[j]);
+        v[2 * j + 1] = bf16hi(w[j]);
+      }
+      bool slow = false;
+#pragma unroll
+      for (int j = 0; j < 8; j += 2) {  // products in pairs (packed fp32, one rounding each)
+        f2_unpack(f2_mul(f2_pack(v[j], v[j + 1]), f2_pack(inv[j], inv[j + 1])), y[j], y[j + 1]);
+        slow = slow || quant_needs_division(y[j]) || quant_needs_division(y[j + 1]);
+      }
+      if (slow) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (quant_needs_division(y[j])) y[j] = __fdiv_rn(v[j], sc[j]);
+      }
+      const uint2 code = pack_e4m3x8(y);  // zero rows (padding) give zero codes
+      // 8 bytes: half of 16-byte unit (unit >> 1), swizzled by 16-row group
+      *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(&tile[r][0]) + 16 * ((unit >> 1) ^ ((r >> 4) & 7)) +
+                                8 * (unit & 1)) = code;
+    }
+    __syncthreads();
+    const int wsw = (cw & 3) | (((cw >> 2) ^ rg) << 2);
+    uint32_t o[4][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = 16 * rg + 4 * q;
+      const uint32_t r0 = tile[r][wsw], r1 = tile[r + 1][wsw], r2 = tile[r + 2][wsw], r3 = tile[r + 3][wsw];
+      const uint32_t t0 = __byte_perm(r0, r1, 0x5140), t1 = __byte_perm(r2, r3, 0x5140);
+      const uint32_t t2 = __byte_perm(r0, r1, 0x7362), t3 = __byte_perm(r2, r3, 0x7362);
+      o[0][q] = __byte_perm(t0, t1, 0x5410);
+      o[1][q] = __byte_perm(t0, t1, 0x7632);
+      o[2][q] = __byte_perm(t2, t3, 0x5410);
+      o[3][q] = __byte_perm(t2, t3, 0x7632);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t c = cb + 4 * cw + k;
+      if (c < C)
+        *reinterpret_cast<uint4*>(dst + c * Mp + jb + 16 * rg) = make_uint4(o[k][0], o[k][1], o[k][2], o[k][3]);
+    }
+  }
+}
+
 // ---- fused SwiGLU: rows outside the local groups, per-row second phase ----
 
 // Rows outside groups [g0, g0 + El) of a fused SwiGLU call get zero codes and
@@ -1534,26 +1650,16 @@ extern "C" size_t tgmm_fp8_workspace_bytes(int64_t M, int64_t K, int64_t N, int 
   return align256(static_cast<size_t>(K * Mp)) + align256(static_cast<size_t>(N * Mp));
 }
 
-extern "C" moe_status tgmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode,
-                               const uint8_t* rhs_q, const float* rhs_scale, moe_scale_mode rhs_mode,
-                               const int32_t* group_sizes, int E, int group_offset, int E_local, int64_t M,
-                               int64_t K, int64_t N, float* out, void* workspace, size_t workspace_bytes,
-                               moe_stream_t stream) {
-  MOE_HOST_CHECK(lhs_q && lhs_scale && rhs_q && rhs_scale && group_sizes && out && workspace, MOE_ERR_INVALID_ARG);
-  MOE_HOST_CHECK((lhs_mode == MOE_SCALE_PER_TENSOR || lhs_mode == MOE_SCALE_PER_GROUP_COL) &&
-                     (rhs_mode == MOE_SCALE_PER_TENSOR || rhs_mode == MOE_SCALE_PER_GROUP_COL),
-                 MOE_ERR_INVALID_ARG);
-  MOE_HOST_CHECK(E > 0 && E <= kMaxGroups && group_offset >= 0 && E_local > 0 && group_offset + E_local <= E,
-                 MOE_ERR_INVALID_ARG);
-  MOE_HOST_CHECK(M >= 0 && M < (1ll << 30) && K > 0 && K % 16 == 0 && K < (1 << 30) && N > 0 && N % 16 == 0 &&
-                     N < (1 << 30),
-                 MOE_ERR_INVALID_ARG);
-  MOE_HOST_CHECK(aligned16(lhs_q) && aligned16(rhs_q) && aligned16(out) && aligned16(workspace),
-                 MOE_ERR_INVALID_ARG);
-  MOE_HOST_CHECK(rhs_mode == MOE_SCALE_PER_TENSOR || aligned16(rhs_scale), MOE_ERR_INVALID_ARG);
-  MOE_HOST_CHECK(workspace_bytes >= tgmm_fp8_workspace_bytes(M, K, N, E_local), MOE_ERR_INVALID_ARG);
-  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
-  cudaStream_t st = as_stream(stream);
+namespace moe {
+namespace {
+// tgmm_fp8 and tgmm_fp8_gcq: lay the rhs out (transposed and group-padded in
+// the workspace) with `rhs_layout`, the lhs likewise from its codes, then
+// contract over the padded rows.
+template <class RhsLayout>
+moe_status tgmm_run(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode, const float* rhs_scale,
+                    moe_scale_mode rhs_mode, const int32_t* group_sizes, int E, int group_offset, int E_local,
+                    int64_t M, int64_t K, int64_t N, float* out, void* workspace, cudaStream_t st,
+                    RhsLayout rhs_layout) {
   const int64_t Mp = padded_rows(M, E_local);
   uint8_t* lhsT = static_cast<uint8_t*>(workspace);
   uint8_t* rhsT = lhsT + align256(static_cast<size_t>(K * Mp));
@@ -1561,7 +1667,7 @@ extern "C" moe_status tgmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe
     const int grid = sm_count() * 8;
     transpose_pad_kernel<<<grid, 256, 0, st>>>(lhs_q, M, K, lhsT, Mp, group_sizes, E, group_offset, E_local);
     MOE_CUDA_TRY(cudaGetLastError());
-    transpose_pad_kernel<<<grid, 256, 0, st>>>(rhs_q, M, N, rhsT, Mp, group_sizes, E, group_offset, E_local);
+    rhs_layout(rhsT, Mp, grid);
     MOE_CUDA_TRY(cudaGetLastError());
   }
   CUtensorMap A, B;
@@ -1588,4 +1694,50 @@ extern "C" moe_status tgmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe
   CUtensorMap O;
   if (!make_map_out_f32(&O, out, N, K, E_local)) return MOE_ERR_CUDA;
   return launch_mma<kTgmm, false>(A, B, O, p, static_cast<int>(tiles > (1 << 30) ? (1 << 30) : tiles), st);
+}
+
+#define MOE_TGMM_COMMON_CHECKS()                                                                               \
+  MOE_HOST_CHECK((lhs_mode == MOE_SCALE_PER_TENSOR || lhs_mode == MOE_SCALE_PER_GROUP_COL), MOE_ERR_INVALID_ARG); \
+  MOE_HOST_CHECK(E > 0 && E <= kMaxGroups && group_offset >= 0 && E_local > 0 && group_offset + E_local <= E,   \
+                 MOE_ERR_INVALID_ARG);                                                                         \
+  MOE_HOST_CHECK(M >= 0 && M < (1ll << 30) && K > 0 && K % 16 == 0 && K < (1 << 30) && N > 0 && N % 16 == 0 &&  \
+                     N < (1 << 30),                                                                            \
+                 MOE_ERR_INVALID_ARG);                                                                         \
+  MOE_HOST_CHECK(aligned16(lhs_q) && aligned16(out) && aligned16(workspace), MOE_ERR_INVALID_ARG);             \
+  MOE_HOST_CHECK(workspace_bytes >= tgmm_fp8_workspace_bytes(M, K, N, E_local), MOE_ERR_INVALID_ARG)
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status tgmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode,
+                               const uint8_t* rhs_q, const float* rhs_scale, moe_scale_mode rhs_mode,
+                               const int32_t* group_sizes, int E, int group_offset, int E_local, int64_t M,
+                               int64_t K, int64_t N, float* out, void* workspace, size_t workspace_bytes,
+                               moe_stream_t stream) {
+  MOE_HOST_CHECK(lhs_q && lhs_scale && rhs_q && rhs_scale && group_sizes && out && workspace, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(rhs_mode == MOE_SCALE_PER_TENSOR || rhs_mode == MOE_SCALE_PER_GROUP_COL, MOE_ERR_INVALID_ARG);
+  MOE_TGMM_COMMON_CHECKS();
+  MOE_HOST_CHECK(aligned16(rhs_q) && (rhs_mode == MOE_SCALE_PER_TENSOR || aligned16(rhs_scale)), MOE_ERR_INVALID_ARG);
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = as_stream(stream);
+  return tgmm_run(lhs_q, lhs_scale, lhs_mode, rhs_scale, rhs_mode, group_sizes, E, group_offset, E_local, M, K, N,
+                  out, workspace, st, [&](uint8_t* rhsT, int64_t Mp, int grid) {
+                    transpose_pad_kernel<<<grid, 256, 0, st>>>(rhs_q, M, N, rhsT, Mp, group_sizes, E, group_offset,
+                                                               E_local);
+                  });
+}
+
+extern "C" moe_status tgmm_fp8_gcq(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode,
+                                   const uint16_t* rhs_g, const float* rhs_scale, const int32_t* group_sizes, int E,
+                                   int group_offset, int E_local, int64_t M, int64_t K, int64_t N, float* out,
+                                   void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  MOE_HOST_CHECK(lhs_q && lhs_scale && rhs_g && rhs_scale && group_sizes && out && workspace, MOE_ERR_INVALID_ARG);
+  MOE_TGMM_COMMON_CHECKS();
+  MOE_HOST_CHECK(aligned16(rhs_g) && aligned16(rhs_scale), MOE_ERR_INVALID_ARG);
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = as_stream(stream);
+  return tgmm_run(lhs_q, lhs_scale, lhs_mode, rhs_scale, MOE_SCALE_PER_GROUP_COL, group_sizes, E, group_offset,
+                  E_local, M, K, N, out, workspace, st, [&](uint8_t* rhsT, int64_t Mp, int grid) {
+                    quant_transpose_pad_kernel<<<grid, 256, 0, st>>>(rhs_g, M, N, rhs_scale, rhsT, Mp, group_sizes,
+                                                                     E, group_offset, E_local);
+                  });
 }

@@ -553,10 +553,10 @@ extern "C" moe_status moe_swiglu_bwd_quant(const uint16_t* dH, const uint16_t* a
 extern "C" moe_status moe_quantize_group_cols(const uint16_t* g, int64_t M, int64_t N, const int32_t* group_sizes,
                                               int E, int group_offset, int E_local, uint8_t* q, float* scale,
                                               moe_stream_t stream) {
-  MOE_HOST_CHECK(g && group_sizes && q && scale && M >= 0 && N > 0 && N % 16 == 0, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(g && group_sizes && scale && M >= 0 && N > 0 && N % 16 == 0, MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(E > 0 && E <= kMaxGroups && group_offset >= 0 && E_local > 0 && group_offset + E_local <= E,
                  MOE_ERR_INVALID_ARG);
-  MOE_HOST_CHECK(aligned16(g) && aligned16(q) && aligned16(scale), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(aligned16(g) && (q == nullptr || aligned16(q)) && aligned16(scale), MOE_ERR_INVALID_ARG);
   cudaStream_t st = as_stream(stream);
   const int64_t ns = static_cast<int64_t>(E_local) * N;
   MOE_CUDA_TRY(cudaMemsetAsync(scale, 0, sizeof(float) * ns, st));
@@ -567,7 +567,7 @@ extern "C" moe_status moe_quantize_group_cols(const uint16_t* g, int64_t M, int6
   }
   finalize_scales_kernel<<<static_cast<unsigned>((ns + 255) / 256), 256, 0, st>>>(scale, ns);
   MOE_CUDA_TRY(cudaGetLastError());
-  if (M > 0) {
+  if (M > 0 && q != nullptr) {  // q == NULL: the scales only (tgmm_fp8_gcq makes the codes)
     dim3 grid(static_cast<unsigned>((N / 8 + 31) / 32), static_cast<unsigned>((M + kGcRows - 1) / kGcRows));
     group_cols_kernel<true><<<grid, 256, 0, st>>>(g, M, N, group_sizes, E, group_offset, E_local, q, scale);
     MOE_CUDA_TRY(cudaGetLastError());

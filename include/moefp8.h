@@ -300,9 +300,10 @@ moe_status moe_swiglu_bwd_quant(const uint16_t* dH, const uint16_t* a, int64_t R
  * (expert, column) over that expert's rows, so that both scales of the
  * weight-gradient contraction factor out of the sum over rows.
  * g bf16 [M, N]; q e4m3 [M, N] (rows outside the local groups are not
- * written); scale fp32 [E_local, N] (an expert without rows, or an all-zero
- * column, gets 1).  N % 16 == 0, E <= 1024.  `scale` is also used as the
- * running maximum while the kernel runs. */
+ * written), or NULL for the scales only (tgmm_fp8_gcq then makes the codes);
+ * scale fp32 [E_local, N] (an expert without rows, or an all-zero column,
+ * gets 1).  N % 16 == 0, E <= 1024.  `scale` is also used as the running
+ * maximum while the kernel runs. */
 moe_status moe_quantize_group_cols(const uint16_t* g, int64_t M, int64_t N, const int32_t* group_sizes, int E,
                                    int group_offset, int E_local, uint8_t* q, float* scale, moe_stream_t stream);
 
@@ -323,6 +324,17 @@ moe_status tgmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode
                     const float* rhs_scale, moe_scale_mode rhs_mode, const int32_t* group_sizes, int E,
                     int group_offset, int E_local, int64_t M, int64_t K, int64_t N, float* out, void* workspace,
                     size_t workspace_bytes, moe_stream_t stream);
+
+/* tgmm_fp8_gcq -- tgmm_fp8 whose rhs is given as the bf16 gradient g [M, N]
+ * with its finished per-(expert, column) scales (moe_quantize_group_cols with
+ * q == NULL): the e4m3 codes of g are made while g is laid out transposed and
+ * group-padded in the workspace, so the row-major codes never go to memory.
+ * The codes, and so the result, are those of moe_quantize_group_cols followed
+ * by tgmm_fp8 with rhs_mode PER_GROUP_COL.  Other arguments as tgmm_fp8. */
+moe_status tgmm_fp8_gcq(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode, const uint16_t* rhs_g,
+                        const float* rhs_scale, const int32_t* group_sizes, int E, int group_offset, int E_local,
+                        int64_t M, int64_t K, int64_t N, float* out, void* workspace, size_t workspace_bytes,
+                        moe_stream_t stream);
 
 /* moe_transpose_u8 -- weight layout preparation for the backward pass (run
  * once, outside the FFN): batched byte transpose src [B, R, C] -> dst

@@ -154,6 +154,30 @@ def test_tgmm_matches_oracle(M, K, N, E, lmode, rmode):
     assert_close(o, ref, f"tgmm M={M} K={K} N={N} E={E}")
 
 
+@pytest.mark.parametrize("M,K,N,E,g0,El", [
+    (1000, 384, 256, 9, 0, 9),
+    (2000, 128, 2816, 16, 0, 16),
+    (700, 256, 272, 6, 1, 4),          # shard, N not a multiple of 128
+    (1, 128, 128, 1, 0, 1),
+])
+def test_tgmm_gcq_equals_quantize_then_tgmm(M, K, N, E, g0, El):
+    """Codes made in the transposed layout: the same result, bit for bit, as
+    moe_quantize_group_cols followed by tgmm_fp8."""
+    rng = np.random.default_rng(M + K + N + El)
+    sizes = ragged_sizes(rng, E, M)
+    x = rand_codes(rng, (M, K))
+    g = oracle.bf16_bits(torch.from_numpy((rng.standard_normal((M, N)) * np.exp(rng.uniform(-3, 3, (1, N)))
+                                           ).astype(np.float32)).to(torch.bfloat16))
+    sx = np.array([0.01], np.float32)
+    gq, gs = moe.quantize_group_cols(dev(g), dev(sizes), g0, El)
+    ref = moe.tgmm(dev(x), dev(sx), RT, gq, gs, GC, dev(sizes), group_offset=g0, E_local=El)
+    _, gs2 = moe.quantize_group_cols(dev(g), dev(sizes), g0, El, scales_only=True)
+    out = moe.tgmm_gcq(dev(x), dev(sx), RT, dev(g), gs2, dev(sizes), group_offset=g0, E_local=El)
+    assert moe.device_error() == 0
+    assert torch.equal(gs, gs2)
+    assert torch.equal(out, ref)
+
+
 # ---- gmm_fp8_swiglu: steps 3 + 4 fused, bit-identical to gmm_fp8 + moe_swiglu_quant
 
 @pytest.mark.parametrize("M,K,F,E,amode,wmode,hmode,shard", [
