@@ -97,8 +97,11 @@ struct SmemCtl {
   int gstart[kMaxGroups + 1];       // gmm: first row of local group; tgmm: padded first row
   int tile_prefix[kMaxGroups + 1];  // gmm: first tile of local group
   int gsize[kMaxGroups];
-  alignas(16) float sw_stage[512];      // promotion: weight scales of the current K block, per warp
-  alignas(16) float pamax[2][4][2][32];  // fused SwiGLU, per-128 h scales: row maxima of the two column halves
+  // per-mode scratch (one mode per kernel)
+  union alignas(16) {
+    float sw_stage[1024];        // promotion: weight scales of the current K block, per warp
+    float pamax[2][4][2][32];    // fused SwiGLU, per-128 h scales: row maxima of the two column halves
+  };
 };
 // sw_stage is read and written with float2 / float4 accesses
 static_assert(offsetof(SmemCtl, sw_stage) % 16 == 0 && offsetof(SmemCtl, pamax) % 16 == 0, "SmemCtl alignment");
@@ -111,7 +114,9 @@ static_assert(sizeof(SmemCtl) % 16 == 0, "SmemCtl size");
 // SwiGLU gmm run on CTA pairs (a 2-CTA cluster): one 256x256 MMA per K step
 // over both CTAs, each CTA holding 128 rows of A and half of the B tile, so a
 // stage is 32 KB per CTA instead of 48 and the operand traffic through each
-// SM's shared memory drops by a third.
+// SM's shared memory drops by a third.  (Promotion on CTA pairs was measured
+// slower at every tile width: each K block's accumulator release then crosses
+// the pair.)
 #ifndef MOE_PROMOTE_BN
 #define MOE_PROMOTE_BN 128
 #endif
@@ -159,7 +164,8 @@ struct Cfg {
   static constexpr size_t CTL_BYTES = (sizeof(SmemCtl) + 1023) / 1024 * 1024;  // keeps the staging 1 KB aligned
   static constexpr size_t SMEM = 1024 + static_cast<size_t>(NSTAGE) * STAGE_BYTES + CTL_BYTES +
                                  static_cast<size_t>(EPI_WARPS) * STG_WARP_BYTES;
-  static_assert(NSTAGE <= kMaxStages && NACC >= 1 && NACC <= kMaxAcc && NACC * BN * SEGS == TMEM_COLS,
+  static_assert(NSTAGE <= kMaxStages && NACC >= 1 && NACC <= kMaxAcc && NACC * BN * SEGS <= TMEM_COLS &&
+                    STAGE_BYTES % 1024 == 0 && BN % 32 == 0,
                 "tile configuration");
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
@@ -243,7 +249,7 @@ struct Tile {
 template <int MODE, bool PAIR>
 __device__ __forceinline__ Tile get_tile(const Params& p, const SmemCtl* ctl, int t, int rank) {
   Tile tl;
-  constexpr int BN = Cfg<MODE>::BN;
+  constexpr int BN = Cfg<MODE, PAIR>::BN;
   if (MODE == kTgmm) {
     const int per = p.ktiles * p.ntiles;
     tl.el = t / per;
@@ -835,8 +841,8 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         ++acc;
       } else {
         // promotion: one fresh accumulator per K block, folded into registers.
-        // Eight warps: TMEM lane quarter q4, columns [half*64, half*64 + 64)
-        // of the 128-column tile.  Only the blockwise side(s) enter the
+        // Eight warps: TMEM lane quarter q4, columns [half*WC, half*WC + WC)
+        // of the tile (WC = BN / 2).  Only the blockwise side(s) enter the
         // per-block update; a scale constant along K is applied at the end.
         uint16_t* out = static_cast<uint16_t*>(p.out);
         const int64_t row = static_cast<int64_t>(tl.row0) + r;
@@ -854,22 +860,18 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
 #pragma unroll
         for (int j = 0; j < WC / 2; ++j) acc2[j] = 0ull;
         // The scales of a K block are loaded PD blocks ahead (a register
-        // ring), so their memory latency stays off the per-block path.
-        constexpr int PD = 4;
-        constexpr int SPL = WC / 32;        // staged column scales per lane
-        const int nw = cbase + SPL * lane;  // this lane's first staged column
+        // ring), so their memory latency stays off the per-block path.  The
+        // first WC/SPL lanes load SPL columns each (N and the tile's columns
+        // are multiples of 16, so a lane's columns are all in range or all
+        // past N).
+        constexpr int SPL = WC == 32 ? 1 : (WC == 64 ? 2 : 4);  // staged column scales per lane
+        constexpr int PD = WC > 64 ? 2 : 4;  // wide spans: the folded sums leave fewer registers
+        const int nw = cbase + SPL * lane;   // this lane's first staged column
+        const bool w_lane = w_blk && SPL * lane < WC && nw < p.N;
         using WVec = typename std::conditional<SPL == 1, float, typename std::conditional<SPL == 2, float2, float4>::type>::type;
         auto load_w = [&](int kb) -> WVec {
           WVec w{};
-          if (w_blk && kb < tl.nkb) {
-            const float* src = swb + static_cast<int64_t>(kb) * p.N + nw;
-            if (nw + SPL - 1 < p.N) {
-              w = __ldg(reinterpret_cast<const WVec*>(src));
-            } else {
-              float* wf = reinterpret_cast<float*>(&w);
-              for (int i = 0; i < SPL; ++i) wf[i] = nw + i < p.N ? __ldg(src + i) : 0.f;
-            }
-          }
+          if (w_lane && kb < tl.nkb) w = __ldg(reinterpret_cast<const WVec*>(swb + static_cast<int64_t>(kb) * p.N + nw));
           return w;
         };
         auto load_a = [&](int kb) -> float { return (a_blk && kb < tl.nkb) ? __ldg(sab + kb) : 1.0f; };
@@ -891,7 +893,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
           const float sa = aq[i];
           wq[i] = load_w(kb + PD);
           aq[i] = load_a(kb + PD);
-          if (w_blk) *reinterpret_cast<WVec*>(stage + SPL * lane) = w2;
+          if (w_blk && SPL * lane < WC) *reinterpret_cast<WVec*>(stage + SPL * lane) = w2;
           const uint64_t sa2 = f2_pack(sa, sa);
           __syncwarp();
           const uint32_t a = acc % NACC;
@@ -944,7 +946,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
 #pragma unroll
             for (int c = 0; c < WC / 16; ++c) fold16(v + 16 * c, 16 * c);
           } else {
-            // 128 columns: fold 16 at a time, release after the last load
+            // wider spans: fold 16 columns at a time, release after the last load
 #pragma unroll
             for (int c = 0; c < WC / 16; ++c) {
               uint32_t v[16];
@@ -968,26 +970,24 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
           const bool w_col = p.rhs_mode == MOE_SCALE_PER_ROW;
           const float sw_t = (w_blk || w_col) ? 1.0f : __ldg(p.rhs_scale);
 #pragma unroll
-          for (int c = 0; c < WC / 32; ++c) {
-            const int nb = cbase + c * 32;
+          for (int c = 0; c < WC / 16; ++c) {
+            const int nb = cbase + c * 16;  // N is a multiple of 16: the 16 columns are all in range or all past N
             if (nb < p.N) {
-              uint32_t pk[16];
+              uint32_t pk[8];
 #pragma unroll
-              for (int g = 0; g < 8; ++g) {  // columns nb + 4g .. nb + 4g + 3
+              for (int g = 0; g < 4; ++g) {  // columns nb + 4g .. nb + 4g + 3
                 float4 w4 = make_float4(sw_t, sw_t, sw_t, sw_t);
-                if (w_col && nb + 4 * g + 3 < p.N) w4 = __ldg(reinterpret_cast<const float4*>(swb + nb) + g);
+                if (w_col) w4 = __ldg(reinterpret_cast<const float4*>(swb + nb) + g);
                 float f0, f1, f2, f3;
-                f2_unpack(acc2[c * 16 + 2 * g], f0, f1);
-                f2_unpack(acc2[c * 16 + 2 * g + 1], f2, f3);
+                f2_unpack(acc2[c * 8 + 2 * g], f0, f1);
+                f2_unpack(acc2[c * 8 + 2 * g + 1], f2, f3);
                 pk[2 * g] = pack_bf16x2(__fmul_rn(__fmul_rn(f0, sa_end), w4.x), __fmul_rn(__fmul_rn(f1, sa_end), w4.y));
                 pk[2 * g + 1] =
                     pack_bf16x2(__fmul_rn(__fmul_rn(f2, sa_end), w4.z), __fmul_rn(__fmul_rn(f3, sa_end), w4.w));
               }
               uint16_t* dst = out + row * p.N + nb;
-#pragma unroll
-              for (int g = 0; g < 4; ++g)
-                if (g * 8 < p.N - nb)
-                  *reinterpret_cast<uint4*>(dst + g * 8) = make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+              *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              *reinterpret_cast<uint4*>(dst + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
           }
         }
@@ -1496,13 +1496,12 @@ extern "C" moe_status gmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_
   }
   CUtensorMap A, B;
   if (!make_map(&A, lhs_q, K, M, K, BM)) return MOE_ERR_CUDA;
-  const int bn = blockwise ? Cfg<kPromote>::BN : Cfg<kFinal>::BN;
   // CTA pairs pay off once the K loop is long enough to amortise the pair's
   // coupling (measured: slower at K <= 2048, 7-9% faster at K = 4096, 14336)
-  const bool pair = !blockwise && K >= kPairMinK;
+  const bool pair = !blockwise && Cfg<kFinal, true>::PAIR && K >= kPairMinK;
+  const int bn = blockwise ? Cfg<kPromote>::BN : Cfg<kFinal>::BN;
   // B box: one tile of N rows, or this CTA's half of it on a CTA pair
-  const uint32_t b_box = blockwise ? Cfg<kPromote>::BN
-                                   : (Cfg<kFinal, true>::PAIR && pair ? Cfg<kFinal>::BN / 2 : Cfg<kFinal>::BN);
+  const uint32_t b_box = pair ? bn / 2 : bn;
   if (!make_map(&B, rhs_q, K, static_cast<uint64_t>(E_local) * N, K, b_box)) return MOE_ERR_CUDA;
   Params p{};
   p.group_sizes = group_sizes;
