@@ -547,33 +547,45 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
       if (MODE == kTgmm) {
         float* out = static_cast<float*>(p.out);
         const int64_t krow = tl.row0 + r;
-        float* orow = out + (static_cast<int64_t>(tl.el) * p.K + krow) * p.N;
         constexpr int WCOLS = BN / (EPI_WARPS / 4);  // columns of the tile this warp writes
         if (tl.nkb == 0) {
-          if (row_ok) {
-            for (int c = half * WCOLS; c < (half + 1) * WCOLS; c += 4)
-              if (tl.n0 + c < p.N) *reinterpret_cast<float4*>(orow + tl.n0 + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
+          // an expert with no rows: dW_e = 0; row by row, the warp's 32 lanes
+          // cover its WCOLS columns (4 each) with one coalesced store per row
+          static_assert(MODE != kTgmm || WCOLS == 128, "zero fill: 32 lanes x 4 columns");
+          const int cz = tl.n0 + half * WCOLS + 4 * lane;
+          float* zbase = out + (static_cast<int64_t>(tl.el) * p.K + tl.row0 + q4 * 32) * p.N + cz;
+          const int zrows = min(32, tl.rows - q4 * 32);
+          if (cz < p.N)
+            for (int i = 0; i < zrows; ++i)
+              *reinterpret_cast<float4*>(zbase + static_cast<int64_t>(i) * p.N) = make_float4(0.f, 0.f, 0.f, 0.f);
           continue;
         }
         const uint32_t a = acc % NACC;
-        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
-          timed_out = true;
-          break;
-        }
-        tc_fence_after();
+        // the scales are requested first, so that their loads are in flight
+        // while the accumulator is awaited; each block's column scales are
+        // loaded while the block before it is written out
         const float sx = row_ok ? group_col_scale(p.lhs_scale, p.lhs_mode, tl.el, static_cast<int>(krow), p.K) : 0.f;
         const bool per_col = p.rhs_mode == MOE_SCALE_PER_GROUP_COL;
         const float* sgb = p.rhs_scale + (per_col ? static_cast<int64_t>(tl.el) * p.N : 0);
         const float sg_t = per_col ? 0.f : __ldg(p.rhs_scale);
         const bool block_rows = tl.rows - q4 * 32 > 0;  // rows >= K are clipped by the store
-#pragma unroll 1
-        for (int c = half * (WCOLS / 32); c < (half + 1) * (WCOLS / 32); ++c) {
+        constexpr int NB = WCOLS / 32;  // 32-column blocks of this warp
+        const int cb0 = half * NB;
+        float sgr[2][32];
+        load_col_scales32(sgb, tl.n0 + cb0 * 32, p.N, per_col, sg_t, sgr[0]);
+        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          const int c = cb0 + i;
           const int nb = tl.n0 + c * 32;
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + c * 32, v);
-          float sg[32];
-          load_col_scales32(sgb, nb, p.N, per_col, sg_t, sg);
+          if (i + 1 < NB) load_col_scales32(sgb, nb + 32, p.N, per_col, sg_t, sgr[(i + 1) & 1]);
+          const float* sg = sgr[i & 1];
           tmem_wait_ld();
           // this warp's 32x32 block, staged in the swizzled box layout and
           // written by one TMA store; the staging buffers rotate
