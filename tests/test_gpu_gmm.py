@@ -154,6 +154,32 @@ def test_tgmm_matches_oracle(M, K, N, E, lmode, rmode):
     assert_close(o, ref, f"tgmm M={M} K={K} N={N} E={E}")
 
 
+@pytest.mark.parametrize("sizes,K,N,g0,El,rmode", [
+    ([3000, 0, 150, 1100, 40, 900, 260], 256, 512, 0, 7, GC),  # heavy groups (>= 8 K blocks) beside light, empty ones
+    ([200, 2500, 1300, 0, 90, 1200], 128, 272, 1, 4, RT),       # a shard of groups 1..4
+])
+def test_tgmm_heavy_and_light_groups(sizes, K, N, g0, El, rmode):
+    """Groups with many 128-row blocks and groups with few are scheduled as two
+    tile streams on separate CTAs; every expert's result must be unchanged."""
+    sizes = np.array(sizes, np.int32)
+    M = int(sizes.sum())
+    rng = np.random.default_rng(M + K + N)
+    x = rand_codes(rng, (M, K))
+    g = rand_codes(rng, (M, N))
+    sx = np.array([0.01], np.float32)
+    E = len(sizes)
+    sg_full = rng.uniform(0.5, 2, (E, N)).astype(np.float32) / 448 if rmode == GC else np.array([0.02], np.float32)
+    ref = oracle.tgmm(x, sx, RT, g, sg_full, rmode, sizes)[g0:g0 + El]
+    sg = sg_full[g0:g0 + El] if rmode == GC else sg_full
+    out = moe.tgmm(dev(x), dev(sx), RT, dev(g), dev(np.ascontiguousarray(sg)), rmode, dev(sizes), group_offset=g0,
+                   E_local=El)
+    assert moe.device_error() == 0
+    o = host(out)
+    for e in np.flatnonzero(sizes[g0:g0 + El] == 0):
+        assert np.all(o[e] == 0)
+    assert_close(o, ref, f"tgmm heavy/light {sizes.tolist()} shard {g0}+{El}")
+
+
 @pytest.mark.parametrize("M,K,N,E,g0,El", [
     (1000, 384, 256, 9, 0, 9),
     (2000, 128, 2816, 16, 0, 16),
