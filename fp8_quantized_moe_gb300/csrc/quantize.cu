@@ -67,36 +67,45 @@ struct ScaleOut {
 struct RowsOp {  // plain bf16 rows
   __device__ __forceinline__ int ndst() const { return 1; }
   __device__ __forceinline__ int64_t dst(int64_t row, int) const { return row; }
-  static constexpr int U = 1;
+  static constexpr int U = 2;
+  static constexpr bool kWide = true;
   const uint16_t* x;
   int64_t cols;
-  __device__ __forceinline__ void operator()(int64_t row, int u, float (&v)[1][8]) const {
-    unpack8(ldg16(x + row * cols + 8 * u), v[0]);
+  __device__ __forceinline__ void operator()(int64_t row, int u, float (&v)[2][8]) const {
+    const uint16_t* r = x + row * cols + 16 * static_cast<int64_t>(u);
+    unpack8(ldg16(r), v[0]);
+    unpack8(ldg16(r + 8), v[1]);
   }
-  __device__ __forceinline__ int64_t col(int u, int) const { return 8 * static_cast<int64_t>(u); }
+  __device__ __forceinline__ int64_t col(int u, int uu) const { return 16 * static_cast<int64_t>(u) + 8 * uu; }
 };
 
 struct SwigluOp {  // h = bf16(silu(a0) * a1), a = [a0 | a1] of width 2F
   __device__ __forceinline__ int ndst() const { return 1; }
   __device__ __forceinline__ int64_t dst(int64_t row, int) const { return row; }
-  static constexpr int U = 1;
+  static constexpr int U = 2;
+  static constexpr bool kWide = true;
   const uint16_t* a;
   int64_t F;
-  __device__ __forceinline__ void operator()(int64_t row, int u, float (&v)[1][8]) const {
-    float a0[8], a1[8];
-    const uint16_t* r = a + row * 2 * F + 8 * static_cast<int64_t>(u);
-    unpack8(ldg16(r), a0);
-    unpack8(ldg16(r + F), a1);
-    uint32_t hb[4];
-    swiglu_h_x2<8>(a0, a1, v[0], hb);
+  __device__ __forceinline__ void operator()(int64_t row, int u, float (&v)[2][8]) const {
+    const uint16_t* r = a + row * 2 * F + 16 * static_cast<int64_t>(u);
+    const uint4 d0 = ldg16(r), d1 = ldg16(r + 8), e0 = ldg16(r + F), e1 = ldg16(r + F + 8);
+#pragma unroll
+    for (int uu = 0; uu < 2; ++uu) {
+      float a0[8], a1[8];
+      unpack8(uu ? d1 : d0, a0);
+      unpack8(uu ? e1 : e0, a1);
+      uint32_t hb[4];
+      swiglu_h_x2<8>(a0, a1, v[uu], hb);
+    }
   }
-  __device__ __forceinline__ int64_t col(int u, int) const { return 8 * static_cast<int64_t>(u); }
+  __device__ __forceinline__ int64_t col(int u, int uu) const { return 16 * static_cast<int64_t>(u) + 8 * uu; }
 };
 
 struct GatherScaleOp {  // dO[r] = bf16(w[i] * G[i / k]), i = sorted_src[r]; also stores dO
   __device__ __forceinline__ int ndst() const { return 1; }
   __device__ __forceinline__ int64_t dst(int64_t row, int) const { return row; }
   static constexpr int U = 1;
+  static constexpr bool kWide = false;
   const uint16_t* G;
   const float* w;
   const int32_t* sorted_src;
@@ -125,7 +134,8 @@ struct GatherScaleOp {  // dO[r] = bf16(w[i] * G[i / k]), i = sorted_src[r]; als
 // token (pos[t * k + j]): the quantisation of step 1 fused into the gather of
 // step 2 (gather(quantize(x)) == quantize(gather(x)) row by row)
 struct RowsGatherOp {
-  static constexpr int U = 1;
+  static constexpr int U = 2;
+  static constexpr bool kWide = true;
   const uint16_t* x;
   int64_t cols;
   const int32_t* pos;
@@ -136,10 +146,12 @@ struct RowsGatherOp {
     const int64_t p = __ldg(pos + row * k + j);
     return (p >= 0 && p < R) ? p : -1;
   }
-  __device__ __forceinline__ void operator()(int64_t row, int u, float (&v)[1][8]) const {
-    unpack8(ldg16(x + row * cols + 8 * u), v[0]);
+  __device__ __forceinline__ void operator()(int64_t row, int u, float (&v)[2][8]) const {
+    const uint16_t* r = x + row * cols + 16 * static_cast<int64_t>(u);
+    unpack8(ldg16(r), v[0]);
+    unpack8(ldg16(r + 8), v[1]);
   }
-  __device__ __forceinline__ int64_t col(int u, int) const { return 8 * static_cast<int64_t>(u); }
+  __device__ __forceinline__ int64_t col(int u, int uu) const { return 16 * static_cast<int64_t>(u) + 8 * uu; }
 };
 
 // sigma' chain of the SwiGLU backward, in a fixed order of fp32 operations:
@@ -157,7 +169,8 @@ __device__ __forceinline__ void bwd_elem(float z, float a1, float dh, float sig,
 struct SwigluBwdOp {  // dA0 = (dH a1) silu'(a0), dA1 = dH silu(a0); also stores dA
   __device__ __forceinline__ int ndst() const { return 1; }
   __device__ __forceinline__ int64_t dst(int64_t row, int) const { return row; }
-  static constexpr int U = 2;
+  static constexpr int U = 2;        // dA0 and dA1 columns (F apart)
+  static constexpr bool kWide = false;
   const uint16_t* dH;
   const uint16_t* a;
   int64_t F;
@@ -201,6 +214,8 @@ template <int MODE, int MAXI, class Op>
 __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, int64_t qcols,
                                                             const float* static_scale, uint8_t* q, ScaleOut so) {
   constexpr int U = Op::U;
+  static_assert(!Op::kWide || U == 2, "a wide unit is two adjacent 8-column vectors");
+  constexpr int kBlockLanes = Op::kWide ? 8 : 16;  // units per 128-column block
   const int64_t row = blockIdx.x;
   const int tid = threadIdx.x;
   uint32_t pk[MAXI][U][4];
@@ -251,10 +266,11 @@ __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, i
     const int u = i * blockDim.x + tid;
     float s = s_row, inv = inv_row;
     if (MODE == MOE_SCALE_PER_ROW_BLOCK128) {
-      // 16 consecutive units (one 128-column block) sit on 16 consecutive lanes
+      // the units of one 128-column block (16 of 8 columns, or 8 of 16) sit
+      // on consecutive lanes
       float m = amax_i[i];
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      for (int o = kBlockLanes / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
       s = absmax_scale(m);
       inv = __frcp_rn(s);
     }
@@ -281,10 +297,16 @@ __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, i
     for (int i = 0; i < MAXI; ++i) {
       const int u = i * blockDim.x + tid;
       if (u < nunits) {
-        if (MODE == MOE_SCALE_PER_ROW_BLOCK128 && (u & 15) == 0) so.scale[so.blk(drow, u >> 4)] = s_blk[i];
+        if (MODE == MOE_SCALE_PER_ROW_BLOCK128 && (u & (kBlockLanes - 1)) == 0)
+          so.scale[so.blk(drow, u / kBlockLanes)] = s_blk[i];
+        if (Op::kWide) {  // 16 adjacent columns: one 16-byte store
+          *reinterpret_cast<uint4*>(q + drow * qcols + op.col(u, 0)) =
+              make_uint4(codes[i][0].x, codes[i][0].y, codes[i][U - 1].x, codes[i][U - 1].y);
+        } else {
 #pragma unroll
-        for (int uu = 0; uu < U; ++uu)
-          *reinterpret_cast<uint2*>(q + drow * qcols + op.col(u, uu)) = codes[i][uu];
+          for (int uu = 0; uu < U; ++uu)
+            *reinterpret_cast<uint2*>(q + drow * qcols + op.col(u, uu)) = codes[i][uu];
+        }
       }
     }
   }
@@ -482,12 +504,12 @@ extern "C" __attribute__((visibility("hidden"))) cudaError_t moe_detail_take_err
 extern "C" __attribute__((visibility("hidden"))) moe_status moe_detail_quantize_gather(
     const uint16_t* x, const int32_t* pos, int64_t T, int k, int64_t D, moe_scale_mode mode, const float* static_scale,
     uint8_t* xs_q, float* xs_scale, cudaStream_t st) {
-  MOE_HOST_CHECK(D <= kMaxCols, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(D % 16 == 0 && D <= kMaxCols, MOE_ERR_INVALID_ARG);
   moe_status stt = check_mode_ptrs(mode, static_scale, xs_scale);
   if (stt != MOE_OK) return stt;
   RowsGatherOp op{x, D, pos, k, T * k};
   ScaleOut so{xs_scale, 0, static_cast<int>((D + 127) / 128)};
-  return launch_rows(op, T, static_cast<int>(D / 8), D, mode, static_scale, xs_q, so, st);
+  return launch_rows(op, T, static_cast<int>(D / 16), D, mode, static_scale, xs_q, so, st);
 }
 
 extern "C" moe_status moe_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, moe_scale_mode mode,
@@ -498,7 +520,7 @@ extern "C" moe_status moe_quantize_rows(const uint16_t* x, int64_t rows, int64_t
   if (st != MOE_OK) return st;
   RowsOp op{x, cols};
   ScaleOut so{scale, 0, static_cast<int>((cols + 127) / 128)};
-  return launch_rows(op, rows, static_cast<int>(cols / 8), cols, mode, static_scale, q, so, as_stream(stream));
+  return launch_rows(op, rows, static_cast<int>(cols / 16), cols, mode, static_scale, q, so, as_stream(stream));
 }
 
 extern "C" moe_status moe_quantize_weights(const uint16_t* w, int64_t E, int64_t N, int64_t K, moe_scale_mode mode,
@@ -511,7 +533,7 @@ extern "C" moe_status moe_quantize_weights(const uint16_t* w, int64_t E, int64_t
   if (st != MOE_OK) return st;
   RowsOp op{w, K};
   ScaleOut so{scale, N, static_cast<int>(K / 128)};
-  return launch_rows(op, E * N, static_cast<int>(K / 8), K, mode, static_scale, q, so, as_stream(stream));
+  return launch_rows(op, E * N, static_cast<int>(K / 16), K, mode, static_scale, q, so, as_stream(stream));
 }
 
 extern "C" moe_status moe_swiglu_quant(const uint16_t* a, int64_t R, int64_t F, moe_scale_mode mode,
@@ -523,7 +545,7 @@ extern "C" moe_status moe_swiglu_quant(const uint16_t* a, int64_t R, int64_t F, 
   if (st != MOE_OK) return st;
   SwigluOp op{a, F};
   ScaleOut so{h_scale, 0, static_cast<int>((F + 127) / 128)};
-  return launch_rows(op, R, static_cast<int>(F / 8), F, mode, static_scale, h_q, so, as_stream(stream));
+  return launch_rows(op, R, static_cast<int>(F / 16), F, mode, static_scale, h_q, so, as_stream(stream));
 }
 
 extern "C" moe_status moe_gather_scale_quant(const uint16_t* G, const float* w, const int32_t* sorted_src,
