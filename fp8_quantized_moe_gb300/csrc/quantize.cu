@@ -104,8 +104,8 @@ struct SwigluOp {  // h = bf16(silu(a0) * a1), a = [a0 | a1] of width 2F
 struct GatherScaleOp {  // dO[r] = bf16(w[i] * G[i / k]), i = sorted_src[r]; also stores dO
   __device__ __forceinline__ int ndst() const { return 1; }
   __device__ __forceinline__ int64_t dst(int64_t row, int) const { return row; }
-  static constexpr int U = 1;
-  static constexpr bool kWide = false;
+  static constexpr int U = 2;
+  static constexpr bool kWide = true;
   const uint16_t* G;
   const float* w;
   const int32_t* sorted_src;
@@ -113,21 +113,30 @@ struct GatherScaleOp {  // dO[r] = bf16(w[i] * G[i / k]), i = sorted_src[r]; als
   int k;
   int64_t D;
   uint16_t* dO;
-  __device__ __forceinline__ void operator()(int64_t row, int u, float (&v)[1][8]) const {
+  __device__ __forceinline__ void operator()(int64_t row, int u, float (&v)[2][8]) const {
     const int64_t i = __ldg(sorted_src + row);
+    const int64_t c = 16 * static_cast<int64_t>(u);
     if (i < 0 || i >= R) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[0][j] = 0.0f;
+      for (int uu = 0; uu < 2; ++uu)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[uu][j] = 0.0f;
     } else {
       const float wi = w ? __ldg(w + i) : 1.0f;
-      float g[8];
-      unpack8(ldg16(G + (i / k) * D + 8 * static_cast<int64_t>(u)), g);
+      const uint16_t* src = G + (i / k) * D + c;
+      const uint4 d0 = ldg16(src), d1 = ldg16(src + 8);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[0][j] = round_bf16(__fmul_rn(wi, g[j]));
+      for (int uu = 0; uu < 2; ++uu) {
+        float g[8];
+        unpack8(uu ? d1 : d0, g);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[uu][j] = round_bf16(__fmul_rn(wi, g[j]));
+      }
     }
-    *reinterpret_cast<uint4*>(dO + row * D + 8 * static_cast<int64_t>(u)) = pack8(v[0]);
+    *reinterpret_cast<uint4*>(dO + row * D + c) = pack8(v[0]);
+    *reinterpret_cast<uint4*>(dO + row * D + c + 8) = pack8(v[1]);
   }
-  __device__ __forceinline__ int64_t col(int u, int) const { return 8 * static_cast<int64_t>(u); }
+  __device__ __forceinline__ int64_t col(int u, int uu) const { return 16 * static_cast<int64_t>(u) + 8 * uu; }
 };
 
 // plain bf16 token rows whose codes and scales go to the k sorted rows of the
@@ -214,7 +223,7 @@ template <int MODE, int MAXI, class Op>
 __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, int64_t qcols,
                                                             const float* static_scale, uint8_t* q, ScaleOut so) {
   constexpr int U = Op::U;
-  static_assert(!Op::kWide || U == 2, "a wide unit is two adjacent 8-column vectors");
+  static_assert(!Op::kWide || U % 2 == 0, "a wide unit is pairs of adjacent 8-column vectors");
   constexpr int kBlockLanes = Op::kWide ? 8 : 16;  // units per 128-column block
   const int64_t row = blockIdx.x;
   const int tid = threadIdx.x;
@@ -299,9 +308,11 @@ __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, i
       if (u < nunits) {
         if (MODE == MOE_SCALE_PER_ROW_BLOCK128 && (u & (kBlockLanes - 1)) == 0)
           so.scale[so.blk(drow, u / kBlockLanes)] = s_blk[i];
-        if (Op::kWide) {  // 16 adjacent columns: one 16-byte store
-          *reinterpret_cast<uint4*>(q + drow * qcols + op.col(u, 0)) =
-              make_uint4(codes[i][0].x, codes[i][0].y, codes[i][U - 1].x, codes[i][U - 1].y);
+        if (Op::kWide) {  // each pair of vectors: 16 adjacent columns, one 16-byte store
+#pragma unroll
+          for (int uu = 0; uu < U; uu += 2)
+            *reinterpret_cast<uint4*>(q + drow * qcols + op.col(u, uu)) =
+                make_uint4(codes[i][uu].x, codes[i][uu].y, codes[i][uu + 1].x, codes[i][uu + 1].y);
         } else {
 #pragma unroll
           for (int uu = 0; uu < U; ++uu)
@@ -556,7 +567,7 @@ extern "C" moe_status moe_gather_scale_quant(const uint16_t* G, const float* w, 
   MOE_HOST_CHECK(aligned16(G) && aligned16(dO) && aligned16(dO_q) && aligned16(dO_scale), MOE_ERR_INVALID_ARG);
   GatherScaleOp op{G, w, sorted_src, T * k, k, D, dO};
   ScaleOut so{dO_scale, 0, 0};
-  return launch_rows(op, T * k, static_cast<int>(D / 8), D, MOE_SCALE_PER_ROW, nullptr, dO_q, so,
+  return launch_rows(op, T * k, static_cast<int>(D / 16), D, MOE_SCALE_PER_ROW, nullptr, dO_q, so,
                      as_stream(stream));
 }
 
