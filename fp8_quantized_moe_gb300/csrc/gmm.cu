@@ -1310,22 +1310,26 @@ __global__ void swiglu_outside_kernel(uint8_t* h_q, float* h_scale, int64_t M, i
 }
 
 // Second phase of the per-token h scales: the codes of one row against its
-// finished amax (one CTA per row, V 16-byte loads in flight per thread, all
-// issued before any is used, and before the row's amax is read), and the
-// row's final scale amax / 448 written over the amax (1 for a row outside the
-// local groups, whose amax slot holds a negative mark).
+// finished amax (one CTA per row; a thread takes V pairs of adjacent 16-byte
+// vectors, 16 columns each, all loads issued before any is used and before
+// the row's amax is read, and writes each pair's codes with one 16-byte
+// store), and the row's final scale amax / 448 written over the amax (1 for a
+// row outside the local groups, whose amax slot holds a negative mark).
 template <int V>
-__global__ void __launch_bounds__(256) h_quant_rows_kernel(const uint16_t* h, float* h_scale, int nvec, uint8_t* q) {
+__global__ void __launch_bounds__(256) h_quant_rows_kernel(const uint16_t* h, float* h_scale, int npair, uint8_t* q) {
   const int64_t row = blockIdx.x;
-  const uint4* hr = reinterpret_cast<const uint4*>(h) + row * nvec;
-  uint2* qr = reinterpret_cast<uint2*>(q) + row * nvec;
+  const uint4* hr = reinterpret_cast<const uint4*>(h) + row * 2 * npair;
+  uint4* qr = reinterpret_cast<uint4*>(q) + row * npair;
   float m = 0.0f, s = 1.0f, inv = 1.0f;
-  for (int base = 0; base < nvec; base += V * blockDim.x) {
-    uint4 d[V];
+  for (int base = 0; base < npair; base += V * blockDim.x) {
+    uint4 d[V][2];
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const int v = base + i * blockDim.x + threadIdx.x;
-      if (v < nvec) d[i] = __ldg(hr + v);
+      if (v < npair) {
+        d[i][0] = __ldg(hr + 2 * v);
+        d[i][1] = __ldg(hr + 2 * v + 1);
+      }
     }
     if (base == 0) {
       m = h_scale[row];
@@ -1338,16 +1342,21 @@ __global__ void __launch_bounds__(256) h_quant_rows_kernel(const uint16_t* h, fl
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const int v = base + i * blockDim.x + threadIdx.x;
-      if (v < nvec) {
-        const uint32_t w[4] = {d[i].x, d[i].y, d[i].z, d[i].w};
-        float x8[8], qv[8];
+      if (v < npair) {
+        uint2 c[2];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          x8[2 * j] = bf16lo(w[j]);
-          x8[2 * j + 1] = bf16hi(w[j]);
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint32_t w[4] = {d[i][hh].x, d[i][hh].y, d[i][hh].z, d[i][hh].w};
+          float x8[8], qv[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            x8[2 * j] = bf16lo(w[j]);
+            x8[2 * j + 1] = bf16hi(w[j]);
+          }
+          quant_n<8>(x8, s, inv, qv);
+          c[hh] = pack_e4m3x8(qv);
         }
-        quant_n<8>(x8, s, inv, qv);
-        qr[v] = pack_e4m3x8(qv);
+        qr[v] = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
       }
     }
   }
@@ -1642,9 +1651,9 @@ extern "C" moe_status gmm_fp8_swiglu(const uint8_t* lhs_q, const float* lhs_scal
                        : launch_mma<kSwiglu, false>(A, B, A, p, gmm_max_units<kSwiglu, false>(M, E_local, p.ntiles), st);
   if (stt != MOE_OK) return stt;
   if (h_mode == MOE_SCALE_PER_ROW) {
-    const int nvec = static_cast<int>(F / 8);
-    const int threads = std::min(256, ((nvec + 8 * 32 - 1) / (8 * 32)) * 32);
-    h_quant_rows_kernel<8><<<static_cast<unsigned>(M), threads, 0, st>>>(h, h_scale, nvec, h_q);
+    const int npair = static_cast<int>(F / 16);  // F is a multiple of 128
+    const int threads = std::min(256, ((npair + 4 * 32 - 1) / (4 * 32)) * 32);
+    h_quant_rows_kernel<4><<<static_cast<unsigned>(M), threads, 0, st>>>(h, h_scale, npair, h_q);
     MOE_CUDA_TRY(cudaGetLastError());
   }
   return MOE_OK;

@@ -79,26 +79,30 @@ struct RowsOp {  // plain bf16 rows
   __device__ __forceinline__ int64_t col(int u, int uu) const { return 16 * static_cast<int64_t>(u) + 8 * uu; }
 };
 
-struct SwigluOp {  // h = bf16(silu(a0) * a1), a = [a0 | a1] of width 2F
+// h = bf16(silu(a0) * a1), a = [a0 | a1] of width 2F.  WIDE: 16 adjacent
+// columns a unit (two vectors); else 8 (measured faster for the per-token h
+// scale of long rows, where the row-wide maximum keeps every value in
+// registers until the codes are made).
+template <bool WIDE>
+struct SwigluOpT {
   __device__ __forceinline__ int ndst() const { return 1; }
   __device__ __forceinline__ int64_t dst(int64_t row, int) const { return row; }
-  static constexpr int U = 2;
-  static constexpr bool kWide = true;
+  static constexpr int U = WIDE ? 2 : 1;
+  static constexpr bool kWide = WIDE;
   const uint16_t* a;
   int64_t F;
-  __device__ __forceinline__ void operator()(int64_t row, int u, float (&v)[2][8]) const {
-    const uint16_t* r = a + row * 2 * F + 16 * static_cast<int64_t>(u);
-    const uint4 d0 = ldg16(r), d1 = ldg16(r + 8), e0 = ldg16(r + F), e1 = ldg16(r + F + 8);
+  __device__ __forceinline__ void operator()(int64_t row, int u, float (&v)[U][8]) const {
+    const uint16_t* r = a + row * 2 * F + 8 * U * static_cast<int64_t>(u);
 #pragma unroll
-    for (int uu = 0; uu < 2; ++uu) {
+    for (int uu = 0; uu < U; ++uu) {
       float a0[8], a1[8];
-      unpack8(uu ? d1 : d0, a0);
-      unpack8(uu ? e1 : e0, a1);
+      unpack8(ldg16(r + 8 * uu), a0);
+      unpack8(ldg16(r + F + 8 * uu), a1);
       uint32_t hb[4];
       swiglu_h_x2<8>(a0, a1, v[uu], hb);
     }
   }
-  __device__ __forceinline__ int64_t col(int u, int uu) const { return 16 * static_cast<int64_t>(u) + 8 * uu; }
+  __device__ __forceinline__ int64_t col(int u, int uu) const { return 8 * U * static_cast<int64_t>(u) + 8 * uu; }
 };
 
 struct GatherScaleOp {  // dO[r] = bf16(w[i] * G[i / k]), i = sorted_src[r]; also stores dO
@@ -554,8 +558,12 @@ extern "C" moe_status moe_swiglu_quant(const uint16_t* a, int64_t R, int64_t F, 
   MOE_HOST_CHECK(R < (1ll << 31) && aligned16(a) && aligned16(h_q), MOE_ERR_INVALID_ARG);
   moe_status st = check_mode_ptrs(mode, static_scale, h_scale);
   if (st != MOE_OK) return st;
-  SwigluOp op{a, F};
   ScaleOut so{h_scale, 0, static_cast<int>((F + 127) / 128)};
+  if (mode == MOE_SCALE_PER_ROW) {
+    SwigluOpT<false> op{a, F};
+    return launch_rows(op, R, static_cast<int>(F / 8), F, mode, static_scale, h_q, so, as_stream(stream));
+  }
+  SwigluOpT<true> op{a, F};
   return launch_rows(op, R, static_cast<int>(F / 16), F, mode, static_scale, h_q, so, as_stream(stream));
 }
 
