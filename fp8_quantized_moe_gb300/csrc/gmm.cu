@@ -859,6 +859,8 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         uint16_t* out = static_cast<uint16_t*>(p.out);
         const int64_t row = static_cast<int64_t>(tl.row0) + r;
         constexpr int WC = BN / (EPI_WARPS / 4);  // columns per epilogue warp
+        static_assert(MODE != kPromote || WC * EPI_WARPS <= static_cast<int>(sizeof(SmemCtl::sw_stage) / sizeof(float)),
+                      "promotion: per-warp scale staging exceeds sw_stage");
         const int cbase = tl.n0 + half * WC;
         float* stage = ctl->sw_stage + (warp - 2) * WC;
         const bool a_blk = p.lhs_mode == MOE_SCALE_PER_ROW_BLOCK128;
