@@ -6,10 +6,11 @@
 //   moe_quantize_group_cols                        (per-(expert, column) scales)
 //
 // All of these are HBM-bound.  One CTA handles one row: each thread loads
-// 16-byte vectors (8 bf16), applies the producer, keeps the bf16 results in
-// registers, the CTA reduces the absolute maximum (warp shuffles, then shared
-// memory; or 16-lane shuffles for 128-column blocks), and the codes are
-// written with 8-byte stores.  Scales follow "Support quantization for
+// 16-byte vectors (8 bf16; two adjacent ones a unit for most producers),
+// applies the producer, keeps the bf16 results in registers, the CTA reduces
+// the absolute maximum (warp shuffles, then shared memory; or shuffles among
+// the lanes of one 128-column block), and the codes are written with 8- or
+// 16-byte stores.  Scales follow "Support quantization for
 // tokamax gmm v2" (absmax for activations and gradients) and "Quantize
 // activations before EP all gather" (quantise before the sort); weights are
 // pre-quantised as in "Keep qwix out of tpu-inference's fused MoE kernel and
