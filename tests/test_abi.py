@@ -60,3 +60,30 @@ def test_host_side_argument_checks(lib):
     assert lib.moe_ragged_sort_workspace_bytes(1000, 8, 256) >= 4 * 256
     assert lib.tgmm_fp8_workspace_bytes(1000, 256, 512, 8) >= (1000 + 8 * 128) * (256 + 512)
     assert lib.moe_status_string(0) == b"ok"
+
+
+def test_host_side_argument_checks_of_the_fused_and_backward_entries(lib):
+    # one violated condition each; all are caught before any CUDA call
+    raw = ctypes.create_string_buffer(512)
+    p = ctypes.c_void_p((ctypes.addressof(raw) + 15) & ~15)  # a 16-byte aligned host address
+    # gmm_fp8_swiglu: null lhs; F not a multiple of 128; blockwise lhs scales
+    assert lib.gmm_fp8_swiglu(None, p, 0, p, p, 0, p, 1, 0, 1, 1, 128, 128, 0, None, None, p, p, p, None) == 1
+    assert lib.gmm_fp8_swiglu(p, p, 0, p, p, 0, p, 1, 0, 1, 1, 128, 64, 0, None, None, p, p, p, None) == 1
+    assert lib.gmm_fp8_swiglu(p, p, 1, p, p, 0, p, 1, 0, 1, 1, 128, 128, 0, None, None, p, p, p, None) == 1
+    # gmm_fp8_ksplit: K_split not a multiple of 128; K_split past K
+    assert lib.gmm_fp8_ksplit(p, p, 0, p, p, 100, p, 1, 0, 1, 1, 256, 256, p, None) == 1
+    assert lib.gmm_fp8_ksplit(p, p, 0, p, p, 384, p, 1, 0, 1, 1, 256, 256, p, None) == 1
+    # tgmm_fp8_gcq: workspace too small; null gradient
+    assert lib.tgmm_fp8_gcq(p, p, 2, p, p, p, 1, 0, 1, 1, 16, 16, p, p, 0, None) == 1
+    assert lib.tgmm_fp8_gcq(p, p, 2, None, p, p, 1, 0, 1, 1, 16, 16, p, p, 1 << 20, None) == 1
+    # moe_quantize_sort: D not a multiple of 16; k > 32
+    assert lib.moe_quantize_sort(p, p, 1, 1, 1, 24, 0, None, p, p, p, p, p, p, p, 1 << 20, None) == 1
+    assert lib.moe_quantize_sort(p, p, 1, 33, 1, 16, 0, None, p, p, p, p, p, p, p, 1 << 20, None) == 1
+    # the backward's requantisers and the weight layout
+    assert lib.moe_gather_scale_quant(p, None, p, 1, 1, 24, p, p, p, None) == 1       # D % 16
+    assert lib.moe_swiglu_bwd_quant(p, p, 1, 24, p, p, p, None) == 1                  # F % 16
+    assert lib.moe_quantize_group_cols(p, 1, 24, p, 1, 0, 1, p, p, None) == 1         # N % 16
+    assert lib.moe_quantize_group_cols(p, 1, 16, p, 1, 1, 1, p, p, None) == 1         # shard past E
+    assert lib.moe_swiglu_quant(p, 1, 24, 0, None, p, p, None) == 1                   # F % 16
+    assert lib.moe_swiglu_quant(p, 1, 16, 2, None, p, p, None) == 1                   # static mode, no scale
+    assert lib.moe_transpose_u8(p, 1, 24, 16, p, None) == 1                           # R % 16
