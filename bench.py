@@ -3,8 +3,12 @@
 One step = one pass of the whole forward path (activation quantisation,
 ragged sort + gather, gmm wi_0|wi_1, SwiGLU + requantisation, gmm wo, ragged
 gather-reduce) over one batch of synthetic tokens.  Default workload: the
-Mixtral-shaped layer (T=8192, d_model=4096, 8 experts, top-2, d_ff=14336),
-per-token activation scales, per-channel weight scales.
+DeepSeek-V3-shaped layer (T=16384, d_model=7168, 256 experts, top-8,
+d_ff=2048), per-token-per-128-channel activation scales and blockwise
+[E, K/128, N] weight scales, the largest of the five layers on every axis.
+The Mixtral-shaped layer (T=8192, d_model=4096, 8 experts, top-2,
+d_ff=14336, per-token / per-channel scales) is timed in the same run and
+reported as a secondary object of the same line.
 
 Prints one JSON line (rank 0).  Launch with torchrun for several GPUs: every
 rank runs its own batch (data parallel over tokens, no collective on the data
@@ -15,6 +19,7 @@ ranks.  `--impl reference` times the CPU oracle instead, on a bounded sample.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import subprocess
@@ -40,7 +45,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="mixtral", choices=list(synth.CONFIGS))
+    ap.add_argument("--config", default="dsv3", choices=list(synth.CONFIGS))
+    ap.add_argument("--secondary", default="mixtral",
+                    help="a second config timed in the same run, reported as a sub-object ('' for none)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (small cases for profiling)")
     ap.add_argument("--experts", type=int, default=0, help="override E (small cases for profiling)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0, help="oracle sample size (0 = auto)")
@@ -141,18 +148,19 @@ def kernel_source_hash() -> str:
 
 
 def recorded_traffic(kname: str, cfg):
-    """DRAM bytes (read + write) per call of `kname`, from the ncu launch list
-    summarised under profiles/ (a `traffic:` JSON line), or None when there is
-    no record for this workload or the kernels changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", f"launches_{cfg.name}_fwd.md")
+    """DRAM bytes (read + write) per call of `kname` on this workload, from the
+    ncu record in profiles/traffic.json, or None when there is no record or
+    the contraction kernels changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        for line in f:
-            if line.startswith("traffic: "):
-                rec = json.loads(line[len("traffic: "):])
-                if rec.get("call") == kname and rec.get("source") == kernel_source_hash() and rec.get("T") == cfg.T:
-                    return rec["bytes_per_call"]
+        recs = json.load(f)
+    src = kernel_source_hash()
+    for rec in recs:
+        if (rec.get("call") == kname and rec.get("config") == cfg.name and rec.get("T") == cfg.T
+                and rec.get("source") == src):
+            return rec["bytes_per_call"]
     return None
 
 
@@ -160,21 +168,96 @@ def recorded_traffic(kname: str, cfg):
 # CPU oracle timing (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_setup(cfg, x_bits, ids, w, w_in, w_out, static):
-    import oracle
-    wq = oracle.prepare_weights(w_in, w_out, cfg.w_mode, static)
-    return wq
+CPU_SAMPLE_EXPERTS = 16
 
 
-def oracle_time(cfg, x_bits, ids, w, wq, static, n_tokens: int, seed: int = 0):
-    """Time the oracle's forward on a sample of n_tokens tokens (the sort and
-    the activation quantisation run over the whole batch, as they must)."""
-    import oracle
-    rng = np.random.default_rng(seed)
-    toks = np.sort(rng.choice(cfg.T, n_tokens, replace=False))
-    t0 = time.perf_counter()
-    oracle.ffn_forward(x_bits, ids, w, wq, cfg.E, cfg.act_mode, static, tokens=toks)
-    return time.perf_counter() - t0
+def sample_experts(cfg):
+    """The experts whose (token, expert) pairs the CPU sample takes: all of
+    them for small E, else a seeded choice of 16."""
+    if cfg.E <= CPU_SAMPLE_EXPERTS:
+        return list(range(cfg.E))
+    rng = np.random.default_rng(12345)
+    return sorted(int(e) for e in rng.choice(cfg.E, CPU_SAMPLE_EXPERTS, replace=False))
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def omp_threads(n: int) -> bool:
+    """Thread count of the oracle's OpenMP regions (libgomp, already loaded
+    with the oracle library)."""
+    try:
+        ctypes.CDLL("libgomp.so.1").omp_set_num_threads(int(n))
+        return True
+    except (OSError, AttributeError):
+        return False
+
+
+class OracleSample:
+    """The oracle forward on a bounded sample of one workload.
+
+    The sample is a seeded selection of the (token, expert) pairs routed to
+    the experts of `sample_experts` (every expert when E <= 16).  Each pair is
+    one row of the oracle's forward: its token's activation quantised, the
+    row gathered, both contractions with its expert's weights, SwiGLU with the
+    requantisation, and the weighted combine; a token's output is the sum of
+    k such rows, so `pairs / k` is the number of tokens of work done.  Only
+    the sampled experts' weights are quantised (beforehand, untimed)."""
+
+    def __init__(self, cfg, x_bits, ids, w, w_in_bits, w_out_bits, experts, static):
+        import oracle
+        self.oracle = oracle
+        self.cfg, self.x, self.static = cfg, x_bits, static
+        self.wq = oracle.prepare_weights(w_in_bits, w_out_bits, cfg.w_mode, static)
+        remap = -np.ones(cfg.E, np.int64)
+        remap[np.asarray(experts)] = np.arange(len(experts))
+        loc = remap[ids]
+        t, j = np.nonzero(loc >= 0)
+        perm = np.random.default_rng(7).permutation(len(t))
+        self.t, self.j = t[perm], j[perm]
+        self.local = loc[self.t, self.j].astype(np.int32)
+        self.w = w[self.t, self.j].astype(np.float32)
+        self.nE = len(experts)
+        self.npairs = len(self.t)
+
+    def time(self, n: int, offset: int = 0) -> float:
+        idx = (offset + np.arange(n)) % self.npairs
+        xs = np.ascontiguousarray(self.x[self.t[idx]])
+        ids = self.local[idx].reshape(-1, 1)
+        w = self.w[idx].reshape(-1, 1)
+        t0 = time.perf_counter()
+        self.oracle.ffn_forward(xs, ids, w, self.wq, self.nE, self.cfg.act_mode, self.static)
+        return time.perf_counter() - t0
+
+    def aim(self, target_s: float, start: int = 64) -> tuple:
+        """(pairs, seconds) of a sample grown towards target_s seconds."""
+        n = min(start, self.npairs)
+        dt = self.time(n)
+        for _ in range(2):
+            if dt >= 0.6 * target_s or n >= self.npairs:
+                break
+            n = int(min(self.npairs, max(n + 1, n * target_s / max(dt, 1e-3))))
+            dt = self.time(n)
+        return n, dt
+
+
+def host_bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
 def host_inputs(cfg, seed=0):
@@ -187,13 +270,17 @@ def host_inputs(cfg, seed=0):
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def run_ours(args, cfg, rank, world, local):
+def run_ours(args, cfg, rank, world, local, secondary=False):
+    """Time `args.steps` forward steps of `cfg`.  A secondary run (a second
+    workload in the same process) skips the end-to-end loop and the CPU
+    baseline and times at most 50 steps."""
     import fp8_quantized_moe_gb300 as moe
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if world > 1:
+    if world > 1 and not torch.distributed.is_initialized():
         torch.distributed.init_process_group("nccl", device_id=dev)
+    steps = min(args.steps, 50) if secondary else args.steps
     static = synth.calibration_scales(cfg, 0) if cfg.act_mode == synth.PER_TENSOR else None
     sx = sh = None
     if static:
@@ -205,10 +292,15 @@ def run_ours(args, cfg, rank, world, local):
     w_in, w_out = synth.expert_weights(cfg, 0, device=dev)
     W = moe.prepare_weights(w_in, w_out, cfg.w_mode, static)
     torch.cuda.synchronize()
-    if rank != 0 or args.no_cpu_baseline:
-        # only the fp8 copies stay resident; the oracle leg needs the bf16 weights
-        w_in = w_out = None
-        torch.cuda.empty_cache()
+    cpu_sample = None
+    if rank == 0 and not args.no_cpu_baseline and not secondary:
+        # the oracle leg quantises its own copy of the sampled experts' bf16 weights
+        ex = sample_experts(cfg)
+        sel = torch.tensor(ex, device=dev)
+        cpu_sample = (ex, host_bits(w_in.index_select(0, sel)), host_bits(w_out.index_select(0, sel)))
+    # only the fp8 copies stay resident
+    w_in = w_out = None
+    torch.cuda.empty_cache()
     x = x_host.to(dev)
     ids = torch.from_numpy(ids_np).to(dev)
     w = torch.from_numpy(w_np).to(dev)
@@ -244,7 +336,7 @@ def run_ours(args, cfg, rank, world, local):
     if moe.device_error():
         raise RuntimeError("device error during warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -254,14 +346,14 @@ def run_ours(args, cfg, rank, world, local):
     clocks.start()
     time.sleep(0.3)
     start.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         step(evs[i])
     end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    ms = start.elapsed_time(end) / args.steps
+    ms = start.elapsed_time(end) / steps
     gmm_ms = [(e[0].elapsed_time(e[1]), e[2].elapsed_time(e[3])) for e in evs]
     if world > 1:
         t = torch.tensor([ms], device=dev)
@@ -274,7 +366,7 @@ def run_ours(args, cfg, rank, world, local):
     # pinned host memory and its y out, double-buffered so that the copies of
     # step i+1 (in) and i-1 (out) run on their own streams beside step i
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not secondary:
         xh = x_host.pin_memory()
         idh = torch.from_numpy(ids_np).pin_memory()
         wh = torch.from_numpy(w_np).pin_memory()
@@ -339,7 +431,8 @@ def run_ours(args, cfg, rank, world, local):
     g_in = float(np.mean([a for a, _ in gmm_ms]))
     g_out = float(np.mean([b for _, b in gmm_ms]))
     pk, pk_kind = peaks()
-    fp8_peak = 2.0 * pk["bf16_tflops_sustained"]
+    # the timed region is well under a second of GPU time: the burst figure applies
+    fp8_peak = 2.0 * pk["bf16_tflops"]
     # the dominant call of the step is the wi_0 | wi_1 contraction
     achieved = fl["gmm_in"] / (g_in / 1e3) / 1e12
     both = (fl["gmm_in"] + fl["gmm_out"]) / ((g_in + g_out) / 1e3) / 1e12
@@ -349,7 +442,7 @@ def run_ours(args, cfg, rank, world, local):
         "value": cfg.T * world / (ms / 1e3),
         "unit": "tokens/s",
         "n_gpus": world,
-        "steps": args.steps,
+        "steps": steps,
         "warmup": max(args.warmup, 3),
         "ms_per_step": ms,
         "higher_is_better": True,
@@ -363,75 +456,83 @@ def run_ours(args, cfg, rank, world, local):
         "roofline": {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": fp8_peak,
                      "unit": "TFLOP/s", "frac": achieved / fp8_peak,
                      "traffic": recorded_traffic(kname, cfg) if not (args.tokens or args.experts) else None,
-                     "peak_note": f"of {pk_kind}: fp8 = 2 x sustained bf16 cuBLAS "
-                                  f"({pk['bf16_tflops_sustained']} TFLOP/s)",
+                     "peak_note": f"of {pk_kind}: fp8 = 2 x burst bf16 cuBLAS ({pk['bf16_tflops']} TFLOP/s; "
+                                  "the nominal dense fp8 / bf16 ratio is 2)",
                      "flops_per_call": fl["gmm_in"], "ms_per_call": g_in,
                      "note": ("one gmm_fp8_swiglu call per step: the tcgen05 contraction with the SwiGLU and "
                               "requantisation epilogue, plus the h code pass of the per-token scales") if fused else
                              "one gmm_fp8 call per step"},
         "gmm_fp8_both": {"achieved": both, "frac": both / fp8_peak, "unit": "TFLOP/s", "gmm_in_ms": g_in,
                          "gmm_out_ms": g_out, "note": "both contractions of the step, timed with events"},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches_per_step * steps,
         "clocks": clk,
     }
     if e2e:
         result["e2e"] = e2e
-    if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(args, cfg, x_host, ids_np, w_np, w_in, w_out, static)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    del buf, W
+    torch.cuda.empty_cache()
+    if cpu_sample is not None:
+        result["cpu_baseline"] = cpu_baseline(args, cfg, x_host, ids_np, w_np, cpu_sample, static)
     return result
 
 
-def cpu_baseline(args, cfg, x_host, ids_np, w_np, w_in, w_out, static):
-    import oracle
-
-    def host_bits(t):
-        return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-
-    xb = host_bits(x_host)
-    wq = oracle_setup(cfg, xb, ids_np, w_np, host_bits(w_in), host_bits(w_out), static)
-    n = args.cpu_sample_tokens or 8
-    dt = oracle_time(cfg, xb, ids_np, w_np, wq, static, n)
-    # grow the sample towards ~15 s of CPU work (the whole-batch sort and
-    # quantisation make small samples look slower per token, so re-aim once)
-    for seed, target in ((1, 10.0), (2, 15.0)):
-        if args.cpu_sample_tokens or dt >= 0.6 * target or n >= cfg.T:
-            break
-        n = int(min(cfg.T, max(n + 1, n * target / max(dt, 1e-3))))
-        dt = oracle_time(cfg, xb, ids_np, w_np, wq, static, n, seed=seed)
-    return {"value": n / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{n} of {cfg.T} tokens through the oracle forward (fp64, OpenMP); weights quantised "
-                      f"beforehand", "seconds": dt}
+def cpu_baseline(args, cfg, x_host, ids_np, w_np, cpu_sample, static):
+    """The oracle, as it stands, on a bounded sample of the workload: ~15 s on
+    all host cores, then ~8 s on one core."""
+    ex, w_in_b, w_out_b = cpu_sample
+    smp = OracleSample(cfg, host_bits(x_host), ids_np, w_np, w_in_b, w_out_b, ex, static)
+    cores = os.cpu_count()
+    omp_threads(cores)
+    if args.cpu_sample_tokens:
+        n = min(smp.npairs, args.cpu_sample_tokens * cfg.k)
+        dt = smp.time(n)
+    else:
+        n, dt = smp.aim(15.0)
+    rate = n / cfg.k / dt
+    res = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+           "sample": f"{n} (token, expert) pairs of {cfg.T * cfg.k} ({n / cfg.k:.0f} tokens of work), routed to "
+                     f"{len(ex)} of the {cfg.E} experts, through the oracle forward (fp64, OpenMP); weights "
+                     f"quantised beforehand", "seconds": dt, "cpu_model": cpu_model()}
+    if omp_threads(1):
+        n1 = max(1, min(smp.npairs, int(n * 8.0 / max(dt * cores, 1e-3))))
+        dt1 = smp.time(n1, offset=n)
+        res["single_thread"] = {"value": n1 / cfg.k / dt1, "unit": "tokens/s", "cores": 1,
+                                "sample": f"{n1} pairs", "seconds": dt1}
+        omp_threads(cores)
+    return res
 
 
 def run_reference(args, cfg, rank, world):
+    """The reference arm: the oracle, as it stands, on the host's cores.  Each
+    step is a bounded sample of the workload (16 tokens of work: 16 k
+    (token, expert) pairs of the sampled experts, see OracleSample).  Only
+    the sampled experts' weights are drawn and quantised (beforehand)."""
     if rank != 0:
         return None
     import oracle
     oracle.build()
     x_host, ids_np, w_np = host_inputs(cfg, seed=0)
-    w_in, w_out = synth.expert_weights(cfg, 0)
+    ex = sample_experts(cfg)
+    w_in, w_out = synth.expert_weights(cfg, 0, experts=ex)
     static = synth.calibration_scales(cfg, 0) if cfg.act_mode == synth.PER_TENSOR else None
-
-    def host_bits(t):
-        return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-
-    xb = host_bits(x_host)
-    wq = oracle_setup(cfg, xb, ids_np, w_np, host_bits(w_in), host_bits(w_out), static)
-    n = args.cpu_sample_tokens or 16
-    for _ in range(args.warmup):
-        oracle_time(cfg, xb, ids_np, w_np, wq, static, max(1, n // 4))
-    times = [oracle_time(cfg, xb, ids_np, w_np, wq, static, n, seed=i) for i in range(args.steps)]
+    smp = OracleSample(cfg, host_bits(x_host), ids_np, w_np, host_bits(w_in), host_bits(w_out), ex, static)
+    del w_in, w_out
+    cores = os.cpu_count()
+    omp_threads(cores)
+    n = min(smp.npairs, (args.cpu_sample_tokens or 16) * cfg.k)
+    for i in range(args.warmup):
+        smp.time(max(1, n // 4), offset=i * n)
+    times = [smp.time(n, offset=i * n) for i in range(args.steps)]
     sec = float(np.sum(times))
-    value = n * args.steps / sec
+    value = n / cfg.k * args.steps / sec
     return {
         "metric": METRIC, "impl": "reference", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": workload_name(cfg)},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": f"{n} tokens per step of {cfg.T}"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} (token, expert) pairs per step ({n / cfg.k:.0f} tokens of work) routed to "
+                                   f"{len(ex)} of the {cfg.E} experts", "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -641,6 +742,13 @@ def main():
         res = run_reference(args, cfg, rank, world)
     else:
         res = run_ours(args, cfg, rank, world, local)
+        if args.secondary and args.secondary != cfg.name and not (args.tokens or args.experts):
+            cfg2 = synth.CONFIGS[args.secondary]
+            r2 = run_ours(args, cfg2, rank, world, local, secondary=True)
+            res["secondary"] = {k: r2[k] for k in ("value", "unit", "ms_per_step", "steps", "config", "roofline",
+                                                   "gmm_fp8_both", "gpu_launches", "clocks")}
+        if world > 1:
+            torch.distributed.destroy_process_group()
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
 

@@ -434,12 +434,13 @@ def ffn_forward(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, W
 
 
 def ffn_backward(dY: torch.Tensor, topk_w: torch.Tensor, W: ExpertWeights, buf: FFNBuffers,
-                 static_x: torch.Tensor, static_h: torch.Tensor):
+                 static_x: torch.Tensor, static_h: torch.Tensor, keep: Optional[dict] = None):
     """Backward pass of the static scheme after ffn_forward on `buf`.
 
     Returns (dX bf16 [T, D], dW_in fp32 [E, D, 2F], dW_out fp32 [E, F, D]):
     dW_in holds grad_wi_0 | grad_wi_1 and dW_out grad_wo, in the pages'
-    [E, in, out] layouts."""
+    [E, in, out] layouts.  With `keep` (a dict), the intermediate gradients
+    (dO, dO_q, dO_s, dA, dA_q, dA_s, dAg_s, dOg_s) are stored in it."""
     s = buf.sort
     k = buf.k
     dO, dO_q, dO_s = gather_scale_quant(dY, topk_w, s["sorted_src"], k)
@@ -453,4 +454,6 @@ def ffn_backward(dY: torch.Tensor, topk_w: torch.Tensor, W: ExpertWeights, buf: 
     _, dOg_s = quantize_group_cols(dO, s["group_sizes"], scales_only=True)
     dW_in = tgmm_gcq(s["xs_q"], static_x, PER_TENSOR, dA, dAg_s, s["group_sizes"])
     dW_out = tgmm_gcq(buf.h_q, static_h, PER_TENSOR, dO, dOg_s, s["group_sizes"])
+    if keep is not None:
+        keep.update(dO=dO, dO_q=dO_q, dO_s=dO_s, dA=dA, dA_q=dA_q, dA_s=dA_s, dAg_s=dAg_s, dOg_s=dOg_s)
     return buf.dX, dW_in, dW_out

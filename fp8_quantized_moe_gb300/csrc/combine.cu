@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* rows, cons
   if (lane < k) {
     const int p = __ldg(pos + t * k + lane);
     my_pos = (p >= 0 && p < R) ? p : -1;
+    if (my_pos < 0) raise_error(&g_err, MOE_DEVERR_BAD_POSITION);  // a corrupted permutation
     my_w = weights ? __ldg(weights + t * k + lane) : 1.0f;
   }
   const int64_t nvec = D / 8;
@@ -88,7 +89,8 @@ extern "C" __attribute__((visibility("hidden"))) cudaError_t moe_detail_take_err
 extern "C" moe_status ragged_gather_reduce(const uint16_t* rows, const int32_t* pos, const float* weights, int64_t T,
                                            int k, int64_t D, uint16_t* out, moe_stream_t stream) {
   MOE_HOST_CHECK(rows && pos && out && T >= 0 && k > 0 && k <= kMaxK && D > 0 && D % 8 == 0, MOE_ERR_INVALID_ARG);
-  MOE_HOST_CHECK(T * k < (1ll << 31) && aligned16(rows) && aligned16(out), MOE_ERR_INVALID_ARG);
+  // T * k < 2^31, tested without forming the product of an unchecked T
+  MOE_HOST_CHECK(T <= ((1ll << 31) - 1) / k && aligned16(rows) && aligned16(out), MOE_ERR_INVALID_ARG);
   if (T == 0) return MOE_OK;
   combine_kernel<<<static_cast<unsigned>((T + 7) / 8), 256, 0, as_stream(stream)>>>(rows, pos, weights, T, k, D,
                                                                                      out);

@@ -56,6 +56,7 @@ constexpr int kMaxStages = 8;
 constexpr int kMaxAcc = 8;
 constexpr int kMaxGroups = 1024;
 constexpr int64_t kPairMinK = 3072;  // gmm K from which the plain and SwiGLU gmm run on CTA pairs
+constexpr int kMaxDevices = 256;     // host-side per-device caches
 
 enum Mode { kFinal = 0, kPromote = 1, kTgmm = 2, kSwiglu = 3, kSplit = 4 };
 
@@ -1461,14 +1462,26 @@ moe_status launch_mma(const CUtensorMap& A, const CUtensorMap& B, const CUtensor
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  static int max_clusters = 0;  // per instantiation
-  int& mc = max_clusters;
+  // resident clusters of this instantiation, cached per device (several
+  // host threads may launch on several devices)
+  static std::mutex mu;
+  static int max_clusters[kMaxDevices] = {};
+  int dev = 0;
+  MOE_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  int mc = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    mc = max_clusters[dev];
+  }
   if (mc == 0) {
     cfg.gridDim = dim3(2 * (sms / 2));
     int n = 0;
     MOE_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, kernel, &cfg));
     if (n <= 0) return MOE_ERR_UNSUPPORTED;
     mc = n;
+    std::lock_guard<std::mutex> lock(mu);
+    max_clusters[dev] = n;
   }
   const int clusters = max_units < mc ? max_units : mc;
   cfg.gridDim = dim3(2 * clusters);

@@ -572,7 +572,7 @@ extern "C" moe_status moe_gather_scale_quant(const uint16_t* G, const float* w, 
                                              int64_t T, int k, int64_t D, uint16_t* dO, uint8_t* dO_q,
                                              float* dO_scale, moe_stream_t stream) {
   MOE_HOST_CHECK(G && sorted_src && dO && dO_q && dO_scale && T >= 0 && k > 0 && D > 0, MOE_ERR_INVALID_ARG);
-  MOE_HOST_CHECK(D % 16 == 0 && D <= kMaxCols && T * k < (1ll << 31), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(D % 16 == 0 && D <= kMaxCols && T <= ((1ll << 31) - 1) / k, MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(aligned16(G) && aligned16(dO) && aligned16(dO_q) && aligned16(dO_scale), MOE_ERR_INVALID_ARG);
   GatherScaleOp op{G, w, sorted_src, T * k, k, D, dO};
   ScaleOut so{dO_scale, 0, 0};

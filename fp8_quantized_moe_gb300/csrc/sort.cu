@@ -204,8 +204,16 @@ extern "C" __attribute__((visibility("hidden"))) cudaError_t moe_detail_take_err
   return e;
 }
 
+namespace moe {
+namespace {
+// T * k < 2^31 (the pair indices are int32), tested without forming the
+// product of an unchecked T.
+bool pairs_fit(int64_t T, int k) { return T >= 0 && k > 0 && T <= ((1ll << 31) - 1) / k; }
+}  // namespace
+}  // namespace moe
+
 extern "C" size_t moe_ragged_sort_workspace_bytes(int64_t T, int k, int E) {
-  if (T < 0 || k <= 0 || E <= 0) return 0;
+  if (!moe::pairs_fit(T, k) || E <= 0) return 0;
   const int64_t nc = num_chunks(T * k);
   return static_cast<size_t>((nc > 0 ? nc : 1) * E) * sizeof(int);
 }
@@ -247,7 +255,7 @@ extern "C" moe_status moe_ragged_sort(const int32_t* topk_ids, int64_t T, int k,
   MOE_HOST_CHECK(topk_ids && x_q && sorted_src && pos && group_sizes && group_offsets && xs_q && workspace,
                  MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(T >= 0 && k > 0 && k <= 32 && E > 0 && E <= kMaxE && D > 0 && D % 16 == 0, MOE_ERR_INVALID_ARG);
-  MOE_HOST_CHECK(T * k < (1ll << 31), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(pairs_fit(T, k), MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(aligned16(x_q) && aligned16(xs_q) && (reinterpret_cast<uintptr_t>(workspace) & 3) == 0,
                  MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(workspace_bytes >= moe_ragged_sort_workspace_bytes(T, k, E), MOE_ERR_INVALID_ARG);
@@ -284,7 +292,7 @@ extern "C" moe_status moe_quantize_sort(const uint16_t* x, const int32_t* topk_i
   MOE_HOST_CHECK(x && topk_ids && sorted_src && pos && group_sizes && group_offsets && xs_q && workspace,
                  MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(T >= 0 && k > 0 && k <= 32 && E > 0 && E <= kMaxE && D > 0 && D % 16 == 0, MOE_ERR_INVALID_ARG);
-  MOE_HOST_CHECK(T * k < (1ll << 31), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(pairs_fit(T, k), MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(aligned16(x) && aligned16(xs_q) && (reinterpret_cast<uintptr_t>(workspace) & 3) == 0,
                  MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(workspace_bytes >= moe_ragged_sort_workspace_bytes(T, k, E), MOE_ERR_INVALID_ARG);
@@ -329,7 +337,7 @@ extern "C" moe_status moe_ragged_sort_noalloc(const int32_t* topk_ids, int64_t T
                                               int32_t* sorted_src, int32_t* pos, int32_t* group_sizes,
                                               int32_t* group_offsets, uint8_t* xs_q, float* xs_scale,
                                               moe_stream_t stream) {
-  if (T < 0 || k <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+  if (!moe::pairs_fit(T, k) || E <= 0) return MOE_ERR_INVALID_ARG;
   // the counts need nchunks * E ints; larger problems do not fit the array
   if (moe_ragged_sort_workspace_bytes(T, k, E) > moe::kNoAllocScratchBytes) return MOE_ERR_INVALID_ARG;
   int dev = 0;

@@ -79,6 +79,7 @@ typedef enum {
 #define MOE_DEVERR_GROUP_SIZES 0x2u   /* gmm/tgmm: negative size or sum != M */
 #define MOE_DEVERR_TIMEOUT 0x4u       /* a bounded wait in a tcgen05 kernel ran out */
 #define MOE_DEVERR_TMEM 0x8u          /* tensor-memory allocation returned no columns */
+#define MOE_DEVERR_BAD_POSITION 0x10u /* ragged_gather_reduce: a pos entry outside [0, T*k) */
 
 const char* moe_status_string(moe_status s);
 
@@ -270,7 +271,8 @@ moe_status moe_swiglu_quant(const uint16_t* a, int64_t R, int64_t F, moe_scale_m
  *   out[t, :] = bf16( sum_{j<k} weights[t, j] * rows[pos[t*k + j], :] )
  * fp32 accumulation in ascending j.  rows bf16 [T*k, D]; pos int32 [T*k];
  * weights fp32 [T, k] or NULL (all ones); out bf16 [T, D].  D % 8 == 0;
- * 1 <= k <= 32.  A pos entry outside [0, T*k) contributes nothing.
+ * 1 <= k <= 32; T*k < 2^31.  A pos entry outside [0, T*k) contributes
+ * nothing to its token's sum and sets MOE_DEVERR_BAD_POSITION.
  */
 moe_status ragged_gather_reduce(const uint16_t* rows, const int32_t* pos, const float* weights, int64_t T, int k,
                                 int64_t D, uint16_t* out, moe_stream_t stream);

@@ -81,21 +81,25 @@ def output_grad(cfg: MoEConfig, seed: int = 0, device="cpu") -> torch.Tensor:
     return torch.randn(cfg.T, cfg.D, generator=g, device=device).to(torch.bfloat16)
 
 
-def expert_weights(cfg: MoEConfig, seed: int = 0, device="cpu", std: float = 0.02):
+def expert_weights(cfg: MoEConfig, seed: int = 0, device="cpu", std: float = 0.02, experts=None):
     """Expert weights in the device layout, bf16, N(0, std).
 
     w_in:  [E, 2F, D]  rows 0..F-1 are wi_0, rows F..2F-1 are wi_1 (output
            channel major, the contracted model dimension D contiguous).
     w_out: [E, D, F]   wo, output channel major, F contiguous.
-    """
-    g = _gen(seed * 7919 + 2, device)
-    w_in = torch.empty(cfg.E, 2 * cfg.F, cfg.D, dtype=torch.bfloat16, device=device)
-    w_out = torch.empty(cfg.E, cfg.D, cfg.F, dtype=torch.bfloat16, device=device)
-    # Draw expert by expert to bound the fp32 temporary.
-    for e in range(cfg.E):
-        w_in[e] = (torch.randn(2 * cfg.F, cfg.D, generator=g, device=device) * std).to(torch.bfloat16)
-    for e in range(cfg.E):
-        w_out[e] = (torch.randn(cfg.D, cfg.F, generator=g, device=device) * std).to(torch.bfloat16)
+
+    Every expert draws from generators of its own, so `experts` (a list of
+    expert ids) yields exactly those experts' rows of the full tensors,
+    without drawing the others."""
+    ids = range(cfg.E) if experts is None else list(experts)
+    w_in = torch.empty(len(ids), 2 * cfg.F, cfg.D, dtype=torch.bfloat16, device=device)
+    w_out = torch.empty(len(ids), cfg.D, cfg.F, dtype=torch.bfloat16, device=device)
+    base = (seed * 7919 + 2) * 4099
+    for i, e in enumerate(ids):
+        g = _gen(base + 2 * e, device)
+        w_in[i] = (torch.randn(2 * cfg.F, cfg.D, generator=g, device=device) * std).to(torch.bfloat16)
+        g = _gen(base + 2 * e + 1, device)
+        w_out[i] = (torch.randn(cfg.D, cfg.F, generator=g, device=device) * std).to(torch.bfloat16)
     return w_in, w_out
 
 

@@ -159,8 +159,9 @@ def test_tgmm_matches_oracle(M, K, N, E, lmode, rmode):
     ([200, 2500, 1300, 0, 90, 1200], 128, 272, 1, 4, RT),       # a shard of groups 1..4
 ])
 def test_tgmm_heavy_and_light_groups(sizes, K, N, g0, El, rmode):
-    """Groups with many 128-row blocks and groups with few are scheduled as two
-    tile streams on separate CTAs; every expert's result must be unchanged."""
+    """Groups with many 128-row blocks (long K loops of the contraction over
+    rows) beside light and empty groups, in the expert-major tile order; every
+    expert's result must match the oracle."""
     sizes = np.array(sizes, np.int32)
     M = int(sizes.sum())
     rng = np.random.default_rng(M + K + N)

@@ -170,6 +170,33 @@ def test_combine_matches_oracle(T, k, D):
         assert np.array_equal(host(y1), o[pos])
 
 
+def test_combine_bad_position_raises_device_error():
+    """A pos entry outside [0, T*k) (a corrupted permutation) contributes
+    nothing and sets MOE_DEVERR_BAD_POSITION; the other tokens are exact and
+    a following call with a valid permutation leaves the word clear."""
+    rng = np.random.default_rng(7)
+    T, k, D, E = 64, 2, 256, 4
+    ids = rng.integers(0, E, (T, k)).astype(np.int32)
+    _, pos, _, _ = oracle.ragged_sort(ids, E)
+    o = oracle.bf16_bits(torch.from_numpy(rng.standard_normal((T * k, D)).astype(np.float32)).to(torch.bfloat16))
+    w = rng.uniform(0, 1, (T, k)).astype(np.float32)
+    y_ref = oracle.combine(o, pos, w, k)
+    bad = pos.copy()
+    bad[5 * k + 1] = T * k + 3
+    assert moe.device_error() == 0
+    y = moe.ragged_gather_reduce(dev(o), dev(bad), dev(w), k)
+    assert moe.device_error() == 0x10
+    yh = host(y)
+    others = np.arange(T) != 5
+    assert_close(yh[others], y_ref[others], "combine, other tokens")
+    # token 5 keeps only its valid row
+    y5 = oracle.combine(o[pos[5 * k: 5 * k + 1]], np.array([0], np.int32), w[5:6, :1], 1)
+    assert_close(yh[5:6], y5, "combine, token with a bad position")
+    y = moe.ragged_gather_reduce(dev(o), dev(pos), dev(w), k)
+    assert moe.device_error() == 0
+    assert_close(host(y), y_ref, "combine after the bad call")
+
+
 @pytest.mark.parametrize("T,k,D", [(1, 1, 16), (64, 6, 256), (300, 2, 4096)])
 def test_gather_scale_quant_bit_exact(T, k, D):
     rng = np.random.default_rng(T + D)

@@ -380,3 +380,90 @@ def test_ffn_backward_quantised_tracks_f64_gradients():
     for got, ref in [(oracle.bf16_to_f64(bwd["dX"]), dX64), (bwd["dW_in"], dWin64), (bwd["dW_out"], dWout64)]:
         rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
         assert rel < 0.25, rel
+
+
+def test_ffn_backward_composition_against_dense_numpy():
+    """Pins every contraction of oracle.ffn_backward against dense numpy
+    products of the oracle's own codes and scales ("Support quantization for
+    tokamax gmm v2", fp8_static_wa: fixed weight and activation scales,
+    absmax-quantised gradients).  wi_0 and wi_1 get static scales a factor
+    4.7 apart, so putting s_w0 on the wrong half of the [dA0 | dA1]
+    contraction, swapping the two, or splitting at the wrong K block changes
+    dXs grossly (the negative controls below check that it would)."""
+    cfg = synth.scaled(synth.CONFIGS["fwdbwd"], T=40, D=128, E=10, F=256)
+    x = oracle.bf16_bits(synth.activations(cfg, 3))
+    ids, w = synth.routing(cfg, 3)
+    G = oracle.bf16_bits(synth.output_grad(cfg, 3))
+    w_in, w_out = synth.expert_weights(cfg, 3)
+    static = dict(synth.calibration_scales(cfg, 3))
+    static["w1"] = float(np.float32(4.7 * static["w0"]))
+    wq = oracle.prepare_weights(oracle.bf16_bits(w_in), oracle.bf16_bits(w_out), cfg.w_mode, static)
+    fwd = oracle.ffn_forward(x, ids, w, wq, cfg.E, cfg.act_mode, static)
+    bwd = oracle.ffn_backward(fwd, G, w, wq, cfg.k, static)
+    qin, _, _, qo, _, _ = wq
+    F, D, k = cfg.F, cfg.D, cfg.k
+    s0, s1, so = np.float64(np.float32(static["w0"])), np.float64(np.float32(static["w1"])), \
+        np.float64(np.float32(static["wo"]))
+    sx, sh = np.float64(np.float32(static["x"])), np.float64(np.float32(static["h"]))
+    sizes = fwd["sizes"]
+    starts = np.concatenate([[0], np.cumsum(sizes)])
+    expert = np.repeat(np.arange(cfg.E), sizes)  # expert of each sorted row
+    W0 = oracle.e4m3_to_f64(qin[:, :F, :])  # [E, F, D] codes of wi_0
+    W1 = oracle.e4m3_to_f64(qin[:, F:, :])
+    Wo = oracle.e4m3_to_f64(qo)             # [E, D, F]
+
+    def close_bf16(got_bits, ref_f64, what):
+        ref = oracle.bf16_to_f64(bf16(ref_f64))
+        got = oracle.bf16_to_f64(got_bits)
+        diff = got != ref
+        # products of e4m3 codes sum exactly in fp64; only the order of the
+        # scale multiplications may move a value across a bf16 rounding edge
+        assert diff.mean() < 1e-3, (what, diff.mean())
+        assert np.all(np.abs(got - ref) <= 2.0 ** -7 * np.abs(ref) + 1e-30), what
+
+    # dH = dO @ wo: per-row dO scale, static wo scale
+    dOq = oracle.e4m3_to_f64(bwd["dO_q"]) * bwd["dO_s"].astype(np.float64)[:, None]
+    dH = np.stack([dOq[r] @ Wo[expert[r]] for r in range(len(expert))]) * so
+    close_bf16(bwd["dH"], dH, "dH")
+    # dXs = dA0 @ wi_0^T-side (s_w0) + dA1 @ wi_1 (s_w1), per-row dA scale
+    dAq = oracle.e4m3_to_f64(bwd["dA_q"])
+    dAs = bwd["dA_s"].astype(np.float64)
+    part0 = np.stack([dAq[r, :F] @ W0[expert[r]] for r in range(len(expert))])
+    part1 = np.stack([dAq[r, F:] @ W1[expert[r]] for r in range(len(expert))])
+    dXs = (s0 * part0 + s1 * part1) * dAs[:, None]
+    close_bf16(bwd["dXs"], dXs, "dXs")
+    got = oracle.bf16_to_f64(bwd["dXs"])
+    for wrong in ((s1 * part0 + s0 * part1) * dAs[:, None],   # scales swapped
+                  (s0 * (part0 + part1)) * dAs[:, None],      # one scale for both halves
+                  (s0 * np.stack([dAq[r, :F - 128] @ W0[expert[r], :F - 128] for r in range(len(expert))])
+                   + s1 * (part1 + np.stack([dAq[r, F - 128:F] @ W0[expert[r], F - 128:] for r in
+                                             range(len(expert))]))) * dAs[:, None]):  # split one block early
+        assert np.linalg.norm(got - wrong) / np.linalg.norm(wrong) > 0.05
+    # dX = the combine's adjoint with unit weights: sum of a token's k rows
+    dX = np.zeros((cfg.T, D))
+    for i in range(cfg.T * k):
+        dX[i // k] += oracle.bf16_to_f64(bwd["dXs"][fwd["pos"][i]])
+    close_bf16(bwd["dX"], dX, "dX")
+    # weight gradients: per-(expert, column) gradient codes, static x / h scales
+    xs = oracle.e4m3_to_f64(fwd["xs_q"]) * sx
+    hq = oracle.e4m3_to_f64(fwd["h_q"]) * sh
+    dAg = oracle.e4m3_to_f64(bwd["dAg_q"])
+    dOg = oracle.e4m3_to_f64(bwd["dOg_q"])
+    for e in range(cfg.E):
+        rows = slice(starts[e], starts[e + 1])
+        ref_in = xs[rows].T @ (dAg[rows] * bwd["dAg_s"][e].astype(np.float64)[None, :])
+        ref_out = hq[rows].T @ (dOg[rows] * bwd["dOg_s"][e].astype(np.float64)[None, :])
+        np.testing.assert_allclose(bwd["dW_in"][e], ref_in, rtol=2e-7, atol=1e-7 * max(np.abs(ref_in).max(), 1e-30))
+        np.testing.assert_allclose(bwd["dW_out"][e], ref_out, rtol=2e-7,
+                                   atol=1e-7 * max(np.abs(ref_out).max(), 1e-30))
+    # the per-(expert, column) gradient codes are the absmax codes of dA / dO over the expert's rows
+    for g_bits, gq, gs in ((bwd["dA"], bwd["dAg_q"], bwd["dAg_s"]), (bwd["dO"], bwd["dOg_q"], bwd["dOg_s"])):
+        gv = oracle.bf16_to_f64(g_bits)
+        for e in range(cfg.E):
+            rows = slice(starts[e], starts[e + 1])
+            if starts[e + 1] == starts[e]:
+                assert np.all(gs[e] == 1.0)
+                continue
+            amax = np.abs(gv[rows]).max(axis=0)
+            exp_s = np.where(amax > 0, (amax.astype(np.float32) / np.float32(448.0)).astype(np.float32), 1.0)
+            assert np.array_equal(gs[e], exp_s.astype(np.float32))
