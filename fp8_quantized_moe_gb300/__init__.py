@@ -211,8 +211,10 @@ def gmm_swiglu(lhs_q, lhs_scale, lhs_mode, rhs_q, rhs_scale, rhs_mode, group_siz
 
 
 def swiglu_fusable(act_mode: int, w_mode: int, F: int) -> bool:
-    """gmm_fp8_swiglu covers per-row / per-tensor operand scales and F % 128 == 0."""
-    return act_mode in (PER_ROW, PER_TENSOR) and w_mode in (PER_ROW, PER_TENSOR) and F % 128 == 0
+    """gmm_fp8_swiglu covers every operand scale mode (per row, per row and
+    128 columns, per tensor) when F % 128 == 0."""
+    modes = (PER_ROW, PER_ROW_BLOCK128, PER_TENSOR)
+    return act_mode in modes and w_mode in modes and F % 128 == 0
 
 
 def swiglu_quant(a: torch.Tensor, mode: int, static_scale: Optional[torch.Tensor] = None, h_q=None, h_scale=None):

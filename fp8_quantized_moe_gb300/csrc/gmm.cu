@@ -58,7 +58,8 @@ constexpr int kMaxGroups = 1024;
 constexpr int64_t kPairMinK = 3072;  // gmm K from which the plain and SwiGLU gmm run on CTA pairs
 constexpr int kMaxDevices = 256;     // host-side per-device caches
 
-enum Mode { kFinal = 0, kPromote = 1, kTgmm = 2, kSwiglu = 3, kSplit = 4 };
+enum Mode { kFinal = 0, kPromote = 1, kTgmm = 2, kSwiglu = 3, kSplit = 4, kPromoteSwiglu = 5 };
+constexpr int kSwSlots = 8;  // promotion: ring of per-K-block weight-scale rows in shared memory
 
 struct Params {
   const int32_t* group_sizes;
@@ -89,6 +90,9 @@ struct SmemCtl {
   uint64_t empty[kMaxStages];
   uint64_t tfull[kMaxAcc];
   uint64_t tempty[kMaxAcc];
+  uint64_t sfull[kSwSlots];   // promotion: a weight-scale row of the ring has landed
+  uint64_t sempty[kSwSlots];  // promotion: a weight-scale row of the ring has been read by every epilogue warp
+  uint64_t xbar[4][2];        // promotion + SwiGLU: the two warps of a lane quarter have posted their h maxima
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -99,28 +103,22 @@ struct SmemCtl {
   int tile_prefix[kMaxGroups + 1];  // gmm: first tile of local group
   int gsize[kMaxGroups];
   // per-mode scratch (one mode per kernel)
-  union alignas(16) {
-    float sw_stage[1024];        // promotion: weight scales of the current K block, per warp
-    float pamax[2][4][2][32];    // fused SwiGLU, per-128 h scales: row maxima of the two column halves
-  };
+  alignas(16) float pamax[2][4][2][32];  // fused SwiGLU, per-128 h scales: row maxima of the two column halves
 };
-// sw_stage is read and written with float2 / float4 accesses
-static_assert(offsetof(SmemCtl, sw_stage) % 16 == 0 && offsetof(SmemCtl, pamax) % 16 == 0, "SmemCtl alignment");
+static_assert(offsetof(SmemCtl, pamax) % 16 == 0, "SmemCtl alignment");
 static_assert(sizeof(SmemCtl) % 16 == 0, "SmemCtl size");
 
-// Tile configuration per mode.  Promotion (a blockwise operand scale) uses
-// 128x128 tiles with four TMEM accumulators, so the MMA can run up to three K
-// blocks ahead of the epilogue that folds each block's partial sums into
-// registers; tgmm uses 128x256 tiles with two accumulators.  The plain and
-// SwiGLU gmm run on CTA pairs (a 2-CTA cluster): one 256x256 MMA per K step
-// over both CTAs, each CTA holding 128 rows of A and half of the B tile, so a
-// stage is 32 KB per CTA instead of 48 and the operand traffic through each
-// SM's shared memory drops by a third.  (Promotion on CTA pairs was measured
-// slower at every tile width: each K block's accumulator release then crosses
-// the pair.)
-#ifndef MOE_PROMOTE_BN
-#define MOE_PROMOTE_BN 128
-#endif
+// Tile configuration per mode.  The plain and SwiGLU gmm run on CTA pairs (a
+// 2-CTA cluster) from K = 3072: one 256x256 MMA per K step over both CTAs,
+// each CTA holding 128 rows of A and half of the B tile, so a stage is 32 KB
+// per CTA instead of 48 and the operand traffic through each SM's shared
+// memory drops by a third.  Promotion (a blockwise operand scale) uses one
+// CTA and 128x256 tiles: an M=128 tcgen05 MMA costs about the same time at
+// N=128 as at N=256 (measured), so only N=256 keeps the tensor pipe at full
+// rate; its two 256-column TMEM accumulators take alternate K blocks, and a
+// one-CTA tile keeps the per-block accumulator hand-off local and wastes at
+// most 127 rows at the end of a group.  tgmm uses 128x256 tiles with two
+// accumulators.
 #ifndef MOE_PROMOTE_EPI_WARPS
 #define MOE_PROMOTE_EPI_WARPS 8
 #endif
@@ -141,20 +139,27 @@ static_assert(sizeof(SmemCtl) % 16 == 0, "SmemCtl size");
 #endif
 template <int MODE, bool PAIR_REQ = false>
 struct Cfg {
-  static constexpr bool PROMOTE = MODE == kPromote;
+  static constexpr bool PROMOTE = MODE == kPromote || MODE == kPromoteSwiglu;
+  static constexpr bool SWIGLU = MODE == kSwiglu || MODE == kPromoteSwiglu;
   static constexpr bool PAIR = PAIR_REQ && MOE_GMM_PAIR && (MODE == kFinal || MODE == kSwiglu);
-  static constexpr int BN = PROMOTE ? MOE_PROMOTE_BN : 256;  // output columns per tile
+  static constexpr int BN = 256;  // output columns per tile
   static constexpr int TMEM_COLS = PAIR ? MOE_PAIR_TMEM_COLS : 512;
   static constexpr int SEGS = MODE == kSplit ? 2 : 1;        // accumulators per tile (one per K segment)
-  static constexpr int NACC = TMEM_COLS / (BN * SEGS);       // tiles in flight in tensor memory
-  static constexpr int NSTAGE = PAIR ? 6 : (BN == 128 ? 6 : (BN == 64 ? 8 : (MODE == kTgmm ? MOE_TGMM_NSTAGE : MOE_GMM_NSTAGE)));
+  static constexpr int NACC = TMEM_COLS / (BN * SEGS);       // tiles (promotion: K blocks) in flight in tensor memory
+  static constexpr int NSTAGE = PAIR ? 6 : (MODE == kTgmm ? MOE_TGMM_NSTAGE : MOE_GMM_NSTAGE);
   static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK;  // this CTA's part of the B tile
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TX_BYTES = (PAIR ? 2 : 1) * STAGE_BYTES;  // what one full barrier waits for
   static constexpr uint32_t IDESC = idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN);
   static constexpr int EPI_WARPS =
-      MODE == kPromote ? MOE_PROMOTE_EPI_WARPS : (MODE == kSwiglu ? 8 : (MODE == kTgmm ? MOE_TGMM_EPI_WARPS : 4));
-  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+      PROMOTE ? MOE_PROMOTE_EPI_WARPS : (MODE == kSwiglu ? 8 : (MODE == kTgmm ? MOE_TGMM_EPI_WARPS : 4));
+  // warps before the epilogue: producer, MMA issuer and, for promotion, two
+  // idle warps that complete the control warpgroup of the register split
+  static constexpr int CTRL_WARPS = PROMOTE ? 4 : 2;
+  static constexpr int THREADS = 32 * (CTRL_WARPS + EPI_WARPS);
+  // promotion register split: the control warpgroup gives registers to the
+  // two epilogue warpgroups, whose 128 running sums per thread need them
+  static constexpr uint32_t CTRL_REGS = 40, EPI_REGS = 232;
   // per-warp staging of 32x32 output blocks: kFinal, bf16 rows padded to 80
   // bytes for row-contiguous stores; kTgmm, two 4 KB fp32 blocks in the
   // 128-byte-swizzled layout of a TMA store box
@@ -163,11 +168,20 @@ struct Cfg {
   static constexpr int STG_WARP_BYTES =
       (MODE == kFinal || MODE == kSplit) ? 32 * STG_PITCH : (MODE == kTgmm ? STG_BUFS * 4096 : 0);
   static constexpr size_t CTL_BYTES = (sizeof(SmemCtl) + 1023) / 1024 * 1024;  // keeps the staging 1 KB aligned
+  // promotion: kSwSlots rows of BN weight scales, one per K block in flight
+  static constexpr int SW_RING_BYTES = PROMOTE ? kSwSlots * BN * 4 : 0;
   static constexpr size_t SMEM = 1024 + static_cast<size_t>(NSTAGE) * STAGE_BYTES + CTL_BYTES +
-                                 static_cast<size_t>(EPI_WARPS) * STG_WARP_BYTES;
+                                 static_cast<size_t>(EPI_WARPS) * STG_WARP_BYTES + SW_RING_BYTES;
   static_assert(NSTAGE <= kMaxStages && NACC >= 1 && NACC <= kMaxAcc && NACC * BN * SEGS <= TMEM_COLS &&
                     STAGE_BYTES % 1024 == 0 && BN % 32 == 0,
                 "tile configuration");
+  // the producer runs at most NSTAGE K blocks ahead of the MMA, which runs at
+  // most NACC ahead of the epilogue: every block in flight has its scale row
+  static_assert(!PROMOTE || kSwSlots >= NSTAGE + NACC, "promotion: weight-scale ring too short");
+  static_assert(!PROMOTE || EPI_WARPS == 8, "promotion epilogue: 8 warps of 32 rows x 128 columns");
+  // 384 threads launch with at most 168 registers each (three warps per SM
+  // sub-partition); the split must fit in what the CTA was launched with
+  static_assert(!PROMOTE || 128 * CTRL_REGS + 256 * EPI_REGS <= 384 * 168, "promotion register split");
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
@@ -287,7 +301,7 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const SmemCtl* ctl, in
     tl.ax = 0;
     tl.ay = tl.row0;
     tl.bx = 0;
-    if (MODE == kSwiglu) {
+    if (MODE == kSwiglu || MODE == kPromoteSwiglu) {
       // 128 h columns: wi_0 channels nt*128.. and the matching wi_1 channels
       // (a CTA pair: the even CTA holds the wi_0 rows, the odd one the wi_1 rows)
       tl.by = lo * 2 * p.F + nt * 128 + (PAIR ? rank * p.F : 0);
@@ -346,6 +360,8 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
   uint8_t* base_ptr = smem_raw + (base - raw_addr);
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(base_ptr + NSTAGE * STAGE_BYTES);
   uint8_t* stg_base = base_ptr + NSTAGE * STAGE_BYTES + C::CTL_BYTES;  // output staging (kFinal, kTgmm)
+  // promotion: ring of per-K-block weight-scale rows (BN floats each)
+  float* sw_ring = reinterpret_cast<float*>(stg_base + EPI_WARPS * C::STG_WARP_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // A CTA pair works on the same sequence of units; its even CTA (rank 0)
   // issues the MMAs and owns the full and accumulator-empty barriers.
@@ -362,6 +378,14 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
     for (int a = 0; a < NACC; ++a) {
       mbar_init(smem_u32(&ctl->tfull[a]), 1);
       mbar_init(smem_u32(&ctl->tempty[a]), (PAIR ? 2 : 1) * EPI_WARPS);
+    }
+    if (C::PROMOTE) {
+      for (int q = 0; q < kSwSlots; ++q) {
+        mbar_init(smem_u32(&ctl->sfull[q]), 1);
+        mbar_init(smem_u32(&ctl->sempty[q]), EPI_WARPS);
+      }
+      for (int q = 0; q < 4; ++q)
+        for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&ctl->xbar[q][b]), 64);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort_flag = 0;
@@ -399,23 +423,42 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
   const int total = ctl->total_tiles;
   volatile int* abort_flag = &ctl->abort_flag;
   bool timed_out = false;
-  // release of accumulator `a` by one epilogue warp (to the pair's even CTA)
+  // release of accumulator `a` by one epilogue warp (to the pair's even CTA;
+  // relaxed: it orders only tensor-memory loads that have already completed)
   auto release_acc = [&](uint32_t a) {
     if (PAIR)
-      mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[a]), 0));
+      mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&ctl->tempty[a]), 0));
     else
       mbar_arrive(smem_u32(&ctl->tempty[a]));
   };
 
+  // Roles: the control warps (producer, MMA issuer, and for promotion two
+  // idle warps) and the epilogue warps.  With promotion each role's register
+  // budget is set at the top of its own branch (a budget set before a join
+  // would bind the code after it to the smaller one).
+  if (warp < C::CTRL_WARPS) {
+  if (C::PROMOTE) setmaxnreg_dec<C::CTRL_REGS>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t it = 0;
+      const bool w_blk = C::PROMOTE && p.rhs_mode == MOE_SCALE_PER_ROW_BLOCK128;
       for (int t = unit0; t < total && !timed_out; t += units) {
         const Tile tl = get_tile<MODE, PAIR>(p, ctl, t, rank);
+        // promotion: bytes of this tile's weight-scale row per K block (a
+        // narrower last N tile copies only its columns)
+        const uint32_t sw_bytes = !w_blk ? 0u
+                                  : (MODE == kPromoteSwiglu ? 2u * 128u * 4u
+                                                            : static_cast<uint32_t>(min(BN, p.N - tl.n0)) * 4u);
         for (int kb = 0; kb < tl.nkb; ++kb) {
           const int s = it % NSTAGE;
           const uint32_t ph = (it / NSTAGE) & 1;
+          const uint32_t q = it % kSwSlots;
+          if (w_blk &&
+              !mbar_wait_bounded(smem_u32(&ctl->sempty[q]), ((it / kSwSlots) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+            timed_out = true;
+            break;
+          }
           if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1, abort_flag, kWaitLimitNs)) {
             timed_out = true;
             break;
@@ -431,12 +474,26 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
             const uint32_t fb = smem_u32(&ctl->full[s]);
             mbar_arrive_expect_tx(fb, C::TX_BYTES);
             tma_load_2d(sa, &tmA, tl.ax + kb * BK, tl.ay, fb);
-            if (MODE == kSwiglu) {
+            if (MODE == kSwiglu || MODE == kPromoteSwiglu) {
               // B rows 0..127: wi_0 channels; rows 128..255: the matching wi_1 channels
               tma_load_2d(sa + A_BYTES, &tmB, tl.bx + kb * BK, tl.by, fb);
               tma_load_2d(sa + 2 * A_BYTES, &tmB, tl.bx + kb * BK, tl.by + p.F, fb);
             } else {
               tma_load_2d(sa + A_BYTES, &tmB, tl.bx + kb * BK, tl.by, fb);
+            }
+            if (w_blk) {
+              // the K block's weight-scale row, into ring slot q (the
+              // epilogue waits for it on its own barrier)
+              const uint32_t sb = smem_u32(&ctl->sfull[q]);
+              mbar_arrive_expect_tx(sb, sw_bytes);
+              const float* row = p.rhs_scale + (static_cast<int64_t>(tl.el) * p.kblocks + kb) * p.N;
+              const uint32_t dst = smem_u32(sw_ring + q * BN);
+              if (MODE == kPromoteSwiglu) {
+                bulk_load(dst, row + tl.n0, 128 * 4, sb);                  // wi_0 channels of the tile
+                bulk_load(dst + 128 * 4, row + p.F + tl.n0, 128 * 4, sb);  // the matching wi_1 channels
+              } else {
+                bulk_load(dst, row + tl.n0, sw_bytes, sb);
+              }
             }
           }
           ++it;
@@ -451,6 +508,9 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         if (!PAIR || rank == 0)
           for (uint32_t j = (it > NSTAGE ? it - NSTAGE : 0); j < it; ++j)
             mbar_wait_bounded(smem_u32(&ctl->full[j % NSTAGE]), (j / NSTAGE) & 1, &ctl->no_abort, kWaitLimitNs);
+        if (w_blk)  // and the scale rows
+          for (uint32_t j = (it > kSwSlots ? it - kSwSlots : 0); j < it; ++j)
+            mbar_wait_bounded(smem_u32(&ctl->sfull[j % kSwSlots]), (j / kSwSlots) & 1, &ctl->no_abort, kWaitLimitNs);
       }
     }
     __syncwarp();
@@ -462,7 +522,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         const Tile tl = get_tile<MODE, PAIR>(p, ctl, t, rank);
         if (tl.nkb == 0) continue;
         uint32_t a = acc % NACC;
-        if (MODE != kPromote) {
+        if (!C::PROMOTE) {
           if (!mbar_wait_bounded(smem_u32(&ctl->tempty[a]), ((acc / NACC) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
             timed_out = true;
             break;
@@ -470,7 +530,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
           tc_fence_after();
         }
         for (int kb = 0; kb < tl.nkb; ++kb) {
-          if (MODE == kPromote) {
+          if (C::PROMOTE) {
             a = acc % NACC;
             if (!mbar_wait_bounded(smem_u32(&ctl->tempty[a]), ((acc / NACC) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
               timed_out = true;
@@ -495,7 +555,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
           const int seg_kb0 = seg1 ? p.kb_split : 0;
 #pragma unroll
           for (int k4 = 0; k4 < BK / UMMA_K; ++k4) {
-            const uint32_t accumulate = (MODE == kPromote) ? (k4 > 0) : (kb > seg_kb0 || k4 > 0);
+            const uint32_t accumulate = C::PROMOTE ? (k4 > 0) : (kb > seg_kb0 || k4 > 0);
             // +32 bytes along K inside the 128-byte swizzled row = +2 in the
             // descriptor's address field (16-byte units)
             if (PAIR)
@@ -507,14 +567,14 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
             mma_commit_pair_mc(smem_u32(&ctl->empty[s]), 0x3);  // frees the stage in both CTAs
           else
             mma_commit(smem_u32(&ctl->empty[s]));
-          if (MODE == kPromote) {
+          if (C::PROMOTE) {
             mma_commit(smem_u32(&ctl->tfull[a]));
             ++acc;
           }
           ++it;
         }
         if (timed_out) break;
-        if (MODE != kPromote) {
+        if (!C::PROMOTE) {
           if (PAIR)
             mma_commit_pair_mc(smem_u32(&ctl->tfull[a]), 0x3);
           else
@@ -534,13 +594,16 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
       }
     }
     __syncwarp();
+  }
   } else {
+    if (C::PROMOTE) setmaxnreg_inc<C::EPI_REGS>();
     // ------------------------------------------------------------ epilogue
     const int q4 = warp & 3;                            // TMEM lane quarter of this warp
-    const int half = (warp - 2) >> 2;  // column part of the warp (0 with 4 epilogue warps)
+    const int half = (warp - C::CTRL_WARPS) >> 2;  // column part of the warp (0 with 4 epilogue warps)
     const int r = q4 * 32 + lane;                       // row of the tile = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
     uint32_t acc = 0;
+    uint32_t tcount = 0;  // promotion: tiles done by this CTA
     int stg_sel = 0;  // kTgmm: staging buffer of this warp's next block
     for (int t = unit0; t < total && !timed_out; t += units) {
       const Tile tl = get_tile<MODE, PAIR>(p, ctl, t, rank);
@@ -590,7 +653,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
           tmem_wait_ld();
           // this warp's 32x32 block, staged in the swizzled box layout and
           // written by one TMA store; the staging buffers rotate
-          uint8_t* buf = stg_base + (warp - 2) * C::STG_WARP_BYTES + stg_sel * 4096;
+          uint8_t* buf = stg_base + (warp - C::CTRL_WARPS) * C::STG_WARP_BYTES + stg_sel * 4096;
           if (lane == 0) bulk_wait_read<C::STG_BUFS - 1>();  // the store last issued from `buf` has read it
           __syncwarp();
 #pragma unroll
@@ -776,7 +839,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
             f[j] = __fmul_rn(has1 ? __fmaf_rn(__uint_as_float(v1[j]), s1, p0) : p0, sa);
           }
           // stage this warp's 32x32 bf16 block, then write 8 rows (64 contiguous bytes each) per instruction
-          uint8_t* stg = stg_base + (warp - 2) * C::STG_WARP_BYTES;
+          uint8_t* stg = stg_base + (warp - C::CTRL_WARPS) * C::STG_WARP_BYTES;
 #pragma unroll
           for (int g = 0; g < 4; ++g)
             *reinterpret_cast<uint4*>(stg + lane * C::STG_PITCH + 16 * g) =
@@ -822,7 +885,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
           load_col_scales32(swb, nb, p.N, per_chan, sw_t, sw);
           tmem_wait_ld();
           // stage this warp's 32x32 bf16 block, then write 8 rows (64 contiguous bytes each) per instruction
-          uint8_t* stg = stg_base + (warp - 2) * C::STG_WARP_BYTES;
+          uint8_t* stg = stg_base + (warp - C::CTRL_WARPS) * C::STG_WARP_BYTES;
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             uint4 q;
@@ -853,159 +916,243 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         if (lane == 0) release_acc(a);
         ++acc;
       } else {
-        // promotion: one fresh accumulator per K block, folded into registers.
-        // Eight warps: TMEM lane quarter q4, columns [half*WC, half*WC + WC)
-        // of the tile (WC = BN / 2).  Only the blockwise side(s) enter the
-        // per-block update; a scale constant along K is applied at the end.
-        uint16_t* out = static_cast<uint16_t*>(p.out);
+        // promotion (a blockwise operand scale): K block kb of the tile lands
+        // in accumulator kb % 2 (the MMA runs one block ahead of this fold).
+        // Eight warps fold it into fp32 registers, each TMEM lane quarter q4
+        // (32 rows) x 128 of the tile's 256 columns: plain gmm, columns
+        // [128 half, +128); fused SwiGLU, the a0 columns [64 half, +64) and
+        // the matching a1 columns 128 + [64 half, +64).  Per element and K
+        // block: acc += (p * s_w[n]) * s_a[m] on packed fp32 pairs, with s_w
+        // from the scale row the producer copied in with the block's operands;
+        // a scale constant along K is applied once at the end.
+        constexpr bool SWG = MODE == kPromoteSwiglu;
         const int64_t row = static_cast<int64_t>(tl.row0) + r;
-        constexpr int WC = BN / (EPI_WARPS / 4);  // columns per epilogue warp
-        static_assert(MODE != kPromote || WC * EPI_WARPS <= static_cast<int>(sizeof(SmemCtl::sw_stage) / sizeof(float)),
-                      "promotion: per-warp scale staging exceeds sw_stage");
-        const int cbase = tl.n0 + half * WC;
-        float* stage = ctl->sw_stage + (warp - 2) * WC;
         const bool a_blk = p.lhs_mode == MOE_SCALE_PER_ROW_BLOCK128;
         const bool w_blk = p.rhs_mode == MOE_SCALE_PER_ROW_BLOCK128;
         const int64_t srow = row_ok ? row : 0;
-        const float* sab = p.lhs_scale + (p.lhs_mode == MOE_SCALE_PER_ROW ? srow : (a_blk ? srow * p.kblocks : 0));
-        const float* swb = p.rhs_scale + (p.rhs_mode == MOE_SCALE_PER_ROW
-                                              ? static_cast<int64_t>(tl.el) * p.N
-                                              : (w_blk ? static_cast<int64_t>(tl.el) * p.kblocks * p.N : 0));
-        uint64_t acc2[WC / 2];
-#pragma unroll
-        for (int j = 0; j < WC / 2; ++j) acc2[j] = 0ull;
-        // The scales of a K block are loaded PD blocks ahead (a register
-        // ring), so their memory latency stays off the per-block path.  The
-        // first WC/SPL lanes load SPL columns each (N and the tile's columns
-        // are multiples of 16, so a lane's columns are all in range or all
-        // past N).
-        constexpr int SPL = WC == 32 ? 1 : (WC == 64 ? 2 : 4);  // staged column scales per lane
-        constexpr int PD = WC > 64 ? 2 : 4;  // wide spans: the folded sums leave fewer registers
-        const int nw = cbase + SPL * lane;   // this lane's first staged column
-        const bool w_lane = w_blk && SPL * lane < WC && nw < p.N;
-        using WVec = typename std::conditional<SPL == 1, float, typename std::conditional<SPL == 2, float2, float4>::type>::type;
-        auto load_w = [&](int kb) -> WVec {
-          WVec w{};
-          if (w_lane && kb < tl.nkb) w = __ldg(reinterpret_cast<const WVec*>(swb + static_cast<int64_t>(kb) * p.N + nw));
-          return w;
+        const float* sab = p.lhs_scale + (a_blk ? srow * p.kblocks : 0);
+        auto ccol = [&](int c) -> int {  // first accumulator column of this warp's 16-column chunk c
+          return SWG ? (c < 4 ? 64 * half + 16 * c : 128 + 64 * half + 16 * (c - 4)) : 128 * half + 16 * c;
         };
+        uint64_t acc2[64];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) acc2[j] = 0ull;
+        constexpr int PD = 4;  // the row's activation scales are loaded PD blocks ahead (a register ring)
         auto load_a = [&](int kb) -> float { return (a_blk && kb < tl.nkb) ? __ldg(sab + kb) : 1.0f; };
-        WVec wq[PD];
         float aq[PD];
 #pragma unroll
-        for (int i = 0; i < PD; ++i) {
-          wq[i] = load_w(i);
-          aq[i] = load_a(i);
-        }
-        // Unrolled by PD so that slot i is consumed and refilled in place
-        // (moving an in-flight load between registers would wait for it).
-        for (int kb0 = 0; kb0 < tl.nkb && !timed_out; kb0 += PD) {
+        for (int i = 0; i < PD; ++i) aq[i] = load_a(i);
+        // the block loop, specialised by the operand(s) with a blockwise scale
+        auto run = [&](auto fm_tag) {
+          constexpr int FM = decltype(fm_tag)::value;  // 1: activations, 2: weights, 3: both
+          for (int kb0 = 0; kb0 < tl.nkb && !timed_out; kb0 += PD) {
+            // unrolled by PD so that ring slot i is consumed and refilled in place
 #pragma unroll
-         for (int i = 0; i < PD; ++i) {
-          const int kb = kb0 + i;
-          if (kb >= tl.nkb || timed_out) break;
-          const WVec w2 = wq[i];
-          const float sa = aq[i];
-          wq[i] = load_w(kb + PD);
-          aq[i] = load_a(kb + PD);
-          if (w_blk && SPL * lane < WC) *reinterpret_cast<WVec*>(stage + SPL * lane) = w2;
-          const uint64_t sa2 = f2_pack(sa, sa);
-          __syncwarp();
-          const uint32_t a = acc % NACC;
-          if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
-            timed_out = true;
-            break;
-          }
-          tc_fence_after();
-          auto fold16 = [&](const uint32_t* v, int j0) {  // 16 columns from column j0 of this warp's span
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {  // columns j0 + 4j .. j0 + 4j + 3
-              const uint64_t p0 = f2_pack(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]));
-              const uint64_t p1 = f2_pack(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-              uint64_t& c0 = acc2[j0 / 2 + 2 * j];
-              uint64_t& c1 = acc2[j0 / 2 + 2 * j + 1];
-              if (w_blk) {
-                const float4 sw = *reinterpret_cast<const float4*>(stage + j0 + 4 * j);  // broadcast
-                if (a_blk) {
-                  c0 = f2_fma(f2_mul(p0, f2_pack(sw.x, sw.y)), sa2, c0);
-                  c1 = f2_fma(f2_mul(p1, f2_pack(sw.z, sw.w)), sa2, c1);
-                } else {
-                  c0 = f2_fma(p0, f2_pack(sw.x, sw.y), c0);
-                  c1 = f2_fma(p1, f2_pack(sw.z, sw.w), c1);
-                }
-              } else {
-                c0 = f2_fma(p0, sa2, c0);
-                c1 = f2_fma(p1, sa2, c1);
+            for (int i = 0; i < PD; ++i) {
+              const int kb = kb0 + i;
+              if (kb >= tl.nkb) break;
+              const float sa = aq[i];
+              aq[i] = load_a(kb + PD);
+              const uint32_t a = acc % NACC;
+              const uint32_t q = acc % kSwSlots;
+              if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs) ||
+                  (FM != 1 &&
+                   !mbar_wait_bounded(smem_u32(&ctl->sfull[q]), (acc / kSwSlots) & 1, abort_flag, kWaitLimitNs))) {
+                timed_out = true;
+                break;
               }
-            }
-          };
-          if (WC == 32) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + half * WC, v);
-            tmem_wait_ld();
-            tc_fence_before();  // the accumulator is in registers: release it
-            __syncwarp();
-            if (lane == 0) release_acc(a);
-            fold16(v, 0);
-            fold16(v + 16, 16);
-          } else if (WC == 64) {
-            // the whole span fits in registers: load it, release the accumulator, then fold
-            uint32_t v[64];
-            tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + half * WC, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-            tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + half * WC + 32,
-                               *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) release_acc(a);
-#pragma unroll
-            for (int c = 0; c < WC / 16; ++c) fold16(v + 16 * c, 16 * c);
-          } else {
-            // wider spans: fold 16 columns at a time, release after the last load
-#pragma unroll
-            for (int c = 0; c < WC / 16; ++c) {
-              uint32_t v[16];
-              tmem_ld_32x32b_x16(tmem_base + lane_addr + a * BN + half * WC + 16 * c, v);
+              tc_fence_after();
+              const float* sw = sw_ring + q * BN;
+              const uint64_t sa2 = f2_pack(sa, sa);
+              const uint32_t tb = tmem_base + lane_addr + a * BN;
+              uint32_t u[2][16];
+              tmem_ld_32x32b_x16(tb + ccol(0), u[0]);
               tmem_wait_ld();
-              if (c == WC / 16 - 1) {
-                tc_fence_before();
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                // the next chunk's load is in flight while this one is folded
+                if (c + 1 < 8) tmem_ld_32x32b_x16(tb + ccol(c + 1), u[(c + 1) & 1]);
+                const uint32_t* v = u[c & 1];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const uint64_t p0 = f2_pack(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]));
+                  const uint64_t p1 = f2_pack(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                  uint64_t& c0 = acc2[8 * c + 2 * j];
+                  uint64_t& c1 = acc2[8 * c + 2 * j + 1];
+                  if (FM == 1) {
+                    c0 = f2_fma(p0, sa2, c0);
+                    c1 = f2_fma(p1, sa2, c1);
+                  } else {
+                    const float4 w4 = *reinterpret_cast<const float4*>(sw + ccol(c) + 4 * j);  // broadcast
+                    if (FM == 3) {
+                      c0 = f2_fma(f2_mul(p0, f2_pack(w4.x, w4.y)), sa2, c0);
+                      c1 = f2_fma(f2_mul(p1, f2_pack(w4.z, w4.w)), sa2, c1);
+                    } else {
+                      c0 = f2_fma(p0, f2_pack(w4.x, w4.y), c0);
+                      c1 = f2_fma(p1, f2_pack(w4.z, w4.w), c1);
+                    }
+                  }
+                }
+                tmem_wait_ld();
+                if (c == 6) {  // the last chunk has landed too: the accumulator is free
+                  tc_fence_before();
+                  __syncwarp();
+                  if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
+                }
+              }
+              if (FM != 1) {  // this warp is done with the scale row
                 __syncwarp();
-                if (lane == 0) release_acc(a);
+                if (lane == 0) mbar_arrive(smem_u32(&ctl->sempty[q]));
               }
-              fold16(v, 16 * c);
+              ++acc;
             }
           }
-          ++acc;
-          __syncwarp();  // the staged scales are read before the next block overwrites them
-         }
-        }
+        };
+        if (a_blk && w_blk)
+          run(std::integral_constant<int, 3>{});
+        else if (w_blk)
+          run(std::integral_constant<int, 2>{});
+        else
+          run(std::integral_constant<int, 1>{});
         if (timed_out) break;
-        if (row_ok) {
-          const float sa_end = a_blk ? 1.0f : __ldg(sab);
-          const bool w_col = p.rhs_mode == MOE_SCALE_PER_ROW;
-          const float sw_t = (w_blk || w_col) ? 1.0f : __ldg(p.rhs_scale);
+        // scales constant along K: per row / per tensor for the activations,
+        // per channel / per tensor for the weights (1 for a blockwise side)
+        const float sa_end = a_blk ? 1.0f
+                                   : (row_ok ? (p.lhs_mode == MOE_SCALE_PER_ROW ? __ldg(p.lhs_scale + row)
+                                                                                 : __ldg(p.lhs_scale))
+                                             : 0.0f);
+        const bool w_col = p.rhs_mode == MOE_SCALE_PER_ROW;
+        const float* swb = p.rhs_scale + (w_col ? static_cast<int64_t>(tl.el) * p.N : 0);
+        const float sw_t = (w_blk || w_col) ? 1.0f : __ldg(p.rhs_scale);
+        // 16 output values of chunk c as gmm_fp8 stores them: bf16((acc s_a) s_w)
+        auto chunk_vals = [&](int c, float* f) {
+          const int n = tl.n0 + ccol(c);  // weight channel (plain gmm)
 #pragma unroll
-          for (int c = 0; c < WC / 16; ++c) {
-            const int nb = cbase + c * 16;  // N is a multiple of 16: the 16 columns are all in range or all past N
-            if (nb < p.N) {
-              uint32_t pk[8];
+          for (int g = 0; g < 4; ++g) {
+            float4 w4 = make_float4(sw_t, sw_t, sw_t, sw_t);
+            if (w_col) {
+              // SwiGLU tiles: accumulator columns 0..127 are wi_0 channels n0.., 128..255 wi_1 channels F + n0..
+              const int ch = SWG ? (ccol(c) < 128 ? tl.n0 + ccol(c) : p.F + tl.n0 + ccol(c) - 128) : n;
+              w4 = __ldg(reinterpret_cast<const float4*>(swb + ch) + g);
+            }
+            float x0, x1, x2, x3;
+            f2_unpack(acc2[8 * c + 2 * g], x0, x1);
+            f2_unpack(acc2[8 * c + 2 * g + 1], x2, x3);
+            f[4 * g] = __fmul_rn(__fmul_rn(x0, sa_end), w4.x);
+            f[4 * g + 1] = __fmul_rn(__fmul_rn(x1, sa_end), w4.y);
+            f[4 * g + 2] = __fmul_rn(__fmul_rn(x2, sa_end), w4.z);
+            f[4 * g + 3] = __fmul_rn(__fmul_rn(x3, sa_end), w4.w);
+          }
+        };
+        if (!SWG) {
+          if (row_ok) {
+            uint16_t* out = static_cast<uint16_t*>(p.out);
 #pragma unroll
-              for (int g = 0; g < 4; ++g) {  // columns nb + 4g .. nb + 4g + 3
-                float4 w4 = make_float4(sw_t, sw_t, sw_t, sw_t);
-                if (w_col) w4 = __ldg(reinterpret_cast<const float4*>(swb + nb) + g);
-                float f0, f1, f2, f3;
-                f2_unpack(acc2[c * 8 + 2 * g], f0, f1);
-                f2_unpack(acc2[c * 8 + 2 * g + 1], f2, f3);
-                pk[2 * g] = pack_bf16x2(__fmul_rn(__fmul_rn(f0, sa_end), w4.x), __fmul_rn(__fmul_rn(f1, sa_end), w4.y));
-                pk[2 * g + 1] =
-                    pack_bf16x2(__fmul_rn(__fmul_rn(f2, sa_end), w4.z), __fmul_rn(__fmul_rn(f3, sa_end), w4.w));
+            for (int c = 0; c < 8; ++c) {
+              const int nb = tl.n0 + ccol(c);  // N is a multiple of 16: the chunk is all in range or all past N
+              if (nb < p.N) {
+                float f[16];
+                chunk_vals(c, f);
+                uint32_t pk[8];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) pk[g] = pack_bf16x2(f[2 * g], f[2 * g + 1]);
+                uint16_t* dst = out + row * p.N + nb;
+                *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4*>(dst + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
               }
-              uint16_t* dst = out + row * p.N + nb;
-              *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              *reinterpret_cast<uint4*>(dst + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+          }
+        } else {
+          // fused SwiGLU: this thread holds a0 and a1 of h columns
+          // n0 + 64 half + [0, 64) of its row; h = bf16(silu(a0) a1) and its
+          // codes as moe_swiglu_quant makes them from the stored a
+          float hs = 1.0f, hinv = 1.0f;
+          if (p.h_mode == MOE_SCALE_PER_TENSOR) {
+            hs = __ldg(p.h_static);
+            hinv = __frcp_rn(hs);
+          }
+          float amax = 0.0f;
+          uint32_t hp[32];  // the 64 h values as bf16 pairs (per-128 h scales)
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            float f0[16], f1[16], h[16];
+            uint32_t hb[8];
+            chunk_vals(cc, f0);
+            chunk_vals(cc + 4, f1);
+            uint32_t a0b[8], a1b[8];
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              a0b[g] = pack_bf16x2(f0[2 * g], f0[2 * g + 1]);
+              a1b[g] = pack_bf16x2(f1[2 * g], f1[2 * g + 1]);
+              f0[2 * g] = bf16lo(a0b[g]);
+              f0[2 * g + 1] = bf16hi(a0b[g]);
+              f1[2 * g] = bf16lo(a1b[g]);
+              f1[2 * g + 1] = bf16hi(a1b[g]);
+            }
+            swiglu_h_x2<16>(f0, f1, h, hb);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(h[j]));
+            const int hc = tl.n0 + 64 * half + 16 * cc;  // first h column of the chunk
+            if (row_ok) {
+              if (p.a_out) {
+                uint4* d0 = reinterpret_cast<uint4*>(p.a_out + row * 2 * p.F + hc);
+                uint4* d1 = reinterpret_cast<uint4*>(p.a_out + row * 2 * p.F + p.F + hc);
+                d0[0] = make_uint4(a0b[0], a0b[1], a0b[2], a0b[3]);
+                d0[1] = make_uint4(a0b[4], a0b[5], a0b[6], a0b[7]);
+                d1[0] = make_uint4(a1b[0], a1b[1], a1b[2], a1b[3]);
+                d1[1] = make_uint4(a1b[4], a1b[5], a1b[6], a1b[7]);
+              }
+              if (p.h_mode == MOE_SCALE_PER_ROW) {
+                uint4* dh = reinterpret_cast<uint4*>(p.h_out + row * p.F + hc);
+                dh[0] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+                dh[1] = make_uint4(hb[4], hb[5], hb[6], hb[7]);
+              } else if (p.h_mode == MOE_SCALE_PER_TENSOR) {
+                float qv[16];
+                quant_n<16>(h, hs, hinv, qv);
+                const uint2 lo8 = pack_e4m3x8(qv), hi8 = pack_e4m3x8(qv + 8);
+                *reinterpret_cast<uint4*>(p.h_q + row * p.F + hc) = make_uint4(lo8.x, lo8.y, hi8.x, hi8.y);
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) hp[cc * 8 + j] = hb[j];
+          }
+          const int par = tcount & 1;
+          if (p.h_mode == MOE_SCALE_PER_ROW) {
+            // non-negative floats order like their bit patterns
+            if (row_ok) atomicMax(reinterpret_cast<unsigned int*>(p.h_scale) + row, __float_as_uint(amax));
+          } else if (p.h_mode == MOE_SCALE_PER_ROW_BLOCK128) {
+            // the tile's 128 h columns are one 128-column scale block, split
+            // over the two warps of this lane quarter: exchange their maxima
+            // (a bounded wait on a barrier of the pair of warps; the two
+            // parities alternate between tiles)
+            ctl->pamax[par][q4][half][lane] = amax;
+            mbar_arrive(smem_u32(&ctl->xbar[q4][par]));
+            if (!mbar_wait_bounded(smem_u32(&ctl->xbar[q4][par]), (tcount >> 1) & 1, abort_flag, kWaitLimitNs)) {
+              timed_out = true;
+              break;
+            }
+            const float m = fmaxf(amax, ctl->pamax[par][q4][half ^ 1][lane]);
+            if (row_ok) {
+              const float sblk = absmax_scale(m);
+              const float inv = __frcp_rn(sblk);
+              if (half == 0) p.h_scale[row * (p.F / 128) + tl.n0 / 128] = sblk;
+              float x16[16], qv[16];
+              uint4* dst = reinterpret_cast<uint4*>(p.h_q + row * p.F + tl.n0 + half * 64);
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  x16[2 * j] = bf16lo(hp[g * 8 + j]);
+                  x16[2 * j + 1] = bf16hi(hp[g * 8 + j]);
+                }
+                quant_n<16>(x16, sblk, inv, qv);
+                const uint2 lo8 = pack_e4m3x8(qv), hi8 = pack_e4m3x8(qv + 8);
+                dst[g] = make_uint4(lo8.x, lo8.y, hi8.x, hi8.y);
+              }
             }
           }
         }
+        ++tcount;
       }
     }
     if (timed_out) {
@@ -1441,6 +1588,14 @@ moe_status launch_mma(const CUtensorMap& A, const CUtensorMap& B, const CUtensor
   auto kernel = mma_kernel<MODE, PAIR_REQ>;
   MOE_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(C::SMEM)));
+  if (C::PROMOTE) {
+    // the register split may only hand out what the CTA is launched with
+    cudaFuncAttributes fa{};
+    MOE_CUDA_TRY(cudaFuncGetAttributes(&fa, kernel));
+    if (static_cast<int64_t>(fa.numRegs) * C::THREADS <
+        128ll * C::CTRL_REGS + 32ll * C::EPI_WARPS * C::EPI_REGS)
+      return MOE_ERR_UNSUPPORTED;
+  }
   const int sms = sm_count();
   if (sms <= 0) return MOE_ERR_CUDA;
   if (max_units <= 0) max_units = 1;
@@ -1610,9 +1765,10 @@ extern "C" moe_status gmm_fp8_swiglu(const uint8_t* lhs_q, const float* lhs_scal
                                      uint16_t* a_out, uint16_t* h, uint8_t* h_q, float* h_scale,
                                      moe_stream_t stream) {
   MOE_HOST_CHECK(lhs_q && lhs_scale && rhs_q && rhs_scale && group_sizes && h_q, MOE_ERR_INVALID_ARG);
-  MOE_HOST_CHECK((lhs_mode == MOE_SCALE_PER_ROW || lhs_mode == MOE_SCALE_PER_TENSOR) &&
-                     (rhs_mode == MOE_SCALE_PER_ROW || rhs_mode == MOE_SCALE_PER_TENSOR),
-                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(valid_lhs_mode(lhs_mode) && valid_lhs_mode(rhs_mode), MOE_ERR_INVALID_ARG);
+  // a blockwise operand scale: the promotion kernel with the SwiGLU epilogue
+  const bool blockwise = lhs_mode == MOE_SCALE_PER_ROW_BLOCK128 || rhs_mode == MOE_SCALE_PER_ROW_BLOCK128;
+  MOE_HOST_CHECK(!blockwise || K % 128 == 0, MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(E > 0 && E <= kMaxGroups && group_offset >= 0 && E_local > 0 && group_offset + E_local <= E,
                  MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(M >= 0 && M < (1ll << 31) && K > 0 && K % 16 == 0 && K < (1 << 30) && F > 0 && F % 128 == 0 &&
@@ -1626,7 +1782,7 @@ extern "C" moe_status gmm_fp8_swiglu(const uint8_t* lhs_q, const float* lhs_scal
     MOE_HOST_CHECK(h_mode == MOE_SCALE_PER_TENSOR && h_static_scale, MOE_ERR_INVALID_ARG);
   }
   MOE_HOST_CHECK(aligned16(lhs_q) && aligned16(rhs_q) && aligned16(h_q) && (!a_out || aligned16(a_out)) &&
-                     (rhs_mode != MOE_SCALE_PER_ROW || aligned16(rhs_scale)),
+                     (rhs_mode == MOE_SCALE_PER_TENSOR || aligned16(rhs_scale)),
                  MOE_ERR_INVALID_ARG);
   if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
   cudaStream_t st = as_stream(stream);
@@ -1661,9 +1817,12 @@ extern "C" moe_status gmm_fp8_swiglu(const uint8_t* lhs_q, const float* lhs_scal
   p.h_out = h;
   p.h_q = h_q;
   p.h_scale = h_scale;
-  moe_status stt = K >= kPairMinK
-                       ? launch_mma<kSwiglu, true>(A, B, A, p, gmm_max_units<kSwiglu, true>(M, E_local, p.ntiles), st)
-                       : launch_mma<kSwiglu, false>(A, B, A, p, gmm_max_units<kSwiglu, false>(M, E_local, p.ntiles), st);
+  moe_status stt =
+      blockwise ? launch_mma<kPromoteSwiglu, false>(A, B, A, p, gmm_max_units<kPromoteSwiglu, false>(M, E_local, p.ntiles),
+                                                    st)
+      : K >= kPairMinK
+          ? launch_mma<kSwiglu, true>(A, B, A, p, gmm_max_units<kSwiglu, true>(M, E_local, p.ntiles), st)
+          : launch_mma<kSwiglu, false>(A, B, A, p, gmm_max_units<kSwiglu, false>(M, E_local, p.ntiles), st);
   if (stt != MOE_OK) return stt;
   if (h_mode == MOE_SCALE_PER_ROW) {
     const int npair = static_cast<int>(F / 16);  // F is a multiple of 128

@@ -237,19 +237,25 @@ moe_status gmm_fp8_ksplit(const uint8_t* lhs_q, const float* lhs_scale, moe_scal
  * (rhs = [wi_0 | wi_1], N = 2F) followed by moe_swiglu_quant: every output tile
  * holds matching wi_0 and wi_1 channels, a0 and a1 are rounded to bf16 exactly
  * as gmm_fp8 stores them, and h = bf16(silu(a0) a1) is computed the same way.
- *   lhs_q e4m3 [M, K], lhs_scale PER_ROW [M] or PER_TENSOR [1]
+ *   lhs_q e4m3 [M, K], lhs_scale PER_ROW [M], PER_ROW_BLOCK128 [M, K/128] or
+ *         PER_TENSOR [1]
  *   rhs_q e4m3 [E_local, 2F, K] (wi_0 channels, then wi_1 channels),
- *         rhs_scale PER_ROW (per channel) [E_local, 2F] or PER_TENSOR [1]
+ *         rhs_scale PER_ROW (per channel) [E_local, 2F], PER_ROW_BLOCK128
+ *         (blockwise) [E_local, K/128, 2F] or PER_TENSOR [1]
  *   h_mode PER_ROW: h_scale [M]; `h` is bf16 [M, F] scratch that receives h
  *          (the row's scale needs all of its F columns first)
- *   h_mode PER_ROW_BLOCK128: h_scale [M, F/128], fully fused (h may be NULL)
+ *   h_mode PER_ROW_BLOCK128: h_scale [M, F/128], fully fused (h may be NULL):
+ *          a 128-column h block is one output tile
  *   h_mode PER_TENSOR: h_static_scale [1], fully fused (h may be NULL)
  *   h_q   e4m3 [M, F]
  *   a_out optional bf16 [M, 2F]: also store a = [a0 | a1] (for a backward pass)
+ * With a blockwise operand scale ("Keep qwix out of tpu-inference's fused MoE
+ * kernel and pre-quantize weights": [E, blocks, 1, N] weight scales) each
+ * 128-wide K block is scaled and summed in fp32 registers, as in gmm_fp8.
  * Rows outside groups [group_offset, group_offset + E_local) get zero codes
- * and scale 1; a_out and h are not written there.  F % 128 == 0, K % 16 == 0,
- * sum(group_sizes) == M, E <= 1024; blockwise operand scales are not fused
- * (use gmm_fp8 + moe_swiglu_quant).  MOE_ERR_UNSUPPORTED off sm_103. */
+ * and scale 1; a_out and h are not written there.  F % 128 == 0, K % 16 == 0
+ * (K % 128 == 0 with a blockwise scale), sum(group_sizes) == M, E <= 1024.
+ * MOE_ERR_UNSUPPORTED off sm_103. */
 moe_status gmm_fp8_swiglu(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode,
                           const uint8_t* rhs_q, const float* rhs_scale, moe_scale_mode rhs_mode,
                           const int32_t* group_sizes, int E, int group_offset, int E_local, int64_t M, int64_t K,

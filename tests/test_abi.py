@@ -66,10 +66,13 @@ def test_host_side_argument_checks_of_the_fused_and_backward_entries(lib):
     # one violated condition each; all are caught before any CUDA call
     raw = ctypes.create_string_buffer(512)
     p = ctypes.c_void_p((ctypes.addressof(raw) + 15) & ~15)  # a 16-byte aligned host address
-    # gmm_fp8_swiglu: null lhs; F not a multiple of 128; blockwise lhs scales
+    # gmm_fp8_swiglu: null lhs; F not a multiple of 128; blockwise lhs scales with K % 128 != 0;
+    # an unknown scale mode
     assert lib.gmm_fp8_swiglu(None, p, 0, p, p, 0, p, 1, 0, 1, 1, 128, 128, 0, None, None, p, p, p, None) == 1
     assert lib.gmm_fp8_swiglu(p, p, 0, p, p, 0, p, 1, 0, 1, 1, 128, 64, 0, None, None, p, p, p, None) == 1
-    assert lib.gmm_fp8_swiglu(p, p, 1, p, p, 0, p, 1, 0, 1, 1, 128, 128, 0, None, None, p, p, p, None) == 1
+    assert lib.gmm_fp8_swiglu(p, p, 1, p, p, 0, p, 1, 0, 1, 1, 144, 128, 0, None, None, p, p, p, None) == 1
+    assert lib.gmm_fp8_swiglu(p, p, 0, p, p, 1, p, 1, 0, 1, 1, 144, 128, 0, None, None, p, p, p, None) == 1
+    assert lib.gmm_fp8_swiglu(p, p, 3, p, p, 0, p, 1, 0, 1, 1, 128, 128, 0, None, None, p, p, p, None) == 1
     # gmm_fp8_ksplit: K_split not a multiple of 128; K_split past K
     assert lib.gmm_fp8_ksplit(p, p, 0, p, p, 100, p, 1, 0, 1, 1, 256, 256, p, None) == 1
     assert lib.gmm_fp8_ksplit(p, p, 0, p, p, 384, p, 1, 0, 1, 1, 256, 256, p, None) == 1

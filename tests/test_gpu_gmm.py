@@ -45,6 +45,9 @@ def make_case(seed, M, K, N, E, amode, wmode, zero_frac=0.25):
     (256, 256, 128, 2, RB, R0),
     (1500, 1024, 768, 16, R0, R0),
     (2048, 2048, 1536, 128, R0, RB),  # prefill-chunk shaped, E = 128
+    (1000, 1024, 272, 7, RB, RB),    # promotion: an N tail of 16 past the 256-column tile
+    (600, 7168, 512, 3, RB, RB),     # promotion: K = 7168 (56 K blocks, the scale ring wraps)
+    (130, 256, 256, 2, RB, RT),      # per-128 lhs, static rhs
     # K >= 3072 runs on CTA pairs: odd M-tile counts leave the odd CTA past its group
     (700, 4096, 512, 5, R0, R0),
     (129, 3072, 272, 2, RT, R0),     # one pair per group, N tail inside the pair's B halves
@@ -219,12 +222,19 @@ def test_tgmm_gcq_equals_quantize_then_tgmm(M, K, N, E, g0, El):
     (700, 4096, 256, 5, R0, R0, R0, None),
     (700, 4096, 256, 5, RT, RT, RT, (1, 3)),
     (450, 3072, 384, 3, R0, R0, RB, None),
+    # a blockwise operand scale: the promotion kernel with the SwiGLU epilogue
+    (384, 384, 256, 3, RB, RB, RB, None),      # DeepSeek-V3 style: per-128 x, h and blockwise weights
+    (700, 1024, 384, 6, RB, RB, RB, (1, 4)),
+    (700, 1024, 256, 5, R0, RB, R0, None),     # prefill style: per-token x and h, blockwise weights
+    (300, 256, 128, 2, RB, R0, RB, None),
+    (640, 512, 384, 8, RB, RB, RT, None),
+    (1, 128, 128, 1, RB, RB, RB, None),
 ])
 def test_gmm_swiglu_equals_gmm_then_swiglu(M, K, F, E, amode, wmode, hmode, shard):
     sizes, a, w, sa, sw = make_case(M + K + F + E + hmode, M, K, 2 * F, E, amode, wmode, zero_frac=0.2)
     g0, El = shard if shard else (0, E)
     w = np.ascontiguousarray(w[g0:g0 + El])
-    if wmode == R0:
+    if wmode in (R0, RB):
         sw = np.ascontiguousarray(sw[g0:g0 + El])
     # give a0/a1 a realistic O(1..5) spread so that silu and the scales are exercised
     sa = (sa * 4).astype(np.float32)
