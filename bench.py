@@ -315,7 +315,7 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
         s = moe.quantize_sort(x, ids, E, cfg.act_mode, sx, out=buf.sort)
         xs_s = s["xs_scale"] if cfg.act_mode != 2 else sx
         ev[0].record(stream)
-        if moe.swiglu_fusable(cfg.act_mode, W.in_mode, cfg.F):
+        if moe.swiglu_fuse_pays(cfg.act_mode, W.in_mode, cfg.F):
             moe.gmm_swiglu(s["xs_q"], xs_s, cfg.act_mode, W.w_in, W.s_in, W.in_mode, s["group_sizes"], cfg.act_mode,
                            sh, h=buf.h, h_q=buf.h_q, h_scale=buf.h_s)
             ev[1].record(stream)
@@ -423,7 +423,7 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
                "note": "public ffn_forward per step; inputs copied in from pinned host memory and y copied out "
                        "every step, on their own streams, double-buffered across steps"}
 
-    fused = moe.swiglu_fusable(cfg.act_mode, W.in_mode, cfg.F)
+    fused = moe.swiglu_fuse_pays(cfg.act_mode, W.in_mode, cfg.F)
     # quantise + sort 4 (histogram, scan, scatter, quantise-gather) + (fused gmm+SwiGLU 1, +1 code
     # pass for per-row h scales | gmm 1 + SwiGLU 1) + gmm 1 + combine 1
     launches_per_step = 4 + ((1 + (1 if cfg.act_mode == 0 else 0)) if fused else 2) + 1 + 1
@@ -588,7 +588,8 @@ def run_suite(args):
         w = torch.from_numpy(w_np).to(dev)
         buf = moe.FFNBuffers(T, D, E, k, F, cfg.act_mode, dev, backward=cfg.backward)
         am = cfg.act_mode
-        fused = moe.swiglu_fusable(am, W.in_mode, F)
+        fused = moe.swiglu_fuse_pays(am, W.in_mode, F)
+        fusable = moe.swiglu_fusable(am, W.in_mode, F)
         moe.ffn_forward(x, ids, w, W, am, buf, sx, sh)  # fills every intermediate
         torch.cuda.synchronize()
         nb = lambda c: (c + 127) // 128
@@ -604,7 +605,7 @@ def run_suite(args):
                                                                out=buf.sort),
              "hbm", T * D + R * D + 16 * R + 2 * sbytes(T, D)),
         ]
-        if fused:
+        if fusable:
             calls.append(("gmm_fp8_swiglu (wi_0|wi_1 + SwiGLU + requant)",
                           lambda: moe.gmm_swiglu(buf.sort["xs_q"], xs_s, am, W.w_in, W.s_in, W.in_mode,
                                                  buf.sort["group_sizes"], am, sh, h=buf.h, h_q=buf.h_q,
@@ -668,8 +669,11 @@ def run_suite(args):
                     bound, ach, peak, unit = "hbm", nbytes / (ms / 1e3) / 1e9, hbm, "GB/s"
                 else:
                     ach, peak, unit = flops / (ms / 1e3) / 1e12, fp8, "TFLOP/s"
-            on_path = not ((fused and label in ("gmm_fp8 wi_0|wi_1", "moe_swiglu_quant")) or
-                           label in ("quantize_rows x", "ragged_sort (+ gather)"))
+            if label.startswith("gmm_fp8_swiglu"):
+                on_path = fused
+            else:
+                on_path = not ((fused and label in ("gmm_fp8 wi_0|wi_1", "moe_swiglu_quant")) or
+                               label in ("quantize_rows x", "ragged_sort (+ gather)"))
             if on_path:
                 total += ms
             line = {"suite": cfg.name, "call": label, "ms": round(ms, 4), "bound": bound,

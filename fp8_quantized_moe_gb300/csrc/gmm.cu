@@ -103,7 +103,7 @@ struct SmemCtl {
   int tile_prefix[kMaxGroups + 1];  // gmm: first tile of local group
   int gsize[kMaxGroups];
   // per-mode scratch (one mode per kernel)
-  alignas(16) float pamax[2][4][2][32];  // fused SwiGLU, per-128 h scales: row maxima of the two column halves
+  alignas(16) float pamax[2][4][4][32];  // fused SwiGLU, per-128 h scales: row maxima of the column parts
 };
 static_assert(offsetof(SmemCtl, pamax) % 16 == 0, "SmemCtl alignment");
 static_assert(sizeof(SmemCtl) % 16 == 0, "SmemCtl size");
@@ -121,6 +121,9 @@ static_assert(sizeof(SmemCtl) % 16 == 0, "SmemCtl size");
 // accumulators.
 #ifndef MOE_PROMOTE_EPI_WARPS
 #define MOE_PROMOTE_EPI_WARPS 8
+#endif
+#ifndef MOE_PROMOTE_CHUNK
+#define MOE_PROMOTE_CHUNK 32
 #endif
 #ifndef MOE_TGMM_EPI_WARPS
 #define MOE_TGMM_EPI_WARPS 8
@@ -158,8 +161,11 @@ struct Cfg {
   static constexpr int CTRL_WARPS = PROMOTE ? 4 : 2;
   static constexpr int THREADS = 32 * (CTRL_WARPS + EPI_WARPS);
   // promotion register split: the control warpgroup gives registers to the
-  // two epilogue warpgroups, whose 128 running sums per thread need them
-  static constexpr uint32_t CTRL_REGS = 40, EPI_REGS = 232;
+  // epilogue warpgroups, whose running sums (256 / (EPI_WARPS / 4) per
+  // thread) need them
+  static constexpr int LAUNCH_REGS = (65536 / THREADS) & ~7;  // what a thread is launched with at most
+  static constexpr uint32_t CTRL_REGS = EPI_WARPS == 8 ? 40 : 32;
+  static constexpr uint32_t EPI_REGS = ((LAUNCH_REGS * THREADS - 128 * CTRL_REGS) / (32 * EPI_WARPS)) & ~7u;
   // per-warp staging of 32x32 output blocks: kFinal, bf16 rows padded to 80
   // bytes for row-contiguous stores; kTgmm, two 4 KB fp32 blocks in the
   // 128-byte-swizzled layout of a TMA store box
@@ -178,10 +184,12 @@ struct Cfg {
   // the producer runs at most NSTAGE K blocks ahead of the MMA, which runs at
   // most NACC ahead of the epilogue: every block in flight has its scale row
   static_assert(!PROMOTE || kSwSlots >= NSTAGE + NACC, "promotion: weight-scale ring too short");
-  static_assert(!PROMOTE || EPI_WARPS == 8, "promotion epilogue: 8 warps of 32 rows x 128 columns");
-  // 384 threads launch with at most 168 registers each (three warps per SM
-  // sub-partition); the split must fit in what the CTA was launched with
-  static_assert(!PROMOTE || 128 * CTRL_REGS + 256 * EPI_REGS <= 384 * 168, "promotion register split");
+  static_assert(!PROMOTE || EPI_WARPS == 8 || EPI_WARPS == 16, "promotion epilogue: 8 or 16 warps");
+  // the split must fit in what the CTA is launched with (the host also
+  // checks the kernel's actual register count before the launch)
+  static_assert(!PROMOTE || (128 * CTRL_REGS + 32 * EPI_WARPS * EPI_REGS <= LAUNCH_REGS * THREADS &&
+                             EPI_REGS <= 255 && EPI_REGS >= 96),
+                "promotion register split");
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
@@ -385,7 +393,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         mbar_init(smem_u32(&ctl->sempty[q]), EPI_WARPS);
       }
       for (int q = 0; q < 4; ++q)
-        for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&ctl->xbar[q][b]), 64);
+        for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&ctl->xbar[q][b]), EPI_WARPS / 4 * 32);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort_flag = 0;
@@ -918,94 +926,118 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
       } else {
         // promotion (a blockwise operand scale): K block kb of the tile lands
         // in accumulator kb % 2 (the MMA runs one block ahead of this fold).
-        // Eight warps fold it into fp32 registers, each TMEM lane quarter q4
-        // (32 rows) x 128 of the tile's 256 columns: plain gmm, columns
-        // [128 half, +128); fused SwiGLU, the a0 columns [64 half, +64) and
-        // the matching a1 columns 128 + [64 half, +64).  Per element and K
-        // block: acc += (p * s_w[n]) * s_a[m] on packed fp32 pairs, with s_w
-        // from the scale row the producer copied in with the block's operands;
-        // a scale constant along K is applied once at the end.
+        // The epilogue warps fold it into fp32 registers: TMEM lane quarter
+        // q4 (32 rows) x WC of the tile's 256 columns per warp -- plain gmm,
+        // columns [WC part, +WC); fused SwiGLU, the a0 columns [WC/2 part,
+        // +WC/2) and the matching a1 columns 128 + [WC/2 part, +WC/2).  Per
+        // element and K block: acc += (p * s_w[n]) * s_a[m] on packed fp32
+        // pairs, with s_w from the scale row the producer copied in with the
+        // block's operands; a scale constant along K is applied at the end.
         constexpr bool SWG = MODE == kPromoteSwiglu;
+        constexpr int NPART = EPI_WARPS / 4;  // warps per lane quarter
+        constexpr int WC = BN / NPART;        // accumulator columns per warp
+        constexpr int CWID = MOE_PROMOTE_CHUNK;  // columns per TMEM load
+        constexpr int NCH = WC / CWID;           // chunks per warp
+        constexpr bool DBUF = NPART == 1 || NPART == 2;  // double-buffered chunk loads (room in registers)
+        const int part = half;
         const int64_t row = static_cast<int64_t>(tl.row0) + r;
         const bool a_blk = p.lhs_mode == MOE_SCALE_PER_ROW_BLOCK128;
         const bool w_blk = p.rhs_mode == MOE_SCALE_PER_ROW_BLOCK128;
         const int64_t srow = row_ok ? row : 0;
         const float* sab = p.lhs_scale + (a_blk ? srow * p.kblocks : 0);
-        auto ccol = [&](int c) -> int {  // first accumulator column of this warp's 16-column chunk c
-          return SWG ? (c < 4 ? 64 * half + 16 * c : 128 + 64 * half + 16 * (c - 4)) : 128 * half + 16 * c;
+        auto ccol = [&](int c) -> int {  // first accumulator column of this warp's chunk c
+          return SWG ? (c < NCH / 2 ? (WC / 2) * part + CWID * c : 128 + (WC / 2) * part + CWID * (c - NCH / 2))
+                     : WC * part + CWID * c;
         };
-        uint64_t acc2[64];
+        // first accumulator column of 16-column group g of this warp (for the tails)
+        auto gcol = [&](int g) -> int {
+          return SWG ? (g < WC / 32 ? (WC / 2) * part + 16 * g : 128 + (WC / 2) * part + 16 * (g - WC / 32))
+                     : WC * part + 16 * g;
+        };
+        uint64_t acc2[WC / 2];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) acc2[j] = 0ull;
-        constexpr int PD = 4;  // the row's activation scales are loaded PD blocks ahead (a register ring)
+        for (int j = 0; j < WC / 2; ++j) acc2[j] = 0ull;
+        // the row's activation scale of the next K block is requested while
+        // this block is folded (a block's fold outlasts the load's latency)
         auto load_a = [&](int kb) -> float { return (a_blk && kb < tl.nkb) ? __ldg(sab + kb) : 1.0f; };
-        float aq[PD];
-#pragma unroll
-        for (int i = 0; i < PD; ++i) aq[i] = load_a(i);
+        float sa_next = load_a(0);
         // the block loop, specialised by the operand(s) with a blockwise scale
         auto run = [&](auto fm_tag) {
           constexpr int FM = decltype(fm_tag)::value;  // 1: activations, 2: weights, 3: both
-          for (int kb0 = 0; kb0 < tl.nkb && !timed_out; kb0 += PD) {
-            // unrolled by PD so that ring slot i is consumed and refilled in place
+          auto fold16 = [&](const uint64_t* v, int c, const float* sw, uint64_t sa2) {  // one chunk of column pairs
 #pragma unroll
-            for (int i = 0; i < PD; ++i) {
-              const int kb = kb0 + i;
-              if (kb >= tl.nkb) break;
-              const float sa = aq[i];
-              aq[i] = load_a(kb + PD);
-              const uint32_t a = acc % NACC;
-              const uint32_t q = acc % kSwSlots;
-              if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs) ||
-                  (FM != 1 &&
-                   !mbar_wait_bounded(smem_u32(&ctl->sfull[q]), (acc / kSwSlots) & 1, abort_flag, kWaitLimitNs))) {
-                timed_out = true;
-                break;
+            for (int j = 0; j < CWID / 4; ++j) {
+              const uint64_t p0 = v[2 * j], p1 = v[2 * j + 1];
+              uint64_t& c0 = acc2[(CWID / 2) * c + 2 * j];
+              uint64_t& c1 = acc2[(CWID / 2) * c + 2 * j + 1];
+              if (FM == 1) {
+                c0 = f2_fma(p0, sa2, c0);
+                c1 = f2_fma(p1, sa2, c1);
+              } else {
+                const float4 w4 = *reinterpret_cast<const float4*>(sw + ccol(c) + 4 * j);  // broadcast
+                if (FM == 3) {
+                  c0 = f2_fma(f2_mul(p0, f2_pack(w4.x, w4.y)), sa2, c0);
+                  c1 = f2_fma(f2_mul(p1, f2_pack(w4.z, w4.w)), sa2, c1);
+                } else {
+                  c0 = f2_fma(p0, f2_pack(w4.x, w4.y), c0);
+                  c1 = f2_fma(p1, f2_pack(w4.z, w4.w), c1);
+                }
               }
-              tc_fence_after();
-              const float* sw = sw_ring + q * BN;
-              const uint64_t sa2 = f2_pack(sa, sa);
-              const uint32_t tb = tmem_base + lane_addr + a * BN;
-              uint32_t u[2][16];
-              tmem_ld_32x32b_x16(tb + ccol(0), u[0]);
+            }
+          };
+          auto release = [&](uint32_t a) {  // every chunk of accumulator a is in registers
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
+          };
+#pragma unroll 1
+          for (int kb = 0; kb < tl.nkb; ++kb) {
+            const float sa = sa_next;
+            sa_next = load_a(kb + 1);
+            const uint32_t a = acc % NACC;
+            const uint32_t q = acc % kSwSlots;
+            if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs) ||
+                (FM != 1 &&
+                 !mbar_wait_bounded(smem_u32(&ctl->sfull[q]), (acc / kSwSlots) & 1, abort_flag, kWaitLimitNs))) {
+              timed_out = true;
+              break;
+            }
+            tc_fence_after();
+            const float* sw = sw_ring + q * BN;
+            const uint64_t sa2 = f2_pack(sa, sa);
+            const uint32_t tb = tmem_base + lane_addr + a * BN;
+            static_assert(CWID == 16 || CWID == 32, "promotion chunk width");
+            auto ld = [&](int c, uint64_t* u) {
+              tmem_ld_32x32b_x16_pairs(tb + ccol(c), *reinterpret_cast<uint64_t(*)[8]>(u));
+              if (CWID == 32) tmem_ld_32x32b_x16_pairs(tb + ccol(c) + 16, *reinterpret_cast<uint64_t(*)[8]>(u + 8));
+            };
+            if (DBUF) {
+              uint64_t u[2][CWID / 2];
+              ld(0, u[0]);
               tmem_wait_ld();
 #pragma unroll
-              for (int c = 0; c < 8; ++c) {
+              for (int c = 0; c < NCH; ++c) {
                 // the next chunk's load is in flight while this one is folded
-                if (c + 1 < 8) tmem_ld_32x32b_x16(tb + ccol(c + 1), u[(c + 1) & 1]);
-                const uint32_t* v = u[c & 1];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const uint64_t p0 = f2_pack(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]));
-                  const uint64_t p1 = f2_pack(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-                  uint64_t& c0 = acc2[8 * c + 2 * j];
-                  uint64_t& c1 = acc2[8 * c + 2 * j + 1];
-                  if (FM == 1) {
-                    c0 = f2_fma(p0, sa2, c0);
-                    c1 = f2_fma(p1, sa2, c1);
-                  } else {
-                    const float4 w4 = *reinterpret_cast<const float4*>(sw + ccol(c) + 4 * j);  // broadcast
-                    if (FM == 3) {
-                      c0 = f2_fma(f2_mul(p0, f2_pack(w4.x, w4.y)), sa2, c0);
-                      c1 = f2_fma(f2_mul(p1, f2_pack(w4.z, w4.w)), sa2, c1);
-                    } else {
-                      c0 = f2_fma(p0, f2_pack(w4.x, w4.y), c0);
-                      c1 = f2_fma(p1, f2_pack(w4.z, w4.w), c1);
-                    }
-                  }
-                }
+                if (c + 1 < NCH) ld(c + 1, u[(c + 1) & 1]);
+                fold16(u[c & 1], c, sw, sa2);
                 tmem_wait_ld();
-                if (c == 6) {  // the last chunk has landed too: the accumulator is free
-                  tc_fence_before();
-                  __syncwarp();
-                  if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[a]));
-                }
+                if (c == NCH - 2) release(a);
               }
-              if (FM != 1) {  // this warp is done with the scale row
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&ctl->sempty[q]));
+            } else {
+#pragma unroll
+              for (int c = 0; c < NCH; ++c) {
+                uint64_t u[CWID / 2];
+                ld(c, u);
+                tmem_wait_ld();
+                if (c == NCH - 1) release(a);
+                fold16(u, c, sw, sa2);
               }
-              ++acc;
             }
+            if (FM != 1) {  // this warp is done with the scale row
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&ctl->sempty[q]));
+            }
+            ++acc;
           }
         };
         if (a_blk && w_blk)
@@ -1024,38 +1056,48 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         const bool w_col = p.rhs_mode == MOE_SCALE_PER_ROW;
         const float* swb = p.rhs_scale + (w_col ? static_cast<int64_t>(tl.el) * p.N : 0);
         const float sw_t = (w_blk || w_col) ? 1.0f : __ldg(p.rhs_scale);
-        // 16 output values of chunk c as gmm_fp8 stores them: bf16((acc s_a) s_w)
-        auto chunk_vals = [&](int c, float* f) {
-          const int n = tl.n0 + ccol(c);  // weight channel (plain gmm)
+        // 8 output values (half h8 of 16-column group g) as gmm_fp8 stores
+        // them: bf16((acc s_a) s_w)
+        auto vals8 = [&](int g, int h8, float* f) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
+          for (int i = 0; i < 2; ++i) {
+            const int q = 2 * h8 + i;  // 4-column quad of the group
             float4 w4 = make_float4(sw_t, sw_t, sw_t, sw_t);
             if (w_col) {
-              // SwiGLU tiles: accumulator columns 0..127 are wi_0 channels n0.., 128..255 wi_1 channels F + n0..
-              const int ch = SWG ? (ccol(c) < 128 ? tl.n0 + ccol(c) : p.F + tl.n0 + ccol(c) - 128) : n;
-              w4 = __ldg(reinterpret_cast<const float4*>(swb + ch) + g);
+              // SwiGLU tiles: accumulator columns 0..127 are wi_0 channels
+              // n0 + [0, 128), columns 128..255 wi_1 channels F + n0 + [0, 128)
+              const int cc = gcol(g);
+              const int ch = SWG ? (cc < 128 ? tl.n0 + cc : p.F + tl.n0 + cc - 128) : tl.n0 + cc;
+              w4 = __ldg(reinterpret_cast<const float4*>(swb + ch) + q);
             }
             float x0, x1, x2, x3;
-            f2_unpack(acc2[8 * c + 2 * g], x0, x1);
-            f2_unpack(acc2[8 * c + 2 * g + 1], x2, x3);
-            f[4 * g] = __fmul_rn(__fmul_rn(x0, sa_end), w4.x);
-            f[4 * g + 1] = __fmul_rn(__fmul_rn(x1, sa_end), w4.y);
-            f[4 * g + 2] = __fmul_rn(__fmul_rn(x2, sa_end), w4.z);
-            f[4 * g + 3] = __fmul_rn(__fmul_rn(x3, sa_end), w4.w);
+            f2_unpack(acc2[8 * g + 2 * q], x0, x1);
+            f2_unpack(acc2[8 * g + 2 * q + 1], x2, x3);
+            f[4 * i] = __fmul_rn(__fmul_rn(x0, sa_end), w4.x);
+            f[4 * i + 1] = __fmul_rn(__fmul_rn(x1, sa_end), w4.y);
+            f[4 * i + 2] = __fmul_rn(__fmul_rn(x2, sa_end), w4.z);
+            f[4 * i + 3] = __fmul_rn(__fmul_rn(x3, sa_end), w4.w);
           }
         };
         if (!SWG) {
           if (row_ok) {
             uint16_t* out = static_cast<uint16_t*>(p.out);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const int nb = tl.n0 + ccol(c);  // N is a multiple of 16: the chunk is all in range or all past N
+            for (int c = 0; c < WC / 16; ++c) {
+              const int nb = tl.n0 + gcol(c);  // N is a multiple of 16: the group is all in range or all past N
               if (nb < p.N) {
-                float f[16];
-                chunk_vals(c, f);
                 uint32_t pk[8];
 #pragma unroll
-                for (int g = 0; g < 8; ++g) pk[g] = pack_bf16x2(f[2 * g], f[2 * g + 1]);
+                for (int g = 0; g < 4; ++g) {  // 4 columns at a time, straight to bf16 pairs
+                  float4 w4 = make_float4(sw_t, sw_t, sw_t, sw_t);
+                  if (w_col) w4 = __ldg(reinterpret_cast<const float4*>(swb + nb) + g);
+                  float x0, x1, x2, x3;
+                  f2_unpack(acc2[8 * c + 2 * g], x0, x1);
+                  f2_unpack(acc2[8 * c + 2 * g + 1], x2, x3);
+                  pk[2 * g] = pack_bf16x2(__fmul_rn(__fmul_rn(x0, sa_end), w4.x), __fmul_rn(__fmul_rn(x1, sa_end), w4.y));
+                  pk[2 * g + 1] =
+                      pack_bf16x2(__fmul_rn(__fmul_rn(x2, sa_end), w4.z), __fmul_rn(__fmul_rn(x3, sa_end), w4.w));
+                }
                 uint16_t* dst = out + row * p.N + nb;
                 *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 *reinterpret_cast<uint4*>(dst + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
@@ -1063,58 +1105,53 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
             }
           }
         } else {
-          // fused SwiGLU: this thread holds a0 and a1 of h columns
-          // n0 + 64 half + [0, 64) of its row; h = bf16(silu(a0) a1) and its
-          // codes as moe_swiglu_quant makes them from the stored a
+          // fused SwiGLU: this thread holds a0 and a1 of the h columns
+          // n0 + (WC/2) part + [0, WC/2) of its row; h = bf16(silu(a0) a1) and
+          // its codes as moe_swiglu_quant makes them from the stored a
+          constexpr int HC = WC / 2;  // h columns of this warp
           float hs = 1.0f, hinv = 1.0f;
           if (p.h_mode == MOE_SCALE_PER_TENSOR) {
             hs = __ldg(p.h_static);
             hinv = __frcp_rn(hs);
           }
           float amax = 0.0f;
-          uint32_t hp[32];  // the 64 h values as bf16 pairs (per-128 h scales)
+          uint32_t hp[HC / 2];  // the h values as bf16 pairs (per-128 h scales)
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            float f0[16], f1[16], h[16];
-            uint32_t hb[8];
-            chunk_vals(cc, f0);
-            chunk_vals(cc + 4, f1);
-            uint32_t a0b[8], a1b[8];
+          for (int s8 = 0; s8 < HC / 8; ++s8) {  // 8 h columns at a time (few live temporaries)
+            const int g = s8 >> 1, h8 = s8 & 1;  // 16-column group of a0 (a1: group g + WC / 32)
+            float f0[8], f1[8], h[8];
+            uint32_t hb[4], a0b[4], a1b[4];
+            vals8(g, h8, f0);
+            vals8(g + WC / 32, h8, f1);
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              a0b[g] = pack_bf16x2(f0[2 * g], f0[2 * g + 1]);
-              a1b[g] = pack_bf16x2(f1[2 * g], f1[2 * g + 1]);
-              f0[2 * g] = bf16lo(a0b[g]);
-              f0[2 * g + 1] = bf16hi(a0b[g]);
-              f1[2 * g] = bf16lo(a1b[g]);
-              f1[2 * g + 1] = bf16hi(a1b[g]);
+            for (int j = 0; j < 4; ++j) {
+              a0b[j] = pack_bf16x2(f0[2 * j], f0[2 * j + 1]);
+              a1b[j] = pack_bf16x2(f1[2 * j], f1[2 * j + 1]);
+              f0[2 * j] = bf16lo(a0b[j]);
+              f0[2 * j + 1] = bf16hi(a0b[j]);
+              f1[2 * j] = bf16lo(a1b[j]);
+              f1[2 * j + 1] = bf16hi(a1b[j]);
             }
-            swiglu_h_x2<16>(f0, f1, h, hb);
+            swiglu_h_x2<8>(f0, f1, h, hb);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(h[j]));
-            const int hc = tl.n0 + 64 * half + 16 * cc;  // first h column of the chunk
+            for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(h[j]));
+            const int hc = tl.n0 + HC * part + 8 * s8;  // first h column of the step
             if (row_ok) {
               if (p.a_out) {
-                uint4* d0 = reinterpret_cast<uint4*>(p.a_out + row * 2 * p.F + hc);
-                uint4* d1 = reinterpret_cast<uint4*>(p.a_out + row * 2 * p.F + p.F + hc);
-                d0[0] = make_uint4(a0b[0], a0b[1], a0b[2], a0b[3]);
-                d0[1] = make_uint4(a0b[4], a0b[5], a0b[6], a0b[7]);
-                d1[0] = make_uint4(a1b[0], a1b[1], a1b[2], a1b[3]);
-                d1[1] = make_uint4(a1b[4], a1b[5], a1b[6], a1b[7]);
+                *reinterpret_cast<uint4*>(p.a_out + row * 2 * p.F + hc) = make_uint4(a0b[0], a0b[1], a0b[2], a0b[3]);
+                *reinterpret_cast<uint4*>(p.a_out + row * 2 * p.F + p.F + hc) =
+                    make_uint4(a1b[0], a1b[1], a1b[2], a1b[3]);
               }
               if (p.h_mode == MOE_SCALE_PER_ROW) {
-                uint4* dh = reinterpret_cast<uint4*>(p.h_out + row * p.F + hc);
-                dh[0] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
-                dh[1] = make_uint4(hb[4], hb[5], hb[6], hb[7]);
+                *reinterpret_cast<uint4*>(p.h_out + row * p.F + hc) = make_uint4(hb[0], hb[1], hb[2], hb[3]);
               } else if (p.h_mode == MOE_SCALE_PER_TENSOR) {
-                float qv[16];
-                quant_n<16>(h, hs, hinv, qv);
-                const uint2 lo8 = pack_e4m3x8(qv), hi8 = pack_e4m3x8(qv + 8);
-                *reinterpret_cast<uint4*>(p.h_q + row * p.F + hc) = make_uint4(lo8.x, lo8.y, hi8.x, hi8.y);
+                float qv[8];
+                quant_n<8>(h, hs, hinv, qv);
+                *reinterpret_cast<uint2*>(p.h_q + row * p.F + hc) = pack_e4m3x8(qv);
               }
             }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) hp[cc * 8 + j] = hb[j];
+            for (int j = 0; j < 4; ++j) hp[s8 * 4 + j] = hb[j];
           }
           const int par = tcount & 1;
           if (p.h_mode == MOE_SCALE_PER_ROW) {
@@ -1122,24 +1159,26 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
             if (row_ok) atomicMax(reinterpret_cast<unsigned int*>(p.h_scale) + row, __float_as_uint(amax));
           } else if (p.h_mode == MOE_SCALE_PER_ROW_BLOCK128) {
             // the tile's 128 h columns are one 128-column scale block, split
-            // over the two warps of this lane quarter: exchange their maxima
-            // (a bounded wait on a barrier of the pair of warps; the two
+            // over the NPART warps of this lane quarter: they exchange their
+            // maxima (a bounded wait on a barrier of those warps; the two
             // parities alternate between tiles)
-            ctl->pamax[par][q4][half][lane] = amax;
+            ctl->pamax[par][q4][part][lane] = amax;
             mbar_arrive(smem_u32(&ctl->xbar[q4][par]));
             if (!mbar_wait_bounded(smem_u32(&ctl->xbar[q4][par]), (tcount >> 1) & 1, abort_flag, kWaitLimitNs)) {
               timed_out = true;
               break;
             }
-            const float m = fmaxf(amax, ctl->pamax[par][q4][half ^ 1][lane]);
+            float m = amax;
+#pragma unroll
+            for (int o = 0; o < NPART; ++o) m = fmaxf(m, ctl->pamax[par][q4][o][lane]);
             if (row_ok) {
               const float sblk = absmax_scale(m);
               const float inv = __frcp_rn(sblk);
-              if (half == 0) p.h_scale[row * (p.F / 128) + tl.n0 / 128] = sblk;
+              if (part == 0) p.h_scale[row * (p.F / 128) + tl.n0 / 128] = sblk;
               float x16[16], qv[16];
-              uint4* dst = reinterpret_cast<uint4*>(p.h_q + row * p.F + tl.n0 + half * 64);
+              uint4* dst = reinterpret_cast<uint4*>(p.h_q + row * p.F + tl.n0 + HC * part);
 #pragma unroll
-              for (int g = 0; g < 4; ++g) {
+              for (int g = 0; g < HC / 16; ++g) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                   x16[2 * j] = bf16lo(hp[g * 8 + j]);
