@@ -84,6 +84,11 @@ def lib():
                 "or_quantize_group_cols": ([P, P, i32, i32, i32, i64, i64, P, P], None),
                 "or_tgmm": ([P, P, i32, P, P, i32, P, i32, i32, i32, i64, i64, i64, P, i64, P, P], None),
                 "or_tgmm_f64": ([P, P, P, i32, i32, i32, i64, i64, i64, P], None),
+                "or_router_logits": ([P, P, i64, i64, i64, P], None),
+                "or_router_topk": ([P, i64, i64, i32, P, P, P], None),
+                "or_router_dw": ([P, P, P, i64, i32, i64, P], None),
+                "or_router_dlogits": ([P, P, P, i64, i64, i32, P], None),
+                "or_router_grads": ([P, P, P, i64, i64, i64, P, P], None),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
@@ -502,3 +507,65 @@ def ffn_backward(fwd: dict, G_bits, topk_w, wq, k: int, static: dict):
                   sizes)
     return dict(dO=dO, dO_q=dO_q, dO_s=dO_s, dH=dH, dA=dA, dA_q=dA_q, dA_s=dA_s, dXs=dXs, dX=dX,
                 dAg_q=dAg_q, dAg_s=dAg_s, dOg_q=dOg_q, dOg_s=dOg_s, dW_in=dW_in, dW_out=dW_out)
+
+
+# --------------------------------------------------------------------------
+# Router: the gate layer, softmax top-k routing and their gradients
+# ("Support quantization for tokamax gmm v2", table 1: grad_gate-kernel and
+# state_grad).  W_gate is [E, D] (one row per expert).
+# --------------------------------------------------------------------------
+
+def router_logits(x_bits, wg_bits):
+    """bf16 x [T, D], bf16 W_gate [E, D] -> float64 logits [T, E]."""
+    x = _c(x_bits, np.uint16)
+    wg = _c(wg_bits, np.uint16)
+    T, D = x.shape
+    E = wg.shape[0]
+    out = np.empty((T, E), np.float64)
+    lib().or_router_logits(_p(x), _p(wg), T, D, E, _p(out))
+    return out
+
+
+def router_topk(logits_f32, k: int, want_p: bool = False):
+    """fp32 logits [T, E] -> (ids int32 [T, k], w float32 [T, k][, p [T, E]])."""
+    l = _c(logits_f32, np.float32)
+    T, E = l.shape
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float32)
+    p = np.empty((T, E), np.float32) if want_p else None
+    lib().or_router_topk(_p(l), T, E, k, _p(ids), _p(w), _p(p))
+    return (ids, w, p) if want_p else (ids, w)
+
+
+def router_dw(G_bits, o_bits, pos, k: int):
+    """dL/dw [T, k] (float64) of the combine: <G[t], o[pos[t k + j]]>."""
+    G = _c(G_bits, np.uint16)
+    o = _c(o_bits, np.uint16)
+    T, D = G.shape
+    dw = np.empty((T, k), np.float64)
+    lib().or_router_dw(_p(G), _p(o), _p(_c(pos, np.int32)), T, k, D, _p(dw))
+    return dw
+
+
+def router_dlogits(logits_f32, ids, dw_f32):
+    """Softmax backward through the selected probabilities -> bf16 bits [T, E]."""
+    l = _c(logits_f32, np.float32)
+    T, E = l.shape
+    ids = _c(ids, np.int32)
+    k = ids.shape[1]
+    out = np.empty((T, E), np.uint16)
+    lib().or_router_dlogits(_p(l), _p(ids), _p(_c(dw_f32, np.float32)), T, E, k, _p(out))
+    return out
+
+
+def router_grads(x_bits, wg_bits, dlogits_bits):
+    """(grad_gate [E, D], state_grad [T, D]) in float64 from bf16 dlogits."""
+    x = _c(x_bits, np.uint16)
+    wg = _c(wg_bits, np.uint16)
+    dl = _c(dlogits_bits, np.uint16)
+    T, D = x.shape
+    E = wg.shape[0]
+    gg = np.empty((E, D), np.float64)
+    sg = np.empty((T, D), np.float64)
+    lib().or_router_grads(_p(x), _p(wg), _p(dl), T, D, E, _p(gg), _p(sg))
+    return gg, sg

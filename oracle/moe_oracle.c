@@ -617,3 +617,135 @@ void or_tgmm_f64(const double* lhs, const double* rhs, const int32_t* group_size
     start += sz;
   }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Router ("Support quantization for tokamax gmm v2", table 1: the gate      */
+/* kernel's gradient grad_gate-kernel and the state gradient state_grad are  */
+/* measured beside the expert weights' gradients).  The gate is a dense      */
+/* bf16 layer W_gate [E, D]; routing takes a softmax over all E logits and   */
+/* the k most probable experts, weighted by their probabilities, not         */
+/* renormalised, ties to the lower expert index.                             */
+/* ------------------------------------------------------------------------ */
+
+/* logits[t, e] = sum_d x[t, d] W_gate[e, d] in double (products of two bf16
+ * values are exact). */
+void or_router_logits(const uint16_t* x, const uint16_t* wg, int64_t T, int64_t D, int64_t E, double* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int64_t d = 0; d < D; ++d) acc += or_bf16_to_f64(x[t * D + d]) * or_bf16_to_f64(wg[e * D + d]);
+      out[t * E + e] = acc;
+    }
+}
+
+/* Softmax probabilities of one row of fp32 logits, in fp32 (the precision in
+ * which the kernels take the top-k decision): m = max l, e_i = exp(l_i - m)
+ * with the fp32 exponential above, Z = e_0 + e_1 + ... summed in ascending i,
+ * p_i = e_i / Z correctly rounded. */
+static void softmax_row_f32(const float* l, int64_t E, float* p) {
+  float m = -INFINITY;
+  for (int64_t i = 0; i < E; ++i) m = l[i] > m ? l[i] : m;
+  float z = 0.0f;
+  for (int64_t i = 0; i < E; ++i) {
+    p[i] = or_exp_f32(l[i] - m);
+    z = z + p[i];
+  }
+  for (int64_t i = 0; i < E; ++i) p[i] = p[i] / z;
+}
+
+/* Top-k routing from fp32 logits [T, E]: ids [T, k] in descending order of
+ * probability (ties to the lower expert index), weights w [T, k] = the
+ * selected probabilities; p [T, E] (optional) receives every probability. */
+void or_router_topk(const float* logits, int64_t T, int64_t E, int k, int32_t* ids, float* w, float* p_out) {
+#pragma omp parallel
+  {
+    float* p = (float*)malloc(sizeof(float) * (size_t)E);
+    char* taken = (char*)malloc((size_t)E);
+#pragma omp for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+      softmax_row_f32(logits + t * E, E, p);
+      memset(taken, 0, (size_t)E);
+      for (int j = 0; j < k; ++j) {
+        int64_t best = -1;
+        for (int64_t i = 0; i < E; ++i)
+          if (!taken[i] && (best < 0 || p[i] > p[best])) best = i; /* strict >: the lower index wins a tie */
+        taken[best] = 1;
+        ids[t * k + j] = (int32_t)best;
+        w[t * k + j] = p[best];
+      }
+      if (p_out) memcpy(p_out + t * E, p, sizeof(float) * (size_t)E);
+    }
+    free(p);
+    free(taken);
+  }
+}
+
+/* Gradient of the loss with respect to the routing weights: the combine
+ * y[t] = sum_j w[t, j] o[pos[t k + j]] gives dL/dw[t, j] = <G[t], o[pos]>, in
+ * double. */
+void or_router_dw(const uint16_t* G, const uint16_t* o, const int32_t* pos, int64_t T, int k, int64_t D,
+                  double* dw) {
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t)
+    for (int j = 0; j < k; ++j) {
+      const int64_t r = pos[t * k + j];
+      double acc = 0.0;
+      for (int64_t d = 0; d < D; ++d) acc += or_bf16_to_f64(G[t * D + d]) * or_bf16_to_f64(o[r * D + d]);
+      dw[t * k + j] = acc;
+    }
+}
+
+/* Softmax backward through the selected probabilities, in fp32, rounded to
+ * bf16 (gradients are bf16 between steps):
+ *   w_j = p[id_j],  s = sum_j w_j dw_j (ascending j),
+ *   dlogits[t, i] = bf16( p_i (g_i - s) ),  g_i = dw_j if i = id_j, else 0. */
+void or_router_dlogits(const float* logits, const int32_t* ids, const float* dw, int64_t T, int64_t E, int k,
+                       uint16_t* dlogits) {
+#pragma omp parallel
+  {
+    float* p = (float*)malloc(sizeof(float) * (size_t)E);
+    float* g = (float*)malloc(sizeof(float) * (size_t)E);
+#pragma omp for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+      softmax_row_f32(logits + t * E, E, p);
+      float s = 0.0f;
+      for (int64_t i = 0; i < E; ++i) g[i] = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        const int32_t e = ids[t * k + j];
+        const float wj = p[e];
+        const float pr = wj * dw[t * k + j];
+        s = s + pr;
+        g[e] = dw[t * k + j];
+      }
+      for (int64_t i = 0; i < E; ++i) {
+        const float diff = g[i] - s;
+        const float v = p[i] * diff;
+        dlogits[t * E + i] = or_f64_to_bf16((double)v); /* an fp32 value rounds to bf16 in one step */
+      }
+    }
+    free(p);
+    free(g);
+  }
+}
+
+/* Gradients of the gate from bf16 dlogits [T, E], in double:
+ *   grad_gate[e, d] = sum_t dlogits[t, e] x[t, d]     (W_gate's layout [E, D])
+ *   state_grad[t, d] = sum_e dlogits[t, e] W_gate[e, d]. */
+void or_router_grads(const uint16_t* x, const uint16_t* wg, const uint16_t* dl, int64_t T, int64_t D, int64_t E,
+                     double* grad_gate, double* state_grad) {
+#pragma omp parallel for schedule(static)
+  for (int64_t e = 0; e < E; ++e)
+    for (int64_t d = 0; d < D; ++d) {
+      double acc = 0.0;
+      for (int64_t t = 0; t < T; ++t) acc += or_bf16_to_f64(dl[t * E + e]) * or_bf16_to_f64(x[t * D + d]);
+      grad_gate[e * D + d] = acc;
+    }
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t d = 0; d < D; ++d) {
+      double acc = 0.0;
+      for (int64_t e = 0; e < E; ++e) acc += or_bf16_to_f64(dl[t * E + e]) * or_bf16_to_f64(wg[e * D + d]);
+      state_grad[t * D + d] = acc;
+    }
+}
