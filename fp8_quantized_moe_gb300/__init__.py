@@ -32,6 +32,7 @@ __all__ = [
     "PER_ROW", "PER_ROW_BLOCK128", "PER_TENSOR", "PER_GROUP_COL", "MoEError", "lib", "device_error",
     "quantize_rows", "quantize_weights", "ragged_sort", "gmm", "gmm_swiglu", "swiglu_fusable", "swiglu_fuse_pays", "swiglu_quant", "ragged_gather_reduce",
     "gather_scale_quant", "swiglu_bwd_quant", "quantize_group_cols", "tgmm", "transpose_u8",
+    "router_topk", "router_backward",
     "ExpertWeights", "prepare_weights", "FFNBuffers", "ffn_forward", "ffn_backward",
 ]
 
@@ -321,6 +322,38 @@ def tgmm_gcq(lhs_q, lhs_scale, lhs_mode, rhs_g, rhs_scale, group_sizes, group_of
                              group_offset, E_local, M, K, N, _p(out), _p(workspace), workspace.numel(), _s()),
           "tgmm_fp8_gcq")
     return out
+
+
+def router_topk(x: torch.Tensor, w_gate: torch.Tensor, k: int):
+    """Gate layer + softmax top-k: (logits fp32 [T, E], ids int32 [T, k], w fp32 [T, k])."""
+    T, D = x.shape
+    E = w_gate.shape[0]
+    dev = x.device
+    logits = torch.empty(T, E, dtype=torch.float32, device=dev)
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    check(lib().moe_router_topk(_p(x), _p(w_gate), T, D, E, k, _p(logits), _p(ids), _p(w), _s()), "moe_router_topk")
+    return logits, ids, w
+
+
+def router_backward(G: torch.Tensor, o: torch.Tensor, pos: torch.Tensor, x: torch.Tensor, w_gate: torch.Tensor,
+                    logits: torch.Tensor, ids: torch.Tensor, workspace: Optional[torch.Tensor] = None):
+    """Router gradient: (dw fp32 [T, k], dlogits bf16 [T, E], grad_gate fp32 [E, D], state_grad bf16 [T, D])."""
+    T, D = x.shape
+    E = w_gate.shape[0]
+    k = ids.shape[1]
+    dev = x.device
+    dw = torch.empty(T, k, dtype=torch.float32, device=dev)
+    dl = torch.empty(T, E, dtype=torch.bfloat16, device=dev)
+    gg = torch.empty(E, D, dtype=torch.float32, device=dev)
+    sg = torch.empty(T, D, dtype=torch.bfloat16, device=dev)
+    nws = lib().moe_router_backward_workspace_bytes(T, D, E)
+    if workspace is None or workspace.numel() < nws:
+        workspace = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+    check(lib().moe_router_backward(_p(G), _p(o), _p(pos), _p(x), _p(w_gate), _p(logits), _p(ids), T, D, E, k,
+                                    _p(dw), _p(dl), _p(gg), _p(sg), _p(workspace), workspace.numel(), _s()),
+          "moe_router_backward")
+    return dw, dl, gg, sg
 
 
 def transpose_u8(x: torch.Tensor) -> torch.Tensor:

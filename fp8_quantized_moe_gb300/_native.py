@@ -41,6 +41,9 @@ SIGNATURES = {
     "moe_transpose_u8": ([P, i64, i64, i64, P, P], i32),
     "gmm_fp8_swiglu": ([P, P, i32, P, P, i32, P, i32, i32, i32, i64, i64, i64, i32, P, P, P, P, P, P], i32),
     "moe_ragged_sort_noalloc": ([P, i64, i32, i32, P, P, i64, i32, P, P, P, P, P, P, P], i32),
+    "moe_router_topk": ([P, P, i64, i64, i32, i32, P, P, P, P], i32),
+    "moe_router_backward_workspace_bytes": ([i64, i64, i32], sz),
+    "moe_router_backward": ([P, P, P, P, P, P, P, i64, i64, i32, i32, P, P, P, P, P, sz, P], i32),
 }
 
 _lock = threading.Lock()

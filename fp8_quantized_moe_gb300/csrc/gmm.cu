@@ -58,7 +58,7 @@ constexpr int kMaxGroups = 1024;
 constexpr int64_t kPairMinK = 3072;  // gmm K from which the plain and SwiGLU gmm run on CTA pairs
 constexpr int kMaxDevices = 256;     // host-side per-device caches
 
-enum Mode { kFinal = 0, kPromote = 1, kTgmm = 2, kSwiglu = 3, kSplit = 4, kPromoteSwiglu = 5 };
+enum Mode { kFinal = 0, kPromote = 1, kTgmm = 2, kSwiglu = 3, kSplit = 4, kPromoteSwiglu = 5, kBf16 = 6, kRouter = 7 };
 constexpr int kSwSlots = 8;  // promotion: ring of per-K-block weight-scale rows in shared memory
 
 struct Params {
@@ -83,6 +83,13 @@ struct Params {
   uint16_t* h_out;     // [M, F] bf16 (per-row h scales)
   uint8_t* h_q;        // [M, F] e4m3 (per-tensor / per-128 h scales)
   float* h_scale;      // per-row: running amax [M]; per-128: [M, F/128]
+  // kBf16: fp32 output rows instead of bf16
+  int out_f32;
+  // kRouter: softmax top-k of the first `E` logit columns of each row
+  int rE, rk;
+  float* logits;       // [M, rE] fp32
+  int32_t* topk_ids;   // [M, rk]
+  float* topk_w;       // [M, rk]
 };
 
 struct SmemCtl {
@@ -143,8 +150,10 @@ static_assert(sizeof(SmemCtl) % 16 == 0, "SmemCtl size");
 template <int MODE, bool PAIR_REQ = false>
 struct Cfg {
   static constexpr bool PROMOTE = MODE == kPromote || MODE == kPromoteSwiglu;
-  static constexpr bool SWIGLU = MODE == kSwiglu || MODE == kPromoteSwiglu;
   static constexpr bool PAIR = PAIR_REQ && MOE_GMM_PAIR && (MODE == kFinal || MODE == kSwiglu);
+  // bf16 operands (kind::f16): a 128-byte K block is 64 elements
+  static constexpr bool BF = MODE == kBf16 || MODE == kRouter;
+  static constexpr int KSTEP = BF ? 64 : 128;  // elements of K per 128-byte block
   static constexpr int BN = 256;  // output columns per tile
   static constexpr int TMEM_COLS = PAIR ? MOE_PAIR_TMEM_COLS : 512;
   static constexpr int SEGS = MODE == kSplit ? 2 : 1;        // accumulators per tile (one per K segment)
@@ -153,7 +162,7 @@ struct Cfg {
   static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK;  // this CTA's part of the B tile
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TX_BYTES = (PAIR ? 2 : 1) * STAGE_BYTES;  // what one full barrier waits for
-  static constexpr uint32_t IDESC = idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN);
+  static constexpr uint32_t IDESC = BF ? idesc_bf16_f32(BM, BN) : idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN);
   static constexpr int EPI_WARPS =
       PROMOTE ? MOE_PROMOTE_EPI_WARPS : (MODE == kSwiglu ? 8 : (MODE == kTgmm ? MOE_TGMM_EPI_WARPS : 4));
   // warps before the epilogue: producer, MMA issuer and, for promotion, two
@@ -169,10 +178,10 @@ struct Cfg {
   // per-warp staging of 32x32 output blocks: kFinal, bf16 rows padded to 80
   // bytes for row-contiguous stores; kTgmm, two 4 KB fp32 blocks in the
   // 128-byte-swizzled layout of a TMA store box
-  static constexpr int STG_PITCH = (MODE == kFinal || MODE == kSplit) ? 80 : 0;
+  static constexpr int STG_PITCH = (MODE == kFinal || MODE == kSplit || MODE == kBf16) ? 80 : 0;
   static constexpr int STG_BUFS = MODE == kTgmm ? MOE_TGMM_STG_BUFS : 1;
   static constexpr int STG_WARP_BYTES =
-      (MODE == kFinal || MODE == kSplit) ? 32 * STG_PITCH : (MODE == kTgmm ? STG_BUFS * 4096 : 0);
+      (MODE == kFinal || MODE == kSplit || MODE == kBf16) ? 32 * STG_PITCH : (MODE == kTgmm ? STG_BUFS * 4096 : 0);
   static constexpr size_t CTL_BYTES = (sizeof(SmemCtl) + 1023) / 1024 * 1024;  // keeps the staging 1 KB aligned
   // promotion: kSwSlots rows of BN weight scales, one per K block in flight
   static constexpr int SW_RING_BYTES = PROMOTE ? kSwSlots * BN * 4 : 0;
@@ -205,7 +214,8 @@ __device__ void build_group_tables(const Params& p, SmemCtl* ctl) {
 #pragma unroll
   for (int c = 0; c < kMaxGroups / 32; ++c) {
     const int g = c * 32 + lane;
-    v[c] = g < p.E ? __ldg(p.group_sizes + g) : 0;
+    // no size table: one group of all M rows (the router's dense contractions)
+    v[c] = g < p.E ? (p.group_sizes ? __ldg(p.group_sizes + g) : static_cast<int>(p.M)) : 0;
   }
   int64_t carry_rows = 0;
   int carry_aux = 0;
@@ -476,18 +486,18 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
             // both CTAs' boxes complete on the even CTA's full barrier
             const uint32_t fb = mapa_shared(smem_u32(&ctl->full[s]), 0);
             if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), C::TX_BYTES);
-            tma_load_2d_pair(sa, &tmA, tl.ax + kb * BK, tl.ay, fb);
-            tma_load_2d_pair(sa + A_BYTES, &tmB, tl.bx + kb * BK, tl.by, fb);
+            tma_load_2d_pair(sa, &tmA, tl.ax + kb * C::KSTEP, tl.ay, fb);
+            tma_load_2d_pair(sa + A_BYTES, &tmB, tl.bx + kb * C::KSTEP, tl.by, fb);
           } else {
             const uint32_t fb = smem_u32(&ctl->full[s]);
             mbar_arrive_expect_tx(fb, C::TX_BYTES);
-            tma_load_2d(sa, &tmA, tl.ax + kb * BK, tl.ay, fb);
+            tma_load_2d(sa, &tmA, tl.ax + kb * C::KSTEP, tl.ay, fb);
             if (MODE == kSwiglu || MODE == kPromoteSwiglu) {
               // B rows 0..127: wi_0 channels; rows 128..255: the matching wi_1 channels
-              tma_load_2d(sa + A_BYTES, &tmB, tl.bx + kb * BK, tl.by, fb);
-              tma_load_2d(sa + 2 * A_BYTES, &tmB, tl.bx + kb * BK, tl.by + p.F, fb);
+              tma_load_2d(sa + A_BYTES, &tmB, tl.bx + kb * C::KSTEP, tl.by, fb);
+              tma_load_2d(sa + 2 * A_BYTES, &tmB, tl.bx + kb * C::KSTEP, tl.by + p.F, fb);
             } else {
-              tma_load_2d(sa + A_BYTES, &tmB, tl.bx + kb * BK, tl.by, fb);
+              tma_load_2d(sa + A_BYTES, &tmB, tl.bx + kb * C::KSTEP, tl.by, fb);
             }
             if (w_blk) {
               // the K block's weight-scale row, into ring slot q (the
@@ -566,7 +576,9 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
             const uint32_t accumulate = C::PROMOTE ? (k4 > 0) : (kb > seg_kb0 || k4 > 0);
             // +32 bytes along K inside the 128-byte swizzled row = +2 in the
             // descriptor's address field (16-byte units)
-            if (PAIR)
+            if (C::BF)
+              mma_bf16(d_tmem, da + 2 * k4, db + 2 * k4, IDESC, accumulate);
+            else if (PAIR)
               mma_f8_pair(d_tmem, da + 2 * k4, db + 2 * k4, IDESC, accumulate);
             else
               mma_f8(d_tmem, da + 2 * k4, db + 2 * k4, IDESC, accumulate);
@@ -922,6 +934,148 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) release_acc(a);
+        ++acc;
+      } else if (MODE == kBf16) {
+        // plain bf16 contraction without scales: bf16 rows staged through
+        // shared memory as in the fp8 gmm, or fp32 rows written directly
+        const int64_t row = static_cast<int64_t>(tl.row0) + r;
+        const uint32_t a = acc % NACC;
+        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          const int nb = tl.n0 + c * 32;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem_base + lane_addr + a * BN + c * 32, v);
+          tmem_wait_ld();
+          if (p.out_f32) {
+            float* out = static_cast<float*>(p.out);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)  // N is a multiple of 16: each 16 columns are all in range or all past N
+              if (row_ok && nb + 16 * h < p.N)
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                  *reinterpret_cast<float4*>(out + row * p.N + nb + 16 * h + 4 * g) =
+                      make_float4(__uint_as_float(v[16 * h + 4 * g]), __uint_as_float(v[16 * h + 4 * g + 1]),
+                                  __uint_as_float(v[16 * h + 4 * g + 2]), __uint_as_float(v[16 * h + 4 * g + 3]));
+          } else {
+            uint16_t* out = static_cast<uint16_t*>(p.out);
+            uint8_t* stg = stg_base + (warp - C::CTRL_WARPS) * C::STG_WARP_BYTES;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              *reinterpret_cast<uint4*>(stg + lane * C::STG_PITCH + 16 * g) =
+                  make_uint4(pack_bf16x2(__uint_as_float(v[8 * g]), __uint_as_float(v[8 * g + 1])),
+                             pack_bf16x2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3])),
+                             pack_bf16x2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5])),
+                             pack_bf16x2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7])));
+            __syncwarp();
+            const int seg = (lane & 3) * 8;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int rr = i * 8 + (lane >> 2);
+              const int64_t orow = static_cast<int64_t>(tl.row0) + q4 * 32 + rr;
+              if (rr < tl.rows - q4 * 32 && nb + seg < p.N)
+                *reinterpret_cast<uint4*>(out + orow * p.N + nb + seg) =
+                    *reinterpret_cast<const uint4*>(stg + rr * C::STG_PITCH + 2 * seg);
+            }
+            __syncwarp();
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) release_acc(a);
+        ++acc;
+      } else if (MODE == kRouter) {
+        // the gate's logits of one token per thread (TMEM lane = row): the
+        // logits to memory, then the softmax over the first E columns in
+        // fp32 -- m = max, e_i = exp(l_i - m), Z summed in ascending i,
+        // p_i = e_i / Z -- and the top-k by probability with ties to the
+        // lower expert index, kept as a sorted list in registers
+        const int64_t row = static_cast<int64_t>(tl.row0) + r;
+        const uint32_t a = acc % NACC;
+        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+        const int E = p.rE;
+        const int nch = (E + 31) / 32;
+        const uint32_t tb = tmem_base + lane_addr + a * BN;
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < nch; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tb + 32 * c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = 32 * c + j;
+            const float l = __uint_as_float(v[j]);
+            if (col < E) {
+              mx = fmaxf(mx, l);
+              if (row_ok) p.logits[row * E + col] = l;
+            }
+          }
+        }
+        float z = 0.0f;
+#pragma unroll 1
+        for (int c = 0; c < nch; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tb + 32 * c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (32 * c + j < E) z = __fadd_rn(z, exp_f32(__fsub_rn(__uint_as_float(v[j]), mx)));
+        }
+        constexpr int KMAX = 8;
+        float tp[KMAX];
+        int ti[KMAX];
+#pragma unroll
+        for (int s = 0; s < KMAX; ++s) {
+          tp[s] = -1.0f;  // below every probability
+          ti[s] = 0x7fffffff;
+        }
+#pragma unroll 1
+        for (int c = 0; c < nch; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tb + 32 * c, v);
+          tmem_wait_ld();
+          if (c == nch - 1) {  // the accumulator is in registers for the last time
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) release_acc(a);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = 32 * c + j;
+            if (col >= E) continue;
+            float cp = __fdiv_rn(exp_f32(__fsub_rn(__uint_as_float(v[j]), mx)), z);
+            int ci = col;
+            // insertion into the sorted list: larger probability first, the
+            // lower index first among equal ones (a displaced entry carries
+            // its own index down)
+#pragma unroll
+            for (int s = 0; s < KMAX; ++s) {
+              const bool better = cp > tp[s] || (cp == tp[s] && ci < ti[s]);
+              const float tf = better ? tp[s] : cp;
+              const int tq = better ? ti[s] : ci;
+              tp[s] = better ? cp : tp[s];
+              ti[s] = better ? ci : ti[s];
+              cp = tf;
+              ci = tq;
+            }
+          }
+        }
+        if (row_ok)
+#pragma unroll
+          for (int s = 0; s < KMAX; ++s)
+            if (s < p.rk) {
+              p.topk_ids[row * p.rk + s] = ti[s];
+              p.topk_w[row * p.rk + s] = tp[s];
+            }
         ++acc;
       } else {
         // promotion (a blockwise operand scale): K block kb of the tile lands
@@ -1582,6 +1736,23 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, ui
   return r == CUDA_SUCCESS;
 }
 
+// 2-D bf16 tensor map: rows x inner elements (row pitch in bytes, a multiple
+// of 16), box rows_box x 64 elements (128 bytes), 128-byte swizzle; reads past
+// the extents return zeros.
+bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint64_t pitch_bytes,
+                   uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 3-D fp32 tensor map of the tgmm output [E_local, K, N] for 32 x 32 stores
 // with the 128-byte swizzle (rows >= K or columns >= N are clipped).
 bool make_map_out_f32(CUtensorMap* m, void* ptr, uint64_t N, uint64_t K, uint64_t El) {
@@ -1973,4 +2144,139 @@ extern "C" moe_status tgmm_fp8_gcq(const uint8_t* lhs_q, const float* lhs_scale,
                     quant_transpose_pad_kernel<<<grid, 256, 0, st>>>(rhs_g, M, N, rhs_scale, rhsT, Mp, group_sizes,
                                                                      E, group_offset, E_local);
                   });
+}
+
+// ---------------------------------------------------------------------------
+// Router ("Support quantization for tokamax gmm v2", table 1: grad_gate-kernel
+// and state_grad).  The gate contraction runs on the tcgen05 tensor cores in
+// bf16 (kind::f16) with the softmax and top-k in its epilogue; the gradients'
+// two contractions use the same kernel without scales.
+// ---------------------------------------------------------------------------
+extern "C" cudaError_t moe_detail_router_dw(const uint16_t* G, const uint16_t* o, const int32_t* pos, int64_t T,
+                                            int k, int64_t D, float* dw, cudaStream_t st);
+extern "C" cudaError_t moe_detail_router_dlogits(const float* logits, const int32_t* ids, const float* dw, int64_t T,
+                                                 int E, int k, int Ep, int64_t Tp, uint16_t* dl, uint16_t* dl_pad,
+                                                 uint16_t* dlT, cudaStream_t st);
+extern "C" cudaError_t moe_detail_transpose_u16(const uint16_t* src, int64_t R, int64_t C, uint16_t* dst, int64_t Rp,
+                                                cudaStream_t st);
+
+namespace moe {
+namespace {
+constexpr int kRouterMaxE = 256;
+constexpr int kRouterMaxK = 8;
+int64_t round8(int64_t v) { return (v + 7) / 8 * 8; }
+
+// out[M, N] = A[M, K] B[N, K]^T for bf16 row-major A and B (row pitches in
+// elements), fp32 or bf16 out, on the tcgen05 kernel without scales.
+moe_status bf16_gemm(const uint16_t* A, int64_t pitchA, const uint16_t* B, int64_t pitchB, int64_t M, int64_t N,
+                     int64_t K, void* out, bool out_f32, cudaStream_t st) {
+  if (M == 0 || N == 0) return MOE_OK;
+  CUtensorMap ma, mb;
+  if (!make_map_bf16(&ma, A, K, M, pitchA * 2, BM)) return MOE_ERR_CUDA;
+  if (!make_map_bf16(&mb, B, K, N, pitchB * 2, Cfg<kBf16>::BN)) return MOE_ERR_CUDA;
+  Params p{};
+  p.group_sizes = nullptr;  // one group of M rows
+  p.E = 1;
+  p.g0 = 0;
+  p.El = 1;
+  p.M = M;
+  p.K = static_cast<int>(K);
+  p.N = static_cast<int>(N);
+  p.kblocks = static_cast<int>((K + Cfg<kBf16>::KSTEP - 1) / Cfg<kBf16>::KSTEP);
+  p.ntiles = static_cast<int>((N + Cfg<kBf16>::BN - 1) / Cfg<kBf16>::BN);
+  p.out = out;
+  p.out_f32 = out_f32 ? 1 : 0;
+  return launch_mma<kBf16, false>(ma, mb, ma, p, gmm_max_units<kBf16, false>(M, 1, p.ntiles), st);
+}
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_router_topk(const uint16_t* x, const uint16_t* w_gate, int64_t T, int64_t D, int E, int k,
+                                      float* logits, int32_t* topk_ids, float* topk_w, moe_stream_t stream) {
+  MOE_HOST_CHECK(x && w_gate && logits && topk_ids && topk_w, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(T >= 0 && T < (1ll << 31) && D > 0 && D % 8 == 0 && D < (1ll << 30), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(E >= 1 && E <= kRouterMaxE && k >= 1 && k <= kRouterMaxK && k <= E, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(aligned16(x) && aligned16(w_gate), MOE_ERR_INVALID_ARG);
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  cudaStream_t st = as_stream(stream);
+  CUtensorMap A, B;
+  if (!make_map_bf16(&A, x, D, T, D * 2, BM)) return MOE_ERR_CUDA;
+  // the gate's E rows, read as a 256-row box (rows past E come in as zeros)
+  if (!make_map_bf16(&B, w_gate, D, E, D * 2, Cfg<kRouter>::BN)) return MOE_ERR_CUDA;
+  Params p{};
+  p.group_sizes = nullptr;
+  p.E = 1;
+  p.g0 = 0;
+  p.El = 1;
+  p.M = T;
+  p.K = static_cast<int>(D);
+  p.N = Cfg<kRouter>::BN;
+  p.kblocks = static_cast<int>((D + Cfg<kRouter>::KSTEP - 1) / Cfg<kRouter>::KSTEP);
+  p.ntiles = 1;
+  p.rE = E;
+  p.rk = k;
+  p.logits = logits;
+  p.topk_ids = topk_ids;
+  p.topk_w = topk_w;
+  return launch_mma<kRouter, false>(A, B, A, p, gmm_max_units<kRouter, false>(T, 1, 1), st);
+}
+
+namespace {
+struct RouterWs {
+  uint16_t *dl_pad, *dlT, *xT, *wgT;
+};
+size_t router_ws_layout(int64_t T, int64_t D, int E, RouterWs* w, void* base) {
+  const int64_t Tp = moe::round8(T), Ep = moe::round8(E);
+  const size_t sizes[4] = {static_cast<size_t>(T * Ep) * 2, static_cast<size_t>(Ep * Tp) * 2,
+                           static_cast<size_t>(D * Tp) * 2, static_cast<size_t>(D * Ep) * 2};
+  size_t off = 0;
+  uint16_t* ptrs[4];
+  for (int i = 0; i < 4; ++i) {
+    ptrs[i] = base ? reinterpret_cast<uint16_t*>(static_cast<char*>(base) + off) : nullptr;
+    off += (sizes[i] + 255) & ~static_cast<size_t>(255);
+  }
+  if (w) *w = RouterWs{ptrs[0], ptrs[1], ptrs[2], ptrs[3]};
+  return off;
+}
+}  // namespace
+
+extern "C" size_t moe_router_backward_workspace_bytes(int64_t T, int64_t D, int E) {
+  if (T < 0 || D <= 0 || E <= 0) return 0;
+  return router_ws_layout(T, D, E, nullptr, nullptr);
+}
+
+extern "C" moe_status moe_router_backward(const uint16_t* G, const uint16_t* o, const int32_t* pos, const uint16_t* x,
+                                          const uint16_t* w_gate, const float* logits, const int32_t* topk_ids,
+                                          int64_t T, int64_t D, int E, int k, float* dw, uint16_t* dlogits,
+                                          float* grad_gate, uint16_t* state_grad, void* workspace,
+                                          size_t workspace_bytes, moe_stream_t stream) {
+  MOE_HOST_CHECK(G && o && pos && x && w_gate && logits && topk_ids && dw && dlogits && grad_gate && state_grad &&
+                     workspace,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(T >= 0 && T <= (1ll << 21) && D > 0 && D % 16 == 0 && D < (1ll << 30), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(E >= 1 && E <= kRouterMaxE && k >= 1 && k <= kRouterMaxK && k <= E, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(aligned16(G) && aligned16(o) && aligned16(x) && aligned16(w_gate) && aligned16(grad_gate) &&
+                     aligned16(state_grad) && aligned16(workspace),
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(workspace_bytes >= moe_router_backward_workspace_bytes(T, D, E), MOE_ERR_INVALID_ARG);
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = as_stream(stream);
+  if (T == 0) {
+    MOE_CUDA_TRY(cudaMemsetAsync(grad_gate, 0, sizeof(float) * static_cast<size_t>(E) * D, st));
+    return MOE_OK;
+  }
+  RouterWs w;
+  router_ws_layout(T, D, E, &w, workspace);
+  const int64_t Tp = round8(T), Ep = round8(E);
+  MOE_CUDA_TRY(moe_detail_router_dw(G, o, pos, T, k, D, dw, st));
+  MOE_CUDA_TRY(moe_detail_router_dlogits(logits, topk_ids, dw, T, E, k, static_cast<int>(Ep), Tp, dlogits, w.dl_pad,
+                                         w.dlT, st));
+  MOE_CUDA_TRY(moe_detail_transpose_u16(x, T, D, w.xT, Tp, st));
+  MOE_CUDA_TRY(moe_detail_transpose_u16(w_gate, E, D, w.wgT, Ep, st));
+  // grad_gate [E, D] = dlogits^T x: rows of dlT against rows of xT, K = T
+  moe_status stt = bf16_gemm(w.dlT, Tp, w.xT, Tp, E, D, T, grad_gate, true, st);
+  if (stt != MOE_OK) return stt;
+  // state_grad [T, D] = dlogits W_gate: rows of dlogits against rows of W_gate^T, K = E
+  return bf16_gemm(w.dl_pad, Ep, w.wgT, Ep, T, D, E, state_grad, false, st);
 }

@@ -344,6 +344,45 @@ moe_status tgmm_fp8_gcq(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_
                         int64_t M, int64_t K, int64_t N, float* out, void* workspace, size_t workspace_bytes,
                         moe_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Router ([Q-GMM] table 1 measures the gate kernel's gradient grad_gate-kernel
+ * and the state gradient state_grad beside the expert weights' gradients).
+ *
+ * moe_router_topk -- the gate layer and the routing decision in one call:
+ *   logits[t, e] = sum_d x[t, d] w_gate[e, d]   (bf16 operands, fp32
+ *                                                accumulation on the tensor cores)
+ *   p = softmax over the E logits of the row, in fp32: m = max, e_i =
+ *       exp(l_i - m), Z = e_0 + e_1 + ... in ascending i, p_i = e_i / Z
+ *   topk_ids[t, :] = the k most probable experts in descending order of p,
+ *                    ties to the lower expert index;
+ *   topk_w[t, j]   = p[topk_ids[t, j]] (not renormalised).
+ * x bf16 [T, D]; w_gate bf16 [E, D]; logits fp32 [T, E] (kept for the
+ * backward); topk_ids int32 [T, k]; topk_w fp32 [T, k].  D % 8 == 0,
+ * 1 <= E <= 256, 1 <= k <= min(8, E); every row needs a finite logit. */
+moe_status moe_router_topk(const uint16_t* x, const uint16_t* w_gate, int64_t T, int64_t D, int E, int k,
+                           float* logits, int32_t* topk_ids, float* topk_w, moe_stream_t stream);
+
+/* moe_router_backward -- the router's gradient from the combine's output
+ * gradient G (the expert FFN's dY):
+ *   dw[t, j]      = <G[t], o[pos[t k + j]]>        fp32 [T, k]
+ *   dlogits[t, i] = bf16( p_i (g_i - s) )          bf16 [T, E]
+ *                   with p recomputed from logits as in moe_router_topk,
+ *                   s = sum_j p[id_j] dw[t, j] (ascending j), g_i = dw[t, j]
+ *                   for i = id_j, else 0
+ *   grad_gate     = dlogits^T x                    fp32 [E, D] (w_gate's layout)
+ *   state_grad    = dlogits w_gate                 bf16 [T, D] (the gradient
+ *                                                   reaching x through the router)
+ * G bf16 [T, D]; o bf16 [T*k, D] (the expert outputs of the forward);
+ * pos int32 [T*k] (moe_ragged_sort); x, w_gate, logits, topk_ids as given to
+ * / returned by moe_router_topk.  workspace: moe_router_backward_workspace_bytes
+ * bytes (x and w_gate transposed, dlogits padded and transposed).
+ * D % 16 == 0, T <= 2^21, 1 <= E <= 256, 1 <= k <= min(8, E). */
+size_t moe_router_backward_workspace_bytes(int64_t T, int64_t D, int E);
+moe_status moe_router_backward(const uint16_t* G, const uint16_t* o, const int32_t* pos, const uint16_t* x,
+                               const uint16_t* w_gate, const float* logits, const int32_t* topk_ids, int64_t T,
+                               int64_t D, int E, int k, float* dw, uint16_t* dlogits, float* grad_gate,
+                               uint16_t* state_grad, void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
 /* moe_transpose_u8 -- weight layout preparation for the backward pass (run
  * once, outside the FFN): batched byte transpose src [B, R, C] -> dst
  * [B, C, R] of e4m3 codes.  The input-gradient gmm contracts over the

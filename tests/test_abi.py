@@ -66,6 +66,16 @@ def test_host_side_argument_checks_of_the_fused_and_backward_entries(lib):
     # one violated condition each; all are caught before any CUDA call
     raw = ctypes.create_string_buffer(512)
     p = ctypes.c_void_p((ctypes.addressof(raw) + 15) & ~15)  # a 16-byte aligned host address
+    # router: null input, k above 8, E above 256, D not a multiple of 8 (16 for the backward), short workspace
+    assert lib.moe_router_topk(None, p, 4, 128, 8, 2, p, p, p, None) == 1
+    assert lib.moe_router_topk(p, p, 4, 128, 16, 9, p, p, p, None) == 1
+    assert lib.moe_router_topk(p, p, 4, 128, 300, 2, p, p, p, None) == 1
+    assert lib.moe_router_topk(p, p, 4, 12, 8, 2, p, p, p, None) == 1
+    assert lib.moe_router_topk(p, p, 4, 128, 8, 9, p, p, p, None) == 1
+    ws = lib.moe_router_backward_workspace_bytes(4, 128, 8)
+    assert ws > 0
+    assert lib.moe_router_backward(p, p, p, p, p, p, p, 4, 24, 8, 2, p, p, p, p, p, 1 << 30, None) == 1
+    assert lib.moe_router_backward(p, p, p, p, p, p, p, 4, 128, 8, 2, p, p, p, p, p, ws - 1, None) == 1
     # gmm_fp8_swiglu: null lhs; F not a multiple of 128; blockwise lhs scales with K % 128 != 0;
     # an unknown scale mode
     assert lib.gmm_fp8_swiglu(None, p, 0, p, p, 0, p, 1, 0, 1, 1, 128, 128, 0, None, None, p, p, p, None) == 1
