@@ -42,6 +42,7 @@ SIGNATURES = {
     "gmm_fp8_swiglu": ([P, P, i32, P, P, i32, P, i32, i32, i32, i64, i64, i64, i32, P, P, P, P, P, P], i32),
     "moe_ragged_sort_noalloc": ([P, i64, i32, i32, P, P, i64, i32, P, P, P, P, P, P, P], i32),
     "moe_router_topk": ([P, P, i64, i64, i32, i32, P, P, P, P], i32),
+    "moe_test_stall_epilogue": ([ctypes.c_uint64], None),
     "moe_router_backward_workspace_bytes": ([i64, i64, i32], sz),
     "moe_router_backward": ([P, P, P, P, P, P, P, i64, i64, i32, i32, P, P, P, P, P, sz, P], i32),
 }

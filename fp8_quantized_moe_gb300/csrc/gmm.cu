@@ -35,6 +35,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -85,6 +86,10 @@ struct Params {
   float* h_scale;      // per-row: running amax [M]; per-128: [M, F/128]
   // kBf16: fp32 output rows instead of bf16
   int out_f32;
+  // test hook: the epilogue first waits (bounded by stall_ns) on a barrier
+  // that nothing arrives on, so the bounded-wait timeout path runs
+  int stall;
+  uint64_t stall_ns;
   // kRouter: softmax top-k of the first `E` logit columns of each row
   int rE, rk;
   float* logits;       // [M, rE] fp32
@@ -101,6 +106,7 @@ struct SmemCtl {
   uint64_t sempty[kSwSlots];  // promotion: a weight-scale row of the ring has been read by every epilogue warp
   uint64_t xbar[4][2];        // promotion + SwiGLU: the two warps of a lane quarter have posted their h maxima
   uint64_t drain;
+  uint64_t never;  // test hook: a barrier that nothing arrives on
   uint32_t tmem_base;
   int abort_flag;
   int no_abort;  // always 0: for waits that must run to completion or to their time limit
@@ -406,6 +412,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&ctl->xbar[q][b]), EPI_WARPS / 4 * 32);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
+    mbar_init(smem_u32(&ctl->never), 1);
     ctl->abort_flag = 0;
     ctl->no_abort = 0;
     fence_mbar_init();
@@ -624,6 +631,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
     uint32_t acc = 0;
     uint32_t tcount = 0;  // promotion: tiles done by this CTA
+    if (p.stall && !mbar_wait_bounded(smem_u32(&ctl->never), 0, abort_flag, p.stall_ns)) timed_out = true;
     int stg_sel = 0;  // kTgmm: staging buffer of this warp's next block
     for (int t = unit0; t < total && !timed_out; t += units) {
       const Tile tl = get_tile<MODE, PAIR>(p, ctl, t, rank);
@@ -1854,6 +1862,9 @@ moe_status launch_mma(const CUtensorMap& A, const CUtensorMap& B, const CUtensor
   return MOE_OK;
 }
 
+// test hook (moe_test_stall_epilogue): 0, or the wait limit in ns
+std::atomic<uint64_t> g_stall_ns{0};
+
 bool valid_lhs_mode(int m) {
   return m == MOE_SCALE_PER_ROW || m == MOE_SCALE_PER_ROW_BLOCK128 || m == MOE_SCALE_PER_TENSOR;
 }
@@ -1872,6 +1883,8 @@ extern "C" __attribute__((visibility("hidden"))) cudaError_t moe_detail_take_err
 }
 
 extern "C" int moe_num_sms(void) { return sm_count(); }
+
+extern "C" void moe_test_stall_epilogue(uint64_t limit_ns) { g_stall_ns.store(limit_ns); }
 
 extern "C" moe_status gmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode,
                               const uint8_t* rhs_q, const float* rhs_scale, moe_scale_mode rhs_mode,
@@ -1920,6 +1933,8 @@ extern "C" moe_status gmm_fp8(const uint8_t* lhs_q, const float* lhs_scale, moe_
   p.rhs_scale = rhs_scale;
   p.rhs_mode = rhs_mode;
   p.out = out;
+  p.stall_ns = g_stall_ns.load();
+  p.stall = p.stall_ns != 0;
   if (blockwise) return launch_mma<kPromote, false>(A, B, A, p, gmm_max_units<kPromote, false>(M, E_local, p.ntiles), st);
   if (pair) return launch_mma<kFinal, true>(A, B, A, p, gmm_max_units<kFinal, true>(M, E_local, p.ntiles), st);
   return launch_mma<kFinal, false>(A, B, A, p, gmm_max_units<kFinal, false>(M, E_local, p.ntiles), st);

@@ -92,6 +92,15 @@ moe_status moe_get_device_error(moe_stream_t stream, int* code);
  * by (the current device's SM count); 0 on error. */
 int moe_num_sms(void);
 
+/* Test hook for the failure path of the tensor-core kernels: while
+ * limit_ns != 0, the epilogue warps of every following gmm_fp8 launch first
+ * wait on a barrier that nothing arrives on, bounded by limit_ns.  The wait
+ * runs out, the kernel stops its producer and MMA issuer, lets their issued
+ * loads and MMAs finish, frees its tensor memory, returns and sets
+ * MOE_DEVERR_TIMEOUT; the output is undefined.  0 restores normal operation.
+ * Process-wide; not for production use. */
+void moe_test_stall_epilogue(uint64_t limit_ns);
+
 /* ------------------------------------------------------------------------
  * Step 1 -- activation quantisation ([Q-EP] description: quantise before the
  * all-gather and the activation sort; [Q-GMM] review reply: fp8_dynamic uses

@@ -254,3 +254,26 @@ def test_gmm_swiglu_equals_gmm_then_swiglu(M, K, F, E, amode, wmode, hmode, shar
     # and against the oracle, from the oracle's own a
     a_or = oracle.gmm(a, sa, amode, w, sw, wmode, sizes, group_offset=g0, E_local=El)
     assert_close(host(a_out)[lo:hi], a_or[lo:hi], "gmm_swiglu a")
+
+
+def test_bounded_wait_timeout_reports_and_recovers():
+    """The failure path of the tensor-core kernels: the epilogue waits on a
+    barrier that nothing arrives on (a test hook) with a 200 us limit; the
+    kernel stops, drains what it issued, frees its tensor memory and sets
+    MOE_DEVERR_TIMEOUT.  The context stays usable: the next call is exact.
+    Also covers a kernel that had already issued loads and MMAs when the
+    wait ran out (several tiles per CTA)."""
+    lib = moe.lib()
+    for M, K, N, E in [(256, 256, 512, 2), (8192, 512, 2048, 8)]:
+        sizes, a, w, sa, sw = make_case(M + K, M, K, N, E, R0, R0)
+        args = (dev(a), dev(sa), R0, dev(w), dev(sw), R0, dev(sizes))
+        assert moe.device_error() == 0
+        lib.moe_test_stall_epilogue(200_000)
+        try:
+            moe.gmm(*args)
+            assert moe.device_error() == 0x4  # MOE_DEVERR_TIMEOUT
+        finally:
+            lib.moe_test_stall_epilogue(0)
+        out = moe.gmm(*args)
+        assert moe.device_error() == 0
+        assert_close(host(out), oracle.gmm(a, sa, R0, w, sw, R0, sizes), "gmm after a timed-out call")
