@@ -657,11 +657,31 @@ def run_suite(args):
                  lambda: moe.tgmm_gcq(buf.h_q, sh, 2, dO, dOg_s, sizes, workspace=ws),
                  "tensor", (2.0 * R * F * D, 4 * E * F * D + R * F + 2 * R * D)),
             ]
+        # the router (gate contraction + softmax top-k, and its gradient): off the FFN step
+        gwg = torch.Generator(device=dev)
+        gwg.manual_seed(3)
+        w_gate = (torch.randn(E, D, generator=gwg, device=dev) * (1.5 / np.sqrt(D))).to(torch.bfloat16)
+        rlog, rids, _ = moe.router_topk(x, w_gate, k)
+        G_r = torch.randn(T, D, generator=gwg, device=dev).to(torch.bfloat16)
+        rws = torch.empty(moe.lib().moe_router_backward_workspace_bytes(T, D, E), dtype=torch.uint8, device=dev)
+        calls += [
+            ("router_topk (gate + softmax top-k)", lambda: moe.router_topk(x, w_gate, k),
+             "tensor_bf16", (2.0 * T * D * E, 2 * T * D + 2 * E * D + 4 * T * E + 8 * T * k)),
+            ("router_backward (dw, dlogits, grad_gate, state_grad)",
+             lambda: moe.router_backward(G_r, buf.o, buf.sort["pos"], x, w_gate, rlog, rids, workspace=rws),
+             "tensor_bf16", (4.0 * T * D * E, 2 * T * D + 2 * R * D + 3 * 2 * T * D + 2 * T * D + 4 * E * D)),
+        ]
         total = 0.0
         for label, fn, bound, work in calls:
             ms = timed(fn)
             if bound == "hbm":
                 ach, peak, unit = work / (ms / 1e3) / 1e9, hbm, "GB/s"
+            elif bound == "tensor_bf16":
+                flops, nbytes = work
+                if nbytes / (hbm * 1e9) > flops / (pk["bf16_tflops"] * 1e12):
+                    bound, ach, peak, unit = "hbm", nbytes / (ms / 1e3) / 1e9, hbm, "GB/s"
+                else:
+                    bound, ach, peak, unit = "tensor", flops / (ms / 1e3) / 1e12, pk["bf16_tflops"], "TFLOP/s"
             else:
                 # a contraction is bound by whichever of its flops and its bytes takes longer
                 flops, nbytes = work
@@ -671,6 +691,8 @@ def run_suite(args):
                     ach, peak, unit = flops / (ms / 1e3) / 1e12, fp8, "TFLOP/s"
             if label.startswith("gmm_fp8_swiglu"):
                 on_path = fused
+            elif label.startswith("router"):
+                on_path = False  # routing is an input of the FFN step
             else:
                 on_path = not ((fused and label in ("gmm_fp8 wi_0|wi_1", "moe_swiglu_quant")) or
                                label in ("quantize_rows x", "ragged_sort (+ gather)"))
