@@ -27,6 +27,10 @@ namespace moe {
 
 constexpr float kE4M3Max = 448.0f;
 
+#ifndef MOE_IDLE_WAIT_HINT_NS
+#define MOE_IDLE_WAIT_HINT_NS 1000
+#endif
+
 // ------------------------------------------------------------------------
 // Device error word.  Each translation unit owns one (no relocatable device
 // code); moe_get_device_error reads and clears all of them.
@@ -356,8 +360,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread may sleep up to `hint_ns`
+// waiting for the phase instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Time limit of every bounded mbarrier wait.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
+// Bounded wait for warps whose waiting should not take issue slots from the
+// warps they share an SM sub-partition with: the same contract as
+// mbar_wait_bounded, with each poll allowed to sleep up to
+// MOE_IDLE_WAIT_HINT_NS.
+__device__ __forceinline__ bool mbar_wait_bounded_idle(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+                                                       uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_hint(bar, parity, MOE_IDLE_WAIT_HINT_NS)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
 
 // Bounded wait: true once the phase with `parity` has completed; false if
 // `abort_flag` becomes non-zero or `limit_ns` of wall time pass first.
