@@ -31,6 +31,7 @@ PER_ROW = 0
 PER_ROW_BLOCK128 = 1
 PER_TENSOR = 2
 PER_GROUP_COL = 3
+MX32 = 4  # MXFP8 variant: E8M0 codes (uint8), one per 32 values along the contracted dimension
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _BUILD = os.path.join(_HERE, "_build")
@@ -89,6 +90,9 @@ def lib():
                 "or_router_dw": ([P, P, P, i64, i32, i64, P], None),
                 "or_router_dlogits": ([P, P, P, i64, i64, i32, P], None),
                 "or_router_grads": ([P, P, P, i64, i64, i64, P, P], None),
+                "or_quantize_rows_mx": ([P, i64, i64, P, P], None),
+                "or_gmm_mx": ([P, P, P, P, P, i32, i32, i32, i64, i64, i64, P, i64, P, P], None),
+                "or_swiglu_quant_mx": ([P, i64, i64, P, P, P], None),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
@@ -197,6 +201,26 @@ def quantize_weights(w_bits, mode: int, static_scale: float = 1.0):
     return q, s
 
 
+def quantize_rows_mx(x_bits):
+    """MXFP8 (OCP MX v1.0): bf16 [rows, cols], cols a multiple of 32 ->
+    (codes uint8 [rows, cols], E8M0 codes uint8 [rows, cols/32])."""
+    x = _c(x_bits, np.uint16)
+    rows, cols = x.shape
+    assert cols % 32 == 0
+    q = np.empty((rows, cols), np.uint8)
+    sf = np.empty((rows, cols // 32), np.uint8)
+    lib().or_quantize_rows_mx(_p(x), rows, cols, _p(q), _p(sf))
+    return q, sf
+
+
+def quantize_weights_mx(w_bits):
+    """MXFP8 weights: bf16 [E, N, K] -> (codes [E, N, K], E8M0 codes [E, N, K/32])."""
+    w = _c(w_bits, np.uint16)
+    E, N, K = w.shape
+    q, sf = quantize_rows_mx(w.reshape(E * N, K))
+    return q.reshape(E, N, K), sf.reshape(E, N, K // 32)
+
+
 def ragged_sort(topk_ids: np.ndarray, E: int):
     ids = _c(topk_ids, np.int32)
     T, k = ids.shape
@@ -250,6 +274,39 @@ def gmm(lhs, lhs_scale, lhs_mode, rhs, rhs_scale, rhs_mode, group_sizes, group_o
     return ob if want == "bf16" else of
 
 
+def gather_rows_mx(x_q, x_sf, sorted_src, k: int):
+    """MXFP8 rows follow their token: sorted row r takes token sorted_src[r] // k's
+    codes and its E8M0 codes (the scales are per token and block, so they are
+    gathered with the rows)."""
+    t = _c(sorted_src, np.int64) // k
+    return _c(x_q, np.uint8)[t], _c(x_sf, np.uint8)[t]
+
+
+def gmm_mx(lhs, lhs_sf, rhs, rhs_sf, group_sizes, group_offset=0, E_local=None, rows=None, want="bf16"):
+    """MXFP8 grouped matmul: lhs [M, K] with E8M0 codes [M, K/32], rhs
+    [E_local, N, K] with [E_local, N, K/32]; bf16 bits or float64 out."""
+    lhs = _c(lhs, np.uint8)
+    rhs = _c(rhs, np.uint8)
+    M, K = lhs.shape
+    El, N, K2 = rhs.shape
+    assert K2 == K and K % 32 == 0
+    lsf = _c(lhs_sf, np.uint8)
+    rsf = _c(rhs_sf, np.uint8)
+    assert lsf.shape == (M, K // 32) and rsf.shape == (El, N, K // 32)
+    sizes = _c(group_sizes, np.int32)
+    E = len(sizes)
+    if E_local is None:
+        E_local = E - group_offset
+    assert El == E_local
+    r = None if rows is None else _c(rows, np.int64)
+    nrows = M if r is None else len(r)
+    ob = np.empty((nrows, N), np.uint16) if want == "bf16" else None
+    of = np.empty((nrows, N), np.float64) if want != "bf16" else None
+    lib().or_gmm_mx(_p(lhs), _p(lsf), _p(rhs), _p(rsf), _p(sizes), E, group_offset, E_local, M, K, N, _p(r), nrows,
+                    _p(ob), _p(of))
+    return ob if want == "bf16" else of
+
+
 def gmm_f64(lhs, rhs, group_sizes, group_offset=0, E_local=None):
     lhs = _c(lhs, np.float64)
     rhs = _c(rhs, np.float64)
@@ -280,6 +337,19 @@ def swiglu_quant(a_bits, mode: int, static_scale: float = 1.0):
     lib().or_swiglu_quant(_p(a), R, F, mode, float(static_scale), _p(hq),
                           _p(hs) if mode != PER_TENSOR else None, _p(hb))
     return hq, hs, hb
+
+
+def swiglu_quant_mx(a_bits):
+    """a = [a0 | a1] bf16 [R, 2F] -> (h codes [R, F], h E8M0 codes [R, F/32], h bf16 bits)."""
+    a = _c(a_bits, np.uint16)
+    R, F2 = a.shape
+    F = F2 // 2
+    assert F % 32 == 0
+    hq = np.empty((R, F), np.uint8)
+    hsf = np.empty((R, F // 32), np.uint8)
+    hb = np.empty((R, F), np.uint16)
+    lib().or_swiglu_quant_mx(_p(a), R, F, _p(hq), _p(hsf), _p(hb))
+    return hq, hsf, hb
 
 
 def combine(o_bits, pos, w, k: int, tokens=None, want="bf16"):
@@ -469,6 +539,47 @@ def ffn_forward(x_bits, topk_ids, topk_w, wq, E: int, act_mode: int, static=None
         o = o_rows
     return dict(x_q=x_q, x_s=x_s, sorted_src=sorted_src, pos=pos, sizes=sizes, offsets=offsets,
                 xs_q=xs_q, xs_s=xs_s, rows=rows, a=a, h_q=h_q, h_s=h_s, h_b=h_b, o=o, y=y)
+
+
+def prepare_weights_mx(w_in_bits, w_out_bits):
+    """MXFP8 expert weights: (w_in codes, w_in E8M0 codes, w_out codes, w_out E8M0 codes)."""
+    qin, sin = quantize_weights_mx(w_in_bits)
+    qo, so = quantize_weights_mx(w_out_bits)
+    return qin, sin, qo, so
+
+
+def ffn_forward_mx(x_bits, topk_ids, topk_w, wq, E: int, tokens=None):
+    """The forward pass in the pages' order on MXFP8 operands: quantise ->
+    sort/gather -> gmm(wi_0|wi_1) -> SwiGLU + MX requantise -> gmm(wo) ->
+    gather-reduce.  wq = prepare_weights_mx(...); `tokens` as in ffn_forward."""
+    qin, sin, qo, so = wq
+    T, D = x_bits.shape
+    k = topk_ids.shape[1]
+    x_q, x_sf = quantize_rows_mx(x_bits)
+    sorted_src, pos, sizes, offsets = ragged_sort(topk_ids, E)
+    xs_q, xs_sf = gather_rows_mx(x_q, x_sf, sorted_src, k)
+    rows = None
+    if tokens is not None:
+        tokens = np.asarray(tokens, np.int64)
+        rows = np.sort(pos.reshape(T, k)[tokens].reshape(-1)).astype(np.int64)
+    a = gmm_mx(xs_q, xs_sf, qin, sin, sizes, rows=rows)
+    h_q, h_sf, h_b = swiglu_quant_mx(a)
+    if rows is None:
+        o = gmm_mx(h_q, h_sf, qo, so, sizes)
+        y = combine(o, pos, topk_w, k)
+    else:
+        R = T * k
+        hq_full = np.zeros((R, h_q.shape[1]), np.uint8)
+        hq_full[rows] = h_q
+        hsf_full = np.full((R, h_sf.shape[1]), 127, np.uint8)
+        hsf_full[rows] = h_sf
+        o_rows = gmm_mx(hq_full, hsf_full, qo, so, sizes, rows=rows)
+        o = np.zeros((R, D), np.uint16)
+        o[rows] = o_rows
+        y = combine(o, pos, topk_w, k, tokens=tokens)
+        o = o_rows
+    return dict(x_q=x_q, x_sf=x_sf, sorted_src=sorted_src, pos=pos, sizes=sizes, offsets=offsets,
+                xs_q=xs_q, xs_sf=xs_sf, rows=rows, a=a, h_q=h_q, h_sf=h_sf, h_b=h_b, o=o, y=y)
 
 
 def ffn_backward(fwd: dict, G_bits, topk_w, wq, k: int, static: dict):

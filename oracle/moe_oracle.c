@@ -24,6 +24,12 @@
  *            [E, blocks, 1, N] scales; the matmul accumulator must be 32-bit
  *            (the Mosaic error quoted in the description).
  *
+ *   [MX]     The MXFP8 variant is not a method of the pages: it is the
+ *            Blackwell block-scaled form of the same path, defined by the OCP
+ *            "Microscaling Formats (MX) Specification" v1.0 (MXFP8: blocks of
+ *            32 e4m3 elements along the contracted dimension sharing one
+ *            power-of-two E8M0 scale).  Its functions are marked [MX].
+ *
  * Arithmetic.  fp8 codes and bf16 values are decoded exactly to double and
  * every contraction accumulates in double.  Products of two e4m3 values carry
  * at most 8 significant bits and lie in [2^-18, 2^17.6], so every raw code
@@ -44,6 +50,7 @@
 #define OR_PER_ROW_BLOCK128 1
 #define OR_PER_TENSOR 2
 #define OR_PER_GROUP_COL 3
+#define OR_MX32 4 /* [MX]: uint8 E8M0 codes, one per 32 values along K */
 
 #define E4M3_MAX 448.0
 
@@ -261,6 +268,53 @@ void or_quantize_weights(const uint16_t* w, int64_t E, int64_t N, int64_t K, int
 }
 
 /* ------------------------------------------------------------------------ */
+/* [MX] MXFP8 quantisation (OCP MX v1.0, MXFP8 with E4M3 elements).  Each   */
+/* block of 32 consecutive values of a row shares the scale 2^X with        */
+/*   X = floor(log2(amax)) - 8,                                             */
+/* 8 being the exponent of the largest power of two that e4m3 holds (256),  */
+/* clamped to the E8M0 range [-127, 127]; the block's E8M0 code is X + 127. */
+/* The elements are e4m3(v / 2^X), nearest with ties to even and saturating */
+/* at 448 (v / 2^X < 512, so only the top binade can saturate).  A block of */
+/* zeros takes X = -127 (code 0), the smallest scale.                       */
+/* ------------------------------------------------------------------------ */
+
+static int mx_shared_exp(float amax) {
+  if (amax == 0.0f) return -127;
+  int e;
+  frexp((double)amax, &e); /* amax = f 2^e with f in [0.5, 1): floor(log2 amax) = e - 1 */
+  int X = e - 1 - 8;
+  if (X < -127) X = -127;
+  if (X > 127) X = 127;
+  return X;
+}
+
+/* fp32 rows [rows, cols] (cols a multiple of 32) -> codes and E8M0 codes [rows, cols/32]. */
+static void quantize_rows_mx_f32(const float* x, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sf) {
+  int64_t nb = cols / 32;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* xb = x + r * cols + b * 32;
+      int X = mx_shared_exp(amax_f32(xb, 32));
+      sf[r * nb + b] = (uint8_t)(X + 127);
+      /* v / 2^X is exact in double; as fp32 it is exact too unless it falls
+       * below 2^-126, far under e4m3's smallest half-step (2^-10) */
+      for (int i = 0; i < 32; ++i) q[r * cols + b * 32 + i] = or_f32_to_e4m3((float)ldexp((double)xb[i], -X));
+    }
+}
+
+/* [MX] bf16 rows -> MXFP8 codes [rows, cols] and E8M0 codes [rows, cols/32].
+ * Expert weights w[E, N, K] are the rows e*N + n, so their scales come out
+ * as [E, N, K/32]. */
+void or_quantize_rows_mx(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sf) {
+  float* xf = (float*)malloc(sizeof(float) * (size_t)(rows * cols));
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < rows * cols; ++i) xf[i] = (float)or_bf16_to_f64(x[i]);
+  quantize_rows_mx_f32(xf, rows, cols, q, sf);
+  free(xf);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Ragged sort by routed expert ([Q-EP]: ragged_sort / ragged_gather).      */
 /* Flat pair i = t*k + j goes to expert ids[i].  Stable counting sort: by   */
 /* expert ascending, then by i ascending.  sorted_src[r] = i, pos[i] = r.   */
@@ -313,16 +367,28 @@ void or_gather_rows(const uint8_t* x_q, const float* x_scale, int mode, int64_t 
 /* rows.                                                                    */
 /* ------------------------------------------------------------------------ */
 
-static double lhs_scale_at(const float* s, int mode, int64_t m, int64_t b, int64_t nb) {
-  if (mode == OR_PER_ROW) return s[m];
-  if (mode == OR_PER_ROW_BLOCK128) return s[m * nb + b];
-  return s[0];
+/* [MX] the power of two an E8M0 code stands for: 2^(c - 127) (c = 255, NaN,
+ * is never produced by the quantiser). */
+static double e8m0_to_f64(uint8_t c) { return ldexp(1.0, (int)c - 127); }
+
+/* Scale of lhs element (m, k): fp32 scales per row, per (row, 128-column
+ * block) or per tensor; [MX] E8M0 codes per (row, 32-column block). */
+static double lhs_scale_at(const void* s, int mode, int64_t m, int64_t kk, int64_t K) {
+  const float* f = (const float*)s;
+  if (mode == OR_PER_ROW) return f[m];
+  if (mode == OR_PER_ROW_BLOCK128) return f[m * ((K + 127) / 128) + kk / 128];
+  if (mode == OR_MX32) return e8m0_to_f64(((const uint8_t*)s)[m * (K / 32) + kk / 32]);
+  return f[0];
 }
 
-static double rhs_scale_at(const float* s, int mode, int64_t e, int64_t n, int64_t b, int64_t N, int64_t nb) {
-  if (mode == OR_PER_ROW) return s[e * N + n];
-  if (mode == OR_PER_ROW_BLOCK128) return s[(e * nb + b) * N + n];
-  return s[0];
+/* Scale of rhs element (e, n, k) of w[E_local, N, K]: per channel [E, N],
+ * blockwise [E, K/128, N], per tensor; [MX] E8M0 codes [E, N, K/32]. */
+static double rhs_scale_at(const void* s, int mode, int64_t e, int64_t n, int64_t kk, int64_t N, int64_t K) {
+  const float* f = (const float*)s;
+  if (mode == OR_PER_ROW) return f[e * N + n];
+  if (mode == OR_PER_ROW_BLOCK128) return f[(e * ((K + 127) / 128) + kk / 128) * N + n];
+  if (mode == OR_MX32) return e8m0_to_f64(((const uint8_t*)s)[(e * N + n) * (K / 32) + kk / 32]);
+  return f[0];
 }
 
 static int group_of_row(const int64_t* starts, int E, int64_t m) {
@@ -336,10 +402,10 @@ static int group_of_row(const int64_t* starts, int E, int64_t m) {
 
 /* rows: optional list of nrows output rows to compute (NULL = all M rows).
  * out_bf16 / out_f64 (either may be NULL) are [nrows, N]. */
-void or_gmm(const uint8_t* lhs, const float* lhs_scale, int lhs_mode, const uint8_t* rhs, const float* rhs_scale,
-            int rhs_mode, const int32_t* group_sizes, int E, int g0, int E_local, int64_t M, int64_t K, int64_t N,
-            const int64_t* rows, int64_t nrows, uint16_t* out_bf16, double* out_f64) {
-  int64_t nb = (K + 127) / 128;
+static void gmm_core(const uint8_t* lhs, const void* lhs_scale, int lhs_mode, const uint8_t* rhs,
+                     const void* rhs_scale, int rhs_mode, const int32_t* group_sizes, int E, int g0, int E_local,
+                     int64_t M, int64_t K, int64_t N, const int64_t* rows, int64_t nrows, uint16_t* out_bf16,
+                     double* out_f64) {
   int64_t* starts = (int64_t*)malloc(sizeof(int64_t) * (size_t)(E + 1));
   starts[0] = 0;
   for (int e = 0; e < E; ++e) starts[e + 1] = starts[e] + group_sizes[e];
@@ -353,7 +419,7 @@ void or_gmm(const uint8_t* lhs, const float* lhs_scale, int lhs_mode, const uint
     int g = (m < starts[E]) ? group_of_row(starts, E, m) : -1;
     grp[i] = (g >= g0 && g < g0 + E_local) ? g : -1;
     for (int64_t kk = 0; kk < K; ++kk)
-      a[i * K + kk] = or_e4m3_to_f64(lhs[m * K + kk]) * lhs_scale_at(lhs_scale, lhs_mode, m, kk / 128, nb);
+      a[i * K + kk] = or_e4m3_to_f64(lhs[m * K + kk]) * lhs_scale_at(lhs_scale, lhs_mode, m, kk, K);
   }
 #pragma omp parallel
   {
@@ -369,7 +435,7 @@ void or_gmm(const uint8_t* lhs, const float* lhs_scale, int lhs_mode, const uint
             int64_t el = g - g0;
             const uint8_t* wr = rhs + (el * N + n) * K;
             for (int64_t kk = 0; kk < K; ++kk)
-              w[kk] = or_e4m3_to_f64(wr[kk]) * rhs_scale_at(rhs_scale, rhs_mode, el, n, kk / 128, N, nb);
+              w[kk] = or_e4m3_to_f64(wr[kk]) * rhs_scale_at(rhs_scale, rhs_mode, el, n, kk, N, K);
             cur = g;
           }
           const double* ar = a + i * K;
@@ -384,6 +450,24 @@ void or_gmm(const uint8_t* lhs, const float* lhs_scale, int lhs_mode, const uint
   free(a);
   free(grp);
   free(starts);
+}
+
+void or_gmm(const uint8_t* lhs, const float* lhs_scale, int lhs_mode, const uint8_t* rhs, const float* rhs_scale,
+            int rhs_mode, const int32_t* group_sizes, int E, int g0, int E_local, int64_t M, int64_t K, int64_t N,
+            const int64_t* rows, int64_t nrows, uint16_t* out_bf16, double* out_f64) {
+  gmm_core(lhs, lhs_scale, lhs_mode, rhs, rhs_scale, rhs_mode, group_sizes, E, g0, E_local, M, K, N, rows, nrows,
+           out_bf16, out_f64);
+}
+
+/* [MX] The same grouped matmul on MXFP8 operands: lhs_sf [M, K/32] and
+ * rhs_sf [E_local, N, K/32] hold the E8M0 codes of each 32-element block
+ * along K, so deq(x)[.., k] = e4m3(x[.., k]) * 2^(sf[.., k/32] - 127).  K is a
+ * multiple of 32. */
+void or_gmm_mx(const uint8_t* lhs, const uint8_t* lhs_sf, const uint8_t* rhs, const uint8_t* rhs_sf,
+               const int32_t* group_sizes, int E, int g0, int E_local, int64_t M, int64_t K, int64_t N,
+               const int64_t* rows, int64_t nrows, uint16_t* out_bf16, double* out_f64) {
+  gmm_core(lhs, lhs_sf, OR_MX32, rhs, rhs_sf, OR_MX32, group_sizes, E, g0, E_local, M, K, N, rows, nrows, out_bf16,
+           out_f64);
 }
 
 /* The same contraction on double operands (no quantisation), used to pin
@@ -412,8 +496,7 @@ void or_gmm_f64(const double* lhs, const double* rhs, const int32_t* group_sizes
 /* wi_0 / wi_1 gmm ([R, 2F]); h = bf16(silu(a0) * a1) in fp32, then h is    */
 /* quantised exactly as the activations are.                                */
 /* ------------------------------------------------------------------------ */
-void or_swiglu_quant(const uint16_t* a, int64_t R, int64_t F, int mode, float static_scale, uint8_t* h_q,
-                     float* h_scale, uint16_t* h_bf16) {
+static float* swiglu_rows(const uint16_t* a, int64_t R, int64_t F, uint16_t* h_bf16) {
   float* h = (float*)malloc(sizeof(float) * (size_t)(R * F));
 #pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < R; ++r)
@@ -425,7 +508,21 @@ void or_swiglu_quant(const uint16_t* a, int64_t R, int64_t F, int mode, float st
       if (h_bf16) h_bf16[r * F + f] = hb;
       h[r * F + f] = (float)or_bf16_to_f64(hb);
     }
+  return h;
+}
+
+void or_swiglu_quant(const uint16_t* a, int64_t R, int64_t F, int mode, float static_scale, uint8_t* h_q,
+                     float* h_scale, uint16_t* h_bf16) {
+  float* h = swiglu_rows(a, R, F, h_bf16);
   quantize_rows_f32(h, R, F, mode, static_scale, h_q, h_scale);
+  free(h);
+}
+
+/* [MX] The same h, requantised to MXFP8 along F (the wo gmm's contracted
+ * dimension): codes [R, F], E8M0 codes [R, F/32]. */
+void or_swiglu_quant_mx(const uint16_t* a, int64_t R, int64_t F, uint8_t* h_q, uint8_t* h_sf, uint16_t* h_bf16) {
+  float* h = swiglu_rows(a, R, F, h_bf16);
+  quantize_rows_mx_f32(h, R, F, h_q, h_sf);
   free(h);
 }
 

@@ -27,6 +27,7 @@ PER_ROW = 0           # one fp32 scale per row
 PER_ROW_BLOCK128 = 1  # one fp32 scale per row and per 128 columns
 PER_TENSOR = 2        # one fixed fp32 scale for the whole tensor
 PER_GROUP_COL = 3     # one fp32 scale per (expert, column) (weight-gradient operands)
+MX32 = 4              # MXFP8: one E8M0 (power-of-two) code per row and per 32 columns
 
 
 @dataclasses.dataclass(frozen=True)
@@ -55,6 +56,10 @@ CONFIGS = {
     "prefill": MoEConfig("prefill", 2048, 2048, 128, 8, 768, PER_ROW, PER_ROW_BLOCK128, "normal"),
     "fwdbwd": MoEConfig("fwdbwd", 8192, 4096, 64, 6, 1408, PER_TENSOR, PER_TENSOR, "zipf",
                         backward=True),
+    # the MXFP8 variant of two of the shapes above (activations, h and
+    # weights all in MXFP8)
+    "dsv3_mx": MoEConfig("dsv3_mx", 16384, 7168, 256, 8, 2048, MX32, MX32, "normal"),
+    "mixtral_mx": MoEConfig("mixtral_mx", 8192, 4096, 8, 2, 14336, MX32, MX32, "uniform"),
 }
 
 
