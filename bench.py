@@ -70,8 +70,8 @@ def dist_env():
 
 
 def workload_name(cfg) -> str:
-    modes = {0: "per-token", 1: "per-token-per-128", 2: "static"}
-    wmodes = {0: "per-channel", 1: "blockwise [E, K/128, N]", 2: "static"}
+    modes = {0: "per-token", 1: "per-token-per-128", 2: "static", 4: "MXFP8 (E8M0 per 32 columns)"}
+    wmodes = {0: "per-channel", 1: "blockwise [E, K/128, N]", 2: "static", 4: "MXFP8 (E8M0 per 32 of K)"}
     return (f"{cfg.name} MoE expert FFN fwd: T={cfg.T} d_model={cfg.D} E={cfg.E} top-k={cfg.k} d_ff={cfg.F} SwiGLU; "
             f"e4m3 {modes[cfg.act_mode]} activation scales, {wmodes[cfg.w_mode]} weight scales")
 
@@ -541,6 +541,29 @@ def run_reference(args, cfg, rank, world):
 # Per-call suite: every step of the path timed alone against its roofline
 # ---------------------------------------------------------------------------
 
+def mx_calls(moe, cfg, x, ids, w, W, buf):
+    """The MXFP8 variant's calls: (label, fn, bound, work), E8M0 codes one
+    byte per 32 values (1/32 of the codes' bytes)."""
+    T, D, E, k, F = cfg.T, cfg.D, cfg.E, cfg.k, cfg.F
+    R = T * k
+    s = buf.sort
+    return [
+        ("quantize_sort_mx (steps 1 + 2 fused)", lambda: moe.quantize_sort_mx(x, ids, E, out=s),
+         "hbm", 2 * T * D + R * D + R * D // 32 + 16 * R),
+        ("gmm_fp8_mx_swiglu (wi_0|wi_1 + SwiGLU + MX requant)",
+         lambda: moe.gmm_mx_swiglu(s["xs_q"], s["xs_scale"], W.w_in, W.s_in, s["group_sizes"], h_q=buf.h_q,
+                                   h_sf=buf.h_s),
+         "tensor", (2.0 * R * D * 2 * F, (R * D + E * 2 * F * D + R * F) * 33 // 32)),
+        ("gmm_fp8_mx wi_0|wi_1", lambda: moe.gmm_mx(s["xs_q"], s["xs_scale"], W.w_in, W.s_in, s["group_sizes"],
+                                                    out=buf.a),
+         "tensor", (2.0 * R * D * 2 * F, (R * D + E * 2 * F * D) * 33 // 32 + 4 * R * F)),
+        ("moe_swiglu_quant_mx", lambda: moe.swiglu_quant_mx(buf.a, h_q=buf.h_q, h_sf=buf.h_s),
+         "hbm", 4 * R * F + R * F * 33 // 32),
+        ("gmm_fp8_mx wo", lambda: moe.gmm_mx(buf.h_q, buf.h_s, W.w_out, W.s_out, s["group_sizes"], out=buf.o),
+         "tensor", (2.0 * R * F * D, (R * F + E * D * F) * 33 // 32 + 2 * R * D)),
+    ]
+
+
 def run_suite(args):
     import fp8_quantized_moe_gb300 as moe
 
@@ -596,7 +619,12 @@ def run_suite(args):
         sbytes = lambda rows, cols: 0 if am == 2 else 4 * rows * (1 if am == 0 else nb(cols))
         xs_s = buf.sort["xs_scale"] if am != 2 else sx
         h_s = buf.h_s if am != 2 else sh
-        calls = [
+        if am == synth.MX32:
+            calls = mx_calls(moe, cfg, x, ids, w, W, buf)
+            fused, fusable = True, True
+        else:
+            calls = []
+        calls += [] if am == synth.MX32 else [
             ("quantize_sort (steps 1 + 2 fused)", lambda: moe.quantize_sort(x, ids, E, am, sx, out=buf.sort),
              "hbm", 2 * T * D + R * D + 16 * R + sbytes(R, D)),
             ("quantize_rows x", lambda: moe.quantize_rows(x, am, sx, q=buf.x_q, scale=buf.x_s),
@@ -605,20 +633,22 @@ def run_suite(args):
                                                                out=buf.sort),
              "hbm", T * D + R * D + 16 * R + 2 * sbytes(T, D)),
         ]
-        if fusable:
+        if fusable and am != synth.MX32:
             calls.append(("gmm_fp8_swiglu (wi_0|wi_1 + SwiGLU + requant)",
                           lambda: moe.gmm_swiglu(buf.sort["xs_q"], xs_s, am, W.w_in, W.s_in, W.in_mode,
                                                  buf.sort["group_sizes"], am, sh, h=buf.h, h_q=buf.h_q,
                                                  h_scale=buf.h_s, a_out=buf.a if buf.keep_a else None),
                           "tensor", (2.0 * R * D * 2 * F, R * D + E * 2 * F * D + (5 if am == 0 else 1) * R * F)))
-        calls.append(("gmm_fp8 wi_0|wi_1", lambda: moe.gmm(buf.sort["xs_q"], xs_s, am, W.w_in, W.s_in, W.in_mode,
-                                                           buf.sort["group_sizes"], out=buf.a),
-                      "tensor", (2.0 * R * D * 2 * F, R * D + E * 2 * F * D + 4 * R * F)))
-        calls.append(("moe_swiglu_quant", lambda: moe.swiglu_quant(buf.a, am, sh, h_q=buf.h_q, h_scale=buf.h_s),
-                      "hbm", 5 * R * F + sbytes(R, F)))
-        calls.append(("gmm_fp8 wo", lambda: moe.gmm(buf.h_q, h_s, am, W.w_out, W.s_out, W.out_mode,
-                                                    buf.sort["group_sizes"], out=buf.o),
-                      "tensor", (2.0 * R * F * D, R * F + E * D * F + 2 * R * D)))
+        if am != synth.MX32:
+            calls.append(("gmm_fp8 wi_0|wi_1", lambda: moe.gmm(buf.sort["xs_q"], xs_s, am, W.w_in, W.s_in,
+                                                               W.in_mode, buf.sort["group_sizes"], out=buf.a),
+                          "tensor", (2.0 * R * D * 2 * F, R * D + E * 2 * F * D + 4 * R * F)))
+            calls.append(("moe_swiglu_quant", lambda: moe.swiglu_quant(buf.a, am, sh, h_q=buf.h_q,
+                                                                       h_scale=buf.h_s),
+                          "hbm", 5 * R * F + sbytes(R, F)))
+            calls.append(("gmm_fp8 wo", lambda: moe.gmm(buf.h_q, h_s, am, W.w_out, W.s_out, W.out_mode,
+                                                        buf.sort["group_sizes"], out=buf.o),
+                          "tensor", (2.0 * R * F * D, R * F + E * D * F + 2 * R * D)))
         calls.append(("ragged_gather_reduce", lambda: moe.ragged_gather_reduce(buf.o, buf.sort["pos"], w, k,
                                                                                 out=buf.y),
                       "hbm", 2 * R * D + 2 * T * D + 8 * R))
@@ -689,7 +719,10 @@ def run_suite(args):
                     bound, ach, peak, unit = "hbm", nbytes / (ms / 1e3) / 1e9, hbm, "GB/s"
                 else:
                     ach, peak, unit = flops / (ms / 1e3) / 1e12, fp8, "TFLOP/s"
-            if label.startswith("gmm_fp8_swiglu"):
+            if am == synth.MX32:
+                on_path = label.startswith(("quantize_sort_mx", "gmm_fp8_mx_swiglu", "gmm_fp8_mx wo",
+                                            "ragged_gather_reduce"))
+            elif label.startswith("gmm_fp8_swiglu"):
                 on_path = fused
             elif label.startswith("router"):
                 on_path = False  # routing is an input of the FFN step

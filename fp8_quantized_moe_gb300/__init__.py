@@ -10,6 +10,11 @@ quantize_rows -> ragged_sort -> gmm (wi_0 | wi_1) -> swiglu_quant ->
 gmm (wo) -> ragged_gather_reduce.  The backward pass of the static scheme
 ("Support quantization for tokamax gmm v2": fp8_static_wa) adds
 gather_scale_quant, swiglu_bwd_quant, quantize_group_cols and tgmm.
+
+The MXFP8 variant (MX32: OCP MX v1.0 blocks of 32 e4m3 values sharing one
+E8M0 power-of-two scale along the contracted dimension) runs the same
+forward path on the block-scaled tensor-core MMA: quantize_sort_mx ->
+gmm_mx_swiglu (or gmm_mx + swiglu_quant_mx) -> gmm_mx -> ragged_gather_reduce.
 """
 
 from __future__ import annotations
@@ -27,12 +32,14 @@ PER_ROW = 0
 PER_ROW_BLOCK128 = 1
 PER_TENSOR = 2
 PER_GROUP_COL = 3
+MX32 = 4  # MXFP8: uint8 E8M0 codes, K-block-major [cols/128, rows, 4]
 
 __all__ = [
     "PER_ROW", "PER_ROW_BLOCK128", "PER_TENSOR", "PER_GROUP_COL", "MoEError", "lib", "device_error",
     "quantize_rows", "quantize_weights", "ragged_sort", "gmm", "gmm_swiglu", "swiglu_fusable", "swiglu_fuse_pays", "swiglu_quant", "ragged_gather_reduce",
     "gather_scale_quant", "swiglu_bwd_quant", "quantize_group_cols", "tgmm", "transpose_u8",
-    "router_topk", "router_backward",
+    "router_topk", "router_backward", "MX32", "quantize_rows_mx", "quantize_weights_mx", "quantize_sort_mx",
+    "gmm_mx", "gmm_mx_swiglu", "swiglu_quant_mx",
     "ExpertWeights", "prepare_weights", "FFNBuffers", "ffn_forward", "ffn_backward",
 ]
 
@@ -75,6 +82,8 @@ def _scale_buf(mode: int, rows: int, cols: int, device, out=None):
         return torch.empty(rows, dtype=torch.float32, device=device)
     if mode == PER_ROW_BLOCK128:
         return torch.empty(rows, _nb(cols), dtype=torch.float32, device=device)
+    if mode == MX32:
+        return torch.empty(cols // 128, rows, 4, dtype=torch.uint8, device=device)
     return None
 
 
@@ -101,6 +110,22 @@ def quantize_weights(w: torch.Tensor, mode: int, static_scale: Optional[torch.Te
     check(lib().moe_quantize_weights(_p(w), E, N, K, mode, _p(static_scale), _p(q), _p(s), _s()),
           "moe_quantize_weights")
     return q, s
+
+
+def quantize_rows_mx(x: torch.Tensor, q=None, sf=None):
+    """MXFP8: bf16 [rows, cols] -> (e4m3 codes [rows, cols], E8M0 codes uint8 [cols/128, rows, 4])."""
+    rows, cols = x.shape
+    q = torch.empty(rows, cols, dtype=torch.uint8, device=x.device) if q is None else q
+    sf = _scale_buf(MX32, rows, cols, x.device, sf)
+    check(lib().moe_quantize_rows_mx(_p(x), rows, cols, _p(q), _p(sf), _s()), "moe_quantize_rows_mx")
+    return q, sf
+
+
+def quantize_weights_mx(w: torch.Tensor):
+    """MXFP8 weights: bf16 [E, N, K] -> (codes [E, N, K], E8M0 codes [K/128, E*N, 4])."""
+    E, N, K = w.shape
+    q, sf = quantize_rows_mx(w.reshape(E * N, K))
+    return q.view(E, N, K), sf
 
 
 def ragged_sort(topk_ids: torch.Tensor, E: int, x_q: torch.Tensor, x_scale: Optional[torch.Tensor], mode: int,
@@ -152,6 +177,75 @@ def quantize_sort(x: torch.Tensor, topk_ids: torch.Tensor, E: int, mode: int,
                                   _p(o["pos"]), _p(o["group_sizes"]), _p(o["group_offsets"]), _p(o["xs_q"]),
                                   _p(xs_scale), _p(o["sort_ws"]), o["sort_ws"].numel(), _s()), "moe_quantize_sort")
     return o
+
+
+def quantize_sort_mx(x: torch.Tensor, topk_ids: torch.Tensor, E: int, out: Optional[dict] = None):
+    """MXFP8 steps 1 + 2: the dict of quantize_sort with xs_scale = E8M0 codes [D/128, T*k, 4]."""
+    T, k = topk_ids.shape
+    D = x.shape[1]
+    R = T * k
+    dev = x.device
+    o = out if out is not None else {}
+    if "sorted_src" not in o:
+        o["sorted_src"] = torch.empty(R, dtype=torch.int32, device=dev)
+        o["pos"] = torch.empty(R, dtype=torch.int32, device=dev)
+        o["group_sizes"] = torch.empty(E, dtype=torch.int32, device=dev)
+        o["group_offsets"] = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        o["xs_q"] = torch.empty(R, D, dtype=torch.uint8, device=dev)
+        o["xs_scale"] = _scale_buf(MX32, R, D, dev)
+    nws = lib().moe_ragged_sort_workspace_bytes(T, k, E)
+    if "sort_ws" not in o or o["sort_ws"].numel() < nws:
+        o["sort_ws"] = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+    check(lib().moe_quantize_sort_mx(_p(x), _p(topk_ids), T, k, E, D, _p(o["sorted_src"]), _p(o["pos"]),
+                                     _p(o["group_sizes"]), _p(o["group_offsets"]), _p(o["xs_q"]), _p(o["xs_scale"]),
+                                     _p(o["sort_ws"]), o["sort_ws"].numel(), _s()), "moe_quantize_sort_mx")
+    return o
+
+
+def gmm_mx(lhs_q, lhs_sf, rhs_q, rhs_sf, group_sizes, group_offset: int = 0, E_local: Optional[int] = None,
+           out=None):
+    """MXFP8 grouped matmul -> bf16 [M, N]; lhs_sf [K/128, M, 4], rhs_sf [K/128, E_local*N, 4]."""
+    M, K = lhs_q.shape
+    El, N, K2 = rhs_q.shape
+    if K2 != K:
+        raise MoEError("lhs/rhs K mismatch")
+    E = group_sizes.numel()
+    E_local = El if E_local is None else E_local
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=lhs_q.device) if out is None else out
+    check(lib().gmm_fp8_mx(_p(lhs_q), _p(lhs_sf), _p(rhs_q), _p(rhs_sf), _p(group_sizes), E, group_offset, E_local,
+                           M, K, N, _p(out), _s()), "gmm_fp8_mx")
+    return out
+
+
+def gmm_mx_swiglu(lhs_q, lhs_sf, rhs_q, rhs_sf, group_sizes, group_offset: int = 0, E_local: Optional[int] = None,
+                  keep_a: bool = False, a_out=None, h_q=None, h_sf=None):
+    """MXFP8 gmm with [wi_0 | wi_1] fused with SwiGLU and the MXFP8
+    requantisation of h.  Returns (h_q [M, F], h_sf [F/128, M, 4], a [M, 2F] bf16 or None)."""
+    M, K = lhs_q.shape
+    El, F2, K2 = rhs_q.shape
+    if K2 != K:
+        raise MoEError("lhs/rhs K mismatch")
+    F = F2 // 2
+    dev = lhs_q.device
+    E = group_sizes.numel()
+    E_local = El if E_local is None else E_local
+    h_q = torch.empty(M, F, dtype=torch.uint8, device=dev) if h_q is None else h_q
+    h_sf = _scale_buf(MX32, M, F, dev, h_sf)
+    if keep_a and a_out is None:
+        a_out = torch.empty(M, F2, dtype=torch.bfloat16, device=dev)
+    check(lib().gmm_fp8_mx_swiglu(_p(lhs_q), _p(lhs_sf), _p(rhs_q), _p(rhs_sf), _p(group_sizes), E, group_offset,
+                                  E_local, M, K, F, _p(a_out), _p(h_q), _p(h_sf), _s()), "gmm_fp8_mx_swiglu")
+    return h_q, h_sf, a_out
+
+
+def swiglu_quant_mx(a: torch.Tensor, h_q=None, h_sf=None):
+    """MXFP8 step 4: a = [a0 | a1] bf16 [R, 2F] -> (h codes [R, F], h E8M0 codes [F/128, R, 4])."""
+    R, F2 = a.shape
+    F = F2 // 2
+    h_q = torch.empty(R, F, dtype=torch.uint8, device=a.device) if h_q is None else h_q
+    h_sf = _scale_buf(MX32, R, F, a.device, h_sf)
+    check(lib().moe_swiglu_quant_mx(_p(a), R, F, _p(h_q), _p(h_sf), _s()), "moe_swiglu_quant_mx")
+    return h_q, h_sf
 
 
 def gmm(lhs_q, lhs_scale, lhs_mode, rhs_q, rhs_scale, rhs_mode, group_sizes, group_offset: int = 0,
@@ -396,6 +490,10 @@ def prepare_weights(w_in: torch.Tensor, w_out: torch.Tensor, w_mode: int, static
     dev = w_in.device
     E, F2, D = w_in.shape
     F = F2 // 2
+    if w_mode == MX32:
+        qin, sin = quantize_weights_mx(w_in)
+        qo, so = quantize_weights_mx(w_out)
+        return ExpertWeights(qin, sin, MX32, qo, so, MX32)
     if w_mode == PER_TENSOR:
         s0 = torch.tensor([static["w0"]], dtype=torch.float32, device=dev)
         s1 = torch.tensor([static["w1"]], dtype=torch.float32, device=dev)
@@ -461,6 +559,19 @@ def ffn_forward(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, W
     a backward pass."""
     E = W.w_in.shape[0]
     k = topk_ids.shape[1]
+    if act_mode == MX32:
+        if W.in_mode != MX32:
+            raise MoEError("the MXFP8 forward needs MXFP8 weights")
+        s = quantize_sort_mx(x, topk_ids, E, out=buf.sort)
+        if fuse_swiglu and buf.F % 128 == 0:
+            gmm_mx_swiglu(s["xs_q"], s["xs_scale"], W.w_in, W.s_in, s["group_sizes"],
+                          a_out=buf.a if buf.keep_a else None, h_q=buf.h_q, h_sf=buf.h_s)
+        else:
+            gmm_mx(s["xs_q"], s["xs_scale"], W.w_in, W.s_in, s["group_sizes"], out=buf.a)
+            swiglu_quant_mx(buf.a, h_q=buf.h_q, h_sf=buf.h_s)
+        gmm_mx(buf.h_q, buf.h_s, W.w_out, W.s_out, s["group_sizes"], out=buf.o)
+        ragged_gather_reduce(buf.o, s["pos"], topk_w, k, out=buf.y)
+        return buf.y
     if fuse_quant_sort:
         s = quantize_sort(x, topk_ids, E, act_mode, static_x, out=buf.sort)
     else:

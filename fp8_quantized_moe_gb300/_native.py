@@ -45,6 +45,11 @@ SIGNATURES = {
     "moe_test_stall_epilogue": ([ctypes.c_uint64], None),
     "moe_router_backward_workspace_bytes": ([i64, i64, i32], sz),
     "moe_router_backward": ([P, P, P, P, P, P, P, i64, i64, i32, i32, P, P, P, P, P, sz, P], i32),
+    "moe_quantize_rows_mx": ([P, i64, i64, P, P, P], i32),
+    "moe_quantize_sort_mx": ([P, P, i64, i32, i32, i64, P, P, P, P, P, P, P, sz, P], i32),
+    "gmm_fp8_mx": ([P, P, P, P, P, i32, i32, i32, i64, i64, i64, P, P], i32),
+    "gmm_fp8_mx_swiglu": ([P, P, P, P, P, i32, i32, i32, i64, i64, i64, P, P, P, P], i32),
+    "moe_swiglu_quant_mx": ([P, i64, i64, P, P, P], i32),
 }
 
 _lock = threading.Lock()

@@ -106,6 +106,20 @@ __device__ __forceinline__ uint2 pack_e4m3x8(const float* v) {
 // Absmax scale in fp32: amax / 448, or 1 for an all-zero span.
 __device__ __forceinline__ float absmax_scale(float amax) { return amax > 0.0f ? __fdiv_rn(amax, kE4M3Max) : 1.0f; }
 
+// MXFP8 (OCP MX v1.0) shared exponent of a 32-value block: floor(log2(amax))
+// - 8, clamped to [-127, 127], -127 for amax = 0.  Read off the fp32 exponent
+// field: a normal amax = 1.f * 2^(field - 127); every subnormal (and zero)
+// amax is below 2^-119 and clamps to -127.
+__device__ __forceinline__ int mx_shared_exp(float amax) {
+  const int field = static_cast<int>(__float_as_uint(amax) >> 23);  // amax >= 0
+  const int x = field - 127 - 8;
+  return field == 0 ? -127 : (x < -127 ? -127 : (x > 127 ? 127 : x));
+}
+// 2^-X as an fp32 value, for the X of a finite bf16 or fp32 amax (X <= 119,
+// so 127 - X lies in [8, 254]): multiplying by it is exact, so the element
+// code is e4m3(v / 2^X) as the format defines it.
+__device__ __forceinline__ float mx_inv_scale(int x) { return __uint_as_float(static_cast<uint32_t>(127 - x) << 23); }
+
 // ------------------------------------------------------------------------
 // fp32 exponential for SwiGLU, written from Cody and Waite's method (Software
 // Manual for the Elementary Functions, 1980): x = n ln2 + r, n = rint(x
@@ -442,6 +456,18 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared through L1 (cp.async); with
+// src_bytes 0 nothing is read and the destination is zero-filled.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's committed cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // 3-D tiled store of one box from this CTA's shared memory; completion is
 // tracked by bulk async-groups (commit, then wait).
 __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int x, int y, int z) {
@@ -564,6 +590,33 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// MXFP8 block-scaled MMA: D[tmem] (+)= (A * 2^(sfa - 127)) (B * 2^(sfb - 127))^T,
+// kind::mxf8f6f4 with one E8M0 scale per 32 elements of K (scale_vec::1X),
+// one CTA, K = 32 per instruction.  The scales are read from tensor memory:
+// A's for row m at (lane m, column sfa + m / 32) and B's for column n at
+// (lane 32 q + n % 32, column sfb + n / 32) in every lane quarter q; each
+// 32-bit cell holds four E8M0 bytes, of which the instruction descriptor's
+// a_sf_id / b_sf_id selects one (the K block of this instruction within the
+// cell's four).
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Shared memory -> tensor memory: 32 rows of 16 bytes (an unswizzled K-major
+// matrix, see smem_desc_plain) to 32 lanes x 4 columns, replicated into all
+// four lane quarters.  Asynchronous; ordered with the tcgen05.mma that this
+// thread issues after it.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation this thread issued so far has
 // completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -651,6 +704,23 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
   return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Shared-memory descriptor of an unswizzled K-major matrix whose 16-byte rows
+// lie back to back: 8-row core matrices 128 bytes apart (leading and stride
+// byte offsets both 128), version 1, layout type 0.  Used for the 32 x 16-byte
+// scale-factor atoms that tcgen05.cp copies.
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(128 >> 4) << 16) |
+         (static_cast<uint64_t>(128 >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
+}
+
+// Instruction descriptor for kind::mxf8f6f4 block scaling: b_sf_id in bits
+// [4,6), A and B e4m3 (format 0), both K-major, N >> 3 in [17,23), E8M0
+// scale type (bit 23), M >> 4 in [24,29), a_sf_id in [29,31).
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int m, int n, int a_sf_id, int b_sf_id) {
+  return (static_cast<uint32_t>(b_sf_id) << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(m >> 4) << 24) | (static_cast<uint32_t>(a_sf_id) << 29);
 }
 
 // Instruction descriptor for kind::f16 with bf16 A and B (format 1 in bits

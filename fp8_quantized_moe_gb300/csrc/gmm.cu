@@ -59,7 +59,19 @@ constexpr int kMaxGroups = 1024;
 constexpr int64_t kPairMinK = 3072;  // gmm K from which the plain and SwiGLU gmm run on CTA pairs
 constexpr int kMaxDevices = 256;     // host-side per-device caches
 
-enum Mode { kFinal = 0, kPromote = 1, kTgmm = 2, kSwiglu = 3, kSplit = 4, kPromoteSwiglu = 5, kBf16 = 6, kRouter = 7 };
+enum Mode {
+  kFinal = 0,
+  kPromote = 1,
+  kTgmm = 2,
+  kSwiglu = 3,
+  kSplit = 4,
+  kPromoteSwiglu = 5,
+  kBf16 = 6,
+  kRouter = 7,
+  kMx = 8,         // MXFP8 operands: block-scaled MMAs, bf16 out
+  kMxSwiglu = 9    // MXFP8 wi gmm with the SwiGLU and MXFP8 requantisation epilogue
+};
+constexpr int kMxSfStageBytes = 3 * 512;  // MXFP8: per stage, one A and two B scale-factor atoms (32 x 16 B each)
 constexpr int kSwSlots = 8;  // promotion: ring of per-K-block weight-scale rows in shared memory
 
 struct Params {
@@ -95,6 +107,13 @@ struct Params {
   float* logits;       // [M, rE] fp32
   int32_t* topk_ids;   // [M, rk]
   float* topk_w;       // [M, rk]
+  // MXFP8: E8M0 codes, one per 32 values along K, K-block-major: the four
+  // codes of row r's 128-wide K block kb form the word [kb][r] (lhs [K/128]
+  // [M], rhs [K/128][E_local * N]); kMxSwiglu also writes h's codes
+  // ([F/128][M])
+  const uint8_t* lhs_sf;
+  const uint8_t* rhs_sf;
+  uint8_t* h_sf;
 };
 
 struct SmemCtl {
@@ -102,6 +121,7 @@ struct SmemCtl {
   uint64_t empty[kMaxStages];
   uint64_t tfull[kMaxAcc];
   uint64_t tempty[kMaxAcc];
+  uint64_t sffull[kMaxStages];  // MXFP8: the stage's scale-factor atoms are in shared memory
   uint64_t sfull[kSwSlots];   // promotion: a weight-scale row of the ring has landed
   uint64_t sempty[kSwSlots];  // promotion: a weight-scale row of the ring has been read by every epilogue warp
   uint64_t xbar[4][2];        // promotion + SwiGLU: the two warps of a lane quarter have posted their h maxima
@@ -156,6 +176,11 @@ static_assert(sizeof(SmemCtl) % 16 == 0, "SmemCtl size");
 template <int MODE, bool PAIR_REQ = false>
 struct Cfg {
   static constexpr bool PROMOTE = MODE == kPromote || MODE == kPromoteSwiglu;
+  // MXFP8: block-scaled MMAs whose E8M0 scales are copied into tensor memory
+  // next to a single accumulator
+  static constexpr bool MX = MODE == kMx || MODE == kMxSwiglu;
+  // the control warpgroup hands registers to the epilogue (setmaxnreg)
+  static constexpr bool SPLIT = PROMOTE || MX;
   static constexpr bool PAIR = PAIR_REQ && MOE_GMM_PAIR && (MODE == kFinal || MODE == kSwiglu);
   // bf16 operands (kind::f16): a 128-byte K block is 64 elements
   static constexpr bool BF = MODE == kBf16 || MODE == kRouter;
@@ -163,17 +188,21 @@ struct Cfg {
   static constexpr int BN = 256;  // output columns per tile
   static constexpr int TMEM_COLS = PAIR ? MOE_PAIR_TMEM_COLS : 512;
   static constexpr int SEGS = MODE == kSplit ? 2 : 1;        // accumulators per tile (one per K segment)
-  static constexpr int NACC = TMEM_COLS / (BN * SEGS);       // tiles (promotion: K blocks) in flight in tensor memory
+  // tiles (promotion: K blocks) in flight in tensor memory; MXFP8 keeps one
+  // 256-column accumulator and puts a scale-factor slot per stage after it
+  static constexpr int NACC = MX ? 1 : TMEM_COLS / (BN * SEGS);
+  static constexpr int SF_COL0 = BN;  // MXFP8: tensor-memory column of stage 0's scale slot (16 columns a stage)
   static constexpr int NSTAGE = PAIR ? 6 : (MODE == kTgmm ? MOE_TGMM_NSTAGE : MOE_GMM_NSTAGE);
   static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK;  // this CTA's part of the B tile
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TX_BYTES = (PAIR ? 2 : 1) * STAGE_BYTES;  // what one full barrier waits for
   static constexpr uint32_t IDESC = BF ? idesc_bf16_f32(BM, BN) : idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN);
   static constexpr int EPI_WARPS =
-      PROMOTE ? MOE_PROMOTE_EPI_WARPS : (MODE == kSwiglu ? 8 : (MODE == kTgmm ? MOE_TGMM_EPI_WARPS : 4));
-  // warps before the epilogue: producer, MMA issuer and, for promotion, two
-  // idle warps that complete the control warpgroup of the register split
-  static constexpr int CTRL_WARPS = PROMOTE ? 4 : 2;
+      PROMOTE ? MOE_PROMOTE_EPI_WARPS : ((MODE == kSwiglu || MX) ? 8 : (MODE == kTgmm ? MOE_TGMM_EPI_WARPS : 4));
+  // warps before the epilogue: producer, MMA issuer and, with the register
+  // split, two more that complete the control warpgroup (MXFP8: the first of
+  // them gathers the scale factors; promotion: both idle)
+  static constexpr int CTRL_WARPS = SPLIT ? 4 : 2;
   static constexpr int THREADS = 32 * (CTRL_WARPS + EPI_WARPS);
   // promotion register split: the control warpgroup gives registers to the
   // epilogue warpgroups, whose running sums (256 / (EPI_WARPS / 4) per
@@ -191,8 +220,10 @@ struct Cfg {
   static constexpr size_t CTL_BYTES = (sizeof(SmemCtl) + 1023) / 1024 * 1024;  // keeps the staging 1 KB aligned
   // promotion: kSwSlots rows of BN weight scales, one per K block in flight
   static constexpr int SW_RING_BYTES = PROMOTE ? kSwSlots * BN * 4 : 0;
+  // MXFP8: each stage's scale-factor atoms
+  static constexpr int SF_RING_BYTES = MX ? NSTAGE * kMxSfStageBytes : 0;
   static constexpr size_t SMEM = 1024 + static_cast<size_t>(NSTAGE) * STAGE_BYTES + CTL_BYTES +
-                                 static_cast<size_t>(EPI_WARPS) * STG_WARP_BYTES + SW_RING_BYTES;
+                                 static_cast<size_t>(EPI_WARPS) * STG_WARP_BYTES + SW_RING_BYTES + SF_RING_BYTES;
   static_assert(NSTAGE <= kMaxStages && NACC >= 1 && NACC <= kMaxAcc && NACC * BN * SEGS <= TMEM_COLS &&
                     STAGE_BYTES % 1024 == 0 && BN % 32 == 0,
                 "tile configuration");
@@ -202,9 +233,10 @@ struct Cfg {
   static_assert(!PROMOTE || EPI_WARPS == 8 || EPI_WARPS == 16, "promotion epilogue: 8 or 16 warps");
   // the split must fit in what the CTA is launched with (the host also
   // checks the kernel's actual register count before the launch)
-  static_assert(!PROMOTE || (128 * CTRL_REGS + 32 * EPI_WARPS * EPI_REGS <= LAUNCH_REGS * THREADS &&
-                             EPI_REGS <= 255 && EPI_REGS >= 96),
-                "promotion register split");
+  static_assert(!SPLIT || (128 * CTRL_REGS + 32 * EPI_WARPS * EPI_REGS <= LAUNCH_REGS * THREADS &&
+                           EPI_REGS <= 255 && EPI_REGS >= 96),
+                "register split");
+  static_assert(!MX || (!PAIR && EPI_WARPS == 8 && SF_COL0 + 16 * NSTAGE <= TMEM_COLS), "MXFP8 configuration");
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
@@ -325,7 +357,7 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const SmemCtl* ctl, in
     tl.ax = 0;
     tl.ay = tl.row0;
     tl.bx = 0;
-    if (MODE == kSwiglu || MODE == kPromoteSwiglu) {
+    if (MODE == kSwiglu || MODE == kPromoteSwiglu || MODE == kMxSwiglu) {
       // 128 h columns: wi_0 channels nt*128.. and the matching wi_1 channels
       // (a CTA pair: the even CTA holds the wi_0 rows, the odd one the wi_1 rows)
       tl.by = lo * 2 * p.F + nt * 128 + (PAIR ? rank * p.F : 0);
@@ -392,6 +424,10 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
   uint8_t* stg_base = base_ptr + NSTAGE * STAGE_BYTES + C::CTL_BYTES;  // output staging (kFinal, kTgmm)
   // promotion: ring of per-K-block weight-scale rows (BN floats each)
   float* sw_ring = reinterpret_cast<float*>(stg_base + EPI_WARPS * C::STG_WARP_BYTES);
+  // MXFP8: per stage, the A scale atom (rows 32 c + l of the tile in row l,
+  // 16 bytes: the E8M0 codes of the stage's four K blocks for c = 0..3) and
+  // the two B atoms (tile rows 0..127, 128..255) laid out the same way
+  const uint32_t sf_ring = smem_u32(reinterpret_cast<uint8_t*>(sw_ring) + C::SW_RING_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // A CTA pair works on the same sequence of units; its even CTA (rank 0)
   // issues the MMAs and owns the full and accumulator-empty barriers.
@@ -409,6 +445,8 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
       mbar_init(smem_u32(&ctl->tfull[a]), 1);
       mbar_init(smem_u32(&ctl->tempty[a]), (PAIR ? 2 : 1) * EPI_WARPS);
     }
+    if (C::MX)
+      for (int s = 0; s < NSTAGE; ++s) mbar_init(smem_u32(&ctl->sffull[s]), 32);
     if (C::PROMOTE) {
       for (int q = 0; q < kSwSlots; ++q) {
         mbar_init(smem_u32(&ctl->sfull[q]), 1);
@@ -468,7 +506,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
   // budget is set at the top of its own branch (a budget set before a join
   // would bind the code after it to the smaller one).
   if (warp < C::CTRL_WARPS) {
-  if (C::PROMOTE) setmaxnreg_dec<C::CTRL_REGS>();
+  if (C::SPLIT) setmaxnreg_dec<C::CTRL_REGS>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -505,7 +543,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
             const uint32_t fb = smem_u32(&ctl->full[s]);
             mbar_arrive_expect_tx(fb, C::TX_BYTES);
             tma_load_2d(sa, &tmA, tl.ax + kb * C::KSTEP, tl.ay, fb);
-            if (MODE == kSwiglu || MODE == kPromoteSwiglu) {
+            if (MODE == kSwiglu || MODE == kPromoteSwiglu || MODE == kMxSwiglu) {
               // B rows 0..127: wi_0 channels; rows 128..255: the matching wi_1 channels
               tma_load_2d(sa + A_BYTES, &tmB, tl.bx + kb * C::KSTEP, tl.by, fb);
               tma_load_2d(sa + 2 * A_BYTES, &tmB, tl.bx + kb * C::KSTEP, tl.by + p.F, fb);
@@ -571,7 +609,8 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
           }
           const int s = it % NSTAGE;
           const uint32_t ph = (it / NSTAGE) & 1;
-          if (!CTRL_WAIT(smem_u32(&ctl->full[s]), ph, abort_flag, kWaitLimitNs)) {
+          if (!CTRL_WAIT(smem_u32(&ctl->full[s]), ph, abort_flag, kWaitLimitNs) ||
+              (C::MX && !CTRL_WAIT(smem_u32(&ctl->sffull[s]), ph, abort_flag, kWaitLimitNs))) {
             timed_out = true;
             break;
           }
@@ -584,12 +623,23 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
           const bool seg1 = MODE == kSplit && kb >= p.kb_split;
           const uint32_t d_tmem = tmem_base + a * BN * C::SEGS + (seg1 ? BN : 0);
           const int seg_kb0 = seg1 ? p.kb_split : 0;
+          // MXFP8: the stage's scale atoms into its tensor-memory slot (A: 4
+          // columns, B: 8), ahead of the MMAs that read them
+          const uint32_t sfa_t = tmem_base + C::SF_COL0 + 16 * s, sfb_t = sfa_t + 4;
+          if (C::MX) {
+            const uint32_t sf_sm = sf_ring + s * kMxSfStageBytes;
+            tmem_cp_32x128b_warpx4(sfa_t, smem_desc_plain(sf_sm));
+            tmem_cp_32x128b_warpx4(sfb_t, smem_desc_plain(sf_sm + 512));
+            tmem_cp_32x128b_warpx4(sfb_t + 4, smem_desc_plain(sf_sm + 1024));
+          }
 #pragma unroll
           for (int k4 = 0; k4 < BK / UMMA_K; ++k4) {
             const uint32_t accumulate = C::PROMOTE ? (k4 > 0) : (kb > seg_kb0 || k4 > 0);
             // +32 bytes along K inside the 128-byte swizzled row = +2 in the
             // descriptor's address field (16-byte units)
-            if (C::BF)
+            if (C::MX)  // K block k4 of the stage: byte k4 of every scale cell
+              mma_mx(d_tmem, da + 2 * k4, db + 2 * k4, idesc_mx_e4m3(BM, BN, k4, k4), sfa_t, sfb_t, accumulate);
+            else if (C::BF)
               mma_bf16(d_tmem, da + 2 * k4, db + 2 * k4, IDESC, accumulate);
             else if (PAIR)
               mma_f8_pair(d_tmem, da + 2 * k4, db + 2 * k4, IDESC, accumulate);
@@ -627,9 +677,72 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
       }
     }
     __syncwarp();
+  } else if (C::MX && warp == 2) {
+    // ------------------------------------------------ MXFP8 scale gatherer
+    // Each stage's E8M0 codes go into the stage's atoms by 4-byte cp.async
+    // copies (lane l: tile rows 32 c + l): 4 A rows and 8 B rows a lane, the
+    // word of a row holding the stage's four K blocks.  The codes are
+    // K-block-major, so the words of a tile's rows for one stage are
+    // adjacent and every copy instruction of the warp reads one 128-byte
+    // line.  A stage is announced
+    // (32 arrivals on sffull) LAG stages later, once its copies have landed
+    // and been made visible to the tensor core's (async-proxy) reads, so
+    // that the lane keeps LAG stages of copies in flight.  The stage's buffer
+    // is free once the MMAs of its previous use completed (empty barrier).
+    constexpr uint32_t LAG = 2;
+    static_assert(!C::MX || LAG < NSTAGE, "the gatherer may run at most NSTAGE - 1 stages ahead of its announcements");
+    uint32_t it = 0;
+    const uint32_t* lsf = reinterpret_cast<const uint32_t*>(p.lhs_sf);
+    const uint32_t* rsf = reinterpret_cast<const uint32_t*>(p.rhs_sf);
+    const int64_t brows = static_cast<int64_t>(p.El) * p.N;  // rows of the rhs (N = 2F for kMxSwiglu)
+    for (int t = unit0; t < total && !timed_out; t += units) {
+      const Tile tl = get_tile<MODE, PAIR>(p, ctl, t, rank);
+      for (int kb = 0; kb < tl.nkb; ++kb) {
+        const int s = it % NSTAGE;
+        if (!CTRL_WAIT(smem_u32(&ctl->empty[s]), ((it / NSTAGE) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        const uint32_t dst = sf_ring + s * kMxSfStageBytes + lane * 16;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // rows past M (end of the last group) read as zeros
+          const int64_t row = static_cast<int64_t>(tl.row0) + 32 * c + lane;
+          const bool ok = row < p.M;
+          cp_async_4(dst + 4 * c, ok ? lsf + kb * p.M + row : lsf, ok ? 4u : 0u);
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int nl = 32 * c + lane;  // B row of the tile
+          int64_t wrow;
+          bool ok = true;
+          if (MODE == kMxSwiglu) {  // rows 0..127: wi_0 channels; 128..255: the matching wi_1 channels
+            wrow = static_cast<int64_t>(tl.el) * 2 * p.F + (nl < 128 ? tl.n0 + nl : p.F + tl.n0 + nl - 128);
+          } else {  // channels past N (a narrower last N tile) read as zeros
+            ok = tl.n0 + nl < p.N;
+            wrow = static_cast<int64_t>(tl.el) * p.N + tl.n0 + nl;
+          }
+          cp_async_4(dst + 512 * (1 + (c >> 2)) + 4 * (c & 3), ok ? rsf + kb * brows + wrow : rsf, ok ? 4u : 0u);
+        }
+        cp_async_commit();
+        if (it >= LAG) {
+          cp_async_wait<LAG>();
+          fence_proxy_async_smem();
+          mbar_arrive(smem_u32(&ctl->sffull[(it - LAG) % NSTAGE]));
+        }
+        ++it;
+      }
+    }
+    // the last LAG stages (and, after a timeout, every copy in flight)
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (uint32_t j = it > LAG ? it - LAG : 0; j < it; ++j) mbar_arrive(smem_u32(&ctl->sffull[j % NSTAGE]));
+    if (timed_out) {
+      *abort_flag = 1;
+      ctl->err = 2;
+    }
   }
   } else {
-    if (C::PROMOTE) setmaxnreg_inc<C::EPI_REGS>();
+    if (C::SPLIT) setmaxnreg_inc<C::EPI_REGS>();
     // ------------------------------------------------------------ epilogue
     const int q4 = warp & 3;                            // TMEM lane quarter of this warp
     const int half = (warp - C::CTRL_WARPS) >> 2;  // column part of the warp (0 with 4 epilogue warps)
@@ -949,6 +1062,108 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         __syncwarp();
         if (lane == 0) release_acc(a);
         ++acc;
+      } else if (MODE == kMx) {
+        // MXFP8: the scales were applied by the MMAs, so out = bf16(acc).
+        // With one accumulator, the tile (8 warps: lane quarter q4, columns
+        // [128 half, 128 half + 128)) is read into registers and released
+        // before any store, so the next tile's MMAs run under the stores.
+        uint16_t* out = static_cast<uint16_t*>(p.out);
+        const int64_t row = static_cast<int64_t>(tl.row0) + r;
+        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[0]), acc & 1, abort_flag, kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+        uint32_t v[4][32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tmem_ld_32x32b_x32(tmem_base + lane_addr + half * 128 + 32 * i, v[i]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) release_acc(0);
+        ++acc;
+        if (row_ok) {
+          uint16_t* orow = out + row * p.N;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              const int c = tl.n0 + half * 128 + 32 * i + 8 * g;
+              const uint32_t* w = v[i] + 8 * g;
+              if (c < p.N)  // N is a multiple of 16
+                *reinterpret_cast<uint4*>(orow + c) =
+                    make_uint4(pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                               pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                               pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                               pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7])));
+            }
+        }
+      } else if (MODE == kMxSwiglu) {
+        // MXFP8 wi gmm + SwiGLU + MXFP8 requantisation.  The accumulator
+        // holds a0 (columns 0..127) and a1 (128..255) of 128 h columns; warp
+        // part `half` takes h columns [64 half, 64 half + 64) of the tile,
+        // i.e. two 32-column MX blocks, both inside this thread's row, so a
+        // block's amax needs no exchange.  a0, a1 are rounded to bf16 as
+        // gmm_fp8_mx stores them, h = bf16(silu(a0) a1), then per block
+        // X = floor(log2 amax) - 8 and codes e4m3(h / 2^X).
+        const int64_t row = static_cast<int64_t>(tl.row0) + r;
+        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[0]), acc & 1, abort_flag, kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+        uint32_t v0[2][32], v1[2][32];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          tmem_ld_32x32b_x32(tmem_base + lane_addr + half * 64 + 32 * i, v0[i]);
+          tmem_ld_32x32b_x32(tmem_base + lane_addr + 128 + half * 64 + 32 * i, v1[i]);
+        }
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) release_acc(0);
+        ++acc;
+        if (row_ok) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int hc = tl.n0 + half * 64 + 32 * i;  // first h column of the block
+            float f0[32], f1[32], h[32];
+            uint32_t a0b[16], a1b[16], hb[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              a0b[j / 2] = pack_bf16x2(__uint_as_float(v0[i][j]), __uint_as_float(v0[i][j + 1]));
+              a1b[j / 2] = pack_bf16x2(__uint_as_float(v1[i][j]), __uint_as_float(v1[i][j + 1]));
+              f0[j] = bf16lo(a0b[j / 2]);
+              f0[j + 1] = bf16hi(a0b[j / 2]);
+              f1[j] = bf16lo(a1b[j / 2]);
+              f1[j + 1] = bf16hi(a1b[j / 2]);
+            }
+            swiglu_h_x2<32>(f0, f1, h, hb);
+            float amax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(h[j]));
+            const int X = mx_shared_exp(amax);
+            const float inv = mx_inv_scale(X);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) h[j] = __fmul_rn(h[j], inv);  // exact: a power of two
+            uint4* dq = reinterpret_cast<uint4*>(p.h_q + row * p.F + hc);
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+              const uint2 lo8 = pack_e4m3x8(h + 16 * g), hi8 = pack_e4m3x8(h + 16 * g + 8);
+              dq[g] = make_uint4(lo8.x, lo8.y, hi8.x, hi8.y);
+            }
+            p.h_sf[((hc >> 7) * p.M + row) * 4 + ((hc >> 5) & 3)] = static_cast<uint8_t>(X + 127);
+            if (p.a_out) {
+              uint4* d0 = reinterpret_cast<uint4*>(p.a_out + row * 2 * p.F + hc);
+              uint4* d1 = reinterpret_cast<uint4*>(p.a_out + row * 2 * p.F + p.F + hc);
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                d0[g] = make_uint4(a0b[4 * g], a0b[4 * g + 1], a0b[4 * g + 2], a0b[4 * g + 3]);
+                d1[g] = make_uint4(a1b[4 * g], a1b[4 * g + 1], a1b[4 * g + 2], a1b[4 * g + 3]);
+              }
+            }
+          }
+        }
       } else if (MODE == kBf16) {
         // plain bf16 contraction without scales: bf16 rows staged through
         // shared memory as in the fp8 gmm, or fp32 rows written directly
@@ -1645,7 +1860,7 @@ __global__ void __launch_bounds__(256) quant_transpose_pad_kernel(const uint16_t
 // scale 1, as the unfused path gives for its zero rows.  In the per-row mode
 // their running maximum is set to -1 so that the code pass skips them and
 // writes scale 1.
-__global__ void swiglu_outside_kernel(uint8_t* h_q, float* h_scale, int64_t M, int64_t F, int h_mode,
+__global__ void swiglu_outside_kernel(uint8_t* h_q, float* h_scale, uint8_t* h_sf, int64_t M, int64_t F, int h_mode,
                                       const int32_t* sizes, int E, int g0, int El) {
   __shared__ int starts[kMaxGroups + 1];
   group_starts_smem(sizes, E, starts);
@@ -1662,6 +1877,8 @@ __global__ void swiglu_outside_kernel(uint8_t* h_q, float* h_scale, int64_t M, i
       h_scale[row] = -1.0f;
     } else if (h_mode == MOE_SCALE_PER_ROW_BLOCK128) {
       for (int64_t b = 0; b < nb; ++b) h_scale[row * nb + b] = 1.0f;
+    } else if (h_sf) {  // MXFP8 (K-block-major words): a zero block's E8M0 code is 0
+      for (int64_t b = 0; b < F / 128; ++b) reinterpret_cast<uint32_t*>(h_sf)[b * M + row] = 0;
     }
   }
 }
@@ -1812,7 +2029,7 @@ moe_status launch_mma(const CUtensorMap& A, const CUtensorMap& B, const CUtensor
   auto kernel = mma_kernel<MODE, PAIR_REQ>;
   MOE_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(C::SMEM)));
-  if (C::PROMOTE) {
+  if (C::SPLIT) {
     // the register split may only hand out what the CTA is launched with
     cudaFuncAttributes fa{};
     MOE_CUDA_TRY(cudaFuncGetAttributes(&fa, kernel));
@@ -2020,8 +2237,8 @@ extern "C" moe_status gmm_fp8_swiglu(const uint8_t* lhs_q, const float* lhs_scal
   if (M == 0) return MOE_OK;
   if (h_mode == MOE_SCALE_PER_ROW) MOE_CUDA_TRY(cudaMemsetAsync(h_scale, 0, sizeof(float) * M, st));
   if (group_offset > 0 || E_local < E) {
-    swiglu_outside_kernel<<<sm_count() * 4, 256, 0, st>>>(h_q, h_scale, M, F, h_mode, group_sizes, E, group_offset,
-                                                            E_local);
+    swiglu_outside_kernel<<<sm_count() * 4, 256, 0, st>>>(h_q, h_scale, nullptr, M, F, h_mode, group_sizes, E,
+                                                            group_offset, E_local);
     MOE_CUDA_TRY(cudaGetLastError());
   }
   CUtensorMap A, B;
@@ -2062,6 +2279,90 @@ extern "C" moe_status gmm_fp8_swiglu(const uint8_t* lhs_q, const float* lhs_scal
     MOE_CUDA_TRY(cudaGetLastError());
   }
   return MOE_OK;
+}
+
+extern "C" moe_status gmm_fp8_mx(const uint8_t* lhs_q, const uint8_t* lhs_sf, const uint8_t* rhs_q,
+                                 const uint8_t* rhs_sf, const int32_t* group_sizes, int E, int group_offset,
+                                 int E_local, int64_t M, int64_t K, int64_t N, uint16_t* out, moe_stream_t stream) {
+  MOE_HOST_CHECK(lhs_q && lhs_sf && rhs_q && rhs_sf && group_sizes && out, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(E > 0 && E <= kMaxGroups && group_offset >= 0 && E_local > 0 && group_offset + E_local <= E,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(M >= 0 && M < (1ll << 31) && K > 0 && K % 128 == 0 && K < (1 << 30) && N > 0 && N % 16 == 0,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(static_cast<int64_t>(E_local) * N < (1ll << 31), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(aligned16(lhs_q) && aligned16(rhs_q) && aligned16(out) && aligned16(lhs_sf) && aligned16(rhs_sf),
+                 MOE_ERR_INVALID_ARG);
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = as_stream(stream);
+  if (M == 0) return MOE_OK;
+  if (group_offset > 0 || E_local < E) {
+    zero_outside_kernel<<<sm_count() * 4, 256, 0, st>>>(out, M, N, group_sizes, E, group_offset, E_local);
+    MOE_CUDA_TRY(cudaGetLastError());
+  }
+  CUtensorMap A, B;
+  if (!make_map(&A, lhs_q, K, M, K, BM)) return MOE_ERR_CUDA;
+  if (!make_map(&B, rhs_q, K, static_cast<uint64_t>(E_local) * N, K, Cfg<kMx>::BN)) return MOE_ERR_CUDA;
+  Params p{};
+  p.group_sizes = group_sizes;
+  p.E = E;
+  p.g0 = group_offset;
+  p.El = E_local;
+  p.M = M;
+  p.K = static_cast<int>(K);
+  p.N = static_cast<int>(N);
+  p.kblocks = static_cast<int>(K / BK);
+  p.ntiles = static_cast<int>((N + Cfg<kMx>::BN - 1) / Cfg<kMx>::BN);
+  p.lhs_sf = lhs_sf;
+  p.rhs_sf = rhs_sf;
+  p.out = out;
+  p.stall_ns = g_stall_ns.load();
+  p.stall = p.stall_ns != 0;
+  return launch_mma<kMx, false>(A, B, A, p, gmm_max_units<kMx, false>(M, E_local, p.ntiles), st);
+}
+
+extern "C" moe_status gmm_fp8_mx_swiglu(const uint8_t* lhs_q, const uint8_t* lhs_sf, const uint8_t* rhs_q,
+                                        const uint8_t* rhs_sf, const int32_t* group_sizes, int E, int group_offset,
+                                        int E_local, int64_t M, int64_t K, int64_t F, uint16_t* a_out, uint8_t* h_q,
+                                        uint8_t* h_sf, moe_stream_t stream) {
+  MOE_HOST_CHECK(lhs_q && lhs_sf && rhs_q && rhs_sf && group_sizes && h_q && h_sf, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(E > 0 && E <= kMaxGroups && group_offset >= 0 && E_local > 0 && group_offset + E_local <= E,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(M >= 0 && M < (1ll << 31) && K > 0 && K % 128 == 0 && K < (1 << 30) && F > 0 && F % 128 == 0 &&
+                     2 * static_cast<int64_t>(E_local) * F < (1ll << 31),
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(aligned16(lhs_q) && aligned16(rhs_q) && aligned16(h_q) && aligned16(lhs_sf) && aligned16(rhs_sf) &&
+                     (!a_out || aligned16(a_out)),
+                 MOE_ERR_INVALID_ARG);
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = as_stream(stream);
+  if (M == 0) return MOE_OK;
+  if (group_offset > 0 || E_local < E) {
+    swiglu_outside_kernel<<<sm_count() * 4, 256, 0, st>>>(h_q, nullptr, h_sf, M, F, -1, group_sizes, E, group_offset,
+                                                            E_local);
+    MOE_CUDA_TRY(cudaGetLastError());
+  }
+  CUtensorMap A, B;
+  if (!make_map(&A, lhs_q, K, M, K, BM)) return MOE_ERR_CUDA;
+  if (!make_map(&B, rhs_q, K, static_cast<uint64_t>(E_local) * 2 * F, K, 128)) return MOE_ERR_CUDA;
+  Params p{};
+  p.group_sizes = group_sizes;
+  p.E = E;
+  p.g0 = group_offset;
+  p.El = E_local;
+  p.M = M;
+  p.K = static_cast<int>(K);
+  p.N = static_cast<int>(2 * F);
+  p.kblocks = static_cast<int>(K / BK);
+  p.ntiles = static_cast<int>(F / 128);
+  p.lhs_sf = lhs_sf;
+  p.rhs_sf = rhs_sf;
+  p.F = static_cast<int>(F);
+  p.a_out = a_out;
+  p.h_q = h_q;
+  p.h_sf = h_sf;
+  p.stall_ns = g_stall_ns.load();
+  p.stall = p.stall_ns != 0;
+  return launch_mma<kMxSwiglu, false>(A, B, A, p, gmm_max_units<kMxSwiglu, false>(M, E_local, p.ntiles), st);
 }
 
 namespace {

@@ -23,6 +23,9 @@ namespace {
 __device__ unsigned int g_err;
 
 constexpr int kThreads = 256;
+// Row-kernel mode of the MXFP8 variant (beside the moe_scale_mode values):
+// one E8M0 code per row and per 32 columns
+constexpr int kModeMx32 = 4;
 
 __device__ __forceinline__ uint4 ldg16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
 
@@ -49,11 +52,16 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// Where the scale of (row, 128-column block b) goes.
+// Where the scale of (row, 128-column block b) goes; MXFP8: the E8M0 code of
+// (row, 32-column block b) goes to sf[((b / 4) * nrows + row) * 4 + b % 4]
+// (K-block-major: the four codes of a row's 128-column block are one word,
+// and the words of consecutive rows are adjacent).
 struct ScaleOut {
   float* scale;
   int64_t group_n;  // > 0: weights [E, KB, N] with row = e * N + n; 0: [rows, KB]
   int kb;
+  uint8_t* sf;
+  int64_t nrows;
   __device__ __forceinline__ int64_t blk(int64_t row, int b) const {
     if (group_n > 0) {
       const int64_t e = row / group_n, n = row - e * group_n;
@@ -222,7 +230,9 @@ struct SwigluBwdOp {  // dA0 = (dH a1) silu'(a0), dA1 = dH silu(a0); also stores
 };
 
 // ---- the row kernel ------------------------------------------------------
-// MODE: MOE_SCALE_PER_ROW, MOE_SCALE_PER_ROW_BLOCK128 or MOE_SCALE_PER_TENSOR.
+// MODE: MOE_SCALE_PER_ROW, MOE_SCALE_PER_ROW_BLOCK128, MOE_SCALE_PER_TENSOR
+// or kModeMx32 (MXFP8, OCP MX v1.0: per 32-column block the shared exponent
+// X = floor(log2(amax)) - 8 and codes e4m3(x / 2^X), the division exact).
 // MAXI: units per thread (ceil(nunits / blockDim.x) <= MAXI).
 template <int MODE, int MAXI, class Op>
 __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, int64_t qcols,
@@ -230,6 +240,8 @@ __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, i
   constexpr int U = Op::U;
   static_assert(!Op::kWide || U % 2 == 0, "a wide unit is pairs of adjacent 8-column vectors");
   constexpr int kBlockLanes = Op::kWide ? 8 : 16;  // units per 128-column block
+  constexpr int kMxLanes = Op::kWide ? 2 : 4;      // units per 32-column block
+  static_assert(MODE != kModeMx32 || Op::kWide, "MXFP8 rows use 16-column units");
   const int64_t row = blockIdx.x;
   const int tid = threadIdx.x;
   uint32_t pk[MAXI][U][4];
@@ -275,10 +287,33 @@ __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, i
   const float inv_row = __frcp_rn(s_row);
   uint2 codes[MAXI][U];
   float s_blk[MAXI];
+  uint8_t e8m0[MAXI];
 #pragma unroll
   for (int i = 0; i < MAXI; ++i) {
     const int u = i * blockDim.x + tid;
     float s = s_row, inv = inv_row;
+    if (MODE == kModeMx32) {
+      // the units of one 32-column block sit on consecutive lanes
+      float m = amax_i[i];
+#pragma unroll
+      for (int o = kMxLanes / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      const int X = mx_shared_exp(m);
+      e8m0[i] = static_cast<uint8_t>(X + 127);
+      inv = mx_inv_scale(X);
+      if (u < nunits) {
+#pragma unroll
+        for (int uu = 0; uu < U; ++uu) {
+          float v[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            v[2 * j] = __fmul_rn(bf16lo(pk[i][uu][j]), inv);  // exact: a power of two
+            v[2 * j + 1] = __fmul_rn(bf16hi(pk[i][uu][j]), inv);
+          }
+          codes[i][uu] = pack_e4m3x8(v);
+        }
+      }
+      continue;
+    }
     if (MODE == MOE_SCALE_PER_ROW_BLOCK128) {
       // the units of one 128-column block (16 of 8 columns, or 8 of 16) sit
       // on consecutive lanes
@@ -313,6 +348,10 @@ __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, i
       if (u < nunits) {
         if (MODE == MOE_SCALE_PER_ROW_BLOCK128 && (u & (kBlockLanes - 1)) == 0)
           so.scale[so.blk(drow, u / kBlockLanes)] = s_blk[i];
+        if (MODE == kModeMx32 && (u & (kMxLanes - 1)) == 0) {
+          const int b = u / kMxLanes;  // 32-column block
+          so.sf[((b >> 2) * so.nrows + drow) * 4 + (b & 3)] = e8m0[i];
+        }
         if (Op::kWide) {  // each pair of vectors: 16 adjacent columns, one 16-byte store
 #pragma unroll
           for (int uu = 0; uu < U; uu += 2)
@@ -359,6 +398,14 @@ moe_status launch_rows(const Op& op, int64_t rows, int nunits, int64_t qcols, mo
   else
     e = launch_rows_m<MOE_SCALE_PER_TENSOR>(op, rows, nunits, qcols, ss, q, so, st);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+template <class Op>
+moe_status launch_rows_mx(const Op& op, int64_t rows, int nunits, int64_t qcols, uint8_t* q, ScaleOut so,
+                          cudaStream_t st) {
+  if (rows == 0) return MOE_OK;
+  return launch_rows_m<kModeMx32>(op, rows, nunits, qcols, nullptr, q, so, st) == cudaSuccess ? MOE_OK
+                                                                                            : MOE_ERR_CUDA;
 }
 
 constexpr int64_t kMaxCols = 16 * kThreads * 8;  // 32768 values per quantised row
@@ -524,8 +571,36 @@ extern "C" __attribute__((visibility("hidden"))) moe_status moe_detail_quantize_
   moe_status stt = check_mode_ptrs(mode, static_scale, xs_scale);
   if (stt != MOE_OK) return stt;
   RowsGatherOp op{x, D, pos, k, T * k};
-  ScaleOut so{xs_scale, 0, static_cast<int>((D + 127) / 128)};
+  ScaleOut so{xs_scale, 0, static_cast<int>((D + 127) / 128), nullptr, 0};
   return launch_rows(op, T, static_cast<int>(D / 16), D, mode, static_scale, xs_q, so, st);
+}
+
+// MXFP8 form of the fused step 1 + gather (moe_quantize_sort_mx).
+extern "C" __attribute__((visibility("hidden"))) moe_status moe_detail_quantize_gather_mx(
+    const uint16_t* x, const int32_t* pos, int64_t T, int k, int64_t D, uint8_t* xs_q, uint8_t* xs_sf,
+    cudaStream_t st) {
+  MOE_HOST_CHECK(D % 128 == 0 && D <= kMaxCols, MOE_ERR_INVALID_ARG);
+  RowsGatherOp op{x, D, pos, k, T * k};
+  ScaleOut so{nullptr, 0, 0, xs_sf, T * k};
+  return launch_rows_mx(op, T, static_cast<int>(D / 16), D, xs_q, so, st);
+}
+
+extern "C" moe_status moe_quantize_rows_mx(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sf,
+                                           moe_stream_t stream) {
+  MOE_HOST_CHECK(x && q && sf && rows >= 0 && cols > 0 && cols % 128 == 0 && cols <= kMaxCols, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(rows < (1ll << 31) && aligned16(x) && aligned16(q), MOE_ERR_INVALID_ARG);
+  RowsOp op{x, cols};
+  ScaleOut so{nullptr, 0, 0, sf, rows};
+  return launch_rows_mx(op, rows, static_cast<int>(cols / 16), cols, q, so, as_stream(stream));
+}
+
+extern "C" moe_status moe_swiglu_quant_mx(const uint16_t* a, int64_t R, int64_t F, uint8_t* h_q, uint8_t* h_sf,
+                                          moe_stream_t stream) {
+  MOE_HOST_CHECK(a && h_q && h_sf && R >= 0 && F > 0 && F % 128 == 0 && F <= kMaxCols, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(R < (1ll << 31) && aligned16(a) && aligned16(h_q), MOE_ERR_INVALID_ARG);
+  SwigluOpT<true> op{a, F};
+  ScaleOut so{nullptr, 0, 0, h_sf, R};
+  return launch_rows_mx(op, R, static_cast<int>(F / 16), F, h_q, so, as_stream(stream));
 }
 
 extern "C" moe_status moe_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, moe_scale_mode mode,
@@ -535,7 +610,7 @@ extern "C" moe_status moe_quantize_rows(const uint16_t* x, int64_t rows, int64_t
   moe_status st = check_mode_ptrs(mode, static_scale, scale);
   if (st != MOE_OK) return st;
   RowsOp op{x, cols};
-  ScaleOut so{scale, 0, static_cast<int>((cols + 127) / 128)};
+  ScaleOut so{scale, 0, static_cast<int>((cols + 127) / 128), nullptr, 0};
   return launch_rows(op, rows, static_cast<int>(cols / 16), cols, mode, static_scale, q, so, as_stream(stream));
 }
 
@@ -548,7 +623,7 @@ extern "C" moe_status moe_quantize_weights(const uint16_t* w, int64_t E, int64_t
   moe_status st = check_mode_ptrs(mode, static_scale, scale);
   if (st != MOE_OK) return st;
   RowsOp op{w, K};
-  ScaleOut so{scale, N, static_cast<int>(K / 128)};
+  ScaleOut so{scale, N, static_cast<int>(K / 128), nullptr, 0};
   return launch_rows(op, E * N, static_cast<int>(K / 16), K, mode, static_scale, q, so, as_stream(stream));
 }
 
@@ -559,7 +634,7 @@ extern "C" moe_status moe_swiglu_quant(const uint16_t* a, int64_t R, int64_t F, 
   MOE_HOST_CHECK(R < (1ll << 31) && aligned16(a) && aligned16(h_q), MOE_ERR_INVALID_ARG);
   moe_status st = check_mode_ptrs(mode, static_scale, h_scale);
   if (st != MOE_OK) return st;
-  ScaleOut so{h_scale, 0, static_cast<int>((F + 127) / 128)};
+  ScaleOut so{h_scale, 0, static_cast<int>((F + 127) / 128), nullptr, 0};
   if (mode == MOE_SCALE_PER_ROW) {
     SwigluOpT<false> op{a, F};
     return launch_rows(op, R, static_cast<int>(F / 8), F, mode, static_scale, h_q, so, as_stream(stream));
@@ -575,7 +650,7 @@ extern "C" moe_status moe_gather_scale_quant(const uint16_t* G, const float* w, 
   MOE_HOST_CHECK(D % 16 == 0 && D <= kMaxCols && T <= ((1ll << 31) - 1) / k, MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(aligned16(G) && aligned16(dO) && aligned16(dO_q) && aligned16(dO_scale), MOE_ERR_INVALID_ARG);
   GatherScaleOp op{G, w, sorted_src, T * k, k, D, dO};
-  ScaleOut so{dO_scale, 0, 0};
+  ScaleOut so{dO_scale, 0, 0, nullptr, 0};
   return launch_rows(op, T * k, static_cast<int>(D / 16), D, MOE_SCALE_PER_ROW, nullptr, dO_q, so,
                      as_stream(stream));
 }
@@ -587,7 +662,7 @@ extern "C" moe_status moe_swiglu_bwd_quant(const uint16_t* dH, const uint16_t* a
   MOE_HOST_CHECK(aligned16(dH) && aligned16(a) && aligned16(dA) && aligned16(dA_q) && aligned16(dA_scale),
                  MOE_ERR_INVALID_ARG);
   SwigluBwdOp op{dH, a, F, dA};
-  ScaleOut so{dA_scale, 0, 0};
+  ScaleOut so{dA_scale, 0, 0, nullptr, 0};
   return launch_rows(op, R, static_cast<int>(F / 8), 2 * F, MOE_SCALE_PER_ROW, nullptr, dA_q, so,
                      as_stream(stream));
 }

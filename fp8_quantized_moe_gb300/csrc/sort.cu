@@ -308,6 +308,30 @@ extern "C" moe_status moe_quantize_sort(const uint16_t* x, const int32_t* topk_i
   return moe_detail_quantize_gather(x, pos, T, k, D, mode, static_scale, xs_q, xs_scale, st);
 }
 
+extern "C" __attribute__((visibility("hidden"))) moe_status moe_detail_quantize_gather_mx(
+    const uint16_t* x, const int32_t* pos, int64_t T, int k, int64_t D, uint8_t* xs_q, uint8_t* xs_sf,
+    cudaStream_t st);
+
+// MXFP8 form of moe_quantize_sort: the codes and the E8M0 codes of each token
+// row go to its k sorted rows.
+extern "C" moe_status moe_quantize_sort_mx(const uint16_t* x, const int32_t* topk_ids, int64_t T, int k, int E,
+                                           int64_t D, int32_t* sorted_src, int32_t* pos, int32_t* group_sizes,
+                                           int32_t* group_offsets, uint8_t* xs_q, uint8_t* xs_sf, void* workspace,
+                                           size_t workspace_bytes, moe_stream_t stream) {
+  MOE_HOST_CHECK(x && topk_ids && sorted_src && pos && group_sizes && group_offsets && xs_q && xs_sf && workspace,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(T >= 0 && k > 0 && k <= 32 && E > 0 && E <= kMaxE && D > 0 && D % 128 == 0, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(pairs_fit(T, k), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(aligned16(x) && aligned16(xs_q) && (reinterpret_cast<uintptr_t>(workspace) & 3) == 0,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(workspace_bytes >= moe_ragged_sort_workspace_bytes(T, k, E), MOE_ERR_INVALID_ARG);
+  cudaStream_t st = as_stream(stream);
+  moe_status stt = sort_indices(topk_ids, T, k, E, sorted_src, pos, group_sizes, group_offsets,
+                                static_cast<int*>(workspace), st);
+  if (stt != MOE_OK || T * k == 0) return stt;
+  return moe_detail_quantize_gather_mx(x, pos, T, k, D, xs_q, xs_sf, st);
+}
+
 // ---------------------------------------------------------------------------
 // moe_ragged_sort_noalloc: the same sort for callers that cannot allocate
 // device memory.  Its scratch (the per-(chunk, expert) counts) lives in a

@@ -400,6 +400,74 @@ moe_status moe_router_backward(const uint16_t* G, const uint16_t* o, const int32
  * transposed weights.  R % 16 == 0, C % 16 == 0. */
 moe_status moe_transpose_u8(const uint8_t* src, int64_t B, int64_t R, int64_t C, uint8_t* dst, moe_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * MXFP8 variant of steps 1-5.  It is not a method of the three pages: it is
+ * the same path on Blackwell's block-scaled tensor-core format, as defined by
+ * the OCP "Microscaling Formats (MX) Specification" v1.0 (MXFP8, E4M3
+ * elements).
+ *
+ * Every 32 consecutive values of a row along the contracted dimension form a
+ * block.  A block shares one E8M0 scale 2^X, stored as the byte X + 127:
+ *   X = floor(log2(amax)) - 8   clamped to [-127, 127]; X = -127 when amax = 0
+ *   q = e4m3(x / 2^X)           round to nearest even, saturating at 448.
+ *   (8 is the exponent of 256, the largest power of two in e4m3.)
+ * E8M0 tensors are K-block-major: uint8_t [cols/128][rows][4].  The code of
+ * (row, 32-column block b) is at ((b / 4) * rows + row) * 4 + b % 4.  So the
+ * four codes of a row's 128-column block form one 32-bit word, and for one
+ * 128-column block the words of consecutive rows are adjacent: a tile of rows
+ * reads its codes for one K step as one contiguous run.  cols is a multiple of
+ * 128.
+ *
+ * The grouped matmuls run tcgen05.mma.kind::mxf8f6f4.block_scale.  The
+ * tensor core applies both operands' scales to each 32-wide K block, so
+ * accumulation stays in fp32 tensor memory across the whole K loop.
+ * ------------------------------------------------------------------------ */
+
+/* Step 1 (MX).  x bf16 [rows, cols] -> q e4m3 [rows, cols], sf E8M0
+ * [cols/128][rows][4].  Expert weights w[E, N, K] are passed as rows = E*N,
+ * cols = K: their codes are [K/128][E*N][4].  cols % 128 == 0,
+ * cols <= 32768, rows < 2^31; x and q 16-byte aligned. */
+moe_status moe_quantize_rows_mx(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sf,
+                                moe_stream_t stream);
+
+/* Steps 1 + 2 (MX), as moe_quantize_sort: the sort indices, and each token
+ * row quantised once with its codes and E8M0 codes written to its k sorted
+ * rows.  xs_q [T*k, D], xs_sf [D/128][T*k][4]; workspace as moe_ragged_sort.
+ * D % 128 == 0, D <= 32768. */
+moe_status moe_quantize_sort_mx(const uint16_t* x, const int32_t* topk_ids, int64_t T, int k, int E, int64_t D,
+                                int32_t* sorted_src, int32_t* pos, int32_t* group_sizes, int32_t* group_offsets,
+                                uint8_t* xs_q, uint8_t* xs_sf, void* workspace, size_t workspace_bytes,
+                                moe_stream_t stream);
+
+/* Steps 3 / 5 (MX).  out[m, n] = bf16( sum_k deq(lhs)[m, k] deq(rhs)[g(m), n, k] )
+ * with deq(x)[.., k] = e4m3(x[.., k]) * 2^(sf[.., k/32] - 127).
+ *   lhs_q [M, K], lhs_sf [K/128][M][4]; rhs_q [E_local, N, K], rhs_sf
+ *   [K/128][E_local * N][4] (row e * N + n); out bf16 [M, N].
+ * Groups, group_offset and E_local are as in gmm_fp8: rows outside the
+ * local groups are zero.  K % 128 == 0, N % 16 == 0.  Every pointer is
+ * 16-byte aligned. */
+moe_status gmm_fp8_mx(const uint8_t* lhs_q, const uint8_t* lhs_sf, const uint8_t* rhs_q, const uint8_t* rhs_sf,
+                      const int32_t* group_sizes, int E, int group_offset, int E_local, int64_t M, int64_t K,
+                      int64_t N, uint16_t* out, moe_stream_t stream);
+
+/* Steps 3 + 4 (MX) in one kernel.  rhs_q [E_local, 2F, K] holds the wi_0
+ * rows and then the wi_1 rows of each expert, rhs_sf [K/128][E_local*2F][4].
+ * The epilogue:
+ *   - rounds a0 and a1 to bf16 as gmm_fp8_mx would store them;
+ *   - forms h = bf16(silu(a0) * a1) (the h of moe_swiglu_quant);
+ *   - quantises h per 32 columns into h_q [M, F] and h_sf [F/128][M][4].
+ * a_out (optional, may be NULL) receives the bf16 [a0 | a1] [M, 2F].
+ * Rows outside the local groups get zero codes and E8M0 code 0.
+ * K % 128 == 0, F % 128 == 0; every pointer 16-byte aligned. */
+moe_status gmm_fp8_mx_swiglu(const uint8_t* lhs_q, const uint8_t* lhs_sf, const uint8_t* rhs_q, const uint8_t* rhs_sf,
+                             const int32_t* group_sizes, int E, int group_offset, int E_local, int64_t M, int64_t K,
+                             int64_t F, uint16_t* a_out, uint8_t* h_q, uint8_t* h_sf, moe_stream_t stream);
+
+/* Step 4 (MX), unfused: a = [a0 | a1] bf16 [R, 2F] -> h = bf16(silu(a0) a1)
+ * quantised per 32 columns: h_q [R, F], h_sf [F/128][R][4].  F % 128 == 0. */
+moe_status moe_swiglu_quant_mx(const uint16_t* a, int64_t R, int64_t F, uint8_t* h_q, uint8_t* h_sf,
+                               moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -100,3 +100,23 @@ def test_host_side_argument_checks_of_the_fused_and_backward_entries(lib):
     assert lib.moe_swiglu_quant(p, 1, 24, 0, None, p, p, None) == 1                   # F % 16
     assert lib.moe_swiglu_quant(p, 1, 16, 2, None, p, p, None) == 1                   # static mode, no scale
     assert lib.moe_transpose_u8(p, 1, 24, 16, p, None) == 1                           # R % 16
+
+
+def test_host_side_argument_checks_of_the_mxfp8_entries(lib):
+    p = ctypes.c_void_p(256)  # a 16-byte aligned dummy address (never dereferenced)
+    # quantiser: cols not a multiple of 32; null scale output
+    assert lib.moe_quantize_rows_mx(p, 4, 48, p, p, None) == 1
+    assert lib.moe_quantize_rows_mx(p, 4, 64, p, None, None) == 1
+    # quantise + sort: D not a multiple of 32; short workspace
+    assert lib.moe_quantize_sort_mx(p, p, 4, 2, 4, 48, p, p, p, p, p, p, p, 1 << 20, None) == 1
+    assert lib.moe_quantize_sort_mx(p, p, 4, 2, 4, 64, p, p, p, p, p, p, p, 0, None) == 1
+    # gmm: K not a multiple of 128; N not a multiple of 16; null rhs scales; shard past E
+    assert lib.gmm_fp8_mx(p, p, p, p, p, 1, 0, 1, 8, 96, 256, p, None) == 1
+    assert lib.gmm_fp8_mx(p, p, p, p, p, 1, 0, 1, 8, 128, 24, p, None) == 1
+    assert lib.gmm_fp8_mx(p, p, p, None, p, 1, 0, 1, 8, 128, 256, p, None) == 1
+    assert lib.gmm_fp8_mx(p, p, p, p, p, 2, 1, 2, 8, 128, 256, p, None) == 1
+    # fused SwiGLU: F not a multiple of 128; null h scales
+    assert lib.gmm_fp8_mx_swiglu(p, p, p, p, p, 1, 0, 1, 8, 128, 96, None, p, p, None) == 1
+    assert lib.gmm_fp8_mx_swiglu(p, p, p, p, p, 1, 0, 1, 8, 128, 128, None, p, None, None) == 1
+    # unfused SwiGLU requantisation: F not a multiple of 32
+    assert lib.moe_swiglu_quant_mx(p, 4, 48, p, p, None) == 1
