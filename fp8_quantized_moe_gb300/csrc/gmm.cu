@@ -72,6 +72,13 @@ enum Mode {
   kMxSwiglu = 9    // MXFP8 wi gmm with the SwiGLU and MXFP8 requantisation epilogue
 };
 constexpr int kMxSfStageBytes = 3 * 512;  // MXFP8: per stage, one A and two B scale-factor atoms (32 x 16 B each)
+// MXFP8: slots of the shared-memory scale-factor ring (more than the operand
+// stages, so that the gatherer keeps several stages of copies in flight
+// without holding back the MMAs)
+constexpr int kMxSfSlots = 8;
+#ifndef MOE_MX_LAG
+#define MOE_MX_LAG 3
+#endif
 constexpr int kSwSlots = 8;  // promotion: ring of per-K-block weight-scale rows in shared memory
 
 struct Params {
@@ -121,7 +128,8 @@ struct SmemCtl {
   uint64_t empty[kMaxStages];
   uint64_t tfull[kMaxAcc];
   uint64_t tempty[kMaxAcc];
-  uint64_t sffull[kMaxStages];  // MXFP8: the stage's scale-factor atoms are in shared memory
+  uint64_t sffull[kMxSfSlots];   // MXFP8: the slot's scale-factor atoms are in shared memory
+  uint64_t sfempty[kMxSfSlots];  // MXFP8: the tensor core has copied the slot out (its MMAs completed)
   uint64_t sfull[kSwSlots];   // promotion: a weight-scale row of the ring has landed
   uint64_t sempty[kSwSlots];  // promotion: a weight-scale row of the ring has been read by every epilogue warp
   uint64_t xbar[4][2];        // promotion + SwiGLU: the two warps of a lane quarter have posted their h maxima
@@ -221,7 +229,7 @@ struct Cfg {
   // promotion: kSwSlots rows of BN weight scales, one per K block in flight
   static constexpr int SW_RING_BYTES = PROMOTE ? kSwSlots * BN * 4 : 0;
   // MXFP8: each stage's scale-factor atoms
-  static constexpr int SF_RING_BYTES = MX ? NSTAGE * kMxSfStageBytes : 0;
+  static constexpr int SF_RING_BYTES = MX ? kMxSfSlots * kMxSfStageBytes : 0;
   static constexpr size_t SMEM = 1024 + static_cast<size_t>(NSTAGE) * STAGE_BYTES + CTL_BYTES +
                                  static_cast<size_t>(EPI_WARPS) * STG_WARP_BYTES + SW_RING_BYTES + SF_RING_BYTES;
   static_assert(NSTAGE <= kMaxStages && NACC >= 1 && NACC <= kMaxAcc && NACC * BN * SEGS <= TMEM_COLS &&
@@ -446,7 +454,10 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
       mbar_init(smem_u32(&ctl->tempty[a]), (PAIR ? 2 : 1) * EPI_WARPS);
     }
     if (C::MX)
-      for (int s = 0; s < NSTAGE; ++s) mbar_init(smem_u32(&ctl->sffull[s]), 32);
+      for (int q = 0; q < kMxSfSlots; ++q) {
+        mbar_init(smem_u32(&ctl->sffull[q]), 32);
+        mbar_init(smem_u32(&ctl->sfempty[q]), 1);
+      }
     if (C::PROMOTE) {
       for (int q = 0; q < kSwSlots; ++q) {
         mbar_init(smem_u32(&ctl->sfull[q]), 1);
@@ -609,8 +620,9 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
           }
           const int s = it % NSTAGE;
           const uint32_t ph = (it / NSTAGE) & 1;
+          const uint32_t q = it % kMxSfSlots;  // MXFP8: scale slot
           if (!CTRL_WAIT(smem_u32(&ctl->full[s]), ph, abort_flag, kWaitLimitNs) ||
-              (C::MX && !CTRL_WAIT(smem_u32(&ctl->sffull[s]), ph, abort_flag, kWaitLimitNs))) {
+              (C::MX && !CTRL_WAIT(smem_u32(&ctl->sffull[q]), (it / kMxSfSlots) & 1, abort_flag, kWaitLimitNs))) {
             timed_out = true;
             break;
           }
@@ -627,7 +639,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
           // columns, B: 8), ahead of the MMAs that read them
           const uint32_t sfa_t = tmem_base + C::SF_COL0 + 16 * s, sfb_t = sfa_t + 4;
           if (C::MX) {
-            const uint32_t sf_sm = sf_ring + s * kMxSfStageBytes;
+            const uint32_t sf_sm = sf_ring + q * kMxSfStageBytes;
             tmem_cp_32x128b_warpx4(sfa_t, smem_desc_plain(sf_sm));
             tmem_cp_32x128b_warpx4(sfb_t, smem_desc_plain(sf_sm + 512));
             tmem_cp_32x128b_warpx4(sfb_t + 4, smem_desc_plain(sf_sm + 1024));
@@ -650,6 +662,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
             mma_commit_pair_mc(smem_u32(&ctl->empty[s]), 0x3);  // frees the stage in both CTAs
           else
             mma_commit(smem_u32(&ctl->empty[s]));
+          if (C::MX) mma_commit(smem_u32(&ctl->sfempty[q]));  // and the scale slot
           if (C::PROMOTE) {
             mma_commit(smem_u32(&ctl->tfull[a]));
             ++acc;
@@ -684,13 +697,15 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
     // word of a row holding the stage's four K blocks.  The codes are
     // K-block-major, so the words of a tile's rows for one stage are
     // adjacent and every copy instruction of the warp reads one 128-byte
-    // line.  A stage is announced
-    // (32 arrivals on sffull) LAG stages later, once its copies have landed
-    // and been made visible to the tensor core's (async-proxy) reads, so
-    // that the lane keeps LAG stages of copies in flight.  The stage's buffer
-    // is free once the MMAs of its previous use completed (empty barrier).
-    constexpr uint32_t LAG = 2;
-    static_assert(!C::MX || LAG < NSTAGE, "the gatherer may run at most NSTAGE - 1 stages ahead of its announcements");
+    // line.  The atoms go to a ring of kMxSfSlots slots; a slot is free once
+    // the MMAs that read its previous contents completed (sfempty, committed
+    // by the MMA issuer).  A slot is announced (32 arrivals on sffull) LAG
+    // stages later, once its copies have landed and been made visible to the
+    // tensor core's (async-proxy) reads, so that each lane keeps LAG stages
+    // of copies in flight; with more slots than LAG the announcements stay
+    // ahead of the MMAs.
+    constexpr uint32_t LAG = MOE_MX_LAG;
+    static_assert(LAG >= 1 && LAG < kMxSfSlots, "the gatherer runs at most kMxSfSlots - 1 stages ahead");
     uint32_t it = 0;
     const uint32_t* lsf = reinterpret_cast<const uint32_t*>(p.lhs_sf);
     const uint32_t* rsf = reinterpret_cast<const uint32_t*>(p.rhs_sf);
@@ -698,12 +713,12 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
     for (int t = unit0; t < total && !timed_out; t += units) {
       const Tile tl = get_tile<MODE, PAIR>(p, ctl, t, rank);
       for (int kb = 0; kb < tl.nkb; ++kb) {
-        const int s = it % NSTAGE;
-        if (!CTRL_WAIT(smem_u32(&ctl->empty[s]), ((it / NSTAGE) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+        const uint32_t q = it % kMxSfSlots;
+        if (!CTRL_WAIT(smem_u32(&ctl->sfempty[q]), ((it / kMxSfSlots) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
           timed_out = true;
           break;
         }
-        const uint32_t dst = sf_ring + s * kMxSfStageBytes + lane * 16;
+        const uint32_t dst = sf_ring + q * kMxSfStageBytes + lane * 16;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {  // rows past M (end of the last group) read as zeros
           const int64_t row = static_cast<int64_t>(tl.row0) + 32 * c + lane;
@@ -727,7 +742,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         if (it >= LAG) {
           cp_async_wait<LAG>();
           fence_proxy_async_smem();
-          mbar_arrive(smem_u32(&ctl->sffull[(it - LAG) % NSTAGE]));
+          mbar_arrive(smem_u32(&ctl->sffull[(it - LAG) % kMxSfSlots]));
         }
         ++it;
       }
@@ -735,7 +750,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
     // the last LAG stages (and, after a timeout, every copy in flight)
     cp_async_wait<0>();
     fence_proxy_async_smem();
-    for (uint32_t j = it > LAG ? it - LAG : 0; j < it; ++j) mbar_arrive(smem_u32(&ctl->sffull[j % NSTAGE]));
+    for (uint32_t j = it > LAG ? it - LAG : 0; j < it; ++j) mbar_arrive(smem_u32(&ctl->sffull[j % kMxSfSlots]));
     if (timed_out) {
       *abort_flag = 1;
       ctl->err = 2;
