@@ -223,7 +223,9 @@ class OracleSample:
         import oracle
         self.oracle = oracle
         self.cfg, self.x, self.static = cfg, x_bits, static
-        self.wq = oracle.prepare_weights(w_in_bits, w_out_bits, cfg.w_mode, static)
+        self.mx = cfg.act_mode == synth.MX32
+        self.wq = (oracle.prepare_weights_mx(w_in_bits, w_out_bits) if self.mx else
+                   oracle.prepare_weights(w_in_bits, w_out_bits, cfg.w_mode, static))
         remap = -np.ones(cfg.E, np.int64)
         remap[np.asarray(experts)] = np.arange(len(experts))
         loc = remap[ids]
@@ -241,7 +243,10 @@ class OracleSample:
         ids = self.local[idx].reshape(-1, 1)
         w = self.w[idx].reshape(-1, 1)
         t0 = time.perf_counter()
-        self.oracle.ffn_forward(xs, ids, w, self.wq, self.nE, self.cfg.act_mode, self.static)
+        if self.mx:
+            self.oracle.ffn_forward_mx(xs, ids, w, self.wq, self.nE)
+        else:
+            self.oracle.ffn_forward(xs, ids, w, self.wq, self.nE, self.cfg.act_mode, self.static)
         return time.perf_counter() - t0
 
     def aim(self, target_s: float, start: int = 64) -> tuple:
@@ -307,11 +312,23 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
     buf = moe.FFNBuffers(cfg.T, cfg.D, cfg.E, cfg.k, cfg.F, cfg.act_mode, dev)
     stream = torch.cuda.current_stream()
 
+    mx = cfg.act_mode == synth.MX32
+
     def step(ev=None):
         if ev is None:
             return moe.ffn_forward(x, ids, w, W, cfg.act_mode, buf, sx, sh)
         # the same calls as ffn_forward, with events around the two gmms
         E = W.w_in.shape[0]
+        if mx:
+            s = moe.quantize_sort_mx(x, ids, E, out=buf.sort)
+            ev[0].record(stream)
+            moe.gmm_mx_swiglu(s["xs_q"], s["xs_scale"], W.w_in, W.s_in, s["group_sizes"], h_q=buf.h_q, h_sf=buf.h_s)
+            ev[1].record(stream)
+            ev[2].record(stream)
+            moe.gmm_mx(buf.h_q, buf.h_s, W.w_out, W.s_out, s["group_sizes"], out=buf.o)
+            ev[3].record(stream)
+            moe.ragged_gather_reduce(buf.o, s["pos"], w, cfg.k, out=buf.y)
+            return buf.y
         s = moe.quantize_sort(x, ids, E, cfg.act_mode, sx, out=buf.sort)
         xs_s = s["xs_scale"] if cfg.act_mode != 2 else sx
         ev[0].record(stream)
@@ -423,7 +440,7 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
                "note": "public ffn_forward per step; inputs copied in from pinned host memory and y copied out "
                        "every step, on their own streams, double-buffered across steps"}
 
-    fused = moe.swiglu_fuse_pays(cfg.act_mode, W.in_mode, cfg.F)
+    fused = mx or moe.swiglu_fuse_pays(cfg.act_mode, W.in_mode, cfg.F)
     # quantise + sort 4 (histogram, scan, scatter, quantise-gather) + (fused gmm+SwiGLU 1, +1 code
     # pass for per-row h scales | gmm 1 + SwiGLU 1) + gmm 1 + combine 1
     launches_per_step = 4 + ((1 + (1 if cfg.act_mode == 0 else 0)) if fused else 2) + 1 + 1
@@ -436,7 +453,7 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
     # the dominant call of the step is the wi_0 | wi_1 contraction
     achieved = fl["gmm_in"] / (g_in / 1e3) / 1e12
     both = (fl["gmm_in"] + fl["gmm_out"]) / ((g_in + g_out) / 1e3) / 1e12
-    kname = "gmm_fp8_swiglu" if fused else "gmm_fp8 (wi_0|wi_1)"
+    kname = "gmm_fp8_mx_swiglu" if mx else ("gmm_fp8_swiglu" if fused else "gmm_fp8 (wi_0|wi_1)")
     result = {
         "metric": METRIC,
         "value": cfg.T * world / (ms / 1e3),
@@ -448,7 +465,8 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3 (fp32 accumulate, bf16 in/out)",
+        "dtype": ("e4m3 with E8M0 block scales (MXFP8), fp32 accumulate, bf16 in/out" if mx else
+                  "e4m3 (fp32 accumulate, bf16 in/out)"),
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, random-init)",
         "config": {"workload": workload_name(cfg), "tokens_per_gpu": cfg.T, "parallelism": f"dp{world} (replicas)",
                    "l2": "inputs larger than L2: fp8 expert weights %.2f GB streamed every step"
@@ -459,7 +477,9 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
                      "peak_note": f"of {pk_kind}: fp8 = 2 x burst bf16 cuBLAS ({pk['bf16_tflops']} TFLOP/s; "
                                   "the nominal dense fp8 / bf16 ratio is 2)",
                      "flops_per_call": fl["gmm_in"], "ms_per_call": g_in,
-                     "note": ("one gmm_fp8_swiglu call per step: the tcgen05 contraction with the SwiGLU and "
+                     "note": ("one gmm_fp8_mx_swiglu call per step: the block-scaled tcgen05 contraction with the "
+                              "SwiGLU and MXFP8 requantisation epilogue") if mx else
+                             ("one gmm_fp8_swiglu call per step: the tcgen05 contraction with the SwiGLU and "
                               "requantisation epilogue, plus the h code pass of the per-token scales") if fused else
                              "one gmm_fp8 call per step"},
         "gmm_fp8_both": {"achieved": both, "frac": both / fp8_peak, "unit": "TFLOP/s", "gmm_in_ms": g_in,
