@@ -6,9 +6,13 @@ gather-reduce) over one batch of synthetic tokens.  Default workload: the
 DeepSeek-V3-shaped layer (T=16384, d_model=7168, 256 experts, top-8,
 d_ff=2048), per-token-per-128-channel activation scales and blockwise
 [E, K/128, N] weight scales, the largest of the five layers on every axis.
-The Mixtral-shaped layer (T=8192, d_model=4096, 8 experts, top-2,
-d_ff=14336, per-token / per-channel scales) is timed in the same run and
-reported as a secondary object of the same line.
+Timed in the same run and reported as sub-objects of the same line
+(`secondary`, `secondaries`):
+- the Mixtral-shaped layer (T=8192, d_model=4096, 8 experts, top-2,
+  d_ff=14336, per-token / per-channel scales);
+- the serving prefill chunk (T=2048, d_model=2048, 128 experts, top-8,
+  d_ff=768, pre-quantised blockwise weights);
+- the MXFP8 variant of the DeepSeek-V3-shaped layer.
 
 Prints one JSON line (rank 0).  Launch with torchrun for several GPUs: every
 rank runs its own batch (data parallel over tokens, no collective on the data
@@ -46,8 +50,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="dsv3", choices=list(synth.CONFIGS))
-    ap.add_argument("--secondary", default="mixtral",
-                    help="a second config timed in the same run, reported as a sub-object ('' for none)")
+    ap.add_argument("--secondary", default="mixtral,prefill,dsv3_mx",
+                    help="comma-separated configs timed in the same run after the main one (at most 50 steps "
+                         "each), reported as sub-objects: 'secondary' (the first) and 'secondaries' (all); "
+                         "'' for none")
     ap.add_argument("--tokens", type=int, default=0, help="override T (small cases for profiling)")
     ap.add_argument("--experts", type=int, default=0, help="override E (small cases for profiling)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0, help="oracle sample size (0 = auto)")
@@ -450,8 +456,24 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
     pk, pk_kind = peaks()
     # the timed region is well under a second of GPU time: the burst figure applies
     fp8_peak = 2.0 * pk["bf16_tflops"]
-    # the dominant call of the step is the wi_0 | wi_1 contraction
-    achieved = fl["gmm_in"] / (g_in / 1e3) / 1e12
+    # the dominant call of the step is the wi_0 | wi_1 contraction; it is
+    # bound by whichever of its flops (fp8 peak) and its bytes (HBM) takes
+    # longer: the weight stream binds the small prefill batch
+    R = cfg.T * cfg.k
+    if mx:
+        nbytes = (R * cfg.D + cfg.E * 2 * cfg.F * cfg.D + R * cfg.F) * 33 // 32
+    else:
+        # codes, the weights, the output, and the fp32 scales the call reads
+        sa = {synth.PER_ROW: 4 * R, synth.PER_ROW_BLOCK128: 4 * R * (cfg.D // 128)}.get(cfg.act_mode, 0)
+        sw = {synth.PER_ROW: 4 * cfg.E * 2 * cfg.F,
+              synth.PER_ROW_BLOCK128: 4 * cfg.E * (cfg.D // 128) * 2 * cfg.F}.get(cfg.w_mode, 0)
+        out = (5 if cfg.act_mode == synth.PER_ROW else 1) * R * cfg.F if fused else 4 * R * cfg.F
+        nbytes = R * cfg.D + cfg.E * 2 * cfg.F * cfg.D + out + sa + sw
+    hbm_bound = nbytes / (pk["hbm_gbs"] * 1e9) > fl["gmm_in"] / (fp8_peak * 1e12)
+    if hbm_bound:
+        achieved, peak, unit = nbytes / (g_in / 1e3) / 1e9, pk["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = fl["gmm_in"] / (g_in / 1e3) / 1e12, fp8_peak, "TFLOP/s"
     both = (fl["gmm_in"] + fl["gmm_out"]) / ((g_in + g_out) / 1e3) / 1e12
     kname = "gmm_fp8_mx_swiglu" if mx else ("gmm_fp8_swiglu" if fused else "gmm_fp8 (wi_0|wi_1)")
     result = {
@@ -471,12 +493,13 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
         "config": {"workload": workload_name(cfg), "tokens_per_gpu": cfg.T, "parallelism": f"dp{world} (replicas)",
                    "l2": "inputs larger than L2: fp8 expert weights %.2f GB streamed every step"
                          % ((2 * cfg.F * cfg.D + cfg.D * cfg.F) * cfg.E / 1e9)},
-        "roofline": {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": fp8_peak,
-                     "unit": "TFLOP/s", "frac": achieved / fp8_peak,
+        "roofline": {"bound": "hbm" if hbm_bound else "tensor", "kernel": kname, "achieved": achieved,
+                     "peak": peak, "unit": unit, "frac": achieved / peak,
                      "traffic": recorded_traffic(kname, cfg) if not (args.tokens or args.experts) else None,
-                     "peak_note": f"of {pk_kind}: fp8 = 2 x burst bf16 cuBLAS ({pk['bf16_tflops']} TFLOP/s; "
-                                  "the nominal dense fp8 / bf16 ratio is 2)",
-                     "flops_per_call": fl["gmm_in"], "ms_per_call": g_in,
+                     "peak_note": (f"of {pk_kind}: STREAM-style copy" if hbm_bound else
+                                   f"of {pk_kind}: fp8 = 2 x burst bf16 cuBLAS ({pk['bf16_tflops']} TFLOP/s; "
+                                   "the nominal dense fp8 / bf16 ratio is 2)"),
+                     "flops_per_call": fl["gmm_in"], "algorithmic_bytes_per_call": nbytes, "ms_per_call": g_in,
                      "note": ("one gmm_fp8_mx_swiglu call per step: the block-scaled tcgen05 contraction with the "
                               "SwiGLU and MXFP8 requantisation epilogue") if mx else
                              ("one gmm_fp8_swiglu call per step: the tcgen05 contraction with the SwiGLU and "
@@ -821,11 +844,15 @@ def main():
         res = run_reference(args, cfg, rank, world)
     else:
         res = run_ours(args, cfg, rank, world, local)
-        if args.secondary and args.secondary != cfg.name and not (args.tokens or args.experts):
-            cfg2 = synth.CONFIGS[args.secondary]
-            r2 = run_ours(args, cfg2, rank, world, local, secondary=True)
-            res["secondary"] = {k: r2[k] for k in ("value", "unit", "ms_per_step", "steps", "config", "roofline",
-                                                   "gmm_fp8_both", "gpu_launches", "clocks")}
+        names = [n for n in (args.secondary or "").split(",") if n and n != cfg.name]
+        if names and not (args.tokens or args.experts):
+            subs = []
+            for n in names:
+                r2 = run_ours(args, synth.CONFIGS[n], rank, world, local, secondary=True)
+                subs.append({k: r2[k] for k in ("value", "unit", "ms_per_step", "steps", "config", "roofline",
+                                                "gmm_fp8_both", "gpu_launches", "clocks", "dtype")})
+            res["secondary"] = subs[0]
+            res["secondaries"] = subs
         if world > 1:
             torch.distributed.destroy_process_group()
     if rank == 0 and res is not None:
