@@ -225,10 +225,11 @@ struct Cfg {
   // 128-byte-swizzled layout of a TMA store box
   static constexpr int STG_PITCH = (MODE == kFinal || MODE == kSplit || MODE == kBf16) ? 80 : 0;
   static constexpr int STG_BUFS = MODE == kTgmm ? MOE_TGMM_STG_BUFS : 1;
-  // kMx, kMxSwiglu: an 8-row staging buffer per warp (warp_store_32x64B)
+  // kSwiglu, kMx, kMxSwiglu: an 8-row staging buffer per warp (warp_store_32x64B)
   static constexpr int STG_WARP_BYTES = (MODE == kFinal || MODE == kSplit || MODE == kBf16)
                                             ? 32 * STG_PITCH
-                                            : (MODE == kTgmm ? STG_BUFS * 4096 : (MX ? kStg8Bytes : 0));
+                                            : (MODE == kTgmm ? STG_BUFS * 4096
+                                                              : ((MX || MODE == kSwiglu) ? kStg8Bytes : 0));
   static constexpr size_t CTL_BYTES = (sizeof(SmemCtl) + 1023) / 1024 * 1024;  // keeps the staging 1 KB aligned
   // promotion: kSwSlots rows of BN weight scales, one per K block in flight
   static constexpr int SW_RING_BYTES = PROMOTE ? kSwSlots * BN * 4 : 0;
@@ -956,26 +957,35 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
                 d1[g] = make_uint4(a1b[4 * g], a1b[4 * g + 1], a1b[4 * g + 2], a1b[4 * g + 3]);
               }
             }
-            if (p.h_mode == MOE_SCALE_PER_ROW) {
-              uint4* dh = reinterpret_cast<uint4*>(p.h_out + row * p.F + hc);
-#pragma unroll
-              for (int g = 0; g < CW / 8; ++g)
-                dh[g] = make_uint4(hb[4 * g], hb[4 * g + 1], hb[4 * g + 2], hb[4 * g + 3]);
-            } else if (p.h_mode == MOE_SCALE_PER_TENSOR) {
-              float qv[CW];
-              quant_n<CW>(h, hs, hinv, qv);
-              uint4* dst = reinterpret_cast<uint4*>(p.h_q + row * p.F + hc);
-#pragma unroll
-              for (int g = 0; g < CW / 16; ++g) {
-                const uint2 lo8 = pack_e4m3x8(qv + 16 * g), hi8 = pack_e4m3x8(qv + 16 * g + 8);
-                dst[g] = make_uint4(lo8.x, lo8.y, hi8.x, hi8.y);
-              }
-            }
           }
-          if (p.h_mode == MOE_SCALE_PER_ROW_BLOCK128) {
+          if (p.h_mode == MOE_SCALE_PER_TENSOR) {  // the chunk's codes (16 bytes) into hp[4 cc ..]
+            float qv[CW];
+            quant_n<CW>(h, hs, hinv, qv);
+            const uint2 lo8 = pack_e4m3x8(qv), hi8 = pack_e4m3x8(qv + 8);
+            hp[4 * cc] = lo8.x;
+            hp[4 * cc + 1] = lo8.y;
+            hp[4 * cc + 2] = hi8.x;
+            hp[4 * cc + 3] = hi8.y;
+          } else {
 #pragma unroll
             for (int j = 0; j < CW / 2; ++j) hp[cc * (CW / 2) + j] = hb[j];
           }
+        }
+        // the warp's rows go out as whole row segments (warp_store_32x64B):
+        // h bf16 [64 columns = 128 bytes] or codes [64 bytes] of each row
+        uint8_t* stg = stg_base + (warp - C::CTRL_WARPS) * C::STG_WARP_BYTES;
+        const int wrows = tl.rows - q4 * 32;
+        const int64_t wrow0 = static_cast<int64_t>(tl.row0) + q4 * 32;
+        const int hc0 = tl.n0 + half * 64;  // first h column of this warp
+        if (p.h_mode == MOE_SCALE_PER_ROW) {
+          uint8_t* hb0 = reinterpret_cast<uint8_t*>(p.h_out + wrow0 * p.F + hc0);
+          warp_store_32x64B(stg, *reinterpret_cast<const uint32_t(*)[16]>(hp), hb0, 2 * static_cast<int64_t>(p.F),
+                            wrows, 64);
+          warp_store_32x64B(stg, *reinterpret_cast<const uint32_t(*)[16]>(hp + 16), hb0 + 64,
+                            2 * static_cast<int64_t>(p.F), wrows, 64);
+        } else if (p.h_mode == MOE_SCALE_PER_TENSOR) {
+          warp_store_32x64B(stg, *reinterpret_cast<const uint32_t(*)[16]>(hp), p.h_q + wrow0 * p.F + hc0, p.F, wrows,
+                            64);
         }
         const int par = acc & 1;
         ++acc;
@@ -988,24 +998,26 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
           ctl->pamax[par][q4][half][lane] = amax;
           named_barrier_sync(1 + q4, 64);
           const float m = fmaxf(amax, ctl->pamax[par][q4][half ^ 1][lane]);
-          if (row_ok) {
-            const float sblk = absmax_scale(m);
-            const float inv = __frcp_rn(sblk);
-            if (half == 0) p.h_scale[row * (p.F / 128) + tl.n0 / 128] = sblk;
+          const float sblk = absmax_scale(m);
+          const float inv = __frcp_rn(sblk);
+          if (row_ok && half == 0) p.h_scale[row * (p.F / 128) + tl.n0 / 128] = sblk;
+          uint32_t cw[16];  // the 64 codes of this warp's part of the row
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
             float x16[16], qv[16];
-            uint4* dst = reinterpret_cast<uint4*>(p.h_q + row * p.F + tl.n0 + half * 64);
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                x16[2 * j] = bf16lo(hp[g * 8 + j]);
-                x16[2 * j + 1] = bf16hi(hp[g * 8 + j]);
-              }
-              quant_n<16>(x16, sblk, inv, qv);
-              const uint2 lo8 = pack_e4m3x8(qv), hi8 = pack_e4m3x8(qv + 8);
-              dst[g] = make_uint4(lo8.x, lo8.y, hi8.x, hi8.y);
+            for (int j = 0; j < 8; ++j) {
+              x16[2 * j] = bf16lo(hp[g * 8 + j]);
+              x16[2 * j + 1] = bf16hi(hp[g * 8 + j]);
             }
+            quant_n<16>(x16, sblk, inv, qv);
+            const uint2 lo8 = pack_e4m3x8(qv), hi8 = pack_e4m3x8(qv + 8);
+            cw[4 * g] = lo8.x;
+            cw[4 * g + 1] = lo8.y;
+            cw[4 * g + 2] = hi8.x;
+            cw[4 * g + 3] = hi8.y;
           }
+          warp_store_32x64B(stg, cw, p.h_q + wrow0 * p.F + hc0, p.F, wrows, 64);
         }
       } else if (MODE == kSplit) {
         // out = bf16((s0 * acc0 + s1 * acc1) * s_a): the two K segments'
