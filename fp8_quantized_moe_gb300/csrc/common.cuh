@@ -419,6 +419,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// The same wait taken by all 32 lanes of a warp, with one outcome for the
+// whole warp: a lane that saw the phase complete while another lane of the
+// warp ran out of time follows the timeout, so that the warp never splits
+// ahead of a warp-wide synchronisation.
+__device__ __forceinline__ bool mbar_wait_bounded_warp(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+                                                       uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort_flag, limit_ns));
+}
+
 // ------------------------------------------------------------------------
 // TMA
 // ------------------------------------------------------------------------

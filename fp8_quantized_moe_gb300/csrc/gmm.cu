@@ -801,7 +801,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
     uint32_t acc = 0;
     uint32_t tcount = 0;  // promotion: tiles done by this CTA
-    if (p.stall && !mbar_wait_bounded(smem_u32(&ctl->never), 0, abort_flag, p.stall_ns)) timed_out = true;
+    if (p.stall && !mbar_wait_bounded_warp(smem_u32(&ctl->never), 0, abort_flag, p.stall_ns)) timed_out = true;
     int stg_sel = 0;  // kTgmm: staging buffer of this warp's next block
     for (int t = unit0; t < total && !timed_out; t += units) {
       const Tile tl = get_tile<MODE, PAIR>(p, ctl, t, rank);
@@ -835,7 +835,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         const int cb0 = half * NB;
         float sgr[2][32];
         load_col_scales32(sgb, tl.n0 + cb0 * 32, p.N, per_col, sg_t, sgr[0]);
-        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
+        if (!mbar_wait_bounded_warp(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
           timed_out = true;
           break;
         }
@@ -880,7 +880,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         // the tile; accumulator columns c*32.. hold a0, 128 + c*32.. hold a1.
         const int64_t row = static_cast<int64_t>(tl.row0) + r;
         const uint32_t a = acc % NACC;
-        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
+        if (!mbar_wait_bounded_warp(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
           timed_out = true;
           break;
         }
@@ -1025,7 +1025,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         uint16_t* out = static_cast<uint16_t*>(p.out);
         const int64_t row = static_cast<int64_t>(tl.row0) + r;
         const uint32_t a = acc % NACC;
-        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
+        if (!mbar_wait_bounded_warp(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
           timed_out = true;
           break;
         }
@@ -1074,7 +1074,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         uint16_t* out = static_cast<uint16_t*>(p.out);
         const int64_t row = static_cast<int64_t>(tl.row0) + r;
         const uint32_t a = acc % NACC;
-        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
+        if (!mbar_wait_bounded_warp(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
           timed_out = true;
           break;
         }
@@ -1131,7 +1131,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         // before any store, so the next tile's MMAs run under the stores.
         uint16_t* out = static_cast<uint16_t*>(p.out);
         const int64_t row = static_cast<int64_t>(tl.row0) + r;
-        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[0]), acc & 1, abort_flag, kWaitLimitNs)) {
+        if (!mbar_wait_bounded_warp(smem_u32(&ctl->tfull[0]), acc & 1, abort_flag, kWaitLimitNs)) {
           timed_out = true;
           break;
         }
@@ -1169,7 +1169,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         // gmm_fp8_mx stores them, h = bf16(silu(a0) a1), then per block
         // X = floor(log2 amax) - 8 and codes e4m3(h / 2^X).
         const int64_t row = static_cast<int64_t>(tl.row0) + r;
-        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[0]), acc & 1, abort_flag, kWaitLimitNs)) {
+        if (!mbar_wait_bounded_warp(smem_u32(&ctl->tfull[0]), acc & 1, abort_flag, kWaitLimitNs)) {
           timed_out = true;
           break;
         }
@@ -1237,7 +1237,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         // shared memory as in the fp8 gmm, or fp32 rows written directly
         const int64_t row = static_cast<int64_t>(tl.row0) + r;
         const uint32_t a = acc % NACC;
-        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
+        if (!mbar_wait_bounded_warp(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
           timed_out = true;
           break;
         }
@@ -1293,7 +1293,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         // lower expert index, kept as a sorted list in registers
         const int64_t row = static_cast<int64_t>(tl.row0) + r;
         const uint32_t a = acc % NACC;
-        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
+        if (!mbar_wait_bounded_warp(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs)) {
           timed_out = true;
           break;
         }
@@ -1447,9 +1447,9 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
             sa_next = load_a(kb + 1);
             const uint32_t a = acc % NACC;
             const uint32_t q = acc % kSwSlots;
-            if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs) ||
+            if (!mbar_wait_bounded_warp(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs) ||
                 (FM != 1 &&
-                 !mbar_wait_bounded(smem_u32(&ctl->sfull[q]), (acc / kSwSlots) & 1, abort_flag, kWaitLimitNs))) {
+                 !mbar_wait_bounded_warp(smem_u32(&ctl->sfull[q]), (acc / kSwSlots) & 1, abort_flag, kWaitLimitNs))) {
               timed_out = true;
               break;
             }
@@ -1619,7 +1619,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
             // parities alternate between tiles)
             ctl->pamax[par][q4][part][lane] = amax;
             mbar_arrive(smem_u32(&ctl->xbar[q4][par]));
-            if (!mbar_wait_bounded(smem_u32(&ctl->xbar[q4][par]), (tcount >> 1) & 1, abort_flag, kWaitLimitNs)) {
+            if (!mbar_wait_bounded_warp(smem_u32(&ctl->xbar[q4][par]), (tcount >> 1) & 1, abort_flag, kWaitLimitNs)) {
               timed_out = true;
               break;
             }
