@@ -1447,9 +1447,13 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
             sa_next = load_a(kb + 1);
             const uint32_t a = acc % NACC;
             const uint32_t q = acc % kSwSlots;
-            if (!mbar_wait_bounded_warp(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs) ||
+            // per-lane waits here, once per K block (a warp vote on each cost
+            // 2 % of this kernel): the converged warp's lanes read the same
+            // barrier phase, abort flag and timer in each instruction of the
+            // wait loop, so they leave it together
+            if (!mbar_wait_bounded(smem_u32(&ctl->tfull[a]), (acc / NACC) & 1, abort_flag, kWaitLimitNs) ||
                 (FM != 1 &&
-                 !mbar_wait_bounded_warp(smem_u32(&ctl->sfull[q]), (acc / kSwSlots) & 1, abort_flag, kWaitLimitNs))) {
+                 !mbar_wait_bounded(smem_u32(&ctl->sfull[q]), (acc / kSwSlots) & 1, abort_flag, kWaitLimitNs))) {
               timed_out = true;
               break;
             }
