@@ -6,7 +6,9 @@
 // output, bf16 output), "Support quantization for tokamax gmm v2" (gmm and
 // tgmm with absmax scales) and "Keep qwix out of tpu-inference's fused MoE
 // kernel and pre-quantize weights" (fp8 weights with [E, blocks, 1, N]
-// scales; 32-bit accumulation).
+// scales; 32-bit accumulation); and, not from those pages,
+//   gmm_fp8_mx the same gmm on MXFP8 operands (OCP Microscaling Formats v1.0:
+//              one E8M0 power-of-two scale per 32 values of K).
 //
 // Design (one persistent CTA per SM, 1 CTA/SM by shared memory):
 //   warp 0      TMA producer: 128x128 A tile + 256x128 B tile per stage into a
@@ -20,6 +22,14 @@
 // operand the scale cannot leave the sum, so every K block gets a fresh TMEM
 // accumulator and eight epilogue warps fold it into fp32 registers
 // ("promotion", packed f32x2 FMAs).
+//
+// MXFP8 (gmm_fp8_mx, gmm_fp8_mx_swiglu): tcgen05.mma.kind::mxf8f6f4 with
+// one E8M0 scale per 32 values of K on each operand, applied by the tensor
+// core, so one accumulator runs over the whole K loop.  A control warp
+// gathers each stage's scale codes into shared-memory atoms (a ring of its
+// own), and the MMA issuer copies them into tensor memory (tcgen05.cp) ahead
+// of the stage's MMAs; the scales' tensor-memory slots take the columns next
+// to the accumulator, so there is one accumulator, not two.
 //
 // Tile scheduler: tiles are ordered expert-major, then N tile, then M tile,
 // so that the CTAs running at the same time share the same expert's weights
@@ -1129,8 +1139,9 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         // With one accumulator, the tile (8 warps: lane quarter q4, columns
         // [128 half, 128 half + 128)) is read into registers and released
         // before any store, so the next tile's MMAs run under the stores.
+        // (Timing variants that skipped this wait, or these loads, ran no
+        // faster: the single accumulator is not what bounds the kernel.)
         uint16_t* out = static_cast<uint16_t*>(p.out);
-        const int64_t row = static_cast<int64_t>(tl.row0) + r;
         if (!mbar_wait_bounded_warp(smem_u32(&ctl->tfull[0]), acc & 1, abort_flag, kWaitLimitNs)) {
           timed_out = true;
           break;
@@ -1148,7 +1159,6 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
         // segments (rows past the group's end are not stored)
         uint8_t* stg = stg_base + (warp - C::CTRL_WARPS) * C::STG_WARP_BYTES;
         uint8_t* obase = reinterpret_cast<uint8_t*>(out + (static_cast<int64_t>(tl.row0) + q4 * 32) * p.N);
-        (void)row;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int nb = tl.n0 + half * 128 + 32 * i;
