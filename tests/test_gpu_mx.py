@@ -146,6 +146,9 @@ def make_mx_case(seed, M, K, N, E, zero_frac=0.25):
     (700, 4096, 512, 5),
     (2048, 2048, 1536, 128),  # E = 128 experts, many empty or short groups
     (129, 384, 256, 2),       # a group of 1 row past a full tile
+    (129, 3072, 272, 2),      # a one-row group, an N tail
+    (1, 4096, 256, 1),
+    (3000, 3072, 768, 24),    # many groups, several tiles per group
 ])
 def test_gmm_mx_matches_oracle(M, K, N, E):
     sizes, a, asf, w, wsf = make_mx_case(M * 31 + K + N + E, M, K, N, E)
@@ -168,9 +171,10 @@ def test_gmm_mx_block_scales_are_per_32_columns():
     assert_close(host(out), ref, "gmm_mx with outlier blocks")
 
 
-def test_gmm_mx_expert_parallel_shard():
-    M, K, N, E = 1000, 512, 384, 9
-    sizes, a, asf, w, wsf = make_mx_case(17, M, K, N, E, zero_frac=0.2)
+@pytest.mark.parametrize("K", [512, 4096])
+def test_gmm_mx_expert_parallel_shard(K):
+    M, N, E = 1000, 384, 9
+    sizes, a, asf, w, wsf = make_mx_case(17 + K, M, K, N, E, zero_frac=0.2)
     g0, El = 2, 4
     w, wsf = np.ascontiguousarray(w[g0:g0 + El]), np.ascontiguousarray(wsf[g0:g0 + El])
     ref = oracle.gmm_mx(a, asf, w, wsf, sizes, group_offset=g0, E_local=El)
@@ -188,6 +192,9 @@ def test_gmm_mx_expert_parallel_shard():
     (1000, 7168, 256, 8, None),
     (1, 128, 128, 1, None),
     (1000, 512, 384, 9, (3, 5)),
+    (700, 4096, 256, 5, None),
+    (1000, 3072, 384, 9, (2, 4)),
+    (1, 4096, 128, 1, None),
 ])
 def test_gmm_mx_swiglu_stagewise(M, K, F, E, shard):
     """a against the oracle's MX gmm; h codes and E8M0 codes bit-exact
@@ -225,19 +232,19 @@ def test_gmm_mx_bounded_wait_timeout_reports_and_recovers():
     producer and the MMA issuer stop, every copy in flight lands, tensor
     memory is freed and MOE_DEVERR_TIMEOUT is raised; the next call is exact."""
     lib = moe.lib()
-    M, K, N, E = 4096, 512, 1024, 8
-    sizes, a, asf, w, wsf = make_mx_case(23, M, K, N, E)
-    args = mx_args(a, asf, w, wsf, sizes)
-    assert moe.device_error() == 0
-    lib.moe_test_stall_epilogue(200_000)
-    try:
-        moe.gmm_mx(*args)
-        assert moe.device_error() == 0x4  # MOE_DEVERR_TIMEOUT
-    finally:
-        lib.moe_test_stall_epilogue(0)
-    out = moe.gmm_mx(*args)
-    assert moe.device_error() == 0
-    assert_close(host(out), oracle.gmm_mx(a, asf, w, wsf, sizes), "gmm_mx after a timed-out call")
+    for M, K, N, E in [(4096, 512, 1024, 8), (2048, 4096, 512, 4)]:  # short and long K loops
+        sizes, a, asf, w, wsf = make_mx_case(23 + K, M, K, N, E)
+        args = mx_args(a, asf, w, wsf, sizes)
+        assert moe.device_error() == 0
+        lib.moe_test_stall_epilogue(200_000)
+        try:
+            moe.gmm_mx(*args)
+            assert moe.device_error() == 0x4  # MOE_DEVERR_TIMEOUT
+        finally:
+            lib.moe_test_stall_epilogue(0)
+        out = moe.gmm_mx(*args)
+        assert moe.device_error() == 0
+        assert_close(host(out), oracle.gmm_mx(a, asf, w, wsf, sizes), f"gmm_mx after a timed-out call (K={K})")
 
 
 # ------------------------------------------------------------------ FFN ----
