@@ -93,6 +93,8 @@ def lib():
                 "or_quantize_rows_mx": ([P, i64, i64, P, P], None),
                 "or_gmm_mx": ([P, P, P, P, P, i32, i32, i32, i64, i64, i64, P, i64, P, P], None),
                 "or_swiglu_quant_mx": ([P, i64, i64, P, P, P], None),
+                "or_quantize_weights_int8": ([P, i64, i64, i64, i32, f32, P, P], None),
+                "or_gmm_w8": ([P, P, i32, P, P, i32, P, i32, i32, i32, i64, i64, i64, P, i64, P, P], None),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
@@ -201,6 +203,25 @@ def quantize_weights(w_bits, mode: int, static_scale: float = 1.0):
     return q, s
 
 
+def quantize_weights_int8(w_bits, mode: int, static_scale: float = 1.0):
+    """int8 expert weights ("Keep qwix out of tpu-inference's fused MoE kernel
+    and pre-quantize weights": float8_e4m3fn or int8 weights with [E, blocks,
+    1, N] scales): bf16 [E, N, K] -> (int8 codes [E, N, K], scales [E, N] |
+    [E, K/128, N] | [1]).  s = fp32(amax / 127), q = rint(fp32(x / s))."""
+    w = _c(w_bits, np.uint16)
+    E, N, K = w.shape
+    q = np.empty((E, N, K), np.int8)
+    if mode == PER_ROW:
+        s = np.empty((E, N), np.float32)
+    elif mode == PER_ROW_BLOCK128:
+        s = np.empty((E, nblocks(K), N), np.float32)
+    else:
+        s = np.array([static_scale], np.float32)
+    lib().or_quantize_weights_int8(_p(w), E, N, K, mode, float(static_scale), _p(q),
+                                   _p(s) if mode != PER_TENSOR else None)
+    return q, s
+
+
 def quantize_rows_mx(x_bits):
     """MXFP8 (OCP MX v1.0): bf16 [rows, cols], cols a multiple of 32 ->
     (codes uint8 [rows, cols], E8M0 codes uint8 [rows, cols/32])."""
@@ -271,6 +292,29 @@ def gmm(lhs, lhs_scale, lhs_mode, rhs, rhs_scale, rhs_mode, group_sizes, group_o
     of = np.empty((nrows, N), np.float64) if want != "bf16" else None
     lib().or_gmm(_p(lhs), _p(_c(lhs_scale, np.float32)), lhs_mode, _p(rhs), _p(_c(rhs_scale, np.float32)),
                  rhs_mode, _p(sizes), E, group_offset, E_local, M, K, N, _p(r), nrows, _p(ob), _p(of))
+    return ob if want == "bf16" else of
+
+
+def gmm_w8(lhs, lhs_scale, lhs_mode, rhs, rhs_scale, rhs_mode, group_sizes, group_offset=0, E_local=None,
+           rows=None, want="bf16"):
+    """Grouped matmul with int8 weights rhs [E_local, N, K] (each code the
+    integer it holds); otherwise as gmm."""
+    lhs = _c(lhs, np.uint8)
+    rhs = _c(rhs, np.int8)
+    M, K = lhs.shape
+    El, N, K2 = rhs.shape
+    assert K2 == K
+    sizes = _c(group_sizes, np.int32)
+    E = len(sizes)
+    if E_local is None:
+        E_local = E - group_offset
+    assert El == E_local
+    r = None if rows is None else _c(rows, np.int64)
+    nrows = M if r is None else len(r)
+    ob = np.empty((nrows, N), np.uint16) if want == "bf16" else None
+    of = np.empty((nrows, N), np.float64) if want != "bf16" else None
+    lib().or_gmm_w8(_p(lhs), _p(_c(lhs_scale, np.float32)), lhs_mode, _p(rhs), _p(_c(rhs_scale, np.float32)),
+                    rhs_mode, _p(sizes), E, group_offset, E_local, M, K, N, _p(r), nrows, _p(ob), _p(of))
     return ob if want == "bf16" else of
 
 
@@ -497,13 +541,23 @@ def prepare_weights(w_in_bits, w_out_bits, w_mode, static=None):
     return qin, sin, w_mode, qo, so, w_mode
 
 
+def prepare_weights_w8(w_in_bits, w_out_bits, w_mode):
+    """int8 expert weights (per channel or blockwise), in prepare_weights' tuple."""
+    qin, sin = quantize_weights_int8(w_in_bits, w_mode)
+    qo, so = quantize_weights_int8(w_out_bits, w_mode)
+    return qin, sin, w_mode, qo, so, w_mode
+
+
 def ffn_forward(x_bits, topk_ids, topk_w, wq, E: int, act_mode: int, static=None, tokens=None):
     """Forward pass; returns a dict of every stage's outputs.
 
-    wq = prepare_weights(...).  With `tokens`, the gmm/SwiGLU/combine stages
-    are evaluated only on the rows those tokens route to (y[t] depends only
-    on x[t]), and the per-row stage outputs are returned for those rows."""
+    wq = prepare_weights(...) or prepare_weights_w8(...) (int8 weight codes:
+    both contractions then take gmm_w8).  With `tokens`, the
+    gmm/SwiGLU/combine stages are evaluated only on the rows those tokens
+    route to (y[t] depends only on x[t]), and the per-row stage outputs are
+    returned for those rows."""
     qin, sin, min_, qo, so, mo = wq
+    mm = gmm_w8 if np.asarray(qin).dtype == np.int8 else gmm
     T, D = x_bits.shape
     k = topk_ids.shape[1]
     sx = static["x"] if act_mode == PER_TENSOR else 1.0
@@ -514,11 +568,11 @@ def ffn_forward(x_bits, topk_ids, topk_w, wq, E: int, act_mode: int, static=None
     if tokens is not None:
         tokens = np.asarray(tokens, np.int64)
         rows = np.sort(pos.reshape(T, k)[tokens].reshape(-1)).astype(np.int64)
-    a = gmm(xs_q, xs_s, act_mode, qin, sin, min_, sizes, rows=rows)
+    a = mm(xs_q, xs_s, act_mode, qin, sin, min_, sizes, rows=rows)
     sh = static["h"] if act_mode == PER_TENSOR else 1.0
     h_q, h_s, h_b = swiglu_quant(a, act_mode, sh)
     if rows is None:
-        o = gmm(h_q, h_s, act_mode, qo, so, mo, sizes)
+        o = mm(h_q, h_s, act_mode, qo, so, mo, sizes)
         y = combine(o, pos, topk_w, k)
     else:
         # place the computed rows in a full-size o (other rows unused)
@@ -532,7 +586,7 @@ def ffn_forward(x_bits, topk_ids, topk_w, wq, E: int, act_mode: int, static=None
         elif act_mode == PER_ROW_BLOCK128:
             hs_full = np.ones((R, h_s.shape[1]), np.float32)
             hs_full[rows] = h_s
-        o_rows = gmm(hq_full, hs_full, act_mode, qo, so, mo, sizes, rows=rows)
+        o_rows = mm(hq_full, hs_full, act_mode, qo, so, mo, sizes, rows=rows)
         o = np.zeros((R, D), np.uint16)
         o[rows] = o_rows
         y = combine(o, pos, topk_w, k, tokens=tokens)

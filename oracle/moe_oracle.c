@@ -29,6 +29,10 @@
  *            "Microscaling Formats (MX) Specification" v1.0 (MXFP8: blocks of
  *            32 e4m3 elements along the contracted dimension sharing one
  *            power-of-two E8M0 scale).  Its functions are marked [MX].
+ *   [W8]     The int8-weight variant follows [Q-FUSE]'s other weight type
+ *            ("float8_e4m3fn (or int8)" with the same [E, blocks, 1, N]
+ *            scales): symmetric absmax codes in [-127, 127], activations and
+ *            h still e4m3.  Its functions are marked [W8].
  *
  * Arithmetic.  fp8 codes and bf16 values are decoded exactly to double and
  * every contraction accumulates in double.  Products of two e4m3 values carry
@@ -268,6 +272,61 @@ void or_quantize_weights(const uint16_t* w, int64_t E, int64_t N, int64_t K, int
 }
 
 /* ------------------------------------------------------------------------ */
+/* [W8] int8 weight quantisation ([Q-FUSE]: weights pre-quantised to int8   */
+/* with [E, blocks, 1, N] scales).  Symmetric absmax, the largest magnitude */
+/* mapping to 127:                                                          */
+/*   s = fp32(amax / 127), s = 1 when amax = 0;                             */
+/*   q = rint(fp32(x / s)) (nearest integer, ties to even), limited to      */
+/*       [-127, 127].                                                       */
+/* ------------------------------------------------------------------------ */
+
+static float int8_scale(float amax) {
+  if (amax == 0.0f) return 1.0f;
+  return amax / 127.0f;
+}
+
+static int8_t f32_to_int8(float v) {
+  float r = rintf(v); /* the default rounding mode: nearest, ties to even */
+  if (r > 127.0f) r = 127.0f;
+  if (r < -127.0f) r = -127.0f;
+  return (int8_t)r;
+}
+
+static void quantize_span_i8(const float* x, int64_t n, float s, int8_t* q) {
+  for (int64_t i = 0; i < n; ++i) q[i] = f32_to_int8(x[i] / s);
+}
+
+/* [W8] Expert weights w[E, N, K] -> int8 codes and fp32 scales, in the scale
+ * layouts of or_quantize_weights: per channel [E, N], blockwise
+ * [E, K/128, N], per tensor (static_scale; scale not written). */
+void or_quantize_weights_int8(const uint16_t* w, int64_t E, int64_t N, int64_t K, int mode, float static_scale,
+                              int8_t* q, float* scale) {
+  const int64_t nb = (K + 127) / 128;
+#pragma omp parallel for schedule(static)
+  for (int64_t row = 0; row < E * N; ++row) {
+    const int64_t e = row / N, n = row % N;
+    float* x = (float*)malloc(sizeof(float) * (size_t)K);
+    for (int64_t kk = 0; kk < K; ++kk) x[kk] = (float)or_bf16_to_f64(w[row * K + kk]);
+    int8_t* qr = q + row * K;
+    if (mode == OR_PER_ROW) {
+      const float s = int8_scale(amax_f32(x, K));
+      scale[row] = s;
+      quantize_span_i8(x, K, s, qr);
+    } else if (mode == OR_PER_ROW_BLOCK128) {
+      for (int64_t b = 0; b < nb; ++b) {
+        const int64_t c0 = b * 128, len = K - c0 < 128 ? K - c0 : 128;
+        const float s = int8_scale(amax_f32(x + c0, len));
+        scale[(e * nb + b) * N + n] = s;
+        quantize_span_i8(x + c0, len, s, qr + c0);
+      }
+    } else {
+      quantize_span_i8(x, K, static_scale, qr);
+    }
+    free(x);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
 /* [MX] MXFP8 quantisation (OCP MX v1.0, MXFP8 with E4M3 elements).  Each   */
 /* block of 32 consecutive values of a row shares the scale 2^X with        */
 /*   X = floor(log2(amax)) - 8,                                             */
@@ -402,7 +461,8 @@ static int group_of_row(const int64_t* starts, int E, int64_t m) {
 
 /* rows: optional list of nrows output rows to compute (NULL = all M rows).
  * out_bf16 / out_f64 (either may be NULL) are [nrows, N]. */
-static void gmm_core(const uint8_t* lhs, const void* lhs_scale, int lhs_mode, const uint8_t* rhs,
+/* rhs_int8: [W8] the rhs codes are int8 integers instead of e4m3 codes. */
+static void gmm_core(const uint8_t* lhs, const void* lhs_scale, int lhs_mode, const uint8_t* rhs, int rhs_int8,
                      const void* rhs_scale, int rhs_mode, const int32_t* group_sizes, int E, int g0, int E_local,
                      int64_t M, int64_t K, int64_t N, const int64_t* rows, int64_t nrows, uint16_t* out_bf16,
                      double* out_f64) {
@@ -435,7 +495,8 @@ static void gmm_core(const uint8_t* lhs, const void* lhs_scale, int lhs_mode, co
             int64_t el = g - g0;
             const uint8_t* wr = rhs + (el * N + n) * K;
             for (int64_t kk = 0; kk < K; ++kk)
-              w[kk] = or_e4m3_to_f64(wr[kk]) * rhs_scale_at(rhs_scale, rhs_mode, el, n, kk, N, K);
+              w[kk] = (rhs_int8 ? (double)(int8_t)wr[kk] : or_e4m3_to_f64(wr[kk])) *
+                      rhs_scale_at(rhs_scale, rhs_mode, el, n, kk, N, K);
             cur = g;
           }
           const double* ar = a + i * K;
@@ -455,8 +516,18 @@ static void gmm_core(const uint8_t* lhs, const void* lhs_scale, int lhs_mode, co
 void or_gmm(const uint8_t* lhs, const float* lhs_scale, int lhs_mode, const uint8_t* rhs, const float* rhs_scale,
             int rhs_mode, const int32_t* group_sizes, int E, int g0, int E_local, int64_t M, int64_t K, int64_t N,
             const int64_t* rows, int64_t nrows, uint16_t* out_bf16, double* out_f64) {
-  gmm_core(lhs, lhs_scale, lhs_mode, rhs, rhs_scale, rhs_mode, group_sizes, E, g0, E_local, M, K, N, rows, nrows,
-           out_bf16, out_f64);
+  gmm_core(lhs, lhs_scale, lhs_mode, rhs, 0, rhs_scale, rhs_mode, group_sizes, E, g0, E_local, M, K, N, rows,
+           nrows, out_bf16, out_f64);
+}
+
+/* [W8] The grouped matmul with int8 weights: deq(rhs)[e, n, k] = q[e, n, k] *
+ * s, the code taken as the integer it holds and s covering it (per channel,
+ * blockwise [E, K/128, N] or per tensor); lhs as in or_gmm. */
+void or_gmm_w8(const uint8_t* lhs, const float* lhs_scale, int lhs_mode, const int8_t* rhs, const float* rhs_scale,
+               int rhs_mode, const int32_t* group_sizes, int E, int g0, int E_local, int64_t M, int64_t K, int64_t N,
+               const int64_t* rows, int64_t nrows, uint16_t* out_bf16, double* out_f64) {
+  gmm_core(lhs, lhs_scale, lhs_mode, (const uint8_t*)rhs, 1, rhs_scale, rhs_mode, group_sizes, E, g0, E_local, M, K,
+           N, rows, nrows, out_bf16, out_f64);
 }
 
 /* [MX] The same grouped matmul on MXFP8 operands: lhs_sf [M, K/32] and
@@ -466,8 +537,8 @@ void or_gmm(const uint8_t* lhs, const float* lhs_scale, int lhs_mode, const uint
 void or_gmm_mx(const uint8_t* lhs, const uint8_t* lhs_sf, const uint8_t* rhs, const uint8_t* rhs_sf,
                const int32_t* group_sizes, int E, int g0, int E_local, int64_t M, int64_t K, int64_t N,
                const int64_t* rows, int64_t nrows, uint16_t* out_bf16, double* out_f64) {
-  gmm_core(lhs, lhs_sf, OR_MX32, rhs, rhs_sf, OR_MX32, group_sizes, E, g0, E_local, M, K, N, rows, nrows, out_bf16,
-           out_f64);
+  gmm_core(lhs, lhs_sf, OR_MX32, rhs, 0, rhs_sf, OR_MX32, group_sizes, E, g0, E_local, M, K, N, rows, nrows,
+           out_bf16, out_f64);
 }
 
 /* The same contraction on double operands (no quantisation), used to pin

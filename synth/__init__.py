@@ -42,6 +42,7 @@ class MoEConfig:
     w_mode: int     # weight scale mode: PER_ROW = per channel, PER_ROW_BLOCK128 = blockwise
     routing: str    # "normal", "uniform" or "zipf"
     backward: bool = False
+    w_int8: bool = False  # weight codes int8 instead of e4m3 (activations stay e4m3)
 
     @property
     def R(self) -> int:
@@ -60,6 +61,11 @@ CONFIGS = {
     # weights all in MXFP8)
     "dsv3_mx": MoEConfig("dsv3_mx", 16384, 7168, 256, 8, 2048, MX32, MX32, "normal"),
     "mixtral_mx": MoEConfig("mixtral_mx", 8192, 4096, 8, 2, 14336, MX32, MX32, "uniform"),
+    # int8 weights (per channel; blockwise for the prefill chunk) with e4m3
+    # activations and h, on two of the shapes above
+    "mixtral_w8": MoEConfig("mixtral_w8", 8192, 4096, 8, 2, 14336, PER_ROW, PER_ROW, "uniform", w_int8=True),
+    "prefill_w8": MoEConfig("prefill_w8", 2048, 2048, 128, 8, 768, PER_ROW, PER_ROW_BLOCK128, "normal",
+                            w_int8=True),
 }
 
 
