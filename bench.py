@@ -12,7 +12,8 @@ Timed in the same run and reported as sub-objects of the same line
   d_ff=14336, per-token / per-channel scales);
 - the serving prefill chunk (T=2048, d_model=2048, 128 experts, top-8,
   d_ff=768, pre-quantised blockwise weights);
-- the MXFP8 variant of the DeepSeek-V3-shaped layer.
+- the MXFP8 variant of the DeepSeek-V3-shaped layer;
+- the int8-weight variants of the Mixtral-shaped layer and the prefill chunk.
 
 Prints one JSON line (rank 0).  Launch with torchrun for several GPUs: every
 rank runs its own batch (data parallel over tokens, no collective on the data
@@ -50,7 +51,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="dsv3", choices=list(synth.CONFIGS))
-    ap.add_argument("--secondary", default="mixtral,prefill,dsv3_mx",
+    ap.add_argument("--secondary", default="mixtral,prefill,dsv3_mx,mixtral_w8,prefill_w8",
                     help="comma-separated configs timed in the same run after the main one (at most 50 steps "
                          "each), reported as sub-objects: 'secondary' (the first) and 'secondaries' (all); "
                          "'' for none")
@@ -79,7 +80,8 @@ def workload_name(cfg) -> str:
     modes = {0: "per-token", 1: "per-token-per-128", 2: "static", 4: "MXFP8 (E8M0 per 32 columns)"}
     wmodes = {0: "per-channel", 1: "blockwise [E, K/128, N]", 2: "static", 4: "MXFP8 (E8M0 per 32 of K)"}
     return (f"{cfg.name} MoE expert FFN fwd: T={cfg.T} d_model={cfg.D} E={cfg.E} top-k={cfg.k} d_ff={cfg.F} SwiGLU; "
-            f"e4m3 {modes[cfg.act_mode]} activation scales, {wmodes[cfg.w_mode]} weight scales")
+            f"e4m3 {modes[cfg.act_mode]} activation scales, {wmodes[cfg.w_mode]} weight scales"
+            + ("; int8 weight codes" if cfg.w_int8 else ""))
 
 
 def fwd_flops(cfg) -> dict:
@@ -230,8 +232,12 @@ class OracleSample:
         self.oracle = oracle
         self.cfg, self.x, self.static = cfg, x_bits, static
         self.mx = cfg.act_mode == synth.MX32
-        self.wq = (oracle.prepare_weights_mx(w_in_bits, w_out_bits) if self.mx else
-                   oracle.prepare_weights(w_in_bits, w_out_bits, cfg.w_mode, static))
+        if self.mx:
+            self.wq = oracle.prepare_weights_mx(w_in_bits, w_out_bits)
+        elif cfg.w_int8:
+            self.wq = oracle.prepare_weights_w8(w_in_bits, w_out_bits, cfg.w_mode)
+        else:
+            self.wq = oracle.prepare_weights(w_in_bits, w_out_bits, cfg.w_mode, static)
         remap = -np.ones(cfg.E, np.int64)
         remap[np.asarray(experts)] = np.arange(len(experts))
         loc = remap[ids]
@@ -301,7 +307,8 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
     # inputs: each rank its own batch (seed = rank)
     x_host, ids_np, w_np = host_inputs(cfg, seed=rank)
     w_in, w_out = synth.expert_weights(cfg, 0, device=dev)
-    W = moe.prepare_weights(w_in, w_out, cfg.w_mode, static)
+    W = (moe.prepare_weights_w8(w_in, w_out, cfg.w_mode) if cfg.w_int8 else
+         moe.prepare_weights(w_in, w_out, cfg.w_mode, static))
     torch.cuda.synchronize()
     cpu_sample = None
     if rank == 0 and not args.no_cpu_baseline and not secondary:
@@ -319,6 +326,7 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
     stream = torch.cuda.current_stream()
 
     mx = cfg.act_mode == synth.MX32
+    w8 = cfg.w_int8
 
     def step(ev=None):
         if ev is None:
@@ -338,6 +346,16 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
         s = moe.quantize_sort(x, ids, E, cfg.act_mode, sx, out=buf.sort)
         xs_s = s["xs_scale"] if cfg.act_mode != 2 else sx
         ev[0].record(stream)
+        if w8:
+            moe.gmm_w8(s["xs_q"], xs_s, cfg.act_mode, W.w_in, W.s_in, W.in_mode, s["group_sizes"], out=buf.a)
+            ev[1].record(stream)
+            moe.swiglu_quant(buf.a, cfg.act_mode, sh, h_q=buf.h_q, h_scale=buf.h_s)
+            h_s = buf.h_s if cfg.act_mode != 2 else sh
+            ev[2].record(stream)
+            moe.gmm_w8(buf.h_q, h_s, cfg.act_mode, W.w_out, W.s_out, W.out_mode, s["group_sizes"], out=buf.o)
+            ev[3].record(stream)
+            moe.ragged_gather_reduce(buf.o, s["pos"], w, cfg.k, out=buf.y)
+            return buf.y
         if moe.swiglu_fuse_pays(cfg.act_mode, W.in_mode, cfg.F):
             moe.gmm_swiglu(s["xs_q"], xs_s, cfg.act_mode, W.w_in, W.s_in, W.in_mode, s["group_sizes"], cfg.act_mode,
                            sh, h=buf.h, h_q=buf.h_q, h_scale=buf.h_s)
@@ -446,7 +464,7 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
                "note": "public ffn_forward per step; inputs copied in from pinned host memory and y copied out "
                        "every step, on their own streams, double-buffered across steps"}
 
-    fused = mx or moe.swiglu_fuse_pays(cfg.act_mode, W.in_mode, cfg.F)
+    fused = mx or (not w8 and moe.swiglu_fuse_pays(cfg.act_mode, W.in_mode, cfg.F))
     # quantise + sort 4 (histogram, scan, scatter, quantise-gather) + (fused gmm+SwiGLU 1, +1 code
     # pass for per-row h scales | gmm 1 + SwiGLU 1) + gmm 1 + combine 1
     launches_per_step = 4 + ((1 + (1 if cfg.act_mode == 0 else 0)) if fused else 2) + 1 + 1
@@ -454,8 +472,11 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
     g_in = float(np.mean([a for a, _ in gmm_ms]))
     g_out = float(np.mean([b for _, b in gmm_ms]))
     pk, pk_kind = peaks()
-    # the timed region is well under a second of GPU time: the burst figure applies
+    # the timed region is well under a second of GPU time: the burst figure
+    # applies; the int8-weight contractions run on the f16 MMA, whose dense
+    # rate is the bf16 one
     fp8_peak = 2.0 * pk["bf16_tflops"]
+    tc_peak = pk["bf16_tflops"] if w8 else fp8_peak
     # the dominant call of the step is the wi_0 | wi_1 contraction; it is
     # bound by whichever of its flops (fp8 peak) and its bytes (HBM) takes
     # longer: the weight stream binds the small prefill batch
@@ -469,13 +490,14 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
               synth.PER_ROW_BLOCK128: 4 * cfg.E * (cfg.D // 128) * 2 * cfg.F}.get(cfg.w_mode, 0)
         out = (5 if cfg.act_mode == synth.PER_ROW else 1) * R * cfg.F if fused else 4 * R * cfg.F
         nbytes = R * cfg.D + cfg.E * 2 * cfg.F * cfg.D + out + sa + sw
-    hbm_bound = nbytes / (pk["hbm_gbs"] * 1e9) > fl["gmm_in"] / (fp8_peak * 1e12)
+    hbm_bound = nbytes / (pk["hbm_gbs"] * 1e9) > fl["gmm_in"] / (tc_peak * 1e12)
     if hbm_bound:
         achieved, peak, unit = nbytes / (g_in / 1e3) / 1e9, pk["hbm_gbs"], "GB/s"
     else:
-        achieved, peak, unit = fl["gmm_in"] / (g_in / 1e3) / 1e12, fp8_peak, "TFLOP/s"
+        achieved, peak, unit = fl["gmm_in"] / (g_in / 1e3) / 1e12, tc_peak, "TFLOP/s"
     both = (fl["gmm_in"] + fl["gmm_out"]) / ((g_in + g_out) / 1e3) / 1e12
-    kname = "gmm_fp8_mx_swiglu" if mx else ("gmm_fp8_swiglu" if fused else "gmm_fp8 (wi_0|wi_1)")
+    kname = ("gmm_fp8_mx_swiglu" if mx else "gmm_fp8_w8 (wi_0|wi_1)" if w8 else
+             "gmm_fp8_swiglu" if fused else "gmm_fp8 (wi_0|wi_1)")
     result = {
         "metric": METRIC,
         "value": cfg.T * world / (ms / 1e3),
@@ -488,7 +510,8 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": ("e4m3 with E8M0 block scales (MXFP8), fp32 accumulate, bf16 in/out" if mx else
-                  "e4m3 (fp32 accumulate, bf16 in/out)"),
+                  "e4m3 activations x int8 weights on the f16 tensor-core MMA (both exact in f16), fp32 "
+                  "accumulate, bf16 in/out" if w8 else "e4m3 (fp32 accumulate, bf16 in/out)"),
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, random-init)",
         "config": {"workload": workload_name(cfg), "tokens_per_gpu": cfg.T, "parallelism": f"dp{world} (replicas)",
                    "l2": "inputs larger than L2: fp8 expert weights %.2f GB streamed every step"
@@ -497,15 +520,19 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
                      "peak": peak, "unit": unit, "frac": achieved / peak,
                      "traffic": recorded_traffic(kname, cfg) if not (args.tokens or args.experts) else None,
                      "peak_note": (f"of {pk_kind}: STREAM-style copy" if hbm_bound else
+                                   f"of {pk_kind}: f16 = burst bf16 cuBLAS ({pk['bf16_tflops']} TFLOP/s; the "
+                                   "nominal dense f16 and bf16 rates are equal)" if w8 else
                                    f"of {pk_kind}: fp8 = 2 x burst bf16 cuBLAS ({pk['bf16_tflops']} TFLOP/s; "
                                    "the nominal dense fp8 / bf16 ratio is 2)"),
                      "flops_per_call": fl["gmm_in"], "algorithmic_bytes_per_call": nbytes, "ms_per_call": g_in,
                      "note": ("one gmm_fp8_mx_swiglu call per step: the block-scaled tcgen05 contraction with the "
                               "SwiGLU and MXFP8 requantisation epilogue") if mx else
+                             ("one gmm_fp8_w8 call per step: int8 weights converted to f16 into tensor memory, "
+                              "e4m3 activations to f16 in shared memory, tcgen05 kind::f16") if w8 else
                              ("one gmm_fp8_swiglu call per step: the tcgen05 contraction with the SwiGLU and "
                               "requantisation epilogue, plus the h code pass of the per-token scales") if fused else
                              "one gmm_fp8 call per step"},
-        "gmm_fp8_both": {"achieved": both, "frac": both / fp8_peak, "unit": "TFLOP/s", "gmm_in_ms": g_in,
+        "gmm_fp8_both": {"achieved": both, "frac": both / tc_peak, "unit": "TFLOP/s", "gmm_in_ms": g_in,
                          "gmm_out_ms": g_out, "note": "both contractions of the step, timed with events"},
         "gpu_launches": launches_per_step * steps,
         "clocks": clk,
@@ -646,7 +673,8 @@ def run_suite(args):
             sh = torch.tensor([static["h"]], dtype=torch.float32, device=dev)
         x_host, ids_np, w_np = host_inputs(cfg, 0)
         w_in, w_out = synth.expert_weights(cfg, 0, device=dev)
-        W = moe.prepare_weights(w_in, w_out, cfg.w_mode, static, for_backward=cfg.backward)
+        W = (moe.prepare_weights_w8(w_in, w_out, cfg.w_mode) if cfg.w_int8 else
+             moe.prepare_weights(w_in, w_out, cfg.w_mode, static, for_backward=cfg.backward))
         del w_in, w_out
         torch.cuda.empty_cache()
         x = x_host.to(dev)
@@ -654,8 +682,9 @@ def run_suite(args):
         w = torch.from_numpy(w_np).to(dev)
         buf = moe.FFNBuffers(T, D, E, k, F, cfg.act_mode, dev, backward=cfg.backward)
         am = cfg.act_mode
-        fused = moe.swiglu_fuse_pays(am, W.in_mode, F)
-        fusable = moe.swiglu_fusable(am, W.in_mode, F)
+        w8 = cfg.w_int8
+        fused = not w8 and moe.swiglu_fuse_pays(am, W.in_mode, F)
+        fusable = not w8 and moe.swiglu_fusable(am, W.in_mode, F)
         moe.ffn_forward(x, ids, w, W, am, buf, sx, sh)  # fills every intermediate
         torch.cuda.synchronize()
         nb = lambda c: (c + 127) // 128
@@ -682,7 +711,20 @@ def run_suite(args):
                                                  buf.sort["group_sizes"], am, sh, h=buf.h, h_q=buf.h_q,
                                                  h_scale=buf.h_s, a_out=buf.a if buf.keep_a else None),
                           "tensor", (2.0 * R * D * 2 * F, R * D + E * 2 * F * D + (5 if am == 0 else 1) * R * F)))
-        if am != synth.MX32:
+        if w8:
+            # the weight scales: per channel [E, N] or blockwise [E, K/128, N]
+            ws = lambda N_, K_: 4 * E * N_ * (1 if cfg.w_mode == synth.PER_ROW else nb(K_))
+            calls.append(("gmm_fp8_w8 wi_0|wi_1", lambda: moe.gmm_w8(buf.sort["xs_q"], xs_s, am, W.w_in, W.s_in,
+                                                                    W.in_mode, buf.sort["group_sizes"], out=buf.a),
+                          "tensor_f16", (2.0 * R * D * 2 * F, R * D + E * 2 * F * D + 4 * R * F + sbytes(R, D)
+                                         + ws(2 * F, D))))
+            calls.append(("moe_swiglu_quant", lambda: moe.swiglu_quant(buf.a, am, sh, h_q=buf.h_q,
+                                                                       h_scale=buf.h_s),
+                          "hbm", 5 * R * F + sbytes(R, F)))
+            calls.append(("gmm_fp8_w8 wo", lambda: moe.gmm_w8(buf.h_q, h_s, am, W.w_out, W.s_out, W.out_mode,
+                                                             buf.sort["group_sizes"], out=buf.o),
+                          "tensor_f16", (2.0 * R * F * D, R * F + E * D * F + 2 * R * D + sbytes(R, F) + ws(D, F))))
+        elif am != synth.MX32:
             calls.append(("gmm_fp8 wi_0|wi_1", lambda: moe.gmm(buf.sort["xs_q"], xs_s, am, W.w_in, W.s_in,
                                                                W.in_mode, buf.sort["group_sizes"], out=buf.a),
                           "tensor", (2.0 * R * D * 2 * F, R * D + E * 2 * F * D + 4 * R * F)))
@@ -749,7 +791,7 @@ def run_suite(args):
             ms = timed(fn)
             if bound == "hbm":
                 ach, peak, unit = work / (ms / 1e3) / 1e9, hbm, "GB/s"
-            elif bound == "tensor_bf16":
+            elif bound in ("tensor_bf16", "tensor_f16"):  # the f16 and bf16 MMAs have one dense rate
                 flops, nbytes = work
                 if nbytes / (hbm * 1e9) > flops / (pk["bf16_tflops"] * 1e12):
                     bound, ach, peak, unit = "hbm", nbytes / (ms / 1e3) / 1e9, hbm, "GB/s"

@@ -7,7 +7,9 @@ arithmetic runs in the library's CUDA kernels; there is no fallback.
 
 Forward path (the order of "Quantize activations before EP all gather"):
 quantize_rows -> ragged_sort -> gmm (wi_0 | wi_1) -> swiglu_quant ->
-gmm (wo) -> ragged_gather_reduce.  The backward pass of the static scheme
+gmm (wo) -> ragged_gather_reduce.  With int8 expert weights ("Keep qwix out
+of tpu-inference's fused MoE kernel and pre-quantize weights": float8_e4m3fn
+or int8 weights) both contractions run gmm_w8.  The backward pass of the static scheme
 ("Support quantization for tokamax gmm v2": fp8_static_wa) adds
 gather_scale_quant, swiglu_bwd_quant, quantize_group_cols and tgmm.
 
@@ -39,7 +41,7 @@ __all__ = [
     "quantize_rows", "quantize_weights", "ragged_sort", "gmm", "gmm_swiglu", "swiglu_fusable", "swiglu_fuse_pays", "swiglu_quant", "ragged_gather_reduce",
     "gather_scale_quant", "swiglu_bwd_quant", "quantize_group_cols", "tgmm", "transpose_u8",
     "router_topk", "router_backward", "MX32", "quantize_rows_mx", "quantize_weights_mx", "quantize_sort_mx",
-    "gmm_mx", "gmm_mx_swiglu", "swiglu_quant_mx",
+    "gmm_mx", "gmm_mx_swiglu", "swiglu_quant_mx", "quantize_weights_int8", "gmm_w8", "prepare_weights_w8",
     "ExpertWeights", "prepare_weights", "FFNBuffers", "ffn_forward", "ffn_backward",
 ]
 
@@ -109,6 +111,21 @@ def quantize_weights(w: torch.Tensor, mode: int, static_scale: Optional[torch.Te
         s = None
     check(lib().moe_quantize_weights(_p(w), E, N, K, mode, _p(static_scale), _p(q), _p(s), _s()),
           "moe_quantize_weights")
+    return q, s
+
+
+def quantize_weights_int8(w: torch.Tensor, mode: int, static_scale: Optional[torch.Tensor] = None):
+    """bf16 [E, N, K] -> (int8 codes [E, N, K], scales [E, N] | [E, K/128, N] | None)."""
+    E, N, K = w.shape
+    q = torch.empty(E, N, K, dtype=torch.int8, device=w.device)
+    if mode == PER_ROW:
+        s = torch.empty(E, N, dtype=torch.float32, device=w.device)
+    elif mode == PER_ROW_BLOCK128:
+        s = torch.empty(E, _nb(K), N, dtype=torch.float32, device=w.device)
+    else:
+        s = None
+    check(lib().moe_quantize_weights_int8(_p(w), E, N, K, mode, _p(static_scale), _p(q), _p(s), _s()),
+          "moe_quantize_weights_int8")
     return q, s
 
 
@@ -260,6 +277,23 @@ def gmm(lhs_q, lhs_scale, lhs_mode, rhs_q, rhs_scale, rhs_mode, group_sizes, gro
     out = torch.empty(M, N, dtype=torch.bfloat16, device=lhs_q.device) if out is None else out
     check(lib().gmm_fp8(_p(lhs_q), _p(lhs_scale), lhs_mode, _p(rhs_q), _p(rhs_scale), rhs_mode, _p(group_sizes),
                         E, group_offset, E_local, M, K, N, _p(out), _s()), "gmm_fp8")
+    return out
+
+
+def gmm_w8(lhs_q, lhs_scale, lhs_mode, rhs_q, rhs_scale, rhs_mode, group_sizes, group_offset: int = 0,
+           E_local: Optional[int] = None, out=None):
+    """Grouped matmul with int8 weights rhs_q [E_local, N, K] -> bf16 [M, N]."""
+    M, K = lhs_q.shape
+    El, N, K2 = rhs_q.shape
+    if K2 != K:
+        raise MoEError("lhs/rhs K mismatch")
+    if rhs_q.dtype != torch.int8:
+        raise MoEError("gmm_w8 takes int8 weight codes")
+    E = group_sizes.numel()
+    E_local = El if E_local is None else E_local
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=lhs_q.device) if out is None else out
+    check(lib().gmm_fp8_w8(_p(lhs_q), _p(lhs_scale), lhs_mode, _p(rhs_q), _p(rhs_scale), rhs_mode,
+                           _p(group_sizes), E, group_offset, E_local, M, K, N, _p(out), _s()), "gmm_fp8_w8")
     return out
 
 
@@ -523,6 +557,16 @@ def prepare_weights(w_in: torch.Tensor, w_out: torch.Tensor, w_mode: int, static
     return ExpertWeights(qin, sin, w_mode, qo, so, w_mode)
 
 
+def prepare_weights_w8(w_in: torch.Tensor, w_out: torch.Tensor, w_mode: int) -> ExpertWeights:
+    """int8 expert weights (per channel or blockwise), quantised once outside
+    the timed FFN; ffn_forward then runs both contractions with gmm_w8."""
+    if w_mode not in (PER_ROW, PER_ROW_BLOCK128):
+        raise MoEError("int8 weights take per-channel or blockwise scales")
+    qin, sin = quantize_weights_int8(w_in, w_mode)
+    qo, so = quantize_weights_int8(w_out, w_mode)
+    return ExpertWeights(qin, sin, w_mode, qo, so, w_mode)
+
+
 class FFNBuffers:
     """Every intermediate of one forward (and backward) pass, allocated once."""
 
@@ -572,6 +616,9 @@ def ffn_forward(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, W
         gmm_mx(buf.h_q, buf.h_s, W.w_out, W.s_out, s["group_sizes"], out=buf.o)
         ragged_gather_reduce(buf.o, s["pos"], topk_w, k, out=buf.y)
         return buf.y
+    w8 = W.w_in.dtype == torch.int8
+    if w8 and act_mode not in (PER_ROW, PER_TENSOR):
+        raise MoEError("int8 weights take per-token or static activation scales")
     if fuse_quant_sort:
         s = quantize_sort(x, topk_ids, E, act_mode, static_x, out=buf.sort)
     else:
@@ -579,14 +626,17 @@ def ffn_forward(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, W
         s = ragged_sort(topk_ids, E, buf.x_q, buf.x_s if act_mode != PER_TENSOR else static_x, act_mode,
                         out=buf.sort)
     xs_s = s["xs_scale"] if act_mode != PER_TENSOR else static_x
-    if fuse_swiglu and swiglu_fuse_pays(act_mode, W.in_mode, buf.F):
+    if w8:
+        gmm_w8(s["xs_q"], xs_s, act_mode, W.w_in, W.s_in, W.in_mode, s["group_sizes"], out=buf.a)
+        swiglu_quant(buf.a, act_mode, static_h, h_q=buf.h_q, h_scale=buf.h_s)
+    elif fuse_swiglu and swiglu_fuse_pays(act_mode, W.in_mode, buf.F):
         gmm_swiglu(s["xs_q"], xs_s, act_mode, W.w_in, W.s_in, W.in_mode, s["group_sizes"], act_mode, static_h,
                    a_out=buf.a if buf.keep_a else None, h=buf.h, h_q=buf.h_q, h_scale=buf.h_s)
     else:
         gmm(s["xs_q"], xs_s, act_mode, W.w_in, W.s_in, W.in_mode, s["group_sizes"], out=buf.a)
         swiglu_quant(buf.a, act_mode, static_h, h_q=buf.h_q, h_scale=buf.h_s)
     h_s = buf.h_s if act_mode != PER_TENSOR else static_h
-    gmm(buf.h_q, h_s, act_mode, W.w_out, W.s_out, W.out_mode, s["group_sizes"], out=buf.o)
+    (gmm_w8 if w8 else gmm)(buf.h_q, h_s, act_mode, W.w_out, W.s_out, W.out_mode, s["group_sizes"], out=buf.o)
     ragged_gather_reduce(buf.o, s["pos"], topk_w, k, out=buf.y)
     return buf.y
 

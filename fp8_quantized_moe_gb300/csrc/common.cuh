@@ -106,6 +106,17 @@ __device__ __forceinline__ uint2 pack_e4m3x8(const float* v) {
 // Absmax scale in fp32: amax / 448, or 1 for an all-zero span.
 __device__ __forceinline__ float absmax_scale(float amax) { return amax > 0.0f ? __fdiv_rn(amax, kE4M3Max) : 1.0f; }
 
+// int8 weights: symmetric absmax scale amax / 127 (1 for an all-zero span),
+// and eight quotients -> the nearest integers (ties to even) limited to
+// [-127, 127], as int8 bytes in little-endian order.
+__device__ __forceinline__ float int8_scale(float amax) { return amax > 0.0f ? __fdiv_rn(amax, 127.0f) : 1.0f; }
+__device__ __forceinline__ uint2 pack_i8x8(const float* v) {
+  uint32_t b[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) b[j] = static_cast<uint32_t>(min(127, max(-127, __float2int_rn(v[j])))) & 0xFFu;
+  return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+}
+
 // MXFP8 (OCP MX v1.0) shared exponent of a 32-value block: floor(log2(amax))
 // - 8, clamped to [-127, 127], -127 for amax = 0.  Read off the fp32 exponent
 // field: a normal amax = 1.f * 2^(field - 127); every subnormal (and zero)
@@ -626,6 +637,19 @@ __device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t 
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 with f16 A and B, one CTA:
+// the A operand (M = 128 rows, K = 16) is read from tensor memory, row m in
+// lane m and elements 2c, 2c + 1 of K in column c (low, high half).
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation this thread issued so far has
 // completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -695,6 +719,22 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16_pairs(uint32_t taddr, uint64_
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 32 lanes x 32 consecutive 32-bit columns from registers: thread i of the
+// warp writes the 32 columns of TMEM lane (lane base + i).
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+// The tensor-memory stores this thread issued have completed.
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Shared-memory matrix descriptor for a K-major operand tile stored with the
 // 128-byte swizzle (rows of 128 bytes, 8-row / 1024-byte swizzle atoms, tile
 // base 1024-byte aligned): start address >> 4 in bits [0,14), leading byte
@@ -730,6 +770,12 @@ __device__ __forceinline__ uint64_t smem_desc_plain(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_mx_e4m3(int m, int n, int a_sf_id, int b_sf_id) {
   return (static_cast<uint32_t>(b_sf_id) << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
          (static_cast<uint32_t>(m >> 4) << 24) | (static_cast<uint32_t>(a_sf_id) << 29);
+}
+
+// Instruction descriptor for kind::f16 with f16 A and B (format 0), fp32
+// accumulator, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 // Instruction descriptor for kind::f16 with bf16 A and B (format 1 in bits

@@ -43,6 +43,7 @@
 // Every wait is bounded (mbarrier try_wait + %globaltimer); on expiry the
 // kernel raises MOE_DEVERR_TIMEOUT, drains what it issued and returns.
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 #include <atomic>
@@ -299,8 +300,8 @@ __device__ __forceinline__ void warp_store_32x64B(uint8_t* stg, const uint32_t (
 // the tables for the local groups [g0, g0 + El).  Returns (in ctl->err) 1 if a
 // size is negative or the sizes do not add up to M.  With PAIR a unit of work
 // is a pair of M tiles (one per CTA of the pair).
-template <bool TGMM, bool PAIR>
-__device__ void build_group_tables(const Params& p, SmemCtl* ctl) {
+template <bool TGMM, bool PAIR, class Ctl>
+__device__ void build_group_tables(const Params& p, Ctl* ctl) {
   const int lane = threadIdx.x & 31;
   int v[kMaxGroups / 32];
 #pragma unroll
@@ -371,8 +372,8 @@ struct Tile {
   int n0;       // first output column
 };
 
-template <int MODE, bool PAIR>
-__device__ __forceinline__ Tile get_tile(const Params& p, const SmemCtl* ctl, int t, int rank) {
+template <int MODE, bool PAIR, class Ctl>
+__device__ __forceinline__ Tile get_tile(const Params& p, const Ctl* ctl, int t, int rank) {
   Tile tl;
   constexpr int BN = Cfg<MODE, PAIR>::BN;
   if (MODE == kTgmm) {
@@ -1499,6 +1500,9 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
               }
             }
             if (FM != 1) {  // this warp is done with the scale row
+              // the row is refilled by a bulk copy (the async proxy): order
+              // this warp's generic reads of it before that write
+              fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) mbar_arrive(smem_u32(&ctl->sempty[q]));
             }
@@ -1680,6 +1684,414 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
       tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
     else
       tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+  if (threadIdx.x == 0 && ctl->err) raise_error(&g_err, MOE_DEVERR_TIMEOUT);
+}
+
+// ---- int8 weights (gmm_fp8_w8) ---------------------------------------------
+// out[m, n] = s_x s_w sum_k e4m3(x)[m, k] q[g(m), n, k] in bf16: gmm_fp8 with
+// the other weight type of "Keep qwix out of tpu-inference's fused MoE
+// kernel and pre-quantize weights" (int8 codes with [E, blocks, 1, N]
+// scales).  No tcgen05 MMA kind multiplies e4m3 by int8, but f16 holds every
+// e4m3 value and every integer in [-127, 127] exactly, so both operands are
+// converted to f16 on the SM and contracted by tcgen05.mma kind::f16 with
+// fp32 accumulation:
+//   - the weights are the A operand, read from tensor memory: eight warps
+//     turn each stage's int8 rows into f16 (the byte under the exponent of
+//     1024 + 128, then one f16 subtraction) and store them with tcgen05.st,
+//     so the converted weights never pass through shared memory;
+//   - the activations are the B operand: four warps turn the stage's e4m3
+//     rows into f16 (cvt.f16x2.e4m3x2) in the 128-byte-swizzled K-major
+//     layout the MMA reads from shared memory.
+// A tile is 256 channels (two M = 128 MMAs into two tensor-memory
+// accumulators whose lanes are channels) by 128 tokens (the MMA's N); the
+// epilogue applies s_x s_w and writes the transposed accumulators, 32
+// channels of one token row a store.  Blockwise weight scales: each block
+// scale is divided by the channel's largest one, S, and the quotient r, held
+// as an f16 pair r_hi + r_lo (r to about 22 bits), multiplies the block's
+// converted codes in one fused f16 multiply-add, q r_hi + (q r_lo), so each
+// converted weight q r carries a single f16 rounding; S leaves the sum, and
+// one accumulator runs over the whole K loop.
+constexpr int kW8Tok = 128;                     // tokens per tile: the MMA's N
+constexpr int kW8Ks = 64;                       // K per stage: 64 code bytes, one 128-byte f16 row
+constexpr int kW8BoxBytes = 128 * kW8Ks;        // one TMA box: 128 rows x 64 bytes (64-byte swizzle)
+constexpr int kW8RawStages = 6;                 // TMA ring: two weight boxes and one activation box a stage
+constexpr int kW8RawBytes = 3 * kW8BoxBytes;
+constexpr int kW8XStages = 4;                   // ring of converted (f16) activation tiles
+constexpr int kW8XBytes = kW8Tok * kW8Ks * 2;
+constexpr int kW8AStages = 4;                   // tensor-memory ring of converted weights, 64 columns a stage
+constexpr int kW8AColBase = 2 * kW8Tok;         // after the two accumulators
+constexpr int kW8WConvWarps = 8, kW8XConvWarps = 4, kW8EpiWarps = 8;
+// warp 0 TMA producer, 1 MMA issuer, 2..9 weight converters, 10..13
+// activation converters, 14..21 epilogue
+constexpr int kW8Warps = 2 + kW8WConvWarps + kW8XConvWarps + kW8EpiWarps;
+constexpr uint32_t kW8Idesc = idesc_f16_f32(128, kW8Tok);
+static_assert(kW8AColBase + 64 * kW8AStages <= 512, "int8-weight tensor-memory plan");
+
+struct W8Ctl {
+  uint64_t rfull[kW8RawStages];   // a stage's three boxes have landed
+  uint64_t rempty[kW8RawStages];  // every converter warp has read the stage
+  uint64_t afull[kW8AStages];     // converted weights are in tensor memory
+  uint64_t aempty[kW8AStages];    // the MMAs that read them completed
+  uint64_t xfull[kW8XStages];     // converted activations are in shared memory
+  uint64_t xempty[kW8XStages];
+  uint64_t dfull, dempty;         // the accumulators hold a finished tile / have been read
+  uint64_t drain;
+  uint64_t never;  // test hook: a barrier that nothing arrives on
+  uint32_t tmem_base;
+  int abort_flag;
+  int no_abort;
+  int err;
+  int total_tiles;
+  int gstart[kMaxGroups + 1];
+  int tile_prefix[kMaxGroups + 1];
+  int gsize[kMaxGroups];
+};
+constexpr size_t kW8Smem =
+    1024 + static_cast<size_t>(kW8RawStages) * kW8RawBytes + static_cast<size_t>(kW8XStages) * kW8XBytes + sizeof(W8Ctl);
+static_assert(kW8Smem <= 232448, "int8-weight gmm: shared memory per CTA");
+
+// Blockwise weight scales of one channel: 1 / (its largest block scale), 0
+// for a channel past N or one whose scales are all zero.
+__device__ __forceinline__ float w8_block_smax(const float* s_blk, int kblocks, int N, bool ok) {
+  float m = 0.0f;
+  if (ok)
+    for (int kb = 0; kb < kblocks; ++kb) m = fmaxf(m, __ldg(s_blk + static_cast<int64_t>(kb) * N));
+  return m;
+}
+
+__global__ void __launch_bounds__(kW8Warps * 32, 1)
+    w8_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_addr);
+  const uint32_t xring = base + kW8RawStages * kW8RawBytes;
+  W8Ctl* ctl = reinterpret_cast<W8Ctl*>(base_ptr + kW8RawStages * kW8RawBytes + kW8XStages * kW8XBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (warp == 0) build_group_tables<false, false>(p, ctl);
+  if (threadIdx.x == 32) {
+    for (int s = 0; s < kW8RawStages; ++s) {
+      mbar_init(smem_u32(&ctl->rfull[s]), 1);
+      mbar_init(smem_u32(&ctl->rempty[s]), kW8WConvWarps + kW8XConvWarps);
+    }
+    for (int a = 0; a < kW8AStages; ++a) {
+      mbar_init(smem_u32(&ctl->afull[a]), kW8WConvWarps);
+      mbar_init(smem_u32(&ctl->aempty[a]), 1);
+    }
+    for (int x = 0; x < kW8XStages; ++x) {
+      mbar_init(smem_u32(&ctl->xfull[x]), kW8XConvWarps);
+      mbar_init(smem_u32(&ctl->xempty[x]), 1);
+    }
+    mbar_init(smem_u32(&ctl->dfull), 1);
+    mbar_init(smem_u32(&ctl->dempty), kW8EpiWarps);
+    mbar_init(smem_u32(&ctl->drain), 1);
+    mbar_init(smem_u32(&ctl->never), 1);
+    ctl->abort_flag = 0;
+    ctl->no_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (ctl->err) {
+    if (threadIdx.x == 0) raise_error(&g_err, MOE_DEVERR_GROUP_SIZES);
+    return;
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+  const int total = ctl->total_tiles;
+  const int nks = (p.K + kW8Ks - 1) / kW8Ks;
+  const bool w_blk = p.rhs_mode == MOE_SCALE_PER_ROW_BLOCK128;
+  volatile int* abort_flag = &ctl->abort_flag;
+  bool timed_out = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
+        const Tile tl = get_tile<kFinal, false>(p, ctl, t, 0);
+        for (int ks = 0; ks < nks; ++ks) {
+          const int s = it % kW8RawStages;
+          if (!mbar_wait_bounded(smem_u32(&ctl->rempty[s]), ((it / kW8RawStages) & 1) ^ 1, abort_flag,
+                                 kWaitLimitNs)) {
+            timed_out = true;
+            break;
+          }
+          const uint32_t sa = base + s * kW8RawBytes, fb = smem_u32(&ctl->rfull[s]);
+          mbar_arrive_expect_tx(fb, kW8RawBytes);
+          tma_load_2d(sa, &tmW, ks * kW8Ks, tl.by, fb);                      // channels n0 .. n0 + 127
+          tma_load_2d(sa + kW8BoxBytes, &tmW, ks * kW8Ks, tl.by + 128, fb);  // n0 + 128 .. n0 + 255
+          tma_load_2d(sa + 2 * kW8BoxBytes, &tmX, ks * kW8Ks, tl.ay, fb);    // the tile's 128 token rows
+          ++it;
+        }
+      }
+      if (timed_out) {
+        *abort_flag = 1;
+        ctl->err = 2;
+        // let the loads already issued land before the CTA can exit
+        for (uint32_t j = (it > kW8RawStages ? it - kW8RawStages : 0); j < it; ++j)
+          mbar_wait_bounded(smem_u32(&ctl->rfull[j % kW8RawStages]), (j / kW8RawStages) & 1, &ctl->no_abort,
+                            kWaitLimitNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, tcount = 0;
+      for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
+        if (!mbar_wait_bounded(smem_u32(&ctl->dempty), (tcount & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+        for (int ks = 0; ks < nks; ++ks) {
+          const int a = it % kW8AStages, x = it % kW8XStages;
+          if (!mbar_wait_bounded(smem_u32(&ctl->afull[a]), (it / kW8AStages) & 1, abort_flag, kWaitLimitNs) ||
+              !mbar_wait_bounded(smem_u32(&ctl->xfull[x]), (it / kW8XStages) & 1, abort_flag, kWaitLimitNs)) {
+            timed_out = true;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t db = smem_desc_sw128(xring + x * kW8XBytes);
+          const uint32_t at = tmem_base + kW8AColBase + 64 * a;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int k16 = 0; k16 < kW8Ks / 16; ++k16)  // K = 16: 8 tensor-memory columns, 32 bytes of a B row
+              mma_f16_tmem_a(tmem_base + kW8Tok * h, at + 32 * h + 8 * k16, db + 2 * k16, kW8Idesc,
+                             (ks > 0 || k16 > 0) ? 1u : 0u);
+          mma_commit(smem_u32(&ctl->aempty[a]));
+          mma_commit(smem_u32(&ctl->xempty[x]));
+          ++it;
+        }
+        if (timed_out) break;
+        mma_commit(smem_u32(&ctl->dfull));
+        ++tcount;
+      }
+      // drain: every MMA this thread issued has completed once `drain` flips
+      mma_commit(smem_u32(&ctl->drain));
+      if (!mbar_wait_bounded(smem_u32(&ctl->drain), 0, &ctl->no_abort, kWaitLimitNs)) timed_out = true;
+      if (timed_out) {
+        *abort_flag = 1;
+        ctl->err = 2;
+      }
+    }
+    __syncwarp();
+  } else if (warp < 2 + kW8WConvWarps) {
+    // --------------------------------------------------- weight converters
+    // warp (h, q): rows 32 q .. 32 q + 31 of weight half h (the tile's
+    // channels 128 h ..), which are the tensor-memory lanes of that quarter
+    const int h = (warp - 2) >> 2, q4 = warp & 3;
+    const int r = 32 * q4 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * q4) << 16;
+    const int swz = (r >> 1) & 3;  // 64-byte swizzle: 16-byte chunk j of row r sits at j ^ ((r / 2) % 4)
+    uint32_t it = 0;
+    for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
+      const Tile tl = get_tile<kFinal, false>(p, ctl, t, 0);
+      const int ch = tl.n0 + 128 * h + r;
+      const bool ch_ok = ch < p.N;
+      const float* s_blk = p.rhs_scale + static_cast<int64_t>(tl.el) * p.kblocks * p.N + (ch_ok ? ch : 0);
+      float inv_smax = 0.0f;
+      if (w_blk) {
+        const float m = w8_block_smax(s_blk, p.kblocks, p.N, ch_ok);
+        inv_smax = m > 0.0f ? __frcp_rn(m) : 0.0f;
+      }
+      uint32_t rhi2 = 0x3C003C00u, rlo2 = 0u;  // f16x2 (1, 1) and (0, 0)
+      for (int ks = 0; ks < nks; ++ks) {
+        const int s = it % kW8RawStages;
+        if (!mbar_wait_bounded_warp(smem_u32(&ctl->rfull[s]), (it / kW8RawStages) & 1, abort_flag, kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        const uint8_t* src = base_ptr + s * kW8RawBytes + h * kW8BoxBytes + r * kW8Ks;
+        uint4 wv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) wv[j] = *reinterpret_cast<const uint4*>(src + 16 * (j ^ swz));
+        // the stage is refilled by TMA (the async proxy): order these generic
+        // reads before that write, or the refill may land under them
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->rempty[s]));
+        if (w_blk && (ks & 1) == 0) {  // a new 128-wide K block (two stages)
+          const float rel = ch_ok ? __fmul_rn(__ldg(s_blk + static_cast<int64_t>(ks >> 1) * p.N), inv_smax) : 0.0f;
+          const __half hi = __float2half_rn(rel);
+          const uint32_t hb = __half_as_ushort(hi);
+          const uint32_t lb = __half_as_ushort(__float2half_rn(__fsub_rn(rel, __half2float(hi))));
+          rhi2 = hb | (hb << 16);
+          rlo2 = lb | (lb << 16);
+        }
+        const int a = it % kW8AStages;
+        if (!mbar_wait_bounded_warp(smem_u32(&ctl->aempty[a]), ((it / kW8AStages) & 1) ^ 1, abort_flag,
+                                    kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+        uint32_t f[32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t wd[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            // bytes b0..b3 (K = 16 j + 4 c ..): b ^ 0x80 = b + 128 under the
+            // f16 exponent of 1024 is 1152 + b exactly; minus 1152 leaves b
+            const uint32_t x = wd[c] ^ 0x80808080u;
+            uint32_t lo, hi;
+            asm("prmt.b32 %0, %1, %2, 0x7170;" : "=r"(lo) : "r"(x), "r"(0x64646464u));
+            asm("prmt.b32 %0, %1, %2, 0x7372;" : "=r"(hi) : "r"(x), "r"(0x64646464u));
+            asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
+            asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
+            if (w_blk) {  // q r_hi + (q r_lo): one rounding of q r
+              uint32_t t0, t1;
+              asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(t0) : "r"(lo), "r"(rlo2));
+              asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(t1) : "r"(hi), "r"(rlo2));
+              asm("fma.rn.f16x2 %0, %0, %1, %2;" : "+r"(lo) : "r"(rhi2), "r"(t0));
+              asm("fma.rn.f16x2 %0, %0, %1, %2;" : "+r"(hi) : "r"(rhi2), "r"(t1));
+            }
+            f[8 * j + 2 * c] = lo;      // K pair (16 j + 4 c, + 1): column 8 j + 2 c
+            f[8 * j + 2 * c + 1] = hi;
+          }
+        }
+        tmem_st_32x32b_x32(tmem_base + lane_addr + kW8AColBase + 64 * a + 32 * h, f);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->afull[a]));
+        ++it;
+      }
+    }
+    if (timed_out) {
+      *abort_flag = 1;
+      ctl->err = 2;
+    }
+  } else if (warp < 2 + kW8WConvWarps + kW8XConvWarps) {
+    // ----------------------------------------------- activation converters
+    const int r = 32 * (warp - 2 - kW8WConvWarps) + lane;  // token row of the tile
+    const int swz = (r >> 1) & 3;
+    uint32_t it = 0;
+    for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
+      for (int ks = 0; ks < nks; ++ks) {
+        const int s = it % kW8RawStages;
+        if (!mbar_wait_bounded_warp(smem_u32(&ctl->rfull[s]), (it / kW8RawStages) & 1, abort_flag, kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        const uint8_t* src = base_ptr + s * kW8RawBytes + 2 * kW8BoxBytes + r * kW8Ks;
+        uint4 xv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) xv[j] = *reinterpret_cast<const uint4*>(src + 16 * (j ^ swz));
+        fence_proxy_async_smem();  // as above: generic reads before the TMA refill
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->rempty[s]));
+        const int x = it % kW8XStages;
+        if (!mbar_wait_bounded_warp(smem_u32(&ctl->xempty[x]), ((it / kW8XStages) & 1) ^ 1, abort_flag,
+                                    kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        // row r of the f16 tile: 128 bytes in 8-row / 1024-byte atoms, its
+        // 16-byte chunk c at c ^ (r % 8) (the 128-byte swizzle)
+        uint8_t* dst = base_ptr + (xring - base) + x * kW8XBytes + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t wd[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+          uint32_t o[8];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint16_t lo16 = static_cast<uint16_t>(wd[c] & 0xFFFFu), hi16 = static_cast<uint16_t>(wd[c] >> 16);
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o[2 * c]) : "h"(lo16));
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o[2 * c + 1]) : "h"(hi16));
+          }
+          *reinterpret_cast<uint4*>(dst + 16 * ((2 * j) ^ (r & 7))) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(dst + 16 * ((2 * j + 1) ^ (r & 7))) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        fence_proxy_async_smem();  // the tensor core reads the tile through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->xfull[x]));
+        ++it;
+      }
+    }
+    if (timed_out) {
+      *abort_flag = 1;
+      ctl->err = 2;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int h = (warp - 2 - kW8WConvWarps - kW8XConvWarps) >> 2, q4 = warp & 3;
+    const int r = 32 * q4 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * q4) << 16;
+    uint16_t* out = static_cast<uint16_t*>(p.out);
+    uint32_t tcount = 0;
+    if (p.stall && !mbar_wait_bounded_warp(smem_u32(&ctl->never), 0, abort_flag, p.stall_ns)) timed_out = true;
+    for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
+      const Tile tl = get_tile<kFinal, false>(p, ctl, t, 0);
+      const int ch = tl.n0 + 128 * h + r;
+      const bool ch_ok = ch < p.N;
+      float s_w;
+      if (w_blk)
+        s_w = w8_block_smax(p.rhs_scale + static_cast<int64_t>(tl.el) * p.kblocks * p.N + (ch_ok ? ch : 0),
+                            p.kblocks, p.N, ch_ok);
+      else if (p.rhs_mode == MOE_SCALE_PER_ROW)
+        s_w = ch_ok ? __ldg(p.rhs_scale + static_cast<int64_t>(tl.el) * p.N + ch) : 0.0f;
+      else
+        s_w = __ldg(p.rhs_scale);
+      // token scales: lane j holds those of the tile's tokens j, 32 + j, 64 + j, 96 + j
+      float sx[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int tok = 32 * c + lane;
+        sx[c] = p.lhs_mode == MOE_SCALE_PER_ROW ? (tok < tl.rows ? __ldg(p.lhs_scale + tl.row0 + tok) : 0.0f)
+                                                : __ldg(p.lhs_scale);
+      }
+      if (!mbar_wait_bounded_warp(smem_u32(&ctl->dfull), tcount & 1, abort_flag, kWaitLimitNs)) {
+        timed_out = true;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < kW8Tok / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_base + lane_addr + kW8Tok * h + 32 * c, v);
+        tmem_wait_ld();
+        if (c == kW8Tok / 32 - 1) {  // the accumulators are read: the next tile's MMAs may start
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctl->dempty));
+        }
+        uint16_t* orow = out + (static_cast<int64_t>(tl.row0) + 32 * c) * p.N + ch;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float sxj = __shfl_sync(0xffffffffu, sx[c], j);
+          if (ch_ok && 32 * c + j < tl.rows)
+            orow[static_cast<int64_t>(j) * p.N] =
+                static_cast<uint16_t>(pack_bf16x2(__fmul_rn(__uint_as_float(v[j]), __fmul_rn(s_w, sxj)), 0.0f));
+        }
+      }
+      ++tcount;
+    }
+    if (timed_out) {
+      *abort_flag = 1;
+      ctl->err = 2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
   }
   if (threadIdx.x == 0 && ctl->err) raise_error(&g_err, MOE_DEVERR_TIMEOUT);
 }
@@ -2049,6 +2461,23 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, ui
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 2-D uint8 tensor map for the int8-weight gmm: box rows_box x 64 bytes,
+// 64-byte swizzle (16-byte chunk j of box row r at j ^ ((r / 2) % 4)); reads
+// past the extents return zeros.
+bool make_map_u8_64(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint64_t pitch,
+                    uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kW8Ks), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -2455,6 +2884,57 @@ namespace {
 int64_t padded_rows(int64_t M, int E_local) { return ((M + 127) / 128) * 128 + 128ll * E_local; }
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 }  // namespace
+
+extern "C" moe_status gmm_fp8_w8(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode,
+                                 const int8_t* rhs_q, const float* rhs_scale, moe_scale_mode rhs_mode,
+                                 const int32_t* group_sizes, int E, int group_offset, int E_local, int64_t M,
+                                 int64_t K, int64_t N, uint16_t* out, moe_stream_t stream) {
+  MOE_HOST_CHECK(lhs_q && lhs_scale && rhs_q && rhs_scale && group_sizes && out, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(lhs_mode == MOE_SCALE_PER_ROW || lhs_mode == MOE_SCALE_PER_TENSOR, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(valid_lhs_mode(rhs_mode), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(E > 0 && E <= kMaxGroups && group_offset >= 0 && E_local > 0 && group_offset + E_local <= E,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(M >= 0 && M < (1ll << 31) && K > 0 && K % 16 == 0 && K < (1 << 30) && N > 0 && N % 16 == 0,
+                 MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(static_cast<int64_t>(E_local) * N < (1ll << 31), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(rhs_mode != MOE_SCALE_PER_ROW_BLOCK128 || K % 128 == 0, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(aligned16(lhs_q) && aligned16(rhs_q) && aligned16(out), MOE_ERR_INVALID_ARG);
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = as_stream(stream);
+  if (M == 0) return MOE_OK;
+  if (group_offset > 0 || E_local < E) {
+    zero_outside_kernel<<<sm_count() * 4, 256, 0, st>>>(out, M, N, group_sizes, E, group_offset, E_local);
+    MOE_CUDA_TRY(cudaGetLastError());
+  }
+  CUtensorMap X, W;
+  if (!make_map_u8_64(&X, lhs_q, K, M, K, kW8Tok)) return MOE_ERR_CUDA;
+  if (!make_map_u8_64(&W, rhs_q, K, static_cast<uint64_t>(E_local) * N, K, 128)) return MOE_ERR_CUDA;
+  Params p{};
+  p.group_sizes = group_sizes;
+  p.E = E;
+  p.g0 = group_offset;
+  p.El = E_local;
+  p.M = M;
+  p.K = static_cast<int>(K);
+  p.N = static_cast<int>(N);
+  p.kblocks = static_cast<int>((K + BK - 1) / BK);
+  p.ntiles = static_cast<int>((N + Cfg<kFinal>::BN - 1) / Cfg<kFinal>::BN);  // 256 channels a tile
+  p.lhs_scale = lhs_scale;
+  p.lhs_mode = lhs_mode;
+  p.rhs_scale = rhs_scale;
+  p.rhs_mode = rhs_mode;
+  p.out = out;
+  p.stall_ns = g_stall_ns.load();
+  p.stall = p.stall_ns != 0;
+  MOE_CUDA_TRY(cudaFuncSetAttribute(w8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kW8Smem)));
+  const int sms = sm_count();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const int units = gmm_max_units<kFinal, false>(M, E_local, p.ntiles);
+  const int grid = units < sms ? units : sms;
+  w8_kernel<<<grid, kW8Warps * 32, kW8Smem, st>>>(X, W, p);
+  MOE_CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
 
 extern "C" size_t tgmm_fp8_workspace_bytes(int64_t M, int64_t K, int64_t N, int E_local) {
   if (M < 0 || K <= 0 || N <= 0 || E_local <= 0) return 0;

@@ -1,5 +1,6 @@
 // Row-wise absmax quantisation to e4m3 and the fused producers that feed it:
 //   moe_quantize_rows, moe_quantize_weights        (plain bf16 rows)
+//   moe_quantize_weights_int8                      (int8 codes, amax / 127)
 //   moe_swiglu_quant                               (h = bf16(silu(a0) a1))
 //   moe_gather_scale_quant                         (dO = bf16(w G[src]))
 //   moe_swiglu_bwd_quant                           (dA0 | dA1)
@@ -233,8 +234,10 @@ struct SwigluBwdOp {  // dA0 = (dH a1) silu'(a0), dA1 = dH silu(a0); also stores
 // MODE: MOE_SCALE_PER_ROW, MOE_SCALE_PER_ROW_BLOCK128, MOE_SCALE_PER_TENSOR
 // or kModeMx32 (MXFP8, OCP MX v1.0: per 32-column block the shared exponent
 // X = floor(log2(amax)) - 8 and codes e4m3(x / 2^X), the division exact).
-// MAXI: units per thread (ceil(nunits / blockDim.x) <= MAXI).
-template <int MODE, int MAXI, class Op>
+// MAXI: units per thread (ceil(nunits / blockDim.x) <= MAXI).  I8: int8
+// codes instead (int8 weights: scale amax / 127, codes the nearest integers
+// of the exact fp32 quotients, ties to even).
+template <int MODE, int MAXI, bool I8, class Op>
 __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, int64_t qcols,
                                                             const float* static_scale, uint8_t* q, ScaleOut so) {
   constexpr int U = Op::U;
@@ -242,6 +245,7 @@ __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, i
   constexpr int kBlockLanes = Op::kWide ? 8 : 16;  // units per 128-column block
   constexpr int kMxLanes = Op::kWide ? 2 : 4;      // units per 32-column block
   static_assert(MODE != kModeMx32 || Op::kWide, "MXFP8 rows use 16-column units");
+  static_assert(!I8 || MODE != kModeMx32, "int8 codes take fp32 scales");
   const int64_t row = blockIdx.x;
   const int tid = threadIdx.x;
   uint32_t pk[MAXI][U][4];
@@ -278,7 +282,7 @@ __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, i
       if (tid == 0) red[0] = t;
     }
     __syncthreads();
-    s_row = absmax_scale(red[0]);
+    s_row = I8 ? int8_scale(red[0]) : absmax_scale(red[0]);
   } else if (MODE == MOE_SCALE_PER_TENSOR) {
     s_row = __ldg(static_scale);
   }
@@ -320,7 +324,7 @@ __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, i
       float m = amax_i[i];
 #pragma unroll
       for (int o = kBlockLanes / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      s = absmax_scale(m);
+      s = I8 ? int8_scale(m) : absmax_scale(m);
       inv = __frcp_rn(s);
     }
     s_blk[i] = s;
@@ -333,8 +337,14 @@ __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, i
           x8[2 * j] = bf16lo(pk[i][uu][j]);
           x8[2 * j + 1] = bf16hi(pk[i][uu][j]);
         }
-        quant_n<8>(x8, s, inv, v);
-        codes[i][uu] = pack_e4m3x8(v);
+        if (I8) {  // weights are quantised once, outside the step: the exact quotients
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = __fdiv_rn(x8[j], s);
+          codes[i][uu] = pack_i8x8(v);
+        } else {
+          quant_n<8>(x8, s, inv, v);
+          codes[i][uu] = pack_e4m3x8(v);
+        }
       }
     }
   }
@@ -367,36 +377,36 @@ __global__ void __launch_bounds__(kThreads) rowquant_kernel(Op op, int nunits, i
   }
 }
 
-template <int MODE, int MAXI, class Op>
+template <int MODE, int MAXI, bool I8, class Op>
 cudaError_t launch_rows_t(const Op& op, int64_t rows, int nunits, int threads, int64_t qcols, const float* ss,
                           uint8_t* q, ScaleOut so, cudaStream_t st) {
-  rowquant_kernel<MODE, MAXI, Op><<<static_cast<unsigned>(rows), threads, 0, st>>>(op, nunits, qcols, ss, q, so);
+  rowquant_kernel<MODE, MAXI, I8, Op><<<static_cast<unsigned>(rows), threads, 0, st>>>(op, nunits, qcols, ss, q, so);
   return cudaGetLastError();
 }
 
-template <int MODE, class Op>
+template <int MODE, bool I8, class Op>
 cudaError_t launch_rows_m(const Op& op, int64_t rows, int nunits, int64_t qcols, const float* ss, uint8_t* q,
                           ScaleOut so, cudaStream_t st) {
   int threads = nunits >= kThreads ? kThreads : ((nunits + 31) / 32) * 32;
   const int per = (nunits + threads - 1) / threads;
-  if (per <= 1) return launch_rows_t<MODE, 1>(op, rows, nunits, threads, qcols, ss, q, so, st);
-  if (per <= 2) return launch_rows_t<MODE, 2>(op, rows, nunits, threads, qcols, ss, q, so, st);
-  if (per <= 4) return launch_rows_t<MODE, 4>(op, rows, nunits, threads, qcols, ss, q, so, st);
-  if (per <= 8) return launch_rows_t<MODE, 8>(op, rows, nunits, threads, qcols, ss, q, so, st);
-  return launch_rows_t<MODE, 16>(op, rows, nunits, threads, qcols, ss, q, so, st);
+  if (per <= 1) return launch_rows_t<MODE, 1, I8>(op, rows, nunits, threads, qcols, ss, q, so, st);
+  if (per <= 2) return launch_rows_t<MODE, 2, I8>(op, rows, nunits, threads, qcols, ss, q, so, st);
+  if (per <= 4) return launch_rows_t<MODE, 4, I8>(op, rows, nunits, threads, qcols, ss, q, so, st);
+  if (per <= 8) return launch_rows_t<MODE, 8, I8>(op, rows, nunits, threads, qcols, ss, q, so, st);
+  return launch_rows_t<MODE, 16, I8>(op, rows, nunits, threads, qcols, ss, q, so, st);
 }
 
-template <class Op>
+template <bool I8 = false, class Op>
 moe_status launch_rows(const Op& op, int64_t rows, int nunits, int64_t qcols, moe_scale_mode mode, const float* ss,
                        uint8_t* q, ScaleOut so, cudaStream_t st) {
   if (rows == 0) return MOE_OK;
   cudaError_t e;
   if (mode == MOE_SCALE_PER_ROW)
-    e = launch_rows_m<MOE_SCALE_PER_ROW>(op, rows, nunits, qcols, ss, q, so, st);
+    e = launch_rows_m<MOE_SCALE_PER_ROW, I8>(op, rows, nunits, qcols, ss, q, so, st);
   else if (mode == MOE_SCALE_PER_ROW_BLOCK128)
-    e = launch_rows_m<MOE_SCALE_PER_ROW_BLOCK128>(op, rows, nunits, qcols, ss, q, so, st);
+    e = launch_rows_m<MOE_SCALE_PER_ROW_BLOCK128, I8>(op, rows, nunits, qcols, ss, q, so, st);
   else
-    e = launch_rows_m<MOE_SCALE_PER_TENSOR>(op, rows, nunits, qcols, ss, q, so, st);
+    e = launch_rows_m<MOE_SCALE_PER_TENSOR, I8>(op, rows, nunits, qcols, ss, q, so, st);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -404,7 +414,7 @@ template <class Op>
 moe_status launch_rows_mx(const Op& op, int64_t rows, int nunits, int64_t qcols, uint8_t* q, ScaleOut so,
                           cudaStream_t st) {
   if (rows == 0) return MOE_OK;
-  return launch_rows_m<kModeMx32>(op, rows, nunits, qcols, nullptr, q, so, st) == cudaSuccess ? MOE_OK
+  return launch_rows_m<kModeMx32, false>(op, rows, nunits, qcols, nullptr, q, so, st) == cudaSuccess ? MOE_OK
                                                                                             : MOE_ERR_CUDA;
 }
 
@@ -625,6 +635,20 @@ extern "C" moe_status moe_quantize_weights(const uint16_t* w, int64_t E, int64_t
   RowsOp op{w, K};
   ScaleOut so{scale, N, static_cast<int>(K / 128), nullptr, 0};
   return launch_rows(op, E * N, static_cast<int>(K / 16), K, mode, static_scale, q, so, as_stream(stream));
+}
+
+extern "C" moe_status moe_quantize_weights_int8(const uint16_t* w, int64_t E, int64_t N, int64_t K,
+                                                moe_scale_mode mode, const float* static_scale, int8_t* q,
+                                                float* scale, moe_stream_t stream) {
+  MOE_HOST_CHECK(w && q && E > 0 && N > 0 && K > 0 && K % 16 == 0 && K <= kMaxCols, MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(E * N < (1ll << 31) && aligned16(w) && aligned16(q), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(mode != MOE_SCALE_PER_ROW_BLOCK128 || K % 128 == 0, MOE_ERR_INVALID_ARG);
+  moe_status st = check_mode_ptrs(mode, static_scale, scale);
+  if (st != MOE_OK) return st;
+  RowsOp op{w, K};
+  ScaleOut so{scale, N, static_cast<int>(K / 128), nullptr, 0};
+  return launch_rows<true>(op, E * N, static_cast<int>(K / 16), K, mode, static_scale, reinterpret_cast<uint8_t*>(q),
+                           so, as_stream(stream));
 }
 
 extern "C" moe_status moe_swiglu_quant(const uint16_t* a, int64_t R, int64_t F, moe_scale_mode mode,

@@ -468,6 +468,45 @@ moe_status gmm_fp8_mx_swiglu(const uint8_t* lhs_q, const uint8_t* lhs_sf, const 
 moe_status moe_swiglu_quant_mx(const uint16_t* a, int64_t R, int64_t F, uint8_t* h_q, uint8_t* h_sf,
                                moe_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * int8-weight variant of steps 3 and 5 ([Q-FUSE], "Keep qwix out of
+ * tpu-inference's fused MoE kernel and pre-quantize weights", description:
+ * the weights are pre-quantised to float8_e4m3fn or int8 with [E, blocks, 1,
+ * N] scales).  The activations and h stay e4m3 with their scales, and steps
+ * 1, 2, 4 and 6 are unchanged.
+ *
+ * int8 codes are symmetric absmax:
+ *   s = fp32(amax / 127), s = 1 when amax = 0;
+ *   q = nearest integer of fp32(x / s), ties to even, limited to [-127, 127].
+ * ------------------------------------------------------------------------ */
+
+/* Weights w[E, N, K] bf16 -> int8 codes q[E, N, K] and fp32 scales in the
+ * layouts of moe_quantize_weights: PER_ROW (per channel) [E, N];
+ * PER_ROW_BLOCK128 (blockwise) [E, K/128, N]; PER_TENSOR uses static_scale.
+ * K % 16 == 0 (% 128 for blockwise), K <= 32768; w and q 16-byte aligned. */
+moe_status moe_quantize_weights_int8(const uint16_t* w, int64_t E, int64_t N, int64_t K, moe_scale_mode mode,
+                                     const float* static_scale, int8_t* q, float* scale, moe_stream_t stream);
+
+/* Steps 3 / 5 with int8 weights:
+ *   out[m, n] = bf16( sum_k deq(lhs)[m, k] * q[g(m), n, k] * s_w )
+ * with deq(lhs) as in gmm_fp8 (lhs_mode PER_ROW or PER_TENSOR), q the int8
+ * code as an integer and s_w its weight scale (rhs_mode PER_ROW [E_local, N],
+ * PER_ROW_BLOCK128 [E_local, K/128, N] or PER_TENSOR [1]).  Groups,
+ * group_offset and E_local are as in gmm_fp8: rows outside the local groups
+ * are zero.
+ *
+ * The contraction runs on the f16 tensor-core MMA (both code types are exact
+ * in f16) with fp32 accumulation.  Blockwise weight scales enter as factors
+ * s_w[kb] / max_kb s_w[kb] on the converted codes, so each converted weight
+ * carries one f16 rounding (relative 2^-12; coarser where the factor falls
+ * below 2^-14, the f16 normal range) beside the fp32 accumulation.
+ * K % 16 == 0 (% 128 for blockwise), N % 16 == 0; lhs_q, rhs_q and out
+ * 16-byte aligned.  MOE_ERR_INVALID_ARG on a bad argument, before any launch. */
+moe_status gmm_fp8_w8(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode, const int8_t* rhs_q,
+                      const float* rhs_scale, moe_scale_mode rhs_mode, const int32_t* group_sizes, int E,
+                      int group_offset, int E_local, int64_t M, int64_t K, int64_t N, uint16_t* out,
+                      moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -45,6 +45,17 @@ def bf16_round_f64(a: np.ndarray) -> np.ndarray:
     return t.to(torch.float64).numpy()
 
 
+def close_errors(got, ref):
+    """(relative Frobenius error, max |delta| / max |ref|) after bf16 rounding."""
+    g = to_f64(got) if got.dtype == np.uint16 else bf16_round_f64(got)
+    r = to_f64(ref) if ref.dtype == np.uint16 else bf16_round_f64(ref)
+    nr = np.linalg.norm(r)
+    fro = np.linalg.norm(g - r) / nr if nr > 0 else np.linalg.norm(g)
+    amax = np.abs(r).max() if r.size else 0.0
+    elt = np.abs(g - r).max() if r.size else 0.0
+    return float(fro), float(elt / amax) if amax > 0 else float(elt)
+
+
 def assert_close(got, ref, what="", rel_fro=REL_FRO, rel_elt=REL_ELT):
     g = to_f64(got) if got.dtype == np.uint16 else bf16_round_f64(got)
     r = to_f64(ref) if ref.dtype == np.uint16 else bf16_round_f64(ref)

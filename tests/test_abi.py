@@ -120,3 +120,20 @@ def test_host_side_argument_checks_of_the_mxfp8_entries(lib):
     assert lib.gmm_fp8_mx_swiglu(p, p, p, p, p, 1, 0, 1, 8, 128, 128, None, p, None, None) == 1
     # unfused SwiGLU requantisation: F not a multiple of 32
     assert lib.moe_swiglu_quant_mx(p, 4, 48, p, p, None) == 1
+
+
+def test_host_side_argument_checks_of_the_int8_weight_entries(lib):
+    p = ctypes.c_void_p(256)  # a 16-byte aligned dummy address (never dereferenced)
+    # quantiser: K not a multiple of 16; blockwise K not a multiple of 128; null scales; static without scale
+    assert lib.moe_quantize_weights_int8(p, 1, 4, 24, 0, None, p, p, None) == 1
+    assert lib.moe_quantize_weights_int8(p, 1, 4, 144, 1, None, p, p, None) == 1
+    assert lib.moe_quantize_weights_int8(p, 1, 4, 128, 0, None, p, None, None) == 1
+    assert lib.moe_quantize_weights_int8(p, 1, 4, 128, 2, None, p, None, None) == 1
+    # gmm: per-128 activation scales (not taken); K % 16; blockwise K % 128; N % 16;
+    # shard past E; null weight scales
+    assert lib.gmm_fp8_w8(p, p, 1, p, p, 0, p, 1, 0, 1, 8, 128, 256, p, None) == 1
+    assert lib.gmm_fp8_w8(p, p, 0, p, p, 0, p, 1, 0, 1, 8, 120, 256, p, None) == 1
+    assert lib.gmm_fp8_w8(p, p, 0, p, p, 1, p, 1, 0, 1, 8, 144, 256, p, None) == 1
+    assert lib.gmm_fp8_w8(p, p, 0, p, p, 0, p, 1, 0, 1, 8, 128, 24, p, None) == 1
+    assert lib.gmm_fp8_w8(p, p, 0, p, p, 0, p, 2, 1, 2, 8, 128, 256, p, None) == 1
+    assert lib.gmm_fp8_w8(p, p, 0, p, None, 0, p, 1, 0, 1, 8, 128, 256, p, None) == 1

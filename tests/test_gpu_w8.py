@@ -1,0 +1,323 @@
+"""GPU parity of the int8-weight variant against the oracle.
+
+The weights are int8 codes with per-channel or blockwise ([E, K/128, N])
+scales; the activations and h stay e4m3.  Parity rules:
+- the int8 weight quantiser gives bit-exact codes and scales;
+- the grouped matmul (gmm_w8) is within relative Frobenius 2e-3 and
+  max |delta| <= 1e-2 max|ref| after bf16 rounding;
+- in the FFN every stage is held to that bar against the oracle fed the
+  GPU's previous-stage output, the requantised h bit-exact, and the composed
+  output within 5e-3 (per-channel weight scales) or 1e-2 (blockwise).
+
+Why the composed bar is wider with blockwise weight scales: the kernel folds
+each block's scale into the converted weight, an f16 operand, so every
+weight carries one f16 rounding (relative 2^-12) that the oracle's exact
+product does not.  That moves a by about 2^-12 relative, which changes the
+bf16 rounding of a few per cent of the a values by one bf16 step (2^-8) and
+so, through SwiGLU, one e4m3 step (2^-3) in a few tenths of a per cent of the
+h codes; measured, the composed y then differs by 6-7e-3.  With per-channel
+scales the converted weights are the exact integers and a matches the
+oracle's to fp32 accumulation order.
+Cases cover several tiles, ragged and empty groups, N tails, K tails, long
+K, blockwise scales spread over many binades, expert-parallel shards and the
+bounded-wait failure path."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.gpu_helpers import assert_close, close_errors, dev, host, rand_codes, ragged_sizes
+
+pytestmark = pytest.mark.gpu
+
+moe = pytest.importorskip("fp8_quantized_moe_gb300")
+
+
+def bf16(a) -> np.ndarray:
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+# ------------------------------------------------------------ quantiser ----
+
+@pytest.mark.parametrize("E,N,K", [(1, 1, 128), (3, 48, 256), (2, 100, 4096), (4, 64, 14336), (2, 16, 7168)])
+@pytest.mark.parametrize("mode", [synth.PER_ROW, synth.PER_ROW_BLOCK128, synth.PER_TENSOR])
+def test_quantize_weights_int8_bit_exact(E, N, K, mode):
+    rng = np.random.default_rng(E * 7 + N + K + mode)
+    w = rng.standard_normal((E, N, K)).astype(np.float32) * 0.02
+    w *= np.repeat(np.ldexp(1.0, rng.integers(-6, 6, (E, N, K // 128))), 128, axis=2).astype(np.float32)
+    w[rng.random(w.shape) < 0.02] = 0.0
+    w[0, 0, :128] = 0.0  # an all-zero block (and row when K = 128)
+    w[0, -1, 5] = 127 * 2.0 ** -5  # ties of the integer rounding at s = 2^-5 once the row's amax is this value
+    w[0, -1, 6] = 2.5 * 2.0 ** -5
+    wb = bf16(w)
+    st = 0.001
+    q_ref, s_ref = oracle.quantize_weights_int8(wb, mode, st)
+    q, s = moe.quantize_weights_int8(dev(wb), mode, torch.tensor([st], device="cuda") if mode == synth.PER_TENSOR
+                                     else None)
+    assert q.dtype == torch.int8
+    assert np.array_equal(host(q), q_ref)
+    if mode != synth.PER_TENSOR:
+        assert np.array_equal(host(s), s_ref)
+
+
+# ------------------------------------------------------------------ gmm ----
+
+def make_w8_case(seed, M, K, N, E, w_mode=synth.PER_ROW, a_mode=synth.PER_ROW, zero_frac=0.25, spread=0):
+    rng = np.random.default_rng(seed)
+    sizes = ragged_sizes(rng, E, M, zero_frac)
+    a = rand_codes(rng, (M, K))
+    q = rng.integers(-127, 128, (E, N, K)).astype(np.int8)
+    # lhs scales near 2^-8, weight scales near 1 / (127 sqrt(K)): O(1) outputs
+    sa = (rng.uniform(0.5, 1.5, M) * 2.0 ** -8).astype(np.float32) if a_mode == synth.PER_ROW \
+        else np.array([2.0 ** -8], np.float32)
+    base = 1.0 / (127 * np.sqrt(K))
+    if w_mode == synth.PER_ROW:
+        sw = (rng.uniform(0.5, 1.5, (E, N)) * base).astype(np.float32)
+    elif w_mode == synth.PER_ROW_BLOCK128:
+        # block scales spread over 2^-spread .. 1 of the channel's largest
+        sw = (rng.uniform(0.5, 1.5, (E, K // 128, N)) * base *
+              np.ldexp(1.0, -rng.integers(0, spread + 1, (E, K // 128, N)))).astype(np.float32)
+    else:
+        sw = np.array([base], np.float32)
+    return sizes, a, sa, q, sw
+
+
+def w8_args(a, sa, a_mode, q, sw, w_mode, sizes):
+    return dev(a), dev(sa), a_mode, dev(q), dev(sw), w_mode, dev(sizes)
+
+
+GMM_CASES = [
+    (128, 128, 256, 1),       # one tile, two stages
+    (1, 128, 256, 1),         # a single row
+    (200, 256, 512, 3),       # ragged groups, several tiles
+    (300, 128, 144, 4),       # N not a multiple of the 256-channel tile
+    (1000, 1024, 272, 7),     # an N tail of 16 past the tile
+    (600, 7168, 512, 3),      # K = 7168: 112 stages, the rings wrap many times
+    (2048, 2048, 1536, 128),  # E = 128 experts, many empty or short groups
+    (129, 384, 256, 2),       # a one-row group past a full tile
+    (3000, 3072, 768, 24),    # many groups, several tiles per group
+    (1, 4096, 256, 1),
+]
+
+
+@pytest.mark.parametrize("M,K,N,E", GMM_CASES)
+def test_gmm_w8_per_channel_matches_oracle(M, K, N, E):
+    sizes, a, sa, q, sw = make_w8_case(M * 31 + K + N + E, M, K, N, E)
+    ref = oracle.gmm_w8(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW, sizes)
+    out = moe.gmm_w8(*w8_args(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW, sizes))
+    assert moe.device_error() == 0
+    assert_close(host(out), ref, f"gmm_w8 per channel M={M} K={K} N={N} E={E}")
+
+
+@pytest.mark.parametrize("M,K,N,E", [c for c in GMM_CASES if c[1] % 128 == 0])
+def test_gmm_w8_blockwise_matches_oracle(M, K, N, E):
+    sizes, a, sa, q, sw = make_w8_case(M * 37 + K + N + E, M, K, N, E, w_mode=synth.PER_ROW_BLOCK128, spread=4)
+    ref = oracle.gmm_w8(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW_BLOCK128, sizes)
+    out = moe.gmm_w8(*w8_args(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW_BLOCK128, sizes))
+    assert moe.device_error() == 0
+    assert_close(host(out), ref, f"gmm_w8 blockwise M={M} K={K} N={N} E={E}")
+
+
+@pytest.mark.parametrize("spread", [0, 8, 12])
+def test_gmm_w8_block_scales_over_many_binades(spread):
+    # a channel's block scales spread over 2^-spread .. 1: the f16 factors
+    # stay normal (>= 2^-14) and each carries one f16 rounding
+    sizes, a, sa, q, sw = make_w8_case(40 + spread, 512, 2048, 512, 3, w_mode=synth.PER_ROW_BLOCK128,
+                                       zero_frac=0, spread=spread)
+    ref = oracle.gmm_w8(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW_BLOCK128, sizes)
+    out = moe.gmm_w8(*w8_args(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW_BLOCK128, sizes))
+    assert moe.device_error() == 0
+    assert_close(host(out), ref, f"gmm_w8 block scales over 2^{spread}")
+
+
+@pytest.mark.parametrize("a_mode,w_mode", [(synth.PER_TENSOR, synth.PER_ROW), (synth.PER_TENSOR, synth.PER_TENSOR),
+                                           (synth.PER_ROW, synth.PER_TENSOR),
+                                           (synth.PER_TENSOR, synth.PER_ROW_BLOCK128)])
+def test_gmm_w8_static_scales(a_mode, w_mode):
+    sizes, a, sa, q, sw = make_w8_case(50 + 3 * a_mode + w_mode, 700, 1024, 384, 5, w_mode=w_mode, a_mode=a_mode,
+                                       spread=3)
+    ref = oracle.gmm_w8(a, sa, a_mode, q, sw, w_mode, sizes)
+    out = moe.gmm_w8(*w8_args(a, sa, a_mode, q, sw, w_mode, sizes))
+    assert moe.device_error() == 0
+    assert_close(host(out), ref, f"gmm_w8 modes {a_mode}/{w_mode}")
+
+
+@pytest.mark.parametrize("K", [80, 208, 1040])
+def test_gmm_w8_k_tail(K):
+    # K a multiple of 16 but not of the 64-wide stage: the last stage's boxes
+    # read zeros past K
+    sizes, a, sa, q, sw = make_w8_case(60 + K, 300, K, 256, 3)
+    ref = oracle.gmm_w8(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW, sizes)
+    out = moe.gmm_w8(*w8_args(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW, sizes))
+    assert moe.device_error() == 0
+    assert_close(host(out), ref, f"gmm_w8 K={K}")
+
+
+@pytest.mark.parametrize("K,w_mode", [(512, synth.PER_ROW), (4096, synth.PER_ROW_BLOCK128)])
+def test_gmm_w8_expert_parallel_shard(K, w_mode):
+    M, N, E = 1000, 384, 9
+    sizes, a, sa, q, sw = make_w8_case(17 + K, M, K, N, E, w_mode=w_mode, zero_frac=0.2, spread=2)
+    g0, El = 2, 4
+    q, sw = np.ascontiguousarray(q[g0:g0 + El]), np.ascontiguousarray(sw[g0:g0 + El])
+    ref = oracle.gmm_w8(a, sa, synth.PER_ROW, q, sw, w_mode, sizes, group_offset=g0, E_local=El)
+    out = host(moe.gmm_w8(*w8_args(a, sa, synth.PER_ROW, q, sw, w_mode, sizes), group_offset=g0, E_local=El))
+    assert moe.device_error() == 0
+    starts = np.concatenate([[0], np.cumsum(sizes)])
+    lo, hi = starts[g0], starts[g0 + El]
+    assert not out[:lo].any() and not out[hi:].any()
+    assert_close(out[lo:hi], ref[lo:hi], "gmm_w8 shard")
+
+
+def tile_errors(got, ref, rows=128, cols=128, top=6):
+    """The (row tile, column tile, relative error) of the worst output tiles."""
+    g, r = host_f64(got), host_f64(ref)
+    out = []
+    for i in range(0, g.shape[0], rows):
+        for j in range(0, g.shape[1], cols):
+            d = np.linalg.norm(g[i:i + rows, j:j + cols] - r[i:i + rows, j:j + cols])
+            out.append((i // rows, j // cols, float(d / (np.linalg.norm(r[i:i + rows, j:j + cols]) + 1e-30))))
+    return sorted(out, key=lambda t: -t[2])[:top]
+
+
+def host_f64(a):
+    return oracle.bf16_to_f64(a) if a.dtype == np.uint16 else a.astype(np.float64)
+
+
+@pytest.mark.parametrize("M,K,N,E,w_mode", [(2048, 4096, 512, 4, synth.PER_ROW), (3000, 1024, 768, 24, synth.PER_ROW),
+                                            (2048, 2048, 1536, 128, synth.PER_ROW_BLOCK128)])
+def test_gmm_w8_is_deterministic(M, K, N, E, w_mode):
+    """The accumulation order is fixed, so repeated calls give the same bits;
+    a pipeline hand-off that let the MMA read a stage before it was written
+    would show up as a difference."""
+    sizes, a, sa, q, sw = make_w8_case(70 + K + N, M, K, N, E, w_mode=w_mode, spread=3)
+    args = w8_args(a, sa, synth.PER_ROW, q, sw, w_mode, sizes)
+    first = host(moe.gmm_w8(*args))
+    ref = oracle.gmm_w8(a, sa, synth.PER_ROW, q, sw, w_mode, sizes)
+    diffs = []
+    for i in range(20):
+        out = host(moe.gmm_w8(*args))
+        if not np.array_equal(out, first):
+            diffs.append((i, int(np.sum(out != first)), tile_errors(out, ref)))
+    assert moe.device_error() == 0
+    assert not diffs, f"repeated calls differ: {diffs[:3]}; first call vs oracle: {tile_errors(first, ref)}"
+    assert_close(first, ref, "gmm_w8 (repeated)")
+
+
+def test_gmm_w8_bounded_wait_timeout_reports_and_recovers():
+    """The failure path: with the epilogue held on a barrier nothing arrives
+    on (200 us limit), the converters, the producer and the MMA issuer stop,
+    every load in flight lands, tensor memory is freed and
+    MOE_DEVERR_TIMEOUT is raised; the next call is exact."""
+    lib = moe.lib()
+    for M, K, N, E in [(4096, 512, 1024, 8), (2048, 4096, 512, 4)]:
+        sizes, a, sa, q, sw = make_w8_case(23 + K, M, K, N, E)
+        args = w8_args(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW, sizes)
+        assert moe.device_error() == 0
+        lib.moe_test_stall_epilogue(200_000)
+        try:
+            moe.gmm_w8(*args)
+            assert moe.device_error() == 0x4  # MOE_DEVERR_TIMEOUT
+        finally:
+            lib.moe_test_stall_epilogue(0)
+        ref = oracle.gmm_w8(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW, sizes)
+        for rep_ in range(3):
+            out = host(moe.gmm_w8(*args))
+            assert moe.device_error() == 0
+            fro, _ = close_errors(out, ref)
+            assert fro <= 2e-3, (f"gmm_w8 call {rep_} after a timed-out call (K={K}): {fro:.3e}; worst tiles "
+                                 f"{tile_errors(out, ref)}")
+
+
+# ------------------------------------------------------------------ FFN ----
+
+@pytest.mark.parametrize("w_mode", [synth.PER_ROW, synth.PER_ROW_BLOCK128])
+def test_ffn_w8_small_matches_oracle(w_mode):
+    """Every stage against the oracle fed the GPU's previous-stage output;
+    the composed chain within 5e-3."""
+    cfg = synth.scaled(synth.CONFIGS["mixtral_w8"], T=256, D=384, E=16, k=4, F=256, w_mode=w_mode)
+    x_t = synth.activations(cfg, 0)
+    ids, w = synth.routing(cfg, 0)
+    w_in, w_out = synth.expert_weights(cfg, 0)
+    xb, wib, wob = (oracle.bf16_bits(t) for t in (x_t, w_in, w_out))
+    wq = oracle.prepare_weights_w8(wib, wob, w_mode)
+    ref = oracle.ffn_forward(xb, ids, w, wq, cfg.E, cfg.act_mode)
+    W = moe.prepare_weights_w8(dev(wib), dev(wob), w_mode)
+    assert np.array_equal(host(W.w_in), wq[0]) and np.array_equal(host(W.s_in), wq[1])
+    assert np.array_equal(host(W.w_out), wq[3]) and np.array_equal(host(W.s_out), wq[4])
+    buf = moe.FFNBuffers(cfg.T, cfg.D, cfg.E, cfg.k, cfg.F, cfg.act_mode, "cuda")
+    y = moe.ffn_forward(dev(xb), dev(ids), dev(w), W, cfg.act_mode, buf)
+    assert moe.device_error() == 0
+    s = buf.sort
+    assert np.array_equal(host(s["xs_q"]), ref["xs_q"]) and np.array_equal(host(s["xs_scale"]), ref["xs_s"])
+    sizes = ref["sizes"]
+    a_gpu = host(buf.a)
+    hq_ref, hs_ref, _ = oracle.swiglu_quant(a_gpu, cfg.act_mode)
+    o_stage = oracle.gmm_w8(hq_ref, hs_ref, cfg.act_mode, wq[3], wq[4], w_mode, sizes)
+    y_stage = oracle.combine(host(buf.o), ref["pos"], w, cfg.k)
+    # (relative Frobenius, max |delta| / max |ref|) of each stage, printed
+    # before the checks
+    err = {"a": close_errors(a_gpu, ref["a"]), "o (stage)": close_errors(host(buf.o), o_stage),
+           "y (stage)": close_errors(host(y), y_stage), "y (composed)": close_errors(host(y), ref["y"]),
+           "h codes differing from the oracle's own h": float(np.mean(hq_ref != ref["h_q"])),
+           "a values differing from the oracle's": float(np.mean(a_gpu != ref["a"]))}
+    print(f"ffn_w8 w_mode={w_mode}:", err)
+    assert_close(a_gpu, ref["a"], "a")
+    assert np.array_equal(host(buf.h_q), hq_ref) and np.array_equal(host(buf.h_s), hs_ref)
+    assert_close(host(buf.o), o_stage, "o (stage)")
+    assert_close(host(y), y_stage, "y (stage)")
+    if w_mode == synth.PER_ROW:
+        assert_close(host(y), ref["y"], "y (composed)", rel_fro=5e-3)
+    else:
+        assert_close(host(y), ref["y"], "y (composed)", rel_fro=1e-2, rel_elt=3e-2)
+
+
+@pytest.mark.parametrize("name", ["mixtral_w8", "prefill_w8"])
+def test_ffn_w8_full_size_sampled_tokens(name):
+    """The full-size int8-weight layers in the benchmark's launch
+    configuration, on sampled tokens that the oracle evaluates one by one:
+    the token's codes bit-exact, a within 2e-3, h codes of the GPU's a
+    bit-exact, o of the GPU's h and y of the GPU's o within 2e-3, the
+    composed y within 5e-3 (1e-2 with blockwise weight scales)."""
+    cfg = synth.CONFIGS[name]
+    x_t = synth.activations(cfg, 0, device="cuda")
+    ids, w = synth.routing(cfg, 0)
+    w_in, w_out = synth.expert_weights(cfg, 0, device="cuda")
+    W = moe.prepare_weights_w8(w_in, w_out, cfg.w_mode)
+    buf = moe.FFNBuffers(cfg.T, cfg.D, cfg.E, cfg.k, cfg.F, cfg.act_mode, "cuda")
+    y = moe.ffn_forward(x_t, dev(ids), dev(w), W, cfg.act_mode, buf)
+    assert moe.device_error() == 0
+    yh, xb, pos = host(y), host(x_t), host(buf.sort["pos"])
+    rng = np.random.default_rng(2)
+    tokens = rng.choice(cfg.T, 3, replace=False)
+    ys, ys_stage = [], []
+    one = np.array([1], np.int32)
+    for t in tokens:
+        xq, xs = oracle.quantize_rows(xb[t:t + 1], cfg.act_mode)
+        acc = np.zeros(cfg.D)
+        o_rows = []
+        for j in range(cfg.k):
+            e = int(ids[t, j])
+            r = int(pos[t * cfg.k + j])
+            assert np.array_equal(host(buf.sort["xs_q"][r:r + 1]), xq)
+            assert np.array_equal(host(buf.sort["xs_scale"][r:r + 1]), xs)
+            qin, sin, _, qo, so, _ = oracle.prepare_weights_w8(host(w_in[e:e + 1]), host(w_out[e:e + 1]), cfg.w_mode)
+            a = oracle.gmm_w8(xq, xs, cfg.act_mode, qin, sin, cfg.w_mode, one)
+            a_gpu = host(buf.a[r:r + 1])
+            assert_close(a_gpu, a, f"{name}: a[t={t}, j={j}]")
+            hq_ref, hs_ref, _ = oracle.swiglu_quant(a_gpu, cfg.act_mode)
+            hq_gpu, hs_gpu = host(buf.h_q[r:r + 1]), host(buf.h_s[r:r + 1])
+            assert np.array_equal(hq_gpu, hq_ref) and np.array_equal(hs_gpu, hs_ref)
+            o_stage = oracle.gmm_w8(hq_gpu, hs_gpu, cfg.act_mode, qo, so, cfg.w_mode, one)
+            o_gpu = host(buf.o[r:r + 1])
+            assert_close(o_gpu, o_stage, f"{name}: o[t={t}, j={j}] (stage)")
+            hq_c, hs_c, _ = oracle.swiglu_quant(a, cfg.act_mode)
+            o_c = oracle.gmm_w8(hq_c, hs_c, cfg.act_mode, qo, so, cfg.w_mode, one)
+            acc += float(w[t, j]) * oracle.bf16_to_f64(o_c)[0]
+            o_rows.append(o_gpu[0])
+        ys.append(oracle.f64_to_bf16(acc))
+        ys_stage.append(oracle.combine(np.stack(o_rows), np.arange(cfg.k, dtype=np.int32), w[t:t + 1], cfg.k)[0])
+    assert_close(yh[tokens], np.stack(ys_stage), f"{name}: y sampled (stage)")
+    assert_close(yh[tokens], np.stack(ys), f"{name}: y sampled (composed)",
+                 rel_fro=5e-3 if cfg.w_mode == synth.PER_ROW else 1e-2)
