@@ -1696,45 +1696,45 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
 // e4m3 value and every integer in [-127, 127] exactly, so both operands are
 // converted to f16 on the SM and contracted by tcgen05.mma kind::f16 with
 // fp32 accumulation:
-//   - the weights are the A operand, read from tensor memory: eight warps
-//     turn each stage's int8 rows into f16 (the byte under the exponent of
-//     1024 + 128, then one f16 subtraction) and store them with tcgen05.st,
-//     so the converted weights never pass through shared memory;
-//   - the activations are the B operand: four warps turn the stage's e4m3
-//     rows into f16 (cvt.f16x2.e4m3x2) in the 128-byte-swizzled K-major
-//     layout the MMA reads from shared memory.
-// A tile is 256 channels (two M = 128 MMAs into two tensor-memory
-// accumulators whose lanes are channels) by 128 tokens (the MMA's N); the
-// epilogue applies s_x s_w and writes the transposed accumulators, 32
-// channels of one token row a store.  Blockwise weight scales: each block
-// scale is divided by the channel's largest one, S, and the quotient r, held
-// as an f16 pair r_hi + r_lo (r to about 22 bits), multiplies the block's
-// converted codes in one fused f16 multiply-add, q r_hi + (q r_lo), so each
-// converted weight q r carries a single f16 rounding; S leaves the sum, and
-// one accumulator runs over the whole K loop.
-constexpr int kW8Tok = 128;                     // tokens per tile: the MMA's N
-constexpr int kW8Ks = 64;                       // K per stage: 64 code bytes, one 128-byte f16 row
-constexpr int kW8BoxBytes = 128 * kW8Ks;        // one TMA box: 128 rows x 64 bytes (64-byte swizzle)
-constexpr int kW8RawStages = 6;                 // TMA ring: two weight boxes and one activation box a stage
+//   - the weights are the A operand, read from tensor memory: four warps per
+//     128 channels turn each stage's int8 rows into f16 (the byte under the
+//     exponent of 1024 + 128, then one f16 subtraction) and store them with
+//     tcgen05.st, so the converted weights never pass through shared memory;
+//   - the activations are the B operand: one warp per 32 token rows turns
+//     the stage's e4m3 rows into f16 (cvt.f16x2.e4m3x2) in the
+//     128-byte-swizzled K-major layout the MMA reads from shared memory.
+// Two tile shapes (the accumulators take tensor-memory columns 0..255 either
+// way, the converted-weight ring the other 256):
+//   TOK = 256: 128 channels x 256 tokens, one M = 128, N = 256 MMA per K step
+//              (an M = 128 MMA runs at the full rate only at N = 256);
+//   TOK = 128: 256 channels x 128 tokens, two M = 128, N = 128 MMAs into two
+//              accumulators, for small groups (less padding of the last tile).
+// The epilogue applies s_x s_w and writes the transposed accumulators (TMEM
+// lanes are channels), 32 channels of one token row a store.  Blockwise
+// weight scales: each block scale is divided by the channel's largest one,
+// S, and the quotient r, held as an f16 pair r_hi + r_lo (r to about 22
+// bits), multiplies the block's converted codes in one fused f16
+// multiply-add, q r_hi + (q r_lo), so each converted weight q r carries a
+// single f16 rounding; S leaves the sum, and one accumulator runs over the
+// whole K loop.
+constexpr int kW8Ks = 64;                 // K per stage: 64 code bytes, one 128-byte f16 row
+constexpr int kW8BoxBytes = 128 * kW8Ks;  // one TMA box: 128 rows x 64 bytes (64-byte swizzle)
+constexpr int kW8RawStages = 6;           // TMA ring: three boxes (weights and activations) a stage
 constexpr int kW8RawBytes = 3 * kW8BoxBytes;
-constexpr int kW8XStages = 4;                   // ring of converted (f16) activation tiles
-constexpr int kW8XBytes = kW8Tok * kW8Ks * 2;
-constexpr int kW8AStages = 4;                   // tensor-memory ring of converted weights, 64 columns a stage
-constexpr int kW8AColBase = 2 * kW8Tok;         // after the two accumulators
-constexpr int kW8WConvWarps = 8, kW8XConvWarps = 4, kW8EpiWarps = 8;
-// warp 0 TMA producer, 1 MMA issuer, 2..9 weight converters, 10..13
-// activation converters, 14..21 epilogue
-constexpr int kW8Warps = 2 + kW8WConvWarps + kW8XConvWarps + kW8EpiWarps;
-constexpr uint32_t kW8Idesc = idesc_f16_f32(128, kW8Tok);
-static_assert(kW8AColBase + 64 * kW8AStages <= 512, "int8-weight tensor-memory plan");
+constexpr int kW8AColBase = 256;          // the converted-weight ring's first tensor-memory column
+constexpr int kW8MaxAStages = 8, kW8MaxXStages = 4;
+constexpr int kW8ConvWarps = 12, kW8EpiWarps = 8;
+// warp 0 TMA producer, 1 MMA issuer, 2.. weight converters, then activation
+// converters (12 converter warps), then 8 epilogue warps
+constexpr int kW8Warps = 2 + kW8ConvWarps + kW8EpiWarps;
 
 struct W8Ctl {
   uint64_t rfull[kW8RawStages];   // a stage's three boxes have landed
   uint64_t rempty[kW8RawStages];  // every converter warp has read the stage
-  uint64_t afull[kW8AStages];     // converted weights are in tensor memory
-  uint64_t aempty[kW8AStages];    // the MMAs that read them completed
-  uint64_t xfull[kW8XStages];     // converted activations are in shared memory
-  uint64_t xempty[kW8XStages];
+  uint64_t afull[kW8MaxAStages];  // converted weights are in tensor memory
+  uint64_t aempty[kW8MaxAStages]; // the MMAs that read them completed
+  uint64_t xfull[kW8MaxXStages];  // converted activations are in shared memory
+  uint64_t xempty[kW8MaxXStages];
   uint64_t dfull, dempty;         // the accumulators hold a finished tile / have been read
   uint64_t drain;
   uint64_t never;  // test hook: a barrier that nothing arrives on
@@ -1747,12 +1747,62 @@ struct W8Ctl {
   int tile_prefix[kMaxGroups + 1];
   int gsize[kMaxGroups];
 };
-constexpr size_t kW8Smem =
-    1024 + static_cast<size_t>(kW8RawStages) * kW8RawBytes + static_cast<size_t>(kW8XStages) * kW8XBytes + sizeof(W8Ctl);
-static_assert(kW8Smem <= 232448, "int8-weight gmm: shared memory per CTA");
 
-// Blockwise weight scales of one channel: 1 / (its largest block scale), 0
-// for a channel past N or one whose scales are all zero.
+template <int TOK>
+struct W8Cfg {
+  static_assert(TOK == 128 || TOK == 256, "int8-weight tile: 128 or 256 tokens");
+  static constexpr int HALVES = TOK == 128 ? 2 : 1;  // 128-channel weight tiles (MMA A operands) per tile
+  static constexpr int CH = 128 * HALVES;             // channels per tile
+  static constexpr int XBOXES = TOK / 128;            // activation boxes per stage
+  static constexpr int WCONV = 4 * HALVES;            // weight converter warps
+  static constexpr int XCONV = TOK / 32;              // activation converter warps
+  static constexpr int XSTAGES = TOK == 128 ? 4 : 2;  // ring of converted activation tiles
+  static constexpr int XBYTES = TOK * kW8Ks * 2;
+  static constexpr int ACOLS = 32 * HALVES;           // tensor-memory columns of one converted-weight stage
+  static constexpr int ASTAGES = (512 - kW8AColBase) / ACOLS;
+  static constexpr uint32_t IDESC = idesc_f16_f32(128, TOK);
+  static constexpr size_t SMEM =
+      1024 + static_cast<size_t>(kW8RawStages) * kW8RawBytes + static_cast<size_t>(XSTAGES) * XBYTES + sizeof(W8Ctl);
+  static_assert(WCONV + XCONV == kW8ConvWarps && HALVES + XBOXES == 3, "int8-weight roles");
+  static_assert(ASTAGES <= kW8MaxAStages && XSTAGES <= kW8MaxXStages && HALVES * TOK <= kW8AColBase,
+                "int8-weight tensor-memory plan");
+  static_assert(SMEM <= 232448, "int8-weight gmm: shared memory per CTA");
+};
+
+struct W8Tile {
+  int el;    // local group
+  int row0;  // first row (token) of the tile
+  int rows;  // valid rows in the tile
+  int n0;    // first channel
+  int by;    // first weight row: el * N + n0
+};
+
+// Tile t: expert-major, then channel tile, then token tile (so that the CTAs
+// running at the same time share one expert's weights), from the group
+// tables built with units of TOK rows.
+template <int TOK>
+__device__ __forceinline__ W8Tile w8_tile(const Params& p, const W8Ctl* ctl, int t) {
+  int lo = 0, hi = p.El;  // tile_prefix[lo] <= t < tile_prefix[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (ctl->tile_prefix[mid] <= t) lo = mid; else hi = mid;
+  }
+  while (lo + 1 < p.El && ctl->tile_prefix[lo + 1] <= t) ++lo;  // skip empty groups
+  const int sz = ctl->gsize[lo];
+  const int mt = (sz + TOK - 1) / TOK;
+  const int local = t - ctl->tile_prefix[lo];
+  const int nt = local / mt, mi = local - nt * mt;
+  W8Tile tl;
+  tl.el = lo;
+  tl.row0 = ctl->gstart[lo] + mi * TOK;
+  tl.rows = min(TOK, sz - mi * TOK);
+  tl.n0 = nt * W8Cfg<TOK>::CH;
+  tl.by = lo * p.N + tl.n0;
+  return tl;
+}
+
+// Blockwise weight scales of one channel: its largest block scale (0 for a
+// channel past N).
 __device__ __forceinline__ float w8_block_smax(const float* s_blk, int kblocks, int N, bool ok) {
   float m = 0.0f;
   if (ok)
@@ -1760,28 +1810,31 @@ __device__ __forceinline__ float w8_block_smax(const float* s_blk, int kblocks, 
   return m;
 }
 
+template <int TOK>
 __global__ void __launch_bounds__(kW8Warps * 32, 1)
     w8_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const Params p) {
+  using C = W8Cfg<TOK>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw_addr);
   const uint32_t xring = base + kW8RawStages * kW8RawBytes;
-  W8Ctl* ctl = reinterpret_cast<W8Ctl*>(base_ptr + kW8RawStages * kW8RawBytes + kW8XStages * kW8XBytes);
+  W8Ctl* ctl = reinterpret_cast<W8Ctl*>(base_ptr + kW8RawStages * kW8RawBytes + C::XSTAGES * C::XBYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  if (warp == 0) build_group_tables<false, false>(p, ctl);
+  // group tables in units of TOK rows (two 128-row M tiles a unit for TOK = 256)
+  if (warp == 0) build_group_tables<false, TOK == 256>(p, ctl);
   if (threadIdx.x == 32) {
     for (int s = 0; s < kW8RawStages; ++s) {
       mbar_init(smem_u32(&ctl->rfull[s]), 1);
-      mbar_init(smem_u32(&ctl->rempty[s]), kW8WConvWarps + kW8XConvWarps);
+      mbar_init(smem_u32(&ctl->rempty[s]), kW8ConvWarps);
     }
-    for (int a = 0; a < kW8AStages; ++a) {
-      mbar_init(smem_u32(&ctl->afull[a]), kW8WConvWarps);
+    for (int a = 0; a < C::ASTAGES; ++a) {
+      mbar_init(smem_u32(&ctl->afull[a]), C::WCONV);
       mbar_init(smem_u32(&ctl->aempty[a]), 1);
     }
-    for (int x = 0; x < kW8XStages; ++x) {
-      mbar_init(smem_u32(&ctl->xfull[x]), kW8XConvWarps);
+    for (int x = 0; x < C::XSTAGES; ++x) {
+      mbar_init(smem_u32(&ctl->xfull[x]), C::XCONV);
       mbar_init(smem_u32(&ctl->xempty[x]), 1);
     }
     mbar_init(smem_u32(&ctl->dfull), 1);
@@ -1820,7 +1873,7 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
     if (lane == 0) {
       uint32_t it = 0;
       for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
-        const Tile tl = get_tile<kFinal, false>(p, ctl, t, 0);
+        const W8Tile tl = w8_tile<TOK>(p, ctl, t);
         for (int ks = 0; ks < nks; ++ks) {
           const int s = it % kW8RawStages;
           if (!mbar_wait_bounded(smem_u32(&ctl->rempty[s]), ((it / kW8RawStages) & 1) ^ 1, abort_flag,
@@ -1830,9 +1883,12 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
           }
           const uint32_t sa = base + s * kW8RawBytes, fb = smem_u32(&ctl->rfull[s]);
           mbar_arrive_expect_tx(fb, kW8RawBytes);
-          tma_load_2d(sa, &tmW, ks * kW8Ks, tl.by, fb);                      // channels n0 .. n0 + 127
-          tma_load_2d(sa + kW8BoxBytes, &tmW, ks * kW8Ks, tl.by + 128, fb);  // n0 + 128 .. n0 + 255
-          tma_load_2d(sa + 2 * kW8BoxBytes, &tmX, ks * kW8Ks, tl.ay, fb);    // the tile's 128 token rows
+#pragma unroll
+          for (int h = 0; h < C::HALVES; ++h)  // weight rows (channels) n0 + 128 h ..
+            tma_load_2d(sa + h * kW8BoxBytes, &tmW, ks * kW8Ks, tl.by + 128 * h, fb);
+#pragma unroll
+          for (int b = 0; b < C::XBOXES; ++b)  // token rows row0 + 128 b ..
+            tma_load_2d(sa + (C::HALVES + b) * kW8BoxBytes, &tmX, ks * kW8Ks, tl.row0 + 128 * b, fb);
           ++it;
         }
       }
@@ -1857,20 +1913,20 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
         }
         tc_fence_after();
         for (int ks = 0; ks < nks; ++ks) {
-          const int a = it % kW8AStages, x = it % kW8XStages;
-          if (!mbar_wait_bounded(smem_u32(&ctl->afull[a]), (it / kW8AStages) & 1, abort_flag, kWaitLimitNs) ||
-              !mbar_wait_bounded(smem_u32(&ctl->xfull[x]), (it / kW8XStages) & 1, abort_flag, kWaitLimitNs)) {
+          const int a = it % C::ASTAGES, x = it % C::XSTAGES;
+          if (!mbar_wait_bounded(smem_u32(&ctl->afull[a]), (it / C::ASTAGES) & 1, abort_flag, kWaitLimitNs) ||
+              !mbar_wait_bounded(smem_u32(&ctl->xfull[x]), (it / C::XSTAGES) & 1, abort_flag, kWaitLimitNs)) {
             timed_out = true;
             break;
           }
           tc_fence_after();
-          const uint64_t db = smem_desc_sw128(xring + x * kW8XBytes);
-          const uint32_t at = tmem_base + kW8AColBase + 64 * a;
+          const uint64_t db = smem_desc_sw128(xring + x * C::XBYTES);
+          const uint32_t at = tmem_base + kW8AColBase + C::ACOLS * a;
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
+          for (int h = 0; h < C::HALVES; ++h)
 #pragma unroll
             for (int k16 = 0; k16 < kW8Ks / 16; ++k16)  // K = 16: 8 tensor-memory columns, 32 bytes of a B row
-              mma_f16_tmem_a(tmem_base + kW8Tok * h, at + 32 * h + 8 * k16, db + 2 * k16, kW8Idesc,
+              mma_f16_tmem_a(tmem_base + TOK * h, at + 32 * h + 8 * k16, db + 2 * k16, C::IDESC,
                              (ks > 0 || k16 > 0) ? 1u : 0u);
           mma_commit(smem_u32(&ctl->aempty[a]));
           mma_commit(smem_u32(&ctl->xempty[x]));
@@ -1889,9 +1945,9 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
       }
     }
     __syncwarp();
-  } else if (warp < 2 + kW8WConvWarps) {
+  } else if (warp < 2 + C::WCONV) {
     // --------------------------------------------------- weight converters
-    // warp (h, q): rows 32 q .. 32 q + 31 of weight half h (the tile's
+    // warp (h, q): rows 32 q .. 32 q + 31 of weight tile h (the tile's
     // channels 128 h ..), which are the tensor-memory lanes of that quarter
     const int h = (warp - 2) >> 2, q4 = warp & 3;
     const int r = 32 * q4 + lane;
@@ -1899,7 +1955,7 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
     const int swz = (r >> 1) & 3;  // 64-byte swizzle: 16-byte chunk j of row r sits at j ^ ((r / 2) % 4)
     uint32_t it = 0;
     for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
-      const Tile tl = get_tile<kFinal, false>(p, ctl, t, 0);
+      const W8Tile tl = w8_tile<TOK>(p, ctl, t);
       const int ch = tl.n0 + 128 * h + r;
       const bool ch_ok = ch < p.N;
       const float* s_blk = p.rhs_scale + static_cast<int64_t>(tl.el) * p.kblocks * p.N + (ch_ok ? ch : 0);
@@ -1932,8 +1988,8 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
           rhi2 = hb | (hb << 16);
           rlo2 = lb | (lb << 16);
         }
-        const int a = it % kW8AStages;
-        if (!mbar_wait_bounded_warp(smem_u32(&ctl->aempty[a]), ((it / kW8AStages) & 1) ^ 1, abort_flag,
+        const int a = it % C::ASTAGES;
+        if (!mbar_wait_bounded_warp(smem_u32(&ctl->aempty[a]), ((it / C::ASTAGES) & 1) ^ 1, abort_flag,
                                     kWaitLimitNs)) {
           timed_out = true;
           break;
@@ -1964,7 +2020,7 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
             f[8 * j + 2 * c + 1] = hi;
           }
         }
-        tmem_st_32x32b_x32(tmem_base + lane_addr + kW8AColBase + 64 * a + 32 * h, f);
+        tmem_st_32x32b_x32(tmem_base + lane_addr + kW8AColBase + C::ACOLS * a + 32 * h, f);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -1976,10 +2032,10 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
       *abort_flag = 1;
       ctl->err = 2;
     }
-  } else if (warp < 2 + kW8WConvWarps + kW8XConvWarps) {
+  } else if (warp < 2 + kW8ConvWarps) {
     // ----------------------------------------------- activation converters
-    const int r = 32 * (warp - 2 - kW8WConvWarps) + lane;  // token row of the tile
-    const int swz = (r >> 1) & 3;
+    const int r = 32 * (warp - 2 - C::WCONV) + lane;  // token row of the tile
+    const int swz = (r >> 1) & 3;                      // the same within its 128-row box
     uint32_t it = 0;
     for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
       for (int ks = 0; ks < nks; ++ks) {
@@ -1988,22 +2044,23 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
           timed_out = true;
           break;
         }
-        const uint8_t* src = base_ptr + s * kW8RawBytes + 2 * kW8BoxBytes + r * kW8Ks;
+        const uint8_t* src =
+            base_ptr + s * kW8RawBytes + (C::HALVES + (r >> 7)) * kW8BoxBytes + (r & 127) * kW8Ks;
         uint4 xv[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) xv[j] = *reinterpret_cast<const uint4*>(src + 16 * (j ^ swz));
         fence_proxy_async_smem();  // as above: generic reads before the TMA refill
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ctl->rempty[s]));
-        const int x = it % kW8XStages;
-        if (!mbar_wait_bounded_warp(smem_u32(&ctl->xempty[x]), ((it / kW8XStages) & 1) ^ 1, abort_flag,
+        const int x = it % C::XSTAGES;
+        if (!mbar_wait_bounded_warp(smem_u32(&ctl->xempty[x]), ((it / C::XSTAGES) & 1) ^ 1, abort_flag,
                                     kWaitLimitNs)) {
           timed_out = true;
           break;
         }
         // row r of the f16 tile: 128 bytes in 8-row / 1024-byte atoms, its
         // 16-byte chunk c at c ^ (r % 8) (the 128-byte swizzle)
-        uint8_t* dst = base_ptr + (xring - base) + x * kW8XBytes + (r >> 3) * 1024 + (r & 7) * 128;
+        uint8_t* dst = base_ptr + (xring - base) + x * C::XBYTES + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint32_t wd[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
@@ -2029,15 +2086,19 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int h = (warp - 2 - kW8WConvWarps - kW8XConvWarps) >> 2, q4 = warp & 3;
+    // warp (g, q): accumulator columns 128 g .. 128 g + 127 in lane quarter
+    // q; with TOK = 128 those are all 128 tokens of channel half g, with
+    // TOK = 256 tokens 128 g .. of the tile's 128 channels
+    const int g = (warp - 2 - kW8ConvWarps) >> 2, q4 = warp & 3;
     const int r = 32 * q4 + lane;
+    const int ch_off = TOK == 128 ? 128 * g : 0, tok0 = TOK == 128 ? 0 : 128 * g;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q4) << 16;
     uint16_t* out = static_cast<uint16_t*>(p.out);
     uint32_t tcount = 0;
     if (p.stall && !mbar_wait_bounded_warp(smem_u32(&ctl->never), 0, abort_flag, p.stall_ns)) timed_out = true;
     for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
-      const Tile tl = get_tile<kFinal, false>(p, ctl, t, 0);
-      const int ch = tl.n0 + 128 * h + r;
+      const W8Tile tl = w8_tile<TOK>(p, ctl, t);
+      const int ch = tl.n0 + ch_off + r;
       const bool ch_ok = ch < p.N;
       float s_w;
       if (w_blk)
@@ -2047,11 +2108,11 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
         s_w = ch_ok ? __ldg(p.rhs_scale + static_cast<int64_t>(tl.el) * p.N + ch) : 0.0f;
       else
         s_w = __ldg(p.rhs_scale);
-      // token scales: lane j holds those of the tile's tokens j, 32 + j, 64 + j, 96 + j
+      // token scales: lane j holds those of the warp's tokens j, 32 + j, 64 + j, 96 + j
       float sx[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int tok = 32 * c + lane;
+        const int tok = tok0 + 32 * c + lane;
         sx[c] = p.lhs_mode == MOE_SCALE_PER_ROW ? (tok < tl.rows ? __ldg(p.lhs_scale + tl.row0 + tok) : 0.0f)
                                                 : __ldg(p.lhs_scale);
       }
@@ -2061,20 +2122,20 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
       }
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < kW8Tok / 32; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_base + lane_addr + kW8Tok * h + 32 * c, v);
+        tmem_ld_32x32b_x32(tmem_base + lane_addr + 128 * g + 32 * c, v);
         tmem_wait_ld();
-        if (c == kW8Tok / 32 - 1) {  // the accumulators are read: the next tile's MMAs may start
+        if (c == 3) {  // the accumulators are read: the next tile's MMAs may start
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&ctl->dempty));
         }
-        uint16_t* orow = out + (static_cast<int64_t>(tl.row0) + 32 * c) * p.N + ch;
+        uint16_t* orow = out + (static_cast<int64_t>(tl.row0) + tok0 + 32 * c) * p.N + ch;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const float sxj = __shfl_sync(0xffffffffu, sx[c], j);
-          if (ch_ok && 32 * c + j < tl.rows)
+          if (ch_ok && tok0 + 32 * c + j < tl.rows)
             orow[static_cast<int64_t>(j) * p.N] =
                 static_cast<uint16_t>(pack_bf16x2(__fmul_rn(__uint_as_float(v[j]), __fmul_rn(s_w, sxj)), 0.0f));
         }
@@ -2603,6 +2664,22 @@ moe_status launch_mma(const CUtensorMap& A, const CUtensorMap& B, const CUtensor
 // test hook (moe_test_stall_epilogue): 0, or the wait limit in ns
 std::atomic<uint64_t> g_stall_ns{0};
 
+// gmm_fp8_w8 with tiles of TOK tokens: one persistent CTA per SM at most.
+template <int TOK>
+moe_status launch_w8(const CUtensorMap& X, const CUtensorMap& W, Params p, int E_local, cudaStream_t st) {
+  using C = W8Cfg<TOK>;
+  p.ntiles = static_cast<int>((p.N + C::CH - 1) / C::CH);
+  MOE_CUDA_TRY(cudaFuncSetAttribute(w8_kernel<TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(C::SMEM)));
+  const int sms = sm_count();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const int64_t units = ((p.M + TOK - 1) / TOK + E_local) * static_cast<int64_t>(p.ntiles);
+  const int grid = units < sms ? static_cast<int>(units) : sms;
+  w8_kernel<TOK><<<grid, kW8Warps * 32, C::SMEM, st>>>(X, W, p);
+  MOE_CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
 bool valid_lhs_mode(int m) {
   return m == MOE_SCALE_PER_ROW || m == MOE_SCALE_PER_ROW_BLOCK128 || m == MOE_SCALE_PER_TENSOR;
 }
@@ -2907,7 +2984,7 @@ extern "C" moe_status gmm_fp8_w8(const uint8_t* lhs_q, const float* lhs_scale, m
     MOE_CUDA_TRY(cudaGetLastError());
   }
   CUtensorMap X, W;
-  if (!make_map_u8_64(&X, lhs_q, K, M, K, kW8Tok)) return MOE_ERR_CUDA;
+  if (!make_map_u8_64(&X, lhs_q, K, M, K, 128)) return MOE_ERR_CUDA;
   if (!make_map_u8_64(&W, rhs_q, K, static_cast<uint64_t>(E_local) * N, K, 128)) return MOE_ERR_CUDA;
   Params p{};
   p.group_sizes = group_sizes;
@@ -2918,7 +2995,6 @@ extern "C" moe_status gmm_fp8_w8(const uint8_t* lhs_q, const float* lhs_scale, m
   p.K = static_cast<int>(K);
   p.N = static_cast<int>(N);
   p.kblocks = static_cast<int>((K + BK - 1) / BK);
-  p.ntiles = static_cast<int>((N + Cfg<kFinal>::BN - 1) / Cfg<kFinal>::BN);  // 256 channels a tile
   p.lhs_scale = lhs_scale;
   p.lhs_mode = lhs_mode;
   p.rhs_scale = rhs_scale;
@@ -2926,14 +3002,9 @@ extern "C" moe_status gmm_fp8_w8(const uint8_t* lhs_q, const float* lhs_scale, m
   p.out = out;
   p.stall_ns = g_stall_ns.load();
   p.stall = p.stall_ns != 0;
-  MOE_CUDA_TRY(cudaFuncSetAttribute(w8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kW8Smem)));
-  const int sms = sm_count();
-  if (sms <= 0) return MOE_ERR_CUDA;
-  const int units = gmm_max_units<kFinal, false>(M, E_local, p.ntiles);
-  const int grid = units < sms ? units : sms;
-  w8_kernel<<<grid, kW8Warps * 32, kW8Smem, st>>>(X, W, p);
-  MOE_CUDA_TRY(cudaGetLastError());
-  return MOE_OK;
+  // the 256-token tile when the local groups average 256 rows or more (the
+  // full-rate N = 256 MMA), else the 128-token tile (less padding)
+  return M >= 256ll * E_local ? launch_w8<256>(X, W, p, E_local, st) : launch_w8<128>(X, W, p, E_local, st);
 }
 
 extern "C" size_t tgmm_fp8_workspace_bytes(int64_t M, int64_t K, int64_t N, int E_local) {

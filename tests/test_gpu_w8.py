@@ -18,9 +18,11 @@ so, through SwiGLU, one e4m3 step (2^-3) in a few tenths of a per cent of the
 h codes; measured, the composed y then differs by 6-7e-3.  With per-channel
 scales the converted weights are the exact integers and a matches the
 oracle's to fp32 accumulation order.
-Cases cover several tiles, ragged and empty groups, N tails, K tails, long
-K, blockwise scales spread over many binades, expert-parallel shards and the
-bounded-wait failure path."""
+Cases cover both tile shapes (256 tokens x 128 channels when the local
+groups average 256 rows or more, else 128 tokens x 256 channels), several
+tiles, ragged and empty groups, N tails, K tails, long K, blockwise scales
+spread over many binades, expert-parallel shards, repeated calls (the bits
+must not change) and the bounded-wait failure path."""
 
 import numpy as np
 import pytest
@@ -89,6 +91,7 @@ def w8_args(a, sa, a_mode, q, sw, w_mode, sizes):
 
 
 GMM_CASES = [
+    # 128-token tiles (the groups average fewer than 256 rows)
     (128, 128, 256, 1),       # one tile, two stages
     (1, 128, 256, 1),         # a single row
     (200, 256, 512, 3),       # ragged groups, several tiles
@@ -99,6 +102,12 @@ GMM_CASES = [
     (129, 384, 256, 2),       # a one-row group past a full tile
     (3000, 3072, 768, 24),    # many groups, several tiles per group
     (1, 4096, 256, 1),
+    # 256-token tiles
+    (257, 256, 256, 1),       # a full tile and a one-row tile
+    (1024, 1024, 512, 2),     # ragged groups
+    (700, 768, 384, 2),       # N tail of a 128-channel tile, partial token tiles
+    (4096, 2048, 272, 4),     # N tail of 16
+    (3000, 4096, 512, 3),     # long K
 ]
 
 
@@ -144,20 +153,21 @@ def test_gmm_w8_static_scales(a_mode, w_mode):
     assert_close(host(out), ref, f"gmm_w8 modes {a_mode}/{w_mode}")
 
 
-@pytest.mark.parametrize("K", [80, 208, 1040])
-def test_gmm_w8_k_tail(K):
+@pytest.mark.parametrize("K,M", [(80, 300), (208, 300), (1040, 300), (208, 1200), (1040, 1200)])
+def test_gmm_w8_k_tail(K, M):
     # K a multiple of 16 but not of the 64-wide stage: the last stage's boxes
-    # read zeros past K
-    sizes, a, sa, q, sw = make_w8_case(60 + K, 300, K, 256, 3)
+    # read zeros past K (M = 300: 128-token tiles; 1200: 256-token tiles)
+    sizes, a, sa, q, sw = make_w8_case(60 + K + M, M, K, 256, 3)
     ref = oracle.gmm_w8(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW, sizes)
     out = moe.gmm_w8(*w8_args(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW, sizes))
     assert moe.device_error() == 0
     assert_close(host(out), ref, f"gmm_w8 K={K}")
 
 
-@pytest.mark.parametrize("K,w_mode", [(512, synth.PER_ROW), (4096, synth.PER_ROW_BLOCK128)])
-def test_gmm_w8_expert_parallel_shard(K, w_mode):
-    M, N, E = 1000, 384, 9
+@pytest.mark.parametrize("K,w_mode,M", [(512, synth.PER_ROW, 1000), (4096, synth.PER_ROW_BLOCK128, 1000),
+                                        (1024, synth.PER_ROW, 4000), (2048, synth.PER_ROW_BLOCK128, 4000)])
+def test_gmm_w8_expert_parallel_shard(K, w_mode, M):
+    N, E = 384, 9
     sizes, a, sa, q, sw = make_w8_case(17 + K, M, K, N, E, w_mode=w_mode, zero_frac=0.2, spread=2)
     g0, El = 2, 4
     q, sw = np.ascontiguousarray(q[g0:g0 + El]), np.ascontiguousarray(sw[g0:g0 + El])
