@@ -41,7 +41,8 @@ __all__ = [
     "quantize_rows", "quantize_weights", "ragged_sort", "gmm", "gmm_swiglu", "swiglu_fusable", "swiglu_fuse_pays", "swiglu_quant", "ragged_gather_reduce",
     "gather_scale_quant", "swiglu_bwd_quant", "quantize_group_cols", "tgmm", "transpose_u8",
     "router_topk", "router_backward", "MX32", "quantize_rows_mx", "quantize_weights_mx", "quantize_sort_mx",
-    "gmm_mx", "gmm_mx_swiglu", "swiglu_quant_mx", "quantize_weights_int8", "gmm_w8", "prepare_weights_w8",
+    "gmm_mx", "gmm_mx_swiglu", "swiglu_quant_mx", "quantize_weights_int8", "gmm_w8", "gmm_w8_workspace_bytes",
+    "prepare_weights_w8",
     "ExpertWeights", "prepare_weights", "FFNBuffers", "ffn_forward", "ffn_backward",
 ]
 
@@ -281,8 +282,12 @@ def gmm(lhs_q, lhs_scale, lhs_mode, rhs_q, rhs_scale, rhs_mode, group_sizes, gro
 
 
 def gmm_w8(lhs_q, lhs_scale, lhs_mode, rhs_q, rhs_scale, rhs_mode, group_sizes, group_offset: int = 0,
-           E_local: Optional[int] = None, out=None):
-    """Grouped matmul with int8 weights rhs_q [E_local, N, K] -> bf16 [M, N]."""
+           E_local: Optional[int] = None, out=None, workspace=None):
+    """Grouped matmul with int8 weights rhs_q [E_local, N, K] -> bf16 [M, N].
+
+    workspace: optional uint8 device buffer of gmm_w8_workspace_bytes(M, K)
+    bytes or more; with it the activations are decoded to f16 there first
+    (the same result, faster where the tensor pipe binds)."""
     M, K = lhs_q.shape
     El, N, K2 = rhs_q.shape
     if K2 != K:
@@ -292,9 +297,15 @@ def gmm_w8(lhs_q, lhs_scale, lhs_mode, rhs_q, rhs_scale, rhs_mode, group_sizes, 
     E = group_sizes.numel()
     E_local = El if E_local is None else E_local
     out = torch.empty(M, N, dtype=torch.bfloat16, device=lhs_q.device) if out is None else out
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     check(lib().gmm_fp8_w8(_p(lhs_q), _p(lhs_scale), lhs_mode, _p(rhs_q), _p(rhs_scale), rhs_mode,
-                           _p(group_sizes), E, group_offset, E_local, M, K, N, _p(out), _s()), "gmm_fp8_w8")
+                           _p(group_sizes), E, group_offset, E_local, M, K, N, _p(out), _p(workspace), ws_bytes,
+                           _s()), "gmm_fp8_w8")
     return out
+
+
+def gmm_w8_workspace_bytes(M: int, K: int) -> int:
+    return int(lib().gmm_fp8_w8_workspace_bytes(M, K))
 
 
 def gmm_ksplit(lhs_q, lhs_scale, lhs_mode, rhs_q, rhs_scale2, K_split: int, group_sizes, group_offset: int = 0,
@@ -584,10 +595,20 @@ class FFNBuffers:
         self.h_s = _scale_buf(act_mode, R, F, device)
         self.o = f(R, D, dt=torch.bfloat16)
         self.y = f(T, D, dt=torch.bfloat16)
+        self._w8_ws = None
         if backward:
             self.dH = f(R, F, dt=torch.bfloat16)
             self.dXs = f(R, D, dt=torch.bfloat16)
             self.dX = f(T, D, dt=torch.bfloat16)
+
+    def w8_workspace(self) -> torch.Tensor:
+        """The int8-weight contractions' f16 activation workspace, allocated on
+        first use: 2 bytes per element of the larger of their two lhs,
+        [T*k, D] and [T*k, F]."""
+        if self._w8_ws is None:
+            n = gmm_w8_workspace_bytes(self.T * self.k, max(self.D, self.F))
+            self._w8_ws = torch.empty(n, dtype=torch.uint8, device=self.y.device)
+        return self._w8_ws
 
 
 def ffn_forward(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, W: ExpertWeights, act_mode: int,
@@ -627,7 +648,8 @@ def ffn_forward(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, W
                         out=buf.sort)
     xs_s = s["xs_scale"] if act_mode != PER_TENSOR else static_x
     if w8:
-        gmm_w8(s["xs_q"], xs_s, act_mode, W.w_in, W.s_in, W.in_mode, s["group_sizes"], out=buf.a)
+        ws = buf.w8_workspace()
+        gmm_w8(s["xs_q"], xs_s, act_mode, W.w_in, W.s_in, W.in_mode, s["group_sizes"], out=buf.a, workspace=ws)
         swiglu_quant(buf.a, act_mode, static_h, h_q=buf.h_q, h_scale=buf.h_s)
     elif fuse_swiglu and swiglu_fuse_pays(act_mode, W.in_mode, buf.F):
         gmm_swiglu(s["xs_q"], xs_s, act_mode, W.w_in, W.s_in, W.in_mode, s["group_sizes"], act_mode, static_h,
@@ -636,7 +658,10 @@ def ffn_forward(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, W
         gmm(s["xs_q"], xs_s, act_mode, W.w_in, W.s_in, W.in_mode, s["group_sizes"], out=buf.a)
         swiglu_quant(buf.a, act_mode, static_h, h_q=buf.h_q, h_scale=buf.h_s)
     h_s = buf.h_s if act_mode != PER_TENSOR else static_h
-    (gmm_w8 if w8 else gmm)(buf.h_q, h_s, act_mode, W.w_out, W.s_out, W.out_mode, s["group_sizes"], out=buf.o)
+    if w8:
+        gmm_w8(buf.h_q, h_s, act_mode, W.w_out, W.s_out, W.out_mode, s["group_sizes"], out=buf.o, workspace=ws)
+    else:
+        gmm(buf.h_q, h_s, act_mode, W.w_out, W.s_out, W.out_mode, s["group_sizes"], out=buf.o)
     ragged_gather_reduce(buf.o, s["pos"], topk_w, k, out=buf.y)
     return buf.y
 

@@ -51,7 +51,8 @@ SIGNATURES = {
     "gmm_fp8_mx_swiglu": ([P, P, P, P, P, i32, i32, i32, i64, i64, i64, P, P, P, P], i32),
     "moe_swiglu_quant_mx": ([P, i64, i64, P, P, P], i32),
     "moe_quantize_weights_int8": ([P, i64, i64, i64, i32, P, P, P, P], i32),
-    "gmm_fp8_w8": ([P, P, i32, P, P, i32, P, i32, i32, i32, i64, i64, i64, P, P], i32),
+    "gmm_fp8_w8": ([P, P, i32, P, P, i32, P, i32, i32, i32, i64, i64, i64, P, P, sz, P], i32),
+    "gmm_fp8_w8_workspace_bytes": ([i64, i64], sz),
 }
 
 _lock = threading.Lock()

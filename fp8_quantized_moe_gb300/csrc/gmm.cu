@@ -1702,7 +1702,10 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
 //     tcgen05.st, so the converted weights never pass through shared memory;
 //   - the activations are the B operand: one warp per 32 token rows turns
 //     the stage's e4m3 rows into f16 (cvt.f16x2.e4m3x2) in the
-//     128-byte-swizzled K-major layout the MMA reads from shared memory.
+//     128-byte-swizzled K-major layout the MMA reads from shared memory; or,
+//     with XF16, a workspace already holds them as f16 (one HBM pass before
+//     the kernel) and TMA lands them in that layout, so that per stage the
+//     converters' reads and the f16 tile's writes leave shared memory.
 // Two tile shapes (the accumulators take tensor-memory columns 0..255 either
 // way, the converted-weight ring the other 256):
 //   TOK = 256: 128 channels x 256 tokens, one M = 128, N = 256 MMA per K step
@@ -1718,19 +1721,15 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR_REQ>::THREADS, 1)
 // single f16 rounding; S leaves the sum, and one accumulator runs over the
 // whole K loop.
 constexpr int kW8Ks = 64;                 // K per stage: 64 code bytes, one 128-byte f16 row
-constexpr int kW8BoxBytes = 128 * kW8Ks;  // one TMA box: 128 rows x 64 bytes (64-byte swizzle)
-constexpr int kW8RawStages = 6;           // TMA ring: three boxes (weights and activations) a stage
-constexpr int kW8RawBytes = 3 * kW8BoxBytes;
+constexpr int kW8BoxBytes = 128 * kW8Ks;  // one u8 TMA box: 128 rows x 64 bytes (64-byte swizzle)
+constexpr int kW8MaxRawStages = 6;
 constexpr int kW8AColBase = 256;          // the converted-weight ring's first tensor-memory column
 constexpr int kW8MaxAStages = 8, kW8MaxXStages = 4;
-constexpr int kW8ConvWarps = 12, kW8EpiWarps = 8;
-// warp 0 TMA producer, 1 MMA issuer, 2.. weight converters, then activation
-// converters (12 converter warps), then 8 epilogue warps
-constexpr int kW8Warps = 2 + kW8ConvWarps + kW8EpiWarps;
+constexpr int kW8EpiWarps = 8;
 
 struct W8Ctl {
-  uint64_t rfull[kW8RawStages];   // a stage's three boxes have landed
-  uint64_t rempty[kW8RawStages];  // every converter warp has read the stage
+  uint64_t rfull[kW8MaxRawStages];   // a stage's boxes have landed
+  uint64_t rempty[kW8MaxRawStages];  // every reader of the stage is done with it
   uint64_t afull[kW8MaxAStages];  // converted weights are in tensor memory
   uint64_t aempty[kW8MaxAStages]; // the MMAs that read them completed
   uint64_t xfull[kW8MaxXStages];  // converted activations are in shared memory
@@ -1748,24 +1747,41 @@ struct W8Ctl {
   int gsize[kMaxGroups];
 };
 
-template <int TOK>
+// XF16: the activations come as f16 codes from global memory (TMA, 128-byte
+// swizzle, read by the MMA where they land) instead of e4m3 codes converted
+// on the SM.
+template <int TOK, bool XF16>
 struct W8Cfg {
   static_assert(TOK == 128 || TOK == 256, "int8-weight tile: 128 or 256 tokens");
   static constexpr int HALVES = TOK == 128 ? 2 : 1;  // 128-channel weight tiles (MMA A operands) per tile
   static constexpr int CH = 128 * HALVES;             // channels per tile
-  static constexpr int XBOXES = TOK / 128;            // activation boxes per stage
-  static constexpr int WCONV = 4 * HALVES;            // weight converter warps
-  static constexpr int XCONV = TOK / 32;              // activation converter warps
-  static constexpr int XSTAGES = TOK == 128 ? 4 : 2;  // ring of converted activation tiles
+  static constexpr int XBOXES = TOK / 128;            // activation boxes (128 rows) per stage
+  static constexpr int XBOX_BYTES = XF16 ? 128 * kW8Ks * 2 : kW8BoxBytes;
+  static constexpr int RAW_BYTES = HALVES * kW8BoxBytes + XBOXES * XBOX_BYTES;
+  static constexpr int RAW_STAGES = RAW_BYTES > 3 * kW8BoxBytes ? 5 : 6;
+  // weight converter warps: four per 128 channels; with XF16 and one weight
+  // tile, two sets of four that take alternate stages (so that a stage's
+  // conversion overlaps the next one's)
+  static constexpr int WSETS = (XF16 && HALVES == 1) ? 2 : 1;
+  static constexpr int WCONV = 4 * HALVES * WSETS;
+  static constexpr int XCONV = XF16 ? 0 : TOK / 32;   // activation converter warps
+  static constexpr int CONV = WCONV + XCONV;
+  // readers of a raw stage: the converter warps, and with XF16 the MMAs (one commit)
+  static constexpr int RAW_READERS = CONV / WSETS + (XF16 ? 1 : 0);
+  static constexpr int XSTAGES = XF16 ? 0 : (TOK == 128 ? 4 : 2);  // ring of converted activation tiles
   static constexpr int XBYTES = TOK * kW8Ks * 2;
   static constexpr int ACOLS = 32 * HALVES;           // tensor-memory columns of one converted-weight stage
   static constexpr int ASTAGES = (512 - kW8AColBase) / ACOLS;
   static constexpr uint32_t IDESC = idesc_f16_f32(128, TOK);
-  static constexpr size_t SMEM =
-      1024 + static_cast<size_t>(kW8RawStages) * kW8RawBytes + static_cast<size_t>(XSTAGES) * XBYTES + sizeof(W8Ctl);
-  static_assert(WCONV + XCONV == kW8ConvWarps && HALVES + XBOXES == 3, "int8-weight roles");
-  static_assert(ASTAGES <= kW8MaxAStages && XSTAGES <= kW8MaxXStages && HALVES * TOK <= kW8AColBase,
-                "int8-weight tensor-memory plan");
+  // warp 0 TMA producer, 1 MMA issuer, then the weight converters, the
+  // activation converters and the 8 epilogue warps
+  static constexpr int WARPS = 2 + CONV + kW8EpiWarps;
+  static constexpr size_t SMEM = 1024 + static_cast<size_t>(RAW_STAGES) * RAW_BYTES +
+                                 static_cast<size_t>(XSTAGES) * XBYTES + sizeof(W8Ctl);
+  static_assert(XF16 || CONV == 12, "int8-weight roles");
+  static_assert(RAW_STAGES <= kW8MaxRawStages && ASTAGES <= kW8MaxAStages && XSTAGES <= kW8MaxXStages &&
+                    HALVES * TOK <= kW8AColBase && RAW_BYTES % 1024 == 0,
+                "int8-weight buffer plan");
   static_assert(SMEM <= 232448, "int8-weight gmm: shared memory per CTA");
 };
 
@@ -1780,7 +1796,7 @@ struct W8Tile {
 // Tile t: expert-major, then channel tile, then token tile (so that the CTAs
 // running at the same time share one expert's weights), from the group
 // tables built with units of TOK rows.
-template <int TOK>
+template <int TOK, int CH>
 __device__ __forceinline__ W8Tile w8_tile(const Params& p, const W8Ctl* ctl, int t) {
   int lo = 0, hi = p.El;  // tile_prefix[lo] <= t < tile_prefix[hi]
   while (hi - lo > 1) {
@@ -1796,7 +1812,7 @@ __device__ __forceinline__ W8Tile w8_tile(const Params& p, const W8Ctl* ctl, int
   tl.el = lo;
   tl.row0 = ctl->gstart[lo] + mi * TOK;
   tl.rows = min(TOK, sz - mi * TOK);
-  tl.n0 = nt * W8Cfg<TOK>::CH;
+  tl.n0 = nt * CH;
   tl.by = lo * p.N + tl.n0;
   return tl;
 }
@@ -1810,27 +1826,28 @@ __device__ __forceinline__ float w8_block_smax(const float* s_blk, int kblocks, 
   return m;
 }
 
-template <int TOK>
-__global__ void __launch_bounds__(kW8Warps * 32, 1)
+template <int TOK, bool XF16>
+__global__ void __launch_bounds__(W8Cfg<TOK, XF16>::WARPS * 32, 1)
     w8_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const Params p) {
-  using C = W8Cfg<TOK>;
+  using C = W8Cfg<TOK, XF16>;
+  constexpr int NRAW = C::RAW_STAGES, RAWB = C::RAW_BYTES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw_addr);
-  const uint32_t xring = base + kW8RawStages * kW8RawBytes;
-  W8Ctl* ctl = reinterpret_cast<W8Ctl*>(base_ptr + kW8RawStages * kW8RawBytes + C::XSTAGES * C::XBYTES);
+  const uint32_t xring = base + NRAW * RAWB;  // converted activation tiles (without XF16)
+  W8Ctl* ctl = reinterpret_cast<W8Ctl*>(base_ptr + NRAW * RAWB + C::XSTAGES * C::XBYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // group tables in units of TOK rows (two 128-row M tiles a unit for TOK = 256)
   if (warp == 0) build_group_tables<false, TOK == 256>(p, ctl);
   if (threadIdx.x == 32) {
-    for (int s = 0; s < kW8RawStages; ++s) {
+    for (int s = 0; s < NRAW; ++s) {
       mbar_init(smem_u32(&ctl->rfull[s]), 1);
-      mbar_init(smem_u32(&ctl->rempty[s]), kW8ConvWarps);
+      mbar_init(smem_u32(&ctl->rempty[s]), C::RAW_READERS);
     }
     for (int a = 0; a < C::ASTAGES; ++a) {
-      mbar_init(smem_u32(&ctl->afull[a]), C::WCONV);
+      mbar_init(smem_u32(&ctl->afull[a]), C::WCONV / C::WSETS);
       mbar_init(smem_u32(&ctl->aempty[a]), 1);
     }
     for (int x = 0; x < C::XSTAGES; ++x) {
@@ -1873,22 +1890,21 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
     if (lane == 0) {
       uint32_t it = 0;
       for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
-        const W8Tile tl = w8_tile<TOK>(p, ctl, t);
+        const W8Tile tl = w8_tile<TOK, C::CH>(p, ctl, t);
         for (int ks = 0; ks < nks; ++ks) {
-          const int s = it % kW8RawStages;
-          if (!mbar_wait_bounded(smem_u32(&ctl->rempty[s]), ((it / kW8RawStages) & 1) ^ 1, abort_flag,
-                                 kWaitLimitNs)) {
+          const int s = it % NRAW;
+          if (!mbar_wait_bounded(smem_u32(&ctl->rempty[s]), ((it / NRAW) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
             timed_out = true;
             break;
           }
-          const uint32_t sa = base + s * kW8RawBytes, fb = smem_u32(&ctl->rfull[s]);
-          mbar_arrive_expect_tx(fb, kW8RawBytes);
+          const uint32_t sa = base + s * RAWB, fb = smem_u32(&ctl->rfull[s]);
+          mbar_arrive_expect_tx(fb, RAWB);
 #pragma unroll
           for (int h = 0; h < C::HALVES; ++h)  // weight rows (channels) n0 + 128 h ..
             tma_load_2d(sa + h * kW8BoxBytes, &tmW, ks * kW8Ks, tl.by + 128 * h, fb);
 #pragma unroll
-          for (int b = 0; b < C::XBOXES; ++b)  // token rows row0 + 128 b ..
-            tma_load_2d(sa + (C::HALVES + b) * kW8BoxBytes, &tmX, ks * kW8Ks, tl.row0 + 128 * b, fb);
+          for (int b = 0; b < C::XBOXES; ++b)  // token rows row0 + 128 b .. (x: K elements either way)
+            tma_load_2d(sa + C::HALVES * kW8BoxBytes + b * C::XBOX_BYTES, &tmX, ks * kW8Ks, tl.row0 + 128 * b, fb);
           ++it;
         }
       }
@@ -1896,9 +1912,8 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
         *abort_flag = 1;
         ctl->err = 2;
         // let the loads already issued land before the CTA can exit
-        for (uint32_t j = (it > kW8RawStages ? it - kW8RawStages : 0); j < it; ++j)
-          mbar_wait_bounded(smem_u32(&ctl->rfull[j % kW8RawStages]), (j / kW8RawStages) & 1, &ctl->no_abort,
-                            kWaitLimitNs);
+        for (uint32_t j = (it > NRAW ? it - NRAW : 0); j < it; ++j)
+          mbar_wait_bounded(smem_u32(&ctl->rfull[j % NRAW]), (j / NRAW) & 1, &ctl->no_abort, kWaitLimitNs);
       }
     }
     __syncwarp();
@@ -1913,14 +1928,19 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
         }
         tc_fence_after();
         for (int ks = 0; ks < nks; ++ks) {
-          const int a = it % C::ASTAGES, x = it % C::XSTAGES;
+          const int a = it % C::ASTAGES;
+          // B: the converted tile (ring x) or, with XF16, the raw stage's f16 boxes
+          const int x = XF16 ? static_cast<int>(it % NRAW) : static_cast<int>(it % (XF16 ? 1 : C::XSTAGES));
+          const uint32_t bfull = XF16 ? smem_u32(&ctl->rfull[x]) : smem_u32(&ctl->xfull[x]);
+          const uint32_t bpar = XF16 ? (it / NRAW) & 1 : (it / (XF16 ? 1 : C::XSTAGES)) & 1;
           if (!mbar_wait_bounded(smem_u32(&ctl->afull[a]), (it / C::ASTAGES) & 1, abort_flag, kWaitLimitNs) ||
-              !mbar_wait_bounded(smem_u32(&ctl->xfull[x]), (it / C::XSTAGES) & 1, abort_flag, kWaitLimitNs)) {
+              !mbar_wait_bounded(bfull, bpar, abort_flag, kWaitLimitNs)) {
             timed_out = true;
             break;
           }
           tc_fence_after();
-          const uint64_t db = smem_desc_sw128(xring + x * C::XBYTES);
+          const uint64_t db = XF16 ? smem_desc_sw128(base + x * RAWB + C::HALVES * kW8BoxBytes)
+                                   : smem_desc_sw128(xring + x * C::XBYTES);
           const uint32_t at = tmem_base + kW8AColBase + C::ACOLS * a;
 #pragma unroll
           for (int h = 0; h < C::HALVES; ++h)
@@ -1929,7 +1949,7 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
               mma_f16_tmem_a(tmem_base + TOK * h, at + 32 * h + 8 * k16, db + 2 * k16, C::IDESC,
                              (ks > 0 || k16 > 0) ? 1u : 0u);
           mma_commit(smem_u32(&ctl->aempty[a]));
-          mma_commit(smem_u32(&ctl->xempty[x]));
+          mma_commit(XF16 ? smem_u32(&ctl->rempty[x]) : smem_u32(&ctl->xempty[x]));
           ++it;
         }
         if (timed_out) break;
@@ -1948,14 +1968,16 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
   } else if (warp < 2 + C::WCONV) {
     // --------------------------------------------------- weight converters
     // warp (h, q): rows 32 q .. 32 q + 31 of weight tile h (the tile's
-    // channels 128 h ..), which are the tensor-memory lanes of that quarter
-    const int h = (warp - 2) >> 2, q4 = warp & 3;
+    // channels 128 h ..), which are the tensor-memory lanes of that quarter;
+    // with two sets, set `wset` takes the stages it with it % 2 == wset
+    const int grp = (warp - 2) >> 2, q4 = warp & 3;
+    const int h = grp % C::HALVES, wset = grp / C::HALVES;
     const int r = 32 * q4 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q4) << 16;
     const int swz = (r >> 1) & 3;  // 64-byte swizzle: 16-byte chunk j of row r sits at j ^ ((r / 2) % 4)
     uint32_t it = 0;
     for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
-      const W8Tile tl = w8_tile<TOK>(p, ctl, t);
+      const W8Tile tl = w8_tile<TOK, C::CH>(p, ctl, t);
       const int ch = tl.n0 + 128 * h + r;
       const bool ch_ok = ch < p.N;
       const float* s_blk = p.rhs_scale + static_cast<int64_t>(tl.el) * p.kblocks * p.N + (ch_ok ? ch : 0);
@@ -1965,13 +1987,18 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
         inv_smax = m > 0.0f ? __frcp_rn(m) : 0.0f;
       }
       uint32_t rhi2 = 0x3C003C00u, rlo2 = 0u;  // f16x2 (1, 1) and (0, 0)
+      int kb_have = -1;                        // the K block rhi2 / rlo2 belong to
       for (int ks = 0; ks < nks; ++ks) {
-        const int s = it % kW8RawStages;
-        if (!mbar_wait_bounded_warp(smem_u32(&ctl->rfull[s]), (it / kW8RawStages) & 1, abort_flag, kWaitLimitNs)) {
+        if (C::WSETS > 1 && static_cast<int>(it % C::WSETS) != wset) {  // the other set's stage
+          ++it;
+          continue;
+        }
+        const int s = it % NRAW;
+        if (!mbar_wait_bounded_warp(smem_u32(&ctl->rfull[s]), (it / NRAW) & 1, abort_flag, kWaitLimitNs)) {
           timed_out = true;
           break;
         }
-        const uint8_t* src = base_ptr + s * kW8RawBytes + h * kW8BoxBytes + r * kW8Ks;
+        const uint8_t* src = base_ptr + s * RAWB + h * kW8BoxBytes + r * kW8Ks;
         uint4 wv[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) wv[j] = *reinterpret_cast<const uint4*>(src + 16 * (j ^ swz));
@@ -1980,8 +2007,9 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ctl->rempty[s]));
-        if (w_blk && (ks & 1) == 0) {  // a new 128-wide K block (two stages)
-          const float rel = ch_ok ? __fmul_rn(__ldg(s_blk + static_cast<int64_t>(ks >> 1) * p.N), inv_smax) : 0.0f;
+        if (w_blk && (ks >> 1) != kb_have) {  // a new 128-wide K block (two stages)
+          kb_have = ks >> 1;
+          const float rel = ch_ok ? __fmul_rn(__ldg(s_blk + static_cast<int64_t>(kb_have) * p.N), inv_smax) : 0.0f;
           const __half hi = __float2half_rn(rel);
           const uint32_t hb = __half_as_ushort(hi);
           const uint32_t lb = __half_as_ushort(__float2half_rn(__fsub_rn(rel, __half2float(hi))));
@@ -2032,28 +2060,28 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
       *abort_flag = 1;
       ctl->err = 2;
     }
-  } else if (warp < 2 + kW8ConvWarps) {
+  } else if (!XF16 && warp < 2 + C::CONV) {
     // ----------------------------------------------- activation converters
     const int r = 32 * (warp - 2 - C::WCONV) + lane;  // token row of the tile
     const int swz = (r >> 1) & 3;                      // the same within its 128-row box
     uint32_t it = 0;
     for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
       for (int ks = 0; ks < nks; ++ks) {
-        const int s = it % kW8RawStages;
-        if (!mbar_wait_bounded_warp(smem_u32(&ctl->rfull[s]), (it / kW8RawStages) & 1, abort_flag, kWaitLimitNs)) {
+        const int s = it % NRAW;
+        if (!mbar_wait_bounded_warp(smem_u32(&ctl->rfull[s]), (it / NRAW) & 1, abort_flag, kWaitLimitNs)) {
           timed_out = true;
           break;
         }
         const uint8_t* src =
-            base_ptr + s * kW8RawBytes + (C::HALVES + (r >> 7)) * kW8BoxBytes + (r & 127) * kW8Ks;
+            base_ptr + s * RAWB + C::HALVES * kW8BoxBytes + (r >> 7) * C::XBOX_BYTES + (r & 127) * kW8Ks;
         uint4 xv[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) xv[j] = *reinterpret_cast<const uint4*>(src + 16 * (j ^ swz));
         fence_proxy_async_smem();  // as above: generic reads before the TMA refill
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ctl->rempty[s]));
-        const int x = it % C::XSTAGES;
-        if (!mbar_wait_bounded_warp(smem_u32(&ctl->xempty[x]), ((it / C::XSTAGES) & 1) ^ 1, abort_flag,
+        const int x = it % (XF16 ? 1 : C::XSTAGES);
+        if (!mbar_wait_bounded_warp(smem_u32(&ctl->xempty[x]), ((it / (XF16 ? 1 : C::XSTAGES)) & 1) ^ 1, abort_flag,
                                     kWaitLimitNs)) {
           timed_out = true;
           break;
@@ -2089,7 +2117,7 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
     // warp (g, q): accumulator columns 128 g .. 128 g + 127 in lane quarter
     // q; with TOK = 128 those are all 128 tokens of channel half g, with
     // TOK = 256 tokens 128 g .. of the tile's 128 channels
-    const int g = (warp - 2 - kW8ConvWarps) >> 2, q4 = warp & 3;
+    const int g = (warp - 2 - C::CONV) >> 2, q4 = warp & 3;
     const int r = 32 * q4 + lane;
     const int ch_off = TOK == 128 ? 128 * g : 0, tok0 = TOK == 128 ? 0 : 128 * g;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q4) << 16;
@@ -2097,7 +2125,7 @@ __global__ void __launch_bounds__(kW8Warps * 32, 1)
     uint32_t tcount = 0;
     if (p.stall && !mbar_wait_bounded_warp(smem_u32(&ctl->never), 0, abort_flag, p.stall_ns)) timed_out = true;
     for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
-      const W8Tile tl = w8_tile<TOK>(p, ctl, t);
+      const W8Tile tl = w8_tile<TOK, C::CH>(p, ctl, t);
       const int ch = tl.n0 + ch_off + r;
       const bool ch_ok = ch < p.N;
       float s_w;
@@ -2192,6 +2220,27 @@ __global__ void zero_outside_kernel(uint16_t* out, int64_t M, int64_t N, const i
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t row = i / nvec;
     if (row < lo || row >= hi) reinterpret_cast<uint4*>(out)[i] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+// e4m3 codes -> their f16 values (exact: f16 holds every e4m3 value), 16
+// codes a thread and step: the int8-weight gmm's activations in the form its
+// MMA reads.
+__global__ void __launch_bounds__(256) e4m3_to_f16_kernel(const uint8_t* src, int64_t n16, uint16_t* dst) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint16_t lo16 = static_cast<uint16_t>(w[c] & 0xFFFFu), hi16 = static_cast<uint16_t>(w[c] >> 16);
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o[2 * c]) : "h"(lo16));
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o[2 * c + 1]) : "h"(hi16));
+    }
+    uint4* d = reinterpret_cast<uint4*>(dst) + 2 * i;
+    d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    d[1] = make_uint4(o[4], o[5], o[6], o[7]);
   }
 }
 
@@ -2665,17 +2714,17 @@ moe_status launch_mma(const CUtensorMap& A, const CUtensorMap& B, const CUtensor
 std::atomic<uint64_t> g_stall_ns{0};
 
 // gmm_fp8_w8 with tiles of TOK tokens: one persistent CTA per SM at most.
-template <int TOK>
+template <int TOK, bool XF16>
 moe_status launch_w8(const CUtensorMap& X, const CUtensorMap& W, Params p, int E_local, cudaStream_t st) {
-  using C = W8Cfg<TOK>;
+  using C = W8Cfg<TOK, XF16>;
   p.ntiles = static_cast<int>((p.N + C::CH - 1) / C::CH);
-  MOE_CUDA_TRY(cudaFuncSetAttribute(w8_kernel<TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  MOE_CUDA_TRY(cudaFuncSetAttribute(w8_kernel<TOK, XF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(C::SMEM)));
   const int sms = sm_count();
   if (sms <= 0) return MOE_ERR_CUDA;
   const int64_t units = ((p.M + TOK - 1) / TOK + E_local) * static_cast<int64_t>(p.ntiles);
   const int grid = units < sms ? static_cast<int>(units) : sms;
-  w8_kernel<TOK><<<grid, kW8Warps * 32, C::SMEM, st>>>(X, W, p);
+  w8_kernel<TOK, XF16><<<grid, C::WARPS * 32, C::SMEM, st>>>(X, W, p);
   MOE_CUDA_TRY(cudaGetLastError());
   return MOE_OK;
 }
@@ -2962,10 +3011,15 @@ int64_t padded_rows(int64_t M, int E_local) { return ((M + 127) / 128) * 128 + 1
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 }  // namespace
 
+extern "C" size_t gmm_fp8_w8_workspace_bytes(int64_t M, int64_t K) {
+  return (M > 0 && K > 0 && M < (1ll << 31) && K < (1 << 30)) ? static_cast<size_t>(2 * M * K) : 0;
+}
+
 extern "C" moe_status gmm_fp8_w8(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode,
                                  const int8_t* rhs_q, const float* rhs_scale, moe_scale_mode rhs_mode,
                                  const int32_t* group_sizes, int E, int group_offset, int E_local, int64_t M,
-                                 int64_t K, int64_t N, uint16_t* out, moe_stream_t stream) {
+                                 int64_t K, int64_t N, uint16_t* out, void* workspace, size_t workspace_bytes,
+                                 moe_stream_t stream) {
   MOE_HOST_CHECK(lhs_q && lhs_scale && rhs_q && rhs_scale && group_sizes && out, MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(lhs_mode == MOE_SCALE_PER_ROW || lhs_mode == MOE_SCALE_PER_TENSOR, MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(valid_lhs_mode(rhs_mode), MOE_ERR_INVALID_ARG);
@@ -2976,6 +3030,15 @@ extern "C" moe_status gmm_fp8_w8(const uint8_t* lhs_q, const float* lhs_scale, m
   MOE_HOST_CHECK(static_cast<int64_t>(E_local) * N < (1ll << 31), MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(rhs_mode != MOE_SCALE_PER_ROW_BLOCK128 || K % 128 == 0, MOE_ERR_INVALID_ARG);
   MOE_HOST_CHECK(aligned16(lhs_q) && aligned16(rhs_q) && aligned16(out), MOE_ERR_INVALID_ARG);
+  MOE_HOST_CHECK(!workspace || (aligned16(workspace) && workspace_bytes >= gmm_fp8_w8_workspace_bytes(M, K)),
+                 MOE_ERR_INVALID_ARG);
+  // the 256-token tile when the local groups average 256 rows or more (the
+  // full-rate N = 256 MMA), else the 128-token tile (less padding); with the
+  // 256-token tile and a workspace the activations are decoded to f16 there
+  // first (the 128-token tile serves small, weight-stream-bound groups, where
+  // the extra pass costs more than it saves)
+  const bool tok256 = M >= 256ll * E_local;
+  const bool xf16 = workspace != nullptr && tok256;
   if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
   cudaStream_t st = as_stream(stream);
   if (M == 0) return MOE_OK;
@@ -2984,7 +3047,16 @@ extern "C" moe_status gmm_fp8_w8(const uint8_t* lhs_q, const float* lhs_scale, m
     MOE_CUDA_TRY(cudaGetLastError());
   }
   CUtensorMap X, W;
-  if (!make_map_u8_64(&X, lhs_q, K, M, K, 128)) return MOE_ERR_CUDA;
+  if (xf16) {
+    const int64_t n16 = M * K / 16;
+    const int64_t blocks = std::min<int64_t>((n16 + 255) / 256, static_cast<int64_t>(sm_count()) * 8);
+    e4m3_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(lhs_q, n16, static_cast<uint16_t*>(workspace));
+    MOE_CUDA_TRY(cudaGetLastError());
+    // f16 rows of K elements, boxes of 128 rows x 64 elements (128-byte swizzle)
+    if (!make_map_bf16(&X, workspace, K, M, 2 * K, 128)) return MOE_ERR_CUDA;
+  } else if (!make_map_u8_64(&X, lhs_q, K, M, K, 128)) {
+    return MOE_ERR_CUDA;
+  }
   if (!make_map_u8_64(&W, rhs_q, K, static_cast<uint64_t>(E_local) * N, K, 128)) return MOE_ERR_CUDA;
   Params p{};
   p.group_sizes = group_sizes;
@@ -3002,9 +3074,9 @@ extern "C" moe_status gmm_fp8_w8(const uint8_t* lhs_q, const float* lhs_scale, m
   p.out = out;
   p.stall_ns = g_stall_ns.load();
   p.stall = p.stall_ns != 0;
-  // the 256-token tile when the local groups average 256 rows or more (the
-  // full-rate N = 256 MMA), else the 128-token tile (less padding)
-  return M >= 256ll * E_local ? launch_w8<256>(X, W, p, E_local, st) : launch_w8<128>(X, W, p, E_local, st);
+  if (tok256)
+    return xf16 ? launch_w8<256, true>(X, W, p, E_local, st) : launch_w8<256, false>(X, W, p, E_local, st);
+  return launch_w8<128, false>(X, W, p, E_local, st);
 }
 
 extern "C" size_t tgmm_fp8_workspace_bytes(int64_t M, int64_t K, int64_t N, int E_local) {

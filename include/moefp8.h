@@ -500,12 +500,25 @@ moe_status moe_quantize_weights_int8(const uint16_t* w, int64_t E, int64_t N, in
  * s_w[kb] / max_kb s_w[kb] on the converted codes, so each converted weight
  * carries one f16 rounding (relative 2^-12; coarser where the factor falls
  * below 2^-14, the f16 normal range) beside the fp32 accumulation.
+ *
+ * workspace (optional, may be NULL): caller-owned device memory of at least
+ * gmm_fp8_w8_workspace_bytes(M, K) bytes, 16-byte aligned.  Where the local
+ * groups average 256 rows or more (the tensor pipe binds), the call then
+ * first decodes lhs_q to f16 there (one pass over the codes) and the
+ * contraction reads the f16 rows directly; otherwise, and without a
+ * workspace, the contraction converts the e4m3 codes on the SM.  The result
+ * is the same, bit for bit.
  * K % 16 == 0 (% 128 for blockwise), N % 16 == 0; lhs_q, rhs_q and out
- * 16-byte aligned.  MOE_ERR_INVALID_ARG on a bad argument, before any launch. */
+ * 16-byte aligned.  MOE_ERR_INVALID_ARG on a bad argument (a workspace too
+ * small or misaligned included), before any launch. */
 moe_status gmm_fp8_w8(const uint8_t* lhs_q, const float* lhs_scale, moe_scale_mode lhs_mode, const int8_t* rhs_q,
                       const float* rhs_scale, moe_scale_mode rhs_mode, const int32_t* group_sizes, int E,
                       int group_offset, int E_local, int64_t M, int64_t K, int64_t N, uint16_t* out,
-                      moe_stream_t stream);
+                      void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* Bytes of gmm_fp8_w8's optional workspace: 2 * M * K (0 for an empty or
+ * out-of-range shape). */
+size_t gmm_fp8_w8_workspace_bytes(int64_t M, int64_t K);
 
 #ifdef __cplusplus
 }

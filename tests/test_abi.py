@@ -131,9 +131,13 @@ def test_host_side_argument_checks_of_the_int8_weight_entries(lib):
     assert lib.moe_quantize_weights_int8(p, 1, 4, 128, 2, None, p, None, None) == 1
     # gmm: per-128 activation scales (not taken); K % 16; blockwise K % 128; N % 16;
     # shard past E; null weight scales
-    assert lib.gmm_fp8_w8(p, p, 1, p, p, 0, p, 1, 0, 1, 8, 128, 256, p, None) == 1
-    assert lib.gmm_fp8_w8(p, p, 0, p, p, 0, p, 1, 0, 1, 8, 120, 256, p, None) == 1
-    assert lib.gmm_fp8_w8(p, p, 0, p, p, 1, p, 1, 0, 1, 8, 144, 256, p, None) == 1
-    assert lib.gmm_fp8_w8(p, p, 0, p, p, 0, p, 1, 0, 1, 8, 128, 24, p, None) == 1
-    assert lib.gmm_fp8_w8(p, p, 0, p, p, 0, p, 2, 1, 2, 8, 128, 256, p, None) == 1
-    assert lib.gmm_fp8_w8(p, p, 0, p, None, 0, p, 1, 0, 1, 8, 128, 256, p, None) == 1
+    assert lib.gmm_fp8_w8(p, p, 1, p, p, 0, p, 1, 0, 1, 8, 128, 256, p, None, 0, None) == 1
+    assert lib.gmm_fp8_w8(p, p, 0, p, p, 0, p, 1, 0, 1, 8, 120, 256, p, None, 0, None) == 1
+    assert lib.gmm_fp8_w8(p, p, 0, p, p, 1, p, 1, 0, 1, 8, 144, 256, p, None, 0, None) == 1
+    assert lib.gmm_fp8_w8(p, p, 0, p, p, 0, p, 1, 0, 1, 8, 128, 24, p, None, 0, None) == 1
+    assert lib.gmm_fp8_w8(p, p, 0, p, p, 0, p, 2, 1, 2, 8, 128, 256, p, None, 0, None) == 1
+    assert lib.gmm_fp8_w8(p, p, 0, p, None, 0, p, 1, 0, 1, 8, 128, 256, p, None, 0, None) == 1
+    # a workspace smaller than 2 M K bytes, or misaligned
+    assert lib.gmm_fp8_w8_workspace_bytes(8, 128) == 2 * 8 * 128
+    assert lib.gmm_fp8_w8(p, p, 0, p, p, 0, p, 1, 0, 1, 8, 128, 256, p, p, 2 * 8 * 128 - 1, None) == 1
+    assert lib.gmm_fp8_w8(p, p, 0, p, p, 0, p, 1, 0, 1, 8, 128, 256, p, ctypes.c_void_p(264), 1 << 20, None) == 1

@@ -18,8 +18,12 @@ so, through SwiGLU, one e4m3 step (2^-3) in a few tenths of a per cent of the
 h codes; measured, the composed y then differs by 6-7e-3.  With per-channel
 scales the converted weights are the exact integers and a matches the
 oracle's to fp32 accumulation order.
-Cases cover both tile shapes (256 tokens x 128 channels when the local
-groups average 256 rows or more, else 128 tokens x 256 channels), several
+Both forms of the call are covered: with a workspace (the activations
+decoded to f16 there first, the kernel's B operand read as TMA lands it) and
+without (the kernel converts the e4m3 codes on the SM); their outputs must be
+identical bit for bit.  Cases cover both tile shapes (256 tokens x 128
+channels when the local groups average 256 rows or more, else 128 tokens x
+256 channels), several
 tiles, ragged and empty groups, N tails, K tails, long K, blockwise scales
 spread over many binades, expert-parallel shards, repeated calls (the bits
 must not change) and the bounded-wait failure path."""
@@ -90,6 +94,18 @@ def w8_args(a, sa, a_mode, q, sw, w_mode, sizes):
     return dev(a), dev(sa), a_mode, dev(q), dev(sw), w_mode, dev(sizes)
 
 
+def w8_ws(M, K):
+    return torch.empty(moe.gmm_w8_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+
+
+def w8_both(args, M, K, **kw):
+    """gmm_w8 without and with a workspace; the two must agree bit for bit."""
+    out = host(moe.gmm_w8(*args, **kw))
+    out_ws = host(moe.gmm_w8(*args, workspace=w8_ws(M, K), **kw))
+    assert np.array_equal(out, out_ws), "gmm_w8 with and without a workspace differ"
+    return out
+
+
 GMM_CASES = [
     # 128-token tiles (the groups average fewer than 256 rows)
     (128, 128, 256, 1),       # one tile, two stages
@@ -115,18 +131,18 @@ GMM_CASES = [
 def test_gmm_w8_per_channel_matches_oracle(M, K, N, E):
     sizes, a, sa, q, sw = make_w8_case(M * 31 + K + N + E, M, K, N, E)
     ref = oracle.gmm_w8(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW, sizes)
-    out = moe.gmm_w8(*w8_args(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW, sizes))
+    out = w8_both(w8_args(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW, sizes), M, K)
     assert moe.device_error() == 0
-    assert_close(host(out), ref, f"gmm_w8 per channel M={M} K={K} N={N} E={E}")
+    assert_close(out, ref, f"gmm_w8 per channel M={M} K={K} N={N} E={E}")
 
 
 @pytest.mark.parametrize("M,K,N,E", [c for c in GMM_CASES if c[1] % 128 == 0])
 def test_gmm_w8_blockwise_matches_oracle(M, K, N, E):
     sizes, a, sa, q, sw = make_w8_case(M * 37 + K + N + E, M, K, N, E, w_mode=synth.PER_ROW_BLOCK128, spread=4)
     ref = oracle.gmm_w8(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW_BLOCK128, sizes)
-    out = moe.gmm_w8(*w8_args(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW_BLOCK128, sizes))
+    out = w8_both(w8_args(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW_BLOCK128, sizes), M, K)
     assert moe.device_error() == 0
-    assert_close(host(out), ref, f"gmm_w8 blockwise M={M} K={K} N={N} E={E}")
+    assert_close(out, ref, f"gmm_w8 blockwise M={M} K={K} N={N} E={E}")
 
 
 @pytest.mark.parametrize("spread", [0, 8, 12])
@@ -148,9 +164,9 @@ def test_gmm_w8_static_scales(a_mode, w_mode):
     sizes, a, sa, q, sw = make_w8_case(50 + 3 * a_mode + w_mode, 700, 1024, 384, 5, w_mode=w_mode, a_mode=a_mode,
                                        spread=3)
     ref = oracle.gmm_w8(a, sa, a_mode, q, sw, w_mode, sizes)
-    out = moe.gmm_w8(*w8_args(a, sa, a_mode, q, sw, w_mode, sizes))
+    out = w8_both(w8_args(a, sa, a_mode, q, sw, w_mode, sizes), 700, 1024)
     assert moe.device_error() == 0
-    assert_close(host(out), ref, f"gmm_w8 modes {a_mode}/{w_mode}")
+    assert_close(out, ref, f"gmm_w8 modes {a_mode}/{w_mode}")
 
 
 @pytest.mark.parametrize("K,M", [(80, 300), (208, 300), (1040, 300), (208, 1200), (1040, 1200)])
@@ -159,9 +175,9 @@ def test_gmm_w8_k_tail(K, M):
     # read zeros past K (M = 300: 128-token tiles; 1200: 256-token tiles)
     sizes, a, sa, q, sw = make_w8_case(60 + K + M, M, K, 256, 3)
     ref = oracle.gmm_w8(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW, sizes)
-    out = moe.gmm_w8(*w8_args(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW, sizes))
+    out = w8_both(w8_args(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW, sizes), M, K)
     assert moe.device_error() == 0
-    assert_close(host(out), ref, f"gmm_w8 K={K}")
+    assert_close(out, ref, f"gmm_w8 K={K}")
 
 
 @pytest.mark.parametrize("K,w_mode,M", [(512, synth.PER_ROW, 1000), (4096, synth.PER_ROW_BLOCK128, 1000),
@@ -172,7 +188,7 @@ def test_gmm_w8_expert_parallel_shard(K, w_mode, M):
     g0, El = 2, 4
     q, sw = np.ascontiguousarray(q[g0:g0 + El]), np.ascontiguousarray(sw[g0:g0 + El])
     ref = oracle.gmm_w8(a, sa, synth.PER_ROW, q, sw, w_mode, sizes, group_offset=g0, E_local=El)
-    out = host(moe.gmm_w8(*w8_args(a, sa, synth.PER_ROW, q, sw, w_mode, sizes), group_offset=g0, E_local=El))
+    out = w8_both(w8_args(a, sa, synth.PER_ROW, q, sw, w_mode, sizes), M, K, group_offset=g0, E_local=El)
     assert moe.device_error() == 0
     starts = np.concatenate([[0], np.cumsum(sizes)])
     lo, hi = starts[g0], starts[g0 + El]
@@ -195,19 +211,21 @@ def host_f64(a):
     return oracle.bf16_to_f64(a) if a.dtype == np.uint16 else a.astype(np.float64)
 
 
+@pytest.mark.parametrize("ws", [False, True])
 @pytest.mark.parametrize("M,K,N,E,w_mode", [(2048, 4096, 512, 4, synth.PER_ROW), (3000, 1024, 768, 24, synth.PER_ROW),
                                             (2048, 2048, 1536, 128, synth.PER_ROW_BLOCK128)])
-def test_gmm_w8_is_deterministic(M, K, N, E, w_mode):
+def test_gmm_w8_is_deterministic(M, K, N, E, w_mode, ws):
     """The accumulation order is fixed, so repeated calls give the same bits;
     a pipeline hand-off that let the MMA read a stage before it was written
     would show up as a difference."""
     sizes, a, sa, q, sw = make_w8_case(70 + K + N, M, K, N, E, w_mode=w_mode, spread=3)
     args = w8_args(a, sa, synth.PER_ROW, q, sw, w_mode, sizes)
-    first = host(moe.gmm_w8(*args))
+    kw = {"workspace": w8_ws(M, K)} if ws else {}
+    first = host(moe.gmm_w8(*args, **kw))
     ref = oracle.gmm_w8(a, sa, synth.PER_ROW, q, sw, w_mode, sizes)
     diffs = []
     for i in range(20):
-        out = host(moe.gmm_w8(*args))
+        out = host(moe.gmm_w8(*args, **kw))
         if not np.array_equal(out, first):
             diffs.append((i, int(np.sum(out != first)), tile_errors(out, ref)))
     assert moe.device_error() == 0
@@ -221,19 +239,21 @@ def test_gmm_w8_bounded_wait_timeout_reports_and_recovers():
     every load in flight lands, tensor memory is freed and
     MOE_DEVERR_TIMEOUT is raised; the next call is exact."""
     lib = moe.lib()
-    for M, K, N, E in [(4096, 512, 1024, 8), (2048, 4096, 512, 4)]:
+    for M, K, N, E, ws in [(4096, 512, 1024, 8, False), (2048, 4096, 512, 4, False), (2048, 4096, 512, 4, True),
+                           (600, 1024, 512, 6, True)]:
         sizes, a, sa, q, sw = make_w8_case(23 + K, M, K, N, E)
         args = w8_args(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW, sizes)
+        kw = {"workspace": w8_ws(M, K)} if ws else {}
         assert moe.device_error() == 0
         lib.moe_test_stall_epilogue(200_000)
         try:
-            moe.gmm_w8(*args)
+            moe.gmm_w8(*args, **kw)
             assert moe.device_error() == 0x4  # MOE_DEVERR_TIMEOUT
         finally:
             lib.moe_test_stall_epilogue(0)
         ref = oracle.gmm_w8(a, sa, synth.PER_ROW, q, sw, synth.PER_ROW, sizes)
         for rep_ in range(3):
-            out = host(moe.gmm_w8(*args))
+            out = host(moe.gmm_w8(*args, **kw))
             assert moe.device_error() == 0
             fro, _ = close_errors(out, ref)
             assert fro <= 2e-3, (f"gmm_w8 call {rep_} after a timed-out call (K={K}): {fro:.3e}; worst tiles "
