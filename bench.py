@@ -470,8 +470,10 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
     fused = mx or (not w8 and moe.swiglu_fuse_pays(cfg.act_mode, W.in_mode, cfg.F))
     # quantise + sort 4 (histogram, scan, scatter, quantise-gather) + (fused gmm+SwiGLU 1, +1 code
     # pass for per-row h scales | gmm 1 + SwiGLU 1) + gmm 1 + combine 1; the int8-weight gmms each
-    # add their f16 decode of the activations
-    launches_per_step = 4 + ((1 + (1 if cfg.act_mode == 0 else 0)) if fused else 2) + 1 + 1 + (2 if w8 else 0)
+    # add their f16 decode of the activations where they take the 256-token tile (groups of 256
+    # rows or more on average)
+    launches_per_step = (4 + ((1 + (1 if cfg.act_mode == 0 else 0)) if fused else 2) + 1 + 1
+                         + (2 if w8 and cfg.T * cfg.k >= 256 * cfg.E else 0))
     fl = fwd_flops(cfg)
     g_in = float(np.mean([a for a, _ in gmm_ms]))
     g_out = float(np.mean([b for _, b in gmm_ms]))
