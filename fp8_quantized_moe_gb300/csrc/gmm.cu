@@ -6,7 +6,10 @@
 // output, bf16 output), "Support quantization for tokamax gmm v2" (gmm and
 // tgmm with absmax scales) and "Keep qwix out of tpu-inference's fused MoE
 // kernel and pre-quantize weights" (fp8 weights with [E, blocks, 1, N]
-// scales; 32-bit accumulation); and, not from those pages,
+// scales; 32-bit accumulation);
+//   gmm_fp8_w8 the same gmm with int8 weights (that page's other weight
+//              type), on the f16 MMA (both code types are exact in f16);
+// and, not from those pages,
 //   gmm_fp8_mx the same gmm on MXFP8 operands (OCP Microscaling Formats v1.0:
 //              one E8M0 power-of-two scale per 32 values of K).
 //
