@@ -4,10 +4,13 @@
 //
 //   out[t, :] = bf16( sum_{j < k} w[t, j] * rows[pos[t*k + j], :] )
 //
-// HBM-bound: one warp per token; per pass each lane loads one 16-byte vector
-// (8 bf16) from each of the k source rows (k independent loads in flight),
-// accumulates in fp32 in ascending j, and writes 8 bf16.  Two passes are
-// unrolled so that small k still keeps enough loads in flight.
+// HBM-bound: one warp per token; per pass each lane loads two 16-byte vectors
+// (8 bf16 each) from every source row, the loads of up to KB rows (KB >= k up
+// to 8) issued before any of them is accumulated (so that a pass costs one
+// memory latency, not k: with few tokens, as in a prefill chunk, the warps
+// cannot hide a chain of them; KB fits k so that small k keeps its registers
+// and occupancy), accumulates in fp32 in ascending j, and writes 8 bf16 a
+// vector.
 #include "common.cuh"
 
 namespace moe {
@@ -17,6 +20,7 @@ __device__ unsigned int g_err;
 
 constexpr int kMaxK = 32;
 
+template <int KB>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* rows, const int32_t* pos,
                                                       const float* weights, int64_t T, int k, int64_t D,
                                                       uint16_t* out) {
@@ -33,27 +37,43 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* rows, cons
     my_w = weights ? __ldg(weights + t * k + lane) : 1.0f;
   }
   const int64_t nvec = D / 8;
-  for (int64_t v0 = lane; v0 < nvec; v0 += 64) {
+  constexpr int kBatch = KB;  // source rows whose loads are in flight together
+  // every lane runs every pass (the row positions and weights are broadcast
+  // by shuffles from the lanes that loaded them), with its own vectors masked
+  for (int64_t vbase = 0; vbase < nvec; vbase += 64) {
+    const int64_t v0 = vbase + lane;
     float acc[2][8];
 #pragma unroll
     for (int u = 0; u < 2; ++u)
 #pragma unroll
       for (int c = 0; c < 8; ++c) acc[u][c] = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      const int p = __shfl_sync(0xffffffffu, my_pos, j);
-      const float w = __shfl_sync(0xffffffffu, my_w, j);
-      if (p < 0) continue;
-      const uint16_t* src = rows + static_cast<int64_t>(p) * D;
+    for (int j0 = 0; j0 < k; j0 += kBatch) {
+      uint4 d[kBatch][2];
+      float w[kBatch];
+      bool ok[kBatch];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int64_t v = v0 + 32 * u;
-        if (v < nvec) {
-          const uint4 d = __ldg(reinterpret_cast<const uint4*>(src + 8 * v));
-          const uint32_t wd[4] = {d.x, d.y, d.z, d.w};
+      for (int jj = 0; jj < kBatch; ++jj) {  // every load of the batch first
+        const int j = j0 + jj;
+        const int p = __shfl_sync(0xffffffffu, my_pos, j & 31);
+        w[jj] = __shfl_sync(0xffffffffu, my_w, j & 31);
+        ok[jj] = j < k && p >= 0;
+        const uint16_t* src = rows + static_cast<int64_t>(ok[jj] ? p : 0) * D;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int64_t v = v0 + 32 * u;
+          d[jj][u] = (ok[jj] && v < nvec) ? __ldg(reinterpret_cast<const uint4*>(src + 8 * v)) : make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < kBatch; ++jj) {  // then the sums, in ascending j
+        if (!ok[jj]) continue;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint32_t wd[4] = {d[jj][u].x, d[jj][u].y, d[jj][u].z, d[jj][u].w};
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            acc[u][2 * c] = __fmaf_rn(w, bf16lo(wd[c]), acc[u][2 * c]);
-            acc[u][2 * c + 1] = __fmaf_rn(w, bf16hi(wd[c]), acc[u][2 * c + 1]);
+            acc[u][2 * c] = __fmaf_rn(w[jj], bf16lo(wd[c]), acc[u][2 * c]);
+            acc[u][2 * c + 1] = __fmaf_rn(w[jj], bf16hi(wd[c]), acc[u][2 * c + 1]);
           }
         }
       }
@@ -92,8 +112,14 @@ extern "C" moe_status ragged_gather_reduce(const uint16_t* rows, const int32_t* 
   // T * k < 2^31, tested without forming the product of an unchecked T
   MOE_HOST_CHECK(T <= ((1ll << 31) - 1) / k && aligned16(rows) && aligned16(out), MOE_ERR_INVALID_ARG);
   if (T == 0) return MOE_OK;
-  combine_kernel<<<static_cast<unsigned>((T + 7) / 8), 256, 0, as_stream(stream)>>>(rows, pos, weights, T, k, D,
-                                                                                     out);
+  const unsigned grid = static_cast<unsigned>((T + 7) / 8);
+  cudaStream_t st = as_stream(stream);
+  if (k <= 2)
+    combine_kernel<2><<<grid, 256, 0, st>>>(rows, pos, weights, T, k, D, out);
+  else if (k <= 4)
+    combine_kernel<4><<<grid, 256, 0, st>>>(rows, pos, weights, T, k, D, out);
+  else
+    combine_kernel<8><<<grid, 256, 0, st>>>(rows, pos, weights, T, k, D, out);
   MOE_CUDA_TRY(cudaGetLastError());
   return MOE_OK;
 }

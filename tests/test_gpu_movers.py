@@ -60,6 +60,10 @@ def test_quantize_weights_bit_exact(mode):
     (333, 6, 64, 256, synth.PER_TENSOR),
     (1000, 8, 256, 384, synth.PER_ROW_BLOCK128),
     (2500, 8, 1024, 64, synth.PER_ROW),       # several chunks, E at its limit
+    (4096, 8, 64, 64, synth.PER_ROW),         # 32768 pairs, 64 experts: the one-CTA sort at its limits
+    (4095, 8, 63, 32, synth.PER_TENSOR),      # the one-CTA sort, ragged last rounds
+    (32769, 1, 32, 16, synth.PER_ROW),        # one pair past the one-CTA limit: the multi-CTA sort
+    (300, 4, 65, 16, synth.PER_ROW),          # one expert past the one-CTA limit: the multi-CTA sort
     (16384, 8, 256, 7168, synth.PER_ROW_BLOCK128),  # DeepSeek-V3-shaped, full size
 ])
 def test_ragged_sort_bit_exact(T, k, E, D, mode):
@@ -153,7 +157,8 @@ def test_swiglu_exp_matches_cuda_expf_bound():
     assert np.max(np.abs(deq - r)) <= 0.07 * np.abs(r).max()
 
 
-@pytest.mark.parametrize("T,k,D", [(1, 1, 8), (256, 2, 128), (100, 8, 7168), (77, 6, 4096), (50, 3, 264)])
+@pytest.mark.parametrize("T,k,D", [(1, 1, 8), (256, 2, 128), (100, 8, 7168), (77, 6, 4096), (50, 3, 264),
+                                   (40, 12, 264), (10, 32, 128), (2048, 8, 2048)])
 def test_combine_matches_oracle(T, k, D):
     rng = np.random.default_rng(T * k + D)
     E = 5
