@@ -42,24 +42,30 @@ __device__ __forceinline__ int load_id(const int32_t* ids, int64_t i, int64_t R,
   return e;
 }
 
+constexpr int kRounds = kPerWarp / 32;  // rounds of 32 pairs per warp
+
 // Per-warp histograms of the chunk; hist is [kWarps][E] in shared memory.
-__device__ __forceinline__ void chunk_hist(const int32_t* ids, int64_t R, int E, int* hist) {
+// The ids of the warp's kRounds rounds are loaded together (one memory
+// latency, not kRounds) and returned in ev for the scatter.
+__device__ __forceinline__ void chunk_hist(const int32_t* ids, int64_t R, int E, int* hist, int (&ev)[kRounds]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
   const int64_t base = static_cast<int64_t>(blockIdx.x) * kChunk + warp * kPerWarp;
   bool bad = false;
-  for (int r = 0; r < kPerWarp / 32; ++r) {
-    const int e = load_id(ids, base + r * 32 + lane, R, E, bad);
-    if (e >= 0) atomicAdd(&hist[warp * E + e], 1);
-  }
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) ev[r] = load_id(ids, base + r * 32 + lane, R, E, bad);
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r)
+    if (ev[r] >= 0) atomicAdd(&hist[warp * E + ev[r]], 1);
   if (bad) raise_error(&g_err, MOE_DEVERR_BAD_EXPERT_ID);
   __syncthreads();
 }
 
 __global__ void __launch_bounds__(256) sort_hist_kernel(const int32_t* ids, int64_t R, int E, int* chunk_counts) {
   extern __shared__ int hist[];
-  chunk_hist(ids, R, E, hist);
+  int ev[kRounds];
+  chunk_hist(ids, R, E, hist, ev);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int s = 0;
 #pragma unroll
@@ -120,7 +126,8 @@ __global__ void __launch_bounds__(256) sort_scatter_kernel(const int32_t* ids, i
                                                            const int* chunk_counts, int32_t* sorted_src,
                                                            int32_t* pos) {
   extern __shared__ int hist[];  // [kWarps][E] counts, then running slots
-  chunk_hist(ids, R, E, hist);
+  int ev[kRounds];
+  chunk_hist(ids, R, E, hist, ev);
   // hist[w][e] <- first slot of warp w's pairs of expert e
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = chunk_counts[static_cast<int64_t>(blockIdx.x) * E + e];
@@ -135,10 +142,10 @@ __global__ void __launch_bounds__(256) sort_scatter_kernel(const int32_t* ids, i
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int* slot = hist + warp * E;
   const int64_t base = static_cast<int64_t>(blockIdx.x) * kChunk + warp * kPerWarp;
-  bool bad = false;
-  for (int r = 0; r < kPerWarp / 32; ++r) {
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
     const int64_t i = base + r * 32 + lane;
-    const int e = load_id(ids, i, R, E, bad);
+    const int e = ev[r];
     const unsigned valid = __ballot_sync(0xffffffffu, e >= 0);
     if (e >= 0) {
       const unsigned peers = __match_any_sync(valid, e);
