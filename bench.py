@@ -468,11 +468,13 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
                        "every step, on their own streams, double-buffered across steps"}
 
     fused = mx or (not w8 and moe.swiglu_fuse_pays(cfg.act_mode, W.in_mode, cfg.F))
-    # quantise + sort 4 (histogram, scan, scatter, quantise-gather) + (fused gmm+SwiGLU 1, +1 code
+    # quantise + sort (histogram, scan, scatter, quantise-gather) + (fused gmm+SwiGLU 1, +1 code
     # pass for per-row h scales | gmm 1 + SwiGLU 1) + gmm 1 + combine 1; the int8-weight gmms each
     # add their f16 decode of the activations where they take the 256-token tile (groups of 256
     # rows or more on average)
-    launches_per_step = (4 + ((1 + (1 if cfg.act_mode == 0 else 0)) if fused else 2) + 1 + 1
+    # the sort's index kernels run as one CTA for up to 32768 pairs and 64 experts
+    sort_launches = 1 if (cfg.T * cfg.k <= 32768 and cfg.E <= 64) else 3
+    launches_per_step = (sort_launches + 1 + ((1 + (1 if cfg.act_mode == 0 else 0)) if fused else 2) + 1 + 1
                          + (2 if w8 and cfg.T * cfg.k >= 256 * cfg.E else 0))
     fl = fwd_flops(cfg)
     g_in = float(np.mean([a for a, _ in gmm_ms]))
