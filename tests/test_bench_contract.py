@@ -17,10 +17,12 @@ def _json_lines(text):
     return [json.loads(l) for l in text.splitlines() if l.startswith("{")]
 
 
+# the headline metric, word for word as the benchmark publishes it
+METRIC = "MoE FFN fwd tokens/s & gmm_fp8 TFLOP/s as % of GB300 FP8 dense peak"
+
+
 def _check_line(d, n_gpus):
-    with open(os.path.join(ROOT, "BASELINE.json")) as f:
-        metric = json.load(f)["metric"]
-    assert d["metric"] == metric
+    assert d["metric"] == METRIC
     assert d["impl"] == "reference"
     assert d["n_gpus"] == n_gpus and d["steps"] == 3 and d["warmup"] == 3
     assert d["value"] > 0 and d["ms_per_step"] > 0
