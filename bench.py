@@ -535,8 +535,10 @@ def run_ours(args, cfg, rank, world, local, secondary=False):
                      "flops_per_call": fl["gmm_in"], "algorithmic_bytes_per_call": nbytes, "ms_per_call": g_in,
                      "note": ("one gmm_fp8_mx_swiglu call per step: the block-scaled tcgen05 contraction with the "
                               "SwiGLU and MXFP8 requantisation epilogue") if mx else
-                             ("one gmm_fp8_w8 call per step: the e4m3 activations decoded to f16 in a workspace, "
-                              "the int8 weights converted to f16 into tensor memory, tcgen05 kind::f16") if w8 else
+                             ("one gmm_fp8_w8 call per step: the e4m3 activations "
+                              + ("decoded to f16 in a workspace (256-token tiles)" if cfg.T * cfg.k >= 256 * cfg.E
+                                 else "converted to f16 on the SM (128-token tiles)")
+                              + ", the int8 weights converted to f16 into tensor memory, tcgen05 kind::f16") if w8 else
                              ("one gmm_fp8_swiglu call per step: the tcgen05 contraction with the SwiGLU and "
                               "requantisation epilogue, plus the h code pass of the per-token scales") if fused else
                              "one gmm_fp8 call per step"},
